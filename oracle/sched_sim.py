@@ -1,0 +1,290 @@
+"""Admission and step-composition policy, in plain Python (oracle).
+
+TEST INFRASTRUCTURE ONLY -- see the package docstring for who may import it.
+
+Source: "20.3 服务、批处理与流式" (golang.design), section 20.3.2 批处理, the
+Forma batch mode and its scaled illustration:
+  * all slots share one pool of fixed-size KV blocks (32 positions; the
+    illustration scales this to 4), allocated on demand;
+  * admitting a request whenever a slot is free can deadlock: every slot
+    busy, the pool empty, no sequence able to grow, so nothing finishes and
+    nothing is freed.  Admission therefore reserves blocks for the prompt
+    *and* for part of the answer, so that an admitted request can finish;
+  * each step first schedules the prefill chunks of sequences that have no
+    first token yet (512 tokens per chunk; 8 in the illustration), then one
+    row for every decoding sequence; rows that do not fit wait for the next
+    step and are not evicted;
+  * at most a fixed number of rows per step (12 in the illustration);
+  * the request queue is served first-come first-served (section 20.3.4).
+Page "大模型推理为什么需要 Continuous Batching", section 2.2 and 3.3: after each
+step finished sequences leave and waiting requests fill the freed slots.
+
+Readings where the pages leave the step open (listed in the design notes):
+  R7  chunk = min(chunk, prompt left, rows left); prefills in admission
+      order; decode rows ordered by (steps waited desc, admission order).
+  R8  lowest free slot; blocks from a min-heap (lowest id first).
+  R9  admit the queue head iff a slot is free and
+          free_blocks - sum(outstanding reservations) >= blocks(prompt +
+          min(max_tokens, answer_budget)),
+      outstanding = reserved - allocated (>= 0).  Growth inside a
+      reservation always succeeds; growth beyond it takes an unreserved free
+      block or the row waits, and admission freezes while any row waits for
+      a block.  If every running sequence is stuck, the youngest is stopped
+      with reason LENGTH_FALLBACK (counted; never happens with an ample pool).
+  R10 strict FCFS: a head that does not fit blocks the queue.
+  R11 no EOS: a request finishes when it has max_tokens generated tokens.
+  Positions: prompt tokens occupy 0..P-1; the last prefill row samples the
+  first generated token; decode row k feeds generated token k at position
+  P + k.  A request needs P + max_tokens - 1 positions.
+
+``reserve_answer=False`` gives the free-slot-only admission the page warns
+about; ``stall_fallback=False`` makes plan() report a deadlock instead of
+stopping a sequence.
+"""
+from __future__ import annotations
+
+import dataclasses
+import heapq
+from collections import deque
+
+FINISH_LENGTH = 1            # reached max_tokens
+FINISH_LENGTH_FALLBACK = 2   # stopped because every running sequence was stuck
+FINISH_ABORTED = 3
+
+
+class Deadlock(Exception):
+    """No running sequence can make progress and no fallback is allowed."""
+
+
+class PoolTooSmall(Exception):
+    """The request can never be admitted."""
+
+
+def blocks_for(positions: int, block_size: int) -> int:
+    return -(-positions // block_size)
+
+
+@dataclasses.dataclass
+class SchedConfig:
+    n_blocks: int
+    block_size: int = 32
+    max_slots: int = 64
+    max_rows: int = 2048
+    chunk: int = 512
+    answer_budget: int = 128
+    max_blocks_per_seq: int = 1024
+    reserve_answer: bool = True
+    stall_fallback: bool = True
+
+
+@dataclasses.dataclass
+class Request:
+    id: int
+    prompt: list
+    max_tokens: int
+    sampling: object = None
+    slot: int = -1
+    blocks: list = dataclasses.field(default_factory=list)
+    reserved: int = 0
+    n_prefilled: int = 0
+    generated: list = dataclasses.field(default_factory=list)
+    waited: int = 0
+    block_wait: bool = False
+    admit_seq: int = -1
+    pending_prefill: int = 0
+
+
+@dataclasses.dataclass
+class Plan:
+    rows: list            # (slot, token, pos, is_prefill, sample)
+    sampled: list         # (request id, token_index) per sampled row, in row order
+    block_tables: dict    # slot -> list of physical block ids (logical order)
+    resets: list          # slots whose penalty counters start at zero
+    stopped: list         # (request id, reason) stopped by the stall fallback
+
+
+class Scheduler:
+    def __init__(self, cfg: SchedConfig):
+        self.cfg = cfg
+        self.free = list(range(cfg.n_blocks))
+        heapq.heapify(self.free)
+        self.slots = [None] * cfg.max_slots
+        self.waiting = deque()
+        self.running = []           # admission order
+        self.finished = {}          # id -> (reason, generated)
+        self._admit_counter = 0
+        self._last_plan = None
+        self.n_fallback = 0
+
+    # -- helpers -------------------------------------------------------
+    def _need(self, req: Request) -> int:
+        c = self.cfg
+        if not c.reserve_answer:
+            return 0
+        return blocks_for(len(req.prompt) + min(req.max_tokens, c.answer_budget), c.block_size)
+
+    def _outstanding(self) -> int:
+        return sum(max(0, r.reserved - len(r.blocks)) for r in self.running)
+
+    def _grow(self, req: Request) -> bool:
+        """Give req one more block; False if none may be taken."""
+        if not self.free:
+            return False
+        if len(req.blocks) < req.reserved:
+            req.blocks.append(heapq.heappop(self.free))
+            return True
+        if len(self.free) - self._outstanding() > 0:
+            req.blocks.append(heapq.heappop(self.free))
+            return True
+        return False
+
+    def _release(self, req: Request, reason: int) -> None:
+        for b in req.blocks:
+            heapq.heappush(self.free, b)
+        req.blocks = []
+        self.slots[req.slot] = None
+        self.running.remove(req)
+        self.finished[req.id] = (reason, list(req.generated))
+
+    # -- public API ----------------------------------------------------
+    def submit(self, req: Request) -> None:
+        c = self.cfg
+        if len(req.prompt) < 1 or req.max_tokens < 1:
+            raise ValueError("empty prompt or max_tokens < 1")
+        total = len(req.prompt) + req.max_tokens - 1
+        if blocks_for(total, c.block_size) > c.max_blocks_per_seq:
+            raise PoolTooSmall("request longer than max_blocks_per_seq")
+        first = blocks_for(len(req.prompt) + min(req.max_tokens, c.answer_budget), c.block_size)
+        if first > c.n_blocks:
+            raise PoolTooSmall("request can never fit the pool")
+        self.waiting.append(req)
+
+    def _admit(self, resets: list) -> None:
+        """Admission (R9, R10): FCFS; frozen while a row waits for a block."""
+        c = self.cfg
+        if any(r.block_wait for r in self.running):
+            return
+        while self.waiting and None in self.slots:
+            head = self.waiting[0]
+            need = self._need(head)
+            if c.reserve_answer and len(self.free) - self._outstanding() < need:
+                return
+            self.waiting.popleft()
+            head.slot = self.slots.index(None)
+            self.slots[head.slot] = head
+            head.reserved = need
+            head.admit_seq = self._admit_counter
+            self._admit_counter += 1
+            self.running.append(head)
+            resets.append(head.slot)
+
+    def _compose(self):
+        """Rows of one step: prefill chunks first, then one row per decoder.
+
+        Returns (rows, sampled, waits) where waits lists (request, for_block)
+        of rows that did not fit; block grants are applied as rows are made.
+        """
+        c = self.cfg
+        rows, sampled, waits = [], [], []
+        budget = c.max_rows
+        prefilling = set()
+        for r in self.running:
+            r.pending_prefill = 0
+        for r in self.running:                                   # prefill chunks
+            if r.n_prefilled >= len(r.prompt):
+                continue
+            if budget == 0:
+                waits.append((r, False))
+                continue
+            n = min(c.chunk, len(r.prompt) - r.n_prefilled, budget)
+            while len(r.blocks) * c.block_size < r.n_prefilled + n and self._grow(r):
+                pass
+            n = min(n, len(r.blocks) * c.block_size - r.n_prefilled)
+            if n <= 0:
+                waits.append((r, True))
+                continue
+            done = r.n_prefilled + n == len(r.prompt)
+            for i in range(n):
+                p = r.n_prefilled + i
+                smp = 1 if (done and i == n - 1) else 0
+                rows.append((r.slot, r.prompt[p], p, 1, smp))
+                if smp:
+                    sampled.append((r.id, 0))
+            r.pending_prefill = n
+            prefilling.add(r.id)
+            budget -= n
+        decoding = [r for r in self.running
+                    if r.n_prefilled == len(r.prompt) and r.id not in prefilling
+                    and 0 < len(r.generated) < r.max_tokens]
+        decoding.sort(key=lambda r: (-r.waited, r.admit_seq))
+        for r in decoding:                                       # one row each
+            pos = len(r.prompt) + len(r.generated) - 1
+            if budget == 0:
+                waits.append((r, False))
+                continue
+            if pos >= len(r.blocks) * c.block_size and not self._grow(r):
+                waits.append((r, True))
+                continue
+            rows.append((r.slot, r.generated[-1], pos, 0, 1))
+            sampled.append((r.id, len(r.generated)))
+            budget -= 1
+        return rows, sampled, waits
+
+    def plan(self) -> Plan:
+        c = self.cfg
+        resets, stopped = [], []
+        self._admit(resets)
+        while True:
+            rows, sampled, waits = self._compose()
+            if rows or not self.running:
+                break
+            if not c.stall_fallback:
+                raise Deadlock("every running sequence is stuck")
+            young = max(self.running, key=lambda r: r.admit_seq)   # R9 fallback
+            stopped.append((young.id, FINISH_LENGTH_FALLBACK))
+            self.n_fallback += 1
+            self._release(young, FINISH_LENGTH_FALLBACK)
+        waiting_ids = {id(r) for r, _ in waits}
+        for r in self.running:
+            if id(r) in waiting_ids:
+                r.waited += 1
+            else:
+                r.waited = 0
+            r.block_wait = False
+        for r, for_block in waits:
+            r.block_wait = r.block_wait or for_block
+        tables = {r.slot: list(r.blocks) for r in self.running}
+        plan = Plan(rows, sampled, tables, resets, stopped)
+        self._last_plan = plan
+        return plan
+
+    def commit(self, tokens) -> list:
+        """Feed the sampled tokens of the last plan (row order).
+
+        Returns [(request id, reason)] of requests finished by this commit.
+        """
+        plan = self._last_plan
+        if plan is None:
+            raise RuntimeError("commit without plan")
+        if len(tokens) != len(plan.sampled):
+            raise ValueError("token count does not match the plan")
+        by_id = {r.id: r for r in self.running}
+        for r in self.running:
+            r.n_prefilled += r.pending_prefill
+            r.pending_prefill = 0
+        for (rid, _), t in zip(plan.sampled, tokens):
+            by_id[rid].generated.append(int(t))
+        done = []
+        for r in list(self.running):
+            if len(r.generated) >= r.max_tokens:
+                self._release(r, FINISH_LENGTH)
+                done.append((r.id, FINISH_LENGTH))
+        self._last_plan = None
+        return done
+
+    def stats(self) -> dict:
+        return dict(running=len(self.running), waiting=len(self.waiting),
+                    free_blocks=len(self.free), outstanding=self._outstanding(),
+                    allocated=sum(len(r.blocks) for r in self.running),
+                    reserved=sum(r.reserved for r in self.running),
+                    fallback_stops=self.n_fallback)
