@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Decode throughput of the batched step on GB300: tok/s vs the
+(W + B*A)/beta HBM roofline.
+
+Workload (default): the 7B-shaped decoder (32 layers, d 4096, 32 q / 8 KV
+heads, head_dim 128, FFN 14336, vocab 65536, bf16 random-init weights) in a
+pure-decode step of B = 32 rows whose cached contexts are drawn from
+U[256, 4096] (seeded), 32-position KV blocks on a randomly permuted
+placement, KV filled with seeded random bf16, every row sampled with
+temperature 1, top_p 0.3, frequency penalty 1, decay 0.996.  One "step" is
+one pass of the whole step (embedding, 32 layers, LM head, sampler) for all
+B rows; the weights (14.5 GB) and KV (~9 GB) are far larger than L2, so no
+flush is needed between steps.
+
+value  = B * n_gpus / step time, inputs resident on the device (Batch API).
+e2e    = the same through cbd_step with host arrays: the step's rows, block
+         tables and sampling parameters go host->device and the sampled
+         tokens come back device->host inside every timed step.
+Multi-GPU: independent replicas (one engine per GPU, no collective on the
+data path); barrier + max-over-ranks timing.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (no GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s on 1 GB300 vs batch B; step HBM GB/s vs (W+B·A)/β roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cbd", choices=["cbd", "reference"])
+    ap.add_argument("--shape", default="7b")
+    ap.add_argument("--B", type=int, default=32)
+    ap.add_argument("--ctx-lo", type=int, default=256)
+    ap.add_argument("--ctx-hi", type=int, default=4096)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="override layer count (profiling cases only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def shape_of(args):
+    from continuous_batching_decode_gb300 import synth
+    s = dict(synth.MODEL_SHAPES[args.shape])
+    if args.layers:
+        s["n_layers"] = args.layers
+    return s
+
+
+def weight_bytes(s):
+    """W: every weight streamed once per step (embedding excluded)."""
+    d, hq, hkv, hd, F, V, L = (s["d_model"], s["n_heads"], s["n_kv_heads"], s["head_dim"], s["ffn_dim"],
+                               s["vocab"], s["n_layers"])
+    per_layer = ((hq + 2 * hkv) * hd * d + d * hq * hd + 2 * F * d + d * F) * 2 + 2 * d * 2
+    return L * per_layer + V * d * 2 + d * 2
+
+
+def kv_pos_bytes(s):
+    return 2 * s["n_layers"] * s["n_kv_heads"] * s["head_dim"] * 2
+
+
+def workload(s, B, lo, hi, seed):
+    from continuous_batching_decode_gb300 import synth
+    db = synth.decode_batch(B, lo, hi, s["vocab"], seed)
+    ctx, toks = db["contexts"], db["tokens"]
+    need = {i: (c + 1 + 31) // 32 for i, c in enumerate(ctx)}
+    mbps = (hi + 1 + 31) // 32
+    n_pool = sum(need.values()) + 8
+    tables, nbps = synth.permuted_tables(need, n_pool, mbps, np.random.default_rng(seed + 1))
+    rows = [(i, toks[i], ctx[i], 0, 1) for i in range(B)]
+    samp = [dict(temperature=1.0, top_p=0.3, top_k=0, frequency_penalty=1.0, penalty_decay=0.996, seed=seed,
+                 request_id=i, token_index=0) for i in range(B)]
+    return dict(ctx=ctx, rows=rows, tables=tables, nbps=nbps, samp=samp, mbps=mbps, n_pool=n_pool)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev, self.lines, self.proc = dev, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_bytes(cls, s, B, ctx):
+    """Algorithmic bytes one launch of a kernel class must move (7B: see the
+    design notes for the per-unit figures)."""
+    d, hq, hkv, hd, F, V = s["d_model"], s["n_heads"], s["n_kv_heads"], s["head_dim"], s["ffn_dim"], s["vocab"]
+    act = lambda k: B * k * 2 * 2            # hi + lo bf16 activations read
+    if cls == "gemm_qkv":
+        return (hq + 2 * hkv) * hd * d * 2 + act(d) + B * hq * hd * 4 + B * 2 * hkv * hd * 2
+    if cls == "gemm_o":
+        return d * hq * hd * 2 + act(hq * hd) + 2 * B * d * 4
+    if cls == "gemm_gate_up":
+        return 2 * F * d * 2 + act(d) + B * F * 2 * 2
+    if cls == "gemm_down":
+        return d * F * 2 + act(F) + 2 * B * d * 4
+    if cls == "gemm_lm_head":
+        return V * d * 2 + act(d) + B * V * 4
+    if cls == "attention":
+        return sum(c + 1 for c in ctx) * hkv * hd * 2 * 2 + B * hq * hd * 4 + B * hq * hd * 2 * 2
+    if cls == "sampler":
+        return B * V * 4 * 4
+    return None
+
+
+def oracle_sample(s, B, ctx, toks, kv_source, weights_l0, seed):
+    """Time the CPU oracle on one layer of the step (all B rows) plus the LM
+    head; returns (seconds for a full step, details)."""
+    from oracle import model as om
+    cfg1 = om.ModelConfig(**dict(s, n_layers=1))
+    m1 = om.OracleModel(cfg1, weights_l0)
+    kv = {}
+    for i, c in enumerate(ctx):
+        q = om.SequenceKV(cfg1, c + 2)
+        K, V = kv_source(i, c)
+        q.K[0][:c] = K
+        q.V[0][:c] = V
+        q.length = c
+        kv[i] = q
+    rows = [(i, toks[i], ctx[i], 1) for i in range(B)]
+    m1.layer(0)
+    if not callable(weights_l0):
+        m1._get("embed")
+    m1._get("final_norm")
+    m1._get("lm_head")
+    t0 = time.perf_counter()
+    om.step(m1, kv, rows)
+    t1 = time.perf_counter()
+    x = np.random.default_rng(seed).normal(size=(B, s["d_model"]))
+    t2 = time.perf_counter()
+    om.rmsnorm(x, m1._get("final_norm"), cfg1.rms_eps) @ m1._get("lm_head").T
+    t3 = time.perf_counter()
+    t_layer = (t1 - t0) - (t3 - t2)
+    full = s["n_layers"] * t_layer + (t3 - t2)
+    return full, dict(layer_s=t_layer, head_s=t3 - t2, sample_s=(t1 - t0) + (t3 - t2))
+
+
+def cpu_weights_l0(s, seed):
+    """Layer-0 weights, embedding rows and LM head on the host (bf16 bits)."""
+    import torch
+    from continuous_batching_decode_gb300 import synth
+    g = torch.Generator().manual_seed(seed)
+    out = {}
+    for name, shape in synth.weight_shapes(s).items():
+        if not (name.startswith("0.") or name in ("embed", "final_norm", "lm_head")):
+            continue
+        if name.endswith("norm"):
+            t = torch.ones(shape, dtype=torch.bfloat16)
+        else:
+            t = (torch.randn(shape, generator=g) * 0.02).to(torch.bfloat16)
+        out[name] = synth.bf16_bits(t)
+    return out
+
+
+def run_reference(args):
+    """CPU oracle arm: each step times one bounded sample of the workload."""
+    s = shape_of(args)
+    B = args.B
+    wl = workload(s, B, args.ctx_lo, args.ctx_hi, args.seed)
+    w0 = cpu_weights_l0(s, args.seed)
+    rng = np.random.default_rng(args.seed + 2)
+
+    def kv_source(i, c):
+        shp = (c, s["n_kv_heads"], s["head_dim"])
+        from oracle.model import round_to_bf16
+        return round_to_bf16(rng.normal(0, 1.3, shp)), round_to_bf16(rng.normal(0, 1.3, shp))
+
+    toks = [r[1] for r in wl["rows"]]
+    ts = []
+    for i in range(args.warmup + args.steps):
+        full, det = oracle_sample(s, B, wl["ctx"], toks, kv_source, w0, args.seed)
+        if i >= args.warmup:
+            ts.append(full)
+    t = statistics.median(ts)
+    value = B / t
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"one of {s['n_layers']} layers for all {B} rows plus the LM head, per step; "
+              f"full step = {s['n_layers']} x layer + head")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.shape}-shaped decode, B={B}, ctx U[{args.ctx_lo},{args.ctx_hi}]",
+                       "B": B, "shape": args.shape},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_cbd(args):
+    import torch
+    import continuous_batching_decode_gb300 as cbd
+    from continuous_batching_decode_gb300 import build, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    cbd.lib()
+    dev = torch.cuda.current_device()
+    s = shape_of(args)
+    B = args.B
+    wl = workload(s, B, args.ctx_lo, args.ctx_hi, args.seed)
+    w = synth.make_weights(s, seed=args.seed, device="cuda")
+    cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"])
+    e = cbd.engine_create(cfg, w)
+    if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
+        del w
+    torch.cuda.empty_cache()
+    pool = cbd.kv_pool_create(e, wl["n_pool"])
+    base, nbytes, nb = cbd.kv_pool_data(pool)
+    kv = cbd.device_view(base, (s["n_layers"], 2, nb, s["n_kv_heads"], 32, s["head_dim"]), "bf16")
+    gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
+    for l in range(s["n_layers"]):
+        kv[l].copy_((torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3).to(torch.bfloat16))
+    stream = torch.cuda.current_stream()
+    b = cbd.batch_create(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"])
+    out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    for _ in range(args.warmup):
+        cbd.batch_run(e, pool, b, out)
+    torch.cuda.synchronize()
+    cbd.engine_check(e)
+
+    clk = Clocks(dev)
+    clk.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        cbd.batch_run(e, pool, b, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    cbd.engine_check(e)
+    value = B * world / (ms / 1000.0)
+    launches = cbd.batch_launches(b) * args.steps
+
+    # per-kernel live timing (same batch, same stream, CUDA events per launch)
+    cbd.engine_profile(e, True)
+    for _ in range(args.steps):
+        cbd.batch_run(e, pool, b, out)
+    prof = cbd.engine_profile_read(e)
+    cbd.engine_profile(e, False)
+    peak, peak_kind = peaks()
+    dom = max(prof, key=lambda k: prof[k][1])
+    ranked = sorted(((v[1], k) for k, v in prof.items()), reverse=True)
+    roof = None
+    for _, k in ranked:
+        byt = kernel_bytes(k, s, B, wl["ctx"])
+        if byt:
+            n_l, tot = prof[k]
+            avg_s = tot / n_l / 1000.0
+            ach = byt / avg_s / 1e9
+            roof = {"kernel": k, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                    "bytes_per_launch": byt, "avg_launch_us": round(avg_s * 1e6, 2)}
+            break
+    W = weight_bytes(s)
+    A = sum(c + 1 for c in wl["ctx"]) * kv_pos_bytes(s)
+    step_bytes = W + A
+    step_roof = {"W_bytes": W, "BA_bytes": A, "bytes_per_step": step_bytes,
+                 "achieved_GBs": round(step_bytes / (ms / 1000.0) / 1e9, 1),
+                 "frac_of_measured": round(step_bytes / (ms / 1000.0) / 1e9 / peak, 4),
+                 "frac_of_8TBs": round(step_bytes / (ms / 1000.0) / 8e12, 4),
+                 "roofline_tok_s_8TBs": round(B / (step_bytes / 8e12), 1)}
+    kernels = {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4),
+                   "share": round(v[1] / sum(x[1] for x in prof.values()), 4)} for k, v in prof.items()}
+
+    # end to end through cbd_step: host arrays in, tokens out, every step
+    e2e = None
+    if not args.no_e2e:
+        host_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
+        for _ in range(2):
+            cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
+            host_tok.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
+            host_tok.copy_(out, non_blocking=True)
+            stream.synchronize()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - t0) / args.steps * 1000.0
+        e_ms = max(ev0.elapsed_time(ev1) / args.steps, wall)
+        if dist:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = len(wl["rows"]) * 20 + wl["tables"].nbytes + wl["nbps"].nbytes + len(wl["samp"]) * 48
+        e2e = {"value": B * world / (e_ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": B * 4, "ms_per_step": round(e_ms, 4)}
+        cbd.engine_check(e)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wbits = {k: synth.bf16_bits(v) for k, v in w.items() if k.startswith("0.") or k in ("final_norm", "lm_head")}
+        wbits["embed"] = None
+        del wbits["embed"]
+        E = w["embed"]
+
+        def src(name, *a):
+            if name == "embed_rows":
+                return synth.bf16_bits(E[torch.as_tensor(a[0], device="cuda")])
+            return wbits[name]
+
+        def kv_source(i, c):
+            ids = torch.as_tensor(wl["tables"][i][: (c + 31) // 32].astype(np.int64), device="cuda")
+            t = kv[0, :, ids].permute(0, 1, 3, 2, 4).reshape(2, -1, s["n_kv_heads"], s["head_dim"])[:, :c]
+            t = t.float().cpu().numpy().astype(np.float64)
+            return t[0], t[1]
+        toks = [r[1] for r in wl["rows"]]
+        full, det = oracle_sample(s, B, wl["ctx"], toks, kv_source, src, args.seed)
+        cpu = {"value": round(B / full, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": (f"layer 0 of {s['n_layers']} for all {B} rows ({det['layer_s']:.2f} s) plus the LM head "
+                          f"({det['head_s']:.2f} s); full step = {s['n_layers']} x layer + head"),
+               "step_s": round(full, 2)}
+        del w
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, random bf16 KV)",
+            "config": {"workload": (f"{args.shape}-shaped pure-decode step, B={B}, ctx U[{args.ctx_lo},{args.ctx_hi}], "
+                                    "32-position blocks, top_p 0.3 sampling"),
+                       "B": B, "shape": args.shape, "layers": s["n_layers"], "mean_ctx": float(np.mean(wl["ctx"])),
+                       "l2": "inputs larger than L2 (weights 14.5 GB + KV); no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for Bs in [int(x) for x in args.sweep.split(",") if x.strip()]:
+        wl2 = workload(s, Bs, args.ctx_lo, args.ctx_hi, args.seed)
+        if wl2["n_pool"] > wl["n_pool"] or Bs > max(B, 8):
+            print(f"sweep B={Bs}: skipped (pool/slots sized for B={B})", file=sys.stderr)
+            continue
+        b2 = cbd.batch_create(e, pool, wl2["rows"], wl2["tables"], wl2["nbps"], wl2["samp"])
+        for _ in range(args.warmup):
+            cbd.batch_run(e, pool, b2, out)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            cbd.batch_run(e, pool, b2, out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms2 = ev0.elapsed_time(ev1) / args.steps
+        by = W + sum(c + 1 for c in wl2["ctx"]) * kv_pos_bytes(s)
+        print(json.dumps({"sweep_B": Bs, "ms_per_step": round(ms2, 4), "tok_s": round(Bs / ms2 * 1000, 1),
+                          "GBs": round(by / ms2 / 1e6, 1), "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}),
+              file=sys.stderr, flush=True)
+        cbd.batch_destroy(b2)
+    cbd.batch_destroy(b)
+    cbd.kv_pool_destroy(pool)
+    cbd.engine_destroy(e)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_cbd(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,767 @@
+// libcbd C ABI: engine, KV pool, batch (validated step inputs) and the step
+// launch sequence.  The Scheduler (sched.cpp) decides what runs; a Batch
+// runs it -- the split "20.3 服务、批处理与流式" section 20.3.2 describes for
+// Forma, which keeps admission bugs and batching bugs apart.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace cbd {
+
+static thread_local std::string g_err;
+
+cbd_status fail(cbd_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+void clear_error() { g_err.clear(); }
+
+static cbd_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(err == cudaErrorMemoryAllocation ? CBD_ENOMEM : CBD_ECUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+#define CBD_CUDA(call)                                   \
+  do {                                                   \
+    cudaError_t _e = (call);                             \
+    if (_e != cudaSuccess) return cuda_fail(_e, #call);  \
+  } while (0)
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Kernel classes for cbd_engine_profile.
+static const char* kKernelClass[] = {"embed", "rmsnorm", "gemm_qkv", "attention", "gemm_o",
+                                     "gemm_gate_up", "gemm_down", "final_norm", "gemm_lm_head", "sampler"};
+enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, kcSamp, kcCount };
+
+
+// ---------------------------------------------------------------- repack
+// dst[r][:] = src[perm[r]][:] (bf16 rows of K elements).
+__global__ void permute_rows_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
+                                    const int32_t* __restrict__ perm, int K) {
+  const int r = blockIdx.x;
+  const uint16_t* s = src + (size_t)perm[r] * K;
+  uint16_t* d = dst + (size_t)r * K;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) d[i] = s[i];
+}
+__global__ void bf16_to_f32_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = bf16_to_f32(src[i]);
+}
+
+struct Arena {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  }
+};
+
+}  // namespace cbd
+
+using namespace cbd;
+
+extern "C" {
+
+const char* cbd_last_error(void) { return g_err.c_str(); }
+const char* cbd_version(void) { return "cbd 0.1 sm_103a"; }
+
+}  // extern "C"
+
+namespace {
+
+cbd_status check_config(const cbd_config* c) {
+  if (!c) return fail(CBD_EINVAL, "cfg is NULL");
+  if (c->n_layers < 1 || c->d_model < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+      c->ffn_dim < 1 || c->vocab < 1)
+    return fail(CBD_EINVAL, "model dimensions must be positive");
+  if (c->n_heads % c->n_kv_heads) return fail(CBD_EINVAL, "n_kv_heads must divide n_heads");
+  if (c->block_size != kBlock) return fail(CBD_EINVAL, "block_size must be 32");
+  if (c->max_rows < 1 || c->max_rows > 4096) return fail(CBD_EINVAL, "max_rows must be in [1, 4096]");
+  if (c->max_slots < 1 || c->max_slots > 65536) return fail(CBD_EINVAL, "max_slots out of range");
+  if (c->max_blocks_per_seq < 1 || c->max_blocks_per_seq > 65536)
+    return fail(CBD_EINVAL, "max_blocks_per_seq out of range");
+  if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return fail(CBD_EINVAL, "rope_base/rms_eps invalid");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(CBD_EUNSUPPORTED, "head_dim must be 64 or 128");
+  const int g = c->n_heads / c->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return fail(CBD_EUNSUPPORTED, "n_heads/n_kv_heads must be 1, 2, 4 or 8");
+  if (c->d_model % 256 || c->ffn_dim % 256 || (c->n_heads * c->head_dim) % 256)
+    return fail(CBD_EUNSUPPORTED, "d_model, ffn_dim and n_heads*head_dim must be multiples of 256");
+  if (c->vocab > kMaxVocab || c->vocab % 32) return fail(CBD_EUNSUPPORTED, "vocab must be a multiple of 32, <= 65536");
+  return CBD_OK;
+}
+
+// Copy `bytes` from a host or device source into device memory.
+cbd_status upload(void* dst, const void* src, size_t bytes, bool on_device) {
+  if (!src) return fail(CBD_EINVAL, "a weight pointer is NULL");
+  CBD_CUDA(cudaMemcpy(dst, src, bytes, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice));
+  return CBD_OK;
+}
+
+}  // namespace
+
+extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights* w, cbd_engine** out) {
+  clear_error();
+  if (!out) return fail(CBD_EINVAL, "out is NULL");
+  *out = nullptr;
+  cbd_status st = check_config(cfg);
+  if (st) return st;
+  if (!w || !w->layers) return fail(CBD_EINVAL, "weights are NULL");
+  int dev = 0;
+  CBD_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  CBD_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(CBD_EUNSUPPORTED, "libcbd is built for sm_103a; device %d is sm_%d%d", dev, prop.major, prop.minor);
+
+  auto e = std::make_unique<cbd_engine>();
+  e->cfg = *cfg;
+  e->device = dev;
+  e->sm_count = prop.multiProcessorCount;
+  Dims& dm = e->dm;
+  dm.L = cfg->n_layers; dm.d = cfg->d_model; dm.hq = cfg->n_heads; dm.hkv = cfg->n_kv_heads;
+  dm.hd = cfg->head_dim; dm.F = cfg->ffn_dim; dm.V = cfg->vocab;
+  dm.qkv_out = (dm.hq + 2 * dm.hkv) * dm.hd;
+  dm.max_rows = cfg->max_rows; dm.max_slots = cfg->max_slots; dm.max_blocks_per_seq = cfg->max_blocks_per_seq;
+  dm.rope_base = cfg->rope_base; dm.eps = cfg->rms_eps;
+  e->max_pos = dm.max_blocks_per_seq * kBlock;
+  const bool ondev = w->on_device != 0;
+  CBD_CUDA(cudaDeviceSynchronize());   // weights produced on any stream are complete
+  const size_t d = dm.d, V = dm.V, F = dm.F, qo = dm.qkv_out, hqd = (size_t)dm.hq * dm.hd;
+
+  // ---- weight arena
+  Arena A;
+  const size_t o_embed = A.take(V * d * 2), o_lm = A.take(V * d * 2), o_fn = A.take(d * 4);
+  std::vector<size_t> o_an(dm.L), o_fnn(dm.L), o_qkv(dm.L), o_o(dm.L), o_gu(dm.L), o_dn(dm.L);
+  for (int l = 0; l < dm.L; ++l) {
+    o_an[l] = A.take(d * 4); o_fnn[l] = A.take(d * 4);
+    o_qkv[l] = A.take(qo * d * 2); o_o[l] = A.take(d * hqd * 2);
+    o_gu[l] = A.take(2 * F * d * 2); o_dn[l] = A.take(d * F * 2);
+  }
+  const size_t o_rope = A.take((size_t)e->max_pos * (dm.hd / 2) * 2 * 4);
+  e->arena_bytes = A.off;
+  CBD_CUDA(cudaMalloc(&e->arena, e->arena_bytes));
+  auto cleanup = [&]() {
+    if (e->arena) cudaFree(e->arena);
+    e->arena = nullptr;
+  };
+  uint8_t* base = static_cast<uint8_t*>(e->arena);
+  e->embed = reinterpret_cast<uint16_t*>(base + o_embed);
+  e->lm_head = reinterpret_cast<uint16_t*>(base + o_lm);
+  e->final_norm = reinterpret_cast<float*>(base + o_fn);
+  e->rope_cs = reinterpret_cast<float*>(base + o_rope);
+
+  // temporary device buffers: the largest source matrix, a permutation, a gain
+  const size_t tmp_elems = std::max({qo * d, 2 * F * d, d * F, d * hqd, V * d});
+  void* tmp = nullptr;
+  int32_t* perm_d = nullptr;
+  cudaError_t ce = cudaMalloc(&tmp, tmp_elems * 2);
+  if (ce == cudaSuccess) ce = cudaMalloc(&perm_d, std::max(qo, 2 * F) * sizeof(int32_t));
+  if (ce != cudaSuccess) {
+    if (tmp) cudaFree(tmp);
+    cleanup();
+    return cuda_fail(ce, "cudaMalloc(repack temporaries)");
+  }
+  auto free_tmp = [&]() { cudaFree(tmp); cudaFree(perm_d); };
+  auto gain = [&](size_t off, const void* src) -> cbd_status {
+    cbd_status s2 = upload(tmp, src, d * 2, ondev);
+    if (s2) return s2;
+    bf16_to_f32_kernel<<<(int)((d + 255) / 256), 256>>>(reinterpret_cast<float*>(base + off),
+                                                          static_cast<uint16_t*>(tmp), (int)d);
+    CBD_CUDA(cudaGetLastError());
+    return CBD_OK;
+  };
+  auto permuted = [&](size_t off, const std::vector<int32_t>& perm, int K) -> cbd_status {
+    CBD_CUDA(cudaMemcpy(perm_d, perm.data(), perm.size() * 4, cudaMemcpyHostToDevice));
+    permute_rows_kernel<<<(int)perm.size(), 256>>>(reinterpret_cast<uint16_t*>(base + off),
+                                                   static_cast<uint16_t*>(tmp), perm_d, K);
+    CBD_CUDA(cudaGetLastError());
+    CBD_CUDA(cudaDeviceSynchronize());
+    return CBD_OK;
+  };
+  // Row orders: q and k rows within each head become (i, i + hd/2) pairs so
+  // the RoPE partners are adjacent outputs; gate/up rows interleave so
+  // SwiGLU partners are adjacent.  v, o, down, embed, lm_head keep their order.
+  std::vector<int32_t> perm_qkv(qo), perm_gu(2 * F);
+  {
+    const int hd = dm.hd, half = hd / 2;
+    for (int h = 0; h < dm.hq + dm.hkv; ++h)
+      for (int i = 0; i < half; ++i) {
+        perm_qkv[(size_t)h * hd + 2 * i] = h * hd + i;
+        perm_qkv[(size_t)h * hd + 2 * i + 1] = h * hd + i + half;
+      }
+    for (size_t r = (size_t)(dm.hq + dm.hkv) * hd; r < qo; ++r) perm_qkv[r] = (int32_t)r;
+    for (int i = 0; i < dm.F; ++i) { perm_gu[2 * i] = i; perm_gu[2 * i + 1] = dm.F + i; }
+  }
+  cbd_status s2 = CBD_OK;
+#define TRY(x) do { s2 = (x); if (s2) { free_tmp(); cleanup(); return s2; } } while (0)
+  TRY(upload(base + o_embed, w->embed, V * d * 2, ondev));
+  TRY(upload(base + o_lm, w->lm_head, V * d * 2, ondev));
+  TRY(gain(o_fn, w->final_norm));
+  e->layers.resize(dm.L);
+  for (int l = 0; l < dm.L; ++l) {
+    const cbd_layer_weights& lw = w->layers[l];
+    TRY(gain(o_an[l], lw.attn_norm));
+    TRY(gain(o_fnn[l], lw.ffn_norm));
+    uint8_t* t = static_cast<uint8_t*>(tmp);
+    TRY(upload(t, lw.wq, hqd * d * 2, ondev));
+    TRY(upload(t + hqd * d * 2, lw.wk, (size_t)dm.hkv * dm.hd * d * 2, ondev));
+    TRY(upload(t + (hqd + (size_t)dm.hkv * dm.hd) * d * 2, lw.wv, (size_t)dm.hkv * dm.hd * d * 2, ondev));
+    TRY(permuted(o_qkv[l], perm_qkv, (int)d));
+    TRY(upload(base + o_o[l], lw.wo, d * hqd * 2, ondev));
+    TRY(upload(t, lw.w_gate, F * d * 2, ondev));
+    TRY(upload(t + F * d * 2, lw.w_up, F * d * 2, ondev));
+    TRY(permuted(o_gu[l], perm_gu, (int)d));
+    TRY(upload(base + o_dn[l], lw.w_down, d * F * 2, ondev));
+    LayerDev& L = e->layers[l];
+    L.attn_norm = reinterpret_cast<float*>(base + o_an[l]);
+    L.ffn_norm = reinterpret_cast<float*>(base + o_fnn[l]);
+    L.w_qkv = reinterpret_cast<uint16_t*>(base + o_qkv[l]);
+    L.w_o = reinterpret_cast<uint16_t*>(base + o_o[l]);
+    L.w_gu = reinterpret_cast<uint16_t*>(base + o_gu[l]);
+    L.w_down = reinterpret_cast<uint16_t*>(base + o_dn[l]);
+  }
+#undef TRY
+  free_tmp();
+  {  // RoPE table: fp64 angles rounded to fp32, [pos][i] = (cos, sin)
+    const int half = dm.hd / 2;
+    std::vector<float> cs((size_t)e->max_pos * half * 2);
+    for (int p = 0; p < e->max_pos; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * std::pow((double)dm.rope_base, -2.0 * i / dm.hd);
+        cs[((size_t)p * half + i) * 2] = (float)std::cos(ang);
+        cs[((size_t)p * half + i) * 2 + 1] = (float)std::sin(ang);
+      }
+    cudaError_t e2 = cudaMemcpy(base + o_rope, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+    if (e2 != cudaSuccess) { cleanup(); return cuda_fail(e2, "upload RoPE table"); }
+  }
+
+  // ---- workspaces
+  const size_t R = dm.max_rows, S = dm.max_slots;
+  const size_t act_w = std::max(d, hqd);
+  const size_t chunks_per_seq = ((size_t)e->max_pos + kAttnChunk - 1) / kAttnChunk;
+  e->max_work = (int)std::min<size_t>(R * chunks_per_seq, (size_t)1 << 16);
+  Arena W;
+  const size_t o_x = W.take(R * d * 4), o_ah = W.take(R * act_w * 2), o_al = W.take(R * act_w * 2);
+  const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
+  const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
+  const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
+  e->work_bytes = W.off;
+  cudaError_t e3 = cudaMalloc(&e->work, e->work_bytes);
+  if (e3 != cudaSuccess) { cleanup(); return cuda_fail(e3, "cudaMalloc(workspaces)"); }
+  uint8_t* wb = static_cast<uint8_t*>(e->work);
+  e->x = reinterpret_cast<float*>(wb + o_x);
+  e->act_hi = reinterpret_cast<uint16_t*>(wb + o_ah);
+  e->act_lo = reinterpret_cast<uint16_t*>(wb + o_al);
+  e->ffn_hi = reinterpret_cast<uint16_t*>(wb + o_fh);
+  e->ffn_lo = reinterpret_cast<uint16_t*>(wb + o_fl);
+  e->q = reinterpret_cast<float*>(wb + o_q);
+  e->attn_o = reinterpret_cast<float*>(wb + o_ao);
+  e->attn_ml = reinterpret_cast<float*>(wb + o_aml);
+  e->logits = reinterpret_cast<float*>(wb + o_lg);
+  e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
+  e->counters = reinterpret_cast<float*>(wb + o_cn);
+  e->err = reinterpret_cast<int32_t*>(wb + o_err);
+  e3 = cudaMemset(e->work, 0, e->work_bytes);
+  // ---- staging for cbd_step / cbd_sample
+  const size_t stage_bytes = align_up(R * sizeof(RowDev), 16) + 2 * align_up(S * 4, 16) +
+                             align_up(S * sizeof(SampDev), 16) + align_up(S * dm.max_blocks_per_seq * 4, 16) +
+                             align_up((size_t)e->max_work * sizeof(AttnWork), 16) + align_up((R + 1) * 4, 16) + 256;
+  for (auto& sg : e->stage) {
+    if (e3 == cudaSuccess) e3 = cudaMallocHost(&sg.host, stage_bytes);
+    if (e3 == cudaSuccess) e3 = cudaMalloc(&sg.dev, stage_bytes);
+    if (e3 == cudaSuccess) e3 = cudaEventCreateWithFlags(&sg.done, cudaEventDisableTiming);
+    sg.bytes = stage_bytes;
+  }
+  if (e3 == cudaSuccess) e3 = cudaDeviceSynchronize();
+  if (e3 != cudaSuccess) {
+    cbd_engine* raw = e.release();
+    cbd_engine_destroy(raw);
+    return cuda_fail(e3, "engine workspaces");
+  }
+  e->step_batch = new cbd_batch();
+  e->step_batch->owns_dev = false;
+  *out = e.release();
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_destroy(cbd_engine* e) {
+  if (!e) return CBD_OK;
+  cudaDeviceSynchronize();
+  for (auto& sg : e->stage) {
+    if (sg.host) cudaFreeHost(sg.host);
+    if (sg.dev) cudaFree(sg.dev);
+    if (sg.done) cudaEventDestroy(sg.done);
+  }
+  if (e->work) cudaFree(e->work);
+  if (e->arena) cudaFree(e->arena);
+  for (auto& r : e->prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+  for (auto ev : e->prof_free) cudaEventDestroy(ev);
+  delete e->step_batch;
+  delete e;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_check(cbd_engine* e) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_CUDA(cudaDeviceSynchronize());
+  int32_t v = 0;
+  CBD_CUDA(cudaMemcpy(&v, e->err, 4, cudaMemcpyDeviceToHost));
+  if (v) {
+    CBD_CUDA(cudaMemset(e->err, 0, 4));
+    return fail(CBD_EDEVICE, "device error code %d", v);
+  }
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_CUDA(cudaDeviceSynchronize());
+  for (auto& r : e->prof_recs) { e->prof_free.push_back(r.a); e->prof_free.push_back(r.b); }
+  e->prof_recs.clear();
+  e->prof = enable != 0;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* out, int32_t cap, int32_t* n) {
+  clear_error();
+  if (!e || !n) return fail(CBD_EINVAL, "NULL argument");
+  CBD_CUDA(cudaDeviceSynchronize());
+  std::vector<double> ms(kcCount, 0.0);
+  std::vector<int64_t> cnt(kcCount, 0);
+  for (auto& r : e->prof_recs) {
+    float t = 0.f;
+    CBD_CUDA(cudaEventElapsedTime(&t, r.a, r.b));
+    ms[r.cls] += t;
+    cnt[r.cls]++;
+  }
+  int32_t k = 0;
+  for (int c = 0; c < kcCount; ++c) {
+    if (!cnt[c]) continue;
+    if (out && k < cap) {
+      std::memset(&out[k], 0, sizeof(out[k]));
+      std::strncpy(out[k].name, kKernelClass[c], sizeof(out[k].name) - 1);
+      out[k].launches = cnt[c];
+      out[k].total_ms = ms[c];
+    }
+    ++k;
+  }
+  *n = std::min(k, cap);
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_counters(cbd_engine* e, float** counters) {
+  if (!e || !counters) return fail(CBD_EINVAL, "NULL argument");
+  *counters = e->counters;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (slot < 0 || slot >= e->dm.max_slots) return fail(CBD_EINVAL, "slot %d out of range", slot);
+  CBD_CUDA(cudaMemsetAsync(e->counters + (size_t)slot * e->dm.V, 0, (size_t)e->dm.V * 4,
+                           static_cast<cudaStream_t>(stream)));
+  return CBD_OK;
+}
+
+// ---------------------------------------------------------------- KV pool
+extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv_pool** out) {
+  clear_error();
+  if (!e || !out) return fail(CBD_EINVAL, "NULL argument");
+  *out = nullptr;
+  if (n_blocks < 1) return fail(CBD_EINVAL, "n_blocks must be >= 1");
+  const size_t bytes = (size_t)e->dm.L * 2 * (size_t)n_blocks * e->dm.hkv * kBlock * e->dm.hd * 2;
+  auto p = std::make_unique<cbd_kv_pool>();
+  p->e = e;
+  p->n_blocks = n_blocks;
+  p->bytes = bytes;
+  void* b = nullptr;
+  CBD_CUDA(cudaMalloc(&b, bytes));
+  p->base = static_cast<uint16_t*>(b);
+  *out = p.release();
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_kv_pool_destroy(cbd_kv_pool* p) {
+  if (!p) return CBD_OK;
+  cudaDeviceSynchronize();
+  cudaFree(p->base);
+  delete p;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_kv_pool_data(cbd_kv_pool* p, void** base, uint64_t* bytes, int32_t* n_blocks) {
+  if (!p) return fail(CBD_EINVAL, "pool is NULL");
+  if (base) *base = p->base;
+  if (bytes) *bytes = p->bytes;
+  if (n_blocks) *n_blocks = p->n_blocks;
+  return CBD_OK;
+}
+
+// ---------------------------------------------------------------- batch
+namespace cbd {
+
+cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const cbd_row* rows, int32_t n_rows,
+                             const int32_t* tables, int32_t table_slots, const int32_t* nbps,
+                             const cbd_sampling* sp, const float* uniforms, BatchImage* img) {
+  if (!e || !pool) return fail(CBD_EINVAL, "engine or pool is NULL");
+  if (pool->e != e) return fail(CBD_EINVAL, "pool belongs to another engine");
+  const Dims& dm = e->dm;
+  if (n_rows < 1 || n_rows > dm.max_rows) return fail(CBD_EINVAL, "n_rows %d not in [1, %d]", n_rows, dm.max_rows);
+  if (!rows || !tables || !nbps) return fail(CBD_EINVAL, "rows, block_tables or n_blocks_per_slot is NULL");
+  if (table_slots < 1 || table_slots > dm.max_slots)
+    return fail(CBD_EINVAL, "table_slots %d not in [1, %d]", table_slots, dm.max_slots);
+  const int mbps = dm.max_blocks_per_seq;
+  // per-slot summaries
+  std::vector<int32_t> cnt(table_slots, 0), pmin(table_slots, INT32_MAX), pmax(table_slots, -1), smp(table_slots, 0);
+  int32_t m = 0;
+  for (int32_t r = 0; r < n_rows; ++r) {
+    const cbd_row& w = rows[r];
+    if (w.slot < 0 || w.slot >= table_slots) return fail(CBD_EINVAL, "row %d: slot %d out of range", r, w.slot);
+    if (w.token < 0 || w.token >= dm.V) return fail(CBD_EINVAL, "row %d: token %d out of range", r, w.token);
+    const int32_t nb = nbps[w.slot];
+    if (nb < 1 || nb > mbps) return fail(CBD_EINVAL, "slot %d: n_blocks %d not in [1, %d]", w.slot, nb, mbps);
+    if (w.pos < 0 || w.pos >= nb * kBlock)
+      return fail(CBD_EINVAL, "row %d: pos %d outside the slot's %d blocks", r, w.pos, nb);
+    cnt[w.slot]++;
+    pmin[w.slot] = std::min(pmin[w.slot], w.pos);
+    pmax[w.slot] = std::max(pmax[w.slot], w.pos);
+    if (w.sample) {
+      if (++smp[w.slot] > 1) return fail(CBD_EINVAL, "slot %d has more than one sampled row", w.slot);
+      ++m;
+    }
+  }
+  // positions of a slot: one contiguous run with no repeats
+  {
+    for (int32_t s = 0; s < table_slots; ++s)
+      if (cnt[s] && pmax[s] - pmin[s] + 1 != cnt[s])
+        return fail(CBD_EINVAL, "slot %d: positions not one contiguous run", s);
+    std::vector<std::vector<uint8_t>> seen(table_slots);
+    for (int32_t r = 0; r < n_rows; ++r) {
+      const int32_t s = rows[r].slot;
+      if (cnt[s] < 2) continue;
+      auto& b = seen[s];
+      if (b.empty()) b.assign(cnt[s], 0);
+      const int32_t k = rows[r].pos - pmin[s];
+      if (b[k]) return fail(CBD_EINVAL, "slot %d: position %d appears twice", s, rows[r].pos);
+      b[k] = 1;
+    }
+  }
+  // blocks: in range and owned by one slot only
+  {
+    std::vector<int32_t> owner(pool->n_blocks, -1);
+    for (int32_t s = 0; s < table_slots; ++s) {
+      if (!cnt[s]) continue;
+      for (int32_t b = 0; b < nbps[s]; ++b) {
+        const int32_t id = tables[(size_t)s * mbps + b];
+        if (id < 0 || id >= pool->n_blocks)
+          return fail(CBD_EINVAL, "slot %d block %d: physical id %d outside the pool", s, b, id);
+        if (owner[id] >= 0 && owner[id] != s)
+          return fail(CBD_EINVAL, "physical block %d shared by slots %d and %d", id, owner[id], s);
+        if (owner[id] == s) return fail(CBD_EINVAL, "physical block %d used twice by slot %d", id, s);
+        owner[id] = s;
+      }
+    }
+  }
+  if (m > 0 && !sp) return fail(CBD_EINVAL, "sampling is NULL but %d rows are sampled", m);
+  if (m > dm.max_slots) return fail(CBD_EINVAL, "too many sampled rows");
+  for (int32_t j = 0; j < m; ++j) {
+    const cbd_sampling& s = sp[j];
+    if (!std::isfinite(s.temperature) || s.temperature < 0.f) return fail(CBD_EINVAL, "sampling %d: temperature", j);
+    if (!std::isfinite(s.top_p) || s.top_p < 0.f || s.top_p > 1.f) return fail(CBD_EINVAL, "sampling %d: top_p", j);
+    if (s.top_k < 0 || s.top_k > dm.V) return fail(CBD_EINVAL, "sampling %d: top_k", j);
+    if (!std::isfinite(s.presence_penalty) || !std::isfinite(s.frequency_penalty) || !std::isfinite(s.penalty_decay))
+      return fail(CBD_EINVAL, "sampling %d: penalty not finite", j);
+    if (s.reserved) return fail(CBD_EINVAL, "sampling %d: reserved field must be 0", j);
+    if (uniforms && !(uniforms[j] >= 0.f && uniforms[j] < 1.f)) return fail(CBD_EINVAL, "uniform %d not in [0,1)", j);
+  }
+  // work list: fixed 256-position chunks of every row
+  int64_t n_work = 0;
+  for (int32_t r = 0; r < n_rows; ++r) n_work += rows[r].pos / kAttnChunk + 1;
+  if (n_work > e->max_work)
+    return fail(CBD_EUNSUPPORTED, "step needs %lld attention chunks, more than the %d the workspace holds",
+                (long long)n_work, e->max_work);
+  // layout
+  BatchImage& I = *img;
+  I.n_rows = n_rows; I.m = m; I.n_work = (int32_t)n_work; I.table_slots = table_slots;
+  size_t off = 0;
+  auto take = [&](size_t b) { size_t o = off; off = align_up(off + b, 16); return o; };
+  I.off_rows = take(n_rows * sizeof(RowDev));
+  I.off_sr = take(std::max(m, 1) * 4);
+  I.off_ss = take(std::max(m, 1) * 4);
+  I.off_samp = take(std::max(m, 1) * sizeof(SampDev));
+  I.off_tables = take((size_t)table_slots * mbps * 4);
+  I.off_work = take(n_work * sizeof(AttnWork));
+  I.off_row_work = take((n_rows + 1) * 4);
+  I.bytes.assign(off, 0);
+  uint8_t* B = I.bytes.data();
+  RowDev* rd = reinterpret_cast<RowDev*>(B + I.off_rows);
+  int32_t* sr = reinterpret_cast<int32_t*>(B + I.off_sr);
+  int32_t* ss = reinterpret_cast<int32_t*>(B + I.off_ss);
+  SampDev* sd = reinterpret_cast<SampDev*>(B + I.off_samp);
+  AttnWork* wk = reinterpret_cast<AttnWork*>(B + I.off_work);
+  int32_t* rw = reinterpret_cast<int32_t*>(B + I.off_row_work);
+  int32_t j = 0, wi = 0;
+  int32_t max_chunks = 0;
+  for (int32_t r = 0; r < n_rows; ++r) {
+    const cbd_row& w = rows[r];
+    rd[r] = RowDev{w.slot, w.token, w.pos, (w.is_prefill ? 1 : 0) | (w.sample ? 2 : 0)};
+    rw[r] = wi;
+    const int32_t nch = w.pos / kAttnChunk + 1;
+    max_chunks = std::max(max_chunks, nch);
+    for (int32_t c = 0; c < nch; ++c) wk[wi++] = AttnWork{r, c * kAttnChunk};
+    if (w.sample) {
+      const cbd_sampling& s = sp[j];
+      sr[j] = r;
+      ss[j] = w.slot;
+      sd[j] = SampDev{s.temperature, s.top_p, s.presence_penalty, s.frequency_penalty, s.penalty_decay, s.top_k,
+                      (uint32_t)(s.seed & 0xffffffffu), (uint32_t)(s.seed >> 32),
+                      (uint32_t)(s.request_id & 0xffffffffu), (uint32_t)(s.request_id >> 32), s.token_index,
+                      uniforms ? uniforms[j] : -1.0f};
+      ++j;
+    }
+  }
+  rw[n_rows] = wi;
+  I.max_chunks = max_chunks;
+  std::memcpy(B + I.off_tables, tables, (size_t)table_slots * mbps * 4);
+  return CBD_OK;
+}
+
+void bind_batch(cbd_batch* b, const BatchImage& I, void* dev) {
+  uint8_t* D = static_cast<uint8_t*>(dev);
+  b->dev = dev;
+  b->dev_bytes = I.bytes.size();
+  b->n_rows = I.n_rows; b->m = I.m; b->n_work = I.n_work; b->table_slots = I.table_slots;
+  b->max_chunks = I.max_chunks;
+  b->rows = reinterpret_cast<RowDev*>(D + I.off_rows);
+  b->sampled_rows = reinterpret_cast<int32_t*>(D + I.off_sr);
+  b->sampled_slots = reinterpret_cast<int32_t*>(D + I.off_ss);
+  b->samp = reinterpret_cast<SampDev*>(D + I.off_samp);
+  b->tables = reinterpret_cast<int32_t*>(D + I.off_tables);
+  b->work = reinterpret_cast<AttnWork*>(D + I.off_work);
+  b->row_work = reinterpret_cast<int32_t*>(D + I.off_row_work);
+}
+
+static cudaEvent_t prof_event(cbd_engine* e) {
+  if (!e->prof_free.empty()) {
+    cudaEvent_t ev = e->prof_free.back();
+    e->prof_free.pop_back();
+    return ev;
+  }
+  cudaEvent_t ev{};
+  cudaEventCreate(&ev);
+  return ev;
+}
+
+// Launch `fn` bracketed by events when profiling is on.
+template <class Fn>
+static cudaError_t timed(cbd_engine* e, int cls, cudaStream_t s, Fn&& fn) {
+  if (!e->prof) return fn();
+  cudaEvent_t a = prof_event(e), b = prof_event(e);
+  cudaEventRecord(a, s);
+  cudaError_t ce = fn();
+  cudaEventRecord(b, s);
+  e->prof_recs.push_back({cls, a, b});
+  return ce;
+}
+
+// The step: embed; per layer norm -> QKV(+RoPE, KV append) -> attention ->
+// O(+residual) -> norm -> gate/up(+SwiGLU) -> down(+residual); final norm of
+// the sampled rows -> LM head -> sampler.
+static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t* out_tokens, float* out_logits,
+                            cudaStream_t s) {
+  const Dims& dm = e->dm;
+  const int n = b->n_rows;
+  const int hqd = dm.hq * dm.hd;
+  int launches = 0;
+  auto chk = [&](cudaError_t ce, const char* what) -> cbd_status {
+    if (ce != cudaSuccess) return cuda_fail(ce, what);
+    return CBD_OK;
+  };
+  cbd_status st;
+  if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, s); }), "embed"))) return st;
+  ++launches;
+  EpiArgs qkv{};
+  qkv.kind = kEpiQKV; qkv.out_f32 = e->q; qkv.ld = hqd;
+  qkv.pool = p->base; qkv.n_blocks = p->n_blocks; qkv.hq = dm.hq; qkv.hkv = dm.hkv; qkv.hd = dm.hd;
+  qkv.max_blocks_per_seq = dm.max_blocks_per_seq; qkv.max_pos = e->max_pos; qkv.rope_cs = e->rope_cs;
+  qkv.rows = b->rows; qkv.tables = b->tables; qkv.err = e->err;
+  EpiArgs res{};
+  res.kind = kEpiResid; res.out_f32 = e->x; res.ld = dm.d; res.err = e->err;
+  EpiArgs glu{};
+  glu.kind = kEpiSwiGLU; glu.out_hi = e->ffn_hi; glu.out_lo = e->ffn_lo; glu.ld_act = dm.F; glu.err = e->err;
+  for (int l = 0; l < dm.L; ++l) {
+    const LayerDev& L = e->layers[l];
+    qkv.layer = l;
+    if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.attn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
+                  "rmsnorm")))
+      return st;
+    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, L.w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d, n, qkv, s); }),
+                  "qkv")))
+      return st;
+    if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, s); }), "attention"))) return st;
+    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, n, res, s); }),
+                  "o_proj")))
+      return st;
+    if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.ffn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
+                  "rmsnorm")))
+      return st;
+    if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, L.w_gu, 2 * dm.F, dm.d, e->act_hi, e->act_lo, dm.d, n, glu, s); }),
+                  "gate_up")))
+      return st;
+    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F, n, res, s); }),
+                  "down")))
+      return st;
+    launches += 8;
+  }
+  if (b->m > 0) {
+    float* lg = out_logits ? out_logits : e->logits;
+    if (!out_tokens) return fail(CBD_EINVAL, "out_tokens is NULL but rows are sampled");
+    if ((st = chk(timed(e, kcFinal, s, [&] { return launch_rmsnorm(e, e->x, e->final_norm, b->m, b->sampled_rows, e->act_hi, e->act_lo, s); }),
+                  "final_norm")))
+      return st;
+    EpiArgs lo{};
+    lo.kind = kEpiLogits; lo.out_f32 = lg; lo.ld = dm.V; lo.err = e->err;
+    if ((st = chk(timed(e, kcLM, s, [&] { return launch_gemm(e, e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d, b->m, lo, s); }),
+                  "lm_head")))
+      return st;
+    if ((st = chk(timed(e, kcSamp, s, [&] { return launch_sampler(e, lg, b->m, b->sampled_slots, b->samp, out_tokens, s); }),
+                  "sampler")))
+      return st;
+    launches += 3;
+  }
+  b->launches = launches;
+  return CBD_OK;
+}
+
+}  // namespace cbd
+
+extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* rows, int32_t n_rows,
+                               const int32_t* block_tables, int32_t table_slots, const int32_t* n_blocks_per_slot,
+                               const cbd_sampling* sampling, const float* uniforms, int32_t* out_tokens,
+                               float* out_logits, void* stream) {
+  clear_error();
+  BatchImage img;
+  cbd_status st = build_batch_image(e, pool, rows, n_rows, block_tables, table_slots, n_blocks_per_slot, sampling,
+                                    uniforms, &img);
+  if (st) return st;
+  if (img.m > 0 && !out_tokens) return fail(CBD_EINVAL, "out_tokens is NULL but rows are sampled");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cbd_engine::Stage& sg = e->stage[e->stage_idx];
+  e->stage_idx ^= 1;
+  if (img.bytes.size() > sg.bytes) return fail(CBD_EUNSUPPORTED, "step image larger than the staging buffer");
+  CBD_CUDA(cudaEventSynchronize(sg.done));  // the step that last used this buffer has finished
+  std::memcpy(sg.host, img.bytes.data(), img.bytes.size());
+  CBD_CUDA(cudaMemcpyAsync(sg.dev, sg.host, img.bytes.size(), cudaMemcpyHostToDevice, s));
+  bind_batch(e->step_batch, img, sg.dev);
+  st = run_batch(e, pool, e->step_batch, out_tokens, out_logits, s);
+  cudaError_t ce = cudaEventRecord(sg.done, s);
+  if (st) return st;
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventRecord");
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_batch_create(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* rows, int32_t n_rows,
+                                       const int32_t* block_tables, int32_t table_slots,
+                                       const int32_t* n_blocks_per_slot, const cbd_sampling* sampling,
+                                       const float* uniforms, cbd_batch** out, void* stream) {
+  clear_error();
+  if (!out) return fail(CBD_EINVAL, "out is NULL");
+  *out = nullptr;
+  BatchImage img;
+  cbd_status st = build_batch_image(e, pool, rows, n_rows, block_tables, table_slots, n_blocks_per_slot, sampling,
+                                    uniforms, &img);
+  if (st) return st;
+  auto b = std::make_unique<cbd_batch>();
+  void* dev = nullptr;
+  CBD_CUDA(cudaMalloc(&dev, img.bytes.size()));
+  cudaError_t ce = cudaMemcpyAsync(dev, img.bytes.data(), img.bytes.size(), cudaMemcpyHostToDevice,
+                                   static_cast<cudaStream_t>(stream));
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) {
+    cudaFree(dev);
+    return cuda_fail(ce, "batch upload");
+  }
+  bind_batch(b.get(), img, dev);
+  b->owns_dev = true;
+  // launch count of one run
+  b->launches = 1 + 8 * e->dm.L + (img.m > 0 ? 3 : 0);
+  *out = b.release();
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_batch_run(cbd_engine* e, cbd_kv_pool* pool, cbd_batch* b, int32_t* out_tokens,
+                                    float* out_logits, void* stream) {
+  clear_error();
+  if (!e || !pool || !b) return fail(CBD_EINVAL, "NULL argument");
+  if (pool->e != e) return fail(CBD_EINVAL, "pool belongs to another engine");
+  return run_batch(e, pool, b, out_tokens, out_logits, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" cbd_status cbd_batch_destroy(cbd_batch* b) {
+  if (!b) return CBD_OK;
+  if (b->owns_dev && b->dev) {
+    cudaDeviceSynchronize();
+    cudaFree(b->dev);
+  }
+  delete b;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_batch_launches(cbd_batch* b, int32_t* n) {
+  if (!b || !n) return fail(CBD_EINVAL, "NULL argument");
+  *n = b->launches;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_sample(cbd_engine* e, const float* logits, int32_t m, const int32_t* slots,
+                                 const cbd_sampling* sampling, const float* uniforms, int32_t* out_tokens,
+                                 void* stream) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (m < 1 || m > e->dm.max_slots) return fail(CBD_EINVAL, "m %d not in [1, %d]", m, e->dm.max_slots);
+  if (!logits || !slots || !sampling || !out_tokens) return fail(CBD_EINVAL, "NULL argument");
+  std::vector<uint8_t> seen(e->dm.max_slots, 0);
+  std::vector<SampDev> sd(m);
+  for (int32_t j = 0; j < m; ++j) {
+    if (slots[j] < 0 || slots[j] >= e->dm.max_slots) return fail(CBD_EINVAL, "slot %d out of range", slots[j]);
+    if (seen[slots[j]]++) return fail(CBD_EINVAL, "slot %d appears twice", slots[j]);
+    const cbd_sampling& s = sampling[j];
+    if (!std::isfinite(s.temperature) || s.temperature < 0.f || !std::isfinite(s.top_p) || s.top_p < 0.f ||
+        s.top_p > 1.f || s.top_k < 0 || s.top_k > e->dm.V || s.reserved)
+      return fail(CBD_EINVAL, "sampling %d invalid", j);
+    if (uniforms && !(uniforms[j] >= 0.f && uniforms[j] < 1.f)) return fail(CBD_EINVAL, "uniform %d not in [0,1)", j);
+    sd[j] = SampDev{s.temperature, s.top_p, s.presence_penalty, s.frequency_penalty, s.penalty_decay, s.top_k,
+                    (uint32_t)(s.seed & 0xffffffffu), (uint32_t)(s.seed >> 32), (uint32_t)(s.request_id & 0xffffffffu),
+                    (uint32_t)(s.request_id >> 32), s.token_index, uniforms ? uniforms[j] : -1.0f};
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cbd_engine::Stage& sg = e->stage[e->stage_idx];
+  e->stage_idx ^= 1;
+  CBD_CUDA(cudaEventSynchronize(sg.done));
+  uint8_t* H = static_cast<uint8_t*>(sg.host);
+  const size_t o_samp = align_up((size_t)m * 4, 16);
+  std::memcpy(H, slots, (size_t)m * 4);
+  std::memcpy(H + o_samp, sd.data(), (size_t)m * sizeof(SampDev));
+  CBD_CUDA(cudaMemcpyAsync(sg.dev, sg.host, o_samp + (size_t)m * sizeof(SampDev), cudaMemcpyHostToDevice, s));
+  uint8_t* D = static_cast<uint8_t*>(sg.dev);
+  cudaError_t ce = launch_sampler(e, logits, m, reinterpret_cast<int32_t*>(D),
+                                  reinterpret_cast<SampDev*>(D + o_samp), out_tokens, s);
+  cudaError_t ce2 = cudaEventRecord(sg.done, s);
+  if (ce != cudaSuccess) return cuda_fail(ce, "sampler");
+  if (ce2 != cudaSuccess) return cuda_fail(ce2, "cudaEventRecord");
+  return CBD_OK;
+}

@@ -1,0 +1,180 @@
+// Internal declarations shared by the libcbd translation units.
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "../../include/cbd.h"
+
+#include <cuda_runtime.h>
+
+namespace cbd {
+
+// Thread-local message of the last failure; returns `code`.
+cbd_status fail(cbd_status code, const char* fmt, ...);
+void clear_error();
+
+constexpr int kBlock = 32;          // positions per KV block
+constexpr int kAttnChunk = 256;     // positions per attention split (8 blocks)
+constexpr int kMaxVocab = 65536;
+
+// Device error codes written to the engine's error word (first one wins).
+enum DeviceError : int32_t {
+  kDevOk = 0,
+  kDevBadRow = 1,        // a row index or position outside the staged tables
+  kDevBadBlock = 2,      // a block id outside the pool
+  kDevWaitTimeout = 3,   // a bounded wait gave up
+  kDevSampler = 4,       // sampler found no token (should not happen)
+};
+
+// Per-step row record as the kernels read it.
+struct RowDev {
+  int32_t slot, token, pos, flags;   // flags: bit0 prefill, bit1 sample
+};
+
+// Sampling parameters as the sampler kernel reads them.
+struct SampDev {
+  float temperature, top_p, presence, frequency, decay;
+  int32_t top_k;
+  uint32_t seed_lo, seed_hi, req_lo, req_hi, token_index;
+  float uniform;                     // >= 0: use it; < 0: draw with Philox
+};
+
+// One attention work item: a row and the first position of its chunk.
+struct AttnWork {
+  int32_t row, start;
+};
+
+struct LayerDev {
+  const float* attn_norm;            // [d] fp32
+  const float* ffn_norm;             // [d] fp32
+  const uint16_t* w_qkv;             // [(Hq+2Hkv)*hd][d], q/k rows rope-interleaved
+  const uint16_t* w_o;               // [d][Hq*hd]
+  const uint16_t* w_gu;              // [2F][d], rows (gate_i, up_i) interleaved
+  const uint16_t* w_down;            // [d][F]
+};
+
+struct Dims {
+  int L, d, hq, hkv, hd, F, V, qkv_out, max_rows, max_slots, max_blocks_per_seq;
+  float rope_base, eps;
+};
+
+}  // namespace cbd
+
+struct cbd_engine {
+  cbd::Dims dm{};
+  cbd_config cfg{};
+  int device = 0;
+  int sm_count = 0;
+  // weights
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  std::vector<cbd::LayerDev> layers;
+  const uint16_t* embed = nullptr;
+  const uint16_t* lm_head = nullptr;
+  const float* final_norm = nullptr;
+  const float* rope_cs = nullptr;     // [max_pos][hd/2][2] fp32 (cos, sin)
+  int max_pos = 0;
+  // activations / workspaces
+  void* work = nullptr;
+  size_t work_bytes = 0;
+  float* x = nullptr;                 // [max_rows][d] residual
+  uint16_t* act_hi = nullptr;         // [max_rows][max(d, Hq*hd)] bf16
+  uint16_t* act_lo = nullptr;
+  uint16_t* ffn_hi = nullptr;         // [max_rows][F] bf16 SwiGLU output
+  uint16_t* ffn_lo = nullptr;
+  float* q = nullptr;                 // [max_rows][Hq*hd]
+  float* attn_o = nullptr;            // [max_work][Hq][hd] partial outputs
+  float* attn_ml = nullptr;           // [max_work][Hq][2] (max, sum)
+  int max_work = 0;
+  float* logits = nullptr;            // [max_slots][V] internal logits
+  float* samp_scratch = nullptr;      // [max_slots][V] sampler scratch
+  float* counters = nullptr;          // [max_slots][V]
+  int32_t* err = nullptr;             // device error word
+  // staging for cbd_step (pinned host + device), double-buffered
+  struct Stage {
+    void* host = nullptr;
+    void* dev = nullptr;
+    size_t bytes = 0;
+    cudaEvent_t done{};
+  } stage[2];
+  int stage_idx = 0;
+  cbd_batch* step_batch = nullptr;    // batch object reused by cbd_step
+  // optional per-launch timing (cbd_engine_profile)
+  bool prof = false;
+  struct ProfRec { int cls; cudaEvent_t a, b; };
+  std::vector<ProfRec> prof_recs;
+  std::vector<cudaEvent_t> prof_free;
+};
+
+struct cbd_kv_pool {
+  cbd_engine* e = nullptr;
+  uint16_t* base = nullptr;
+  int32_t n_blocks = 0;
+  size_t bytes = 0;
+};
+
+struct cbd_batch {
+  bool owns_dev = true;
+  void* dev = nullptr;                // device copy of everything below
+  size_t dev_bytes = 0;
+  int32_t n_rows = 0, m = 0, n_work = 0, table_slots = 0, max_chunks = 0;
+  // device pointers into `dev`
+  cbd::RowDev* rows = nullptr;
+  int32_t* sampled_rows = nullptr;    // [m] row index of each sampled row
+  int32_t* sampled_slots = nullptr;   // [m]
+  cbd::SampDev* samp = nullptr;       // [m]
+  int32_t* tables = nullptr;          // [table_slots][max_blocks_per_seq]
+  cbd::AttnWork* work = nullptr;      // [n_work]
+  int32_t* row_work = nullptr;        // [n_rows + 1] prefix: first work item of each row
+  int32_t launches = 0;
+};
+
+namespace cbd {
+
+// Host-side builder: validates a step's inputs and lays out the staging
+// image (host buffer `img`) with its offsets.  Returns CBD_OK or CBD_EINVAL.
+struct BatchImage {
+  std::vector<uint8_t> bytes;
+  size_t off_rows, off_sr, off_ss, off_samp, off_tables, off_work, off_row_work;
+  int32_t n_rows, m, n_work, table_slots, max_chunks;
+};
+cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const cbd_row* rows,
+                             int32_t n_rows, const int32_t* tables, int32_t table_slots,
+                             const int32_t* nbps, const cbd_sampling* sp, const float* uniforms,
+                             BatchImage* img);
+void bind_batch(cbd_batch* b, const BatchImage& img, void* dev);
+
+#ifdef __CUDACC__
+// Kernel launchers (stream-ordered).  Each returns cudaGetLastError().
+cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s);
+cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
+                           const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s);
+enum Epilogue : int { kEpiQKV = 0, kEpiResid = 1, kEpiSwiGLU = 2, kEpiLogits = 3 };
+struct EpiArgs {
+  int kind;
+  float* out_f32;            // logits [n][ld]; residual x [n][ld]; q [n][Hq*hd]
+  int ld;
+  uint16_t* out_hi;          // SwiGLU output split
+  uint16_t* out_lo;
+  int ld_act;
+  // QKV epilogue
+  uint16_t* pool;            // layer-0 base of the pool
+  int layer, n_blocks, hq, hkv, hd, max_blocks_per_seq, max_pos;
+  const float* rope_cs;
+  const RowDev* rows;
+  const int32_t* tables;
+  int32_t* err;
+};
+cudaError_t launch_gemm(const cbd_engine* e, const uint16_t* W, int M, int K, const uint16_t* a_hi,
+                        const uint16_t* a_lo, int lda, int n, const EpiArgs& epi, cudaStream_t s);
+cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
+                             cudaStream_t s);
+cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
+                           const SampDev* samp, int32_t* out_tokens, cudaStream_t s);
+#endif
+
+}  // namespace cbd

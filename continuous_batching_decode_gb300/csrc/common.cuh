@@ -1,0 +1,103 @@
+// Device helpers shared by the kernels: bf16 <-> fp32, the hi/lo split,
+// warp reductions and the GEMM epilogues (one definition used by every
+// GEMM variant, so all variants store identical results).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "cbd_internal.h"
+
+namespace cbd {
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ float bf16lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): 16 significant bits.
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  hi = f32_to_bf16(x);
+  lo = f32_to_bf16(x - bf16_to_f32(hi));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void set_err(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Pool element offset of (layer, kv, block, kv head, position-in-block, dim).
+__device__ __forceinline__ size_t pool_off(int layer, int kv, int nblocks, int blk, int hkv, int kvh,
+                                           int hd, int p, int dim) {
+  return ((((size_t)layer * 2 + kv) * nblocks + blk) * hkv + kvh) * (size_t)(kBlock * hd) +
+         (size_t)p * hd + dim;
+}
+
+// Epilogue for a pair of adjacent output features (f, f+1), f even, of
+// one row.  QKV: f, f+1 are RoPE partners (dims i, i + hd/2 of one q or k
+// head, rows interleaved by the engine's repack) or two consecutive v dims.
+// SwiGLU: f = 2i is gate_i and f+1 is up_i.
+__device__ __forceinline__ void epi_pair(const EpiArgs& ep, int f, int row, float a, float b) {
+  if (ep.kind == kEpiSwiGLU) {
+    float y = (a / (1.0f + expf(-a))) * b;
+    uint16_t hi, lo;
+    split_bf16(y, hi, lo);
+    size_t o = (size_t)row * ep.ld_act + (f >> 1);
+    ep.out_hi[o] = hi;
+    ep.out_lo[o] = lo;
+    return;
+  }
+  // QKV
+  const RowDev rw = ep.rows[row];
+  const int hd = ep.hd, half = hd >> 1;
+  const int nq = ep.hq * hd, nk = ep.hkv * hd;
+  if (f < nq + nk) {
+    const int head = (f < nq ? f : f - nq) / hd;
+    const int i = ((f < nq ? f : f - nq) % hd) >> 1;
+    const float2 cs = reinterpret_cast<const float2*>(ep.rope_cs)[(size_t)rw.pos * half + i];
+    const float ra = a * cs.x - b * cs.y;
+    const float rb = b * cs.x + a * cs.y;
+    if (f < nq) {
+      float* qrow = ep.out_f32 + (size_t)row * nq + head * hd;
+      qrow[i] = ra;
+      qrow[i + half] = rb;
+    } else {
+      const int blk = ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)];
+      if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+      size_t o = pool_off(ep.layer, 0, ep.n_blocks, blk, ep.hkv, head, hd, rw.pos & 31, i);
+      ep.pool[o] = f32_to_bf16(ra);
+      ep.pool[o + half] = f32_to_bf16(rb);
+    }
+  } else {
+    const int fv = f - nq - nk;
+    const int head = fv / hd, j = fv % hd;
+    const int blk = ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)];
+    if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+    size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk, ep.hkv, head, hd, rw.pos & 31, j);
+    ep.pool[o] = f32_to_bf16(a);
+    ep.pool[o + 1] = f32_to_bf16(b);
+  }
+}
+
+// Epilogue for one output feature of one row: residual add or logits store.
+__device__ __forceinline__ void epi_single(const EpiArgs& ep, int f, int row, float v) {
+  float* p = ep.out_f32 + (size_t)row * ep.ld + f;
+  if (ep.kind == kEpiResid) *p += v;
+  else *p = v;
+}
+
+__device__ __forceinline__ bool epi_is_pair(int kind) { return kind == kEpiQKV || kind == kEpiSwiGLU; }
+
+}  // namespace cbd

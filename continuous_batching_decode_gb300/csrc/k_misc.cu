@@ -1,0 +1,63 @@
+// Embedding gather and RMSNorm (with the hi/lo bf16 split of its output).
+#include "common.cuh"
+
+namespace cbd {
+
+// x[r][:] = E[token_r][:] as fp32 (the residual stream starts at the
+// embedding row of the row's token).
+__global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
+                             float* __restrict__ x) {
+  const int r = blockIdx.x;
+  const uint16_t* src = E + (size_t)rows[r].token * d;
+  float* dst = x + (size_t)r * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = bf16_to_f32(src[i]);
+}
+
+cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s) {
+  embed_kernel<<<b->n_rows, 256, 0, s>>>(e->embed, b->rows, e->dm.d, e->x);
+  return cudaGetLastError();
+}
+
+// h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.
+// One CTA per output row; `gather` (optional) picks the source row.  The
+// sum of squares is reduced in a fixed order (per-thread strided sums, then
+// a fixed tree), so a row's result does not depend on the other rows.
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
+                               const int32_t* __restrict__ gather, int d, float eps,
+                               uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int src = gather ? gather[r] : r;
+  const float* xr = x + (size_t)src * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = xr[i];
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = ss;
+  __syncthreads();
+  if (w == 0) {
+    float t = l < (int)(blockDim.x >> 5) ? red[l] : 0.f;
+    t = warp_sum(t);
+    if (l == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    uint16_t h, lw;
+    split_bf16(xr[i] * inv * g[i], h, lw);
+    hi[(size_t)r * d + i] = h;
+    lo[(size_t)r * d + i] = lw;
+  }
+}
+
+cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
+                           const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  rmsnorm_kernel<<<n_rows, 256, 0, s>>>(x, g, gather, e->dm.d, e->dm.eps, hi, lo);
+  return cudaGetLastError();
+}
+
+}  // namespace cbd

@@ -1,0 +1,341 @@
+/*
+ * cbd.h -- C ABI of libcbd: one iteration-level ("continuous") batched step
+ * of a decoder-only GQA transformer on one GB300 (sm_103a).
+ *
+ * The method, as the pages state it:
+ *   - "20.3 服务、批处理与流式" (golang.design, under-the-hood ch. 20),
+ *     section 20.3.2 批处理: a decode step reads every weight once for the
+ *     whole batch, costing about (W + B*A)/beta; scheduling is per model
+ *     iteration, so requests join and leave every step; KV lives in a pool
+ *     of fixed-size blocks shared by all slots (Forma: 32 positions per
+ *     block, 512-token prefill chunks); admission reserves blocks for the
+ *     prompt plus part of the answer, because admitting on a free slot alone
+ *     can exhaust the pool with no sequence able to finish; each step runs
+ *     prefill chunks first, then one row per decoding sequence, and rows
+ *     that do not fit wait instead of being evicted; the Scheduler (what to
+ *     run) is kept apart from the Batch (running it).
+ *   - "0.8MB 跑通 Qwen 第 14-1 篇" (developer.aliyun.com), sections 1-3: the
+ *     rows of one step form a dynamic set whose KV is indexed per request,
+ *     computed by batched GQA / normalisation workers; batching must leave
+ *     every output unchanged.
+ *   - Albatross backend article (discosf.com/news/5420690), sections
+ *     "适配器" and "Worker 主循环": per-slot sampling parameters held on the
+ *     device (temperature, top_p, top_k, presence / frequency penalty with
+ *     decay 0.996), applied to every row of the batch after the forward.
+ *
+ * Conventions for every function:
+ *   - Returns a cbd_status (int32): CBD_OK == 0, negative on failure.  On
+ *     failure cbd_last_error() returns a message for the calling thread.
+ *   - No function aborts the process, throws across the ABI or traps the GPU.
+ *   - "host" pointers are ordinary CPU memory, read during the call only;
+ *     "device" pointers are CUDA global memory of the engine's device.
+ *   - Calls that take a `stream` (a cudaStream_t passed as void*, NULL for
+ *     the legacy default stream) are stream-ordered: they enqueue work and
+ *     return; outputs are valid once the stream reaches that point.
+ *   - An engine, its pools and its batches belong to one device and must be
+ *     used from one host thread at a time.
+ *   - Everything libcbd allocates it frees in the matching _destroy call.
+ */
+#ifndef CBD_H
+#define CBD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status */
+#define CBD_OK 0
+#define CBD_EINVAL (-1)        /* an argument or an input row is invalid      */
+#define CBD_ENOMEM (-2)        /* device or host allocation failed            */
+#define CBD_ECUDA (-3)         /* a CUDA runtime/driver call failed           */
+#define CBD_EPOOL (-4)         /* request can never fit the KV pool           */
+#define CBD_EUNSUPPORTED (-5)  /* shape or device not supported               */
+#define CBD_EDEVICE (-6)       /* a kernel flagged an error (cbd_engine_check) */
+#define CBD_EDEADLOCK (-7)     /* scheduler: no running sequence can progress */
+#define CBD_ESTATE (-8)        /* call out of order (e.g. commit w/o plan)    */
+
+typedef int32_t cbd_status;
+
+/* Message of the last failing call on this thread ("" if none).  The
+ * pointer stays valid until the thread's next libcbd call. */
+const char* cbd_last_error(void);
+
+/* Library version string, e.g. "cbd 0.1 sm_103a". */
+const char* cbd_version(void);
+
+/* ------------------------------------------------------------ model */
+/* Shape of the decoder.  Block size is fixed at 32 positions (Forma's
+ * constant, "20.3 服务、批处理与流式" section 20.3.2). */
+typedef struct cbd_config {
+  int32_t n_layers;           /* L                                          */
+  int32_t d_model;            /* d, multiple of 64                          */
+  int32_t n_heads;            /* H_q                                        */
+  int32_t n_kv_heads;         /* H_kv, divides H_q                          */
+  int32_t head_dim;           /* hd, 64 or 128                              */
+  int32_t ffn_dim;            /* F, multiple of 64                          */
+  int32_t vocab;              /* V, <= 65536                                */
+  float rope_base;            /* RoPE base (10000)                          */
+  float rms_eps;              /* RMSNorm epsilon (1e-6)                     */
+  int32_t block_size;         /* must be 32                                 */
+  int32_t max_rows;           /* rows per step (decode + prefill), <= 4096  */
+  int32_t max_slots;          /* sequence slots (penalty counters per slot) */
+  int32_t max_blocks_per_seq; /* block-table width; max positions / 32      */
+} cbd_config;
+
+/* Weights of one layer: bf16, row-major [out][in], no biases. */
+typedef struct cbd_layer_weights {
+  const void* attn_norm;  /* [d]                  RMSNorm gain before attention */
+  const void* wq;         /* [H_q*hd][d]                                        */
+  const void* wk;         /* [H_kv*hd][d]                                       */
+  const void* wv;         /* [H_kv*hd][d]                                       */
+  const void* wo;         /* [d][H_q*hd]                                        */
+  const void* ffn_norm;   /* [d]                  RMSNorm gain before the FFN   */
+  const void* w_gate;     /* [F][d]                                             */
+  const void* w_up;       /* [F][d]                                             */
+  const void* w_down;     /* [d][F]                                             */
+} cbd_layer_weights;
+
+typedef struct cbd_weights {
+  int32_t on_device;                 /* 1: pointers are device memory; 0: host */
+  const void* embed;                 /* [V][d] bf16 (untied from lm_head)      */
+  const void* final_norm;            /* [d] bf16                               */
+  const void* lm_head;               /* [V][d] bf16                            */
+  const cbd_layer_weights* layers;   /* host array of n_layers structs         */
+} cbd_weights;
+
+typedef struct cbd_engine cbd_engine;
+typedef struct cbd_kv_pool cbd_kv_pool;
+typedef struct cbd_batch cbd_batch;
+
+/* Create an engine on the current CUDA device.  The weights are copied and
+ * repacked into an engine-owned device arena (row orders chosen for the
+ * kernels' epilogues); the caller may free its buffers when this returns.
+ * Also allocates the step's activations, workspaces and the per-slot
+ * penalty counters ([max_slots][V] fp32, zero).  Errors: CBD_EINVAL (shape),
+ * CBD_EUNSUPPORTED (not an sm_103 device, or a shape the kernels do not
+ * cover), CBD_ENOMEM, CBD_ECUDA.  *out is NULL on failure. */
+cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights* w, cbd_engine** out);
+cbd_status cbd_engine_destroy(cbd_engine* e);
+
+/* Synchronise the device and report a kernel-detected error: CBD_OK, or
+ * CBD_EDEVICE with the recorded code (a bounded wait that ran out, an index
+ * a kernel refused) in the message; the error word is then cleared. */
+cbd_status cbd_engine_check(cbd_engine* e);
+
+/* Device pointer of the per-slot occurrence counters, [max_slots][V] fp32,
+ * owned by the engine (for inspection and for seeding tests). */
+cbd_status cbd_engine_counters(cbd_engine* e, float** counters);
+
+/* Per-kernel timing.  cbd_engine_profile(e, 1) clears the record and makes
+ * every later launch of this engine bracket itself with CUDA events on its
+ * own stream; cbd_engine_profile(e, 0) stops recording.  cbd_engine_profile_read
+ * synchronises the device and writes up to `cap` per-kernel-class totals
+ * (name, launches, summed event time) to `out`, *n = classes recorded.
+ * Profiling serialises nothing but adds one event pair per launch. */
+typedef struct cbd_kernel_stat {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+} cbd_kernel_stat;
+cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable);
+cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* out, int32_t cap, int32_t* n);
+
+/* Zero slot `slot`'s counters (a request was admitted to it). */
+cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream);
+
+/* ------------------------------------------------------------ KV pool */
+/* Paged KV pool ("20.3 服务、批处理与流式" section 20.3.2: fixed-size blocks
+ * allocated on demand; Forma: 32 positions per block).  Layout, bf16:
+ *     pool[L][2][n_blocks][H_kv][32][hd]     (index 0 = K, 1 = V)
+ * so one (layer, K|V, block, kv head) is a contiguous 32*hd*2-byte tile.
+ * The pool is owned by libcbd; its contents start undefined. */
+cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv_pool** out);
+cbd_status cbd_kv_pool_destroy(cbd_kv_pool* p);
+
+/* Base device pointer and size in bytes of the pool (layout above). */
+cbd_status cbd_kv_pool_data(cbd_kv_pool* p, void** base, uint64_t* bytes, int32_t* n_blocks);
+
+/* ------------------------------------------------------------ step */
+/* One row of a step.  A decode row feeds the request's last token at
+ * position pos = number of cached positions; a prefill row feeds prompt
+ * token `token` at position pos.  Every row writes its K/V at (slot, pos)
+ * and attends causally over positions 0..pos of its slot, so a prefill row
+ * sees the earlier rows of its own chunk.  sample != 0 marks rows whose
+ * logits are produced and sampled (every decode row; the last row of a
+ * prefill chunk that completes its prompt). */
+typedef struct cbd_row {
+  int32_t slot;
+  int32_t token;
+  int32_t pos;
+  int32_t is_prefill;
+  int32_t sample;
+} cbd_row;
+
+/* Per sampled row.  Order (Albatross "Worker 主循环" lists the parameters;
+ * the order is this library's reading): penalty
+ *   l' = (l - presence*[cnt>0]) - frequency*cnt   (fp32, no fused multiply-add)
+ * then greedy argmax (ties to the lowest id) if temperature == 0 or
+ * top_k == 1; else z = l'/temperature, top-k (k > 0) by (z desc, id asc),
+ * top-p: shortest prefix by (p desc, id asc) with mass >= top_p, then the
+ * first id in ascending order whose cumulative kept mass exceeds u * total.
+ * Afterwards cnt[slot][:] *= penalty_decay; cnt[slot][token] += 1.
+ * u = (Philox4x32-10(ctr=(token_index, request_id lo, request_id hi, 0),
+ *                    key=(seed lo, seed hi)).x >> 8) * 2^-24. */
+typedef struct cbd_sampling {
+  float temperature;
+  float top_p;
+  int32_t top_k;
+  float presence_penalty;
+  float frequency_penalty;
+  float penalty_decay;
+  uint64_t seed;
+  uint64_t request_id;
+  uint32_t token_index;   /* index of the token being generated in its request */
+  uint32_t reserved;      /* must be 0 */
+} cbd_sampling;
+
+/* Run one batched step on `stream`.
+ *   rows [n_rows] (host): the step's row set, any order, 1 <= n_rows <= max_rows.
+ *   block_tables (host): [table_slots][max_blocks_per_seq] int32, row s maps
+ *     slot s's logical block b to a physical pool block; entries past
+ *     n_blocks_per_slot[s] are ignored.  Every row's slot must be < table_slots.
+ *   n_blocks_per_slot (host): [table_slots].
+ *   sampling (host): one entry per row with sample != 0, in row order (m of them).
+ *   uniforms (host, nullable): m values in [0,1) that replace the Philox draw.
+ *   out_tokens (device): [m] int32 sampled token ids.
+ *   out_logits (device, nullable): [m][V] fp32 raw logits (before penalty).
+ * Host-side validation (CBD_EINVAL, nothing enqueued): slot/token/pos ranges,
+ * pos < n_blocks_per_slot[slot]*32 <= max_blocks_per_seq*32, physical block
+ * ids inside the pool and not shared between slots used by the step, distinct
+ * positions per slot forming one contiguous run, at most one sampled row per
+ * slot, m <= max_slots, sampling parameters finite (temperature >= 0,
+ * 0 <= top_p <= 1, 0 <= top_k <= V).  The arrays are copied into pinned
+ * staging before return; the caller may reuse them immediately. */
+cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool,
+                    const cbd_row* rows, int32_t n_rows,
+                    const int32_t* block_tables, int32_t table_slots,
+                    const int32_t* n_blocks_per_slot,
+                    const cbd_sampling* sampling, const float* uniforms,
+                    int32_t* out_tokens, float* out_logits, void* stream);
+
+/* A Batch: the same inputs as cbd_step, validated once and kept resident in
+ * device memory, so the step can be re-run (timing, CUDA-graph capture)
+ * without host->device traffic.  Running a batch twice re-writes the same
+ * K/V values and updates the counters again.  cbd_batch_create enqueues the
+ * upload on `stream`.  The batch may outlive neither the engine nor the pool. */
+cbd_status cbd_batch_create(cbd_engine* e, cbd_kv_pool* pool,
+                            const cbd_row* rows, int32_t n_rows,
+                            const int32_t* block_tables, int32_t table_slots,
+                            const int32_t* n_blocks_per_slot,
+                            const cbd_sampling* sampling, const float* uniforms,
+                            cbd_batch** out, void* stream);
+cbd_status cbd_batch_run(cbd_engine* e, cbd_kv_pool* pool, cbd_batch* b,
+                         int32_t* out_tokens, float* out_logits, void* stream);
+cbd_status cbd_batch_destroy(cbd_batch* b);
+
+/* Number of kernel launches one run of this batch enqueues. */
+cbd_status cbd_batch_launches(cbd_batch* b, int32_t* n_launches);
+
+/* Sample m rows of given logits with the same kernel cbd_step uses.
+ *   logits (device) [m][V] fp32 (raw); slots (host) [m], distinct;
+ *   sampling (host) [m]; uniforms (host, nullable) [m]; out_tokens (device) [m].
+ * Updates the slots' counters exactly as a step does. */
+cbd_status cbd_sample(cbd_engine* e, const float* logits, int32_t m,
+                      const int32_t* slots, const cbd_sampling* sampling,
+                      const float* uniforms, int32_t* out_tokens, void* stream);
+
+/* ------------------------------------------------------------ scheduler */
+/* Host-side scheduler ("20.3 服务、批处理与流式" section 20.3.2 and 20.3.4):
+ * first-come first-served admission that reserves blocks for the prompt
+ * plus min(max_tokens, answer_budget) positions, lowest free slot, blocks
+ * handed out lowest id first; each plan puts prefill chunks (admission
+ * order, at most `chunk` rows each) before one decode row per decoding
+ * sequence (longest-waiting first, then admission order) within max_rows;
+ * rows that do not fit wait, nothing is evicted.  Growth beyond a
+ * reservation takes an unreserved free block or waits, and admission
+ * freezes while a row waits for a block.  If every running sequence is
+ * stuck, the youngest is stopped (reason CBD_FINISH_FALLBACK) unless
+ * stall_fallback == 0, in which case cbd_sched_plan returns CBD_EDEADLOCK.
+ * No EOS: a request finishes after max_tokens generated tokens.
+ * reserve_answer == 0 gives the free-slot-only admission the page warns
+ * about (for tests). */
+typedef struct cbd_sched_config {
+  int32_t n_blocks;
+  int32_t block_size;          /* positions per block (32 in the engine)  */
+  int32_t max_slots;
+  int32_t max_rows;
+  int32_t chunk;               /* prefill rows per sequence per step (512) */
+  int32_t answer_budget;       /* reserved answer positions (128)          */
+  int32_t max_blocks_per_seq;
+  int32_t reserve_answer;      /* 1: reservation policy; 0: free slot only */
+  int32_t stall_fallback;      /* 1: stop the youngest when all are stuck  */
+} cbd_sched_config;
+
+typedef struct cbd_request {
+  uint64_t id;                 /* unique per scheduler                     */
+  const int32_t* prompt;       /* host [prompt_len], copied on submit      */
+  int32_t prompt_len;          /* >= 1                                     */
+  int32_t max_tokens;          /* >= 1                                     */
+  cbd_sampling sampling;       /* token_index is filled in by the plan     */
+} cbd_request;
+
+/* A plan: the rows of the next step and everything cbd_step needs.  All
+ * pointers are owned by the scheduler and stay valid until the next
+ * cbd_sched_plan / cbd_sched_commit / cbd_sched_destroy. */
+typedef struct cbd_plan {
+  int32_t n_rows;
+  const cbd_row* rows;                 /* prefill rows first, then decode rows */
+  int32_t n_sampled;
+  const cbd_sampling* sampling;        /* [n_sampled], row order               */
+  const uint64_t* sampled_ids;         /* [n_sampled] request id per sampled row */
+  int32_t table_slots;                 /* = max_slots                          */
+  const int32_t* block_tables;         /* [max_slots][max_blocks_per_seq], -1 pad */
+  const int32_t* n_blocks_per_slot;    /* [max_slots]                          */
+  int32_t n_resets;
+  const int32_t* reset_slots;          /* slots admitted by this plan: zero their counters */
+  int32_t n_stopped;
+  const uint64_t* stopped_ids;         /* requests stopped by the stall fallback */
+} cbd_plan;
+
+#define CBD_FINISH_LENGTH 1
+#define CBD_FINISH_FALLBACK 2
+#define CBD_FINISH_ABORTED 3
+
+typedef struct cbd_finished {
+  uint64_t id;
+  int32_t reason;                      /* CBD_FINISH_*                          */
+  int32_t n_tokens;                    /* generated tokens                      */
+} cbd_finished;
+
+typedef struct cbd_sched_stats {
+  int32_t running, waiting, free_blocks, allocated, reserved, outstanding;
+  int64_t steps, rows_prefill, rows_decode, fallback_stops, stalled_rows;
+} cbd_sched_stats;
+
+typedef struct cbd_sched cbd_sched;
+
+cbd_status cbd_sched_create(const cbd_sched_config* cfg, cbd_sched** out);
+cbd_status cbd_sched_destroy(cbd_sched* s);
+/* Queue a request.  CBD_EPOOL if blocks(prompt + min(max_tokens, budget))
+ * exceeds the pool, or prompt + max_tokens - 1 positions exceed
+ * max_blocks_per_seq blocks; CBD_EINVAL for an empty prompt, max_tokens < 1
+ * or a duplicate id. */
+cbd_status cbd_sched_submit(cbd_sched* s, const cbd_request* r);
+/* Admit and compose the next step.  n_rows == 0 only when nothing runs. */
+cbd_status cbd_sched_plan(cbd_sched* s, cbd_plan* out);
+/* Feed back the step's sampled tokens (host [m], row order of the last
+ * plan).  Writes up to `cap` finished records to `finished` and their count
+ * to *n_finished.  CBD_ESTATE without a preceding plan. */
+cbd_status cbd_sched_commit(cbd_sched* s, const int32_t* tokens, int32_t m,
+                            cbd_finished* finished, int32_t cap, int32_t* n_finished);
+/* Copy up to `cap` generated tokens of a finished request; *n = its count.
+ * CBD_EINVAL if the id has not finished. */
+cbd_status cbd_sched_output(cbd_sched* s, uint64_t id, int32_t* tokens, int32_t cap, int32_t* n);
+cbd_status cbd_sched_stats_get(cbd_sched* s, cbd_sched_stats* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CBD_H */

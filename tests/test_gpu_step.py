@@ -1,0 +1,251 @@
+"""GPU parity tests of the batched step through the C ABI (tiny decoder).
+
+Oracle = the fp64 CPU decoder over contiguous KV.  Bars: logits max-abs
+<= 1e-2 * max|z| and mean-abs <= 2e-3; greedy ids identical outside near
+ties (top-two gap < 1e-3); sampled ids and counters bit-exact when the
+oracle sampler runs on the GPU's own logits; paging and row order leave
+every output bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import continuous_batching_decode_gb300 as cbd
+    from continuous_batching_decode_gb300 import synth
+    from oracle import model as om
+    from oracle import sampler as osamp
+    from tests import gpu_util as gu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    from continuous_batching_decode_gb300 import build
+    build.build()
+    m = gu.Model("tiny", max_rows=128, max_slots=8, mbps=8)
+    yield m
+    m.close()
+
+
+def tiny_setup(tiny, placement_seed):
+    """The tiny workload: slots 0-3 hold 5/17/33/64 prefilled positions;
+    slot 4 gets a 40-token prompt chunk.  Returns pool, tables, rows, etc."""
+    wl = synth.tiny_step(seed=0)
+    need = {s: (c + 1 + 31) // 32 for s, c in enumerate(wl["contexts"])}
+    need[4] = 2
+    rng = np.random.default_rng(placement_seed)
+    tables, nbps = synth.permuted_tables(need, wl["pool_blocks"], 8, rng)
+    pool = tiny.pool(wl["pool_blocks"])
+    for s, prior in enumerate(wl["prior"]):
+        gu.gpu_prefill(tiny, pool, s, prior, tables, nbps, chunk=16)
+    rows = [(s, wl["next_tokens"][s], c, 0, 1) for s, c in enumerate(wl["contexts"])]
+    rows += [(4, t, i, 1, 1 if i == 39 else 0) for i, t in enumerate(wl["prompt"])]
+    greedy = dict(temperature=0.0, penalty_decay=0.996, frequency_penalty=1.0, seed=1, request_id=10)
+    sampled = dict(temperature=1.0, top_p=0.3, top_k=0, frequency_penalty=1.0, penalty_decay=0.996, seed=1234,
+                   request_id=77, token_index=0)
+    sampling = [dict(greedy, request_id=10 + s) for s in range(4)] + [sampled]
+    return wl, pool, tables, nbps, rows, sampling
+
+
+def preload_counters(tiny, wl):
+    cv = gu.counters_view(tiny)
+    cv.zero_()
+    c = np.zeros(tiny.shape["vocab"], np.float32)
+    for t in wl["replay"]:
+        c = osamp.update_counters(c, t, 0.996)
+    cv[4] = torch.from_numpy(c).cuda()
+    return cv, c
+
+
+def test_tiny_step_matches_oracle(tiny):
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 1)
+    cv, c4 = preload_counters(tiny, wl)
+    pre = cv.cpu().numpy().copy()
+    toks, z_gpu = gu.run_step(tiny, pool, rows, tables, nbps, sampling)
+    post = cv.cpu().numpy()
+    # oracle: prefill the same priors, then the same step
+    om_ = tiny.oracle()
+    kv = {s: om.SequenceKV(om_.cfg, 128) for s in range(5)}
+    for s, prior in enumerate(wl["prior"]):
+        om.prefill(om_, kv, s, prior)
+    z = om.step(om_, kv, [(r[0], r[1], r[2], r[4]) for r in rows])
+    mx, mean = gu.assert_logits_close(z_gpu, z, "tiny step")
+    # greedy rows
+    for j in range(4):
+        if not gu.greedy_near_tie(z[j]):
+            l2 = osamp.penalize(z_gpu[j].astype(np.float32), pre[j], 0.0, 1.0)
+            assert toks[j] == int(np.argmax(l2))
+            assert toks[j] == int(np.argmax(z[j]))
+    # sampler on the GPU's own logits: bit-exact tokens and counters
+    slots = [0, 1, 2, 3, 4]
+    for j, s in enumerate(slots):
+        p = gu.sampling_params(sampling[j])
+        u = gu.uniform_of(sampling[j])
+        lf = z_gpu[j].astype(np.float32)
+        if not gu.sampling_near_tie(lf, pre[s], p, u):
+            assert toks[j] == osamp.sample_row(lf, pre[s], p, u), f"row {j}"
+        np.testing.assert_array_equal(post[s], osamp.update_counters(pre[s], int(toks[j]), p.penalty_decay))
+    # KV written by the step and the prefill equals the oracle's bf16 KV
+    # (up to one bf16 ulp where fp32 and fp64 round differently)
+    for s, c in enumerate(wl["contexts"] + [39]):
+        n = c + 1
+        K, V = pool.gather(tables, s, n)
+        for l in range(om_.cfg.n_layers):
+            for A, B in ((K[l], kv[s].K[l][:n]), (V[l], kv[s].V[l][:n])):
+                ulp = np.abs(B) * 2.0 ** -7 + 1e-30
+                assert np.all(np.abs(A - B) <= ulp), f"slot {s} layer {l}"
+    pool.close()
+    print(f"tiny step: max-abs {mx:.3g} mean-abs {mean:.3g}")
+
+
+def test_paging_and_row_order_are_bit_exact(tiny):
+    outs = []
+    for placement in (1, 2):
+        wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, placement)
+        preload_counters(tiny, wl)
+        toks, z = gu.run_step(tiny, pool, rows, tables, nbps, sampling)
+        K0, V0 = pool.gather(tables, 3, 65)
+        outs.append((toks, z, K0[1], V0[1]))
+        if placement == 2:    # same placement, rows reversed
+            preload_counters(tiny, wl)
+            rr = rows[::-1]
+            samp_r = [sampling[4]] + sampling[:4][::-1]
+            pool2 = pool
+            # rebuild the KV the reversed step overwrites with identical values
+            toks_r, z_r = gu.run_step(tiny, pool2, rr, tables, nbps, samp_r)
+            order = [4, 3, 2, 1, 0]
+            np.testing.assert_array_equal(z_r[order], z)
+            np.testing.assert_array_equal(toks_r[order], toks)
+        pool.close()
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][2], outs[1][2])
+    np.testing.assert_array_equal(outs[0][3], outs[1][3])
+
+
+def test_batched_equals_one_row_at_a_time(tiny):
+    """Batching must not change results: the step's rows run one per step
+    (prompt rows in order) give the same logits."""
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
+    g = [dict(temperature=0.0)] * 5
+    toks_b, z_b = gu.run_step(tiny, pool, rows, tables, nbps, g)
+    pool.close()
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
+    zs = []
+    for r in rows:
+        t, z = gu.run_step(tiny, pool, [r], tables, nbps, [dict(temperature=0.0)] if r[4] else [])
+        if r[4]:
+            zs.append(z[0])
+    pool.close()
+    zs = np.array(zs)
+    gu.assert_logits_close(zs, z_b, "batched vs single")
+    np.testing.assert_array_equal(zs, z_b)
+
+
+def test_chunked_prefill_on_gpu(tiny):
+    V = tiny.shape["vocab"]
+    prompt = list(np.random.default_rng(5).integers(0, V, 40))
+    tables = np.array([[3, 7, 0, 0, 0, 0, 0, 0]], np.int32)
+    nbps = np.array([2], np.int32)
+    res = []
+    for chunk in (40, 8, 1):
+        pool = tiny.pool(8)
+        gu.gpu_prefill(tiny, pool, 0, prompt[:-1], tables, nbps, chunk=chunk)
+        _, z = gu.run_step(tiny, pool, [(0, prompt[-1], 39, 1, 1)], tables, nbps, [dict(temperature=0.0)])
+        res.append(z[0])
+        pool.close()
+    for z in res[1:]:
+        gu.assert_logits_close(z[None], res[0][None], "chunking")
+    om_ = tiny.oracle()
+    kv = {0: om.SequenceKV(om_.cfg, 64)}
+    zo = om.prefill(om_, kv, 0, prompt, chunk=8)
+    gu.assert_logits_close(res[0][None], zo[None], "chunked vs oracle")
+
+
+def test_sampler_matches_oracle_on_gpu_logits(tiny):
+    rng = np.random.default_rng(9)
+    V = tiny.shape["vocab"]
+    cv = gu.counters_view(tiny)
+    configs = [dict(temperature=0.0, frequency_penalty=1.0, penalty_decay=0.996),
+               dict(temperature=1.0, top_p=0.3, frequency_penalty=1.0, penalty_decay=0.996),
+               dict(temperature=0.7, top_p=0.9, top_k=50, presence_penalty=0.5, frequency_penalty=0.3,
+                    penalty_decay=0.99),
+               dict(temperature=1.3, top_p=1.0, top_k=0),
+               dict(temperature=1.0, top_k=1),
+               dict(temperature=2.0, top_p=0.05, top_k=7)]
+    mism = 0
+    checked = 0
+    for trial in range(12):
+        m = 6
+        lg = (rng.normal(0, 2.0, (m, V))).astype(np.float32)
+        lg[:, :5] = lg[:, 5:10]                      # exact ties in value
+        c0 = np.where(rng.random((8, V)) < 0.05, rng.integers(1, 5, (8, V)), 0).astype(np.float32)
+        cv.copy_(torch.from_numpy(c0).cuda())
+        slots = list(rng.permutation(8)[:m])
+        samp = [dict(configs[j % len(configs)], seed=trial, request_id=1000 + j, token_index=trial) for j in range(m)]
+        use_u = trial % 2 == 0
+        us = [float(rng.random()) for _ in range(m)] if use_u else None
+        out = torch.zeros(m, dtype=torch.int32, device="cuda")
+        cbd.sample(tiny.e, torch.from_numpy(lg).cuda(), slots, samp, us, out)
+        cbd.engine_check(tiny.e)
+        toks = out.cpu().numpy()
+        post = cv.cpu().numpy()
+        for j in range(m):
+            p = gu.sampling_params(samp[j])
+            u = us[j] if use_u else gu.uniform_of(samp[j])
+            s = slots[j]
+            checked += 1
+            if gu.sampling_near_tie(lg[j], c0[s], p, u):
+                continue
+            want = osamp.sample_row(lg[j], c0[s], p, u)
+            mism += int(toks[j] != want)
+            np.testing.assert_array_equal(post[s], osamp.update_counters(c0[s], int(toks[j]), p.penalty_decay))
+    assert mism == 0, f"{mism} of {checked} sampled ids differ"
+
+
+def test_philox_on_gpu_matches_host(tiny):
+    """Draws with Philox on the device equal draws with the host Philox
+    uniforms passed in (full distribution, so every bit of u matters)."""
+    rng = np.random.default_rng(10)
+    V = tiny.shape["vocab"]
+    m = 8
+    for trial in range(16):
+        lg = torch.from_numpy(rng.normal(0, 0.5, (m, V)).astype(np.float32)).cuda()
+        samp = [dict(temperature=1.0, top_p=1.0, seed=2 ** 40 + trial, request_id=2 ** 33 + j, token_index=trial * 3)
+                for j in range(m)]
+        us = [gu.uniform_of(s) for s in samp]
+        a = torch.zeros(m, dtype=torch.int32, device="cuda")
+        b = torch.zeros(m, dtype=torch.int32, device="cuda")
+        cbd.sample(tiny.e, lg, list(range(m)), samp, None, a)
+        cbd.sample(tiny.e, lg, list(range(m)), samp, us, b)
+        np.testing.assert_array_equal(a.cpu().numpy(), b.cpu().numpy())
+
+
+def test_step_validation(tiny):
+    pool = tiny.pool(8)
+    tok = torch.zeros(4, dtype=torch.int32, device="cuda")
+    tables = np.array([[0, 1, 0, 0, 0, 0, 0, 0], [2, 3, 0, 0, 0, 0, 0, 0]], np.int32)
+    nbps = np.array([2, 2], np.int32)
+    g = [dict(temperature=0.0)]
+    ok = [(0, 1, 0, 1, 0), (0, 2, 1, 1, 1)]
+    cbd.step(tiny.e, pool.p, ok, tables, nbps, g, None, tok)
+    bad_cases = [
+        ([(0, 1, 64, 0, 1)], tables, nbps, g),                    # pos beyond the slot's blocks
+        ([(0, 99999, 0, 0, 1)], tables, nbps, g),                 # token out of range
+        ([(0, 1, 0, 1, 0), (0, 1, 2, 1, 1)], tables, nbps, g),    # gap in positions
+        ([(0, 1, 0, 1, 0), (0, 1, 0, 1, 1)], tables, nbps, g),    # repeated position
+        ([(0, 1, 0, 1, 1), (0, 1, 1, 1, 1)], tables, nbps, g * 2),  # two sampled rows, one slot
+        ([(0, 1, 0, 0, 1), (1, 1, 0, 0, 1)], np.array([[0, 1] + [0] * 6, [1, 3] + [0] * 6], np.int32), nbps, g * 2),
+        ([(0, 1, 0, 0, 1)], np.array([[0, 9] + [0] * 6, [2, 3] + [0] * 6], np.int32), nbps, g),  # block outside pool
+        ([(5, 1, 0, 0, 1)], tables, nbps, g),                     # slot outside the table
+        ([(0, 1, 0, 0, 1)], tables, nbps, [dict(temperature=-1.0)]),
+        ([(0, 1, 0, 0, 1)], tables, nbps, [dict(temperature=1.0, top_p=1.5)]),
+    ]
+    for rows, tb, nb, sp in bad_cases:
+        with pytest.raises(cbd.CbdError) as ei:
+            cbd.step(tiny.e, pool.p, rows, tb, nb, sp, None, tok)
+        assert ei.value.status == cbd.EINVAL, rows
+    cbd.engine_check(tiny.e)
+    pool.close()
