@@ -87,15 +87,19 @@ def test_tiny_step_matches_oracle(tiny):
         if not gu.sampling_near_tie(lf, pre[s], p, u):
             assert toks[j] == osamp.sample_row(lf, pre[s], p, u), f"row {j}"
         np.testing.assert_array_equal(post[s], osamp.update_counters(pre[s], int(toks[j]), p.penalty_decay))
-    # KV written by the step and the prefill equals the oracle's bf16 KV
-    # (up to one bf16 ulp where fp32 and fp64 round differently)
+    # KV written by the step and the prefill equals the oracle's bf16 KV:
+    # one bf16 ulp where fp32 and fp64 round differently, plus an absolute
+    # slack for near-zero entries (the GEMM input h carries ~2^-17 relative
+    # error from its hi/lo bf16 split, which exceeds the ulp of tiny values)
     for s, c in enumerate(wl["contexts"] + [39]):
         n = c + 1
         K, V = pool.gather(tables, s, n)
         for l in range(om_.cfg.n_layers):
             for A, B in ((K[l], kv[s].K[l][:n]), (V[l], kv[s].V[l][:n])):
-                ulp = np.abs(B) * 2.0 ** -7 + 1e-30
-                assert np.all(np.abs(A - B) <= ulp), f"slot {s} layer {l}"
+                tol = np.abs(B) * 2.0 ** -7 + 1e-4 * np.sqrt(np.mean(B * B))
+                bad = np.abs(A - B) > tol
+                assert not bad.any(), f"slot {s} layer {l}: {bad.sum()} of {bad.size}, worst {np.abs(A - B).max():.3g}"
+                assert np.mean(A != B) < 0.01, f"slot {s} layer {l}: {np.mean(A != B):.3%} entries differ"
     pool.close()
     print(f"tiny step: max-abs {mx:.3g} mean-abs {mean:.3g}")
 
