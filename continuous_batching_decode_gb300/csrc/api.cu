@@ -256,6 +256,9 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
+  const size_t max_t = std::max({V, 2 * F, qo, d}) / 128 + 1;
+  const long long max_units = (long long)max_t * (long long)std::max<size_t>(1, (R + 127) / 128);
+  const size_t o_part = W.take((size_t)2 * e->sm_count * 128 * 128 * 4), o_ctr = W.take((size_t)max_units * 4);
   e->work_bytes = W.off;
   cudaError_t e3 = cudaMalloc(&e->work, e->work_bytes);
   if (e3 != cudaSuccess) { cleanup(); return cuda_fail(e3, "cudaMalloc(workspaces)"); }
@@ -272,6 +275,9 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
   e->counters = reinterpret_cast<float*>(wb + o_cn);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
+  e->tcw.part = reinterpret_cast<float*>(wb + o_part);
+  e->tcw.counters = reinterpret_cast<int32_t*>(wb + o_ctr);
+  e->tcw.max_units = max_units;
   e3 = cudaMemset(e->work, 0, e->work_bytes);
   // ---- staging for cbd_step / cbd_sample
   const size_t stage_bytes = align_up(R * sizeof(RowDev), 16) + 2 * align_up(S * 4, 16) +
@@ -288,6 +294,33 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     cbd_engine* raw = e.release();
     cbd_engine_destroy(raw);
     return cuda_fail(e3, "engine workspaces");
+  }
+  // tensor maps for the tcgen05 GEMM: weights (box 128 rows) and the
+  // activation matrices in each layout the step uses (box 16 rows)
+  {
+    const int L = dm.L;
+    e->tmaps.resize((size_t)4 * L + 1 + 6);
+    bool ok = true;
+    for (int l = 0; l < L && ok; ++l) {
+      const LayerDev& Ld = e->layers[l];
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, d, qo, d, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, hqd, d, hqd, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, d, 2 * F, d, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, F, d, F, 128);
+    }
+    const size_t a0 = (size_t)4 * L + 1;
+    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, d, V, d, 128);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 3], e->act_lo, hqd, R, hqd, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 4], e->ffn_hi, F, R, F, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 5], e->ffn_lo, F, R, F, 16);
+    if (!ok) {
+      cbd_engine* raw = e.release();
+      cbd_engine_destroy(raw);
+      return fail(CBD_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point missing or bad layout)");
+    }
   }
   e->step_batch = new cbd_batch();
   e->step_batch->owns_dev = false;
@@ -359,6 +392,16 @@ extern "C" cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* ou
     ++k;
   }
   *n = std::min(k, cap);
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_max_rows) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (path < 0 || path > 2) return fail(CBD_EINVAL, "gemm path must be 0, 1 or 2");
+  if (gemv_max_rows < 0) return fail(CBD_EINVAL, "gemv_max_rows must be >= 0");
+  e->gemm_path = path;
+  e->gemv_max_rows = gemv_max_rows;
   return CBD_OK;
 }
 
@@ -603,26 +646,35 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   res.kind = kEpiResid; res.out_f32 = e->x; res.ld = dm.d; res.err = e->err;
   EpiArgs glu{};
   glu.kind = kEpiSwiGLU; glu.out_hi = e->ffn_hi; glu.out_lo = e->ffn_lo; glu.ld_act = dm.F; glu.err = e->err;
+  const size_t a0 = (size_t)4 * dm.L + 1;
+  const CUtensorMap* tm = e->tmaps.data();
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
     qkv.layer = l;
+    const GemmOp g_qkv{L.w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d,
+                       {&tm[4 * l + 0], &tm[a0 + 0], &tm[a0 + 1], dm.qkv_out, dm.d}};
+    const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd}};
+    const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, e->act_hi, e->act_lo, dm.d,
+                      {&tm[4 * l + 2], &tm[a0 + 0], &tm[a0 + 1], 2 * dm.F, dm.d}};
+    const GemmOp g_dn{L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F,
+                      {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F}};
     if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.attn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
                   "rmsnorm")))
       return st;
-    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, L.w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d, n, qkv, s); }),
+    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, s); }),
                   "qkv")))
       return st;
     if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, s); }), "attention"))) return st;
-    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, n, res, s); }),
+    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res, s); }),
                   "o_proj")))
       return st;
     if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.ffn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
                   "rmsnorm")))
       return st;
-    if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, L.w_gu, 2 * dm.F, dm.d, e->act_hi, e->act_lo, dm.d, n, glu, s); }),
+    if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, g_gu, n, glu, s); }),
                   "gate_up")))
       return st;
-    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F, n, res, s); }),
+    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res, s); }),
                   "down")))
       return st;
     launches += 8;
@@ -635,7 +687,9 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
       return st;
     EpiArgs lo{};
     lo.kind = kEpiLogits; lo.out_f32 = lg; lo.ld = dm.V; lo.err = e->err;
-    if ((st = chk(timed(e, kcLM, s, [&] { return launch_gemm(e, e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d, b->m, lo, s); }),
+    const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
+                      {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d}};
+    if ((st = chk(timed(e, kcLM, s, [&] { return launch_gemm(e, g_lm, b->m, lo, s); }),
                   "lm_head")))
       return st;
     if ((st = chk(timed(e, kcSamp, s, [&] { return launch_sampler(e, lg, b->m, b->sampled_slots, b->samp, out_tokens, s); }),

@@ -9,6 +9,7 @@
 
 #include "../../include/cbd.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace cbd {
@@ -57,6 +58,29 @@ struct LayerDev {
   const uint16_t* w_down;            // [d][F]
 };
 
+// One weight matrix as the tcgen05 GEMM sees it: tensor maps of the
+// weights and of the hi / lo activation matrices it multiplies.
+struct TcGemm {
+  const CUtensorMap* w;
+  const CUtensorMap* hi;
+  const CUtensorMap* lo;
+  int M, K;
+};
+struct TcWork {
+  float* part;            // [2 * sm_count][128][128] partial tiles
+  int32_t* counters;      // [max_units] arrival counters (zero between launches)
+  long long max_units;
+};
+// A GEMM of the step: weights W [M][K] times activations (hi + lo) [n][lda].
+struct GemmOp {
+  const uint16_t* W;
+  int M, K;
+  const uint16_t* a_hi;
+  const uint16_t* a_lo;
+  int lda;
+  TcGemm tc;
+};
+
 struct Dims {
   int L, d, hq, hkv, hd, F, V, qkv_out, max_rows, max_slots, max_blocks_per_seq;
   float rope_base, eps;
@@ -103,6 +127,11 @@ struct cbd_engine {
   } stage[2];
   int stage_idx = 0;
   cbd_batch* step_batch = nullptr;    // batch object reused by cbd_step
+  // tcgen05 GEMM: tensor maps (built once), partial tiles, counters
+  std::vector<CUtensorMap> tmaps;     // per layer: qkv, o, gu, down; then lm_head; then activations
+  cbd::TcWork tcw{};
+  int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
+  int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   // optional per-launch timing (cbd_engine_profile)
   bool prof = false;
   struct ProfRec { int cls; cudaEvent_t a, b; };
@@ -169,8 +198,13 @@ struct EpiArgs {
   const int32_t* tables;
   int32_t* err;
 };
-cudaError_t launch_gemm(const cbd_engine* e, const uint16_t* W, int M, int K, const uint16_t* a_hi,
-                        const uint16_t* a_lo, int lda, int n, const EpiArgs& epi, cudaStream_t s);
+cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
+                        int n, const EpiArgs& ep, cudaStream_t s);
+cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const TcWork& w, int sm_count,
+                           cudaStream_t s);
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
+                    uint32_t box_rows);
+cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& epi, cudaStream_t s);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                              cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,

@@ -110,11 +110,13 @@ cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const cbd_engine* e, const uint16_t* W, int M, int K, const uint16_t* a_hi,
-                        const uint16_t* a_lo, int lda, int n, const EpiArgs& ep, cudaStream_t s) {
-  (void)e;
+// Path choice: the CUDA-core GEMV for a handful of rows, the tcgen05 GEMM
+// above that (or as forced by cbd_engine_set_gemm_path).
+cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& ep, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  return launch_gemv(W, M, K, a_hi, a_lo, lda, n, ep, s);
+  const bool tc = e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
+  if (tc) return launch_gemm_tc(op.tc, n, ep, e->tcw, e->sm_count, s);
+  return launch_gemv(op.W, op.M, op.K, op.a_hi, op.a_lo, op.lda, n, ep, s);
 }
 
 }  // namespace cbd

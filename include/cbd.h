@@ -124,6 +124,13 @@ cbd_status cbd_engine_destroy(cbd_engine* e);
  * a kernel refused) in the message; the error word is then cleared. */
 cbd_status cbd_engine_check(cbd_engine* e);
 
+/* Choose how the step's weight contractions run: path 0 = automatic (the
+ * CUDA-core GEMV for up to gemv_max_rows rows, tcgen05 tensor cores above),
+ * 1 = always the CUDA-core GEMV, 2 = always tcgen05.  Both paths compute
+ * the same sums (fp32 accumulation of bf16 weights times hi + lo bf16
+ * activations); they differ only in summation order.  Default: 0 and 4. */
+cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_max_rows);
+
 /* Device pointer of the per-slot occurrence counters, [max_slots][V] fp32,
  * owned by the engine (for inspection and for seeding tests). */
 cbd_status cbd_engine_counters(cbd_engine* e, float** counters);

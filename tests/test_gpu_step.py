@@ -20,11 +20,14 @@ if torch.cuda.is_available():
     from tests import gpu_util as gu
 
 
-@pytest.fixture(scope="module")
-def tiny():
+@pytest.fixture(scope="module", params=[1, 2], ids=["gemv", "tcgen05"])
+def tiny(request):
+    """The tiny decoder with every contraction forced onto one GEMM path:
+    1 = CUDA-core GEMV, 2 = tcgen05 tensor cores."""
     from continuous_batching_decode_gb300 import build
     build.build()
-    m = gu.Model("tiny", max_rows=128, max_slots=8, mbps=8)
+    m = gu.Model("tiny", max_rows=512, max_slots=8, mbps=16)
+    cbd.engine_set_gemm_path(m.e, request.param)
     yield m
     m.close()
 
@@ -36,7 +39,7 @@ def tiny_setup(tiny, placement_seed):
     need = {s: (c + 1 + 31) // 32 for s, c in enumerate(wl["contexts"])}
     need[4] = 2
     rng = np.random.default_rng(placement_seed)
-    tables, nbps = synth.permuted_tables(need, wl["pool_blocks"], 8, rng)
+    tables, nbps = synth.permuted_tables(need, wl["pool_blocks"], 16, rng)
     pool = tiny.pool(wl["pool_blocks"])
     for s, prior in enumerate(wl["prior"]):
         gu.gpu_prefill(tiny, pool, s, prior, tables, nbps, chunk=16)
@@ -151,7 +154,7 @@ def test_batched_equals_one_row_at_a_time(tiny):
 def test_chunked_prefill_on_gpu(tiny):
     V = tiny.shape["vocab"]
     prompt = list(np.random.default_rng(5).integers(0, V, 40))
-    tables = np.array([[3, 7, 0, 0, 0, 0, 0, 0]], np.int32)
+    tables = np.array([[3, 7] + [0] * 14], np.int32)
     nbps = np.array([2], np.int32)
     res = []
     for chunk in (40, 8, 1):
@@ -230,7 +233,7 @@ def test_philox_on_gpu_matches_host(tiny):
 def test_step_validation(tiny):
     pool = tiny.pool(8)
     tok = torch.zeros(4, dtype=torch.int32, device="cuda")
-    tables = np.array([[0, 1, 0, 0, 0, 0, 0, 0], [2, 3, 0, 0, 0, 0, 0, 0]], np.int32)
+    tables = np.array([[0, 1] + [0] * 14, [2, 3] + [0] * 14], np.int32)
     nbps = np.array([2, 2], np.int32)
     g = [dict(temperature=0.0)]
     ok = [(0, 1, 0, 1, 0), (0, 2, 1, 1, 1)]
@@ -241,8 +244,8 @@ def test_step_validation(tiny):
         ([(0, 1, 0, 1, 0), (0, 1, 2, 1, 1)], tables, nbps, g),    # gap in positions
         ([(0, 1, 0, 1, 0), (0, 1, 0, 1, 1)], tables, nbps, g),    # repeated position
         ([(0, 1, 0, 1, 1), (0, 1, 1, 1, 1)], tables, nbps, g * 2),  # two sampled rows, one slot
-        ([(0, 1, 0, 0, 1), (1, 1, 0, 0, 1)], np.array([[0, 1] + [0] * 6, [1, 3] + [0] * 6], np.int32), nbps, g * 2),
-        ([(0, 1, 0, 0, 1)], np.array([[0, 9] + [0] * 6, [2, 3] + [0] * 6], np.int32), nbps, g),  # block outside pool
+        ([(0, 1, 0, 0, 1), (1, 1, 0, 0, 1)], np.array([[0, 1] + [0] * 14, [1, 3] + [0] * 14], np.int32), nbps, g * 2),
+        ([(0, 1, 0, 0, 1)], np.array([[0, 9] + [0] * 14, [2, 3] + [0] * 14], np.int32), nbps, g),  # block outside pool
         ([(5, 1, 0, 0, 1)], tables, nbps, g),                     # slot outside the table
         ([(0, 1, 0, 0, 1)], tables, nbps, [dict(temperature=-1.0)]),
         ([(0, 1, 0, 0, 1)], tables, nbps, [dict(temperature=1.0, top_p=1.5)]),
@@ -253,3 +256,20 @@ def test_step_validation(tiny):
         assert ei.value.status == cbd.EINVAL, rows
     cbd.engine_check(tiny.e)
     pool.close()
+
+
+def test_gemm_paths_agree_on_long_prefill(tiny):
+    """A 300-row prefill chunk (several 128-row N tiles on the tensor-core
+    path) gives the oracle's logits on either GEMM path."""
+    V = tiny.shape["vocab"]
+    prompt = list(np.random.default_rng(21).integers(0, V, 300))
+    tables = np.array([list(np.random.default_rng(22).permutation(16)[:10]) + [0] * 6], np.int32)
+    nbps = np.array([10], np.int32)
+    pool = tiny.pool(16)
+    rows = [(0, t, i, 1, 1 if i == 299 else 0) for i, t in enumerate(prompt)]
+    toks, z = gu.run_step(tiny, pool, rows, tables, nbps, [dict(temperature=0.0)])
+    pool.close()
+    om_ = tiny.oracle()
+    kv = {0: om.SequenceKV(om_.cfg, 320)}
+    zo = om.prefill(om_, kv, 0, prompt)
+    gu.assert_logits_close(z, zo[None], "300-row prefill")
