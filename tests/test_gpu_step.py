@@ -90,21 +90,37 @@ def test_tiny_step_matches_oracle(tiny):
         if not gu.sampling_near_tie(lf, pre[s], p, u):
             assert toks[j] == osamp.sample_row(lf, pre[s], p, u), f"row {j}"
         np.testing.assert_array_equal(post[s], osamp.update_counters(pre[s], int(toks[j]), p.penalty_decay))
-    # KV written by the step and the prefill equals the oracle's bf16 KV:
-    # one bf16 ulp where fp32 and fp64 round differently, plus an absolute
-    # slack for near-zero entries (the GEMM input h carries ~2^-17 relative
-    # error from its hi/lo bf16 split, which exceeds the ulp of tiny values)
+    # KV written by the step and the prefill equals the oracle's bf16 KV.
+    # Layer 0 depends only on the embedding and one GEMM: one bf16 ulp where
+    # fp32 and fp64 round differently, plus a small absolute slack near zero
+    # (the GEMM input carries ~2^-17 relative error from its hi/lo split).
+    # Deeper layers inherit the layer-0 entries that rounded to different bf16
+    # neighbours (each weighs ~1/context in attention), so they are bounded in
+    # aggregate: a few ulps, and most entries identical.
     for s, c in enumerate(wl["contexts"] + [39]):
         n = c + 1
         K, V = pool.gather(tables, s, n)
         for l in range(om_.cfg.n_layers):
             for A, B in ((K[l], kv[s].K[l][:n]), (V[l], kv[s].V[l][:n])):
-                tol = np.abs(B) * 2.0 ** -7 + 1e-4 * np.sqrt(np.mean(B * B))
+                rms = np.sqrt(np.mean(B * B))
+                if l == 0:
+                    tol = np.abs(B) * 2.0 ** -7 + 1e-4 * rms
+                    assert np.mean(A != B) < 0.01, f"slot {s} layer 0: {np.mean(A != B):.3%} entries differ"
+                else:
+                    tol = np.abs(B) * 2.0 ** -5 + 2e-3 * rms
+                    assert np.mean(A != B) < 0.15, f"slot {s} layer {l}: {np.mean(A != B):.3%} entries differ"
                 bad = np.abs(A - B) > tol
                 assert not bad.any(), f"slot {s} layer {l}: {bad.sum()} of {bad.size}, worst {np.abs(A - B).max():.3g}"
-                assert np.mean(A != B) < 0.01, f"slot {s} layer {l}: {np.mean(A != B):.3%} entries differ"
+    # With the GPU's own KV as the oracle's prior state the only differences
+    # left are the step's arithmetic: far inside the logit tolerance.
+    prior = {s: c for s, c in enumerate(wl["contexts"])}
+    kv2 = gu.oracle_kv_from_gpu(tiny, pool, tables, prior)
+    kv2[4] = om.SequenceKV(om_.cfg, 64)
+    z2 = om.step(om_, kv2, [(r[0], r[1], r[2], r[4]) for r in rows])
+    err2 = np.abs(z_gpu - z2)
+    assert err2.mean() <= 2e-4 and err2.max() <= 2e-3 * np.abs(z2).max(), (err2.mean(), err2.max())
     pool.close()
-    print(f"tiny step: max-abs {mx:.3g} mean-abs {mean:.3g}")
+    print(f"tiny step: max-abs {mx:.3g} mean-abs {mean:.3g}; over GPU KV mean-abs {err2.mean():.3g}")
 
 
 def test_paging_and_row_order_are_bit_exact(tiny):
