@@ -112,6 +112,7 @@ PROTOS = {
     "cbd_batch_destroy": (c_i32, [c_vp]),
     "cbd_batch_launches": (c_i32, [c_vp, _P(c_i32)]),
     "cbd_sample": (c_i32, [c_vp, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
+    "cbd_sample_static": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
     "cbd_sched_create": (c_i32, [_P(SchedConfig), _P(c_vp)]),
     "cbd_sched_destroy": (c_i32, [c_vp]),
     "cbd_sched_submit": (c_i32, [c_vp, _P(Request)]),
@@ -321,6 +322,20 @@ def sample(e, logits, slots, sampling, uniforms, out_tokens, stream=None) -> Non
     sa = sampling_array(sampling)
     ua, uap = _f32(uniforms)
     _check(lib().cbd_sample(e, _ptr(logits), len(sl), slp, sa, uap, _ptr(out_tokens), _stream(stream)))
+
+
+SAMPLE_STATIC_MAX_ROWS = 16
+SAMPLE_STATIC_MAX_VOCAB = 65536
+
+
+def sample_static(logits, counters, slots, sampling, uniforms, out_tokens, stream=None) -> None:
+    """Allocation-free sampler: logits [m][V] and counters [rows][V] are
+    caller-owned device tensors; see cbd_sample_static in include/cbd.h."""
+    sl, slp = _i32(slots)
+    sa = sampling_array(sampling)
+    ua, uap = _f32(uniforms)
+    _check(lib().cbd_sample_static(_ptr(logits), len(sl), int(logits.shape[1]), _ptr(counters),
+                                   int(counters.shape[0]), slp, sa, uap, _ptr(out_tokens), _stream(stream)))
 
 
 # ------------------------------------------------------------------ scheduler

@@ -1,0 +1,117 @@
+// cbd_sample_static: the step's sampler for callers that cannot allocate
+// device memory.
+//
+// Some embedders cannot call cudaMalloc: a host framework whose caching
+// allocator has already reserved the device's memory budget (a raw
+// cudaMalloc there either fails or fragments the pool the framework
+// manages), or a latency-critical serving loop that forbids allocation after
+// warm-up because an allocation can synchronise the device and stall every
+// other stream.  Those callers still own their inputs and outputs; what the
+// sampler needs beyond them -- a scratch row of temperature-scaled logits
+// per sampled row, plus the rows' slots and parameters on the device -- lives
+// here in one file-scope device array of fixed size, so this entry point
+// allocates nothing.
+//
+// The array is part of the library image: every GPU that loads libcbd holds
+// it until the process exits.  It is shared by every call on a device and
+// keeps the last call's contents; everything a call reads from it is written
+// earlier by the same call.  Calls whose work overlaps on the GPU (different
+// streams, no ordering between them) race on the array.
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cbd {
+
+// The sampler kernel of k_sampler.cu (launched unchanged).
+__global__ void sampler_kernel(const float* __restrict__ logits, int V, float* __restrict__ counters,
+                               const int32_t* __restrict__ slots, const SampDev* __restrict__ samp,
+                               float* __restrict__ scratch, int32_t* __restrict__ out, int32_t* err);
+
+namespace {
+
+constexpr int kStaticRows = CBD_SAMPLE_STATIC_MAX_ROWS;
+constexpr int kStaticVocab = CBD_SAMPLE_STATIC_MAX_VOCAB;
+constexpr size_t kZBytes = (size_t)kStaticRows * kStaticVocab * sizeof(float);
+constexpr size_t kSampOff = kZBytes;
+constexpr size_t kSlotOff = kSampOff + ((kStaticRows * sizeof(SampDev) + 255) / 256) * 256;
+constexpr size_t kAreaBytes = kSlotOff + ((kStaticRows * sizeof(int32_t) + 255) / 256) * 256;
+
+// [rows][vocab] fp32 scratch, then [rows] SampDev, then [rows] int32 slots.
+static __device__ __align__(256) unsigned char g_sample_area[kAreaBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned char* g_area_ptr[kMaxDevices] = {};
+
+// Device address of g_sample_area on the current device (looked up once per
+// device; host code cannot use the symbol's name as a device address).
+cbd_status area_on_current_device(unsigned char** out) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CBD_EUNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_area_ptr[dev]) {
+    void* p = nullptr;
+    ce = cudaGetSymbolAddress(&p, g_sample_area);
+    if (ce != cudaSuccess || !p)
+      return fail(CBD_ECUDA, "cudaGetSymbolAddress(sampler scratch): %s", cudaGetErrorString(ce));
+    g_area_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_area_ptr[dev];
+  return CBD_OK;
+}
+
+}  // namespace
+}  // namespace cbd
+
+using namespace cbd;
+
+extern "C" cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t vocab, float* counters,
+                                        int32_t counter_rows, const int32_t* slots, const cbd_sampling* sampling,
+                                        const float* uniforms, int32_t* out_tokens, void* stream) {
+  clear_error();
+  if (m < 1 || m > kStaticRows)
+    return fail(CBD_EINVAL, "cbd_sample_static: m = %d rows, the static scratch holds 1..%d", m, kStaticRows);
+  if (vocab < 1 || vocab > kStaticVocab)
+    return fail(CBD_EINVAL, "cbd_sample_static: vocab = %d, the static scratch holds 1..%d", vocab, kStaticVocab);
+  if (!logits || !counters || !slots || !sampling || !out_tokens)
+    return fail(CBD_EINVAL, "cbd_sample_static: NULL argument");
+  if (counter_rows < 1) return fail(CBD_EINVAL, "cbd_sample_static: counter_rows must be >= 1");
+  SampDev sd[kStaticRows];
+  int32_t sl[kStaticRows];
+  for (int32_t j = 0; j < m; ++j) {
+    if (slots[j] < 0 || slots[j] >= counter_rows)
+      return fail(CBD_EINVAL, "cbd_sample_static: slot %d outside the %d counter rows", slots[j], counter_rows);
+    for (int32_t i = 0; i < j; ++i)
+      if (slots[i] == slots[j]) return fail(CBD_EINVAL, "cbd_sample_static: slot %d appears twice", slots[j]);
+    const cbd_sampling& s = sampling[j];
+    if (!std::isfinite(s.temperature) || s.temperature < 0.f || !std::isfinite(s.top_p) || s.top_p < 0.f ||
+        s.top_p > 1.f || s.top_k < 0 || s.top_k > vocab || s.reserved || !std::isfinite(s.presence_penalty) ||
+        !std::isfinite(s.frequency_penalty) || !std::isfinite(s.penalty_decay))
+      return fail(CBD_EINVAL, "cbd_sample_static: sampling %d invalid", j);
+    if (uniforms && !(uniforms[j] >= 0.f && uniforms[j] < 1.f))
+      return fail(CBD_EINVAL, "cbd_sample_static: uniform %d not in [0,1)", j);
+    sd[j] = SampDev{s.temperature, s.top_p, s.presence_penalty, s.frequency_penalty, s.penalty_decay, s.top_k,
+                    (uint32_t)(s.seed & 0xffffffffu), (uint32_t)(s.seed >> 32),
+                    (uint32_t)(s.request_id & 0xffffffffu), (uint32_t)(s.request_id >> 32), s.token_index,
+                    uniforms ? uniforms[j] : -1.0f};
+    sl[j] = slots[j];
+  }
+  unsigned char* area = nullptr;
+  cbd_status st = area_on_current_device(&area);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t ce = cudaMemcpyAsync(area + kSampOff, sd, (size_t)m * sizeof(SampDev), cudaMemcpyHostToDevice, s);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpyAsync(area + kSlotOff, sl, (size_t)m * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: parameter copy: %s", cudaGetErrorString(ce));
+  sampler_kernel<<<m, 1024, 0, s>>>(logits, vocab, counters, reinterpret_cast<const int32_t*>(area + kSlotOff),
+                                    reinterpret_cast<const SampDev*>(area + kSampOff),
+                                    reinterpret_cast<float*>(area), out_tokens, nullptr);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: launch: %s", cudaGetErrorString(ce));
+  return CBD_OK;
+}

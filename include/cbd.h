@@ -253,6 +253,32 @@ cbd_status cbd_sample(cbd_engine* e, const float* logits, int32_t m,
                       const int32_t* slots, const cbd_sampling* sampling,
                       const float* uniforms, int32_t* out_tokens, void* stream);
 
+/* Allocation-free sampler.  The paper has no counterpart to this entry
+ * point; it exists for callers that cannot call cudaMalloc -- for example a
+ * host framework whose caching allocator already holds the device memory
+ * budget, or a serving loop that forbids allocation after warm-up because an
+ * allocation can synchronise the device.  It runs the same sampler kernel as
+ * cbd_sample on caller-owned buffers, with its scratch (one fp32 row per
+ * sampled row plus the rows' parameters) in a fixed-size device array inside
+ * libcbd instead of engine memory:
+ *   logits (device) [m][vocab] fp32; counters (device) [counter_rows][vocab]
+ *   fp32, updated in place exactly as a step updates the engine's counters;
+ *   slots (host) [m], distinct, < counter_rows; sampling (host) [m];
+ *   uniforms (host, nullable) [m]; out_tokens (device) [m].
+ * Limits: 1 <= m <= CBD_SAMPLE_STATIC_MAX_ROWS, 1 <= vocab <=
+ * CBD_SAMPLE_STATIC_MAX_VOCAB; larger sizes return CBD_EINVAL with a message.
+ * The array (4 MB + 1 KB) is held by every GPU that loads libcbd until the
+ * process exits.  The first call on a device looks up the array's device
+ * address; make that first call before any stream capture.  All calls on a
+ * device share the array and it keeps the last call's contents (each call
+ * writes what it reads); calls that overlap on the GPU race.  Calls no
+ * cudaMalloc, cudaFree or other allocating routine. */
+#define CBD_SAMPLE_STATIC_MAX_ROWS 16
+#define CBD_SAMPLE_STATIC_MAX_VOCAB 65536
+cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t vocab, float* counters,
+                             int32_t counter_rows, const int32_t* slots, const cbd_sampling* sampling,
+                             const float* uniforms, int32_t* out_tokens, void* stream);
+
 /* ------------------------------------------------------------ scheduler */
 /* Host-side scheduler ("20.3 服务、批处理与流式" section 20.3.2 and 20.3.4):
  * first-come first-served admission that reserves blocks for the prompt
