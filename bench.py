@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
+    ap.add_argument("--attn-path", type=int, default=0, help="0 mma.sync tensor cores, 1 CUDA cores")
     return ap.parse_args()
 
 
@@ -290,6 +291,7 @@ def run_cbd(args):
     cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"])
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
+    cbd.engine_set_attention_path(e, args.attn_path)
     if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
         del w
     torch.cuda.empty_cache()
@@ -422,7 +424,8 @@ def run_cbd(args):
                                     "32-position blocks, top_p 0.3 sampling"),
                        "B": B, "shape": args.shape, "layers": s["n_layers"], "mean_ctx": float(np.mean(wl["ctx"])),
                        "l2": "inputs larger than L2 (weights 14.5 GB + KV); no flush",
-                       "parallelism": f"replicas x{world}", "gemm_path": args.gemm_path},
+                       "parallelism": f"replicas x{world}", "gemm_path": args.gemm_path,
+                       "attn_path": args.attn_path},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu}
     if rank == 0:

@@ -100,6 +100,7 @@ PROTOS = {
     "cbd_slot_reset": (c_i32, [c_vp, c_i32, c_vp]),
     "cbd_engine_profile": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_gemm_path": (c_i32, [c_vp, c_i32, c_i32]),
+    "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_profile_read": (c_i32, [c_vp, _P(KernelStat), c_i32, _P(c_i32)]),
     "cbd_kv_pool_create": (c_i32, [c_vp, c_i32, _P(c_vp)]),
     "cbd_kv_pool_destroy": (c_i32, [c_vp]),
@@ -208,6 +209,11 @@ def engine_counters(e) -> int:
 def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 4) -> None:
     """0 automatic, 1 CUDA-core GEMV only, 2 tcgen05 only."""
     _check(lib().cbd_engine_set_gemm_path(e, path, gemv_max_rows))
+
+
+def engine_set_attention_path(e, path: int) -> None:
+    """0 tensor cores (mma.sync), 1 CUDA cores."""
+    _check(lib().cbd_engine_set_attention_path(e, path))
 
 
 def engine_profile(e, enable: bool) -> None:

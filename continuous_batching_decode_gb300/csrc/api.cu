@@ -45,13 +45,21 @@ enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, 
 
 
 // ---------------------------------------------------------------- repack
-// dst[r][:] = src[perm[r]][:] (bf16 rows of K elements).
-__global__ void permute_rows_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
+// Weight layout for the kernels: row r of the (row-permuted) matrix, column
+// k, lives at [r / 128][k / 64][r % 128][k % 64] -- 16 KB tiles of 128 rows
+// by 64 columns, each one contiguous.  perm (nullable) gives the source row
+// of each destination row.
+__global__ void permute_tile_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
                                     const int32_t* __restrict__ perm, int K) {
   const int r = blockIdx.x;
-  const uint16_t* s = src + (size_t)perm[r] * K;
-  uint16_t* d = dst + (size_t)r * K;
-  for (int i = threadIdx.x; i < K; i += blockDim.x) d[i] = s[i];
+  const int sr = perm ? perm[r] : r;
+  const int KB = K / 64;
+  const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)sr * K);
+  for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
+    const int k = c * 8;
+    uint4* d = reinterpret_cast<uint4*>(dst + ((((size_t)(r >> 7) * KB + (k >> 6)) << 7) + (r & 127)) * 64 + (k & 63));
+    *d = s[c];
+  }
 }
 __global__ void bf16_to_f32_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -181,15 +189,16 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     CBD_CUDA(cudaGetLastError());
     return CBD_OK;
   };
-  auto permuted = [&](size_t off, const std::vector<int32_t>& perm, int K) -> cbd_status {
-    CBD_CUDA(cudaMemcpy(perm_d, perm.data(), perm.size() * 4, cudaMemcpyHostToDevice));
-    permute_rows_kernel<<<(int)perm.size(), 256>>>(reinterpret_cast<uint16_t*>(base + off),
-                                                   static_cast<uint16_t*>(tmp), perm_d, K);
+  // tmp (row-major [M][K]) -> arena (tiled), rows permuted when perm is given
+  auto tiled = [&](size_t off, const std::vector<int32_t>* perm, int M, int K) -> cbd_status {
+    if (perm) CBD_CUDA(cudaMemcpy(perm_d, perm->data(), perm->size() * 4, cudaMemcpyHostToDevice));
+    permute_tile_kernel<<<M, 256>>>(reinterpret_cast<uint16_t*>(base + off), static_cast<uint16_t*>(tmp),
+                                    perm ? perm_d : nullptr, K);
     CBD_CUDA(cudaGetLastError());
     CBD_CUDA(cudaDeviceSynchronize());
     return CBD_OK;
   };
-  // Row orders: q and k rows within each head become (i, i + hd/2) pairs so
+  // Row orders (then tiled, see permute_tile_kernel): q and k rows within each head become (i, i + hd/2) pairs so
   // the RoPE partners are adjacent outputs; gate/up rows interleave so
   // SwiGLU partners are adjacent.  v, o, down, embed, lm_head keep their order.
   std::vector<int32_t> perm_qkv(qo), perm_gu(2 * F);
@@ -206,7 +215,8 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   cbd_status s2 = CBD_OK;
 #define TRY(x) do { s2 = (x); if (s2) { free_tmp(); cleanup(); return s2; } } while (0)
   TRY(upload(base + o_embed, w->embed, V * d * 2, ondev));
-  TRY(upload(base + o_lm, w->lm_head, V * d * 2, ondev));
+  TRY(upload(tmp, w->lm_head, V * d * 2, ondev));
+  TRY(tiled(o_lm, nullptr, (int)V, (int)d));
   TRY(gain(o_fn, w->final_norm));
   e->layers.resize(dm.L);
   for (int l = 0; l < dm.L; ++l) {
@@ -217,12 +227,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     TRY(upload(t, lw.wq, hqd * d * 2, ondev));
     TRY(upload(t + hqd * d * 2, lw.wk, (size_t)dm.hkv * dm.hd * d * 2, ondev));
     TRY(upload(t + (hqd + (size_t)dm.hkv * dm.hd) * d * 2, lw.wv, (size_t)dm.hkv * dm.hd * d * 2, ondev));
-    TRY(permuted(o_qkv[l], perm_qkv, (int)d));
-    TRY(upload(base + o_o[l], lw.wo, d * hqd * 2, ondev));
+    TRY(tiled(o_qkv[l], &perm_qkv, (int)qo, (int)d));
+    TRY(upload(t, lw.wo, d * hqd * 2, ondev));
+    TRY(tiled(o_o[l], nullptr, (int)d, (int)hqd));
     TRY(upload(t, lw.w_gate, F * d * 2, ondev));
     TRY(upload(t + F * d * 2, lw.w_up, F * d * 2, ondev));
-    TRY(permuted(o_gu[l], perm_gu, (int)d));
-    TRY(upload(base + o_dn[l], lw.w_down, d * F * 2, ondev));
+    TRY(tiled(o_gu[l], &perm_gu, (int)(2 * F), (int)d));
+    TRY(upload(t, lw.w_down, d * F * 2, ondev));
+    TRY(tiled(o_dn[l], nullptr, (int)d, (int)F));
     LayerDev& L = e->layers[l];
     L.attn_norm = reinterpret_cast<float*>(base + o_an[l]);
     L.ffn_norm = reinterpret_cast<float*>(base + o_fnn[l]);
@@ -303,13 +315,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     bool ok = true;
     for (int l = 0; l < L && ok; ++l) {
       const LayerDev& Ld = e->layers[l];
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, d, qo, d, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, hqd, d, hqd, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, d, 2 * F, d, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, F, d, F, 128);
+      // tiled weights: a [M*K/64][64] matrix, one 128-row box per 16 KB tile
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, 128);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, 128);
     }
     const size_t a0 = (size_t)4 * L + 1;
-    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, d, V, d, 128);
+    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, 128);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);
@@ -405,6 +418,14 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
   return CBD_OK;
 }
 
+extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (path < 0 || path > 1) return fail(CBD_EINVAL, "attention path must be 0 or 1");
+  e->attn_path = path;
+  return CBD_OK;
+}
+
 extern "C" cbd_status cbd_engine_counters(cbd_engine* e, float** counters) {
   if (!e || !counters) return fail(CBD_EINVAL, "NULL argument");
   *counters = e->counters;
@@ -434,6 +455,11 @@ extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv
   void* b = nullptr;
   CBD_CUDA(cudaMalloc(&b, bytes));
   p->base = static_cast<uint16_t*>(b);
+  const uint64_t rows = (uint64_t)e->dm.L * 2 * (uint64_t)n_blocks * e->dm.hkv * kBlock;
+  if (rows >= (1ull << 31) || !make_tmap_bf16(&p->tmap, p->base, e->dm.hd, rows, e->dm.hd, 32)) {
+    cudaFree(b);
+    return fail(CBD_EUNSUPPORTED, "KV pool too large for a tensor map (%llu rows)", (unsigned long long)rows);
+  }
   *out = p.release();
   return CBD_OK;
 }

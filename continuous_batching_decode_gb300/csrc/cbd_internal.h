@@ -19,7 +19,7 @@ cbd_status fail(cbd_status code, const char* fmt, ...);
 void clear_error();
 
 constexpr int kBlock = 32;          // positions per KV block
-constexpr int kAttnChunk = 256;     // positions per attention split (8 blocks)
+constexpr int kAttnChunk = 128;     // positions per attention split (4 blocks)
 constexpr int kMaxVocab = 65536;
 
 // Device error codes written to the engine's error word (first one wins).
@@ -132,6 +132,7 @@ struct cbd_engine {
   cbd::TcWork tcw{};
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
+  int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   // optional per-launch timing (cbd_engine_profile)
   bool prof = false;
   struct ProfRec { int cls; cudaEvent_t a, b; };
@@ -144,6 +145,7 @@ struct cbd_kv_pool {
   uint16_t* base = nullptr;
   int32_t n_blocks = 0;
   size_t bytes = 0;
+  CUtensorMap tmap;                   // the pool as [L*2*n_blocks*H_kv*32][hd] bf16, box 32 x 64, 128B swizzle
 };
 
 struct cbd_batch {

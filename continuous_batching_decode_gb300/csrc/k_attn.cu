@@ -9,15 +9,23 @@
 // sees the earlier rows of its own chunk (causal chunked prefill) with no
 // separate mask.
 //
-// Split-K: each row's positions are cut into fixed 256-position chunks (a
+// Split-K: each row's positions are cut into fixed 128-position chunks (a
 // host-built work list); one CTA handles one (chunk, KV head) for the H_q /
 // H_kv query heads that share the KV head, keeping an online softmax
-// (running max, running sum, unnormalised output).  A second kernel merges
+// (running max, running sum, unnormalised output).
+//
+// Two kernels compute the chunk: attn_mma_kernel (default) stages the four
+// 32-position K and V tiles of the chunk in shared memory with TMA (128-byte
+// swizzle) and runs q.K and P.V on the tensor cores with mma.sync, in a
+// swapped form -- positions (or head dims) on the MMA's M side, the <= 8
+// query heads of the KV group on its N side -- with q and P split into hi +
+// lo bf16 halves so the products keep ~16 significant bits; K and V are
+// bf16 already.  attn_partial_kernel is the CUDA-core version.  A second kernel merges
 // the chunks of each (row, head) in chunk order and writes the output as
 // hi + lo bf16 halves for the O projection.  The chunking depends only on
 // the row's position, and the merge order is fixed, so a row's result does
 // not depend on the other rows of the step or on block placement.
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace cbd {
 
@@ -137,6 +145,230 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(
   }
 }
 
+// ---------------------------------------------------------------- tensor cores
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// (a, b) -> packed bf16x2 hi and lo halves (a in the low 16 bits)
+__device__ __forceinline__ void split_pack(float a, float b, uint32_t& hi, uint32_t& lo) {
+  uint16_t ah, al, bh, bl;
+  split_bf16(a, ah, al);
+  split_bf16(b, bh, bl);
+  hi = (uint32_t)ah | ((uint32_t)bh << 16);
+  lo = (uint32_t)al | ((uint32_t)bl << 16);
+}
+// Byte offset of (row, 16-byte chunk c) in a 128-byte-swizzled 32 x 64 bf16 tile.
+__device__ __forceinline__ uint32_t swz(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
+
+constexpr int kAttnWarps = 4;
+
+template <int HD>
+constexpr int attn_mma_smem() {
+  return kAttnWarps * 2 * 32 * HD * 2 + kAttnWarps * 8 * 32 * 4 + 1024;
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(128) attn_mma_kernel(const __grid_constant__ CUtensorMap tmKV,
+                                                       const float* __restrict__ q, const RowDev* __restrict__ rows,
+                                                       const int32_t* __restrict__ tables,
+                                                       const AttnWork* __restrict__ work, int layer, int n_blocks,
+                                                       int hkv, int mbps, float* __restrict__ part_o,
+                                                       float* __restrict__ part_ml, int32_t* err) {
+  static_assert(G >= 1 && G <= 8, "a KV group must fit the MMA's N = 8");
+  constexpr int TILE = 32 * HD * 2;       // bytes of one 32-position K or V tile
+  constexpr int KS = HD / 16;             // 16-dim steps
+  extern __shared__ uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t bar[kAttnWarps];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tid4 = lane & 3;
+  const uint32_t raw = tc::smem_u32(sm_raw);
+  uint8_t* base = sm_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* kt = base + warp * 2 * TILE;   // this warp's K tile, then V tile
+  uint8_t* vt = kt + TILE;
+  float* Pw = reinterpret_cast<float*>(base + kAttnWarps * 2 * TILE) + warp * 8 * 32;
+  const AttnWork wk = work[blockIdx.x];
+  const int kvh = blockIdx.y;
+  const RowDev rw = rows[wk.row];
+  const int hq = hkv * G;
+  const int end = min(wk.start + kAttnChunk, rw.pos + 1);
+  const int p0 = wk.start + warp * 32;
+  int blk = -1;
+  if (p0 < end) blk = tables[(size_t)rw.slot * mbps + (p0 >> 5)];
+  const bool have = p0 < end && blk >= 0 && blk < n_blocks;
+  if (p0 < end && !have && lane == 0) set_err(err, kDevBadBlock);
+  const int nvalid = have ? min(32, end - p0) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kAttnWarps; ++w) tc::mbar_init(&bar[w], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (have && lane == 0) {
+    tc::mbar_arrive_expect_tx(&bar[warp], 2 * TILE);
+    const size_t rk = ((((size_t)layer * 2 + 0) * n_blocks + blk) * hkv + kvh) * 32;
+    const size_t rv = ((((size_t)layer * 2 + 1) * n_blocks + blk) * hkv + kvh) * 32;
+#pragma unroll
+    for (int h = 0; h < HD / 64; ++h) {
+      tc::tma_load_2d(kt + h * 4096, &tmKV, h * 64, (int)rk, &bar[warp]);
+      tc::tma_load_2d(vt + h * 4096, &tmKV, h * 64, (int)rv, &bar[warp]);
+    }
+  }
+  // q of the group's heads (scaled by 1/sqrt(hd)) as hi / lo B fragments
+  const float scale = 1.0f / sqrtf((float)HD);
+  uint32_t qh[KS][2], ql[KS][2];
+  const float* qrow = q + ((size_t)wk.row * hq + kvh * G) * HD;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int dd = ks * 16 + r * 8 + tid4 * 2;
+      float a = 0.f, b = 0.f;
+      if (gid < G) {
+        a = qrow[gid * HD + dd] * scale;
+        b = qrow[gid * HD + dd + 1] * scale;
+      }
+      split_pack(a, b, qh[ks][r], ql[ks][r]);
+    }
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[KS][4];
+#pragma unroll
+  for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[dt][c] = 0.f;
+  bool ok = have;
+  if (have) ok = tc::mbar_wait(&bar[warp], 0, err, &abort_flag);
+  if (ok) {
+    // rows past the valid positions may hold stale bits: zero their V
+    for (int i = lane; i < (32 - nvalid) * (HD / 8); i += 32) {
+      const int r = nvalid + i / (HD / 8), ch = i % (HD / 8);
+      *reinterpret_cast<uint4*>(vt + (ch >> 3) * 4096 + swz(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    const uint32_t ks_base = tc::smem_u32(kt), vs_base = tc::smem_u32(vt);
+    const int mi = lane >> 3, ri = lane & 7;
+    // S^T[pos][head] = K q^T
+    float sc[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sc[mt][c] = 0.f;
+      const int r = mt * 16 + (mi & 1) * 8 + ri;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int dc = ks * 16 + (mi >> 1) * 8;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
+        mma_bf16_16816(sc[mt], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+        mma_bf16_16816(sc[mt], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+      }
+    }
+    // softmax over this block's positions, per head (heads tid4*2, tid4*2+1)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v[4] = {sc[0][hh], sc[0][hh + 2], sc[1][hh], sc[1][hh + 2]};
+      const int pos[4] = {gid, gid + 8, 16 + gid, 24 + gid};
+      float bm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (pos[i] >= nvalid) v[i] = -INFINITY;
+        bm = fmaxf(bm, v[i]);
+      }
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+      float bs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float pv = pos[i] < nvalid ? expf(v[i] - bm) : 0.f;
+        bs += pv;
+        Pw[(tid4 * 2 + hh) * 32 + pos[i]] = pv;
+      }
+      bs += __shfl_xor_sync(0xffffffffu, bs, 4);
+      bs += __shfl_xor_sync(0xffffffffu, bs, 8);
+      bs += __shfl_xor_sync(0xffffffffu, bs, 16);
+      m[hh] = bm;
+      l[hh] = bs;
+    }
+    __syncwarp();
+    // P as hi / lo B fragments: B[pos][head] = P[head][pos]
+    uint32_t ph[2][2], pl[2][2];
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int j = k2 * 16 + r * 8 + tid4 * 2;
+        split_pack(Pw[gid * 32 + j], Pw[gid * 32 + j + 1], ph[k2][r], pl[k2][r]);
+      }
+    // O^T[dim][head] = V^T P^T
+#pragma unroll
+    for (int dt = 0; dt < KS; ++dt) {
+      const int dc = dt * 16 + (mi & 1) * 8;
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int r = k2 * 16 + (mi >> 1) * 8 + ri;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vs_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
+        mma_bf16_16816(o[dt], a0, a1, a2, a3, ph[k2][0], ph[k2][1]);
+        mma_bf16_16816(o[dt], a0, a1, a2, a3, pl[k2][0], pl[k2][1]);
+      }
+    }
+  }
+  // merge the four warps' blocks (fixed warp order) into the chunk's partial
+  __syncthreads();
+  float* mo = reinterpret_cast<float*>(base);            // [4][8][HD]
+  float* mml = mo + kAttnWarps * 8 * HD;                  // [4][8][2]
+#pragma unroll
+  for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int head = tid4 * 2 + (c & 1);
+      const int dim = dt * 16 + gid + (c >= 2 ? 8 : 0);
+      mo[(warp * 8 + head) * HD + dim] = o[dt][c];
+    }
+  if (gid == 0) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mml[(warp * 8 + tid4 * 2 + hh) * 2] = ok ? m[hh] : -INFINITY;
+      mml[(warp * 8 + tid4 * 2 + hh) * 2 + 1] = ok ? l[hh] : 0.f;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * HD; i += blockDim.x) {
+    const int g = i / HD, dd = i % HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mml[(w * 8 + g) * 2]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float mw = mml[(w * 8 + g) * 2];
+      const float c = mw == -INFINITY ? 0.f : expf(mw - M);
+      L += mml[(w * 8 + g) * 2 + 1] * c;
+      O += mo[(w * 8 + g) * HD + dd] * c;
+    }
+    const size_t h = (size_t)blockIdx.x * hq + kvh * G + g;
+    part_o[h * HD + dd] = O;
+    if (dd == 0) { part_ml[h * 2] = M; part_ml[h * 2 + 1] = L; }
+  }
+}
+
 // Merge a row's chunks for one head (chunk order), normalise, split.
 template <int HD>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
@@ -164,9 +396,22 @@ template <int HD, int G>
 static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                  cudaStream_t s) {
   const Dims& dm = e->dm;
-  attn_partial_kernel<HD, G><<<dim3(b->n_work, dm.hkv), 128, 0, s>>>(
-      e->q, p->base, b->rows, b->tables, b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq,
-      e->attn_o, e->attn_ml, e->err);
+  if (e->attn_path == 0) {
+    constexpr int smem = attn_mma_smem<HD>();
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t ce = cudaFuncSetAttribute(attn_mma_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (ce != cudaSuccess) return ce;
+      attr = true;
+    }
+    attn_mma_kernel<HD, G><<<dim3(b->n_work, dm.hkv), 128, smem, s>>>(
+        p->tmap, e->q, b->rows, b->tables, b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o,
+        e->attn_ml, e->err);
+  } else {
+    attn_partial_kernel<HD, G><<<dim3(b->n_work, dm.hkv), 128, 0, s>>>(
+        e->q, p->base, b->rows, b->tables, b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq,
+        e->attn_o, e->attn_ml, e->err);
+  }
   attn_combine_kernel<HD><<<dim3(b->n_rows, dm.hq), HD, 0, s>>>(e->attn_o, e->attn_ml, b->row_work, dm.hq,
                                                                  e->act_hi, e->act_lo);
   return cudaGetLastError();

@@ -2,6 +2,9 @@
 //
 //   Y[n][m] = sum_k W[m][k] * (a_hi[n][k] + a_lo[n][k])    (fp32 accumulate)
 //
+// Weights are stored pre-tiled, [M/128][K/64][128][64] bf16, so the
+// 128 x 64 box each pipeline stage loads is one contiguous 16 KB read.
+//
 // then one of the shared epilogues (RoPE + paged KV append, residual add,
 // SwiGLU, logits).  The decode step reads every weight once for all rows
 // ("0.8MB 跑通 Qwen 第 14-1 篇", section 1; "20.3 服务、批处理与流式", section
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc::mbar_wait(&empty_bar[s], ph ^ 1, a.err, abort_p)) { ok = false; break; }
           uint8_t* st = ring + (size_t)s * kStageBytes;
           tc::mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-          tc::tma_load_2d(st, &tmW, kb * kTcBK, t * kTcBM, &full_bar[s]);
+          tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb) * kTcBM, &full_bar[s]);
 #pragma unroll
           for (int j = 0; j < NT / 16; ++j) {
             tc::tma_load_2d(st + kWBytes + j * 16 * 128, &tmH, kb * kTcBK, nt * NT + j * 16, &full_bar[s]);
@@ -232,8 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         } else {
+          float4* dst = reinterpret_cast<float4*>(mypart + (size_t)m_loc * NT + c0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) mypart[(size_t)(c0 + j) * kTcBM + m_loc] = v[j];
+          for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
       }
       tc::tc_fence_before();
@@ -250,21 +254,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (last_flag) {
           __threadfence();
+          // sum the partial tiles in k order (fixed), 16 columns at a time,
+          // each thread reading its own contiguous columns
 #pragma unroll 1
-          for (int j = 0; j < NT; ++j) {
-            const int row = nt * NT + j;
-            float acc = 0.f;
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll 1
             for (int c = c_first; c <= c_last; ++c) {
               const long long bc = tc_begin(c, total, G);
               const int slot = 2 * c + (bc >= first_it ? 0 : 1);
-              acc += __ldcg(a.part + (size_t)slot * NT * kTcBM + (size_t)j * kTcBM + m_loc);
+              const float4* src = reinterpret_cast<const float4*>(a.part + (size_t)slot * NT * kTcBM +
+                                                                   (size_t)m_loc * NT + c0);
+              float4 t4[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) t4[j] = __ldcg(src + j);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                acc[4 * j] += t4[j].x; acc[4 * j + 1] += t4[j].y; acc[4 * j + 2] += t4[j].z; acc[4 * j + 3] += t4[j].w;
+              }
             }
-            const float pv = __shfl_xor_sync(0xffffffffu, acc, 1);
-            if (row < a.n) {
-              if (epi_is_pair(ep.kind)) {
-                if (!(lane & 1)) epi_pair(ep, m, row, acc, pv);
-              } else {
-                epi_single(ep, m, row, acc);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int row = nt * NT + c0 + j;
+              const float pv = __shfl_xor_sync(0xffffffffu, acc[j], 1);
+              if (row < a.n) {
+                if (epi_is_pair(ep.kind)) {
+                  if (!(lane & 1)) epi_pair(ep, m, row, acc[j], pv);
+                } else {
+                  epi_single(ep, m, row, acc[j]);
+                }
               }
             }
           }

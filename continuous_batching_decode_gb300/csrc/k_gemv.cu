@@ -5,6 +5,8 @@
 // reads each weight once for all rows ("0.8MB 跑通 Qwen 第 14-1 篇", section 1;
 // "20.3 服务、批处理与流式" section 20.3.2, cost (W + B*A)/beta).
 //
+// Weights are read from the pre-tiled layout [M/128][K/64][128][64] that
+// the tensor-core path uses (16-byte chunks stay contiguous).
 // CTA = 8 warps; a warp owns 4 consecutive output features, so RoPE and
 // SwiGLU partners (features 2i, 2i+1) live in one warp.  Activations for
 // the CTA's NB rows are staged in shared memory 256 columns at a time as
@@ -49,9 +51,13 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
     if (f0 < M) {
       const int kc = lane * 8;
       uint4 w[kGemvFeat];
+      const int kk = k0 + kc, KB = K / 64;
 #pragma unroll
-      for (int i = 0; i < kGemvFeat; ++i)
-        w[i] = __ldg(reinterpret_cast<const uint4*>(W + (size_t)(f0 + i) * K + k0 + kc));
+      for (int i = 0; i < kGemvFeat; ++i) {
+        const int f = f0 + i;
+        w[i] = __ldg(reinterpret_cast<const uint4*>(
+            W + ((((size_t)(f >> 7) * KB + (kk >> 6)) << 7) + (f & 127)) * 64 + (kk & 63)));
+      }
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
         const float4 x0 = *reinterpret_cast<const float4*>(&act[j][kc]);

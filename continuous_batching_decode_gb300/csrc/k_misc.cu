@@ -1,4 +1,6 @@
 // Embedding gather and RMSNorm (with the hi/lo bf16 split of its output).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace cbd {
@@ -19,20 +21,22 @@ cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.
-// One CTA per output row; `gather` (optional) picks the source row.  The
-// sum of squares is reduced in a fixed order (per-thread strided sums, then
-// a fixed tree), so a row's result does not depend on the other rows.
+// One CTA per output row, one float4 per thread and pass; `gather`
+// (optional) picks the source row.  The sum of squares is reduced in a fixed
+// order (per-thread sums, then a fixed tree), so a row's result does not
+// depend on the other rows.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
                                const int32_t* __restrict__ gather, int d, float eps,
                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const int src = gather ? gather[r] : r;
-  const float* xr = x + (size_t)src * d;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
+  const int n4 = d >> 2;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = xr[i];
-    ss += v * v;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = warp_sum(ss);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -45,18 +49,26 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
   }
   __syncthreads();
   const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    uint16_t h, lw;
-    split_bf16(xr[i] * inv * g[i], h, lw);
-    hi[(size_t)r * d + i] = h;
-    lo[(size_t)r * d + i] = lw;
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  uint2* h2 = reinterpret_cast<uint2*>(hi + (size_t)r * d);
+  uint2* l2 = reinterpret_cast<uint2*>(lo + (size_t)r * d);
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i], gg = g4[i];
+    uint16_t h[4], q[4];
+    split_bf16(v.x * inv * gg.x, h[0], q[0]);
+    split_bf16(v.y * inv * gg.y, h[1], q[1]);
+    split_bf16(v.z * inv * gg.z, h[2], q[2]);
+    split_bf16(v.w * inv * gg.w, h[3], q[3]);
+    h2[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+    l2[i] = make_uint2(q[0] | ((uint32_t)q[1] << 16), q[2] | ((uint32_t)q[3] << 16));
   }
 }
 
 cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
                            const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<n_rows, 256, 0, s>>>(x, g, gather, e->dm.d, e->dm.eps, hi, lo);
+  const int threads = std::min(1024, e->dm.d / 4);
+  rmsnorm_kernel<<<n_rows, threads, 0, s>>>(x, g, gather, e->dm.d, e->dm.eps, hi, lo);
   return cudaGetLastError();
 }
 

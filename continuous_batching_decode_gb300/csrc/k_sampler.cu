@@ -47,6 +47,12 @@ __device__ __forceinline__ uint32_t ord_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Radix histograms: every warp owns a private [256] count and mass
+// histogram in dynamic shared memory (no atomics contend across warps);
+// the block then sums them bin by bin in warp order.
+constexpr int kHistBins = 256;
+constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * (sizeof(uint32_t) + sizeof(unsigned long long));
+
 struct SampShared {
   unsigned long long wsum[32];
   uint32_t wkey[32];
@@ -94,6 +100,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       float* __restrict__ scratch,
                                                       int32_t* __restrict__ out, int32_t* err) {
   __shared__ SampShared sh;
+  extern __shared__ __align__(16) uint8_t samp_dyn[];
+  unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn);             // [32][256]
+  uint32_t* whc = reinterpret_cast<uint32_t*>(samp_dyn + (kST / 32) * kHistBins * 8);  // [32][256]
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const SampDev sp = samp[row];
   const float* lg = logits + (size_t)row * V;
@@ -147,11 +156,17 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       uint32_t prefix = 0, mask = 0;
       unsigned long long rem = (unsigned long long)sp.top_k;
       for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kST) sh.hc[i] = 0;
+        for (int i = tid; i < (kST / 32) * kHistBins; i += kST) whc[i] = 0;
         __syncthreads();
         for (int v = i0; v < i1; ++v) {
           const uint32_t k = ord_key(z[v]);
-          if ((k & mask) == prefix) atomicAdd(&sh.hc[(k >> shift) & 255u], 1u);
+          if ((k & mask) == prefix) atomicAdd(&whc[w * kHistBins + ((k >> shift) & 255u)], 1u);
+        }
+        __syncthreads();
+        for (int b = tid; b < kHistBins; b += kST) {
+          uint32_t c = 0;
+          for (int ww = 0; ww < kST / 32; ++ww) c += whc[ww * kHistBins + b];
+          sh.hc[b] = c;
         }
         __syncthreads();
         if (tid == 0) {
@@ -208,7 +223,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         uint32_t prefix = 0, mask = 0;
         unsigned long long above = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int i = tid; i < 256; i += kST) { sh.hc[i] = 0; sh.hm[i] = 0; }
+          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
           __syncthreads();
           for (int v = i0; v < i1; ++v) {
             const float zv = z[v];
@@ -216,9 +231,20 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             const uint32_t k = ord_key(zv);
             if ((k & mask) == prefix) {
               const uint32_t dg = (k >> shift) & 255u;
-              atomicAdd(&sh.hc[dg], 1u);
-              atomicAdd(&sh.hm[dg], mass(zv));
+              atomicAdd(&whc[w * kHistBins + dg], 1u);
+              atomicAdd(&whm[w * kHistBins + dg], mass(zv));
             }
+          }
+          __syncthreads();
+          for (int b = tid; b < kHistBins; b += kST) {
+            uint32_t c = 0;
+            unsigned long long mm = 0;
+            for (int ww = 0; ww < kST / 32; ++ww) {
+              c += whc[ww * kHistBins + b];
+              mm += whm[ww * kHistBins + b];
+            }
+            sh.hc[b] = c;
+            sh.hm[b] = mm;
           }
           __syncthreads();
           if (tid == 0) {
@@ -307,12 +333,24 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   }
 }
 
+// One launch of the sampler over m rows (shared by cbd_step, cbd_sample and
+// cbd_sample_static).
+cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
+                           const SampDev* samp, float* scratch, int32_t* out_tokens, int32_t* err, cudaStream_t s) {
+  if (m <= 0) return cudaSuccess;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t ce = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampDynSmem);
+    if (ce != cudaSuccess) return ce;
+    attr = true;
+  }
+  sampler_kernel<<<m, kST, kSampDynSmem, s>>>(logits, V, counters, slots, samp, scratch, out_tokens, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
                            const SampDev* samp, int32_t* out_tokens, cudaStream_t s) {
-  if (m <= 0) return cudaSuccess;
-  sampler_kernel<<<m, kST, 0, s>>>(logits, e->dm.V, e->counters, slots, samp, e->samp_scratch, out_tokens,
-                                   e->err);
-  return cudaGetLastError();
+  return sampler_launch(logits, m, e->dm.V, e->counters, slots, samp, e->samp_scratch, out_tokens, e->err, s);
 }
 
 }  // namespace cbd

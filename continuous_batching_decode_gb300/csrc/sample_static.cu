@@ -24,10 +24,9 @@
 
 namespace cbd {
 
-// The sampler kernel of k_sampler.cu (launched unchanged).
-__global__ void sampler_kernel(const float* __restrict__ logits, int V, float* __restrict__ counters,
-                               const int32_t* __restrict__ slots, const SampDev* __restrict__ samp,
-                               float* __restrict__ scratch, int32_t* __restrict__ out, int32_t* err);
+// The sampler launch of k_sampler.cu (same kernel as cbd_sample).
+cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
+                           const SampDev* samp, float* scratch, int32_t* out_tokens, int32_t* err, cudaStream_t s);
 
 namespace {
 
@@ -108,10 +107,9 @@ extern "C" cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t 
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(area + kSlotOff, sl, (size_t)m * sizeof(int32_t), cudaMemcpyHostToDevice, s);
   if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: parameter copy: %s", cudaGetErrorString(ce));
-  sampler_kernel<<<m, 1024, 0, s>>>(logits, vocab, counters, reinterpret_cast<const int32_t*>(area + kSlotOff),
-                                    reinterpret_cast<const SampDev*>(area + kSampOff),
-                                    reinterpret_cast<float*>(area), out_tokens, nullptr);
-  ce = cudaGetLastError();
+  ce = sampler_launch(logits, m, vocab, counters, reinterpret_cast<const int32_t*>(area + kSlotOff),
+                      reinterpret_cast<const SampDev*>(area + kSampOff), reinterpret_cast<float*>(area), out_tokens,
+                      nullptr, s);
   if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: launch: %s", cudaGetErrorString(ce));
   return CBD_OK;
 }
