@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/cbd.h"
@@ -180,6 +181,23 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
 void bind_batch(cbd_batch* b, const BatchImage& img, void* dev);
 
 #ifdef __CUDACC__
+// Launch with programmatic stream serialisation (the kernel may start while
+// the previous kernel on the stream finishes; it synchronises with
+// griddepcontrol.wait).
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
 // Kernel launchers (stream-ordered).  Each returns cudaGetLastError().
 cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s);
 cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,

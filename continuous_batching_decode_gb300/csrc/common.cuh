@@ -34,6 +34,14 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch: every kernel of the step lets the next one
+// launch as soon as all of its CTAs have started, and waits for the
+// previous kernel to complete (and its writes to be visible) before it
+// touches anything that kernel wrote.  Without the launch attribute both
+// are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void set_err(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
@@ -99,5 +107,91 @@ __device__ __forceinline__ void epi_single(const EpiArgs& ep, int f, int row, fl
 }
 
 __device__ __forceinline__ bool epi_is_pair(int kind) { return kind == kEpiQKV || kind == kEpiSwiGLU; }
+
+// Epilogue for NB consecutive rows row0..row0+NB-1 of output feature m held
+// by this lane (all 32 lanes of the warp call it; lanes hold consecutive
+// features).  Same arithmetic as epi_pair / epi_single, but every global
+// read a group of rows needs (residual x, row records, block table, RoPE
+// table) is issued before any is used, so a group costs one memory round
+// trip instead of one per row.
+template <int NB>
+__device__ __forceinline__ void epi_rows(const EpiArgs& ep, int m, int lane, int row0, int n, const float (&v)[NB]) {
+  float pv[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) pv[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
+  if (ep.kind == kEpiLogits) {
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) ep.out_f32[(size_t)(row0 + j) * ep.ld + m] = v[j];
+    return;
+  }
+  if (ep.kind == kEpiResid) {
+    float x[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) x[j] = ep.out_f32[(size_t)(row0 + j) * ep.ld + m];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) ep.out_f32[(size_t)(row0 + j) * ep.ld + m] = x[j] + v[j];
+    return;
+  }
+  if (lane & 1) return;                       // pair kinds: even lane owns (m, m+1)
+  if (ep.kind == kEpiSwiGLU) {
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) epi_pair(ep, m, row0 + j, v[j], pv[j]);
+    return;
+  }
+  // QKV: row records, then RoPE factors and block ids, then compute + store
+  const int hd = ep.hd, half = hd >> 1, nq = ep.hq * hd, nk = ep.hkv * hd;
+  RowDev rw[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j)
+    if (row0 + j < n) rw[j] = ep.rows[row0 + j];
+  if (m < nq) {
+    const int head = m / hd, i = (m % hd) >> 1;
+    float2 cs[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) cs[j] = reinterpret_cast<const float2*>(ep.rope_cs)[(size_t)rw[j].pos * half + i];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) {
+        float* qrow = ep.out_f32 + (size_t)(row0 + j) * nq + head * hd;
+        qrow[i] = v[j] * cs[j].x - pv[j] * cs[j].y;
+        qrow[i + half] = pv[j] * cs[j].x + v[j] * cs[j].y;
+      }
+    return;
+  }
+  int blk[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j)
+    if (row0 + j < n) blk[j] = ep.tables[(size_t)rw[j].slot * ep.max_blocks_per_seq + (rw[j].pos >> 5)];
+  if (m < nq + nk) {
+    const int head = (m - nq) / hd, i = ((m - nq) % hd) >> 1;
+    float2 cs[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) cs[j] = reinterpret_cast<const float2*>(ep.rope_cs)[(size_t)rw[j].pos * half + i];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      if (row0 + j < n) {
+        if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
+        const size_t o = pool_off(ep.layer, 0, ep.n_blocks, blk[j], ep.hkv, head, hd, rw[j].pos & 31, i);
+        ep.pool[o] = f32_to_bf16(v[j] * cs[j].x - pv[j] * cs[j].y);
+        ep.pool[o + half] = f32_to_bf16(pv[j] * cs[j].x + v[j] * cs[j].y);
+      }
+    return;
+  }
+  const int fv = m - nq - nk, head = fv / hd, jd = fv % hd;
+#pragma unroll
+  for (int j = 0; j < NB; ++j)
+    if (row0 + j < n) {
+      if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
+      const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk[j], ep.hkv, head, hd, rw[j].pos & 31, jd);
+      ep.pool[o] = f32_to_bf16(v[j]);
+      ep.pool[o + 1] = f32_to_bf16(pv[j]);
+    }
+}
 
 }  // namespace cbd

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(
   __shared__ __align__(16) float qs[G][HD];
   __shared__ float wm[NW][G], wl[NW][G];
   __shared__ __align__(16) float wo[NW][G][HD];
+  pdl_trigger();
+  pdl_wait();
   const int wi = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const AttnWork wk = work[wi];
@@ -195,6 +197,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __grid_constant__ C
   extern __shared__ uint8_t sm_raw[];
   __shared__ __align__(8) uint64_t bar[kAttnWarps];
   __shared__ int abort_flag;
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid4 = lane & 3;
   const uint32_t raw = tc::smem_u32(sm_raw);
@@ -374,6 +378,8 @@ template <int HD>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                     const int32_t* __restrict__ row_work, int hq,
                                     uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
   const int w0 = row_work[r], w1 = row_work[r + 1];
   float M = -INFINITY;
@@ -404,17 +410,20 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
       if (ce != cudaSuccess) return ce;
       attr = true;
     }
-    attn_mma_kernel<HD, G><<<dim3(b->n_work, dm.hkv), 128, smem, s>>>(
-        p->tmap, e->q, b->rows, b->tables, b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o,
-        e->attn_ml, e->err);
+    cudaError_t ce = launch_pdl(attn_mma_kernel<HD, G>, dim3(b->n_work, dm.hkv), dim3(128), smem, s, p->tmap,
+                                (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
+                                (const AttnWork*)b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq,
+                                e->attn_o, e->attn_ml, e->err);
+    if (ce != cudaSuccess) return ce;
   } else {
-    attn_partial_kernel<HD, G><<<dim3(b->n_work, dm.hkv), 128, 0, s>>>(
-        e->q, p->base, b->rows, b->tables, b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq,
-        e->attn_o, e->attn_ml, e->err);
+    cudaError_t ce = launch_pdl(attn_partial_kernel<HD, G>, dim3(b->n_work, dm.hkv), dim3(128), 0, s,
+                                (const float*)e->q, (const uint16_t*)p->base, (const RowDev*)b->rows,
+                                (const int32_t*)b->tables, (const AttnWork*)b->work, layer, p->n_blocks, dm.hkv,
+                                dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
+    if (ce != cudaSuccess) return ce;
   }
-  attn_combine_kernel<HD><<<dim3(b->n_rows, dm.hq), HD, 0, s>>>(e->attn_o, e->attn_ml, b->row_work, dm.hq,
-                                                                 e->act_hi, e->act_lo);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel<HD>, dim3(b->n_rows, dm.hq), dim3(HD), 0, s, (const float*)e->attn_o,
+                    (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq, e->act_hi, e->act_lo);
 }
 
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,

@@ -44,6 +44,8 @@ constexpr int kTcBK = 64;           // k per stage: one 128-byte swizzle row of 
 constexpr int kTcThreads = 192;
 constexpr int kTcMaxStages = 16;
 constexpr int kTcSmemBudget = 200 * 1024;
+constexpr int kTcMaxSegs = 256;     // partial slots a reduction reads from shared memory
+constexpr int kTcSegBatch = 8;      // segments whose loads are in flight together
 
 struct TcArgs {
   int M, K, n;                       // weight rows, reduction length, activation rows
@@ -81,6 +83,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int last_flag;
+  __shared__ int seg_slot[kTcMaxSegs];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = tc::smem_u32(smem_raw);
@@ -106,45 +109,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::prefetch_tmap(&tmH);
     tc::prefetch_tmap(&tmL);
   }
+  pdl_trigger();
   if (warp == 1) tc::tmem_alloc(&tmem_base, kTmemCols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   volatile int* abort_p = &abort_flag;
+  if (warp != 0) pdl_wait();          // the producer waits after prefetching weights
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      long long it = begin;
-      uint32_t q = 0;                       // ring position
-      bool ok = true;
-      while (it < end && ok) {
-        const int u = (int)(it / a.KB);
-        const int kb0 = (int)(it - (long long)u * a.KB);
-        const int kb1 = tc_seg_end(a.KB, kb0, end - it);
-        const int t = u % a.T, nt = u / a.T;
-        for (int kb = kb0; kb < kb1; ++kb, ++q) {
-          const int s = q % a.stages;
-          const uint32_t ph = (q / a.stages) & 1;
-          if (!tc::mbar_wait(&empty_bar[s], ph ^ 1, a.err, abort_p)) { ok = false; break; }
-          uint8_t* st = ring + (size_t)s * kStageBytes;
-          tc::mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-          tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb) * kTcBM, &full_bar[s]);
+      // iteration it = (unit u, k-block kb), u = nt * T + t; ring slot q = it - begin
+      const long long n_it = end - begin;
+      auto issue_w = [&](long long q) {
+        const long long it = begin + q;
+        const int u = (int)(it / a.KB), kb = (int)(it - (long long)u * a.KB);
+        const int s = (int)(q % a.stages);
+        uint8_t* st = ring + (size_t)s * kStageBytes;
+        tc::mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+        tc::tma_load_2d(st, &tmW, 0, ((u % a.T) * a.KB + kb) * kTcBM, &full_bar[s]);
+      };
+      auto issue_a = [&](long long q) {
+        const long long it = begin + q;
+        const int u = (int)(it / a.KB), kb = (int)(it - (long long)u * a.KB);
+        const int nt = u / a.T;
+        const int s = (int)(q % a.stages);
+        uint8_t* st = ring + (size_t)s * kStageBytes;
 #pragma unroll
-          for (int j = 0; j < NT / 16; ++j) {
-            tc::tma_load_2d(st + kWBytes + j * 16 * 128, &tmH, kb * kTcBK, nt * NT + j * 16, &full_bar[s]);
-            tc::tma_load_2d(st + kWBytes + kABytes + j * 16 * 128, &tmL, kb * kTcBK, nt * NT + j * 16, &full_bar[s]);
-          }
+        for (int j = 0; j < NT / 16; ++j) {
+          tc::tma_load_2d(st + kWBytes + j * 16 * 128, &tmH, kb * kTcBK, nt * NT + j * 16, &full_bar[s]);
+          tc::tma_load_2d(st + kWBytes + kABytes + j * 16 * 128, &tmL, kb * kTcBK, nt * NT + j * 16, &full_bar[s]);
         }
-        it += kb1 - kb0;
+      };
+      // weights do not depend on the previous kernel: start streaming them
+      // before waiting for it, then add the activations
+      const long long npre = n_it < a.stages ? n_it : a.stages;
+      for (long long q = 0; q < npre; ++q) issue_w(q);
+      pdl_wait();
+      for (long long q = 0; q < npre; ++q) issue_a(q);
+      long long q = npre;
+      bool ok = true;
+      for (; q < n_it; ++q) {
+        const int s = (int)(q % a.stages);
+        const uint32_t ph = (uint32_t)((q / a.stages) & 1);
+        if (!tc::mbar_wait(&empty_bar[s], ph ^ 1, a.err, abort_p)) { ok = false; break; }
+        issue_w(q);
+        issue_a(q);
       }
       // wind-down: every load issued must land before the CTA exits
-      if (!ok && q > 0) {
-        const uint32_t first = q > (uint32_t)a.stages ? q - a.stages : 0;
-        for (uint32_t r = first; r < q; ++r) {
+      if (!ok) {
+        const long long first = q > a.stages ? q - a.stages : 0;
+        for (long long r = first; r < q; ++r) {
           int dummy_abort = 0;
-          tc::mbar_wait(&full_bar[r % a.stages], (r / a.stages) & 1, nullptr, &dummy_abort);
+          tc::mbar_wait(&full_bar[r % a.stages], (uint32_t)((r / a.stages) & 1), nullptr, &dummy_abort);
         }
       }
     }
@@ -222,18 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float v[16];
         tc::tmem_ld16(taddr + c0, v);
         if (whole) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int row = nt * NT + c0 + j;
-            const float pv = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            if (row < a.n) {
-              if (epi_is_pair(ep.kind)) {
-                if (!(lane & 1)) epi_pair(ep, m, row, v[j], pv);
-              } else {
-                epi_single(ep, m, row, v[j]);
-              }
-            }
-          }
+          epi_rows<16>(ep, m, lane, nt * NT + c0, a.n, v);
         } else {
           float4* dst = reinterpret_cast<float4*>(mypart + (size_t)m_loc * NT + c0);
 #pragma unroll
@@ -254,39 +262,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (last_flag) {
           __threadfence();
-          // sum the partial tiles in k order (fixed), 16 columns at a time,
-          // each thread reading its own contiguous columns
+          // the tile's partial slots in k order, computed once in parallel
+          const int nseg = c_last - c_first + 1;
+          for (int i = threadIdx.x - 64; i < nseg && i < kTcMaxSegs; i += 128) {
+            const int c = c_first + i;
+            seg_slot[i] = 2 * c + (tc_begin(c, total, G) >= first_it ? 0 : 1);
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          // sum in k order (fixed), 8 columns at a time, with the loads of up
+          // to kTcSegBatch segments in flight together
 #pragma unroll 1
-          for (int c0 = 0; c0 < NT; c0 += 16) {
-            float acc[16];
+          for (int c0 = 0; c0 < NT; c0 += 8) {
+            float acc[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll 1
-            for (int c = c_first; c <= c_last; ++c) {
-              const long long bc = tc_begin(c, total, G);
-              const int slot = 2 * c + (bc >= first_it ? 0 : 1);
-              const float4* src = reinterpret_cast<const float4*>(a.part + (size_t)slot * NT * kTcBM +
-                                                                   (size_t)m_loc * NT + c0);
-              float4 t4[4];
+            for (int sb = 0; sb < nseg; sb += kTcSegBatch) {
+              float4 t4[kTcSegBatch][2];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) t4[j] = __ldcg(src + j);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                acc[4 * j] += t4[j].x; acc[4 * j + 1] += t4[j].y; acc[4 * j + 2] += t4[j].z; acc[4 * j + 3] += t4[j].w;
+              for (int i = 0; i < kTcSegBatch; ++i) {
+                if (sb + i < nseg) {
+                  const int c = c_first + sb + i;
+                  const int slot = sb + i < kTcMaxSegs ? seg_slot[sb + i]
+                                                        : 2 * c + (tc_begin(c, total, G) >= first_it ? 0 : 1);
+                  const float4* src = reinterpret_cast<const float4*>(a.part + (size_t)slot * NT * kTcBM +
+                                                                       (size_t)m_loc * NT + c0);
+                  t4[i][0] = __ldcg(src);
+                  t4[i][1] = __ldcg(src + 1);
+                }
               }
-            }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int row = nt * NT + c0 + j;
-              const float pv = __shfl_xor_sync(0xffffffffu, acc[j], 1);
-              if (row < a.n) {
-                if (epi_is_pair(ep.kind)) {
-                  if (!(lane & 1)) epi_pair(ep, m, row, acc[j], pv);
-                } else {
-                  epi_single(ep, m, row, acc[j]);
+              for (int i = 0; i < kTcSegBatch; ++i) {
+                if (sb + i < nseg) {
+                  acc[0] += t4[i][0].x; acc[1] += t4[i][0].y; acc[2] += t4[i][0].z; acc[3] += t4[i][0].w;
+                  acc[4] += t4[i][1].x; acc[5] += t4[i][1].y; acc[6] += t4[i][1].z; acc[7] += t4[i][1].w;
                 }
               }
             }
+            epi_rows<8>(ep, m, lane, nt * NT + c0, a.n, acc);
           }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -353,8 +366,7 @@ static cudaError_t launch_tc_t(const TcGemm& g, int n, const EpiArgs& ep, const 
   a.stages = stages;
   a.part = w.part; a.counters = w.counters; a.err = ep.err;
   if ((long long)a.T * a.NTILES > w.max_units) return cudaErrorInvalidValue;
-  gemm_tc_kernel<NT><<<a.G, kTcThreads, smem, s>>>(*g.w, *g.hi, *g.lo, a, ep);
-  return cudaGetLastError();
+  return launch_pdl(gemm_tc_kernel<NT>, dim3(a.G), dim3(kTcThreads), smem, s, *g.w, *g.hi, *g.lo, a, ep);
 }
 
 cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const TcWork& w, int sm_count,

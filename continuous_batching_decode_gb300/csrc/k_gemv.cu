@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
                                                    const uint16_t* __restrict__ a_lo, int lda, int n,
                                                    EpiArgs ep) {
   __shared__ __align__(16) float act[NB][kKTile];
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int f0 = (blockIdx.x * kGemvWarps + warp) * kGemvFeat;
   const int r0 = blockIdx.y * NB;
@@ -103,17 +105,18 @@ cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, c
                         int lda, int n, const EpiArgs& ep, cudaStream_t s) {
   const int feat_per_cta = kGemvWarps * kGemvFeat;
   dim3 block(32 * kGemvWarps);
+  cudaError_t ce = cudaSuccess;
   if (n <= 1) {
-    gemv_kernel<1><<<dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s>>>(W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<1>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
   } else if (n <= 2) {
-    gemv_kernel<2><<<dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s>>>(W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<2>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
   } else if (n <= 4) {
-    gemv_kernel<4><<<dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s>>>(W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<4>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
   } else {
     dim3 grid((M + feat_per_cta - 1) / feat_per_cta, (n + 7) / 8);
-    gemv_kernel<8><<<grid, block, 0, s>>>(W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<8>, grid, block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
   }
-  return cudaGetLastError();
+  return ce;
 }
 
 // Path choice: the CUDA-core GEMV for a handful of rows, the tcgen05 GEMM

@@ -9,6 +9,8 @@ namespace cbd {
 // embedding row of the row's token).
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
                              float* __restrict__ x) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const uint16_t* src = E + (size_t)rows[r].token * d;
   float* dst = x + (size_t)r * d;
@@ -16,8 +18,8 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
 }
 
 cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s) {
-  embed_kernel<<<b->n_rows, 256, 0, s>>>(e->embed, b->rows, e->dm.d, e->x);
-  return cudaGetLastError();
+  return launch_pdl(embed_kernel, dim3(b->n_rows), dim3(256), 0, s, (const uint16_t*)e->embed,
+                    (const RowDev*)b->rows, e->dm.d, e->x);
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.
@@ -29,6 +31,8 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
                                const int32_t* __restrict__ gather, int d, float eps,
                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int src = gather ? gather[r] : r;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
@@ -68,8 +72,7 @@ cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, 
                            const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   const int threads = std::min(1024, e->dm.d / 4);
-  rmsnorm_kernel<<<n_rows, threads, 0, s>>>(x, g, gather, e->dm.d, e->dm.eps, hi, lo);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(n_rows), dim3(threads), 0, s, x, g, gather, e->dm.d, e->dm.eps, hi, lo);
 }
 
 }  // namespace cbd

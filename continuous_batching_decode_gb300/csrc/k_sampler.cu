@@ -12,8 +12,9 @@
 //   the token is the first id, ascending, whose cumulative kept mass
 //   exceeds u times the kept total.  Then cnt *= decay; cnt[tok] += 1.
 //
-// One CTA of 1024 threads per sampled row; thread t owns a contiguous id
-// range, so id-ordered prefix sums are block scans.  Probability masses are
+// One CTA of 1024 threads per sampled row; warp w owns a contiguous id
+// range walked in coalesced 32-id rounds, so id-ordered prefix sums are a
+// prefix over warps plus per-round warp scans.  Probability masses are
 // fixed-point integers (exp(z - zmax) * 2^40), so every sum, threshold and
 // scan is exact and independent of thread timing; the k-th largest key and
 // the top-p cutoff are found by 8-bit radix selection over order-preserving
@@ -65,32 +66,41 @@ struct SampShared {
   int32_t cut_id;
 };
 
-// Exclusive scan of one u64 per thread over the block; returns the prefix
-// and writes the block total to *total.
-__device__ unsigned long long block_exscan(unsigned long long v, SampShared& sh, unsigned long long* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  unsigned long long inc = v;
+// Warp w owns the contiguous ids [w*PW, (w+1)*PW) and walks them in
+// rounds of 32 consecutive ids (lane = offset), so every load is coalesced
+// and id-ordered prefix sums are a warp scan per round plus a carry.
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
   }
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Exclusive prefix over the 32 warps of one value per warp (lane 0's value
+// counts); returns this warp's prefix and the block total.
+__device__ unsigned long long warp_prefix(unsigned long long mine, SampShared& sh, unsigned long long* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   __syncthreads();
-  if (lane == 31) sh.wsum[w] = inc;
+  if (lane == 0) sh.wsum[w] = mine;
   __syncthreads();
   if (w == 0) {
-    unsigned long long s = sh.wsum[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long t = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += t;
-    }
-    sh.wsum[lane] = s;     // inclusive warp-prefix totals
+    const unsigned long long x = sh.wsum[lane];
+    const unsigned long long inc = warp_incl_scan_u64(x, lane);
+    sh.wsum[lane] = inc - x;
+    if (lane == 31) sh.sel_above = inc;
   }
   __syncthreads();
-  const unsigned long long before = (w ? sh.wsum[w - 1] : 0ull) + inc - v;
-  *total = sh.wsum[31];
-  return before;
+  *total = sh.sel_above;
+  const unsigned long long r = sh.wsum[w];
+  __syncthreads();
+  return r;
 }
 
 __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ logits, int V,
@@ -103,19 +113,23 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   extern __shared__ __align__(16) uint8_t samp_dyn[];
   unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn);             // [32][256]
   uint32_t* whc = reinterpret_cast<uint32_t*>(samp_dyn + (kST / 32) * kHistBins * 8);  // [32][256]
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const SampDev sp = samp[row];
   const float* lg = logits + (size_t)row * V;
   float* cnt = counters + (size_t)slots[row] * V;
   float* z = scratch + (size_t)row * V;
-  const int per = (V + kST - 1) / kST;
-  const int i0 = min(V, tid * per), i1 = min(V, i0 + per);
+  const int PW = ((V + 32 * 32 - 1) / (32 * 32)) * 32;   // ids per warp, a multiple of 32
+  const int v0 = w * PW;
+  const int v1 = min(V, v0 + PW);
   const bool greedy = sp.temperature == 0.0f || sp.top_k == 1;
+  const unsigned lt_mask = (1u << lane) - 1u;
 
   // 1. penalty (and temperature); best key, lowest id on ties
   uint32_t bk = 0;
   int32_t bi = 0x7fffffff;
-  for (int v = i0; v < i1; ++v) {
+  for (int v = v0 + lane; v < v1; v += 32) {
     const float c = cnt[v];
     const float l1 = __fsub_rn(lg[v], c > 0.0f ? sp.presence : 0.0f);
     const float l2 = __fsub_rn(l1, __fmul_rn(sp.frequency, c));
@@ -149,16 +163,13 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     const float zmax = z[sh.tok];
     // 2. top-k: radix-select the k-th largest key; keep key > tk, and the
     //    lowest-id `need` elements with key == tk.
-    uint32_t tk = 0;
-    long long need_eq = 0x7fffffffffffffffLL;
-    const bool do_topk = sp.top_k > 0 && sp.top_k < V;
-    if (do_topk) {
+    if (sp.top_k > 0 && sp.top_k < V) {
       uint32_t prefix = 0, mask = 0;
       unsigned long long rem = (unsigned long long)sp.top_k;
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < (kST / 32) * kHistBins; i += kST) whc[i] = 0;
         __syncthreads();
-        for (int v = i0; v < i1; ++v) {
+        for (int v = v0 + lane; v < v1; v += 32) {
           const uint32_t k = ord_key(z[v]);
           if ((k & mask) == prefix) atomicAdd(&whc[w * kHistBins + ((k >> shift) & 255u)], 1u);
         }
@@ -184,22 +195,24 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         prefix = sh.sel_prefix;
         mask = sh.sel_mask;
         rem = sh.sel_rem;
-        __syncthreads();
       }
-      tk = prefix;
-      need_eq = (long long)rem;
-      // rank of equal keys by id: keep the first need_eq of them
-      unsigned long long mine = 0;
-      for (int v = i0; v < i1; ++v) mine += ord_key(z[v]) == tk;
+      const uint32_t tk = prefix;
+      const unsigned long long need_eq = rem;
+      // rank among equal keys in id order
+      unsigned long long eq = 0;
+      for (int v = v0 + lane; v < v1; v += 32) eq += ord_key(z[v]) == tk;
       unsigned long long tot;
-      unsigned long long rank = block_exscan(mine, sh, &tot);
-      for (int v = i0; v < i1; ++v) {
-        const uint32_t k = ord_key(z[v]);
-        if (k < tk) z[v] = -INFINITY;
-        else if (k == tk) {
-          if ((long long)rank >= need_eq) z[v] = -INFINITY;
-          ++rank;
+      unsigned long long base = warp_prefix(warp_sum_u64(eq), sh, &tot);
+      for (int v0r = v0; v0r < v1; v0r += 32) {
+        const int v = v0r + lane;
+        const bool valid = v < v1;
+        const uint32_t k = valid ? ord_key(z[v]) : 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, valid && k == tk);
+        if (valid) {
+          if (k < tk) z[v] = -INFINITY;
+          else if (k == tk && base + __popc(bal & lt_mask) >= need_eq) z[v] = -INFINITY;
         }
+        base += __popc(bal);
       }
       __syncthreads();
     }
@@ -214,9 +227,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     int32_t cut_id = 0x7fffffff;
     if (sp.top_p < 1.0f) {
       unsigned long long mine = 0;
-      for (int v = i0; v < i1; ++v) mine += mass(z[v]);
+      for (int v = v0 + lane; v < v1; v += 32) mine += mass(z[v]);
       unsigned long long S;
-      (void)block_exscan(mine, sh, &S);
+      (void)warp_prefix(warp_sum_u64(mine), sh, &S);
       const double target = (double)sp.top_p * (double)S;
       if ((double)S >= target) {
         use_cut = true;
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         for (int shift = 24; shift >= 0; shift -= 8) {
           for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
           __syncthreads();
-          for (int v = i0; v < i1; ++v) {
+          for (int v = v0 + lane; v < v1; v += 32) {
             const float zv = z[v];
             if (zv == -INFINITY) continue;
             const uint32_t k = ord_key(zv);
@@ -256,36 +269,44 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
               above += sh.hm[d];
             }
             if (d < 0) d = last;        // rounding: take the lowest non-empty digit
-            sh.sel_above = above;
+            sh.sel_rem = above;
             sh.sel_prefix = prefix | ((uint32_t)d << shift);
             sh.sel_mask = mask | (255u << shift);
           }
           __syncthreads();
           prefix = sh.sel_prefix;
           mask = sh.sel_mask;
-          above = sh.sel_above;
-          __syncthreads();
+          above = sh.sel_rem;
         }
         tp = prefix;
         // among key == tp, ascending id: first id where above + cum >= target
         unsigned long long eqm = 0;
-        for (int v = i0; v < i1; ++v)
+        for (int v = v0 + lane; v < v1; v += 32)
           if (z[v] != -INFINITY && ord_key(z[v]) == tp) eqm += mass(z[v]);
         unsigned long long tot;
-        unsigned long long before = block_exscan(eqm, sh, &tot);
+        const unsigned long long wbase = warp_prefix(warp_sum_u64(eqm), sh, &tot);
+        const unsigned long long wtot = warp_sum_u64(eqm);
         if (tid == 0) sh.cut_id = 0x7fffffff;
         __syncthreads();
-        unsigned long long run = above + before;
-        for (int v = i0; v < i1; ++v) {
-          if (z[v] == -INFINITY || ord_key(z[v]) != tp) continue;
-          run += mass(z[v]);
-          if ((double)run >= target) { atomicMin(&sh.cut_id, v); break; }
+        if ((double)(above + wbase + wtot) >= target) {   // the crossing may lie in this warp
+          unsigned long long run = above + wbase;
+          for (int v0r = v0; v0r < v1; v0r += 32) {
+            const int v = v0r + lane;
+            unsigned long long mv = 0;
+            if (v < v1 && z[v] != -INFINITY && ord_key(z[v]) == tp) mv = mass(z[v]);
+            const unsigned long long inc = warp_incl_scan_u64(mv, lane);
+            const bool hit = mv > 0 || (v < v1 && z[v] != -INFINITY && ord_key(z[v]) == tp);
+            const unsigned bal = __ballot_sync(0xffffffffu, hit && (double)(run + inc) >= target);
+            if (bal) {
+              if (lane == __ffs(bal) - 1) atomicMin(&sh.cut_id, v);
+              break;
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
+          }
         }
         __syncthreads();
         cut_id = sh.cut_id;
-        if (cut_id == 0x7fffffff) {      // rounding: keep every element of the tie group
-          cut_id = V;
-        }
+        if (cut_id == 0x7fffffff) cut_id = V;   // rounding: keep every element of the tie group
       }
     }
     auto kept_mass = [&](int v) -> unsigned long long {
@@ -304,17 +325,25 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       u = (float)(x >> 8) * (1.0f / 16777216.0f);
     }
     unsigned long long mine = 0;
-    for (int v = i0; v < i1; ++v) mine += kept_mass(v);
+    for (int v = v0 + lane; v < v1; v += 32) mine += kept_mass(v);
+    const unsigned long long wtot = warp_sum_u64(mine);
     unsigned long long Sk;
-    const unsigned long long before = block_exscan(mine, sh, &Sk);
+    const unsigned long long wbase = warp_prefix(wtot, sh, &Sk);
     const unsigned long long T = (unsigned long long)floor((double)u * (double)Sk);
     if (tid == 0) sh.tok = 0x7fffffff;
     __syncthreads();
-    if (before <= T && before + mine > T) {
-      unsigned long long run = before;
-      for (int v = i0; v < i1; ++v) {
-        run += kept_mass(v);
-        if (run > T) { sh.tok = v; break; }
+    if (wbase <= T && wbase + wtot > T) {
+      unsigned long long run = wbase;
+      for (int v0r = v0; v0r < v1; v0r += 32) {
+        const int v = v0r + lane;
+        const unsigned long long mv = v < v1 ? kept_mass(v) : 0ull;
+        const unsigned long long inc = warp_incl_scan_u64(mv, lane);
+        const unsigned bal = __ballot_sync(0xffffffffu, run + inc > T && mv > 0);
+        if (bal) {
+          if (lane == __ffs(bal) - 1) sh.tok = v;
+          break;
+        }
+        run += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
     __syncthreads();
@@ -325,7 +354,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   }
   // 6. counters: decay everything, then count the drawn token
   const int tok = sh.tok;
-  for (int v = i0; v < i1; ++v) cnt[v] = __fmul_rn(cnt[v], sp.decay);
+  for (int v = v0 + lane; v < v1; v += 32) cnt[v] = __fmul_rn(cnt[v], sp.decay);
   __syncthreads();
   if (tid == 0) {
     cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
@@ -344,8 +373,8 @@ cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, c
     if (ce != cudaSuccess) return ce;
     attr = true;
   }
-  sampler_kernel<<<m, kST, kSampDynSmem, s>>>(logits, V, counters, slots, samp, scratch, out_tokens, err);
-  return cudaGetLastError();
+  return launch_pdl(sampler_kernel, dim3(m), dim3(kST), kSampDynSmem, s, logits, V, counters, slots, samp, scratch,
+                    out_tokens, err);
 }
 
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
