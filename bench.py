@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
-    ap.add_argument("--attn-path", type=int, default=0, help="0 mma.sync tensor cores, 1 CUDA cores")
+    ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     return ap.parse_args()
 
 

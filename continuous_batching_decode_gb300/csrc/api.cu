@@ -421,7 +421,7 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
 extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
-  if (path < 0 || path > 1) return fail(CBD_EINVAL, "attention path must be 0 or 1");
+  if (path < 0 || path > 2) return fail(CBD_EINVAL, "attention path must be 0, 1 or 2");
   e->attn_path = path;
   return CBD_OK;
 }

@@ -14,7 +14,9 @@
 // H_kv query heads that share the KV head, keeping an online softmax
 // (running max, running sum, unnormalised output).
 //
-// Two kernels compute the chunk: attn_mma_kernel (default) stages the four
+// Three kernels compute the chunks.  attn_stream_kernel (default) is the
+// persistent, per-warp-pipelined form described below.  attn_mma_kernel
+// (one CTA per chunk) stages the four
 // 32-position K and V tiles of the chunk in shared memory with TMA (128-byte
 // swizzle) and runs q.K and P.V on the tensor cores with mma.sync, in a
 // swapped form -- positions (or head dims) on the MMA's M side, the <= 8
@@ -25,6 +27,8 @@
 // hi + lo bf16 halves for the O projection.  The chunking depends only on
 // the row's position, and the merge order is fixed, so a row's result does
 // not depend on the other rows of the step or on block placement.
+#include <algorithm>
+
 #include "tc.cuh"
 
 namespace cbd {
@@ -373,6 +377,239 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __grid_constant__ C
   }
 }
 
+// ---------------------------------------------------------------- streaming
+// Persistent form of the tensor-core kernel: every warp owns the tasks
+// gw, gw + W, gw + 2W, ... (task = one 128-position chunk of one row for one
+// KV head; W = warps in the grid) and streams their 32-position K/V tiles
+// through a private ring of shared-memory stages filled by TMA, running
+// ahead across task boundaries.  Within a task the warp keeps an online
+// softmax over its blocks; at the task's end it writes the chunk's partial
+// (max, sum, unnormalised output).  No warp waits for another.
+template <int HD>
+__host__ __device__ constexpr int attn_stream_stages() { return HD == 128 ? 3 : 6; }
+template <int HD>
+__host__ __device__ constexpr int attn_stream_smem() {
+  return kAttnWarps * attn_stream_stages<HD>() * 2 * (32 * HD * 2) + kAttnWarps * 8 * 32 * 4 + 1024;
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(128, 1) attn_stream_kernel(
+    const __grid_constant__ CUtensorMap tmKV, const float* __restrict__ q, const RowDev* __restrict__ rows,
+    const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, int n_tasks, int layer, int n_blocks,
+    int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
+  static_assert(G >= 1 && G <= 8, "a KV group must fit the MMA's N = 8");
+  constexpr int TILE = 32 * HD * 2;
+  constexpr int KS = HD / 16;
+  constexpr int ST = attn_stream_stages<HD>();
+  extern __shared__ uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t bar[kAttnWarps][ST];
+  __shared__ int abort_flag;
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tid4 = lane & 3;
+  const uint32_t raw = tc::smem_u32(sm_raw);
+  uint8_t* base = sm_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* ring = base + warp * ST * 2 * TILE;           // stage s: K at s*2*TILE, V after it
+  float* Pw = reinterpret_cast<float*>(base + kAttnWarps * ST * 2 * TILE) + warp * 8 * 32;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kAttnWarps; ++w)
+      for (int s = 0; s < ST; ++s) tc::mbar_init(&bar[w][s], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  const int hq = hkv * G;
+  const int gw = blockIdx.x * kAttnWarps + warp, nwarps = gridDim.x * kAttnWarps;
+  struct Task {
+    int wi, kvh, row, start, end, slot, nb;
+  };
+  auto task_of = [&](int t) {
+    Task k;
+    k.wi = t / hkv;
+    k.kvh = t - k.wi * hkv;
+    const AttnWork wk = work[k.wi];
+    const RowDev rw = rows[wk.row];
+    k.row = wk.row;
+    k.start = wk.start;
+    k.end = min(wk.start + kAttnChunk, rw.pos + 1);
+    k.slot = rw.slot;
+    k.nb = (k.end - k.start + 31) >> 5;
+    return k;
+  };
+  // producer cursor (lane 0 issues; all lanes track it identically)
+  int p_task = gw, p_blk = 0;
+  Task pt = p_task < n_tasks ? task_of(p_task) : Task{};
+  uint32_t p_q = 0;
+  auto issue_next = [&]() {
+    if (p_task >= n_tasks) return;
+    const int s = p_q % ST;
+    if (lane == 0) {
+      int blk = tables[(size_t)pt.slot * mbps + (pt.start >> 5) + p_blk];
+      if (blk < 0 || blk >= n_blocks) { set_err(err, kDevBadBlock); blk = 0; }
+      uint8_t* kt = ring + s * 2 * TILE;
+      tc::mbar_arrive_expect_tx(&bar[warp][s], 2 * TILE);
+      const size_t rk = ((((size_t)layer * 2 + 0) * n_blocks + blk) * hkv + pt.kvh) * 32;
+      const size_t rv = ((((size_t)layer * 2 + 1) * n_blocks + blk) * hkv + pt.kvh) * 32;
+#pragma unroll
+      for (int h = 0; h < HD / 64; ++h) {
+        tc::tma_load_2d(kt + h * 4096, &tmKV, h * 64, (int)rk, &bar[warp][s]);
+        tc::tma_load_2d(kt + TILE + h * 4096, &tmKV, h * 64, (int)rv, &bar[warp][s]);
+      }
+    }
+    ++p_q;
+    if (++p_blk == pt.nb) {
+      p_blk = 0;
+      p_task += nwarps;
+      if (p_task < n_tasks) pt = task_of(p_task);
+    }
+  };
+  for (int i = 0; i < ST; ++i) issue_next();
+
+  const float scale = 1.0f / sqrtf((float)HD);
+  const int mi = lane >> 3, ri = lane & 7;
+  uint32_t c_q = 0;
+  bool alive = true;
+  for (int t = gw; t < n_tasks && alive; t += nwarps) {
+    const Task tk = task_of(t);
+    // q of the group's heads (scaled) as hi / lo B fragments
+    uint32_t qh[KS][2], ql[KS][2];
+    const float* qrow = q + ((size_t)tk.row * hq + tk.kvh * G) * HD;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int dd = ks * 16 + r * 8 + tid4 * 2;
+        float a = 0.f, b = 0.f;
+        if (gid < G) {
+          a = qrow[gid * HD + dd] * scale;
+          b = qrow[gid * HD + dd + 1] * scale;
+        }
+        split_pack(a, b, qh[ks][r], ql[ks][r]);
+      }
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[KS][4];
+#pragma unroll
+    for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[dt][c] = 0.f;
+    for (int b = 0; b < tk.nb; ++b, ++c_q) {
+      const int s = c_q % ST;
+      if (!tc::mbar_wait(&bar[warp][s], (c_q / ST) & 1, err, &abort_flag)) { alive = false; break; }
+      uint8_t* kt = ring + s * 2 * TILE;
+      uint8_t* vt = kt + TILE;
+      const int nvalid = min(32, tk.end - (tk.start + b * 32));
+      for (int i = lane; i < (32 - nvalid) * (HD / 8); i += 32) {
+        const int r = nvalid + i / (HD / 8), ch = i % (HD / 8);
+        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 4096 + swz(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      const uint32_t ks_base = tc::smem_u32(kt), vs_base = tc::smem_u32(vt);
+      float sc[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sc[mt][c] = 0.f;
+        const int r = mt * 16 + (mi & 1) * 8 + ri;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int dc = ks * 16 + (mi >> 1) * 8;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(ks_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
+          mma_bf16_16816(sc[mt], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+          mma_bf16_16816(sc[mt], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[4] = {sc[0][hh], sc[0][hh + 2], sc[1][hh], sc[1][hh + 2]};
+        const int pos[4] = {gid, gid + 8, 16 + gid, 24 + gid};
+        float bm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (pos[i] >= nvalid) v[i] = -INFINITY;
+          bm = fmaxf(bm, v[i]);
+        }
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+        const float mn = fmaxf(m[hh], bm);
+        float bs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float pv = pos[i] < nvalid ? expf(v[i] - mn) : 0.f;
+          bs += pv;
+          Pw[(tid4 * 2 + hh) * 32 + pos[i]] = pv;
+        }
+        bs += __shfl_xor_sync(0xffffffffu, bs, 4);
+        bs += __shfl_xor_sync(0xffffffffu, bs, 8);
+        bs += __shfl_xor_sync(0xffffffffu, bs, 16);
+        const float corr = m[hh] == -INFINITY ? 0.f : expf(m[hh] - mn);
+        l[hh] = l[hh] * corr + bs;
+        m[hh] = mn;
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) {
+          o[dt][hh] *= corr;
+          o[dt][hh + 2] *= corr;
+        }
+      }
+      __syncwarp();
+      uint32_t ph[2][2], pl[2][2];
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int j = k2 * 16 + r * 8 + tid4 * 2;
+          split_pack(Pw[gid * 32 + j], Pw[gid * 32 + j + 1], ph[k2][r], pl[k2][r]);
+        }
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt) {
+        const int dc = dt * 16 + (mi & 1) * 8;
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int r = k2 * 16 + (mi >> 1) * 8 + ri;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vs_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
+          mma_bf16_16816(o[dt], a0, a1, a2, a3, ph[k2][0], ph[k2][1]);
+          mma_bf16_16816(o[dt], a0, a1, a2, a3, pl[k2][0], pl[k2][1]);
+        }
+      }
+      __syncwarp();          // every lane is done with stage s (and Pw)
+      issue_next();          // refill it with the block ST ahead
+    }
+    if (!alive) break;
+    // the chunk's partial for the group's heads
+#pragma unroll
+    for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int head = tid4 * 2 + (c & 1);
+        if (head < G) {
+          const int dim = dt * 16 + gid + (c >= 2 ? 8 : 0);
+          part_o[(((size_t)tk.wi * hq + tk.kvh * G + head) * HD) + dim] = o[dt][c];
+        }
+      }
+    if (gid == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int head = tid4 * 2 + hh;
+        if (head < G) {
+          const size_t h = (size_t)tk.wi * hq + tk.kvh * G + head;
+          part_ml[h * 2] = m[hh];
+          part_ml[h * 2 + 1] = l[hh];
+        }
+      }
+    }
+  }
+  // wind-down after a failed wait: let issued loads land before exiting
+  if (!alive) {
+    for (uint32_t r = c_q; r < p_q; ++r) {
+      int no_abort = 0;
+      tc::mbar_wait(&bar[warp][r % ST], (r / ST) & 1, nullptr, &no_abort);
+    }
+  }
+}
+
 // Merge a row's chunks for one head (chunk order), normalise, split.
 template <int HD>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
@@ -403,6 +640,20 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
                                  cudaStream_t s) {
   const Dims& dm = e->dm;
   if (e->attn_path == 0) {
+    constexpr int smem = attn_stream_smem<HD>();
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t ce = cudaFuncSetAttribute(attn_stream_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (ce != cudaSuccess) return ce;
+      attr = true;
+    }
+    const int n_tasks = b->n_work * dm.hkv;
+    const int grid = std::min(e->sm_count, (n_tasks + kAttnWarps - 1) / kAttnWarps);
+    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(128), smem, s, p->tmap, (const float*)e->q,
+                                (const RowDev*)b->rows, (const int32_t*)b->tables, (const AttnWork*)b->work, n_tasks,
+                                layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
+    if (ce != cudaSuccess) return ce;
+  } else if (e->attn_path == 2) {
     constexpr int smem = attn_mma_smem<HD>();
     static bool attr = false;
     if (!attr) {

@@ -50,9 +50,12 @@ __device__ __forceinline__ uint32_t ord_key(float f) {
 
 // Radix histograms: every warp owns a private [256] count and mass
 // histogram in dynamic shared memory (no atomics contend across warps);
-// the block then sums them bin by bin in warp order.
+// the block then sums them bin by bin in warp order.  A mass (< 2^41) is
+// accumulated as two 32-bit halves, low 20 bits and the rest, so every
+// shared-memory atomic is a native 32-bit add: a warp's bin holds at most
+// 2048 elements, so neither half can overflow.
 constexpr int kHistBins = 256;
-constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * (sizeof(uint32_t) + sizeof(unsigned long long));
+constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * 3 * sizeof(uint32_t);
 
 struct SampShared {
   unsigned long long wsum[32];
@@ -111,8 +114,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       int32_t* __restrict__ out, int32_t* err) {
   __shared__ SampShared sh;
   extern __shared__ __align__(16) uint8_t samp_dyn[];
-  unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn);             // [32][256]
-  uint32_t* whc = reinterpret_cast<uint32_t*>(samp_dyn + (kST / 32) * kHistBins * 8);  // [32][256]
+  uint32_t* whm_lo = reinterpret_cast<uint32_t*>(samp_dyn);              // [32][256] mass bits 0..19
+  uint32_t* whm_hi = whm_lo + (kST / 32) * kHistBins;                    // [32][256] mass >> 20
+  uint32_t* whc = whm_hi + (kST / 32) * kHistBins;                       // [32][256] counts
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         uint32_t prefix = 0, mask = 0;
         unsigned long long above = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
+          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm_lo[i] = 0; whm_hi[i] = 0; }
           __syncthreads();
           for (int v = v0 + lane; v < v1; v += 32) {
             const float zv = z[v];
@@ -244,8 +248,10 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             const uint32_t k = ord_key(zv);
             if ((k & mask) == prefix) {
               const uint32_t dg = (k >> shift) & 255u;
+              const unsigned long long mv = mass(zv);
               atomicAdd(&whc[w * kHistBins + dg], 1u);
-              atomicAdd(&whm[w * kHistBins + dg], mass(zv));
+              atomicAdd(&whm_lo[w * kHistBins + dg], (uint32_t)(mv & 0xFFFFFull));
+              atomicAdd(&whm_hi[w * kHistBins + dg], (uint32_t)(mv >> 20));
             }
           }
           __syncthreads();
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             unsigned long long mm = 0;
             for (int ww = 0; ww < kST / 32; ++ww) {
               c += whc[ww * kHistBins + b];
-              mm += whm[ww * kHistBins + b];
+              mm += ((unsigned long long)whm_hi[ww * kHistBins + b] << 20) + whm_lo[ww * kHistBins + b];
             }
             sh.hc[b] = c;
             sh.hm[b] = mm;

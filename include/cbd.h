@@ -131,8 +131,10 @@ cbd_status cbd_engine_check(cbd_engine* e);
  * activations); they differ only in summation order.  Default: 0 and 4. */
 cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_max_rows);
 
-/* Choose the attention kernel: 0 = tensor cores (mma.sync on K/V tiles
- * staged by TMA; default), 1 = CUDA cores.  Same chunking and merge order. */
+/* Choose the attention kernel: 0 = persistent streaming kernel (each warp
+ * pipelines its chunks' K/V tiles through a TMA ring; mma.sync; default),
+ * 1 = CUDA cores, 2 = one CTA per chunk with mma.sync.  All use the same
+ * 128-position chunks and the same merge order. */
 cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path);
 
 /* Device pointer of the per-slot occurrence counters, [max_slots][V] fp32,

@@ -20,11 +20,12 @@ if torch.cuda.is_available():
     from tests import gpu_util as gu
 
 
-@pytest.fixture(scope="module", params=[(1, 1), (2, 0)], ids=["gemv+cuda_core_attn", "tcgen05+mma_attn"])
+@pytest.fixture(scope="module", params=[(1, 1), (2, 0), (2, 2)],
+                ids=["gemv+cuda_core_attn", "tcgen05+stream_attn", "tcgen05+chunk_attn"])
 def tiny(request):
     """The tiny decoder with every contraction forced onto one GEMM path
     (1 = CUDA-core GEMV, 2 = tcgen05) and one attention kernel (1 = CUDA
-    cores, 0 = mma.sync on TMA-staged tiles)."""
+    cores, 0 = persistent streaming mma.sync, 2 = one CTA per chunk)."""
     from continuous_batching_decode_gb300 import build
     build.build()
     m = gu.Model("tiny", max_rows=512, max_slots=8, mbps=16)
