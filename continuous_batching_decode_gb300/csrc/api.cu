@@ -46,7 +46,7 @@ enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, 
 
 // ---------------------------------------------------------------- repack
 // Weight layout for the kernels: row r of the (row-permuted) matrix, column
-// k, lives at [r / 128][k / 64][r % 128][k % 64] -- 16 KB tiles of 128 rows
+// k, lives at [r / 256][k / 64][r % 256][k % 64] -- 32 KB tiles of 256 rows
 // by 64 columns, each one contiguous.  perm (nullable) gives the source row
 // of each destination row.
 __global__ void permute_tile_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
@@ -57,7 +57,7 @@ __global__ void permute_tile_kernel(uint16_t* __restrict__ dst, const uint16_t* 
   const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)sr * K);
   for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
     const int k = c * 8;
-    uint4* d = reinterpret_cast<uint4*>(dst + ((((size_t)(r >> 7) * KB + (k >> 6)) << 7) + (r & 127)) * 64 + (k & 63));
+    uint4* d = reinterpret_cast<uint4*>(dst + ((((size_t)(r >> 8) * KB + (k >> 6)) << 8) + (r & 255)) * 64 + (k & 63));
     *d = s[c];
   }
 }
@@ -105,7 +105,9 @@ cbd_status check_config(const cbd_config* c) {
   if (g != 1 && g != 2 && g != 4 && g != 8) return fail(CBD_EUNSUPPORTED, "n_heads/n_kv_heads must be 1, 2, 4 or 8");
   if (c->d_model % 256 || c->ffn_dim % 256 || (c->n_heads * c->head_dim) % 256)
     return fail(CBD_EUNSUPPORTED, "d_model, ffn_dim and n_heads*head_dim must be multiples of 256");
-  if (c->vocab > kMaxVocab || c->vocab % 32) return fail(CBD_EUNSUPPORTED, "vocab must be a multiple of 32, <= 65536");
+  if (c->vocab > kMaxVocab || c->vocab % 256) return fail(CBD_EUNSUPPORTED, "vocab must be a multiple of 256, <= 65536");
+  if (((c->n_heads + 2 * c->n_kv_heads) * c->head_dim) % 256)
+    return fail(CBD_EUNSUPPORTED, "(n_heads + 2 n_kv_heads) * head_dim must be a multiple of 256");
   return CBD_OK;
 }
 
@@ -268,9 +270,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
-  const size_t max_t = std::max({V, 2 * F, qo, d}) / 128 + 1;
-  const long long max_units = (long long)max_t * (long long)std::max<size_t>(1, (R + 127) / 128);
-  const size_t o_part = W.take((size_t)2 * e->sm_count * 128 * 128 * 4), o_ctr = W.take((size_t)max_units * 4);
+
   e->work_bytes = W.off;
   cudaError_t e3 = cudaMalloc(&e->work, e->work_bytes);
   if (e3 != cudaSuccess) { cleanup(); return cuda_fail(e3, "cudaMalloc(workspaces)"); }
@@ -287,9 +287,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
   e->counters = reinterpret_cast<float*>(wb + o_cn);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
-  e->tcw.part = reinterpret_cast<float*>(wb + o_part);
-  e->tcw.counters = reinterpret_cast<int32_t*>(wb + o_ctr);
-  e->tcw.max_units = max_units;
+
   e3 = cudaMemset(e->work, 0, e->work_bytes);
   // ---- staging for cbd_step / cbd_sample
   const size_t stage_bytes = align_up(R * sizeof(RowDev), 16) + 2 * align_up(S * 4, 16) +
@@ -315,14 +313,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     bool ok = true;
     for (int l = 0; l < L && ok; ++l) {
       const LayerDev& Ld = e->layers[l];
-      // tiled weights: a [M*K/64][64] matrix, one 128-row box per 16 KB tile
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, 128);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, 128);
+      // tiled weights: a [M*K/64][64] matrix, one 256-row box per 32 KB tile
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, 256);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, 256);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, 256);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, 256);
     }
     const size_t a0 = (size_t)4 * L + 1;
-    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, 128);
+    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, 256);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);

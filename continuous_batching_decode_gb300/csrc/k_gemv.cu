@@ -5,7 +5,7 @@
 // reads each weight once for all rows ("0.8MB 跑通 Qwen 第 14-1 篇", section 1;
 // "20.3 服务、批处理与流式" section 20.3.2, cost (W + B*A)/beta).
 //
-// Weights are read from the pre-tiled layout [M/128][K/64][128][64] that
+// Weights are read from the pre-tiled layout [M/256][K/64][256][64] that
 // the tensor-core path uses (16-byte chunks stay contiguous).
 // CTA = 8 warps; a warp owns 4 consecutive output features, so RoPE and
 // SwiGLU partners (features 2i, 2i+1) live in one warp.  Activations for
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
       for (int i = 0; i < kGemvFeat; ++i) {
         const int f = f0 + i;
         w[i] = __ldg(reinterpret_cast<const uint4*>(
-            W + ((((size_t)(f >> 7) * KB + (kk >> 6)) << 7) + (f & 127)) * 64 + (kk & 63)));
+            W + ((((size_t)(f >> 8) * KB + (kk >> 6)) << 8) + (f & 255)) * 64 + (kk & 63)));
       }
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
