@@ -505,21 +505,40 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       }
       __syncwarp();
       const uint32_t ks_base = tc::smem_u32(kt), vs_base = tc::smem_u32(vt);
+      // q.K over 8 independent accumulator chains (m-tile x hi/lo x k
+      // parity) so consecutive MMAs never wait on each other; summed in a
+      // fixed order afterwards
+      float acc[2][2][2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+          for (int par = 0; par < 2; ++par)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][hl][par][c] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int dc = ks * 16 + (mi >> 1) * 8;
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r = mt * 16 + (mi & 1) * 8 + ri;
+          ldsm_x4(ks_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a[mt][0], a[mt][1], a[mt][2], a[mt][3]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          mma_bf16_16816(acc[mt][0][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], qh[ks][0], qh[ks][1]);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          mma_bf16_16816(acc[mt][1][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], ql[ks][0], ql[ks][1]);
+      }
       float sc[2][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sc[mt][c] = 0.f;
-        const int r = mt * 16 + (mi & 1) * 8 + ri;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const int dc = ks * 16 + (mi >> 1) * 8;
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(ks_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
-          mma_bf16_16816(sc[mt], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
-          mma_bf16_16816(sc[mt], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
-        }
-      }
+        for (int c = 0; c < 4; ++c)
+          sc[mt][c] = (acc[mt][0][0][c] + acc[mt][0][1][c]) + (acc[mt][1][0][c] + acc[mt][1][1][c]);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float v[4] = {sc[0][hh], sc[0][hh + 2], sc[1][hh], sc[1][hh + 2]};
@@ -562,17 +581,21 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
           const int j = k2 * 16 + r * 8 + tid4 * 2;
           split_pack(Pw[gid * 32 + j], Pw[gid * 32 + j + 1], ph[k2][r], pl[k2][r]);
         }
+      // P.V: the KS head-dim tiles are independent chains; issue them
+      // interleaved (k2, then hi / lo, then tile) so no MMA waits on the last
 #pragma unroll
-      for (int dt = 0; dt < KS; ++dt) {
-        const int dc = dt * 16 + (mi & 1) * 8;
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int r = k2 * 16 + (mi >> 1) * 8 + ri;
+        uint32_t a[KS][4];
 #pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int r = k2 * 16 + (mi >> 1) * 8 + ri;
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vs_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a0, a1, a2, a3);
-          mma_bf16_16816(o[dt], a0, a1, a2, a3, ph[k2][0], ph[k2][1]);
-          mma_bf16_16816(o[dt], a0, a1, a2, a3, pl[k2][0], pl[k2][1]);
+        for (int dt = 0; dt < KS; ++dt) {
+          const int dc = dt * 16 + (mi & 1) * 8;
+          ldsm_x4_t(vs_base + (dc >> 6) * 4096 + swz(r, (dc & 63) >> 3), a[dt][0], a[dt][1], a[dt][2], a[dt][3]);
         }
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], ph[k2][0], ph[k2][1]);
+#pragma unroll
+        for (int dt = 0; dt < KS; ++dt) mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], pl[k2][0], pl[k2][1]);
       }
       __syncwarp();          // every lane is done with stage s (and Pw)
       issue_next();          // refill it with the block ST ahead

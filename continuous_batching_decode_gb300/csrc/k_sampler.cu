@@ -86,6 +86,28 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
+// Visit this warp's ids in coalesced 32-id rounds, loading kRoundsAhead
+// rounds of `src` before running the rounds' bodies in order: a pass costs a
+// few memory round trips instead of one per round.  f(v, valid, value) runs
+// on every lane for every round (so it may use ballots and shuffles).
+constexpr int kRoundsAhead = 16;
+template <class F>
+__device__ __forceinline__ void for_each_id(const float* __restrict__ src, int v0, int v1, int lane, F&& f) {
+  for (int base = v0; base < v1; base += 32 * kRoundsAhead) {
+    float val[kRoundsAhead];
+#pragma unroll
+    for (int u = 0; u < kRoundsAhead; ++u) {
+      const int v = base + u * 32 + lane;
+      val[u] = v < v1 ? src[v] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kRoundsAhead; ++u) {
+      const int v = base + u * 32 + lane;
+      f(v, v < v1, val[u]);
+    }
+  }
+}
+
 // Exclusive prefix over the 32 warps of one value per warp (lane 0's value
 // counts); returns this warp's prefix and the block total.
 __device__ unsigned long long warp_prefix(unsigned long long mine, SampShared& sh, unsigned long long* total) {
@@ -133,14 +155,26 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   // 1. penalty (and temperature); best key, lowest id on ties
   uint32_t bk = 0;
   int32_t bi = 0x7fffffff;
-  for (int v = v0 + lane; v < v1; v += 32) {
-    const float c = cnt[v];
-    const float l1 = __fsub_rn(lg[v], c > 0.0f ? sp.presence : 0.0f);
-    const float l2 = __fsub_rn(l1, __fmul_rn(sp.frequency, c));
-    const float val = greedy ? l2 : __fdiv_rn(l2, sp.temperature);
-    z[v] = val;
-    const uint32_t k = ord_key(val);
-    if (bi == 0x7fffffff || k > bk) { bk = k; bi = v; }
+  for (int base = v0; base < v1; base += 32 * kRoundsAhead) {
+    float cv[kRoundsAhead], lv[kRoundsAhead];
+#pragma unroll
+    for (int u = 0; u < kRoundsAhead; ++u) {
+      const int v = base + u * 32 + lane;
+      cv[u] = v < v1 ? cnt[v] : 0.f;
+      lv[u] = v < v1 ? lg[v] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kRoundsAhead; ++u) {
+      const int v = base + u * 32 + lane;
+      if (v >= v1) continue;
+      const float c = cv[u];
+      const float l1 = __fsub_rn(lv[u], c > 0.0f ? sp.presence : 0.0f);
+      const float l2 = __fsub_rn(l1, __fmul_rn(sp.frequency, c));
+      const float val = greedy ? l2 : __fdiv_rn(l2, sp.temperature);
+      z[v] = val;
+      const uint32_t k = ord_key(val);
+      if (bi == 0x7fffffff || k > bk) { bk = k; bi = v; }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -173,10 +207,11 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < (kST / 32) * kHistBins; i += kST) whc[i] = 0;
         __syncthreads();
-        for (int v = v0 + lane; v < v1; v += 32) {
-          const uint32_t k = ord_key(z[v]);
+        for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+          if (!valid) return;
+          const uint32_t k = ord_key(zv);
           if ((k & mask) == prefix) atomicAdd(&whc[w * kHistBins + ((k >> shift) & 255u)], 1u);
-        }
+        });
         __syncthreads();
         for (int b = tid; b < kHistBins; b += kST) {
           uint32_t c = 0;
@@ -204,20 +239,18 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       const unsigned long long need_eq = rem;
       // rank among equal keys in id order
       unsigned long long eq = 0;
-      for (int v = v0 + lane; v < v1; v += 32) eq += ord_key(z[v]) == tk;
+      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { eq += valid && ord_key(zv) == tk; });
       unsigned long long tot;
       unsigned long long base = warp_prefix(warp_sum_u64(eq), sh, &tot);
-      for (int v0r = v0; v0r < v1; v0r += 32) {
-        const int v = v0r + lane;
-        const bool valid = v < v1;
-        const uint32_t k = valid ? ord_key(z[v]) : 0u;
+      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+        const uint32_t k = valid ? ord_key(zv) : 0u;
         const unsigned bal = __ballot_sync(0xffffffffu, valid && k == tk);
         if (valid) {
           if (k < tk) z[v] = -INFINITY;
           else if (k == tk && base + __popc(bal & lt_mask) >= need_eq) z[v] = -INFINITY;
         }
         base += __popc(bal);
-      }
+      });
       __syncthreads();
     }
     // 3. fixed-point masses of the kept set
@@ -231,7 +264,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     int32_t cut_id = 0x7fffffff;
     if (sp.top_p < 1.0f) {
       unsigned long long mine = 0;
-      for (int v = v0 + lane; v < v1; v += 32) mine += mass(z[v]);
+      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += mass(zv); });
       unsigned long long S;
       (void)warp_prefix(warp_sum_u64(mine), sh, &S);
       const double target = (double)sp.top_p * (double)S;
@@ -242,9 +275,8 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         for (int shift = 24; shift >= 0; shift -= 8) {
           for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm_lo[i] = 0; whm_hi[i] = 0; }
           __syncthreads();
-          for (int v = v0 + lane; v < v1; v += 32) {
-            const float zv = z[v];
-            if (zv == -INFINITY) continue;
+          for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+            if (!valid || zv == -INFINITY) return;
             const uint32_t k = ord_key(zv);
             if ((k & mask) == prefix) {
               const uint32_t dg = (k >> shift) & 255u;
@@ -253,7 +285,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
               atomicAdd(&whm_lo[w * kHistBins + dg], (uint32_t)(mv & 0xFFFFFull));
               atomicAdd(&whm_hi[w * kHistBins + dg], (uint32_t)(mv >> 20));
             }
-          }
+          });
           __syncthreads();
           for (int b = tid; b < kHistBins; b += kST) {
             uint32_t c = 0;
@@ -287,8 +319,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         tp = prefix;
         // among key == tp, ascending id: first id where above + cum >= target
         unsigned long long eqm = 0;
-        for (int v = v0 + lane; v < v1; v += 32)
-          if (z[v] != -INFINITY && ord_key(z[v]) == tp) eqm += mass(z[v]);
+        for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+          if (valid && zv != -INFINITY && ord_key(zv) == tp) eqm += mass(zv);
+        });
         unsigned long long tot;
         const unsigned long long wbase = warp_prefix(warp_sum_u64(eqm), sh, &tot);
         const unsigned long long wtot = warp_sum_u64(eqm);
@@ -296,27 +329,33 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         __syncthreads();
         if ((double)(above + wbase + wtot) >= target) {   // the crossing may lie in this warp
           unsigned long long run = above + wbase;
-          for (int v0r = v0; v0r < v1; v0r += 32) {
-            const int v = v0r + lane;
-            unsigned long long mv = 0;
-            if (v < v1 && z[v] != -INFINITY && ord_key(z[v]) == tp) mv = mass(z[v]);
+          bool found = false;
+          for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+            if (found) return;
+            const bool eqk = valid && zv != -INFINITY && ord_key(zv) == tp;
+            const unsigned long long mv = eqk ? mass(zv) : 0ull;
             const unsigned long long inc = warp_incl_scan_u64(mv, lane);
-            const bool hit = mv > 0 || (v < v1 && z[v] != -INFINITY && ord_key(z[v]) == tp);
-            const unsigned bal = __ballot_sync(0xffffffffu, hit && (double)(run + inc) >= target);
+            const unsigned bal = __ballot_sync(0xffffffffu, eqk && (double)(run + inc) >= target);
             if (bal) {
               if (lane == __ffs(bal) - 1) atomicMin(&sh.cut_id, v);
-              break;
+              found = true;
+              return;
             }
             run += __shfl_sync(0xffffffffu, inc, 31);
-          }
+          });
         }
         __syncthreads();
         cut_id = sh.cut_id;
         if (cut_id == 0x7fffffff) cut_id = V;   // rounding: keep every element of the tie group
       }
     }
-    auto kept_mass = [&](int v) -> unsigned long long {
-      const float zv = z[v];
+    // 5. inverse CDF in ascending id order
+    float u = sp.uniform;
+    if (u < 0.0f) {
+      const uint32_t x = philox_x(sp.token_index, sp.req_lo, sp.req_hi, 0u, sp.seed_lo, sp.seed_hi);
+      u = (float)(x >> 8) * (1.0f / 16777216.0f);
+    }
+    auto kept_mass_z = [&](int v, float zv) -> unsigned long long {
       if (zv == -INFINITY) return 0ull;
       if (use_cut) {
         const uint32_t k = ord_key(zv);
@@ -324,14 +363,8 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       }
       return mass(zv);
     };
-    // 5. inverse CDF in ascending id order
-    float u = sp.uniform;
-    if (u < 0.0f) {
-      const uint32_t x = philox_x(sp.token_index, sp.req_lo, sp.req_hi, 0u, sp.seed_lo, sp.seed_hi);
-      u = (float)(x >> 8) * (1.0f / 16777216.0f);
-    }
     unsigned long long mine = 0;
-    for (int v = v0 + lane; v < v1; v += 32) mine += kept_mass(v);
+    for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += kept_mass_z(v, zv); });
     const unsigned long long wtot = warp_sum_u64(mine);
     unsigned long long Sk;
     const unsigned long long wbase = warp_prefix(wtot, sh, &Sk);
@@ -340,17 +373,19 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     __syncthreads();
     if (wbase <= T && wbase + wtot > T) {
       unsigned long long run = wbase;
-      for (int v0r = v0; v0r < v1; v0r += 32) {
-        const int v = v0r + lane;
-        const unsigned long long mv = v < v1 ? kept_mass(v) : 0ull;
+      bool found = false;
+      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+        if (found) return;
+        const unsigned long long mv = valid ? kept_mass_z(v, zv) : 0ull;
         const unsigned long long inc = warp_incl_scan_u64(mv, lane);
         const unsigned bal = __ballot_sync(0xffffffffu, run + inc > T && mv > 0);
         if (bal) {
           if (lane == __ffs(bal) - 1) sh.tok = v;
-          break;
+          found = true;
+          return;
         }
         run += __shfl_sync(0xffffffffu, inc, 31);
-      }
+      });
     }
     __syncthreads();
     if (sh.tok == 0x7fffffff) {
@@ -360,7 +395,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   }
   // 6. counters: decay everything, then count the drawn token
   const int tok = sh.tok;
-  for (int v = v0 + lane; v < v1; v += 32) cnt[v] = __fmul_rn(cnt[v], sp.decay);
+  for_each_id(cnt, v0, v1, lane, [&](int v, bool valid, float c) { if (valid) cnt[v] = __fmul_rn(c, sp.decay); });
   __syncthreads();
   if (tid == 0) {
     cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
