@@ -49,13 +49,35 @@ __device__ __forceinline__ uint32_t ord_key(float f) {
 }
 
 // Radix histograms: every warp owns a private [256] count and mass
-// histogram in dynamic shared memory (no atomics contend across warps);
-// the block then sums them bin by bin in warp order.  A mass (< 2^41) is
-// accumulated as two 32-bit halves, low 20 bits and the rest, so every
-// shared-memory atomic is a native 32-bit add: a warp's bin holds at most
-// 2048 elements, so neither half can overflow.
+// histogram in dynamic shared memory; the block then sums them bin by bin
+// in warp order.  A warp updates its histogram one digit group at a time:
+// the lanes holding the same digit are found with a ballot, their count is
+// a popcount and their mass a warp reduction, and only the group's leader
+// lane writes -- no atomics, and in the early passes (where almost every
+// element falls in one or two bins) one update per round instead of 32.
 constexpr int kHistBins = 256;
-constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * 3 * sizeof(uint32_t);
+constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * (sizeof(uint32_t) + sizeof(unsigned long long));
+
+// Add the participating lanes' (digit, mass) to this warp's histogram.
+__device__ __forceinline__ void warp_hist_add(bool part, uint32_t dg, unsigned long long mv, uint32_t* hc,
+                                              unsigned long long* hm, int lane) {
+  unsigned active = __ballot_sync(0xffffffffu, part);
+  while (active) {
+    const int leader = __ffs(active) - 1;
+    const uint32_t d = __shfl_sync(0xffffffffu, dg, leader);
+    const bool mine = part && dg == d;
+    const unsigned grp = __ballot_sync(0xffffffffu, mine);
+    if (hm) {
+      // masses < 2^41: sum the low 20 bits and the rest separately (each sum
+      // of at most 32 lanes fits 32 bits)
+      const uint32_t slo = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)(mv & 0xFFFFFull) : 0u);
+      const uint32_t shi = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)(mv >> 20) : 0u);
+      if (lane == leader) hm[d] += ((unsigned long long)shi << 20) + slo;
+    }
+    if (lane == leader) hc[d] += __popc(grp);
+    active &= ~grp;
+  }
+}
 
 struct SampShared {
   unsigned long long wsum[32];
@@ -136,9 +158,8 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       int32_t* __restrict__ out, int32_t* err) {
   __shared__ SampShared sh;
   extern __shared__ __align__(16) uint8_t samp_dyn[];
-  uint32_t* whm_lo = reinterpret_cast<uint32_t*>(samp_dyn);              // [32][256] mass bits 0..19
-  uint32_t* whm_hi = whm_lo + (kST / 32) * kHistBins;                    // [32][256] mass >> 20
-  uint32_t* whc = whm_hi + (kST / 32) * kHistBins;                       // [32][256] counts
+  unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn);       // [32][256] masses
+  uint32_t* whc = reinterpret_cast<uint32_t*>(whm + (kST / 32) * kHistBins);       // [32][256] counts
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -208,9 +229,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         for (int i = tid; i < (kST / 32) * kHistBins; i += kST) whc[i] = 0;
         __syncthreads();
         for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
-          if (!valid) return;
           const uint32_t k = ord_key(zv);
-          if ((k & mask) == prefix) atomicAdd(&whc[w * kHistBins + ((k >> shift) & 255u)], 1u);
+          warp_hist_add(valid && (k & mask) == prefix, (k >> shift) & 255u, 0ull, whc + w * kHistBins, nullptr,
+                        lane);
         });
         __syncthreads();
         for (int b = tid; b < kHistBins; b += kST) {
@@ -273,18 +294,13 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         uint32_t prefix = 0, mask = 0;
         unsigned long long above = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm_lo[i] = 0; whm_hi[i] = 0; }
+          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
           __syncthreads();
           for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
-            if (!valid || zv == -INFINITY) return;
             const uint32_t k = ord_key(zv);
-            if ((k & mask) == prefix) {
-              const uint32_t dg = (k >> shift) & 255u;
-              const unsigned long long mv = mass(zv);
-              atomicAdd(&whc[w * kHistBins + dg], 1u);
-              atomicAdd(&whm_lo[w * kHistBins + dg], (uint32_t)(mv & 0xFFFFFull));
-              atomicAdd(&whm_hi[w * kHistBins + dg], (uint32_t)(mv >> 20));
-            }
+            const bool part = valid && zv != -INFINITY && (k & mask) == prefix;
+            warp_hist_add(part, (k >> shift) & 255u, part ? mass(zv) : 0ull, whc + w * kHistBins, whm + w * kHistBins,
+                          lane);
           });
           __syncthreads();
           for (int b = tid; b < kHistBins; b += kST) {
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             unsigned long long mm = 0;
             for (int ww = 0; ww < kST / 32; ++ww) {
               c += whc[ww * kHistBins + b];
-              mm += ((unsigned long long)whm_hi[ww * kHistBins + b] << 20) + whm_lo[ww * kHistBins + b];
+              mm += whm[ww * kHistBins + b];
             }
             sh.hc[b] = c;
             sh.hm[b] = mm;
