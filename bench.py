@@ -297,7 +297,8 @@ def run_cbd(args):
     torch.cuda.empty_cache()
     pool = cbd.kv_pool_create(e, wl["n_pool"])
     base, nbytes, nb = cbd.kv_pool_data(pool)
-    kv = cbd.device_view(base, (s["n_layers"], 2, nb, s["n_kv_heads"], 32, s["head_dim"]), "bf16")
+    # [L][n_blocks][H_kv][K|V][32 * hd]: each tile in 128-byte-swizzled order
+    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "bf16")
     gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
     for l in range(s["n_layers"]):
         kv[l].copy_((torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3).to(torch.bfloat16))
@@ -404,9 +405,16 @@ def run_cbd(args):
                 return synth.bf16_bits(E[torch.as_tensor(a[0], device="cuda")])
             return wbits[name]
 
+        hd = s["head_dim"]
+        rr, dd = np.arange(32)[:, None], np.arange(hd)[None, :]
+        tidx = torch.as_tensor(((dd // 64) * 2048 + rr * 64 + ((((dd % 64) // 8) ^ (rr % 8)) * 8) + dd % 8).reshape(-1),
+                               device="cuda")
+
         def kv_source(i, c):
-            ids = torch.as_tensor(wl["tables"][i][: (c + 31) // 32].astype(np.int64), device="cuda")
-            t = kv[0, :, ids].permute(0, 1, 3, 2, 4).reshape(2, -1, s["n_kv_heads"], s["head_dim"])[:, :c]
+            nbk = (c + 31) // 32
+            ids = torch.as_tensor(wl["tables"][i][:nbk].astype(np.int64), device="cuda")
+            t = kv[0, ids][..., tidx].reshape(nbk, s["n_kv_heads"], 2, 32, hd)      # unswizzled
+            t = t.permute(2, 0, 3, 1, 4).reshape(2, nbk * 32, s["n_kv_heads"], hd)[:, :c]
             t = t.float().cpu().numpy().astype(np.float64)
             return t[0], t[1]
         toks = [r[1] for r in wl["rows"]]

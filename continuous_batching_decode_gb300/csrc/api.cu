@@ -453,11 +453,6 @@ extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv
   void* b = nullptr;
   CBD_CUDA(cudaMalloc(&b, bytes));
   p->base = static_cast<uint16_t*>(b);
-  const uint64_t rows = (uint64_t)e->dm.L * 2 * (uint64_t)n_blocks * e->dm.hkv * kBlock;
-  if (rows >= (1ull << 31) || !make_tmap_bf16(&p->tmap, p->base, e->dm.hd, rows, e->dm.hd, 32)) {
-    cudaFree(b);
-    return fail(CBD_EUNSUPPORTED, "KV pool too large for a tensor map (%llu rows)", (unsigned long long)rows);
-  }
   *out = p.release();
   return CBD_OK;
 }

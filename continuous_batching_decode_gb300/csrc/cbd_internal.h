@@ -146,7 +146,6 @@ struct cbd_kv_pool {
   uint16_t* base = nullptr;
   int32_t n_blocks = 0;
   size_t bytes = 0;
-  CUtensorMap tmap;                   // the pool as [L*2*n_blocks*H_kv*32][hd] bf16, box 32 x 64, 128B swizzle
 };
 
 struct cbd_batch {

@@ -46,11 +46,21 @@ __device__ __forceinline__ void set_err(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-// Pool element offset of (layer, kv, block, kv head, position-in-block, dim).
-__device__ __forceinline__ size_t pool_off(int layer, int kv, int nblocks, int blk, int hkv, int kvh,
-                                           int hd, int p, int dim) {
-  return ((((size_t)layer * 2 + kv) * nblocks + blk) * hkv + kvh) * (size_t)(kBlock * hd) +
-         (size_t)p * hd + dim;
+// KV pool layout: [L][n_blocks][H_kv][K|V][tile], one tile = 32 positions x
+// hd dims of bf16 stored in the order a 128-byte-swizzled shared-memory copy
+// of it has: dims in 64-wide halves, each half 32 rows of 128 bytes, and
+// the 16-byte chunk c of row r at chunk position c ^ (r & 7).  So K and V of
+// one (layer, block, KV head) are one contiguous 2 * 32 * hd * 2-byte run
+// that a single bulk copy lands in shared memory ready for ldmatrix.
+__host__ __device__ __forceinline__ int tile_elem(int r, int d) {
+  return (d >> 6) * 2048 + r * 64 + ((((d & 63) >> 3) ^ (r & 7)) << 3) + (d & 7);
+}
+__host__ __device__ __forceinline__ size_t pool_tile(int layer, int nblocks, int blk, int hkv, int kvh, int kv, int hd) {
+  return ((((size_t)layer * nblocks + blk) * hkv + kvh) * 2 + kv) * (size_t)(kBlock * hd);
+}
+__device__ __forceinline__ size_t pool_off(int layer, int kv, int nblocks, int blk, int hkv, int kvh, int hd, int p,
+                                           int dim) {
+  return pool_tile(layer, nblocks, blk, hkv, kvh, kv, hd) + tile_elem(p, dim);
 }
 
 // Epilogue for a pair of adjacent output features (f, f+1), f even, of
@@ -84,9 +94,9 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& ep, int f, int row, floa
     } else {
       const int blk = ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)];
       if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
-      size_t o = pool_off(ep.layer, 0, ep.n_blocks, blk, ep.hkv, head, hd, rw.pos & 31, i);
-      ep.pool[o] = f32_to_bf16(ra);
-      ep.pool[o + half] = f32_to_bf16(rb);
+      const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 0, hd);
+      ep.pool[t0 + tile_elem(rw.pos & 31, i)] = f32_to_bf16(ra);
+      ep.pool[t0 + tile_elem(rw.pos & 31, i + half)] = f32_to_bf16(rb);
     }
   } else {
     const int fv = f - nq - nk;
@@ -177,9 +187,9 @@ __device__ __forceinline__ void epi_rows(const EpiArgs& ep, int m, int lane, int
     for (int j = 0; j < NB; ++j)
       if (row0 + j < n) {
         if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
-        const size_t o = pool_off(ep.layer, 0, ep.n_blocks, blk[j], ep.hkv, head, hd, rw[j].pos & 31, i);
-        ep.pool[o] = f32_to_bf16(v[j] * cs[j].x - pv[j] * cs[j].y);
-        ep.pool[o + half] = f32_to_bf16(pv[j] * cs[j].x + v[j] * cs[j].y);
+        const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk[j], ep.hkv, head, 0, hd);
+        ep.pool[t0 + tile_elem(rw[j].pos & 31, i)] = f32_to_bf16(v[j] * cs[j].x - pv[j] * cs[j].y);
+        ep.pool[t0 + tile_elem(rw[j].pos & 31, i + half)] = f32_to_bf16(pv[j] * cs[j].x + v[j] * cs[j].y);
       }
     return;
   }

@@ -3,30 +3,32 @@
 // A row (slot s, position p) attends to positions 0..p of its slot.  K/V
 // live in the paged pool ("20.3 服务、批处理与流式" section 20.3.2: PagedAttention
 // splits the KV cache into fixed-size blocks allocated on demand); the row
-// reaches its blocks through the slot's block table, one 32-position tile
-// per (layer, K|V, block, KV head).  Because every row's K/V of this layer
-// has been stored by the QKV epilogue before this kernel runs, a prefill row
-// sees the earlier rows of its own chunk (causal chunked prefill) with no
-// separate mask.
+// reaches its blocks through the slot's block table.  Per (layer, block, KV
+// head) the pool holds the K tile and then the V tile (32 positions each),
+// each stored in 128-byte-swizzled shared-memory order, so one contiguous
+// bulk copy brings a block into shared memory ready for ldmatrix.  Because
+// every row's K/V of this layer has been stored by the QKV epilogue before
+// this kernel runs, a prefill row sees the earlier rows of its own chunk
+// (causal chunked prefill) with no separate mask.
 //
 // Split-K: each row's positions are cut into fixed 128-position chunks (a
-// host-built work list); one CTA handles one (chunk, KV head) for the H_q /
-// H_kv query heads that share the KV head, keeping an online softmax
-// (running max, running sum, unnormalised output).
+// host-built work list); a chunk is computed for one KV head and the H_q /
+// H_kv query heads that share it, keeping an online softmax (running max,
+// running sum, unnormalised output).
 //
-// Three kernels compute the chunks.  attn_stream_kernel (default) is the
-// persistent, per-warp-pipelined form described below.  attn_mma_kernel
-// (one CTA per chunk) stages the four
-// 32-position K and V tiles of the chunk in shared memory with TMA (128-byte
-// swizzle) and runs q.K and P.V on the tensor cores with mma.sync, in a
-// swapped form -- positions (or head dims) on the MMA's M side, the <= 8
-// query heads of the KV group on its N side -- with q and P split into hi +
-// lo bf16 halves so the products keep ~16 significant bits; K and V are
-// bf16 already.  attn_partial_kernel is the CUDA-core version.  A second kernel merges
-// the chunks of each (row, head) in chunk order and writes the output as
-// hi + lo bf16 halves for the O projection.  The chunking depends only on
-// the row's position, and the merge order is fixed, so a row's result does
-// not depend on the other rows of the step or on block placement.
+// Three kernels compute the chunks.  attn_stream_kernel (default): every
+// warp owns a strided sequence of chunks and streams their blocks through a
+// private ring of shared-memory stages.  attn_mma_kernel: one CTA per chunk,
+// one block per warp.  Both run q.K and P.V on the tensor cores with
+// mma.sync in a swapped form -- positions (or head dims) on the MMA's M
+// side, the <= 8 query heads of the KV group on its N side -- with q and P
+// split into hi + lo bf16 halves so the products keep ~16 significant bits
+// (K and V are bf16 already).  attn_partial_kernel is the CUDA-core
+// version.  A second kernel merges the chunks of each (row, head) in chunk
+// order and writes the output as hi + lo bf16 halves for the O projection.
+// The chunking depends only on the row's position and the merge order is
+// fixed, so a row's result does not depend on the other rows of the step or
+// on block placement.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -68,16 +70,15 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(
     const int blk = tables[(size_t)rw.slot * mbps + bi];
     if (blk < 0 || blk >= n_blocks) { set_err(err, kDevBadBlock); break; }
     const int nvalid = min(kBlock, end - b0);
-    const uint16_t* Kt = pool + pool_off(layer, 0, n_blocks, blk, hkv, kvh, HD, 0, 0);
-    const uint16_t* Vt = pool + pool_off(layer, 1, n_blocks, blk, hkv, kvh, HD, 0, 0);
+    const uint16_t* Kt = pool + pool_tile(layer, n_blocks, blk, hkv, kvh, 0, HD);
+    const uint16_t* Vt = pool + pool_tile(layer, n_blocks, blk, hkv, kvh, 1, HD);
     float s[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) s[g] = 0.f;
     if (lane < nvalid) {
-      const uint4* kr = reinterpret_cast<const uint4*>(Kt + (size_t)lane * HD);
 #pragma unroll 4
       for (int c = 0; c < HD / 8; ++c) {
-        const uint4 kv = __ldg(kr + c);
+        const uint4 kv = __ldg(reinterpret_cast<const uint4*>(Kt + tile_elem(lane, c * 8)));
         const float kf[8] = {bf16lo_f32(kv.x), bf16hi_f32(kv.x), bf16lo_f32(kv.y), bf16hi_f32(kv.y),
                              bf16lo_f32(kv.z), bf16hi_f32(kv.z), bf16lo_f32(kv.w), bf16hi_f32(kv.w)};
 #pragma unroll
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(
       m[g] = mn;
     }
     for (int j = 0; j < nvalid; ++j) {
-      const uint16_t* vr = Vt + (size_t)j * HD + lane * DPL;
+      const uint16_t* vr = Vt + tile_elem(j, lane * DPL);
       float vf[DPL];
       if constexpr (DPL == 4) {
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(vr));
@@ -189,7 +190,7 @@ constexpr int attn_mma_smem() {
 }
 
 template <int HD, int G>
-__global__ void __launch_bounds__(128) attn_mma_kernel(const __grid_constant__ CUtensorMap tmKV,
+__global__ void __launch_bounds__(128) attn_mma_kernel(const uint16_t* __restrict__ pool,
                                                        const float* __restrict__ q, const RowDev* __restrict__ rows,
                                                        const int32_t* __restrict__ tables,
                                                        const AttnWork* __restrict__ work, int layer, int n_blocks,
@@ -230,13 +231,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const __grid_constant__ C
   __syncthreads();
   if (have && lane == 0) {
     tc::mbar_arrive_expect_tx(&bar[warp], 2 * TILE);
-    const size_t rk = ((((size_t)layer * 2 + 0) * n_blocks + blk) * hkv + kvh) * 32;
-    const size_t rv = ((((size_t)layer * 2 + 1) * n_blocks + blk) * hkv + kvh) * 32;
-#pragma unroll
-    for (int h = 0; h < HD / 64; ++h) {
-      tc::tma_load_2d(kt + h * 4096, &tmKV, h * 64, (int)rk, &bar[warp]);
-      tc::tma_load_2d(vt + h * 4096, &tmKV, h * 64, (int)rv, &bar[warp]);
-    }
+    tc::bulk_load(kt, pool + pool_tile(layer, n_blocks, blk, hkv, kvh, 0, HD), 2 * TILE, &bar[warp]);
   }
   // q of the group's heads (scaled by 1/sqrt(hd)) as hi / lo B fragments
   const float scale = 1.0f / sqrtf((float)HD);
@@ -394,7 +389,7 @@ __host__ __device__ constexpr int attn_stream_smem() {
 
 template <int HD, int G>
 __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
-    const __grid_constant__ CUtensorMap tmKV, const float* __restrict__ q, const RowDev* __restrict__ rows,
+    const uint16_t* __restrict__ pool, const float* __restrict__ q, const RowDev* __restrict__ rows,
     const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, int n_tasks, int layer, int n_blocks,
     int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
   static_assert(G >= 1 && G <= 8, "a KV group must fit the MMA's N = 8");
@@ -449,13 +444,7 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       if (blk < 0 || blk >= n_blocks) { set_err(err, kDevBadBlock); blk = 0; }
       uint8_t* kt = ring + s * 2 * TILE;
       tc::mbar_arrive_expect_tx(&bar[warp][s], 2 * TILE);
-      const size_t rk = ((((size_t)layer * 2 + 0) * n_blocks + blk) * hkv + pt.kvh) * 32;
-      const size_t rv = ((((size_t)layer * 2 + 1) * n_blocks + blk) * hkv + pt.kvh) * 32;
-#pragma unroll
-      for (int h = 0; h < HD / 64; ++h) {
-        tc::tma_load_2d(kt + h * 4096, &tmKV, h * 64, (int)rk, &bar[warp][s]);
-        tc::tma_load_2d(kt + TILE + h * 4096, &tmKV, h * 64, (int)rv, &bar[warp][s]);
-      }
+      tc::bulk_load(kt, pool + pool_tile(layer, n_blocks, blk, hkv, pt.kvh, 0, HD), 2 * TILE, &bar[warp][s]);
     }
     ++p_q;
     if (++p_blk == pt.nb) {
@@ -672,7 +661,8 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     }
     const int n_tasks = b->n_work * dm.hkv;
     const int grid = std::min(e->sm_count, (n_tasks + kAttnWarps - 1) / kAttnWarps);
-    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(128), smem, s, p->tmap, (const float*)e->q,
+    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(128), smem, s, (const uint16_t*)p->base,
+                                (const float*)e->q,
                                 (const RowDev*)b->rows, (const int32_t*)b->tables, (const AttnWork*)b->work, n_tasks,
                                 layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
     if (ce != cudaSuccess) return ce;
@@ -684,8 +674,8 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
       if (ce != cudaSuccess) return ce;
       attr = true;
     }
-    cudaError_t ce = launch_pdl(attn_mma_kernel<HD, G>, dim3(b->n_work, dm.hkv), dim3(128), smem, s, p->tmap,
-                                (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
+    cudaError_t ce = launch_pdl(attn_mma_kernel<HD, G>, dim3(b->n_work, dm.hkv), dim3(128), smem, s,
+                                (const uint16_t*)p->base, (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
                                 (const AttnWork*)b->work, layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq,
                                 e->attn_o, e->attn_ml, e->err);
     if (ce != cudaSuccess) return ce;

@@ -154,9 +154,9 @@ __device__ __forceinline__ void epi_pairs(const EpiArgs& ep, const int (&row)[NB
     if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
     if (fj < nq + nk) {
       const int head = (fj - nq) / hd, i = ((fj - nq) % hd) >> 1;
-      const size_t o = pool_off(ep.layer, 0, ep.n_blocks, blk[j], ep.hkv, head, hd, pos[j] & 31, i);
-      ep.pool[o] = f32_to_bf16(a[j] * cs[j].x - b[j] * cs[j].y);
-      ep.pool[o + half] = f32_to_bf16(b[j] * cs[j].x + a[j] * cs[j].y);
+      const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk[j], ep.hkv, head, 0, hd);
+      ep.pool[t0 + tile_elem(pos[j] & 31, i)] = f32_to_bf16(a[j] * cs[j].x - b[j] * cs[j].y);
+      ep.pool[t0 + tile_elem(pos[j] & 31, i + half)] = f32_to_bf16(b[j] * cs[j].x + a[j] * cs[j].y);
     } else {
       const int fv = fj - nq - nk, head = fv / hd, jd = fv % hd;
       const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk[j], ep.hkv, head, hd, pos[j] & 31, jd);

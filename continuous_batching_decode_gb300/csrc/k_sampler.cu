@@ -24,7 +24,7 @@
 namespace cbd {
 
 constexpr int kST = 1024;            // threads per sampler CTA
-constexpr double kFix = 1099511627776.0;   // 2^40
+constexpr float kFix = 1099511627776.0f;   // 2^40 (exact in fp32)
 
 // Philox-4x32-10 (Salmon et al., SC'11): 10 rounds of the 4x32 bijection
 // with multipliers 0xD2511F53, 0xCD9E8D57 and Weyl key increments
@@ -275,9 +275,11 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       __syncthreads();
     }
     // 3. fixed-point masses of the kept set
+    // exp(z - zmax) * 2^40 is exact in fp32 (a power-of-two scale of an fp32
+    // value), so rounding it to an integer needs no fp64 arithmetic
     auto mass = [&](float zv) -> unsigned long long {
       if (zv == -INFINITY) return 0ull;
-      return __double2ull_rn((double)expf(zv - zmax) * kFix);
+      return __float2ull_rn(expf(zv - zmax) * kFix);
     };
     // 4. top-p cutoff: shortest prefix by (key desc, id asc) with mass >= top_p * S
     bool use_cut = false;
@@ -288,8 +290,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += mass(zv); });
       unsigned long long S;
       (void)warp_prefix(warp_sum_u64(mine), sh, &S);
-      const double target = (double)sp.top_p * (double)S;
-      if ((double)S >= target) {
+      // cumulative mass >= top_p * S  <=>  cumulative >= ceil(top_p * S)
+      const unsigned long long target = (unsigned long long)ceil((double)sp.top_p * (double)S);
+      if (S >= target) {
         use_cut = true;
         uint32_t prefix = 0, mask = 0;
         unsigned long long above = 0;
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             for (; d >= 0; --d) {
               if (sh.hc[d] == 0) continue;
               last = d;
-              if ((double)(above + sh.hm[d]) >= target) break;
+              if (above + sh.hm[d] >= target) break;
               above += sh.hm[d];
             }
             if (d < 0) d = last;        // rounding: take the lowest non-empty digit
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         const unsigned long long wtot = warp_sum_u64(eqm);
         if (tid == 0) sh.cut_id = 0x7fffffff;
         __syncthreads();
-        if ((double)(above + wbase + wtot) >= target) {   // the crossing may lie in this warp
+        if (above + wbase + wtot >= target) {   // the crossing may lie in this warp
           unsigned long long run = above + wbase;
           bool found = false;
           for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             const bool eqk = valid && zv != -INFINITY && ord_key(zv) == tp;
             const unsigned long long mv = eqk ? mass(zv) : 0ull;
             const unsigned long long inc = warp_incl_scan_u64(mv, lane);
-            const unsigned bal = __ballot_sync(0xffffffffu, eqk && (double)(run + inc) >= target);
+            const unsigned bal = __ballot_sync(0xffffffffu, eqk && run + inc >= target);
             if (bal) {
               if (lane == __ffs(bal) - 1) atomicMin(&sh.cut_id, v);
               found = true;

@@ -161,9 +161,13 @@ cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream);
 /* ------------------------------------------------------------ KV pool */
 /* Paged KV pool ("20.3 服务、批处理与流式" section 20.3.2: fixed-size blocks
  * allocated on demand; Forma: 32 positions per block).  Layout, bf16:
- *     pool[L][2][n_blocks][H_kv][32][hd]     (index 0 = K, 1 = V)
- * so one (layer, K|V, block, kv head) is a contiguous 32*hd*2-byte tile.
- * The pool is owned by libcbd; its contents start undefined. */
+ *     pool[L][n_blocks][H_kv][2][tile]     (index 0 = K, 1 = V)
+ * where a tile holds 32 positions x hd dims in 128-byte-swizzled order:
+ * element (position r, dim d) sits at
+ *     (d / 64) * 2048 + r * 64 + (((d % 64) / 8) XOR (r % 8)) * 8 + d % 8.
+ * So K and V of one (layer, block, KV head) are one contiguous
+ * 2 * 32 * hd * 2-byte run.  The pool is owned by libcbd; its contents
+ * start undefined. */
 cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv_pool** out);
 cbd_status cbd_kv_pool_destroy(cbd_kv_pool* p);
 

@@ -44,7 +44,14 @@ class Pool:
         self.p = cbd.kv_pool_create(model.e, n_blocks)
         base, nbytes, nb = cbd.kv_pool_data(self.p)
         s = model.shape
-        self.view = cbd.device_view(base, (s["n_layers"], 2, nb, s["n_kv_heads"], 32, s["head_dim"]), "bf16")
+        hd = s["head_dim"]
+        # [L][n_blocks][H_kv][K|V][tile]; a tile stores (position, dim) at a
+        # 128-byte-swizzled offset (see cbd_kv_pool_data in include/cbd.h)
+        self.view = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * hd), "bf16")
+        r = np.arange(32)[:, None]
+        d = np.arange(hd)[None, :]
+        self.tile_index = torch.as_tensor(((d // 64) * 2048 + r * 64 + ((((d % 64) // 8) ^ (r % 8)) * 8) + d % 8)
+                                          .reshape(-1), device="cuda")
 
     def close(self):
         cbd.kv_pool_destroy(self.p)
@@ -53,10 +60,12 @@ class Pool:
         """Contiguous K, V of a slot: lists per layer of [n_pos, H_kv, hd] fp64."""
         nb = (n_pos + 31) // 32
         ids = torch.as_tensor(tables[slot][:nb].astype(np.int64), device="cuda")
-        kv = self.view[:, :, ids]                        # [L, 2, nb, Hkv, 32, hd]
-        kv = kv.permute(0, 1, 2, 4, 3, 5).reshape(kv.shape[0], 2, nb * 32, kv.shape[3], kv.shape[5])
+        L, _, hkv, _, te = self.view.shape
+        hd = te // 32
+        kv = self.view[:, ids][..., self.tile_index].reshape(L, nb, hkv, 2, 32, hd)   # unswizzled
+        kv = kv.permute(0, 3, 1, 4, 2, 5).reshape(L, 2, nb * 32, hkv, hd)
         kv = kv[:, :, :n_pos].float().cpu().numpy().astype(np.float64)
-        return [kv[l, 0] for l in range(kv.shape[0])], [kv[l, 1] for l in range(kv.shape[0])]
+        return [kv[l, 0] for l in range(L)], [kv[l, 1] for l in range(L)]
 
 
 def gpu_prefill(model, pool, slot, tokens, tables, nbps, start=0, chunk=512):
