@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
+    ap.add_argument("--l2-prefetch-mb", type=int, default=48,
+                    help="MiB of the next weight contraction each kernel prefetches into L2 (0: off)")
     return ap.parse_args()
 
 
@@ -308,6 +310,7 @@ def run_cbd(args):
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
     cbd.engine_set_attention_path(e, args.attn_path)
+    cbd.engine_set_l2_prefetch(e, args.l2_prefetch_mb << 20)
     if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
         del w
     torch.cuda.empty_cache()
@@ -445,7 +448,8 @@ def run_cbd(args):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, random bf16 KV)",
-            "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path),
+            "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path,
+                           l2_prefetch_mb=args.l2_prefetch_mb),
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu}
     if rank == 0:

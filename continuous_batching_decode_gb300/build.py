@@ -35,18 +35,21 @@ def _newest_header() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def build(verbose: bool = False, force: bool = False, extra: list | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra: list | None = None, lib: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile and link; `extra` nvcc flags (e.g. -DCBD_TRACE for the
+    timeline-tracing variant) go with `lib` / `build_dir` of their own."""
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdr = _newest_header()
     cc = nvcc()
     jobs = []
     for s in srcs:
-        obj = os.path.join(BUILD, os.path.basename(s) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(s) + ".o")
         if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(s), hdr):
             cmd = [cc, *ARCH, *FLAGS, *(extra or []), "-c", s, "-o", obj]
             jobs.append((s, cmd))
-    objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
+    objs = [os.path.join(build_dir, os.path.basename(s) + ".o") for s in srcs]
 
     def run(job):
         s, cmd = job
@@ -60,8 +63,8 @@ def build(verbose: bool = False, force: bool = False, extra: list | None = None)
                 print(r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed on {os.path.basename(s)}")
-    if jobs or force or not os.path.exists(LIB):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-lcudart_static", "-ldl", "-lrt",
+    if jobs or force or not os.path.exists(lib):
+        cmd = [cc, *ARCH, "-shared", "-o", lib, *objs, "-lcudart_static", "-ldl", "-lrt",
                "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if verbose or r.returncode:
@@ -69,7 +72,7 @@ def build(verbose: bool = False, force: bool = False, extra: list | None = None)
             print(r.stdout + r.stderr)
         if r.returncode:
             raise RuntimeError("link of libcbd.so failed")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -424,6 +424,15 @@ extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path)
   return CBD_OK;
 }
 
+extern "C" cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (bytes > ((uint64_t)1 << 30)) return fail(CBD_EINVAL, "prefetch of %llu bytes is more than 1 GiB",
+                                              (unsigned long long)bytes);
+  e->l2_prefetch = (size_t)bytes;
+  return CBD_OK;
+}
+
 extern "C" cbd_status cbd_engine_counters(cbd_engine* e, float** counters) {
   if (!e || !counters) return fail(CBD_EINVAL, "NULL argument");
   *counters = e->counters;
@@ -653,6 +662,9 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
     if (ce != cudaSuccess) return cuda_fail(ce, what);
     return CBD_OK;
   };
+  if (out_logits && (reinterpret_cast<uintptr_t>(out_logits) & 15))
+    return fail(CBD_EINVAL, "out_logits must be 16-byte aligned");
+  if (b->m > 0 && !out_tokens) return fail(CBD_EINVAL, "out_tokens is NULL but rows are sampled");
   cbd_status st;
   if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, s); }), "embed"))) return st;
   ++launches;
@@ -667,33 +679,45 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   glu.kind = kEpiSwiGLU; glu.out_hi = e->ffn_hi; glu.out_lo = e->ffn_lo; glu.ld_act = dm.F; glu.err = e->err;
   const size_t a0 = (size_t)4 * dm.L + 1;
   const CUtensorMap* tm = e->tmaps.data();
+  // The step's GEMMs in order; each kernel prefetches (into L2) the first
+  // k-blocks of the GEMM after it, so HBM keeps streaming across launches.
+  auto g_qkv_of = [&](int l) {
+    return GemmOp{e->layers[l].w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d,
+                  {&tm[4 * l + 0], &tm[a0 + 0], &tm[a0 + 1], dm.qkv_out, dm.d}};
+  };
+  const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
+                    {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d}};
+  const PfSpec pf_none{};
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
     qkv.layer = l;
-    const GemmOp g_qkv{L.w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d,
-                       {&tm[4 * l + 0], &tm[a0 + 0], &tm[a0 + 1], dm.qkv_out, dm.d}};
+    const GemmOp g_qkv = g_qkv_of(l);
     const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd}};
     const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, e->act_hi, e->act_lo, dm.d,
                       {&tm[4 * l + 2], &tm[a0 + 0], &tm[a0 + 1], 2 * dm.F, dm.d}};
     const GemmOp g_dn{L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F,
                       {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F}};
+    const PfSpec pf_o = next_prefetch(e, g_o, n), pf_gu = next_prefetch(e, g_gu, n),
+                 pf_dn = next_prefetch(e, g_dn, n);
+    const PfSpec pf_after_dn = l + 1 < dm.L ? next_prefetch(e, g_qkv_of(l + 1), n)
+                                            : (b->m > 0 ? next_prefetch(e, g_lm, b->m) : pf_none);
     if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.attn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
                   "rmsnorm")))
       return st;
-    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, s); }),
+    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, pf_none, s); }),
                   "qkv")))
       return st;
-    if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, s); }), "attention"))) return st;
-    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res, s); }),
+    if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, pf_o, s); }), "attention"))) return st;
+    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res, pf_gu, s); }),
                   "o_proj")))
       return st;
     if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.ffn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
                   "rmsnorm")))
       return st;
-    if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, g_gu, n, glu, s); }),
+    if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, g_gu, n, glu, pf_dn, s); }),
                   "gate_up")))
       return st;
-    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res, s); }),
+    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res, pf_after_dn, s); }),
                   "down")))
       return st;
     launches += 8;
@@ -706,9 +730,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
       return st;
     EpiArgs lo{};
     lo.kind = kEpiLogits; lo.out_f32 = lg; lo.ld = dm.V; lo.err = e->err;
-    const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
-                      {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d}};
-    if ((st = chk(timed(e, kcLM, s, [&] { return launch_gemm(e, g_lm, b->m, lo, s); }),
+    if ((st = chk(timed(e, kcLM, s, [&] { return launch_gemm(e, g_lm, b->m, lo, pf_none, s); }),
                   "lm_head")))
       return st;
     if ((st = chk(timed(e, kcSamp, s, [&] { return launch_sampler(e, lg, b->m, b->sampled_slots, b->samp, out_tokens, s); }),
@@ -732,6 +754,8 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
                                     uniforms, &img);
   if (st) return st;
   if (img.m > 0 && !out_tokens) return fail(CBD_EINVAL, "out_tokens is NULL but rows are sampled");
+  if (out_logits && (reinterpret_cast<uintptr_t>(out_logits) & 15))
+    return fail(CBD_EINVAL, "out_logits must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cbd_engine::Stage& sg = e->stage[e->stage_idx];
   e->stage_idx ^= 1;

@@ -72,6 +72,19 @@ struct TcWork {
   int32_t* counters;      // [max_units] arrival counters (zero between launches)
   long long max_units;
 };
+// Pre-tiled weights: tile (t, kb) -- 256 output features x 64 k -- is one
+// contiguous 32 KB run at byte offset (t * KB + kb) * kWTileBytes.
+constexpr int kWTileBytes = 256 * 64 * 2;
+
+// L2 prefetch of an upcoming tcgen05 GEMM's weights: the first P k-blocks
+// of each of its T x S (feature tile, K split) work units, so that HBM keeps
+// streaming while a kernel boundary drains and the next kernel starts.  A
+// prefetch is only a hint to the cache; it never changes a result.
+struct PfSpec {
+  const uint8_t* w;          // the GEMM's pre-tiled weights; null: nothing
+  int32_t T, KB, S, P;
+};
+
 // A GEMM of the step: weights W [M][K] times activations (hi + lo) [n][lda].
 struct GemmOp {
   const uint16_t* W;
@@ -132,6 +145,7 @@ struct cbd_engine {
   std::vector<CUtensorMap> tmaps;     // per layer: qkv, o, gu, down; then lm_head; then activations
   cbd::TcWork tcw{};
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
+  size_t l2_prefetch = 48u << 20;     // bytes of the next GEMM's weights each kernel prefetches to L2
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   // optional per-launch timing (cbd_engine_profile)
@@ -219,13 +233,19 @@ struct EpiArgs {
 };
 cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
                         int n, const EpiArgs& ep, cudaStream_t s);
-cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const TcWork& w, int sm_count,
-                           cudaStream_t s);
+cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s);
+// The tcgen05 GEMM's work split for M x K weights and n rows: feature tiles,
+// row tiles, k-blocks and the cluster (K split) size.
+void gemm_tc_plan(int M, int K, int n, int* T, int* NR, int* KB, int* S);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
                     uint32_t box_rows);
-cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& epi, cudaStream_t s);
+cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& epi, const PfSpec& pf,
+                        cudaStream_t s);
+// The L2 prefetch a kernel issues for the GEMM `op` that follows it on n rows
+// (nothing when that GEMM takes the CUDA-core path or prefetch is off).
+PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                             cudaStream_t s);
+                             const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
                            const SampDev* samp, int32_t* out_tokens, cudaStream_t s);
 #endif

@@ -42,6 +42,53 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Timeline tracing, compiled in only with -DCBD_TRACE (a separate debug
+// build of the library): thread 0 of every CTA records %globaltimer at the
+// CTA's start, after its dependency wait (TR_MARK1), at one kernel-specific
+// milestone (TR_MARK2) and at its end, with the kernel kind and the SM.
+// Each translation unit has its own trace pointer, bound from the host by
+// its exported cbd_trace_bind_<unit>(buffer) (5 x u64 per record, at most
+// 2^20 records; buffer = null turns tracing off).
+#ifdef CBD_TRACE
+static __device__ unsigned long long* g_trace = nullptr;
+static __device__ unsigned int g_trace_n = 0;
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_put(unsigned kind, unsigned long long t0, unsigned long long t1,
+                                          unsigned long long t2, unsigned long long t3) {
+  if (!g_trace) return;
+  const unsigned i = atomicAdd(&g_trace_n, 1u);
+  if (i >= (1u << 20)) return;
+  unsigned sm;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+  unsigned long long* p = g_trace + (size_t)i * 5;
+  p[0] = ((unsigned long long)kind << 32) | ((unsigned long long)sm << 24) | (blockIdx.x + blockIdx.y * gridDim.x);
+  p[1] = t0; p[2] = t1; p[3] = t2; p[4] = t3;
+}
+#define TR_DECL unsigned long long _tr0 = gtimer(), _tr1 = 0, _tr2 = 0
+#define TR_MARK1 (_tr1 = gtimer())
+#define TR_MARK2 (_tr2 = gtimer())
+#define TR_END(kind) do { if (threadIdx.x == 0) trace_put((kind), _tr0, _tr1, _tr2, gtimer()); } while (0)
+#define CBD_TRACE_BIND(unit)                                                             \
+  extern "C" int cbd_trace_bind_##unit(void* buf) {                                      \
+    unsigned long long* p = static_cast<unsigned long long*>(buf);                       \
+    unsigned int z = 0;                                                                  \
+    if (cudaMemcpyToSymbol(g_trace, &p, sizeof p) != cudaSuccess) return -1;             \
+    return cudaMemcpyToSymbol(g_trace_n, &z, sizeof z) == cudaSuccess ? 0 : -1;          \
+  }
+#else
+#define TR_DECL
+#define TR_MARK1
+#define TR_MARK2
+#define TR_END(kind)
+#define CBD_TRACE_BIND(unit)
+#endif
+// kinds: 1 embed, 2 rmsnorm, 3 attention stream, 4 attention merge,
+// 5 sampler, 6 GEMV, (16 << 12) | M/256 tcgen05 GEMM
+
 __device__ __forceinline__ void set_err(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }

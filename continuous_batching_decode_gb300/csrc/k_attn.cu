@@ -390,8 +390,9 @@ __host__ __device__ constexpr int attn_stream_smem() {
 template <int HD, int G>
 __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
     const uint16_t* __restrict__ pool, const float* __restrict__ q, const RowDev* __restrict__ rows,
-    const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, int n_tasks, int layer, int n_blocks,
-    int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
+    const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, const int32_t* __restrict__ row_work,
+    int n_tasks, int layer, int n_blocks, int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml,
+    uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo, const PfSpec pf, int32_t* err) {
   static_assert(G >= 1 && G <= 8, "a KV group must fit the MMA's N = 8");
   constexpr int TILE = 32 * HD * 2;
   constexpr int KS = HD / 16;
@@ -399,6 +400,7 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
   extern __shared__ uint8_t sm_raw[];
   __shared__ __align__(8) uint64_t bar[kAttnWarps][ST];
   __shared__ int abort_flag;
+  TR_DECL;
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid4 = lane & 3;
@@ -413,7 +415,6 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
     tc::fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();
   const int hq = hkv * G;
   const int gw = blockIdx.x * kAttnWarps + warp, nwarps = gridDim.x * kAttnWarps;
   struct Task {
@@ -436,8 +437,15 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
   int p_task = gw, p_blk = 0;
   Task pt = p_task < n_tasks ? task_of(p_task) : Task{};
   uint32_t p_q = 0;
+  bool pf_sent = false;
   auto issue_next = [&]() {
-    if (p_task >= n_tasks) return;
+    if (p_task >= n_tasks) {
+      // this warp has issued its last K/V load: pull its share of the next
+      // GEMM's weights into L2 while the remaining blocks and other warps drain
+      if (!pf_sent && lane == 0) tc::pf_issue(pf, gw, nwarps);
+      pf_sent = true;
+      return;
+    }
     const int s = p_q % ST;
     if (lane == 0) {
       int blk = tables[(size_t)pt.slot * mbps + (pt.start >> 5) + p_blk];
@@ -453,6 +461,8 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       if (p_task < n_tasks) pt = task_of(p_task);
     }
   };
+  pdl_wait();
+  TR_MARK1;
   for (int i = 0; i < ST; ++i) issue_next();
 
   const float scale = 1.0f / sqrtf((float)HD);
@@ -590,6 +600,26 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       issue_next();          // refill it with the block ST ahead
     }
     if (!alive) break;
+    const int w0 = row_work[tk.row], nch = row_work[tk.row + 1] - w0;
+    if (nch == 1) {
+      // the row's only chunk: normalise and write the output directly (the
+      // merge kernel skips such rows; o * e^0 / (l * e^0) is the same value)
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int head = tid4 * 2 + (c & 1);
+          if (head < G) {
+            const int dim = dt * 16 + gid + (c >= 2 ? 8 : 0);
+            uint16_t hi, lo;
+            split_bf16(o[dt][c] / l[c & 1], hi, lo);
+            const size_t oi = ((size_t)tk.row * hq + tk.kvh * G + head) * HD + dim;
+            out_hi[oi] = hi;
+            out_lo[oi] = lo;
+          }
+        }
+      continue;
+    }
     // the chunk's partial for the group's heads
 #pragma unroll
     for (int dt = 0; dt < KS; ++dt)
@@ -613,6 +643,7 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       }
     }
   }
+  TR_MARK2;
   // wind-down after a failed wait: let issued loads land before exiting
   if (!alive) {
     for (uint32_t r = c_q; r < p_q; ++r) {
@@ -620,36 +651,77 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       tc::mbar_wait(&bar[warp][r % ST], (r / ST) & 1, nullptr, &no_abort);
     }
   }
+#ifdef CBD_TRACE
+  __syncthreads();
+#endif
+  TR_END(3);
 }
 
-// Merge a row's chunks for one head (chunk order), normalise, split.
-template <int HD>
+// Merge the chunk partials of one (row, KV head) for the group's G heads,
+// in chunk order: M = max of the chunk maxima, L = sum_c l_c e^(m_c - M),
+// O = sum_c o_c e^(m_c - M), output O / L as hi + lo bf16.  One CTA of
+// G * HD / 4 threads per (row, KV head), each thread owning 4 dims of one
+// head.  The (max, sum) pairs of all chunks are staged in shared memory in
+// one pass; the partial outputs are independent loads, issued 8 chunks at
+// a time.  Rows with a single chunk were finished by the attention kernel.
+template <int HD, int G>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                    const int32_t* __restrict__ row_work, int hq,
+                                    const int32_t* __restrict__ row_work, int hq, int skip_single,
                                     uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo) {
+  extern __shared__ float2 sml[];          // [nch][G] (max, sum)
+  TR_DECL;
   pdl_trigger();
+  const int r = blockIdx.x, kvh = blockIdx.y;
+  const int w0 = row_work[r], nch = row_work[r + 1] - w0;
+  if (skip_single && nch == 1) return;
   pdl_wait();
-  const int r = blockIdx.x, h = blockIdx.y, dd = threadIdx.x;
-  const int w0 = row_work[r], w1 = row_work[r + 1];
-  float M = -INFINITY;
-  for (int w = w0; w < w1; ++w) M = fmaxf(M, part_ml[((size_t)w * hq + h) * 2]);
-  float L = 0.f, O = 0.f;
-  for (int w = w0; w < w1; ++w) {
-    const size_t i = (size_t)w * hq + h;
-    const float c = expf(part_ml[i * 2] - M);
-    L += part_ml[i * 2 + 1] * c;
-    O += part_o[i * HD + dd] * c;
+  TR_MARK1;
+  for (int i = threadIdx.x; i < nch * G; i += blockDim.x) {
+    const int c = i / G, g = i - c * G;
+    sml[i] = reinterpret_cast<const float2*>(part_ml)[(size_t)(w0 + c) * hq + kvh * G + g];
   }
-  uint16_t hi, lo;
-  split_bf16(O / L, hi, lo);
-  const size_t o = ((size_t)r * hq + h) * HD + dd;
-  out_hi[o] = hi;
-  out_lo[o] = lo;
+  __syncthreads();
+  constexpr int Q = HD / 4;                // float4s per head
+  const int g = threadIdx.x / Q, d4 = threadIdx.x - g * Q;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, sml[c * G + g].x);
+  float L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* po = reinterpret_cast<const float4*>(part_o) + ((size_t)w0 * hq + kvh * G + g) * Q + d4;
+  const size_t cstride = (size_t)hq * Q;   // float4s between consecutive chunks
+  int c = 0;
+  for (; c + 8 <= nch; c += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = po[(size_t)(c + j) * cstride];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 ml = sml[(c + j) * G + g];
+      const float sc = expf(ml.x - M);
+      L += ml.y * sc;
+      O.x += v[j].x * sc; O.y += v[j].y * sc; O.z += v[j].z * sc; O.w += v[j].w * sc;
+    }
+  }
+  for (; c < nch; ++c) {
+    const float4 v = po[(size_t)c * cstride];
+    const float2 ml = sml[c * G + g];
+    const float sc = expf(ml.x - M);
+    L += ml.y * sc;
+    O.x += v.x * sc; O.y += v.y * sc; O.z += v.z * sc; O.w += v.w * sc;
+  }
+  const float o4[4] = {O.x / L, O.y / L, O.z / L, O.w / L};
+  uint16_t hi[4], lo[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) split_bf16(o4[j], hi[j], lo[j]);
+  const size_t oi = ((size_t)r * hq + kvh * G + g) * HD + d4 * 4;
+  *reinterpret_cast<uint2*>(out_hi + oi) = make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+  *reinterpret_cast<uint2*>(out_lo + oi) = make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+  TR_END(4);
 }
 
 template <int HD, int G>
 static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                                 cudaStream_t s) {
+                                 const PfSpec& pf, cudaStream_t s) {
   const Dims& dm = e->dm;
   if (e->attn_path == 0) {
     constexpr int smem = attn_stream_smem<HD>();
@@ -662,9 +734,9 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     const int n_tasks = b->n_work * dm.hkv;
     const int grid = std::min(e->sm_count, (n_tasks + kAttnWarps - 1) / kAttnWarps);
     cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(128), smem, s, (const uint16_t*)p->base,
-                                (const float*)e->q,
-                                (const RowDev*)b->rows, (const int32_t*)b->tables, (const AttnWork*)b->work, n_tasks,
-                                layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
+                                (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
+                                (const AttnWork*)b->work, (const int32_t*)b->row_work, n_tasks, layer, p->n_blocks,
+                                dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi, e->act_lo, pf, e->err);
     if (ce != cudaSuccess) return ce;
   } else if (e->attn_path == 2) {
     constexpr int smem = attn_mma_smem<HD>();
@@ -686,23 +758,33 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
                                 dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
     if (ce != cudaSuccess) return ce;
   }
-  return launch_pdl(attn_combine_kernel<HD>, dim3(b->n_rows, dm.hq), dim3(HD), 0, s, (const float*)e->attn_o,
-                    (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq, e->act_hi, e->act_lo);
+  // single-chunk rows: the streaming kernel wrote them; the others write partials only
+  const size_t csmem = (size_t)b->max_chunks * G * sizeof(float2);
+  if (csmem > 48 * 1024) {
+    cudaError_t ce = cudaFuncSetAttribute(attn_combine_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)csmem);
+    if (ce != cudaSuccess) return ce;
+  }
+  return launch_pdl(attn_combine_kernel<HD, G>, dim3(b->n_rows, dm.hkv), dim3(G * HD / 4), csmem, s,
+                    (const float*)e->attn_o, (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq,
+                    e->attn_path == 0 ? 1 : 0, e->act_hi, e->act_lo);
 }
 
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                             cudaStream_t s) {
+                             const PfSpec& pf, cudaStream_t s) {
   const int G = e->dm.hq / e->dm.hkv;
   const int HD = e->dm.hd;
-  if (HD == 64 && G == 1) return launch_attn_t<64, 1>(e, p, b, layer, s);
-  if (HD == 64 && G == 2) return launch_attn_t<64, 2>(e, p, b, layer, s);
-  if (HD == 64 && G == 4) return launch_attn_t<64, 4>(e, p, b, layer, s);
-  if (HD == 64 && G == 8) return launch_attn_t<64, 8>(e, p, b, layer, s);
-  if (HD == 128 && G == 1) return launch_attn_t<128, 1>(e, p, b, layer, s);
-  if (HD == 128 && G == 2) return launch_attn_t<128, 2>(e, p, b, layer, s);
-  if (HD == 128 && G == 4) return launch_attn_t<128, 4>(e, p, b, layer, s);
-  if (HD == 128 && G == 8) return launch_attn_t<128, 8>(e, p, b, layer, s);
+  if (HD == 64 && G == 1) return launch_attn_t<64, 1>(e, p, b, layer, pf, s);
+  if (HD == 64 && G == 2) return launch_attn_t<64, 2>(e, p, b, layer, pf, s);
+  if (HD == 64 && G == 4) return launch_attn_t<64, 4>(e, p, b, layer, pf, s);
+  if (HD == 64 && G == 8) return launch_attn_t<64, 8>(e, p, b, layer, pf, s);
+  if (HD == 128 && G == 1) return launch_attn_t<128, 1>(e, p, b, layer, pf, s);
+  if (HD == 128 && G == 2) return launch_attn_t<128, 2>(e, p, b, layer, pf, s);
+  if (HD == 128 && G == 4) return launch_attn_t<128, 4>(e, p, b, layer, pf, s);
+  if (HD == 128 && G == 8) return launch_attn_t<128, 8>(e, p, b, layer, pf, s);
   return cudaErrorInvalidValue;
 }
+
+CBD_TRACE_BIND(attn)
 
 }  // namespace cbd

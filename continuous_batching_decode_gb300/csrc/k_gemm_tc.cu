@@ -53,7 +53,6 @@ constexpr int kTcWBytes = kTcBN * kTcBK * 2;            // 32 KB
 constexpr int kTcABytes = 2 * kTcRows * kTcBK * 2;      // 16 KB (hi rows, then lo rows)
 constexpr int kTcStageBytes = kTcWBytes + kTcABytes;
 constexpr int kTcPStride = kTcBN + 4;                   // fp32 partial row stride (padded)
-constexpr int kTcLoStride = 32 + 4;
 constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024;
 constexpr int kTcMaxCluster = 8;
 
@@ -76,106 +75,175 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float2 ld_peer_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
-// Load 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  float a[16], b[16];
-  tc::tmem_ld16(taddr, a);
-  tc::tmem_ld16(taddr + 16, b);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) { v[i] = a[i]; v[16 + i] = b[i]; }
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
 }
 
-// Epilogue for NB (row, feature pair) items: features f, f+1 (f even) of
-// row `row` with values a, b.  Same arithmetic as epi_pair / epi_single;
-// all global reads of the batch are issued before any is used.
-template <int NB>
-__device__ __forceinline__ void epi_pairs(const EpiArgs& ep, const int (&row)[NB], const int (&f)[NB],
-                                          const bool (&ok)[NB], const float (&a)[NB], const float (&b)[NB]) {
-  if (ep.kind == kEpiLogits) {
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (ok[j]) *reinterpret_cast<float2*>(ep.out_f32 + (size_t)row[j] * ep.ld + f[j]) = make_float2(a[j], b[j]);
-    return;
-  }
-  if (ep.kind == kEpiResid) {
-    float2 x[NB];
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (ok[j]) x[j] = *reinterpret_cast<const float2*>(ep.out_f32 + (size_t)row[j] * ep.ld + f[j]);
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (ok[j])
-        *reinterpret_cast<float2*>(ep.out_f32 + (size_t)row[j] * ep.ld + f[j]) = make_float2(x[j].x + a[j], x[j].y + b[j]);
-    return;
-  }
-  if (ep.kind == kEpiSwiGLU) {
-#pragma unroll
-    for (int j = 0; j < NB; ++j)
-      if (ok[j]) epi_pair(ep, f[j], row[j], a[j], b[j]);
-    return;
-  }
-  // QKV: row records, then RoPE factors and block ids, then compute + store
-  const int hd = ep.hd, half = hd >> 1, nq = ep.hq * hd, nk = ep.hkv * hd;
-  int pos[NB], slot[NB];
-#pragma unroll
-  for (int j = 0; j < NB; ++j)
-    if (ok[j]) {
-      const RowDev rw = ep.rows[row[j]];
-      pos[j] = rw.pos;
-      slot[j] = rw.slot;
+// Address of the epilogue operand that comes from global memory: the
+// residual x (residual epilogue) or the RoPE factors (cos, sin) of the
+// quad's two rotation pairs (QKV q / k features); null if none.
+template <int KIND>
+__device__ __forceinline__ const float* epi_pre_addr(const EpiArgs& ep, int row, int fg, const int2* rinfo, int ri) {
+  if constexpr (KIND == kEpiResid) return ep.out_f32 + (size_t)row * ep.ld + fg;
+  if constexpr (KIND == kEpiQKV) {
+    const int hd = ep.hd, nq = ep.hq * hd, nk = ep.hkv * hd;
+    if (fg < nq + nk) {
+      const int i = ((fg < nq ? fg : fg - nq) % hd) >> 1;
+      return ep.rope_cs + ((size_t)rinfo[ri].x * (hd >> 1) + i) * 2;
     }
-  int blk[NB];
-  float2 cs[NB];
-#pragma unroll
-  for (int j = 0; j < NB; ++j)
-    if (ok[j]) {
-      if (f[j] >= nq) blk[j] = ep.tables[(size_t)slot[j] * ep.max_blocks_per_seq + (pos[j] >> 5)];
-      if (f[j] < nq + nk) {
-        const int i = ((f[j] < nq ? f[j] : f[j] - nq) % hd) >> 1;
-        cs[j] = reinterpret_cast<const float2*>(ep.rope_cs)[(size_t)pos[j] * half + i];
+  }
+  return nullptr;
+}
+template <int KIND>
+__device__ __forceinline__ float4 epi_preload(const EpiArgs& ep, int row, int fg, const int2* rinfo, int ri) {
+  if constexpr (KIND == kEpiResid || KIND == kEpiQKV) {
+    const float* p = epi_pre_addr<KIND>(ep, row, fg, rinfo, ri);
+    if (p) return *reinterpret_cast<const float4*>(p);
+  }
+  return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Epilogue for one (row, feature quad): features fg..fg+3 (fg % 4 == 0) of
+// row `row` with values v.  Per element the arithmetic is that of
+// epi_pair / epi_single (the GEMV path's epilogue); stores are 8-16 bytes.
+//   QKV: (fg, fg+1) and (fg+2, fg+3) are RoPE partners (dims i, i + hd/2
+//        and i+1, i+1 + hd/2 of one q or k head) or four v dims.
+//   SwiGLU: (fg, fg+1) = (gate, up) of output fg/2, (fg+2, fg+3) of fg/2+1.
+template <int KIND>
+__device__ __forceinline__ void epi_quad(const EpiArgs& ep, int row, int fg, float4 v, float4 pre,
+                                         const int2* rinfo, int ri) {
+  if constexpr (KIND == kEpiLogits) {
+    *reinterpret_cast<float4*>(ep.out_f32 + (size_t)row * ep.ld + fg) = v;
+  } else if constexpr (KIND == kEpiResid) {
+    *reinterpret_cast<float4*>(ep.out_f32 + (size_t)row * ep.ld + fg) =
+        make_float4(pre.x + v.x, pre.y + v.y, pre.z + v.z, pre.w + v.w);
+  } else if constexpr (KIND == kEpiSwiGLU) {
+    const float y0 = (v.x / (1.0f + expf(-v.x))) * v.y;
+    const float y1 = (v.z / (1.0f + expf(-v.z))) * v.w;
+    uint16_t h0, l0, h1, l1;
+    split_bf16(y0, h0, l0);
+    split_bf16(y1, h1, l1);
+    const size_t o = (size_t)row * ep.ld_act + (fg >> 1);
+    *reinterpret_cast<uint32_t*>(ep.out_hi + o) = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    *reinterpret_cast<uint32_t*>(ep.out_lo + o) = (uint32_t)l0 | ((uint32_t)l1 << 16);
+  } else {
+    const int hd = ep.hd, half = hd >> 1, nq = ep.hq * hd, nk = ep.hkv * hd;
+    const int pos = rinfo[ri].x;
+    if (fg < nq + nk) {
+      const float r0 = v.x * pre.x - v.y * pre.y, r1 = v.y * pre.x + v.x * pre.y;   // dims i, i + half
+      const float r2 = v.z * pre.z - v.w * pre.w, r3 = v.w * pre.z + v.z * pre.w;   // dims i + 1, i + 1 + half
+      const int fh = fg < nq ? fg : fg - nq;
+      const int head = fh / hd, i = (fh % hd) >> 1;
+      if (fg < nq) {
+        float* qrow = ep.out_f32 + (size_t)row * nq + head * hd;
+        *reinterpret_cast<float2*>(qrow + i) = make_float2(r0, r2);
+        *reinterpret_cast<float2*>(qrow + i + half) = make_float2(r1, r3);
+        return;
       }
+      const int blk = rinfo[ri].y;
+      if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+      const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 0, hd);
+      *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i)) = pack_bf16x2(r0, r2);
+      *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i + half)) = pack_bf16x2(r1, r3);
+      return;
     }
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-    if (!ok[j]) continue;
-    const int fj = f[j];
-    if (fj < nq) {
-      const int head = fj / hd, i = (fj % hd) >> 1;
-      float* qrow = ep.out_f32 + (size_t)row[j] * nq + head * hd;
-      qrow[i] = a[j] * cs[j].x - b[j] * cs[j].y;
-      qrow[i + half] = b[j] * cs[j].x + a[j] * cs[j].y;
-      continue;
-    }
-    if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
-    if (fj < nq + nk) {
-      const int head = (fj - nq) / hd, i = ((fj - nq) % hd) >> 1;
-      const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk[j], ep.hkv, head, 0, hd);
-      ep.pool[t0 + tile_elem(pos[j] & 31, i)] = f32_to_bf16(a[j] * cs[j].x - b[j] * cs[j].y);
-      ep.pool[t0 + tile_elem(pos[j] & 31, i + half)] = f32_to_bf16(b[j] * cs[j].x + a[j] * cs[j].y);
+    const int blk = rinfo[ri].y;
+    if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+    const int fv = fg - nq - nk, head = fv / hd, jd = fv % hd;
+    const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk, ep.hkv, head, hd, pos & 31, jd);
+    *reinterpret_cast<uint2*>(ep.pool + o) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+// Epilogue phase 2 for one epilogue kind (128 threads, et = 0..127).  CTA
+// rank r of the cluster finalises feature quads [r*64/S, (r+1)*64/S) of the
+// tile for every row: the S partials are read (over distributed shared
+// memory when S > 1) and summed in rank order, then the epilogue runs.
+// Item it = (row it / nq, quad it % nq) belongs to thread it % 128.
+template <int KIND>
+__device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
+                                           uint32_t Pbase, const int2* rinfo) {
+  const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
+  const int nq = q1 - q0;
+  const int items = rows_here * nq;
+  // Rolled loops: this code runs once per CTA, so its size (instruction
+  // fetch while HBM is saturated) costs more than per-item latency.
+#pragma unroll 1
+  for (int it = et; it < items; it += 128) {
+    const int i = it / nq;
+    const int f = 4 * (q0 + it - i * nq);      // feature within the tile
+    const uint32_t off = (uint32_t)(i * kTcPStride + f) * 4u;
+    const int fg = t * kTcBN + f;
+    const float4 pre = epi_preload<KIND>(ep, nr * kTcRows + i, fg, rinfo, i);
+    float4 acc;
+    if (S == 1) {
+      acc = ld_shared_f4(Pbase + off);
     } else {
-      const int fv = fj - nq - nk, head = fv / hd, jd = fv % hd;
-      const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk[j], ep.hkv, head, hd, pos[j] & 31, jd);
-      ep.pool[o] = f32_to_bf16(a[j]);
-      ep.pool[o + 1] = f32_to_bf16(b[j]);
+      float4 pv[kTcMaxCluster];
+#pragma unroll
+      for (int qr = 0; qr < kTcMaxCluster; ++qr)
+        if (qr < S) pv[qr] = ld_peer_f4(map_peer(Pbase + off, (uint32_t)qr));
+      acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int qr = 0; qr < kTcMaxCluster; ++qr)
+        if (qr < S) {
+          acc.x += pv[qr].x; acc.y += pv[qr].y;
+          acc.z += pv[qr].z; acc.w += pv[qr].w;
+        }
+    }
+    epi_quad<KIND>(ep, nr * kTcRows + i, fg, acc, pre, rinfo, i);
+  }
+}
+
+// While the mainloop runs: pull each epilogue thread's global operands
+// (residual x, RoPE factors) into L1 so phase 2 does not wait on memory
+// round trips that are long while HBM is saturated.
+template <int KIND>
+__device__ __forceinline__ void epi_prefetch(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
+                                             const int2* rinfo) {
+  if constexpr (KIND == kEpiResid || KIND == kEpiQKV) {
+    const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
+    const int nq = q1 - q0;
+    const int items = rows_here * nq;
+    for (int it = et; it < items; it += 128) {
+      const int i = it / nq;
+      const float* p = epi_pre_addr<KIND>(ep, nr * kTcRows + i, t * kTcBN + 4 * (q0 + it - i * nq), rinfo, i);
+      if (p) asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
     }
   }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-                   const __grid_constant__ CUtensorMap tmL, const TcArgs a, const EpiArgs ep) {
+                   const __grid_constant__ CUtensorMap tmL, const TcArgs a, const EpiArgs ep, const PfSpec pf) {
   constexpr uint32_t kIdesc = tc::idesc_bf16(2 * kTcRows, kTcBN);
+  TR_DECL;
+#ifdef CBD_TRACE
+  unsigned long long _e0 = 0, _e1 = 0;    // epilogue: accumulator ready, hi + lo folded
+#endif
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kTcStages], empty_bar[kTcStages];
   __shared__ __align__(8) uint64_t accum_full, mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int decision;
+  __shared__ int2 rinfo[kTcRows];           // QKV epilogue: (position, KV block) of each tile row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = tc::smem_u32(smem_raw);
@@ -215,18 +283,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
+      // activation rows are loaded in 16-row boxes, only as many as the
+      // tile has rows; the MMA rows past them read stale shared memory and
+      // land in TMEM lanes the epilogue never reads
+      const int nbox = (min(kTcRows, a.n - nr * kTcRows) + 15) / 16;
+      const uint32_t stage_tx = kTcWBytes + 2u * nbox * 2048u;
       auto issue_w = [&](int q) {
         const int s = q % kTcStages;
         uint8_t* st = ring + (size_t)s * kTcStageBytes;
-        tc::mbar_arrive_expect_tx(&full_bar[s], kTcStageBytes);
+        tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
         tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb0 + q) * kTcBN, &full_bar[s]);
       };
       auto issue_a = [&](int q) {
         const int s = q % kTcStages;
         uint8_t* st = ring + (size_t)s * kTcStageBytes + kTcWBytes;
         const int kx = (kb0 + q) * kTcBK;
-#pragma unroll
-        for (int j = 0; j < kTcRows / 16; ++j) {
+        for (int j = 0; j < nbox; ++j) {
           tc::tma_load_2d(st + j * 2048, &tmH, kx, nr * kTcRows + j * 16, &full_bar[s]);
           tc::tma_load_2d(st + kTcABytes / 2 + j * 2048, &tmL, kx, nr * kTcRows + j * 16, &full_bar[s]);
         }
@@ -236,6 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int npre = n_it < kTcStages ? n_it : kTcStages;
       for (int q = 0; q < npre; ++q) issue_w(q);
       pdl_wait();
+      TR_MARK1;
       for (int q = 0; q < npre; ++q) issue_a(q);
       int q = npre;
       bool ok = true;
@@ -245,6 +318,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         issue_w(q);
         issue_a(q);
       }
+      // this CTA's stream is fully issued: start pulling the next GEMM's
+      // first k-blocks into L2 while the last stages, the epilogue and the
+      // kernel boundary drain
+      TR_MARK2;
+      if (ok) tc::pf_issue(pf, blockIdx.x, gridDim.x);
       if (!ok) {     // every load issued must land before the CTA exits
         for (int r = q > kTcStages ? q - kTcStages : 0; r < q; ++r) {
           int no_abort = 0;
@@ -276,97 +354,113 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue phase 1: fold hi + lo into the partial
-    const int lg = warp & 3;                       // TMEM lane group: rows 32*lg..+31
-    const int r = lg * 32 + lane;                  // row of the hi|lo tile
+    // TMEM lane group lg = warp % 4 holds tile rows 32 * (lg % 2) + lane,
+    // hi halves for lg < 2 and lo halves for lg >= 2.  The lo warps copy
+    // their lanes to shared memory, then the hi warps add them to their own
+    // (hi + lo per element) and write the partial P; warps whose lanes hold
+    // no row of this tile skip their loads.
+    const int lg = warp & 3;
+    const int rows_here = min(kTcRows, a.n - nr * kTcRows);
+    const int rl = (lg & 1) * 32 + lane;           // tile row of this lane
+    const bool has_rows = (lg & 1) * 32 < rows_here;
     const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16);
-    float* P = reinterpret_cast<float*>(ring);                                // [64][kTcPStride]
-    float* LO = reinterpret_cast<float*>(ring + 64 * kTcPStride * 4);          // [64][kTcLoStride]
+    float* P = reinterpret_cast<float*>(ring);                         // [64][kTcPStride] hi + lo
+    float* LO = reinterpret_cast<float*>(ring + 64 * kTcPStride * 4);   // [64][kTcPStride] lo
+    const int et = threadIdx.x - 64;
+    if (ep.kind == kEpiQKV) {
+      // the rows' positions and KV blocks, read while the mainloop runs
+      for (int i = et; i < rows_here; i += 128) {
+        const RowDev rw = ep.rows[nr * kTcRows + i];
+        rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      epi_prefetch<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, rinfo);
+    } else if (ep.kind == kEpiResid) {
+      epi_prefetch<kEpiResid>(ep, S, rank, t, nr, rows_here, et, rinfo);
+    }
     if (n_it > 0) tc::mbar_wait(&accum_full, 0, a.err, abort_p);
+#ifdef CBD_TRACE
+    _e0 = gtimer();
+#endif
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (threadIdx.x == 64) decision = *abort_p || n_it == 0;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const bool skip = decision != 0;
     tc::tc_fence_after();
+    auto load64 = [&](int c0, float (&v)[64]) {
+      if (skip) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) v[j] = 0.f;
+        return;
+      }
+      uint32_t x0[32], x1[32];
+      tc::tmem_ld32_nowait(taddr + c0, x0);
+      tc::tmem_ld32_nowait(taddr + c0 + 32, x1);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) { v[j] = __uint_as_float(x0[j]); v[32 + j] = __uint_as_float(x1[j]); }
+    };
+    if (lg >= 2 && has_rows) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < kTcBN; c0 += 32) {
-      float v[32];
-      if (!skip) {
-        tmem_ld32(taddr + c0, v);
-      } else {
+      for (int c0 = 0; c0 < kTcBN; c0 += 64) {
+        float v[64];
+        load64(c0, v);
+        float4* lo = reinterpret_cast<float4*>(LO + rl * kTcPStride + c0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        for (int j = 0; j < 16; ++j) lo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
-      if (r >= 64) {
-        float4* lo = reinterpret_cast<float4*>(LO + (r - 64) * kTcLoStride);
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (lg < 2 && has_rows) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < kTcBN; c0 += 64) {
+        float v[64];
+        load64(c0, v);
+        const float4* lo = reinterpret_cast<const float4*>(LO + rl * kTcPStride + c0);
+        float4* p = reinterpret_cast<float4*>(P + rl * kTcPStride + c0);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) lo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (r < 64) {
-        const float4* lo = reinterpret_cast<const float4*>(LO + r * kTcLoStride);
-        float4* p = reinterpret_cast<float4*>(P + r * kTcPStride + c0);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           const float4 l4 = lo[j];
           p[j] = make_float4(v[4 * j] + l4.x, v[4 * j + 1] + l4.y, v[4 * j + 2] + l4.z, v[4 * j + 3] + l4.w);
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
     }
+#ifdef CBD_TRACE
+    _e1 = gtimer();
+#endif
     tc::tc_fence_before();
   }
   // ------------------------------------------------ cluster: every partial is in shared memory
   __syncwarp();
   if (S > 1) cluster_sync_all();
   else __syncthreads();
+#ifdef CBD_TRACE
+  const unsigned long long _e_sync = gtimer();
+#endif
   if (warp >= 2) {
     // ------------------------------------------------ epilogue phase 2: reduce over ranks, finish
-    const int et = threadIdx.x - 64;                            // 0..127
-    const int p0 = rank * (kTcBN / 2) / S, p1 = (rank + 1) * (kTcBN / 2) / S;   // feature pairs
-    const int np = p1 - p0;
+    const int et = threadIdx.x - 64;
     const int rows_here = min(kTcRows, a.n - nr * kTcRows);
-    const int items = rows_here * np;
     const uint32_t Pbase = tc::smem_u32(ring);
-    constexpr int NB = 4;
-#pragma unroll 1
-    for (int i0 = et; i0 < items; i0 += 128 * NB) {
-      int row[NB], f[NB];
-      bool ok[NB];
-      float va[NB], vb[NB];
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        const int it = i0 + j * 128;
-        ok[j] = it < items;
-        const int i = ok[j] ? it / np : 0, pp = ok[j] ? it - (it / np) * np : 0;
-        row[j] = nr * kTcRows + i;
-        f[j] = 2 * (p0 + pp);                    // feature within the tile
-        va[j] = 0.f;
-        vb[j] = 0.f;
-      }
-#pragma unroll 1
-      for (int qr = 0; qr < S; ++qr) {
-        float2 pv[NB];
-#pragma unroll
-        for (int j = 0; j < NB; ++j) {
-          if (!ok[j]) continue;
-          const uint32_t off = (uint32_t)((row[j] - nr * kTcRows) * kTcPStride + f[j]) * 4u;
-          pv[j] = S > 1 ? ld_peer_f2(map_peer(Pbase + off, (uint32_t)qr))
-                        : *reinterpret_cast<const float2*>(ring + off);
-        }
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-          if (ok[j]) { va[j] += pv[j].x; vb[j] += pv[j].y; }
-      }
-#pragma unroll
-      for (int j = 0; j < NB; ++j) f[j] += t * kTcBN;
-      epi_pairs<NB>(ep, row, f, ok, va, vb);
+    switch (ep.kind) {
+      case kEpiQKV: epi_phase2<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
+      case kEpiResid: epi_phase2<kEpiResid>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
+      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
+      default: epi_phase2<kEpiLogits>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
     }
   }
+#ifdef CBD_TRACE
+  if (threadIdx.x == 64) {
+    const unsigned long long te = gtimer();
+    trace_put((17u << 12) | (unsigned)(a.M >> 8), _e0, _e1, _e_sync, te);
+  }
+#endif
   // peers keep their partials alive until every rank has read them
   __syncwarp();
   if (S > 1) cluster_sync_all();
   tc::tc_fence_before();
   __syncthreads();
+  TR_END((16u << 12) | (unsigned)(a.M >> 8));
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTcBN);
@@ -446,18 +540,21 @@ static int choose_cluster(long long U, int KB) {
   return best;
 }
 
-cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const TcWork& w, int sm_count,
-                           cudaStream_t s) {
-  (void)w;
-  (void)sm_count;
+void gemm_tc_plan(int M, int K, int n, int* T, int* NR, int* KB, int* S) {
+  *T = M / kTcBN;
+  *NR = (n + kTcRows - 1) / kTcRows;
+  *KB = K / kTcBK;
+  *S = choose_cluster((long long)*T * *NR, *KB);
+}
+
+cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   if (g.M % kTcBN || g.K % kTcBK) return cudaErrorInvalidValue;
   TcArgs a{};
   a.M = g.M; a.K = g.K; a.n = n;
-  a.T = g.M / kTcBN; a.NR = (n + kTcRows - 1) / kTcRows; a.KB = g.K / kTcBK;
+  gemm_tc_plan(g.M, g.K, n, &a.T, &a.NR, &a.KB, &a.S);
   a.err = ep.err;
   const long long U = (long long)a.T * a.NR;
-  a.S = choose_cluster(U, a.KB);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(U * a.S));
   cfg.blockDim = dim3(kTcThreads);
@@ -477,7 +574,9 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const TcWo
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *g.w, *g.hi, *g.lo, a, ep);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *g.w, *g.hi, *g.lo, a, ep, pf);
 }
+
+CBD_TRACE_BIND(gemm_tc)
 
 }  // namespace cbd

@@ -121,11 +121,30 @@ cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, c
 
 // Path choice: the CUDA-core GEMV for a handful of rows, the tcgen05 GEMM
 // above that (or as forced by cbd_engine_set_gemm_path).
-cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& ep, cudaStream_t s) {
+static bool uses_tc(const cbd_engine* e, int n) {
+  return e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
+}
+
+cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& ep, const PfSpec& pf,
+                        cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  const bool tc = e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
-  if (tc) return launch_gemm_tc(op.tc, n, ep, e->tcw, e->sm_count, s);
+  if (uses_tc(e, n)) return launch_gemm_tc(op.tc, n, ep, pf, s);
   return launch_gemv(op.W, op.M, op.K, op.a_hi, op.a_lo, op.lda, n, ep, s);
+}
+
+PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n) {
+  PfSpec pf{};
+  if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n)) return pf;
+  int T, NR, KB, S;
+  gemm_tc_plan(op.tc.M, op.tc.K, n, &T, &NR, &KB, &S);
+  const long long units = (long long)T * S;
+  const long long per_unit = (KB + S - 1) / S;
+  long long P = (long long)(e->l2_prefetch / kWTileBytes) / units;
+  if (P < 1) P = 1;
+  if (P > per_unit) P = per_unit;
+  pf.w = reinterpret_cast<const uint8_t*>(op.W);
+  pf.T = T; pf.KB = KB; pf.S = S; pf.P = (int32_t)P;
+  return pf;
 }
 
 }  // namespace cbd

@@ -9,12 +9,15 @@ namespace cbd {
 // embedding row of the row's token).
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
                              float* __restrict__ x) {
+  TR_DECL;
   pdl_trigger();
   pdl_wait();
+  TR_MARK1;
   const int r = blockIdx.x;
   const uint16_t* src = E + (size_t)rows[r].token * d;
   float* dst = x + (size_t)r * d;
   for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = bf16_to_f32(src[i]);
+  TR_END(1);
 }
 
 cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s) {
@@ -31,8 +34,10 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
                                const int32_t* __restrict__ gather, int d, float eps,
                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
   __shared__ float red[32];
+  TR_DECL;
   pdl_trigger();
   pdl_wait();
+  TR_MARK1;
   const int r = blockIdx.x;
   const int src = gather ? gather[r] : r;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
@@ -66,6 +71,7 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
     h2[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
     l2[i] = make_uint2(q[0] | ((uint32_t)q[1] << 16), q[2] | ((uint32_t)q[3] << 16));
   }
+  TR_END(2);
 }
 
 cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
@@ -75,4 +81,8 @@ cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, 
   return launch_pdl(rmsnorm_kernel, dim3(n_rows), dim3(threads), 0, s, x, g, gather, e->dm.d, e->dm.eps, hi, lo);
 }
 
+}  // namespace cbd
+
+namespace cbd {
+CBD_TRACE_BIND(misc)
 }  // namespace cbd

@@ -77,6 +77,29 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// Issue share `part` of `nparts` of an upcoming GEMM's L2 prefetch (one
+// 32 KB weight tile per instruction, k-block-major so the first k-blocks of
+// every unit go first).  Called by one thread per part.
+__device__ __forceinline__ void pf_issue(const PfSpec& pf, int part, int nparts) {
+  if (!pf.w || pf.P <= 0) return;
+  const long long units = (long long)pf.T * pf.S;
+  const long long total = units * pf.P;
+  const long long c0 = total * part / nparts, c1 = total * (part + 1) / nparts;
+  for (long long c = c0; c < c1; ++c) {
+    const int j = (int)(c / units), u = (int)(c - (long long)j * units);
+    const int t = u / pf.S, r = u - t * pf.S;
+    const int kb0 = r * pf.KB / pf.S, kb1 = (r + 1) * pf.KB / pf.S;
+    if (kb0 + j >= kb1) continue;
+    prefetch_l2(pf.w + ((size_t)t * pf.KB + kb0 + j) * kWTileBytes, kWTileBytes);
+  }
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Allocate `ncols` (power of two >= 32) TMEM columns; one full warp calls.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -145,6 +168,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Load 32 consecutive fp32 columns of this thread's TMEM lane without
+// waiting; call tmem_wait_ld() before using the registers.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 }  // namespace tc
 }  // namespace cbd

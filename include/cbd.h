@@ -137,6 +137,16 @@ cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_ma
  * 128-position chunks and the same merge order. */
 cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path);
 
+/* L2 prefetch across kernel boundaries: once a kernel of the step has issued
+ * its last load, it asks L2 to fetch the first k-blocks of the next weight
+ * contraction's work units, up to `bytes` in all (default 48 MiB; 0 turns
+ * it off), so HBM keeps streaming while one launch drains and the next
+ * starts ("20.3 服务、批处理与流式", 20.3.2: a decode step costs
+ * (W + B*A)/beta, so every idle HBM cycle is lost throughput).  A prefetch
+ * is a cache hint only: results are identical with any setting.
+ * Errors: CBD_EINVAL for a NULL engine or more than 1 GiB. */
+cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes);
+
 /* Device pointer of the per-slot occurrence counters, [max_slots][V] fp32,
  * owned by the engine (for inspection and for seeding tests). */
 cbd_status cbd_engine_counters(cbd_engine* e, float** counters);
@@ -222,7 +232,8 @@ typedef struct cbd_sampling {
  *   sampling (host): one entry per row with sample != 0, in row order (m of them).
  *   uniforms (host, nullable): m values in [0,1) that replace the Philox draw.
  *   out_tokens (device): [m] int32 sampled token ids.
- *   out_logits (device, nullable): [m][V] fp32 raw logits (before penalty).
+ *   out_logits (device, nullable, 16-byte aligned): [m][V] fp32 raw logits
+ *     (before penalty).
  * Host-side validation (CBD_EINVAL, nothing enqueued): slot/token/pos ranges,
  * pos < n_blocks_per_slot[slot]*32 <= max_blocks_per_seq*32, physical block
  * ids inside the pool and not shared between slots used by the step, distinct

@@ -292,3 +292,39 @@ def test_gemm_paths_agree_on_long_prefill(tiny):
     kv = {0: om.SequenceKV(om_.cfg, 320)}
     zo = om.prefill(om_, kv, 0, prompt)
     gu.assert_logits_close(z, zo[None], "300-row prefill")
+
+
+def test_multi_chunk_rows_and_l2_prefetch(tiny):
+    """Rows whose context spans several 128-position attention chunks (so
+    the chunk partials are merged) match the oracle, and turning the L2
+    prefetch off leaves every logit bit-identical (a prefetch is a cache
+    hint only)."""
+    V = tiny.shape["vocab"]
+    rng = np.random.default_rng(31)
+    prompts = [list(rng.integers(0, V, 300)), list(rng.integers(0, V, 200))]
+    perm = list(rng.permutation(16))
+    tables = np.zeros((2, 16), np.int32)
+    tables[0, :10] = perm[:10]
+    tables[1, :6] = perm[10:16]
+    tables[1, 6] = 16
+    nbps = np.array([10, 7], np.int32)
+    pool = tiny.pool(18)
+    for s, p in enumerate(prompts):
+        gu.gpu_prefill(tiny, pool, s, p[:-1], tables, nbps)
+    rows = [(0, prompts[0][-1], 299, 0, 1), (1, prompts[1][-1], 199, 0, 1)]
+    g = [dict(temperature=0.0)] * 2
+    res = []
+    for nbytes in (48 << 20, 0, 1 << 20):
+        cbd.engine_set_l2_prefetch(tiny.e, nbytes)
+        _, z = gu.run_step(tiny, pool, rows, tables, nbps, g)
+        res.append(z)
+    cbd.engine_set_l2_prefetch(tiny.e, 48 << 20)
+    pool.close()
+    for z in res[1:]:
+        np.testing.assert_array_equal(z, res[0])
+    om_ = tiny.oracle()
+    zo = []
+    for s, p in enumerate(prompts):
+        kv = {s: om.SequenceKV(om_.cfg, 320)}
+        zo.append(om.prefill(om_, kv, s, p))
+    gu.assert_logits_close(res[0], np.array(zo), "multi-chunk rows")
