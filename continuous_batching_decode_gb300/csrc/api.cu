@@ -270,6 +270,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
+  const size_t o_anext = W.take((size_t)dm.L * 4);
 
   e->work_bytes = W.off;
   cudaError_t e3 = cudaMalloc(&e->work, e->work_bytes);
@@ -287,6 +288,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
   e->counters = reinterpret_cast<float*>(wb + o_cn);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
+  e->attn_next = reinterpret_cast<int32_t*>(wb + o_anext);
 
   e3 = cudaMemset(e->work, 0, e->work_bytes);
   // ---- staging for cbd_step / cbd_sample
@@ -593,7 +595,18 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
     rw[r] = wi;
     const int32_t nch = w.pos / kAttnChunk + 1;
     max_chunks = std::max(max_chunks, nch);
-    for (int32_t c = 0; c < nch; ++c) wk[wi++] = AttnWork{r, c * kAttnChunk};
+    for (int32_t c = 0; c < nch; ++c) {
+      AttnWork a{};
+      a.row = r;
+      a.start = c * kAttnChunk;
+      a.end = std::min(a.start + kAttnChunk, w.pos + 1);
+      a.wn = (wi << 16) | nch;
+      for (int32_t j = 0; j < kAttnChunk / kBlock; ++j) {
+        const int32_t p0 = a.start + j * kBlock;
+        a.blk[j] = p0 < a.end ? tables[(size_t)w.slot * mbps + p0 / kBlock] : -1;
+      }
+      wk[wi++] = a;
+    }
     if (w.sample) {
       const cbd_sampling& s = sp[j];
       sr[j] = r;
@@ -607,6 +620,11 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   }
   rw[n_rows] = wi;
   I.max_chunks = max_chunks;
+  // largest chunks first (ties in chunk order): dynamic scheduling then
+  // ends on the short last chunks of rows
+  std::stable_sort(wk, wk + wi, [](const AttnWork& x, const AttnWork& y) {
+    return (x.end - x.start) > (y.end - y.start);
+  });
   std::memcpy(B + I.off_tables, tables, (size_t)table_slots * mbps * 4);
   return CBD_OK;
 }

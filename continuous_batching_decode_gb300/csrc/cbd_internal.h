@@ -45,10 +45,18 @@ struct SampDev {
   float uniform;                     // >= 0: use it; < 0: draw with Philox
 };
 
-// One attention work item: a row and the first position of its chunk.
+// One attention work item: a row's chunk of positions [start, end) (at
+// most kAttnChunk), its index wi among the step's chunks (a row's chunks are
+// consecutive, chunk c at wi = first + c) and the row's chunk count packed
+// as wn = wi << 16 | nch, and the physical KV blocks of the chunk (-1 past
+// its end), resolved through the block table on the host.  The list is
+// stored largest chunk first, so dynamically scheduled warps finish on the
+// smallest ones.
 struct AttnWork {
-  int32_t row, start;
+  int32_t row, start, end, wn;
+  int32_t blk[kAttnChunk / kBlock];
 };
+static_assert(sizeof(AttnWork) == 32, "two 16-byte loads per record");
 
 struct LayerDev {
   const float* attn_norm;            // [d] fp32
@@ -127,6 +135,7 @@ struct cbd_engine {
   float* q = nullptr;                 // [max_rows][Hq*hd]
   float* attn_o = nullptr;            // [max_work][Hq][hd] partial outputs
   float* attn_ml = nullptr;           // [max_work][Hq][2] (max, sum)
+  int32_t* attn_next = nullptr;       // [L] attention task counters, zeroed at the start of each step
   int max_work = 0;
   float* logits = nullptr;            // [max_slots][V] internal logits
   float* samp_scratch = nullptr;      // [max_slots][V] sampler scratch

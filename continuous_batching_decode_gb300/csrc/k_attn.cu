@@ -47,9 +47,10 @@ __global__ void __launch_bounds__(128) attn_partial_kernel(
   __shared__ __align__(16) float wo[NW][G][HD];
   pdl_trigger();
   pdl_wait();
-  const int wi = blockIdx.x, kvh = blockIdx.y;
+  const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const AttnWork wk = work[wi];
+  const AttnWork wk = work[blockIdx.x];
+  const int wi = wk.wn >> 16;          // the chunk's index among the step's chunks
   const RowDev rw = rows[wk.row];
   const int hq = hkv * G;
   const int end = min(wk.start + kAttnChunk, rw.pos + 1);
@@ -366,78 +367,115 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const uint16_t* __restric
       L += mml[(w * 8 + g) * 2 + 1] * c;
       O += mo[(w * 8 + g) * HD + dd] * c;
     }
-    const size_t h = (size_t)blockIdx.x * hq + kvh * G + g;
+    const size_t h = (size_t)(wk.wn >> 16) * hq + kvh * G + g;
     part_o[h * HD + dd] = O;
     if (dd == 0) { part_ml[h * 2] = M; part_ml[h * 2 + 1] = L; }
   }
 }
 
 // ---------------------------------------------------------------- streaming
-// Persistent form of the tensor-core kernel: every warp owns the tasks
-// gw, gw + W, gw + 2W, ... (task = one 128-position chunk of one row for one
-// KV head; W = warps in the grid) and streams their 32-position K/V tiles
-// through a private ring of shared-memory stages filled by TMA, running
-// ahead across task boundaries.  Within a task the warp keeps an online
-// softmax over its blocks; at the task's end it writes the chunk's partial
-// (max, sum, unnormalised output).  No warp waits for another.
+// Persistent form of the tensor-core kernel: eight warps per CTA (two per
+// scheduler, so one warp's latencies overlap the other's work), each taking
+// tasks (task = one 128-position chunk of one row for one KV head) and
+// streaming their 32-position K and V tiles -- as separate 8 KB (hd 128)
+// copies, K then V -- through a private ring of NS shared-memory slots
+// filled by TMA, running ahead across task boundaries.  Within a task the
+// warp keeps an online softmax over its blocks; at the task's end it writes
+// the chunk's partial (max, sum, unnormalised output).  No warp waits for
+// another.
+constexpr int kStreamWarps = 8;
 template <int HD>
-__host__ __device__ constexpr int attn_stream_stages() { return HD == 128 ? 3 : 6; }
+__host__ __device__ constexpr int attn_stream_slots() { return HD == 128 ? 3 : 6; }
 template <int HD>
 __host__ __device__ constexpr int attn_stream_smem() {
-  return kAttnWarps * attn_stream_stages<HD>() * 2 * (32 * HD * 2) + kAttnWarps * 8 * 32 * 4 + 1024;
+  return kStreamWarps * attn_stream_slots<HD>() * (32 * HD * 2) + kStreamWarps * 8 * 32 * 4 + 1024;
 }
 
 template <int HD, int G>
-__global__ void __launch_bounds__(128, 1) attn_stream_kernel(
+__global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
     const uint16_t* __restrict__ pool, const float* __restrict__ q, const RowDev* __restrict__ rows,
     const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, const int32_t* __restrict__ row_work,
     int n_tasks, int layer, int n_blocks, int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml,
-    uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo, const PfSpec pf, int32_t* err) {
+    uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo, int32_t* __restrict__ next_task, const PfSpec pf,
+    int32_t* err) {
   static_assert(G >= 1 && G <= 8, "a KV group must fit the MMA's N = 8");
   constexpr int TILE = 32 * HD * 2;
   constexpr int KS = HD / 16;
-  constexpr int ST = attn_stream_stages<HD>();
+  constexpr int NS = attn_stream_slots<HD>();   // ring slots per warp, one K or V tile each
+  constexpr int QN = 8;                    // task queue entries per warp (>= NS + 1)
   extern __shared__ uint8_t sm_raw[];
-  __shared__ __align__(8) uint64_t bar[kAttnWarps][ST];
+  __shared__ __align__(8) uint64_t bar[kStreamWarps][NS];
   __shared__ int abort_flag;
+  // tasks whose blocks this warp's producer has started issuing:
+  // (row, start, end, kvh), (wi, task, -, -)
+  __shared__ __align__(16) int tq[kStreamWarps][QN][8];
   TR_DECL;
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tid4 = lane & 3;
   const uint32_t raw = tc::smem_u32(sm_raw);
   uint8_t* base = sm_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* ring = base + warp * ST * 2 * TILE;           // stage s: K at s*2*TILE, V after it
-  float* Pw = reinterpret_cast<float*>(base + kAttnWarps * ST * 2 * TILE) + warp * 8 * 32;
+  uint8_t* ring = base + warp * NS * TILE;               // slot s at s * TILE
+  float* Pw = reinterpret_cast<float*>(base + kStreamWarps * NS * TILE) + warp * 8 * 32;
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kAttnWarps; ++w)
-      for (int s = 0; s < ST; ++s) tc::mbar_init(&bar[w][s], 1);
+    for (int w = 0; w < kStreamWarps; ++w)
+      for (int s = 0; s < NS; ++s) tc::mbar_init(&bar[w][s], 1);
     abort_flag = 0;
     tc::fence_mbar_init();
   }
   __syncthreads();
   const int hq = hkv * G;
-  const int gw = blockIdx.x * kAttnWarps + warp, nwarps = gridDim.x * kAttnWarps;
-  struct Task {
-    int wi, kvh, row, start, end, slot, nb;
+  const int gw = blockIdx.x * kStreamWarps + warp, nwarps = gridDim.x * kStreamWarps;
+  // A task is one 128-position chunk (work item wi) for one KV head; its
+  // record (row, positions, physical blocks) was built on the host.
+  struct Rec {
+    int row, start, end, nch, kvh, wi, b0, b1, b2, b3;
   };
-  auto task_of = [&](int t) {
-    Task k;
-    k.wi = t / hkv;
-    k.kvh = t - k.wi * hkv;
-    const AttnWork wk = work[k.wi];
-    const RowDev rw = rows[wk.row];
-    k.row = wk.row;
-    k.start = wk.start;
-    k.end = min(wk.start + kAttnChunk, rw.pos + 1);
-    k.slot = rw.slot;
-    k.nb = (k.end - k.start + 31) >> 5;
-    return k;
+  auto load_rec = [&](int t) {
+    Rec r;
+    const int k = t / hkv;                 // position in the (size-ordered) work list
+    r.kvh = t - k * hkv;
+    const int4* w = reinterpret_cast<const int4*>(work + k);
+    const int4 h = w[0], bl = w[1];
+    r.row = h.x; r.start = h.y; r.end = h.z; r.nch = h.w & 0xffff;
+    r.wi = h.w >> 16;
+    r.b0 = bl.x; r.b1 = bl.y; r.b2 = bl.z; r.b3 = bl.w;
+    return r;
   };
-  // producer cursor (lane 0 issues; all lanes track it identically)
-  int p_task = gw, p_blk = 0;
-  Task pt = p_task < n_tasks ? task_of(p_task) : Task{};
+  auto shfl_rec = [&](const Rec& r) {
+    Rec o;
+    o.row = __shfl_sync(0xffffffffu, r.row, 0); o.start = __shfl_sync(0xffffffffu, r.start, 0);
+    o.end = __shfl_sync(0xffffffffu, r.end, 0); o.kvh = __shfl_sync(0xffffffffu, r.kvh, 0);
+    o.nch = __shfl_sync(0xffffffffu, r.nch, 0);
+    o.wi = __shfl_sync(0xffffffffu, r.wi, 0); o.b0 = __shfl_sync(0xffffffffu, r.b0, 0);
+    o.b1 = __shfl_sync(0xffffffffu, r.b1, 0); o.b2 = __shfl_sync(0xffffffffu, r.b2, 0);
+    o.b3 = __shfl_sync(0xffffffffu, r.b3, 0);
+    return o;
+  };
+  // Tasks are handed out dynamically: every warp starts with task gw; later
+  // tasks come from the per-launch counter (nwarps + ticket).  Nothing the
+  // warp waits for per block or per task is a global-memory round trip:
+  // tickets are taken two tasks ahead, records loaded one task ahead, block
+  // ids come with the record, and the next task's query is prefetched into
+  // registers.  Which warp computes a task does not change its result.
+  // Producer (lane 0 issues the copies; all lanes track the cursor).  The
+  // copy sequence is K(0), V(0), K(1), V(1), ... of the warp's tasks' blocks;
+  // copy h goes to slot h % NS.
+  int p_task = gw, p_blk = 0, p_half = 0;
+  Rec pr{};
   uint32_t p_q = 0;
   bool pf_sent = false;
+  int q_head = 0, q_tail = 0;              // tasks pushed / popped (warp-uniform)
+  int n1 = n_tasks, n2 = n_tasks;          // lane 0: next task id, the one after it (ticket in flight)
+  Rec r1{};                                // lane 0: record of n1 (load in flight)
+  auto push = [&](int t, const Rec& r) {
+    if (lane == 0) {
+      int4* e = reinterpret_cast<int4*>(&tq[warp][q_head % QN][0]);
+      e[0] = make_int4(r.row, r.start, r.end, r.kvh);
+      e[1] = make_int4(r.wi, t, r.nch, 0);
+    }
+    ++q_head;
+  };
   auto issue_next = [&]() {
     if (p_task >= n_tasks) {
       // this warp has issued its last K/V load: pull its share of the next
@@ -446,64 +484,99 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
       pf_sent = true;
       return;
     }
-    const int s = p_q % ST;
+    const int s = p_q % NS;
     if (lane == 0) {
-      int blk = tables[(size_t)pt.slot * mbps + (pt.start >> 5) + p_blk];
+      int blk = p_blk == 0 ? pr.b0 : p_blk == 1 ? pr.b1 : p_blk == 2 ? pr.b2 : pr.b3;
       if (blk < 0 || blk >= n_blocks) { set_err(err, kDevBadBlock); blk = 0; }
-      uint8_t* kt = ring + s * 2 * TILE;
-      tc::mbar_arrive_expect_tx(&bar[warp][s], 2 * TILE);
-      tc::bulk_load(kt, pool + pool_tile(layer, n_blocks, blk, hkv, pt.kvh, 0, HD), 2 * TILE, &bar[warp][s]);
+      tc::mbar_arrive_expect_tx(&bar[warp][s], TILE);
+      tc::bulk_load(ring + s * TILE, pool + pool_tile(layer, n_blocks, blk, hkv, pr.kvh, p_half, HD), TILE,
+                    &bar[warp][s]);
     }
     ++p_q;
-    if (++p_blk == pt.nb) {
+    if (p_half == 0) {
+      p_half = 1;
+      return;
+    }
+    p_half = 0;
+    if (++p_blk == (pr.end - pr.start + 31) >> 5) {
       p_blk = 0;
-      p_task += nwarps;
-      if (p_task < n_tasks) pt = task_of(p_task);
+      p_task = __shfl_sync(0xffffffffu, n1, 0);
+      if (p_task < n_tasks) {
+        pr = shfl_rec(r1);
+        push(p_task, pr);
+        if (lane == 0) {
+          n1 = n2;
+          if (n1 < n_tasks) r1 = load_rec(n1);
+          n2 = nwarps + atomicAdd(next_task, 1);
+        }
+      }
     }
   };
   pdl_wait();
   TR_MARK1;
-  for (int i = 0; i < ST; ++i) issue_next();
+  if (p_task < n_tasks) {
+    if (lane == 0) {
+      n1 = nwarps + atomicAdd(next_task, 1);
+      n2 = nwarps + atomicAdd(next_task, 1);
+    }
+    pr = load_rec(p_task);
+    push(p_task, pr);
+    if (lane == 0 && n1 < n_tasks) r1 = load_rec(n1);
+  }
+  for (int i = 0; i < NS; ++i) issue_next();
 
   const float scale = 1.0f / sqrtf((float)HD);
   const int mi = lane >> 3, ri = lane & 7;
   uint32_t c_q = 0;
   bool alive = true;
-  for (int t = gw; t < n_tasks && alive; t += nwarps) {
-    const Task tk = task_of(t);
-    // q of the group's heads (scaled) as hi / lo B fragments
-    uint32_t qh[KS][2], ql[KS][2];
-    const float* qrow = q + ((size_t)tk.row * hq + tk.kvh * G) * HD;
+  // the next task's query (raw fp32, this lane's fragment elements)
+  float qn[KS][2][2];
+  bool qn_valid = false;
+  auto load_q = [&](int row, int kvh, float (&d)[KS][2][2]) {
+    const float* qrow = q + ((size_t)row * hq + kvh * G) * HD;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int dd = ks * 16 + r * 8 + tid4 * 2;
-        float a = 0.f, b = 0.f;
         if (gid < G) {
-          a = qrow[gid * HD + dd] * scale;
-          b = qrow[gid * HD + dd + 1] * scale;
+          const float2 v = *reinterpret_cast<const float2*>(qrow + gid * HD + dd);
+          d[ks][r][0] = v.x;
+          d[ks][r][1] = v.y;
+        } else {
+          d[ks][r][0] = 0.f;
+          d[ks][r][1] = 0.f;
         }
-        split_pack(a, b, qh[ks][r], ql[ks][r]);
       }
+  };
+  while (alive && q_tail < q_head) {
+    __syncwarp();
+    const int4 e0 = reinterpret_cast<const int4*>(&tq[warp][q_tail % QN][0])[0];
+    const int4 e1 = reinterpret_cast<const int4*>(&tq[warp][q_tail % QN][0])[1];
+    ++q_tail;
+    struct {
+      int row, start, end, kvh, wi, nb, nch;
+    } tk{e0.x, e0.y, e0.z, e0.w, e1.x, (e0.z - e0.y + 31) >> 5, e1.z};
+    if (!qn_valid) load_q(tk.row, tk.kvh, qn);
+    qn_valid = false;
+    // q of the group's heads (scaled) as hi / lo B fragments
+    uint32_t qh[KS][2], ql[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) split_pack(qn[ks][r][0] * scale, qn[ks][r][1] * scale, qh[ks][r], ql[ks][r]);
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float o[KS][4];
 #pragma unroll
     for (int dt = 0; dt < KS; ++dt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) o[dt][c] = 0.f;
-    for (int b = 0; b < tk.nb; ++b, ++c_q) {
-      const int s = c_q % ST;
-      if (!tc::mbar_wait(&bar[warp][s], (c_q / ST) & 1, err, &abort_flag)) { alive = false; break; }
-      uint8_t* kt = ring + s * 2 * TILE;
-      uint8_t* vt = kt + TILE;
+    for (int b = 0; b < tk.nb; ++b) {
       const int nvalid = min(32, tk.end - (tk.start + b * 32));
-      for (int i = lane; i < (32 - nvalid) * (HD / 8); i += 32) {
-        const int r = nvalid + i / (HD / 8), ch = i % (HD / 8);
-        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 4096 + swz(r, ch & 7)) = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-      const uint32_t ks_base = tc::smem_u32(kt), vs_base = tc::smem_u32(vt);
+      // ---- K tile of block b
+      int s = c_q % NS;
+      if (!tc::mbar_wait(&bar[warp][s], (c_q / NS) & 1, err, &abort_flag)) { alive = false; break; }
+      const uint32_t ks_base = tc::smem_u32(ring + s * TILE);
       // q.K over 8 independent accumulator chains (m-tile x hi/lo x k
       // parity) so consecutive MMAs never wait on each other; summed in a
       // fixed order afterwards
@@ -532,6 +605,9 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
         for (int mt = 0; mt < 2; ++mt)
           mma_bf16_16816(acc[mt][1][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], ql[ks][0], ql[ks][1]);
       }
+      __syncwarp();          // every lane's K fragments are in registers
+      issue_next();          // refill the K slot NS copies ahead
+      ++c_q;
       float sc[2][4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
@@ -580,6 +656,17 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
           const int j = k2 * 16 + r * 8 + tid4 * 2;
           split_pack(Pw[gid * 32 + j], Pw[gid * 32 + j + 1], ph[k2][r], pl[k2][r]);
         }
+      // ---- V tile of block b (rows past the valid positions may hold stale
+      // bits: zero them, P is 0 there)
+      s = c_q % NS;
+      if (!tc::mbar_wait(&bar[warp][s], (c_q / NS) & 1, err, &abort_flag)) { alive = false; break; }
+      uint8_t* vt = ring + s * TILE;
+      for (int i = lane; i < (32 - nvalid) * (HD / 8); i += 32) {
+        const int r = nvalid + i / (HD / 8), ch = i % (HD / 8);
+        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 4096 + swz(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      const uint32_t vs_base = tc::smem_u32(vt);
       // P.V: the KS head-dim tiles are independent chains; issue them
       // interleaved (k2, then hi / lo, then tile) so no MMA waits on the last
 #pragma unroll
@@ -596,11 +683,20 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
 #pragma unroll
         for (int dt = 0; dt < KS; ++dt) mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], pl[k2][0], pl[k2][1]);
       }
-      __syncwarp();          // every lane is done with stage s (and Pw)
-      issue_next();          // refill it with the block ST ahead
+      __syncwarp();          // every lane is done with the V slot (and Pw)
+      issue_next();          // refill it NS copies ahead
+      ++c_q;
+      if (!qn_valid && q_tail < q_head) {
+        // the next task is known: start loading its query now
+        __syncwarp();
+        const int4 n0 = reinterpret_cast<const int4*>(&tq[warp][q_tail % QN][0])[0];
+        load_q(n0.x, n0.w, qn);
+        qn_valid = true;
+      }
     }
     if (!alive) break;
-    const int w0 = row_work[tk.row], nch = row_work[tk.row + 1] - w0;
+    // the row's chunks are consecutive work items, this one is chunk start / 128
+    const int nch = tk.nch, w0 = tk.wi - tk.start / kAttnChunk;
     if (nch == 1) {
       // the row's only chunk: normalise and write the output directly (the
       // merge kernel skips such rows; o * e^0 / (l * e^0) is the same value)
@@ -648,7 +744,7 @@ __global__ void __launch_bounds__(128, 1) attn_stream_kernel(
   if (!alive) {
     for (uint32_t r = c_q; r < p_q; ++r) {
       int no_abort = 0;
-      tc::mbar_wait(&bar[warp][r % ST], (r / ST) & 1, nullptr, &no_abort);
+      tc::mbar_wait(&bar[warp][r % NS], (r / NS) & 1, nullptr, &no_abort);
     }
   }
 #ifdef CBD_TRACE
@@ -689,25 +785,22 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(part_o) + ((size_t)w0 * hq + kvh * G + g) * Q + d4;
   const size_t cstride = (size_t)hq * Q;   // float4s between consecutive chunks
-  int c = 0;
-  for (; c + 8 <= nch; c += 8) {
-    float4 v[8];
+  // up to 32 chunks' partials in flight at once (one memory round trip for
+  // rows up to 4096 positions), then accumulated in chunk order
+  constexpr int CB = 32;
+  for (int c0 = 0; c0 < nch; c0 += CB) {
+    float4 v[CB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = po[(size_t)(c + j) * cstride];
+    for (int j = 0; j < CB; ++j)
+      if (c0 + j < nch) v[j] = po[(size_t)(c0 + j) * cstride];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float2 ml = sml[(c + j) * G + g];
-      const float sc = expf(ml.x - M);
-      L += ml.y * sc;
-      O.x += v[j].x * sc; O.y += v[j].y * sc; O.z += v[j].z * sc; O.w += v[j].w * sc;
-    }
-  }
-  for (; c < nch; ++c) {
-    const float4 v = po[(size_t)c * cstride];
-    const float2 ml = sml[c * G + g];
-    const float sc = expf(ml.x - M);
-    L += ml.y * sc;
-    O.x += v.x * sc; O.y += v.y * sc; O.z += v.z * sc; O.w += v.w * sc;
+    for (int j = 0; j < CB; ++j)
+      if (c0 + j < nch) {
+        const float2 ml = sml[(c0 + j) * G + g];
+        const float sc = expf(ml.x - M);
+        L += ml.y * sc;
+        O.x += v[j].x * sc; O.y += v[j].y * sc; O.z += v[j].z * sc; O.w += v[j].w * sc;
+      }
   }
   const float o4[4] = {O.x / L, O.y / L, O.z / L, O.w / L};
   uint16_t hi[4], lo[4];
@@ -732,11 +825,13 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
       attr = true;
     }
     const int n_tasks = b->n_work * dm.hkv;
-    const int grid = std::min(e->sm_count, (n_tasks + kAttnWarps - 1) / kAttnWarps);
-    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(128), smem, s, (const uint16_t*)p->base,
+    const int grid = std::min(e->sm_count, (n_tasks + kStreamWarps - 1) / kStreamWarps);
+    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(kStreamWarps * 32), smem, s,
+                                (const uint16_t*)p->base,
                                 (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
                                 (const AttnWork*)b->work, (const int32_t*)b->row_work, n_tasks, layer, p->n_blocks,
-                                dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi, e->act_lo, pf, e->err);
+                                dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi, e->act_lo,
+                                e->attn_next + layer, pf, e->err);
     if (ce != cudaSuccess) return ce;
   } else if (e->attn_path == 2) {
     constexpr int smem = attn_mma_smem<HD>();

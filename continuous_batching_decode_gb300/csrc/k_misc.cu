@@ -7,13 +7,18 @@ namespace cbd {
 
 // x[r][:] = E[token_r][:] as fp32 (the residual stream starts at the
 // embedding row of the row's token).
+// CTA 0 also zeroes the step's per-layer attention task counters (every
+// kernel of the previous step has completed once this kernel passes its
+// dependency wait).
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
-                             float* __restrict__ x) {
+                             float* __restrict__ x, int32_t* __restrict__ attn_next, int n_layers) {
   TR_DECL;
   pdl_trigger();
   pdl_wait();
   TR_MARK1;
   const int r = blockIdx.x;
+  if (r == 0)
+    for (int i = threadIdx.x; i < n_layers; i += blockDim.x) attn_next[i] = 0;
   const uint16_t* src = E + (size_t)rows[r].token * d;
   float* dst = x + (size_t)r * d;
   for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = bf16_to_f32(src[i]);
@@ -22,7 +27,7 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
 
 cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s) {
   return launch_pdl(embed_kernel, dim3(b->n_rows), dim3(256), 0, s, (const uint16_t*)e->embed,
-                    (const RowDev*)b->rows, e->dm.d, e->x);
+                    (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L);
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.
