@@ -102,6 +102,7 @@ PROTOS = {
     "cbd_engine_set_gemm_path": (c_i32, [c_vp, c_i32, c_i32]),
     "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_l2_prefetch": (c_i32, [c_vp, c_u64]),
+    "cbd_engine_set_fused_norm": (c_i32, [c_vp, c_i32]),
     "cbd_engine_profile_read": (c_i32, [c_vp, _P(KernelStat), c_i32, _P(c_i32)]),
     "cbd_kv_pool_create": (c_i32, [c_vp, c_i32, _P(c_vp)]),
     "cbd_kv_pool_destroy": (c_i32, [c_vp]),
@@ -215,6 +216,11 @@ def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 4) -> None:
 def engine_set_attention_path(e, path: int) -> None:
     """0 streaming tensor-core kernel (default), 1 CUDA cores, 2 one CTA per chunk."""
     _check(lib().cbd_engine_set_attention_path(e, path))
+
+
+def engine_set_fused_norm(e, enable: bool) -> None:
+    """RMSNorm folded into the tensor-core GEMM epilogues (default on)."""
+    _check(lib().cbd_engine_set_fused_norm(e, 1 if enable else 0))
 
 
 def engine_set_l2_prefetch(e, nbytes: int) -> None:

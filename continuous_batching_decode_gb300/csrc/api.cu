@@ -268,6 +268,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   Arena W;
   const size_t o_x = W.take(R * d * 4), o_ah = W.take(R * act_w * 2), o_al = W.take(R * act_w * 2);
   const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
+  const size_t o_nh = W.take(R * d * 2), o_nl = W.take(R * d * 2), o_ssq = W.take(R * kMaxSsqParts * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
   const size_t o_anext = W.take((size_t)dm.L * 4);
@@ -279,6 +280,9 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->x = reinterpret_cast<float*>(wb + o_x);
   e->act_hi = reinterpret_cast<uint16_t*>(wb + o_ah);
   e->act_lo = reinterpret_cast<uint16_t*>(wb + o_al);
+  e->norm_hi = reinterpret_cast<uint16_t*>(wb + o_nh);
+  e->norm_lo = reinterpret_cast<uint16_t*>(wb + o_nl);
+  e->ssq = reinterpret_cast<float*>(wb + o_ssq);
   e->ffn_hi = reinterpret_cast<uint16_t*>(wb + o_fh);
   e->ffn_lo = reinterpret_cast<uint16_t*>(wb + o_fl);
   e->q = reinterpret_cast<float*>(wb + o_q);
@@ -311,7 +315,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   // activation matrices in each layout the step uses (box 16 rows)
   {
     const int L = dm.L;
-    e->tmaps.resize((size_t)4 * L + 1 + 6);
+    e->tmaps.resize((size_t)4 * L + 1 + 8);
     bool ok = true;
     for (int l = 0; l < L && ok; ++l) {
       const LayerDev& Ld = e->layers[l];
@@ -329,6 +333,8 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 3], e->act_lo, hqd, R, hqd, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 4], e->ffn_hi, F, R, F, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 5], e->ffn_lo, F, R, F, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 6], e->norm_hi, d, R, d, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 7], e->norm_lo, d, R, d, 16);
     if (!ok) {
       cbd_engine* raw = e.release();
       cbd_engine_destroy(raw);
@@ -423,6 +429,13 @@ extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path)
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   if (path < 0 || path > 2) return fail(CBD_EINVAL, "attention path must be 0, 1 or 2");
   e->attn_path = path;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  e->fuse_norm = enable != 0;
   return CBD_OK;
 }
 
@@ -683,8 +696,15 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   if (out_logits && (reinterpret_cast<uintptr_t>(out_logits) & 15))
     return fail(CBD_EINVAL, "out_logits must be 16-byte aligned");
   if (b->m > 0 && !out_tokens) return fail(CBD_EINVAL, "out_tokens is NULL but rows are sampled");
+  // Fused RMSNorm on the tensor-core path: the embedding and the residual
+  // epilogues write split(x * g) and per-row partial sums of x^2, and the
+  // QKV / gate-up GEMMs apply 1/rms in their epilogues (no norm launches).
+  const int o_parts = gemm_tc_units(dm.d, hqd, n), dn_parts = gemm_tc_units(dm.d, dm.F, n);
+  const bool fused = e->fuse_norm && gemm_uses_tc(e, n) && o_parts <= kMaxSsqParts && dn_parts <= kMaxSsqParts;
   cbd_status st;
-  if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, s); }), "embed"))) return st;
+  if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, fused ? e->layers[0].attn_norm : nullptr, s); }),
+                "embed")))
+    return st;
   ++launches;
   EpiArgs qkv{};
   qkv.kind = kEpiQKV; qkv.out_f32 = e->q; qkv.ld = hqd;
@@ -693,15 +713,27 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   qkv.rows = b->rows; qkv.tables = b->tables; qkv.err = e->err;
   EpiArgs res{};
   res.kind = kEpiResid; res.out_f32 = e->x; res.ld = dm.d; res.err = e->err;
+  EpiArgs resn = res;
+  resn.kind = kEpiResidNorm; resn.norm_hi = e->norm_hi; resn.norm_lo = e->norm_lo; resn.ssq_out = e->ssq;
   EpiArgs glu{};
   glu.kind = kEpiSwiGLU; glu.out_hi = e->ffn_hi; glu.out_lo = e->ffn_lo; glu.ld_act = dm.F; glu.err = e->err;
+  if (fused) {
+    qkv.ssq_in = e->ssq; qkv.d_norm = dm.d; qkv.eps = dm.eps;
+    glu.ssq_in = e->ssq; glu.d_norm = dm.d; glu.eps = dm.eps; glu.n_parts_in = o_parts;
+  }
   const size_t a0 = (size_t)4 * dm.L + 1;
   const CUtensorMap* tm = e->tmaps.data();
+  // normalised-input activations: the rmsnorm kernel's act_hi / act_lo, or
+  // the fused epilogues' norm_hi / norm_lo
+  const uint16_t* in_hi = fused ? e->norm_hi : e->act_hi;
+  const uint16_t* in_lo = fused ? e->norm_lo : e->act_lo;
+  const CUtensorMap* tm_in_hi = fused ? &tm[a0 + 6] : &tm[a0 + 0];
+  const CUtensorMap* tm_in_lo = fused ? &tm[a0 + 7] : &tm[a0 + 1];
   // The step's GEMMs in order; each kernel prefetches (into L2) the first
   // k-blocks of the GEMM after it, so HBM keeps streaming across launches.
   auto g_qkv_of = [&](int l) {
-    return GemmOp{e->layers[l].w_qkv, dm.qkv_out, dm.d, e->act_hi, e->act_lo, dm.d,
-                  {&tm[4 * l + 0], &tm[a0 + 0], &tm[a0 + 1], dm.qkv_out, dm.d}};
+    return GemmOp{e->layers[l].w_qkv, dm.qkv_out, dm.d, in_hi, in_lo, dm.d,
+                  {&tm[4 * l + 0], tm_in_hi, tm_in_lo, dm.qkv_out, dm.d}};
   };
   const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
                     {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d}};
@@ -709,36 +741,52 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
     qkv.layer = l;
+    qkv.n_parts_in = l == 0 ? 1 : dn_parts;
     const GemmOp g_qkv = g_qkv_of(l);
     const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd}};
-    const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, e->act_hi, e->act_lo, dm.d,
-                      {&tm[4 * l + 2], &tm[a0 + 0], &tm[a0 + 1], 2 * dm.F, dm.d}};
+    const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, in_hi, in_lo, dm.d,
+                      {&tm[4 * l + 2], tm_in_hi, tm_in_lo, 2 * dm.F, dm.d}};
     const GemmOp g_dn{L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F,
                       {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F}};
     const PfSpec pf_o = next_prefetch(e, g_o, n), pf_gu = next_prefetch(e, g_gu, n),
                  pf_dn = next_prefetch(e, g_dn, n);
     const PfSpec pf_after_dn = l + 1 < dm.L ? next_prefetch(e, g_qkv_of(l + 1), n)
                                             : (b->m > 0 ? next_prefetch(e, g_lm, b->m) : pf_none);
-    if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.attn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
-                  "rmsnorm")))
-      return st;
+    EpiArgs res_o = res, res_dn = res;
+    if (fused) {
+      res_o = resn;
+      res_o.norm_g = L.ffn_norm;
+      if (l + 1 < dm.L) {
+        res_dn = resn;
+        res_dn.norm_g = e->layers[l + 1].attn_norm;
+      }
+    }
+    if (!fused) {
+      if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.attn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
+                    "rmsnorm")))
+        return st;
+      ++launches;
+    }
     if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, pf_none, s); }),
                   "qkv")))
       return st;
     if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, pf_o, s); }), "attention"))) return st;
-    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res, pf_gu, s); }),
+    if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res_o, pf_gu, s); }),
                   "o_proj")))
       return st;
-    if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.ffn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
-                  "rmsnorm")))
-      return st;
+    if (!fused) {
+      if ((st = chk(timed(e, kcNorm, s, [&] { return launch_rmsnorm(e, e->x, L.ffn_norm, n, nullptr, e->act_hi, e->act_lo, s); }),
+                    "rmsnorm")))
+        return st;
+      ++launches;
+    }
     if ((st = chk(timed(e, kcGU, s, [&] { return launch_gemm(e, g_gu, n, glu, pf_dn, s); }),
                   "gate_up")))
       return st;
-    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res, pf_after_dn, s); }),
+    if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res_dn, pf_after_dn, s); }),
                   "down")))
       return st;
-    launches += 8;
+    launches += 6;
   }
   if (b->m > 0) {
     float* lg = out_logits ? out_logits : e->logits;

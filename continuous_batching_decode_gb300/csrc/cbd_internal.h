@@ -130,6 +130,9 @@ struct cbd_engine {
   float* x = nullptr;                 // [max_rows][d] residual
   uint16_t* act_hi = nullptr;         // [max_rows][max(d, Hq*hd)] bf16
   uint16_t* act_lo = nullptr;
+  uint16_t* norm_hi = nullptr;        // [max_rows][d] bf16 split(x * g): fused-RMSNorm GEMM input
+  uint16_t* norm_lo = nullptr;
+  float* ssq = nullptr;               // [max_rows][kMaxSsqParts] partial sums of x^2
   uint16_t* ffn_hi = nullptr;         // [max_rows][F] bf16 SwiGLU output
   uint16_t* ffn_lo = nullptr;
   float* q = nullptr;                 // [max_rows][Hq*hd]
@@ -155,6 +158,7 @@ struct cbd_engine {
   cbd::TcWork tcw{};
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   size_t l2_prefetch = 48u << 20;     // bytes of the next GEMM's weights each kernel prefetches to L2
+  bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   // optional per-launch timing (cbd_engine_profile)
@@ -221,10 +225,18 @@ inline cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
 }
 // Kernel launchers (stream-ordered).  Each returns cudaGetLastError().
-cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s);
+// Embedding gather; with fused RMSNorm (g != null) also writes split(x * g)
+// to norm_hi / norm_lo and each row's sum of x^2 as its single partial.
+cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, const float* g, cudaStream_t s);
 cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
                            const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s);
-enum Epilogue : int { kEpiQKV = 0, kEpiResid = 1, kEpiSwiGLU = 2, kEpiLogits = 3 };
+enum Epilogue : int { kEpiQKV = 0, kEpiResid = 1, kEpiSwiGLU = 2, kEpiLogits = 3, kEpiResidNorm = 4 };
+// Fused RMSNorm (tcgen05 path): a residual-norm epilogue writes x += Y and
+// also the next norm's input without its 1/rms factor, split(x * g) as hi +
+// lo bf16, plus one partial sum of x^2 per row and CTA feature range; the
+// GEMM that consumes it multiplies its sums by 1/sqrt(sum of the row's
+// partials / d + eps) (RMSNorm(x) W^T = (1/rms) (x * g) W^T).
+constexpr int kMaxSsqParts = 256;   // partials per row: feature tiles x K splits of the producing GEMM
 struct EpiArgs {
   int kind;
   float* out_f32;            // logits [n][ld]; residual x [n][ld]; q [n][Hq*hd]
@@ -239,6 +251,16 @@ struct EpiArgs {
   const RowDev* rows;
   const int32_t* tables;
   int32_t* err;
+  // residual-norm epilogue (kEpiResidNorm)
+  const float* norm_g;       // [d] gain of the next RMSNorm
+  uint16_t* norm_hi;         // [n][d] split(x * g)
+  uint16_t* norm_lo;
+  float* ssq_out;            // [n][kMaxSsqParts] partial sums of x^2
+  // consumer of a fused norm: ssq_in != null scales every sum of row r by
+  // 1/sqrt(sum(ssq_in[r][0..n_parts_in)) / d_norm + eps)
+  const float* ssq_in;
+  int n_parts_in, d_norm;
+  float eps;
 };
 cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
                         int n, const EpiArgs& ep, cudaStream_t s);
@@ -253,6 +275,10 @@ cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiA
 // The L2 prefetch a kernel issues for the GEMM `op` that follows it on n rows
 // (nothing when that GEMM takes the CUDA-core path or prefetch is off).
 PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n);
+// Whether a GEMM of M x K weights on n rows takes the tcgen05 path, and
+// its number of (feature tile x K split) units.
+bool gemm_uses_tc(const cbd_engine* e, int n);
+int gemm_tc_units(int M, int K, int n);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                              const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,

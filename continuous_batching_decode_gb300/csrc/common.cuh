@@ -23,6 +23,12 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
   lo = f32_to_bf16(x - bf16_to_f32(hi));
 }
 
+// SwiGLU's gate: silu(a) * b = a / (1 + e^-a) * b, with the hardware
+// exponential and divide (a few ulp; the result is rounded to hi + lo bf16
+// right after).  For a very negative, e^-a overflows to +inf and the
+// quotient is 0, the limit of silu.
+__device__ __forceinline__ float silu_mul(float a, float b) { return __fdividef(a, 1.0f + __expf(-a)) * b; }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -116,7 +122,7 @@ __device__ __forceinline__ size_t pool_off(int layer, int kv, int nblocks, int b
 // SwiGLU: f = 2i is gate_i and f+1 is up_i.
 __device__ __forceinline__ void epi_pair(const EpiArgs& ep, int f, int row, float a, float b) {
   if (ep.kind == kEpiSwiGLU) {
-    float y = (a / (1.0f + expf(-a))) * b;
+    float y = silu_mul(a, b);
     uint16_t hi, lo;
     split_bf16(y, hi, lo);
     size_t o = (size_t)row * ep.ld_act + (f >> 1);

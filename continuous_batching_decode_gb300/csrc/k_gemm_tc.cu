@@ -26,15 +26,15 @@
 // (256-feature tile, 64-row tile); CTA rank r accumulates k-blocks
 // [r*KB/S, (r+1)*KB/S).  Each CTA folds its hi and lo lanes into a 64 x 256
 // fp32 partial in its own shared memory; after a cluster barrier, CTA r
-// finalises feature pairs [r*128/S, (r+1)*128/S) by reading all S partials
+// finalises feature quads [r*64/S, (r+1)*64/S) by reading all S partials
 // over distributed shared memory in rank order (fixed, so results do not
 // depend on timing) and runs the epilogue.  No partials go to global memory
 // and no CTA waits on a flag.
 //
-// CTA = 6 warps: warp 0 issues TMA loads into a ring of shared-memory
-// stages; warp 1 owns TMEM and issues the MMAs (one thread); warps 2-5 read
-// the accumulator back (warp w owns TMEM lanes 32*(w%4)..+31) and run the
-// epilogue.
+// CTA = 10 warps: warp 0 issues TMA loads into a ring of shared-memory
+// stages; warp 1 owns TMEM and issues the MMAs (one thread); warps 2-9 read
+// the accumulator back (warp w owns TMEM lanes 32*(w%4)..+31, warps w and
+// w+4 split the columns) and run the epilogue.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -47,7 +47,8 @@ namespace cbd {
 constexpr int kTcBN = 256;          // weight rows per tile (MMA N)
 constexpr int kTcRows = 64;         // activation rows per tile (MMA M = 2 x 64: hi, lo)
 constexpr int kTcBK = 64;           // k per stage: one 128-byte swizzle row of bf16
-constexpr int kTcThreads = 192;
+constexpr int kEpiThreads = 256;   // 8 epilogue warps (two per TMEM lane quarter)
+constexpr int kTcThreads = 64 + kEpiThreads;
 constexpr int kTcStages = 4;
 constexpr int kTcWBytes = kTcBN * kTcBK * 2;            // 32 KB
 constexpr int kTcABytes = 2 * kTcRows * kTcBK * 2;      // 16 KB (hi rows, then lo rows)
@@ -100,7 +101,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // quad's two rotation pairs (QKV q / k features); null if none.
 template <int KIND>
 __device__ __forceinline__ const float* epi_pre_addr(const EpiArgs& ep, int row, int fg, const int2* rinfo, int ri) {
-  if constexpr (KIND == kEpiResid) return ep.out_f32 + (size_t)row * ep.ld + fg;
+  if constexpr (KIND == kEpiResid || KIND == kEpiResidNorm) return ep.out_f32 + (size_t)row * ep.ld + fg;
   if constexpr (KIND == kEpiQKV) {
     const int hd = ep.hd, nq = ep.hq * hd, nk = ep.hkv * hd;
     if (fg < nq + nk) {
@@ -112,7 +113,7 @@ __device__ __forceinline__ const float* epi_pre_addr(const EpiArgs& ep, int row,
 }
 template <int KIND>
 __device__ __forceinline__ float4 epi_preload(const EpiArgs& ep, int row, int fg, const int2* rinfo, int ri) {
-  if constexpr (KIND == kEpiResid || KIND == kEpiQKV) {
+  if constexpr (KIND == kEpiResid || KIND == kEpiResidNorm || KIND == kEpiQKV) {
     const float* p = epi_pre_addr<KIND>(ep, row, fg, rinfo, ri);
     if (p) return *reinterpret_cast<const float4*>(p);
   }
@@ -125,17 +126,34 @@ __device__ __forceinline__ float4 epi_preload(const EpiArgs& ep, int row, int fg
 //   QKV: (fg, fg+1) and (fg+2, fg+3) are RoPE partners (dims i, i + hd/2
 //        and i+1, i+1 + hd/2 of one q or k head) or four v dims.
 //   SwiGLU: (fg, fg+1) = (gate, up) of output fg/2, (fg+2, fg+3) of fg/2+1.
+//   ResidNorm: x += v, then split(x * g) of the next norm; returns the
+//        quad's sum of x^2 (every other kind returns 0).
 template <int KIND>
-__device__ __forceinline__ void epi_quad(const EpiArgs& ep, int row, int fg, float4 v, float4 pre,
-                                         const int2* rinfo, int ri) {
-  if constexpr (KIND == kEpiLogits) {
+__device__ __forceinline__ float epi_quad(const EpiArgs& ep, int row, int fg, float4 v, float4 pre,
+                                          const int2* rinfo, int ri) {
+  if constexpr (KIND == kEpiResidNorm) {
+    const float4 x = make_float4(pre.x + v.x, pre.y + v.y, pre.z + v.z, pre.w + v.w);
+    *reinterpret_cast<float4*>(ep.out_f32 + (size_t)row * ep.ld + fg) = x;
+    const float4 g = *reinterpret_cast<const float4*>(ep.norm_g + fg);
+    uint16_t h[4], l[4];
+    split_bf16(x.x * g.x, h[0], l[0]);
+    split_bf16(x.y * g.y, h[1], l[1]);
+    split_bf16(x.z * g.z, h[2], l[2]);
+    split_bf16(x.w * g.w, h[3], l[3]);
+    const size_t o = (size_t)row * ep.ld + fg;
+    *reinterpret_cast<uint2*>(ep.norm_hi + o) =
+        make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+    *reinterpret_cast<uint2*>(ep.norm_lo + o) =
+        make_uint2((uint32_t)l[0] | ((uint32_t)l[1] << 16), (uint32_t)l[2] | ((uint32_t)l[3] << 16));
+    return x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+  } else if constexpr (KIND == kEpiLogits) {
     *reinterpret_cast<float4*>(ep.out_f32 + (size_t)row * ep.ld + fg) = v;
   } else if constexpr (KIND == kEpiResid) {
     *reinterpret_cast<float4*>(ep.out_f32 + (size_t)row * ep.ld + fg) =
         make_float4(pre.x + v.x, pre.y + v.y, pre.z + v.z, pre.w + v.w);
   } else if constexpr (KIND == kEpiSwiGLU) {
-    const float y0 = (v.x / (1.0f + expf(-v.x))) * v.y;
-    const float y1 = (v.z / (1.0f + expf(-v.z))) * v.w;
+    const float y0 = silu_mul(v.x, v.y);
+    const float y1 = silu_mul(v.z, v.w);
     uint16_t h0, l0, h1, l1;
     split_bf16(y0, h0, l0);
     split_bf16(y1, h1, l1);
@@ -154,38 +172,43 @@ __device__ __forceinline__ void epi_quad(const EpiArgs& ep, int row, int fg, flo
         float* qrow = ep.out_f32 + (size_t)row * nq + head * hd;
         *reinterpret_cast<float2*>(qrow + i) = make_float2(r0, r2);
         *reinterpret_cast<float2*>(qrow + i + half) = make_float2(r1, r3);
-        return;
+        return 0.f;
       }
       const int blk = rinfo[ri].y;
-      if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+      if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return 0.f; }
       const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 0, hd);
       *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i)) = pack_bf16x2(r0, r2);
       *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i + half)) = pack_bf16x2(r1, r3);
-      return;
+      return 0.f;
     }
     const int blk = rinfo[ri].y;
-    if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+    if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return 0.f; }
     const int fv = fg - nq - nk, head = fv / hd, jd = fv % hd;
     const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk, ep.hkv, head, hd, pos & 31, jd);
     *reinterpret_cast<uint2*>(ep.pool + o) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
+  return 0.f;
 }
 
-// Epilogue phase 2 for one epilogue kind (128 threads, et = 0..127).  CTA
+// Epilogue phase 2 for one epilogue kind (256 threads, et = 0..255).  CTA
 // rank r of the cluster finalises feature quads [r*64/S, (r+1)*64/S) of the
 // tile for every row: the S partials are read (over distributed shared
 // memory when S > 1) and summed in rank order, then the epilogue runs.
-// Item it = (row it / nq, quad it % nq) belongs to thread it % 128.
+// Item it = (row it / nq, quad it % nq) belongs to thread it % 256.
+// A norm consumer (ep.ssq_in) scales each row's sums by rinv[row] first; a
+// residual-norm producer collects each quad's sum of x^2 in sq[row][quad]
+// and then writes the row's partial for this CTA (quads in order).
 template <int KIND>
 __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
-                                           uint32_t Pbase, const int2* rinfo) {
+                                           uint32_t Pbase, const int2* rinfo, const float* rinv, float* sq) {
   const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
   const int nq = q1 - q0;
   const int items = rows_here * nq;
-  // Rolled loops: this code runs once per CTA, so its size (instruction
-  // fetch while HBM is saturated) costs more than per-item latency.
+  const bool scale = ep.ssq_in != nullptr;
+  // Rolled loop: this code runs once per CTA, and fetching a larger
+  // (unrolled) body while HBM is saturated costs more than it saves.
 #pragma unroll 1
-  for (int it = et; it < items; it += 128) {
+  for (int it = et; it < items; it += kEpiThreads) {
     const int i = it / nq;
     const int f = 4 * (q0 + it - i * nq);      // feature within the tile
     const uint32_t off = (uint32_t)(i * kTcPStride + f) * 4u;
@@ -207,7 +230,20 @@ __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, i
           acc.z += pv[qr].z; acc.w += pv[qr].w;
         }
     }
-    epi_quad<KIND>(ep, nr * kTcRows + i, fg, acc, pre, rinfo, i);
+    if (scale) {
+      const float r = rinv[i];
+      acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+    }
+    const float q2 = epi_quad<KIND>(ep, nr * kTcRows + i, fg, acc, pre, rinfo, i);
+    if constexpr (KIND == kEpiResidNorm) sq[i * 64 + (it - i * nq)] = q2;
+  }
+  if constexpr (KIND == kEpiResidNorm) {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    if (et < rows_here) {
+      float acc = 0.f;
+      for (int j = 0; j < nq; ++j) acc += sq[et * 64 + j];
+      ep.ssq_out[(size_t)(nr * kTcRows + et) * kMaxSsqParts + t * S + rank] = acc;
+    }
   }
 }
 
@@ -217,11 +253,11 @@ __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, i
 template <int KIND>
 __device__ __forceinline__ void epi_prefetch(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
                                              const int2* rinfo) {
-  if constexpr (KIND == kEpiResid || KIND == kEpiQKV) {
+  if constexpr (KIND == kEpiResid || KIND == kEpiResidNorm || KIND == kEpiQKV) {
     const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
     const int nq = q1 - q0;
     const int items = rows_here * nq;
-    for (int it = et; it < items; it += 128) {
+    for (int it = et; it < items; it += kEpiThreads) {
       const int i = it / nq;
       const float* p = epi_pre_addr<KIND>(ep, nr * kTcRows + i, t * kTcBN + 4 * (q0 + it - i * nq), rinfo, i);
       if (p) asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
@@ -244,6 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int abort_flag;
   __shared__ int decision;
   __shared__ int2 rinfo[kTcRows];           // QKV epilogue: (position, KV block) of each tile row
+  __shared__ float rinv[kTcRows];           // fused RMSNorm consumer: 1/rms of each tile row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = tc::smem_u32(smem_raw);
@@ -355,11 +392,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------------------------ epilogue phase 1: fold hi + lo into the partial
     // TMEM lane group lg = warp % 4 holds tile rows 32 * (lg % 2) + lane,
-    // hi halves for lg < 2 and lo halves for lg >= 2.  The lo warps copy
-    // their lanes to shared memory, then the hi warps add them to their own
-    // (hi + lo per element) and write the partial P; warps whose lanes hold
-    // no row of this tile skip their loads.
+    // hi halves for lg < 2 and lo halves for lg >= 2; two warps share each
+    // lane group, one per half of the columns.  The lo warps copy their
+    // lanes to shared memory, then the hi warps add them to their own (hi +
+    // lo per element) and write the partial P; warps whose lanes hold no row
+    // of this tile skip their loads.
     const int lg = warp & 3;
+    const int c_lo = ((warp - 2) >> 2) * (kTcBN / 2), c_hi = c_lo + kTcBN / 2;
     const int rows_here = min(kTcRows, a.n - nr * kTcRows);
     const int rl = (lg & 1) * 32 + lane;           // tile row of this lane
     const bool has_rows = (lg & 1) * 32 < rows_here;
@@ -369,22 +408,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;
     if (ep.kind == kEpiQKV) {
       // the rows' positions and KV blocks, read while the mainloop runs
-      for (int i = et; i < rows_here; i += 128) {
+      for (int i = et; i < rows_here; i += kEpiThreads) {
         const RowDev rw = ep.rows[nr * kTcRows + i];
         rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       epi_prefetch<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, rinfo);
     } else if (ep.kind == kEpiResid) {
       epi_prefetch<kEpiResid>(ep, S, rank, t, nr, rows_here, et, rinfo);
+    } else if (ep.kind == kEpiResidNorm) {
+      epi_prefetch<kEpiResidNorm>(ep, S, rank, t, nr, rows_here, et, rinfo);
+    }
+    if (ep.ssq_in) {
+      // fused RMSNorm: 1/rms of each row from the producer's partials; a
+      // warp per row, lanes over the partials (all loads in flight), then a
+      // fixed shuffle tree
+      for (int i = warp - 2; i < rows_here; i += kEpiThreads / 32) {
+        const float* sp = ep.ssq_in + (size_t)(nr * kTcRows + i) * kMaxSsqParts;
+        float v[kMaxSsqParts / 32];
+#pragma unroll
+        for (int j = 0; j < kMaxSsqParts / 32; ++j) v[j] = lane + 32 * j < ep.n_parts_in ? sp[lane + 32 * j] : 0.f;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxSsqParts / 32; ++j) acc += v[j];
+        acc = warp_sum(acc);
+        if (lane == 0) rinv[i] = 1.0f / sqrtf(acc / (float)ep.d_norm + ep.eps);
+      }
     }
     if (n_it > 0) tc::mbar_wait(&accum_full, 0, a.err, abort_p);
 #ifdef CBD_TRACE
     _e0 = gtimer();
 #endif
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     if (threadIdx.x == 64) decision = *abort_p || n_it == 0;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     const bool skip = decision != 0;
     tc::tc_fence_after();
     auto load64 = [&](int c0, float (&v)[64]) {
@@ -402,7 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     if (lg >= 2 && has_rows) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kTcBN; c0 += 64) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
         float v[64];
         load64(c0, v);
         float4* lo = reinterpret_cast<float4*>(LO + rl * kTcPStride + c0);
@@ -410,10 +467,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < 16; ++j) lo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     if (lg < 2 && has_rows) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kTcBN; c0 += 64) {
+      for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
         float v[64];
         load64(c0, v);
         const float4* lo = reinterpret_cast<const float4*>(LO + rl * kTcPStride + c0);
@@ -442,11 +499,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;
     const int rows_here = min(kTcRows, a.n - nr * kTcRows);
     const uint32_t Pbase = tc::smem_u32(ring);
+    float* sq = reinterpret_cast<float*>(ring + 64 * kTcPStride * 4);   // the LO area, free after phase 1
     switch (ep.kind) {
-      case kEpiQKV: epi_phase2<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
-      case kEpiResid: epi_phase2<kEpiResid>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
-      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
-      default: epi_phase2<kEpiLogits>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo); break;
+      case kEpiQKV: epi_phase2<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResid: epi_phase2<kEpiResid>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResidNorm: epi_phase2<kEpiResidNorm>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      default: epi_phase2<kEpiLogits>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
     }
   }
 #ifdef CBD_TRACE

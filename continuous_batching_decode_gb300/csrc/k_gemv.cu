@@ -124,6 +124,12 @@ cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, c
 static bool uses_tc(const cbd_engine* e, int n) {
   return e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
 }
+bool gemm_uses_tc(const cbd_engine* e, int n) { return uses_tc(e, n); }
+int gemm_tc_units(int M, int K, int n) {
+  int T, NR, KB, S;
+  gemm_tc_plan(M, K, n, &T, &NR, &KB, &S);
+  return T * S;
+}
 
 cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& ep, const PfSpec& pf,
                         cudaStream_t s) {

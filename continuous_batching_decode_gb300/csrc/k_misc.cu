@@ -10,8 +10,14 @@ namespace cbd {
 // CTA 0 also zeroes the step's per-layer attention task counters (every
 // kernel of the previous step has completed once this kernel passes its
 // dependency wait).
+// With g != null (fused RMSNorm of layer 0) it also writes split(x * g) to
+// norm_hi / norm_lo and the row's sum of x^2 (per-thread sums, then a fixed
+// tree) as the row's only partial in ssq.
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
-                             float* __restrict__ x, int32_t* __restrict__ attn_next, int n_layers) {
+                             float* __restrict__ x, int32_t* __restrict__ attn_next, int n_layers,
+                             const float* __restrict__ g, uint16_t* __restrict__ norm_hi,
+                             uint16_t* __restrict__ norm_lo, float* __restrict__ ssq) {
+  __shared__ float red[32];
   TR_DECL;
   pdl_trigger();
   pdl_wait();
@@ -21,13 +27,36 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
     for (int i = threadIdx.x; i < n_layers; i += blockDim.x) attn_next[i] = 0;
   const uint16_t* src = E + (size_t)rows[r].token * d;
   float* dst = x + (size_t)r * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = bf16_to_f32(src[i]);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = bf16_to_f32(src[i]);
+    dst[i] = v;
+    if (g) {
+      uint16_t h, l;
+      split_bf16(v * g[i], h, l);
+      norm_hi[(size_t)r * d + i] = h;
+      norm_lo[(size_t)r * d + i] = l;
+      ss += v * v;
+    }
+  }
+  if (g) {
+    ss = warp_sum(ss);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = ss;
+    __syncthreads();
+    if (w == 0) {
+      float t = l < (int)(blockDim.x >> 5) ? red[l] : 0.f;
+      t = warp_sum(t);
+      if (l == 0) ssq[(size_t)r * kMaxSsqParts] = t;
+    }
+  }
   TR_END(1);
 }
 
-cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, cudaStream_t s) {
+cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, const float* g, cudaStream_t s) {
   return launch_pdl(embed_kernel, dim3(b->n_rows), dim3(256), 0, s, (const uint16_t*)e->embed,
-                    (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L);
+                    (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L, g, e->norm_hi, e->norm_lo,
+                    e->ssq);
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.

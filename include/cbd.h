@@ -137,6 +137,16 @@ cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_ma
  * 128-position chunks and the same merge order. */
 cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path);
 
+/* RMSNorm fused into the weight contractions (default on): on the tcgen05
+ * path the embedding and the residual epilogues write the next norm's input
+ * x * g (hi + lo bf16) and per-row partial sums of x^2, and the QKV and
+ * gate/up contractions multiply their sums by 1/sqrt(mean(x^2) + eps),
+ * which is RMSNorm(x) W^T with no separate normalisation launch.  Off (0),
+ * or on the CUDA-core GEMV path, a normalisation kernel runs before each of
+ * those contractions.  The two agree to rounding (they round the
+ * activations at different points).  Errors: CBD_EINVAL for a NULL engine. */
+cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable);
+
 /* L2 prefetch across kernel boundaries: once a kernel of the step has issued
  * its last load, it asks L2 to fetch the first k-blocks of the next weight
  * contraction's work units, up to `bytes` in all (default 48 MiB; 0 turns

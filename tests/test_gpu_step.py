@@ -296,9 +296,10 @@ def test_gemm_paths_agree_on_long_prefill(tiny):
 
 def test_multi_chunk_rows_and_l2_prefetch(tiny):
     """Rows whose context spans several 128-position attention chunks (so
-    the chunk partials are merged) match the oracle, and turning the L2
+    the chunk partials are merged) match the oracle; turning the L2
     prefetch off leaves every logit bit-identical (a prefetch is a cache
-    hint only)."""
+    hint only); a separate RMSNorm launch instead of the fused one agrees
+    within the logit tolerance."""
     V = tiny.shape["vocab"]
     rng = np.random.default_rng(31)
     prompts = [list(rng.integers(0, V, 300)), list(rng.integers(0, V, 200))]
@@ -319,9 +320,15 @@ def test_multi_chunk_rows_and_l2_prefetch(tiny):
         _, z = gu.run_step(tiny, pool, rows, tables, nbps, g)
         res.append(z)
     cbd.engine_set_l2_prefetch(tiny.e, 48 << 20)
+    # RMSNorm folded into the GEMM epilogues vs a separate norm launch:
+    # the same sums, rounded at different points
+    cbd.engine_set_fused_norm(tiny.e, False)
+    _, z_unfused = gu.run_step(tiny, pool, rows, tables, nbps, g)
+    cbd.engine_set_fused_norm(tiny.e, True)
     pool.close()
     for z in res[1:]:
         np.testing.assert_array_equal(z, res[0])
+    gu.assert_logits_close(z_unfused, res[0], "fused vs separate RMSNorm")
     om_ = tiny.oracle()
     zo = []
     for s, p in enumerate(prompts):
