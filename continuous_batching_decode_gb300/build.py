@@ -36,11 +36,12 @@ def _newest_header() -> float:
 
 
 def build(verbose: bool = False, force: bool = False, extra: list | None = None, lib: str = LIB,
-          build_dir: str = BUILD) -> str:
+          build_dir: str = BUILD, src_dir: str = CSRC) -> str:
     """Compile and link; `extra` nvcc flags (e.g. -DCBD_TRACE for the
-    timeline-tracing variant) go with `lib` / `build_dir` of their own."""
+    timeline-tracing variant) or another `src_dir` go with `lib` /
+    `build_dir` of their own."""
     os.makedirs(build_dir, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    srcs = sorted(glob.glob(os.path.join(src_dir, "*.cu")) + glob.glob(os.path.join(src_dir, "*.cpp")))
     hdr = _newest_header()
     cc = nvcc()
     jobs = []

@@ -50,15 +50,14 @@ enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, 
 // by 64 columns, each one contiguous.  perm (nullable) gives the source row
 // of each destination row.
 __global__ void permute_tile_kernel(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src,
-                                    const int32_t* __restrict__ perm, int K) {
+                                    const int32_t* __restrict__ perm, int K, int N) {
   const int r = blockIdx.x;
   const int sr = perm ? perm[r] : r;
   const int KB = K / 64;
   const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)sr * K);
   for (int c = threadIdx.x; c < K / 8; c += blockDim.x) {
     const int k = c * 8;
-    uint4* d = reinterpret_cast<uint4*>(dst + ((((size_t)(r >> 8) * KB + (k >> 6)) << 8) + (r & 255)) * 64 + (k & 63));
-    *d = s[c];
+    *reinterpret_cast<uint4*>(dst + tiled_off(r, k, N, KB)) = s[c];
   }
 }
 __global__ void bf16_to_f32_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, int n) {
@@ -191,11 +190,17 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     CBD_CUDA(cudaGetLastError());
     return CBD_OK;
   };
-  // tmp (row-major [M][K]) -> arena (tiled), rows permuted when perm is given
-  auto tiled = [&](size_t off, const std::vector<int32_t>* perm, int M, int K) -> cbd_status {
+  // tile widths (weight rows per tile) per matrix shape, for this GPU
+  e->tile_qkv = gemm_tc_pick_tile((int)qo, (int)d);
+  e->tile_o = gemm_tc_pick_tile((int)d, (int)hqd);
+  e->tile_gu = gemm_tc_pick_tile((int)(2 * F), (int)d);
+  e->tile_dn = gemm_tc_pick_tile((int)d, (int)F);
+  e->tile_lm = gemm_tc_pick_tile((int)V, (int)d);
+  // tmp (row-major [M][K]) -> arena (tiled, N rows per tile), rows permuted when perm is given
+  auto tiled = [&](size_t off, const std::vector<int32_t>* perm, int M, int K, int N) -> cbd_status {
     if (perm) CBD_CUDA(cudaMemcpy(perm_d, perm->data(), perm->size() * 4, cudaMemcpyHostToDevice));
     permute_tile_kernel<<<M, 256>>>(reinterpret_cast<uint16_t*>(base + off), static_cast<uint16_t*>(tmp),
-                                    perm ? perm_d : nullptr, K);
+                                    perm ? perm_d : nullptr, K, N);
     CBD_CUDA(cudaGetLastError());
     CBD_CUDA(cudaDeviceSynchronize());
     return CBD_OK;
@@ -218,7 +223,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
 #define TRY(x) do { s2 = (x); if (s2) { free_tmp(); cleanup(); return s2; } } while (0)
   TRY(upload(base + o_embed, w->embed, V * d * 2, ondev));
   TRY(upload(tmp, w->lm_head, V * d * 2, ondev));
-  TRY(tiled(o_lm, nullptr, (int)V, (int)d));
+  TRY(tiled(o_lm, nullptr, (int)V, (int)d, e->tile_lm));
   TRY(gain(o_fn, w->final_norm));
   e->layers.resize(dm.L);
   for (int l = 0; l < dm.L; ++l) {
@@ -229,14 +234,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     TRY(upload(t, lw.wq, hqd * d * 2, ondev));
     TRY(upload(t + hqd * d * 2, lw.wk, (size_t)dm.hkv * dm.hd * d * 2, ondev));
     TRY(upload(t + (hqd + (size_t)dm.hkv * dm.hd) * d * 2, lw.wv, (size_t)dm.hkv * dm.hd * d * 2, ondev));
-    TRY(tiled(o_qkv[l], &perm_qkv, (int)qo, (int)d));
+    TRY(tiled(o_qkv[l], &perm_qkv, (int)qo, (int)d, e->tile_qkv));
     TRY(upload(t, lw.wo, d * hqd * 2, ondev));
-    TRY(tiled(o_o[l], nullptr, (int)d, (int)hqd));
+    TRY(tiled(o_o[l], nullptr, (int)d, (int)hqd, e->tile_o));
     TRY(upload(t, lw.w_gate, F * d * 2, ondev));
     TRY(upload(t + F * d * 2, lw.w_up, F * d * 2, ondev));
-    TRY(tiled(o_gu[l], &perm_gu, (int)(2 * F), (int)d));
+    TRY(tiled(o_gu[l], &perm_gu, (int)(2 * F), (int)d, e->tile_gu));
     TRY(upload(t, lw.w_down, d * F * 2, ondev));
-    TRY(tiled(o_dn[l], nullptr, (int)d, (int)F));
+    TRY(tiled(o_dn[l], nullptr, (int)d, (int)F, e->tile_dn));
     LayerDev& L = e->layers[l];
     L.attn_norm = reinterpret_cast<float*>(base + o_an[l]);
     L.ffn_norm = reinterpret_cast<float*>(base + o_fnn[l]);
@@ -320,13 +325,13 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     for (int l = 0; l < L && ok; ++l) {
       const LayerDev& Ld = e->layers[l];
       // tiled weights: a [M*K/64][64] matrix, one 256-row box per 32 KB tile
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, 256);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, 256);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, 256);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, 256);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, e->tile_qkv);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, e->tile_o);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, e->tile_gu);
+      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, e->tile_dn);
     }
     const size_t a0 = (size_t)4 * L + 1;
-    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, 256);
+    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, e->tile_lm);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);
@@ -699,7 +704,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   // Fused RMSNorm on the tensor-core path: the embedding and the residual
   // epilogues write split(x * g) and per-row partial sums of x^2, and the
   // QKV / gate-up GEMMs apply 1/rms in their epilogues (no norm launches).
-  const int o_parts = gemm_tc_units(dm.d, hqd, n), dn_parts = gemm_tc_units(dm.d, dm.F, n);
+  const int o_parts = gemm_tc_units(dm.d, hqd, e->tile_o, n), dn_parts = gemm_tc_units(dm.d, dm.F, e->tile_dn, n);
   const bool fused = e->fuse_norm && gemm_uses_tc(e, n) && o_parts <= kMaxSsqParts && dn_parts <= kMaxSsqParts;
   cbd_status st;
   if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, fused ? e->layers[0].attn_norm : nullptr, s); }),
@@ -733,21 +738,22 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   // k-blocks of the GEMM after it, so HBM keeps streaming across launches.
   auto g_qkv_of = [&](int l) {
     return GemmOp{e->layers[l].w_qkv, dm.qkv_out, dm.d, in_hi, in_lo, dm.d,
-                  {&tm[4 * l + 0], tm_in_hi, tm_in_lo, dm.qkv_out, dm.d}};
+                  {&tm[4 * l + 0], tm_in_hi, tm_in_lo, dm.qkv_out, dm.d, e->tile_qkv}};
   };
   const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
-                    {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d}};
+                    {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d, e->tile_lm}};
   const PfSpec pf_none{};
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
     qkv.layer = l;
     qkv.n_parts_in = l == 0 ? 1 : dn_parts;
     const GemmOp g_qkv = g_qkv_of(l);
-    const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd, {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd}};
+    const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd,
+                     {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd, e->tile_o}};
     const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, in_hi, in_lo, dm.d,
-                      {&tm[4 * l + 2], tm_in_hi, tm_in_lo, 2 * dm.F, dm.d}};
+                      {&tm[4 * l + 2], tm_in_hi, tm_in_lo, 2 * dm.F, dm.d, e->tile_gu}};
     const GemmOp g_dn{L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F,
-                      {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F}};
+                      {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F, e->tile_dn}};
     const PfSpec pf_o = next_prefetch(e, g_o, n), pf_gu = next_prefetch(e, g_gu, n),
                  pf_dn = next_prefetch(e, g_dn, n);
     const PfSpec pf_after_dn = l + 1 < dm.L ? next_prefetch(e, g_qkv_of(l + 1), n)

@@ -74,15 +74,20 @@ struct TcGemm {
   const CUtensorMap* hi;
   const CUtensorMap* lo;
   int M, K;
+  int N;                  // weight rows per tile (the weights' tiling)
 };
 struct TcWork {
   float* part;            // [2 * sm_count][128][128] partial tiles
   int32_t* counters;      // [max_units] arrival counters (zero between launches)
   long long max_units;
 };
-// Pre-tiled weights: tile (t, kb) -- 256 output features x 64 k -- is one
-// contiguous 32 KB run at byte offset (t * KB + kb) * kWTileBytes.
-constexpr int kWTileBytes = 256 * 64 * 2;
+// Pre-tiled weights: with a tile width of N rows (chosen per matrix), tile
+// (t, kb) -- N output features x 64 k -- is one contiguous N * 128-byte run
+// at byte offset (t * KB + kb) * N * 128; element (r, k) sits at
+// ((r / N) * KB + k / 64) * N * 64 + (r % N) * 64 + k % 64.
+__host__ __device__ inline size_t tiled_off(int r, int k, int N, int KB) {
+  return ((size_t)(r / N) * KB + (k >> 6)) * (size_t)N * 64 + (size_t)(r % N) * 64 + (k & 63);
+}
 
 // L2 prefetch of an upcoming tcgen05 GEMM's weights: the first P k-blocks
 // of each of its T x S (feature tile, K split) work units, so that HBM keeps
@@ -90,7 +95,7 @@ constexpr int kWTileBytes = 256 * 64 * 2;
 // prefetch is only a hint to the cache; it never changes a result.
 struct PfSpec {
   const uint8_t* w;          // the GEMM's pre-tiled weights; null: nothing
-  int32_t T, KB, S, P;
+  int32_t N, T, KB, S, P;    // tile width, tiles, k-blocks, K split, k-blocks per unit to fetch
 };
 
 // A GEMM of the step: weights W [M][K] times activations (hi + lo) [n][lda].
@@ -156,6 +161,7 @@ struct cbd_engine {
   // tcgen05 GEMM: tensor maps (built once), partial tiles, counters
   std::vector<CUtensorMap> tmaps;     // per layer: qkv, o, gu, down; then lm_head; then activations
   cbd::TcWork tcw{};
+  int tile_qkv = 256, tile_o = 256, tile_gu = 256, tile_dn = 256, tile_lm = 256;   // weight tile widths
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   size_t l2_prefetch = 48u << 20;     // bytes of the next GEMM's weights each kernel prefetches to L2
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
@@ -262,12 +268,14 @@ struct EpiArgs {
   int n_parts_in, d_norm;
   float eps;
 };
-cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
+cudaError_t launch_gemv(const uint16_t* W, int M, int K, int N, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
                         int n, const EpiArgs& ep, cudaStream_t s);
 cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s);
 // The tcgen05 GEMM's work split for M x K weights and n rows: feature tiles,
 // row tiles, k-blocks and the cluster (K split) size.
-void gemm_tc_plan(int M, int K, int n, int* T, int* NR, int* KB, int* S);
+void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S);
+// Tile width (weight rows per tile) for an M x K weight matrix on this GPU.
+int gemm_tc_pick_tile(int M, int K);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
                     uint32_t box_rows);
 cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& epi, const PfSpec& pf,
@@ -278,7 +286,7 @@ PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n);
 // Whether a GEMM of M x K weights on n rows takes the tcgen05 path, and
 // its number of (feature tile x K split) units.
 bool gemm_uses_tc(const cbd_engine* e, int n);
-int gemm_tc_units(int M, int K, int n);
+int gemm_tc_units(int M, int K, int N, int n);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                              const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,

@@ -44,21 +44,23 @@
 
 namespace cbd {
 
-constexpr int kTcBN = 256;          // weight rows per tile (MMA N)
+constexpr int kTcMaxBN = 256;       // weight rows per tile (MMA N) at most; TMEM columns allocated
 constexpr int kTcRows = 64;         // activation rows per tile (MMA M = 2 x 64: hi, lo)
 constexpr int kTcBK = 64;           // k per stage: one 128-byte swizzle row of bf16
-constexpr int kEpiThreads = 256;   // 8 epilogue warps (two per TMEM lane quarter)
+constexpr int kEpiThreads = 256;    // 8 epilogue warps (two per TMEM lane quarter)
 constexpr int kTcThreads = 64 + kEpiThreads;
-constexpr int kTcStages = 4;
-constexpr int kTcWBytes = kTcBN * kTcBK * 2;            // 32 KB
 constexpr int kTcABytes = 2 * kTcRows * kTcBK * 2;      // 16 KB (hi rows, then lo rows)
-constexpr int kTcStageBytes = kTcWBytes + kTcABytes;
-constexpr int kTcPStride = kTcBN + 4;                   // fp32 partial row stride (padded)
-constexpr int kTcSmem = kTcStages * kTcStageBytes + 1024;
+// Pipeline stages: 4 at N = 256 (6 at 128).  A larger ring (224 KB) cost
+// ~2% of the step on GB300: shared memory and L1 share 256 KB per SM, and
+// the epilogue's residual / RoPE reads hit L1.
+constexpr int kTcRing = 4 * (kTcMaxBN * kTcBK * 2 + kTcABytes);
+constexpr int kTcMaxStages = 8;
+constexpr int kTcSmem = kTcRing + 1024;
 constexpr int kTcMaxCluster = 8;
 
 struct TcArgs {
   int M, K, n;                       // weight rows, reduction length, activation rows
+  int N;                             // weight rows per tile (MMA N): the weights' tiling
   int T, NR, KB, S;                  // feature tiles, row tiles, k blocks, cluster size
   int32_t* err;
 };
@@ -198,10 +200,11 @@ __device__ __forceinline__ float epi_quad(const EpiArgs& ep, int row, int fg, fl
 // A norm consumer (ep.ssq_in) scales each row's sums by rinv[row] first; a
 // residual-norm producer collects each quad's sum of x^2 in sq[row][quad]
 // and then writes the row's partial for this CTA (quads in order).
-template <int KIND>
-__device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
-                                           uint32_t Pbase, const int2* rinfo, const float* rinv, float* sq) {
-  const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
+template <int KIND, int N>
+__device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here,
+                                           int et, uint32_t Pbase, const int2* rinfo, const float* rinv, float* sq) {
+  const int q0 = rank * (N / 4) / S, q1 = (rank + 1) * (N / 4) / S;
+  constexpr int PS = N + 4;                    // fp32 partial row stride (padded)
   const int nq = q1 - q0;
   const int items = rows_here * nq;
   const bool scale = ep.ssq_in != nullptr;
@@ -211,8 +214,8 @@ __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, i
   for (int it = et; it < items; it += kEpiThreads) {
     const int i = it / nq;
     const int f = 4 * (q0 + it - i * nq);      // feature within the tile
-    const uint32_t off = (uint32_t)(i * kTcPStride + f) * 4u;
-    const int fg = t * kTcBN + f;
+    const uint32_t off = (uint32_t)(i * PS + f) * 4u;
+    const int fg = t * N + f;
     const float4 pre = epi_preload<KIND>(ep, nr * kTcRows + i, fg, rinfo, i);
     float4 acc;
     if (S == 1) {
@@ -250,31 +253,43 @@ __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, i
 // While the mainloop runs: pull each epilogue thread's global operands
 // (residual x, RoPE factors) into L1 so phase 2 does not wait on memory
 // round trips that are long while HBM is saturated.
-template <int KIND>
-__device__ __forceinline__ void epi_prefetch(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here, int et,
-                                             const int2* rinfo) {
+template <int KIND, int N>
+__device__ __forceinline__ void epi_prefetch(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here,
+                                             int et, const int2* rinfo) {
   if constexpr (KIND == kEpiResid || KIND == kEpiResidNorm || KIND == kEpiQKV) {
-    const int q0 = rank * (kTcBN / 4) / S, q1 = (rank + 1) * (kTcBN / 4) / S;
+    const int q0 = rank * (N / 4) / S, q1 = (rank + 1) * (N / 4) / S;
     const int nq = q1 - q0;
     const int items = rows_here * nq;
     for (int it = et; it < items; it += kEpiThreads) {
       const int i = it / nq;
-      const float* p = epi_pre_addr<KIND>(ep, nr * kTcRows + i, t * kTcBN + 4 * (q0 + it - i * nq), rinfo, i);
+      const float* p = epi_pre_addr<KIND>(ep, nr * kTcRows + i, t * N + 4 * (q0 + it - i * nq), rinfo, i);
       if (p) asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
     }
   }
 }
 
+template <int N>
+__host__ __device__ constexpr int tc_stages() {
+  return kTcRing / (N * kTcBK * 2 + kTcABytes) < kTcMaxStages ? kTcRing / (N * kTcBK * 2 + kTcABytes) : kTcMaxStages;
+}
+
+// One instantiation per tile width N (weight rows per tile, MMA N).
+template <int N>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmL, const TcArgs a, const EpiArgs ep, const PfSpec pf) {
-  constexpr uint32_t kIdesc = tc::idesc_bf16(2 * kTcRows, kTcBN);
+  static_assert(N % 32 == 0 && N >= 64 && N <= kTcMaxBN, "tile width");
+  constexpr uint32_t idesc = tc::idesc_bf16(2 * kTcRows, N);
+  constexpr int ST = tc_stages<N>();
+  constexpr uint32_t w_bytes = (uint32_t)N * kTcBK * 2;        // one weight tile per stage
+  constexpr uint32_t stage_bytes = w_bytes + kTcABytes;
+  constexpr int PS = N + 4;                                     // fp32 partial row stride (padded)
   TR_DECL;
 #ifdef CBD_TRACE
   unsigned long long _e0 = 0, _e1 = 0;    // epilogue: accumulator ready, hi + lo folded
 #endif
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kTcStages], empty_bar[kTcStages];
+  __shared__ __align__(8) uint64_t full_bar[kTcMaxStages], empty_bar[kTcMaxStages];
   __shared__ __align__(8) uint64_t accum_full, mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -294,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_it = kb1 - kb0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       tc::mbar_init(&full_bar[s], 1);
       tc::mbar_init(&empty_bar[s], 1);
     }
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::prefetch_tmap(&tmL);
   }
   pdl_trigger();
-  if (warp == 1) tc::tmem_alloc(&tmem_base, kTcBN);
+  if (warp == 1) tc::tmem_alloc(&tmem_base, kTcMaxBN);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -324,16 +339,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // tile has rows; the MMA rows past them read stale shared memory and
       // land in TMEM lanes the epilogue never reads
       const int nbox = (min(kTcRows, a.n - nr * kTcRows) + 15) / 16;
-      const uint32_t stage_tx = kTcWBytes + 2u * nbox * 2048u;
+      const uint32_t stage_tx = w_bytes + 2u * nbox * 2048u;
       auto issue_w = [&](int q) {
-        const int s = q % kTcStages;
-        uint8_t* st = ring + (size_t)s * kTcStageBytes;
+        const int s = q % ST;
+        uint8_t* st = ring + (size_t)s * stage_bytes;
         tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
-        tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb0 + q) * kTcBN, &full_bar[s]);
+        tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s]);
       };
       auto issue_a = [&](int q) {
-        const int s = q % kTcStages;
-        uint8_t* st = ring + (size_t)s * kTcStageBytes + kTcWBytes;
+        const int s = q % ST;
+        uint8_t* st = ring + (size_t)s * stage_bytes + w_bytes;
         const int kx = (kb0 + q) * kTcBK;
         for (int j = 0; j < nbox; ++j) {
           tc::tma_load_2d(st + j * 2048, &tmH, kx, nr * kTcRows + j * 16, &full_bar[s]);
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       // weights do not depend on the previous kernel: start streaming them
       // before waiting for it, then add the activations
-      const int npre = n_it < kTcStages ? n_it : kTcStages;
+      const int npre = n_it < ST ? n_it : ST;
       for (int q = 0; q < npre; ++q) issue_w(q);
       pdl_wait();
       TR_MARK1;
@@ -350,8 +365,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int q = npre;
       bool ok = true;
       for (; q < n_it; ++q) {
-        const int s = q % kTcStages;
-        if (!tc::mbar_wait(&empty_bar[s], ((q / kTcStages) & 1) ^ 1, a.err, abort_p)) { ok = false; break; }
+        const int s = q % ST;
+        if (!tc::mbar_wait(&empty_bar[s], ((q / ST) & 1) ^ 1, a.err, abort_p)) { ok = false; break; }
         issue_w(q);
         issue_a(q);
       }
@@ -361,9 +376,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       TR_MARK2;
       if (ok) tc::pf_issue(pf, blockIdx.x, gridDim.x);
       if (!ok) {     // every load issued must land before the CTA exits
-        for (int r = q > kTcStages ? q - kTcStages : 0; r < q; ++r) {
+        for (int r = q > ST ? q - ST : 0; r < q; ++r) {
           int no_abort = 0;
-          tc::mbar_wait(&full_bar[r % kTcStages], (r / kTcStages) & 1, nullptr, &no_abort);
+          tc::mbar_wait(&full_bar[r % ST], (r / ST) & 1, nullptr, &no_abort);
         }
       }
     }
@@ -372,15 +387,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       bool ok = true;
       for (int q = 0; q < n_it; ++q) {
-        const int s = q % kTcStages;
-        if (!tc::mbar_wait(&full_bar[s], (q / kTcStages) & 1, a.err, abort_p)) { ok = false; break; }
+        const int s = q % ST;
+        if (!tc::mbar_wait(&full_bar[s], (q / ST) & 1, a.err, abort_p)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t st = tc::smem_u32(ring + (size_t)s * kTcStageBytes);
+        const uint32_t st = tc::smem_u32(ring + (size_t)s * stage_bytes);
         const uint64_t dW = tc::sdesc_sw128(st);
-        const uint64_t dA = tc::sdesc_sw128(st + kTcWBytes);
+        const uint64_t dA = tc::sdesc_sw128(st + w_bytes);
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes along K inside the swizzled rows
-          tc::mma_bf16(tmem, dA + 2 * k, dW + 2 * k, kIdesc, (q > 0 || k > 0) ? 1u : 0u);
+          tc::mma_bf16(tmem, dA + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(&empty_bar[s]);
       }
       if (ok && n_it > 0) tc::mma_commit(&accum_full);
@@ -398,13 +413,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // lo per element) and write the partial P; warps whose lanes hold no row
     // of this tile skip their loads.
     const int lg = warp & 3;
-    const int c_lo = ((warp - 2) >> 2) * (kTcBN / 2), c_hi = c_lo + kTcBN / 2;
+    // column halves on 32-column boundaries
+    constexpr int c_mid = ((N / 2 + 31) / 32) * 32;
+    const int c_lo = (warp - 2) < 4 ? 0 : c_mid, c_hi = (warp - 2) < 4 ? c_mid : N;
     const int rows_here = min(kTcRows, a.n - nr * kTcRows);
     const int rl = (lg & 1) * 32 + lane;           // tile row of this lane
     const bool has_rows = (lg & 1) * 32 < rows_here;
     const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16);
-    float* P = reinterpret_cast<float*>(ring);                         // [64][kTcPStride] hi + lo
-    float* LO = reinterpret_cast<float*>(ring + 64 * kTcPStride * 4);   // [64][kTcPStride] lo
+    float* P = reinterpret_cast<float*>(ring);                  // [64][PS] hi + lo
+    float* LO = reinterpret_cast<float*>(ring + 64 * PS * 4);    // [64][PS] lo
     const int et = threadIdx.x - 64;
     if (ep.kind == kEpiQKV) {
       // the rows' positions and KV blocks, read while the mainloop runs
@@ -413,11 +430,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      epi_prefetch<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      epi_prefetch<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
     } else if (ep.kind == kEpiResid) {
-      epi_prefetch<kEpiResid>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      epi_prefetch<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
     } else if (ep.kind == kEpiResidNorm) {
-      epi_prefetch<kEpiResidNorm>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      epi_prefetch<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
     }
     if (ep.ssq_in) {
       // fused RMSNorm: 1/rms of each row from the producer's partials; a
@@ -444,7 +461,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     const bool skip = decision != 0;
     tc::tc_fence_after();
-    auto load64 = [&](int c0, float (&v)[64]) {
+    // 64 columns per TMEM wait where two 32-column chunks remain, else 32
+    auto load64 = [&](int c0, bool two, float (&v)[64]) {
       if (skip) {
 #pragma unroll
         for (int j = 0; j < 64; ++j) v[j] = 0.f;
@@ -452,34 +470,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       uint32_t x0[32], x1[32];
       tc::tmem_ld32_nowait(taddr + c0, x0);
-      tc::tmem_ld32_nowait(taddr + c0 + 32, x1);
+      if (two) tc::tmem_ld32_nowait(taddr + c0 + 32, x1);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) { v[j] = __uint_as_float(x0[j]); v[32 + j] = __uint_as_float(x1[j]); }
+      for (int j = 0; j < 32; ++j) { v[j] = __uint_as_float(x0[j]); v[32 + j] = two ? __uint_as_float(x1[j]) : 0.f; }
     };
     if (lg >= 2 && has_rows) {
 #pragma unroll 1
       for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+        const bool two = c0 + 64 <= c_hi;
         float v[64];
-        load64(c0, v);
-        float4* lo = reinterpret_cast<float4*>(LO + rl * kTcPStride + c0);
+        load64(c0, two, v);
+        float4* lo = reinterpret_cast<float4*>(LO + rl * PS + c0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) lo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int j = 0; j < 16; ++j)
+          if (j < 8 || two) lo[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     if (lg < 2 && has_rows) {
 #pragma unroll 1
       for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+        const bool two = c0 + 64 <= c_hi;
         float v[64];
-        load64(c0, v);
-        const float4* lo = reinterpret_cast<const float4*>(LO + rl * kTcPStride + c0);
-        float4* p = reinterpret_cast<float4*>(P + rl * kTcPStride + c0);
+        load64(c0, two, v);
+        const float4* lo = reinterpret_cast<const float4*>(LO + rl * PS + c0);
+        float4* p = reinterpret_cast<float4*>(P + rl * PS + c0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float4 l4 = lo[j];
-          p[j] = make_float4(v[4 * j] + l4.x, v[4 * j + 1] + l4.y, v[4 * j + 2] + l4.z, v[4 * j + 3] + l4.w);
-        }
+        for (int j = 0; j < 16; ++j)
+          if (j < 8 || two) {
+            const float4 l4 = lo[j];
+            p[j] = make_float4(v[4 * j] + l4.x, v[4 * j + 1] + l4.y, v[4 * j + 2] + l4.z, v[4 * j + 3] + l4.w);
+          }
       }
     }
 #ifdef CBD_TRACE
@@ -499,13 +521,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;
     const int rows_here = min(kTcRows, a.n - nr * kTcRows);
     const uint32_t Pbase = tc::smem_u32(ring);
-    float* sq = reinterpret_cast<float*>(ring + 64 * kTcPStride * 4);   // the LO area, free after phase 1
+    float* sq = reinterpret_cast<float*>(ring + 64 * PS * 4);   // the LO area, free after phase 1
     switch (ep.kind) {
-      case kEpiQKV: epi_phase2<kEpiQKV>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiResid: epi_phase2<kEpiResid>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiResidNorm: epi_phase2<kEpiResidNorm>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      default: epi_phase2<kEpiLogits>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiQKV: epi_phase2<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResid: epi_phase2<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResidNorm: epi_phase2<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      default: epi_phase2<kEpiLogits, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
     }
   }
 #ifdef CBD_TRACE
@@ -522,7 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   TR_END((16u << 12) | (unsigned)(a.M >> 8));
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, kTcBN);
+    tc::tmem_dealloc(tmem, kTcMaxBN);
   }
 }
 
@@ -561,7 +583,9 @@ static int max_clusters(int S) {
   static int cache[kTcMaxCluster + 1] = {0};
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    for (auto k : {gemm_tc_kernel<256>, gemm_tc_kernel<224>, gemm_tc_kernel<192>, gemm_tc_kernel<160>,
+                   gemm_tc_kernel<128>})
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     for (int s = 1; s <= kTcMaxCluster; ++s) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(s * 64);
@@ -575,7 +599,7 @@ static int max_clusters(int S) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN>, &cfg) != cudaSuccess) n = 0;
       cache[s] = n;
     }
     cudaGetLastError();
@@ -599,19 +623,32 @@ static int choose_cluster(long long U, int KB) {
   return best;
 }
 
-void gemm_tc_plan(int M, int K, int n, int* T, int* NR, int* KB, int* S) {
-  *T = M / kTcBN;
+void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S) {
+  *T = M / N;
   *NR = (n + kTcRows - 1) / kTcRows;
   *KB = K / kTcBK;
   *S = choose_cluster((long long)*T * *NR, *KB);
 }
 
+// Weight rows per tile for an M x K matrix.  Measured on GB300 (7B decode
+// step): narrower tiles that let more CTAs stream (e.g. 128 rows, K split 4
+// ways, 128 CTAs instead of 96 for a 4096 x 4096 matrix) ran slower -- HBM
+// is already saturated while the weights stream, and the per-stage cost and
+// the activation traffic per weight byte grow as the tile narrows -- so the
+// widest tile that divides M is used.
+int gemm_tc_pick_tile(int M, int K) {
+  (void)K;
+  for (int N : {256, 224, 192, 160, 128})
+    if (M % N == 0) return N;
+  return kTcMaxBN;
+}
+
 cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  if (g.M % kTcBN || g.K % kTcBK) return cudaErrorInvalidValue;
+  if (g.M % g.N || g.K % kTcBK) return cudaErrorInvalidValue;
   TcArgs a{};
-  a.M = g.M; a.K = g.K; a.n = n;
-  gemm_tc_plan(g.M, g.K, n, &a.T, &a.NR, &a.KB, &a.S);
+  a.M = g.M; a.K = g.K; a.n = n; a.N = g.N;
+  gemm_tc_plan(g.M, g.K, g.N, n, &a.T, &a.NR, &a.KB, &a.S);
   a.err = ep.err;
   const long long U = (long long)a.T * a.NR;
   cudaLaunchConfig_t cfg = {};
@@ -633,7 +670,15 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, *g.w, *g.hi, *g.lo, a, ep, pf);
+  max_clusters(1);   // sets the kernels' shared-memory limit once
+  switch (g.N) {
+    case 256: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 224: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 192: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 160: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 128: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 CBD_TRACE_BIND(gemm_tc)

@@ -5,8 +5,8 @@
 // reads each weight once for all rows ("0.8MB 跑通 Qwen 第 14-1 篇", section 1;
 // "20.3 服务、批处理与流式" section 20.3.2, cost (W + B*A)/beta).
 //
-// Weights are read from the pre-tiled layout [M/256][K/64][256][64] that
-// the tensor-core path uses (16-byte chunks stay contiguous).
+// Weights are read from the pre-tiled layout [M/N][K/64][N][64] that the
+// tensor-core path uses (16-byte chunks stay contiguous).
 // CTA = 8 warps; a warp owns 4 consecutive output features, so RoPE and
 // SwiGLU partners (features 2i, 2i+1) live in one warp.  Activations for
 // the CTA's NB rows are staged in shared memory 256 columns at a time as
@@ -21,7 +21,7 @@ constexpr int kGemvFeat = 4;   // features per warp
 constexpr int kKTile = 256;    // k columns per shared-memory tile
 
 template <int NB>
-__global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ W, int M, int K,
+__global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ W, int M, int K, int TN,
                                                    const uint16_t* __restrict__ a_hi,
                                                    const uint16_t* __restrict__ a_lo, int lda, int n,
                                                    EpiArgs ep) {
@@ -57,8 +57,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
 #pragma unroll
       for (int i = 0; i < kGemvFeat; ++i) {
         const int f = f0 + i;
-        w[i] = __ldg(reinterpret_cast<const uint4*>(
-            W + ((((size_t)(f >> 8) * KB + (kk >> 6)) << 8) + (f & 255)) * 64 + (kk & 63)));
+        w[i] = __ldg(reinterpret_cast<const uint4*>(W + tiled_off(f, kk, TN, KB)));
       }
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
@@ -101,20 +100,20 @@ __global__ void __launch_bounds__(256) gemv_kernel(const uint16_t* __restrict__ 
   }
 }
 
-cudaError_t launch_gemv(const uint16_t* W, int M, int K, const uint16_t* a_hi, const uint16_t* a_lo,
+cudaError_t launch_gemv(const uint16_t* W, int M, int K, int TN, const uint16_t* a_hi, const uint16_t* a_lo,
                         int lda, int n, const EpiArgs& ep, cudaStream_t s) {
   const int feat_per_cta = kGemvWarps * kGemvFeat;
   dim3 block(32 * kGemvWarps);
   cudaError_t ce = cudaSuccess;
   if (n <= 1) {
-    ce = launch_pdl(gemv_kernel<1>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<1>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, TN, a_hi, a_lo, lda, n, ep);
   } else if (n <= 2) {
-    ce = launch_pdl(gemv_kernel<2>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<2>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, TN, a_hi, a_lo, lda, n, ep);
   } else if (n <= 4) {
-    ce = launch_pdl(gemv_kernel<4>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<4>, dim3((M + feat_per_cta - 1) / feat_per_cta, 1), block, 0, s, W, M, K, TN, a_hi, a_lo, lda, n, ep);
   } else {
     dim3 grid((M + feat_per_cta - 1) / feat_per_cta, (n + 7) / 8);
-    ce = launch_pdl(gemv_kernel<8>, grid, block, 0, s, W, M, K, a_hi, a_lo, lda, n, ep);
+    ce = launch_pdl(gemv_kernel<8>, grid, block, 0, s, W, M, K, TN, a_hi, a_lo, lda, n, ep);
   }
   return ce;
 }
@@ -125,9 +124,9 @@ static bool uses_tc(const cbd_engine* e, int n) {
   return e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
 }
 bool gemm_uses_tc(const cbd_engine* e, int n) { return uses_tc(e, n); }
-int gemm_tc_units(int M, int K, int n) {
+int gemm_tc_units(int M, int K, int N, int n) {
   int T, NR, KB, S;
-  gemm_tc_plan(M, K, n, &T, &NR, &KB, &S);
+  gemm_tc_plan(M, K, N, n, &T, &NR, &KB, &S);
   return T * S;
 }
 
@@ -135,21 +134,21 @@ cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiA
                         cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   if (uses_tc(e, n)) return launch_gemm_tc(op.tc, n, ep, pf, s);
-  return launch_gemv(op.W, op.M, op.K, op.a_hi, op.a_lo, op.lda, n, ep, s);
+  return launch_gemv(op.W, op.M, op.K, op.tc.N, op.a_hi, op.a_lo, op.lda, n, ep, s);
 }
 
 PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n) {
   PfSpec pf{};
   if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n)) return pf;
   int T, NR, KB, S;
-  gemm_tc_plan(op.tc.M, op.tc.K, n, &T, &NR, &KB, &S);
+  gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N, n, &T, &NR, &KB, &S);
   const long long units = (long long)T * S;
   const long long per_unit = (KB + S - 1) / S;
-  long long P = (long long)(e->l2_prefetch / kWTileBytes) / units;
+  long long P = (long long)(e->l2_prefetch / ((size_t)op.tc.N * 128)) / units;
   if (P < 1) P = 1;
   if (P > per_unit) P = per_unit;
   pf.w = reinterpret_cast<const uint8_t*>(op.W);
-  pf.T = T; pf.KB = KB; pf.S = S; pf.P = (int32_t)P;
+  pf.N = op.tc.N; pf.T = T; pf.KB = KB; pf.S = S; pf.P = (int32_t)P;
   return pf;
 }
 

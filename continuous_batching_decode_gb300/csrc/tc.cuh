@@ -84,8 +84,8 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 }
 
 // Issue share `part` of `nparts` of an upcoming GEMM's L2 prefetch (one
-// 32 KB weight tile per instruction, k-block-major so the first k-blocks of
-// every unit go first).  Called by one thread per part.
+// weight tile, N rows x 64 k, per instruction, k-block-major so the first
+// k-blocks of every unit go first).  Called by one thread per part.
 __device__ __forceinline__ void pf_issue(const PfSpec& pf, int part, int nparts) {
   if (!pf.w || pf.P <= 0) return;
   const long long units = (long long)pf.T * pf.S;
@@ -96,7 +96,8 @@ __device__ __forceinline__ void pf_issue(const PfSpec& pf, int part, int nparts)
     const int t = u / pf.S, r = u - t * pf.S;
     const int kb0 = r * pf.KB / pf.S, kb1 = (r + 1) * pf.KB / pf.S;
     if (kb0 + j >= kb1) continue;
-    prefetch_l2(pf.w + ((size_t)t * pf.KB + kb0 + j) * kWTileBytes, kWTileBytes);
+    const uint32_t tile = (uint32_t)pf.N * 128u;     // N rows x 64 k of bf16
+    prefetch_l2(pf.w + ((size_t)t * pf.KB + kb0 + j) * tile, tile);
   }
 }
 
