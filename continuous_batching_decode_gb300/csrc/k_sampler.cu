@@ -12,9 +12,11 @@
 //   the token is the first id, ascending, whose cumulative kept mass
 //   exceeds u times the kept total.  Then cnt *= decay; cnt[tok] += 1.
 //
-// One CTA of 1024 threads per sampled row; warp w owns a contiguous id
-// range walked in coalesced 32-id rounds, so id-ordered prefix sums are a
-// prefix over warps plus per-round warp scans.  Probability masses are
+// A cluster of kSC CTAs (1024 threads each) per sampled row: CTA rank r
+// owns ids [r*V/kSC, (r+1)*V/kSC) and its warp w a contiguous part of that,
+// walked in coalesced 32-id rounds, so id-ordered prefix sums are a prefix
+// over the cluster's CTAs (read over distributed shared memory, rank order)
+// plus one over warps plus per-round warp scans.  Probability masses are
 // fixed-point integers (exp(z - zmax) * 2^40), so every sum, threshold and
 // scan is exact and independent of thread timing; the k-th largest key and
 // the top-p cutoff are found by 8-bit radix selection over order-preserving
@@ -24,6 +26,7 @@
 namespace cbd {
 
 constexpr int kST = 1024;            // threads per sampler CTA
+constexpr int kSC = 4;               // CTAs (one cluster) per sampled row
 constexpr float kFix = 1099511627776.0f;   // 2^40 (exact in fp32)
 
 // Philox-4x32-10 (Salmon et al., SC'11): 10 rounds of the 4x32 bijection
@@ -83,13 +86,87 @@ struct SampShared {
   unsigned long long wsum[32];
   uint32_t wkey[32];
   int32_t widx[32];
-  unsigned long long hm[256];
+  unsigned long long hm[256];        // this CTA's histogram
   uint32_t hc[256];
+  unsigned long long chm[256];       // the cluster's histogram (rank order sum)
+  uint32_t chc[256];
   uint32_t sel_prefix, sel_mask;
   unsigned long long sel_above, sel_rem;
   int32_t tok;
   int32_t cut_id;
+  unsigned long long cx;             // a value this CTA shares with its cluster
+  uint32_t ckey;
+  int32_t cidx;
 };
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ void csync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t crank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cmap(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ unsigned long long cld_u64(const unsigned long long* p, uint32_t rank) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cmap(p, rank)) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t cld_u32(const void* p, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cmap(p, rank)) : "memory");
+  return v;
+}
+// Every CTA of the cluster contributes x (thread 0's value counts); all
+// threads get the sum over lower ranks and the cluster total (rank order).
+__device__ __forceinline__ void cluster_scan(unsigned long long x, SampShared& sh, uint32_t my,
+                                             unsigned long long* before, unsigned long long* total) {
+  if (threadIdx.x == 0) sh.cx = x;
+  csync();
+  unsigned long long b = 0, t = 0;
+#pragma unroll
+  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
+    const unsigned long long v = cld_u64(&sh.cx, r);
+    if (r < my) b += v;
+    t += v;
+  }
+  csync();      // every peer has read sh.cx before it is written again
+  *before = b;
+  *total = t;
+}
+// The cluster's histogram: each CTA's sh.hc (and sh.hm when `masses`) summed
+// bin by bin in rank order into sh.chc / sh.chm (every CTA the same).
+__device__ __forceinline__ void cluster_hist(SampShared& sh, bool masses) {
+  csync();
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) {
+    uint32_t c = 0;
+    unsigned long long mm = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
+      c += cld_u32(&sh.hc[b], r);
+      if (masses) mm += cld_u64(&sh.hm[b], r);
+    }
+    sh.chc[b] = c;
+    sh.chm[b] = mm;
+  }
+  csync();
+}
+// Smallest of one int per CTA (e.g. a token id found by one of them).
+__device__ __forceinline__ int32_t cluster_min_i32(int32_t x, SampShared& sh) {
+  if (threadIdx.x == 0) sh.cidx = x;
+  csync();
+  int32_t m = 0x7fffffff;
+#pragma unroll
+  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) m = min(m, (int32_t)cld_u32(&sh.cidx, r));
+  csync();
+  return m;
+}
 
 // Warp w owns the contiguous ids [w*PW, (w+1)*PW) and walks them in
 // rounds of 32 consecutive ids (lane = offset), so every load is coalesced
@@ -162,14 +239,17 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   uint32_t* whc = reinterpret_cast<uint32_t*>(whm + (kST / 32) * kHistBins);       // [32][256] counts
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int row = blockIdx.x / kSC, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint32_t my = crank();
   const SampDev sp = samp[row];
   const float* lg = logits + (size_t)row * V;
   float* cnt = counters + (size_t)slots[row] * V;
   float* z = scratch + (size_t)row * V;
-  const int PW = ((V + 32 * 32 - 1) / (32 * 32)) * 32;   // ids per warp, a multiple of 32
-  const int v0 = w * PW;
-  const int v1 = min(V, v0 + PW);
+  // this CTA's ids [c0, c1); warp w's part of them [v0, v1)
+  const int c0 = (int)((long long)V * my / kSC), c1 = (int)((long long)V * (my + 1) / kSC);
+  const int PW = ((c1 - c0 + 32 * 32 - 1) / (32 * 32)) * 32;   // ids per warp, a multiple of 32
+  const int v0 = min(c1, c0 + w * PW);
+  const int v1 = min(c1, v0 + PW);
   const bool greedy = sp.temperature == 0.0f || sp.top_k == 1;
   const unsigned lt_mask = (1u << lane) - 1u;
 
@@ -214,9 +294,21 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (oi != 0x7fffffff && (bi == 0x7fffffff || ok > bk || (ok == bk && oi < bi))) { bk = ok; bi = oi; }
     }
-    if (lane == 0) sh.tok = bi;
+    if (lane == 0) { sh.ckey = bk; sh.cidx = bi; }
   }
-  __syncthreads();
+  // the cluster's best: key desc, then lowest id (rank order)
+  csync();
+  if (tid == 0) {
+    uint32_t k = 0;
+    int32_t idx = 0x7fffffff;
+    for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
+      const uint32_t ok = cld_u32(&sh.ckey, r);
+      const int32_t oi = (int32_t)cld_u32(&sh.cidx, r);
+      if (oi != 0x7fffffff && (idx == 0x7fffffff || ok > k || (ok == k && oi < idx))) { k = ok; idx = oi; }
+    }
+    sh.tok = idx;
+  }
+  csync();
 
   if (!greedy) {
     const float zmax = z[sh.tok];
@@ -239,13 +331,13 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
           for (int ww = 0; ww < kST / 32; ++ww) c += whc[ww * kHistBins + b];
           sh.hc[b] = c;
         }
-        __syncthreads();
+        cluster_hist(sh, false);
         if (tid == 0) {
           unsigned long long cum = 0;
           int d = 255;
           for (; d > 0; --d) {
-            if (cum + sh.hc[d] >= rem) break;
-            cum += sh.hc[d];
+            if (cum + sh.chc[d] >= rem) break;
+            cum += sh.chc[d];
           }
           sh.sel_rem = rem - cum;
           sh.sel_prefix = prefix | ((uint32_t)d << shift);
@@ -261,8 +353,10 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       // rank among equal keys in id order
       unsigned long long eq = 0;
       for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { eq += valid && ord_key(zv) == tk; });
-      unsigned long long tot;
+      unsigned long long tot, cbefore, ctot;
       unsigned long long base = warp_prefix(warp_sum_u64(eq), sh, &tot);
+      cluster_scan(tot, sh, my, &cbefore, &ctot);
+      base += cbefore;
       for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
         const uint32_t k = valid ? ord_key(zv) : 0u;
         const unsigned bal = __ballot_sync(0xffffffffu, valid && k == tk);
@@ -288,8 +382,9 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     if (sp.top_p < 1.0f) {
       unsigned long long mine = 0;
       for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += mass(zv); });
-      unsigned long long S;
+      unsigned long long S, Sb;
       (void)warp_prefix(warp_sum_u64(mine), sh, &S);
+      cluster_scan(S, sh, my, &Sb, &S);
       // cumulative mass >= top_p * S  <=>  cumulative >= ceil(top_p * S)
       const unsigned long long target = (unsigned long long)ceil((double)sp.top_p * (double)S);
       if (S >= target) {
@@ -316,14 +411,14 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
             sh.hc[b] = c;
             sh.hm[b] = mm;
           }
-          __syncthreads();
+          cluster_hist(sh, true);
           if (tid == 0) {
             int d = 255, last = -1;
             for (; d >= 0; --d) {
-              if (sh.hc[d] == 0) continue;
+              if (sh.chc[d] == 0) continue;
               last = d;
-              if (above + sh.hm[d] >= target) break;
-              above += sh.hm[d];
+              if (above + sh.chm[d] >= target) break;
+              above += sh.chm[d];
             }
             if (d < 0) d = last;        // rounding: take the lowest non-empty digit
             sh.sel_rem = above;
@@ -341,8 +436,10 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
           if (valid && zv != -INFINITY && ord_key(zv) == tp) eqm += mass(zv);
         });
-        unsigned long long tot;
-        const unsigned long long wbase = warp_prefix(warp_sum_u64(eqm), sh, &tot);
+        unsigned long long tot, cbefore, ctot;
+        const unsigned long long wbase0 = warp_prefix(warp_sum_u64(eqm), sh, &tot);
+        cluster_scan(tot, sh, my, &cbefore, &ctot);
+        const unsigned long long wbase = wbase0 + cbefore;
         const unsigned long long wtot = warp_sum_u64(eqm);
         if (tid == 0) sh.cut_id = 0x7fffffff;
         __syncthreads();
@@ -364,7 +461,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
           });
         }
         __syncthreads();
-        cut_id = sh.cut_id;
+        cut_id = cluster_min_i32(sh.cut_id, sh);
         if (cut_id == 0x7fffffff) cut_id = V;   // rounding: keep every element of the tie group
       }
     }
@@ -385,8 +482,10 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     unsigned long long mine = 0;
     for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += kept_mass_z(v, zv); });
     const unsigned long long wtot = warp_sum_u64(mine);
-    unsigned long long Sk;
-    const unsigned long long wbase = warp_prefix(wtot, sh, &Sk);
+    unsigned long long Sk, cbefore;
+    const unsigned long long wbase0 = warp_prefix(wtot, sh, &Sk);
+    cluster_scan(Sk, sh, my, &cbefore, &Sk);
+    const unsigned long long wbase = wbase0 + cbefore;
     const unsigned long long T = (unsigned long long)floor((double)u * (double)Sk);
     if (tid == 0) sh.tok = 0x7fffffff;
     __syncthreads();
@@ -407,18 +506,24 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       });
     }
     __syncthreads();
-    if (sh.tok == 0x7fffffff) {
-      if (tid == 0) { set_err(err, kDevSampler); sh.tok = 0; }
-      __syncthreads();
+    const int32_t found = cluster_min_i32(sh.tok, sh);
+    if (tid == 0) {
+      sh.tok = found;
+      if (found == 0x7fffffff) {
+        if (my == 0) set_err(err, kDevSampler);
+        sh.tok = 0;
+      }
     }
+    __syncthreads();
   }
-  // 6. counters: decay everything, then count the drawn token
+  // 6. counters: every CTA decays its ids, then the drawn token's owner
+  //    counts it
   const int tok = sh.tok;
   for_each_id(cnt, v0, v1, lane, [&](int v, bool valid, float c) { if (valid) cnt[v] = __fmul_rn(c, sp.decay); });
   __syncthreads();
   if (tid == 0) {
-    cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
-    out[row] = tok;
+    if (tok >= c0 && tok < c1) cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
+    if (my == 0) out[row] = tok;
   }
 }
 
@@ -433,8 +538,21 @@ cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, c
     if (ce != cudaSuccess) return ce;
     attr = true;
   }
-  return launch_pdl(sampler_kernel, dim3(m), dim3(kST), kSampDynSmem, s, logits, V, counters, slots, samp, scratch,
-                    out_tokens, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m * kSC);
+  cfg.blockDim = dim3(kST);
+  cfg.dynamicSmemBytes = kSampDynSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = kSC;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, sampler_kernel, logits, V, counters, slots, samp, scratch, out_tokens, err);
 }
 
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
