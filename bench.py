@@ -60,7 +60,7 @@ def parse():
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
-    ap.add_argument("--l2-prefetch-mb", type=int, default=48,
+    ap.add_argument("--l2-prefetch-mb", type=int, default=0,
                     help="MiB of the next weight contraction each kernel prefetches into L2 (0: off)")
     return ap.parse_args()
 

@@ -163,7 +163,7 @@ struct cbd_engine {
   cbd::TcWork tcw{};
   int tile_qkv = 256, tile_o = 256, tile_gu = 256, tile_dn = 256, tile_lm = 256;   // weight tile widths
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
-  size_t l2_prefetch = 48u << 20;     // bytes of the next GEMM's weights each kernel prefetches to L2
+  size_t l2_prefetch = 0;             // bytes of the next GEMM's weights each kernel prefetches to L2 (off)
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores

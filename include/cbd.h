@@ -149,11 +149,13 @@ cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable);
 
 /* L2 prefetch across kernel boundaries: once a kernel of the step has issued
  * its last load, it asks L2 to fetch the first k-blocks of the next weight
- * contraction's work units, up to `bytes` in all (default 48 MiB; 0 turns
- * it off), so HBM keeps streaming while one launch drains and the next
- * starts ("20.3 服务、批处理与流式", 20.3.2: a decode step costs
- * (W + B*A)/beta, so every idle HBM cycle is lost throughput).  A prefetch
- * is a cache hint only: results are identical with any setting.
+ * contraction's work units, up to `bytes` in all, so HBM could keep
+ * streaming while one launch drains and the next starts ("20.3 服务、批处理
+ * 与流式", 20.3.2: a decode step costs (W + B*A)/beta).  Default 0 (off):
+ * on GB300 the prefetched lines were largely not found by the next kernel's
+ * copies, so the prefetch added DRAM reads and slowed the 7B step (5.11 ms
+ * off, 5.20 ms at 16 MiB, 5.33 ms at 48 MiB).  A prefetch is a cache hint
+ * only: results are identical with any setting.
  * Errors: CBD_EINVAL for a NULL engine or more than 1 GiB. */
 cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes);
 
