@@ -453,9 +453,11 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
     return o;
   };
   // Tasks are handed out dynamically: every warp starts with task gw; later
-  // tasks come from the per-launch counter (nwarps + ticket).  Nothing the
-  // warp waits for per block or per task is a global-memory round trip:
-  // tickets are taken two tasks ahead, records loaded one task ahead, block
+  // tasks come from the per-launch counter (nwarps + ticket).  A warp holds
+  // at most one claimed task beyond the one it is issuing (more would leave
+  // whole tasks stranded on some warps at the end), and almost nothing it
+  // waits for is a global-memory round trip: the next ticket is claimed when
+  // a task starts issuing, its record is loaded at the next copy issue, block
   // ids come with the record, and the next task's query is prefetched into
   // registers.  Which warp computes a task does not change its result.
   // Producer (lane 0 issues the copies; all lanes track the cursor).  The
@@ -466,8 +468,10 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
   uint32_t p_q = 0;
   bool pf_sent = false;
   int q_head = 0, q_tail = 0;              // tasks pushed / popped (warp-uniform)
-  int n1 = n_tasks, n2 = n_tasks;          // lane 0: next task id, the one after it (ticket in flight)
-  Rec r1{};                                // lane 0: record of n1 (load in flight)
+  int n1 = n_tasks;                        // lane 0: next task id (ticket claimed)
+  bool r1_pending = false;                 // its record still to be loaded (warp-uniform)
+  bool lazy = false;                       // near the end: claim at the switch, not ahead
+  Rec r1{};                                // lane 0: record of n1
   auto push = [&](int t, const Rec& r) {
     if (lane == 0) {
       int4* e = reinterpret_cast<int4*>(&tq[warp][q_head % QN][0]);
@@ -483,6 +487,13 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
       if (!pf_sent && lane == 0) tc::pf_issue(pf, gw, nwarps);
       pf_sent = true;
       return;
+    }
+    if (r1_pending) {                      // the ticket claimed at the last task switch has arrived by now
+      if (lane == 0 && n1 < n_tasks) r1 = load_rec(n1);
+      r1_pending = false;
+      // fewer tickets left than warps: stop claiming ahead, so no warp sits
+      // on a task another warp could have run
+      lazy = __shfl_sync(0xffffffffu, n1, 0) + nwarps >= n_tasks;
     }
     const int s = p_q % NS;
     if (lane == 0) {
@@ -500,14 +511,26 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
     p_half = 0;
     if (++p_blk == (pr.end - pr.start + 31) >> 5) {
       p_blk = 0;
+      if (lazy && !r1_pending && n1 == -1) {
+        // claim now (the warp waits two memory round trips, only at the end)
+        if (lane == 0) {
+          n1 = nwarps + atomicAdd(next_task, 1);
+          if (n1 < n_tasks) r1 = load_rec(n1);
+        }
+      }
       p_task = __shfl_sync(0xffffffffu, n1, 0);
       if (p_task < n_tasks) {
+        if (r1_pending) {                  // a one-block task: the record was not loaded yet
+          if (lane == 0) r1 = load_rec(n1);
+          r1_pending = false;
+        }
         pr = shfl_rec(r1);
         push(p_task, pr);
-        if (lane == 0) {
-          n1 = n2;
-          if (n1 < n_tasks) r1 = load_rec(n1);
-          n2 = nwarps + atomicAdd(next_task, 1);
+        if (!lazy) {
+          if (lane == 0) n1 = nwarps + atomicAdd(next_task, 1);
+          r1_pending = true;
+        } else {
+          n1 = -1;                         // nothing claimed ahead
         }
       }
     }
@@ -515,18 +538,25 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
   pdl_wait();
   TR_MARK1;
   if (p_task < n_tasks) {
-    if (lane == 0) {
-      n1 = nwarps + atomicAdd(next_task, 1);
-      n2 = nwarps + atomicAdd(next_task, 1);
-    }
+    if (lane == 0) n1 = nwarps + atomicAdd(next_task, 1);
     pr = load_rec(p_task);
     push(p_task, pr);
-    if (lane == 0 && n1 < n_tasks) r1 = load_rec(n1);
+    r1_pending = true;
   }
   for (int i = 0; i < NS; ++i) issue_next();
 
-  const float scale = 1.0f / sqrtf((float)HD);
+  // Scores in log2 units: q is pre-scaled by log2(e) / sqrt(hd) and the
+  // softmax uses exp2 (partials' maxima are log2-scaled for the merge).
+  const float scale = 1.4426950408889634f / sqrtf((float)HD);
   const int mi = lane >> 3, ri = lane & 7;
+  // With G <= 4 the MMA's 8 columns hold q hi (columns 0-3) and q lo
+  // (columns 4-7) of the group's heads, so one MMA does both halves; column
+  // n of a fragment is lane group gid = n: head gid & 3, half gid >> 2.
+  // A head's hi and lo sums then sit in lanes tid4 and tid4 ^ 2.  With
+  // G = 8, hi and lo take one MMA each.
+  constexpr bool PK = G <= 4;
+  const int qhead = PK ? (gid & 3) : gid;   // head whose q / P this lane's fragment column carries
+  const bool qlo = PK && gid >= 4;          // ... and which half
   uint32_t c_q = 0;
   bool alive = true;
   // the next task's query (raw fp32, this lane's fragment elements)
@@ -539,8 +569,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int dd = ks * 16 + r * 8 + tid4 * 2;
-        if (gid < G) {
-          const float2 v = *reinterpret_cast<const float2*>(qrow + gid * HD + dd);
+        if (qhead < G) {
+          const float2 v = *reinterpret_cast<const float2*>(qrow + qhead * HD + dd);
           d[ks][r][0] = v.x;
           d[ks][r][1] = v.y;
         } else {
@@ -559,12 +589,18 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
     } tk{e0.x, e0.y, e0.z, e0.w, e1.x, (e0.z - e0.y + 31) >> 5, e1.z};
     if (!qn_valid) load_q(tk.row, tk.kvh, qn);
     qn_valid = false;
-    // q of the group's heads (scaled) as hi / lo B fragments
+    // q of the group's heads (scaled) as B fragments: packed hi | lo, or
+    // separate hi and lo
     uint32_t qh[KS][2], ql[KS][2];
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) split_pack(qn[ks][r][0] * scale, qn[ks][r][1] * scale, qh[ks][r], ql[ks][r]);
+      for (int r = 0; r < 2; ++r) {
+        uint32_t h, l;
+        split_pack(qn[ks][r][0] * scale, qn[ks][r][1] * scale, h, l);
+        qh[ks][r] = PK ? (qlo ? l : h) : h;
+        ql[ks][r] = l;
+      }
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float o[KS][4];
 #pragma unroll
@@ -577,14 +613,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
       int s = c_q % NS;
       if (!tc::mbar_wait(&bar[warp][s], (c_q / NS) & 1, err, &abort_flag)) { alive = false; break; }
       const uint32_t ks_base = tc::smem_u32(ring + s * TILE);
-      // q.K over 8 independent accumulator chains (m-tile x hi/lo x k
+      // q.K over independent accumulator chains (m-tile x [hi/lo] x k
       // parity) so consecutive MMAs never wait on each other; summed in a
       // fixed order afterwards
-      float acc[2][2][2][4];
+      constexpr int HL = PK ? 1 : 2;
+      float acc[2][HL][2][4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int hl = 0; hl < 2; ++hl)
+        for (int hl = 0; hl < HL; ++hl)
 #pragma unroll
           for (int par = 0; par < 2; ++par)
 #pragma unroll
@@ -601,9 +638,11 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
           mma_bf16_16816(acc[mt][0][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], qh[ks][0], qh[ks][1]);
+        if constexpr (!PK) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-          mma_bf16_16816(acc[mt][1][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], ql[ks][0], ql[ks][1]);
+          for (int mt = 0; mt < 2; ++mt)
+            mma_bf16_16816(acc[mt][HL - 1][ks & 1], a[mt][0], a[mt][1], a[mt][2], a[mt][3], ql[ks][0], ql[ks][1]);
+        }
       }
       __syncwarp();          // every lane's K fragments are in registers
       issue_next();          // refill the K slot NS copies ahead
@@ -612,8 +651,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          sc[mt][c] = (acc[mt][0][0][c] + acc[mt][0][1][c]) + (acc[mt][1][0][c] + acc[mt][1][1][c]);
+        for (int c = 0; c < 4; ++c) {
+          if constexpr (PK) {
+            // this lane's column half plus the other half (lane ^ 2)
+            const float own = acc[mt][0][0][c] + acc[mt][0][1][c];
+            sc[mt][c] = own + __shfl_xor_sync(0xffffffffu, own, 2);
+          } else {
+            sc[mt][c] = (acc[mt][0][0][c] + acc[mt][0][1][c]) + (acc[mt][HL - 1][0][c] + acc[mt][HL - 1][1][c]);
+          }
+        }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float v[4] = {sc[0][hh], sc[0][hh + 2], sc[1][hh], sc[1][hh + 2]};
@@ -629,16 +675,17 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
         const float mn = fmaxf(m[hh], bm);
         float bs = 0.f;
+        const int head = (PK ? (tid4 & 1) : tid4) * 2 + hh;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float pv = pos[i] < nvalid ? expf(v[i] - mn) : 0.f;
+          const float pv = pos[i] < nvalid ? exp2f(v[i] - mn) : 0.f;
           bs += pv;
-          Pw[(tid4 * 2 + hh) * 32 + pos[i]] = pv;
+          if (!PK || tid4 < 2) Pw[head * 32 + pos[i]] = pv;
         }
         bs += __shfl_xor_sync(0xffffffffu, bs, 4);
         bs += __shfl_xor_sync(0xffffffffu, bs, 8);
         bs += __shfl_xor_sync(0xffffffffu, bs, 16);
-        const float corr = m[hh] == -INFINITY ? 0.f : expf(m[hh] - mn);
+        const float corr = m[hh] == -INFINITY ? 0.f : exp2f(m[hh] - mn);
         l[hh] = l[hh] * corr + bs;
         m[hh] = mn;
 #pragma unroll
@@ -654,7 +701,10 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int j = k2 * 16 + r * 8 + tid4 * 2;
-          split_pack(Pw[gid * 32 + j], Pw[gid * 32 + j + 1], ph[k2][r], pl[k2][r]);
+          uint32_t h = 0, lo = 0;
+          if (qhead < G) split_pack(Pw[qhead * 32 + j], Pw[qhead * 32 + j + 1], h, lo);
+          ph[k2][r] = PK ? (qlo ? lo : h) : h;
+          pl[k2][r] = lo;
         }
       // ---- V tile of block b (rows past the valid positions may hold stale
       // bits: zero them, P is 0 there)
@@ -680,8 +730,11 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
         }
 #pragma unroll
         for (int dt = 0; dt < KS; ++dt) mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], ph[k2][0], ph[k2][1]);
+        if constexpr (!PK) {
 #pragma unroll
-        for (int dt = 0; dt < KS; ++dt) mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], pl[k2][0], pl[k2][1]);
+          for (int dt = 0; dt < KS; ++dt)
+            mma_bf16_16816(o[dt], a[dt][0], a[dt][1], a[dt][2], a[dt][3], pl[k2][0], pl[k2][1]);
+        }
       }
       __syncwarp();          // every lane is done with the V slot (and Pw)
       issue_next();          // refill it NS copies ahead
@@ -694,6 +747,13 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
         qn_valid = true;
       }
     }
+    if constexpr (PK) {
+      // each head's output is its hi-column sum plus its lo-column sum
+#pragma unroll
+      for (int dt = 0; dt < KS; ++dt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[dt][c] += __shfl_xor_sync(0xffffffffu, o[dt][c], 2);
+    }
     if (!alive) break;
     // the row's chunks are consecutive work items, this one is chunk start / 128
     const int nch = tk.nch, w0 = tk.wi - tk.start / kAttnChunk;
@@ -705,7 +765,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int head = tid4 * 2 + (c & 1);
-          if (head < G) {
+          if (head < G && (!PK || tid4 < 2)) {
             const int dim = dt * 16 + gid + (c >= 2 ? 8 : 0);
             uint16_t hi, lo;
             split_bf16(o[dt][c] / l[c & 1], hi, lo);
@@ -722,12 +782,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int head = tid4 * 2 + (c & 1);
-        if (head < G) {
+        if (head < G && (!PK || tid4 < 2)) {
           const int dim = dt * 16 + gid + (c >= 2 ? 8 : 0);
           part_o[(((size_t)tk.wi * hq + tk.kvh * G + head) * HD) + dim] = o[dt][c];
         }
       }
-    if (gid == 0) {
+    if (gid == 0 && (!PK || tid4 < 2)) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int head = tid4 * 2 + hh;
@@ -754,13 +814,14 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
 }
 
 // Merge the chunk partials of one (row, KV head) for the group's G heads,
-// in chunk order: M = max of the chunk maxima, L = sum_c l_c e^(m_c - M),
+// in chunk order: M = max of the chunk maxima, L = sum_c l_c e^(m_c - M)
+// (2^(m_c - M) when the maxima are in log2 units, LOG2),
 // O = sum_c o_c e^(m_c - M), output O / L as hi + lo bf16.  One CTA of
 // G * HD / 4 threads per (row, KV head), each thread owning 4 dims of one
 // head.  The (max, sum) pairs of all chunks are staged in shared memory in
 // one pass; the partial outputs are independent loads, issued 8 chunks at
 // a time.  Rows with a single chunk were finished by the attention kernel.
-template <int HD, int G>
+template <int HD, int G, bool LOG2>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                     const int32_t* __restrict__ row_work, int hq, int skip_single,
                                     uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo) {
@@ -797,7 +858,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
     for (int j = 0; j < CB; ++j)
       if (c0 + j < nch) {
         const float2 ml = sml[(c0 + j) * G + g];
-        const float sc = expf(ml.x - M);
+        const float sc = LOG2 ? exp2f(ml.x - M) : expf(ml.x - M);
         L += ml.y * sc;
         O.x += v[j].x * sc; O.y += v[j].y * sc; O.z += v[j].z * sc; O.w += v[j].w * sc;
       }
@@ -854,15 +915,16 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     if (ce != cudaSuccess) return ce;
   }
   // single-chunk rows: the streaming kernel wrote them; the others write partials only
+  // the streaming kernel keeps its maxima in log2 units (exp2 softmax)
   const size_t csmem = (size_t)b->max_chunks * G * sizeof(float2);
+  auto combine = e->attn_path == 0 ? attn_combine_kernel<HD, G, true> : attn_combine_kernel<HD, G, false>;
   if (csmem > 48 * 1024) {
-    cudaError_t ce = cudaFuncSetAttribute(attn_combine_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)csmem);
+    cudaError_t ce = cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     if (ce != cudaSuccess) return ce;
   }
-  return launch_pdl(attn_combine_kernel<HD, G>, dim3(b->n_rows, dm.hkv), dim3(G * HD / 4), csmem, s,
-                    (const float*)e->attn_o, (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq,
-                    e->attn_path == 0 ? 1 : 0, e->act_hi, e->act_lo);
+  return launch_pdl(combine, dim3(b->n_rows, dm.hkv), dim3(G * HD / 4), csmem, s, (const float*)e->attn_o,
+                    (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq, e->attn_path == 0 ? 1 : 0,
+                    e->act_hi, e->act_lo);
 }
 
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
