@@ -191,6 +191,29 @@ def kernel_bytes(cls, s, B, ctx):
     return None
 
 
+def measured_traffic(cls, args):
+    """DRAM bytes per launch of a kernel class from a committed ncu summary
+    under profiles/ (dram__bytes_read + dram__bytes_write), when it was taken
+    on this workload and the kernel's source is unchanged since; else None."""
+    import hashlib
+    files = {"attention": ("attn_stream_7b_B32_2layer.md", "k_attn.cu")}
+    if cls not in files or (args.shape, args.B, args.ctx_lo, args.ctx_hi, args.seed) != ("7b", 32, 256, 4096, 0):
+        return None
+    prof, src = files[cls]
+    try:
+        text = open(os.path.join(ROOT, "profiles", prof)).read()
+        cur = hashlib.sha256(open(os.path.join(ROOT, "continuous_batching_decode_gb300", "csrc", src), "rb").read())
+    except OSError:
+        return None
+    val = sha = None
+    for line in text.splitlines():
+        if line.startswith("traffic_per_launch_bytes:"):
+            val = int(line.split(":")[1])
+        if line.startswith(f"source_sha256 {src}:"):
+            sha = line.split(":")[1].strip()
+    return val if val is not None and sha == cur.hexdigest() else None
+
+
 def oracle_sample(s, B, ctx, toks, kv_source, weights_l0, seed, min_s=0.0):
     """Time the CPU oracle on one layer of the step (all B rows) plus the LM
     head; returns (seconds for a full step, details)."""
@@ -369,7 +392,7 @@ def run_cbd(args):
             avg_s = tot / n_l / 1000.0
             ach = byt / avg_s / 1e9
             roof = {"kernel": k, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(ach / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                    "frac": round(ach / peak, 4), "traffic": measured_traffic(k, args), "peak_kind": peak_kind,
                     "bytes_per_launch": byt, "avg_launch_us": round(avg_s * 1e6, 2)}
             break
     W = weight_bytes(s)
