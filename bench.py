@@ -307,7 +307,7 @@ def run_reference(args):
 def run_cbd(args):
     import torch
     import continuous_batching_decode_gb300 as cbd
-    from continuous_batching_decode_gb300 import build, synth
+    from continuous_batching_decode_gb300 import build, replicas, synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -366,13 +366,11 @@ def run_cbd(args):
     if dist:
         dist.barrier()
     clocks = clk.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms_local = ev0.elapsed_time(ev1) / args.steps
     cbd.engine_check(e)
-    value = B * world / (ms / 1000.0)
+    # replicas: the units all ranks processed / the slowest rank's time
+    ms = replicas.max_over_ranks(ms_local, dist, "cuda")
+    value = replicas.job_throughput(float(B), ms_local / 1000.0, dist, "cuda")
     launches = cbd.batch_launches(b) * args.steps
 
     # per-kernel live timing (same batch, same stream, CUDA events per launch)
@@ -425,11 +423,7 @@ def run_cbd(args):
         ev1.record(stream)
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) / args.steps * 1000.0
-        e_ms = max(ev0.elapsed_time(ev1) / args.steps, wall)
-        if dist:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = replicas.max_over_ranks(max(ev0.elapsed_time(ev1) / args.steps, wall), dist, "cuda")
         h2d = len(wl["rows"]) * 20 + wl["tables"].nbytes + wl["nbps"].nbytes + len(wl["samp"]) * 48
         e2e = {"value": B * world / (e_ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": B * 4, "ms_per_step": round(e_ms, 4)}
