@@ -53,33 +53,30 @@ __device__ __forceinline__ uint32_t ord_key(float f) {
 
 // Radix histograms: every warp owns a private [256] count and mass
 // histogram in dynamic shared memory; the block then sums them bin by bin
-// in warp order.  A warp updates its histogram one digit group at a time:
-// the lanes holding the same digit are found with a ballot, their count is
-// a popcount and their mass a warp reduction, and only the group's leader
-// lane writes -- no atomics, and in the early passes (where almost every
-// element falls in one or two bins) one update per round instead of 32.
+// in warp order (and the cluster over its CTAs in rank order).
 constexpr int kHistBins = 256;
 constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * (sizeof(uint32_t) + sizeof(unsigned long long));
 
-// Add the participating lanes' (digit, mass) to this warp's histogram.
+// Add the participating lanes' (digit, mass) to this warp's histogram: the
+// lanes holding the same digit are one match group; its count is a popcount
+// and its mass a reduction over the group's own mask, and only the group's
+// leader lane writes (groups have distinct digits, and every warp owns its
+// histogram) -- no atomics, one round of instructions however many digits
+// the 32 lanes hold.
 __device__ __forceinline__ void warp_hist_add(bool part, uint32_t dg, unsigned long long mv, uint32_t* hc,
                                               unsigned long long* hm, int lane) {
-  unsigned active = __ballot_sync(0xffffffffu, part);
-  while (active) {
-    const int leader = __ffs(active) - 1;
-    const uint32_t d = __shfl_sync(0xffffffffu, dg, leader);
-    const bool mine = part && dg == d;
-    const unsigned grp = __ballot_sync(0xffffffffu, mine);
-    if (hm) {
-      // masses < 2^41: sum the low 20 bits and the rest separately (each sum
-      // of at most 32 lanes fits 32 bits)
-      const uint32_t slo = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)(mv & 0xFFFFFull) : 0u);
-      const uint32_t shi = __reduce_add_sync(0xffffffffu, mine ? (uint32_t)(mv >> 20) : 0u);
-      if (lane == leader) hm[d] += ((unsigned long long)shi << 20) + slo;
-    }
-    if (lane == leader) hc[d] += __popc(grp);
-    active &= ~grp;
+  const unsigned act = __ballot_sync(0xffffffffu, part);
+  if (!part) return;
+  const unsigned grp = __match_any_sync(act, dg);
+  const bool leader = lane == __ffs(grp) - 1;
+  if (hm) {
+    // masses < 2^41: sum the low 20 bits and the rest separately (each sum
+    // of at most 32 lanes fits 32 bits)
+    const uint32_t slo = __reduce_add_sync(grp, (uint32_t)(mv & 0xFFFFFull));
+    const uint32_t shi = __reduce_add_sync(grp, (uint32_t)(mv >> 20));
+    if (leader) hm[dg] += ((unsigned long long)shi << 20) + slo;
   }
+  if (leader) hc[dg] += __popc(grp);
 }
 
 struct SampShared {
