@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
   __syncthreads();
   const int hq = hkv * G;
   const int gw = blockIdx.x * kStreamWarps + warp, nwarps = gridDim.x * kStreamWarps;
+  const uint64_t kv_policy = tc::policy_evict_first();   // each K/V tile is read once per step
   // A task is one 128-position chunk (work item wi) for one KV head; its
   // record (row, positions, physical blocks) was built on the host.
   struct Rec {
@@ -500,8 +501,8 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
       int blk = p_blk == 0 ? pr.b0 : p_blk == 1 ? pr.b1 : p_blk == 2 ? pr.b2 : pr.b3;
       if (blk < 0 || blk >= n_blocks) { set_err(err, kDevBadBlock); blk = 0; }
       tc::mbar_arrive_expect_tx(&bar[warp][s], TILE);
-      tc::bulk_load(ring + s * TILE, pool + pool_tile(layer, n_blocks, blk, hkv, pr.kvh, p_half, HD), TILE,
-                    &bar[warp][s]);
+      tc::bulk_load_hint(ring + s * TILE, pool + pool_tile(layer, n_blocks, blk, hkv, pr.kvh, p_half, HD), TILE,
+                         &bar[warp][s], kv_policy);
     }
     ++p_q;
     if (p_half == 0) {

@@ -340,11 +340,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // land in TMEM lanes the epilogue never reads
       const int nbox = (min(kTcRows, a.n - nr * kTcRows) + 15) / 16;
       const uint32_t stage_tx = w_bytes + 2u * nbox * 2048u;
+      const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
       auto issue_w = [&](int q) {
         const int s = q % ST;
         uint8_t* st = ring + (size_t)s * stage_bytes;
         tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
-        tc::tma_load_2d(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s]);
+        tc::tma_load_2d_hint(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s], w_policy);
       };
       auto issue_a = [&](int q) {
         const int s = q % ST;

@@ -74,6 +74,7 @@ def gpu_prefill(model, pool, slot, tokens, tables, nbps, start=0, chunk=512):
         part = tokens[c0:c0 + chunk]
         rows = [(slot, int(t), start + c0 + i, 1, 0) for i, t in enumerate(part)]
         cbd.step(model.e, pool.p, rows, tables, nbps, [], None, dummy)
+        cbd.engine_check(model.e)       # a kernel-flagged error fails at the step that raised it
 
 
 def run_step(model, pool, rows, tables, nbps, sampling, uniforms=None):
