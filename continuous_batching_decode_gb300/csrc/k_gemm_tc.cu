@@ -631,17 +631,21 @@ void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S) 
   *S = choose_cluster((long long)*T * *NR, *KB);
 }
 
-// Weight rows per tile for an M x K matrix.  Measured on GB300 (7B decode
-// step): narrower tiles that let more CTAs stream (e.g. 128 rows, K split 4
-// ways, 128 CTAs instead of 96 for a 4096 x 4096 matrix) ran slower -- HBM
-// is already saturated while the weights stream, and the per-stage cost and
-// the activation traffic per weight byte grow as the tile narrows -- so the
-// widest tile that divides M is used.
+// Weight rows per tile for an M x K matrix: the widest tile that divides M,
+// except that a matrix with fewer than 20 such tiles (the 4096-row O and down
+// projections of a 7B model) takes 128-row tiles.  Measured on GB300 (7B
+// decode step, B = 32): 128-row tiles for O and down let 128 CTAs stream
+// instead of 96 (4.79 vs 4.81 ms per step); narrower tiles for the wide
+// matrices ran slower (QKV 4.94, gate/up 5.20 ms): HBM is already saturated
+// while their weights stream, and the per-stage cost and the activation
+// traffic per weight byte grow as the tile narrows.
 int gemm_tc_pick_tile(int M, int K) {
   (void)K;
+  int best = kTcMaxBN;
   for (int N : {256, 224, 192, 160, 128})
-    if (M % N == 0) return N;
-  return kTcMaxBN;
+    if (M % N == 0) { best = N; break; }
+  if (M / best < 20 && M % 128 == 0) best = 128;
+  return best;
 }
 
 cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s) {
