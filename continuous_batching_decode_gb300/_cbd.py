@@ -17,8 +17,8 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcbd.so")
 
-OK, EINVAL, ENOMEM, ECUDA, EPOOL, EUNSUPPORTED, EDEVICE, EDEADLOCK, ESTATE = 0, -1, -2, -3, -4, -5, -6, -7, -8
-FINISH_LENGTH, FINISH_FALLBACK, FINISH_ABORTED = 1, 2, 3
+OK, EINVAL, ENOMEM, ECUDA, EPOOL, EUNSUPPORTED, EDEVICE, EDEADLOCK, ESTATE, EBUSY = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+FINISH_LENGTH, FINISH_FALLBACK, FINISH_ABORTED, FINISH_TIMEOUT, FINISH_LAGGING = 1, 2, 3, 4, 5
 
 
 class CbdError(RuntimeError):
@@ -62,7 +62,8 @@ class KernelStat(ctypes.Structure):
 
 class SchedConfig(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("n_blocks", "block_size", "max_slots", "max_rows", "chunk", "answer_budget",
-                                     "max_blocks_per_seq", "reserve_answer", "stall_fallback")]
+                                     "max_blocks_per_seq", "reserve_answer", "stall_fallback",
+                                     "queue_per_slot", "queue_timeout_ms", "out_buffer")]
 
 
 class Request(ctypes.Structure):
@@ -86,7 +87,9 @@ class SchedStats(ctypes.Structure):
     _fields_ = [("running", c_i32), ("waiting", c_i32), ("free_blocks", c_i32), ("allocated", c_i32),
                 ("reserved", c_i32), ("outstanding", c_i32), ("steps", ctypes.c_int64),
                 ("rows_prefill", ctypes.c_int64), ("rows_decode", ctypes.c_int64),
-                ("fallback_stops", ctypes.c_int64), ("stalled_rows", ctypes.c_int64)]
+                ("fallback_stops", ctypes.c_int64), ("stalled_rows", ctypes.c_int64),
+                ("rejected_busy", ctypes.c_int64), ("timed_out", ctypes.c_int64), ("aborted", ctypes.c_int64),
+                ("lagging", ctypes.c_int64)]
 
 
 _P = ctypes.POINTER
@@ -123,6 +126,10 @@ PROTOS = {
     "cbd_sched_commit": (c_i32, [c_vp, _P(c_i32), c_i32, _P(Finished), c_i32, _P(c_i32)]),
     "cbd_sched_output": (c_i32, [c_vp, c_u64, _P(c_i32), c_i32, _P(c_i32)]),
     "cbd_sched_stats_get": (c_i32, [c_vp, _P(SchedStats)]),
+    "cbd_sched_abort": (c_i32, [c_vp, c_u64]),
+    "cbd_sched_set_time": (c_i32, [c_vp, ctypes.c_int64]),
+    "cbd_sched_read": (c_i32, [c_vp, c_u64, _P(c_i32), c_i32, _P(c_i32)]),
+    "cbd_sched_finished": (c_i32, [c_vp, _P(Finished), c_i32, _P(c_i32)]),
 }
 
 _lib = None
@@ -358,9 +365,11 @@ def sample_static(logits, counters, slots, sampling, uniforms, out_tokens, strea
 
 # ------------------------------------------------------------------ scheduler
 def sched_create(n_blocks, block_size=32, max_slots=64, max_rows=2048, chunk=512, answer_budget=128,
-                 max_blocks_per_seq=1024, reserve_answer=True, stall_fallback=True):
+                 max_blocks_per_seq=1024, reserve_answer=True, stall_fallback=True, queue_per_slot=0,
+                 queue_timeout_ms=0, out_buffer=0):
     cfg = SchedConfig(n_blocks, block_size, max_slots, max_rows, chunk, answer_budget, max_blocks_per_seq,
-                      1 if reserve_answer else 0, 1 if stall_fallback else 0)
+                      1 if reserve_answer else 0, 1 if stall_fallback else 0, queue_per_slot, queue_timeout_ms,
+                      out_buffer)
     out = c_vp()
     _check(lib().cbd_sched_create(ctypes.byref(cfg), ctypes.byref(out)))
     _sched_width[out.value] = max_blocks_per_seq
@@ -412,6 +421,28 @@ def sched_output(s, req_id: int) -> list:
     buf = (c_i32 * max(1, n.value))()
     _check(lib().cbd_sched_output(s, req_id, buf, n.value, ctypes.byref(n)))
     return list(buf[: n.value])
+
+
+def sched_abort(s, req_id: int) -> None:
+    _check(lib().cbd_sched_abort(s, req_id))
+
+
+def sched_set_time(s, now_ms: int) -> None:
+    _check(lib().cbd_sched_set_time(s, int(now_ms)))
+
+
+def sched_read(s, req_id: int, cap: int = 4096) -> list:
+    buf = (c_i32 * max(1, cap))()
+    n = c_i32()
+    _check(lib().cbd_sched_read(s, req_id, buf, cap, ctypes.byref(n)))
+    return list(buf[: n.value])
+
+
+def sched_finished(s, cap: int = 4096) -> list:
+    fin = (Finished * max(1, cap))()
+    n = c_i32()
+    _check(lib().cbd_sched_finished(s, fin, cap, ctypes.byref(n)))
+    return [(fin[i].id, fin[i].reason, fin[i].n_tokens) for i in range(n.value)]
 
 
 def sched_stats(s) -> dict:

@@ -16,6 +16,25 @@
 //   4. If no row could be planned while sequences run, the youngest is
 //      stopped (or CBD_EDEADLOCK is returned when the fallback is off).
 // Blocks come from a min-heap (lowest id first) so plans are reproducible.
+//
+// Overload and backpressure (section 20.3.4 背压与取消), each off when its
+// config field is 0:
+//   * bounded admission queue: at most queue_per_slot * max_slots requests
+//     wait; a submit beyond that is refused at once (CBD_EBUSY, "busy,
+//     retry later");
+//   * queue timeout: a request still waiting more than queue_timeout_ms
+//     after its submit (caller-driven clock) finishes TIMEOUT before the
+//     next admission -- a different outcome from a client cancel;
+//   * non-blocking delivery: every request has a buffer of out_buffer
+//     undelivered tokens that its client drains (cbd_sched_read); a token
+//     that finds the buffer full is not delivered and the request is
+//     cancelled (LAGGING), so one slow client never holds up the batch;
+//   * abort (client gone): the request stops at once and returns its slot
+//     and blocks -- at the commit of a step in flight, whose KV writes
+//     still target them.
+// The page wakes queued requests with a coalescing capacity signal; here
+// admission is re-evaluated in every plan, which sees every release since
+// the last one, so no wake-up can be lost.
 #include <algorithm>
 #include <cstring>
 #include <deque>
@@ -44,11 +63,15 @@ struct Req {
   bool block_wait = false;
   int64_t admit_seq = -1;
   int32_t pending_prefill = 0;
+  int64_t arrival_ms = 0;
+  bool aborted = false;            // abort requested while a step was in flight
+  std::deque<int32_t> outbox;      // delivered, not yet read by the client
 };
 
 struct Finished {
   int32_t reason;
   std::vector<int32_t> tokens;
+  std::deque<int32_t> outbox;
 };
 
 int64_t blocks_for(int64_t positions, int64_t bs) { return (positions + bs - 1) / bs; }
@@ -63,7 +86,9 @@ struct cbd_sched {
   std::vector<std::unique_ptr<Req>> running;  // admission order
   std::unordered_map<uint64_t, Finished> finished;
   std::unordered_set<uint64_t> known_ids;
+  std::deque<cbd_finished> side_finished;    // finished outside a commit
   int64_t admit_counter = 0;
+  int64_t now_ms = 0;
   bool have_plan = false;
   cbd_sched_stats st{};
   // plan storage
@@ -97,12 +122,27 @@ struct cbd_sched {
     for (int32_t b : r->blocks) free_heap.push(b);
     r->blocks.clear();
     slots[r->slot] = nullptr;
-    finished[r->id] = Finished{reason, r->generated};
+    finished[r->id] = Finished{reason, r->generated, std::move(r->outbox)};
     for (size_t i = 0; i < running.size(); ++i)
       if (running[i].get() == r) {
         running.erase(running.begin() + (ptrdiff_t)i);
         break;
       }
+  }
+  // Waiters older than the queue timeout leave the queue (reason TIMEOUT).
+  void expire() {
+    if (cfg.queue_timeout_ms <= 0) return;
+    for (size_t i = 0; i < waiting.size();) {
+      Req& r = *waiting[i];
+      if (now_ms - r.arrival_ms > cfg.queue_timeout_ms) {
+        finished[r.id] = Finished{CBD_FINISH_TIMEOUT, {}, {}};
+        side_finished.push_back(cbd_finished{r.id, CBD_FINISH_TIMEOUT, 0});
+        st.timed_out++;
+        waiting.erase(waiting.begin() + (ptrdiff_t)i);
+      } else {
+        ++i;
+      }
+    }
   }
   void admit() {
     for (auto& r : running)
@@ -196,7 +236,8 @@ cbd_status cbd_sched_create(const cbd_sched_config* cfg, cbd_sched** out) {
   if (!cfg) return cbd::fail(CBD_EINVAL, "cfg is NULL");
   const cbd_sched_config& c = *cfg;
   if (c.n_blocks < 1 || c.block_size < 1 || c.max_slots < 1 || c.max_rows < 1 || c.chunk < 1 ||
-      c.answer_budget < 0 || c.max_blocks_per_seq < 1)
+      c.answer_budget < 0 || c.max_blocks_per_seq < 1 || c.queue_per_slot < 0 || c.queue_timeout_ms < 0 ||
+      c.out_buffer < 0)
     return cbd::fail(CBD_EINVAL, "scheduler config out of range");
   try {
     auto s = std::make_unique<cbd_sched>();
@@ -226,12 +267,17 @@ cbd_status cbd_sched_submit(cbd_sched* s, const cbd_request* r) {
     return cbd::fail(CBD_EPOOL, "request longer than max_blocks_per_seq blocks");
   int64_t first = blocks_for((int64_t)r->prompt_len + std::min(r->max_tokens, c.answer_budget), c.block_size);
   if (first > c.n_blocks) return cbd::fail(CBD_EPOOL, "request can never fit the pool");
+  if (c.queue_per_slot > 0 && (int64_t)s->waiting.size() >= (int64_t)c.queue_per_slot * c.max_slots) {
+    s->st.rejected_busy++;
+    return cbd::fail(CBD_EBUSY, "admission queue full; retry later");
+  }
   try {
     auto q = std::make_unique<Req>();
     q->id = r->id;
     q->prompt.assign(r->prompt, r->prompt + r->prompt_len);
     q->max_tokens = r->max_tokens;
     q->sampling = r->sampling;
+    q->arrival_ms = s->now_ms;
     s->known_ids.insert(r->id);
     s->waiting.push_back(std::move(q));
   } catch (...) {
@@ -246,6 +292,7 @@ cbd_status cbd_sched_plan(cbd_sched* s, cbd_plan* out) {
   const cbd_sched_config& c = s->cfg;
   s->resets.clear();
   s->stopped.clear();
+  s->expire();
   s->admit();
   std::vector<cbd_sched::Wait> waits;
   for (;;) {
@@ -304,24 +351,111 @@ cbd_status cbd_sched_commit(cbd_sched* s, const int32_t* tokens, int32_t m, cbd_
   if (!s->have_plan) return cbd::fail(CBD_ESTATE, "commit without a plan");
   if (m != (int32_t)s->samp_ids.size()) return cbd::fail(CBD_EINVAL, "token count does not match the plan");
   if (m > 0 && !tokens) return cbd::fail(CBD_EINVAL, "tokens is NULL");
+  const int32_t ob = s->cfg.out_buffer;
   std::unordered_map<uint64_t, Req*> by_id;
   for (auto& r : s->running) {
     by_id[r->id] = r.get();
     r->n_prefilled += r->pending_prefill;
     r->pending_prefill = 0;
   }
-  for (int32_t j = 0; j < m; ++j) by_id.at(s->samp_ids[j])->generated.push_back(tokens[j]);
+  // Delivery in row order: a token that finds its request's buffer full is
+  // dropped and the request is cancelled (reason LAGGING).
+  std::unordered_map<Req*, int32_t> reason;
+  for (int32_t j = 0; j < m; ++j) {
+    Req* r = by_id.at(s->samp_ids[j]);
+    if (r->aborted || reason.count(r)) continue;
+    if (ob > 0 && (int32_t)r->outbox.size() >= ob) {
+      reason[r] = CBD_FINISH_LAGGING;
+      continue;
+    }
+    r->generated.push_back(tokens[j]);
+    if (ob > 0) r->outbox.push_back(tokens[j]);
+  }
   int32_t k = 0;
-  std::vector<Req*> done;
-  for (auto& r : s->running)
-    if ((int32_t)r->generated.size() >= r->max_tokens) done.push_back(r.get());
-  for (Req* r : done) {
-    if (fin && k < cap) fin[k] = cbd_finished{r->id, CBD_FINISH_LENGTH, (int32_t)r->generated.size()};
+  std::vector<std::pair<Req*, int32_t>> done;
+  for (auto& r : s->running) {
+    if (r->aborted) done.emplace_back(r.get(), CBD_FINISH_ABORTED);
+    else if (reason.count(r.get())) done.emplace_back(r.get(), reason[r.get()]);
+    else if ((int32_t)r->generated.size() >= r->max_tokens) done.emplace_back(r.get(), CBD_FINISH_LENGTH);
+  }
+  for (auto& [r, why] : done) {
+    if (fin && k < cap) fin[k] = cbd_finished{r->id, why, (int32_t)r->generated.size()};
     ++k;
-    s->release(r, CBD_FINISH_LENGTH);
+    if (why == CBD_FINISH_ABORTED) s->st.aborted++;
+    if (why == CBD_FINISH_LAGGING) s->st.lagging++;
+    s->release(r, why);
   }
   if (n_fin) *n_fin = std::min(k, cap);
   s->have_plan = false;
+  return CBD_OK;
+}
+
+cbd_status cbd_sched_abort(cbd_sched* s, uint64_t id) {
+  if (!s) return cbd::fail(CBD_EINVAL, "NULL scheduler");
+  for (size_t i = 0; i < s->waiting.size(); ++i)
+    if (s->waiting[i]->id == id) {
+      s->finished[id] = Finished{CBD_FINISH_ABORTED, {}, {}};
+      s->side_finished.push_back(cbd_finished{id, CBD_FINISH_ABORTED, 0});
+      s->st.aborted++;
+      s->waiting.erase(s->waiting.begin() + (ptrdiff_t)i);
+      return CBD_OK;
+    }
+  for (auto& r : s->running)
+    if (r->id == id) {
+      if (r->aborted) return cbd::fail(CBD_EINVAL, "request already aborted");
+      if (s->have_plan) {          // the step in flight still writes its KV blocks
+        r->aborted = true;
+        return CBD_OK;
+      }
+      s->side_finished.push_back(cbd_finished{id, CBD_FINISH_ABORTED, (int32_t)r->generated.size()});
+      s->st.aborted++;
+      s->release(r.get(), CBD_FINISH_ABORTED);
+      return CBD_OK;
+    }
+  return cbd::fail(CBD_EINVAL, "unknown or finished request id");
+}
+
+cbd_status cbd_sched_set_time(cbd_sched* s, int64_t now_ms) {
+  if (!s) return cbd::fail(CBD_EINVAL, "NULL scheduler");
+  if (now_ms < s->now_ms) return cbd::fail(CBD_EINVAL, "the scheduler clock must not go backwards");
+  s->now_ms = now_ms;
+  return CBD_OK;
+}
+
+cbd_status cbd_sched_read(cbd_sched* s, uint64_t id, int32_t* tokens, int32_t cap, int32_t* n) {
+  if (!s || !n) return cbd::fail(CBD_EINVAL, "NULL argument");
+  if (cap > 0 && !tokens) return cbd::fail(CBD_EINVAL, "tokens is NULL");
+  *n = 0;
+  std::deque<int32_t>* box = nullptr;
+  for (auto& r : s->running)
+    if (r->id == id) box = &r->outbox;
+  if (!box) {
+    auto it = s->finished.find(id);
+    if (it != s->finished.end()) box = &it->second.outbox;
+  }
+  if (!box) {
+    for (auto& r : s->waiting)
+      if (r->id == id) return CBD_OK;           // queued: nothing generated yet
+    return cbd::fail(CBD_EINVAL, "unknown request id");
+  }
+  int32_t k = 0;
+  while (k < cap && !box->empty()) {
+    tokens[k++] = box->front();
+    box->pop_front();
+  }
+  *n = k;
+  return CBD_OK;
+}
+
+cbd_status cbd_sched_finished(cbd_sched* s, cbd_finished* out, int32_t cap, int32_t* n) {
+  if (!s || !n) return cbd::fail(CBD_EINVAL, "NULL argument");
+  if (cap > 0 && !out) return cbd::fail(CBD_EINVAL, "out is NULL");
+  int32_t k = 0;
+  while (k < cap && !s->side_finished.empty()) {
+    out[k++] = s->side_finished.front();
+    s->side_finished.pop_front();
+  }
+  *n = k;
   return CBD_OK;
 }
 

@@ -55,6 +55,7 @@ extern "C" {
 #define CBD_EDEVICE (-6)       /* a kernel flagged an error (cbd_engine_check) */
 #define CBD_EDEADLOCK (-7)     /* scheduler: no running sequence can progress */
 #define CBD_ESTATE (-8)        /* call out of order (e.g. commit w/o plan)    */
+#define CBD_EBUSY (-9)         /* admission queue full: retry later (HTTP 429) */
 
 typedef int32_t cbd_status;
 
@@ -337,6 +338,16 @@ typedef struct cbd_sched_config {
   int32_t max_blocks_per_seq;
   int32_t reserve_answer;      /* 1: reservation policy; 0: free slot only */
   int32_t stall_fallback;      /* 1: stop the youngest when all are stuck  */
+  /* Overload and backpressure ("20.3 服务、批处理与流式" section 20.3.4;
+   * 0 disables each; the page's defaults are 8, 30000 and a small buffer): */
+  int32_t queue_per_slot;      /* waiting requests allowed per slot; submit
+                                * beyond max_slots * queue_per_slot waiters
+                                * returns CBD_EBUSY                         */
+  int32_t queue_timeout_ms;    /* a request still waiting this long after
+                                * submit finishes CBD_FINISH_TIMEOUT        */
+  int32_t out_buffer;          /* undelivered tokens a request may hold; a
+                                * token that finds its buffer full cancels
+                                * the request (CBD_FINISH_LAGGING)           */
 } cbd_sched_config;
 
 typedef struct cbd_request {
@@ -367,7 +378,9 @@ typedef struct cbd_plan {
 
 #define CBD_FINISH_LENGTH 1
 #define CBD_FINISH_FALLBACK 2
-#define CBD_FINISH_ABORTED 3
+#define CBD_FINISH_ABORTED 3          /* cbd_sched_abort: client went away (HTTP 499) */
+#define CBD_FINISH_TIMEOUT 4          /* waited longer than queue_timeout_ms (HTTP 429) */
+#define CBD_FINISH_LAGGING 5          /* delivery buffer full: slow client cancelled    */
 
 typedef struct cbd_finished {
   uint64_t id;
@@ -378,6 +391,7 @@ typedef struct cbd_finished {
 typedef struct cbd_sched_stats {
   int32_t running, waiting, free_blocks, allocated, reserved, outstanding;
   int64_t steps, rows_prefill, rows_decode, fallback_stops, stalled_rows;
+  int64_t rejected_busy, timed_out, aborted, lagging;
 } cbd_sched_stats;
 
 typedef struct cbd_sched cbd_sched;
@@ -399,6 +413,26 @@ cbd_status cbd_sched_commit(cbd_sched* s, const int32_t* tokens, int32_t m,
 /* Copy up to `cap` generated tokens of a finished request; *n = its count.
  * CBD_EINVAL if the id has not finished. */
 cbd_status cbd_sched_output(cbd_sched* s, uint64_t id, int32_t* tokens, int32_t cap, int32_t* n);
+/* Cancel a request because its client went away (section 20.3.4: stop
+ * generating at once and return the KV blocks).  A waiting request leaves
+ * the queue; a running one frees its slot and blocks now, or, if the last
+ * plan (not yet committed) has rows of it, at that commit, which drops its
+ * token.  It finishes CBD_FINISH_ABORTED (reported by the commit or by
+ * cbd_sched_finished).  CBD_EINVAL for an unknown or finished id. */
+cbd_status cbd_sched_abort(cbd_sched* s, uint64_t id);
+/* The scheduler's clock in milliseconds (caller-driven, so runs replay):
+ * submit stamps a request's arrival with it, and cbd_sched_plan expires
+ * waiters older than queue_timeout_ms.  Must not go backwards. */
+cbd_status cbd_sched_set_time(cbd_sched* s, int64_t now_ms);
+/* The client side of a request's delivery buffer: move up to `cap` of its
+ * undelivered tokens (oldest first) to `tokens`; *n = how many.  Works for
+ * running and finished requests (a finished request keeps its undelivered
+ * tokens).  With out_buffer == 0 nothing is buffered and *n = 0. */
+cbd_status cbd_sched_read(cbd_sched* s, uint64_t id, int32_t* tokens, int32_t cap, int32_t* n);
+/* Requests finished outside a commit (abort of a request not in flight,
+ * queue timeouts at plan time) since the last call: up to `cap` records,
+ * *n = how many were written; the rest stay for the next call. */
+cbd_status cbd_sched_finished(cbd_sched* s, cbd_finished* out, int32_t cap, int32_t* n);
 cbd_status cbd_sched_stats_get(cbd_sched* s, cbd_sched_stats* out);
 
 #ifdef __cplusplus

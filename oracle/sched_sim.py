@@ -40,6 +40,26 @@ Readings where the pages leave the step open (listed in the design notes):
 ``reserve_answer=False`` gives the free-slot-only admission the page warns
 about; ``stall_fallback=False`` makes plan() report a deadlock instead of
 stopping a sequence.
+
+Overload and backpressure, same page, section 20.3.4 背压与取消 (each is off
+when its config value is 0):
+  * the admission queue is bounded (Forma: 8 waiters per slot); a request
+    that arrives to a full queue is refused at once ("busy, retry later");
+  * a request that has waited longer than the wait budget (Forma: 30 s) is
+    turned away -- an outcome distinct from the client cancelling;
+  * tokens go to each request through a bounded buffer that the client
+    drains; a send that finds the buffer full is not made, the client is
+    judged to be lagging and its request is cancelled, so a slow client
+    never stalls the batch (the page's two-stream program: buffer 2, the
+    slow stream is cancelled at step 3 holding 2 tokens);
+  * a client that goes away stops its generation at once and gives back its
+    KV blocks.
+Readings: R30 a lagging request keeps the tokens it had delivered; the one
+that did not fit is dropped.  R31 the queue bound counts requests not yet
+admitted.  R32 expiry is checked at each plan, before admission, with a
+caller-driven clock in milliseconds (wait > budget).  R33 an abort of a
+request whose step is in flight (planned, not committed) takes effect at
+that commit, which drops its token, since the step still writes its blocks.
 """
 from __future__ import annotations
 
@@ -49,7 +69,9 @@ from collections import deque
 
 FINISH_LENGTH = 1            # reached max_tokens
 FINISH_LENGTH_FALLBACK = 2   # stopped because every running sequence was stuck
-FINISH_ABORTED = 3
+FINISH_ABORTED = 3           # the client went away
+FINISH_TIMEOUT = 4           # waited longer than the queue's wait budget
+FINISH_LAGGING = 5           # delivery buffer full: slow client cancelled
 
 
 class Deadlock(Exception):
@@ -58,6 +80,10 @@ class Deadlock(Exception):
 
 class PoolTooSmall(Exception):
     """The request can never be admitted."""
+
+
+class Busy(Exception):
+    """The admission queue is full; the client should retry later."""
 
 
 def blocks_for(positions: int, block_size: int) -> int:
@@ -75,6 +101,9 @@ class SchedConfig:
     max_blocks_per_seq: int = 1024
     reserve_answer: bool = True
     stall_fallback: bool = True
+    queue_per_slot: int = 0      # waiting requests per slot (0: unbounded)
+    queue_timeout_ms: int = 0    # wait budget (0: none)
+    out_buffer: int = 0          # undelivered tokens per request (0: unbounded, untracked)
 
 
 @dataclasses.dataclass
@@ -92,6 +121,9 @@ class Request:
     block_wait: bool = False
     admit_seq: int = -1
     pending_prefill: int = 0
+    arrival_ms: int = 0
+    aborted: bool = False
+    outbox: deque = dataclasses.field(default_factory=deque)
 
 
 @dataclasses.dataclass
@@ -115,6 +147,10 @@ class Scheduler:
         self._admit_counter = 0
         self._last_plan = None
         self.n_fallback = 0
+        self.now_ms = 0
+        self.side_finished = []     # (id, reason, n_tokens) finished outside a commit
+        self.outboxes = {}          # id -> deque of undelivered tokens of finished requests
+        self.counts = dict(rejected_busy=0, timed_out=0, aborted=0, lagging=0)
 
     # -- helpers -------------------------------------------------------
     def _need(self, req: Request) -> int:
@@ -145,6 +181,7 @@ class Scheduler:
         self.slots[req.slot] = None
         self.running.remove(req)
         self.finished[req.id] = (reason, list(req.generated))
+        self.outboxes[req.id] = req.outbox
 
     # -- public API ----------------------------------------------------
     def submit(self, req: Request) -> None:
@@ -157,7 +194,76 @@ class Scheduler:
         first = blocks_for(len(req.prompt) + min(req.max_tokens, c.answer_budget), c.block_size)
         if first > c.n_blocks:
             raise PoolTooSmall("request can never fit the pool")
+        if c.queue_per_slot and len(self.waiting) >= c.queue_per_slot * c.max_slots:
+            self.counts["rejected_busy"] += 1
+            raise Busy("admission queue full")
+        req.arrival_ms = self.now_ms
         self.waiting.append(req)
+
+    def set_time(self, now_ms: int) -> None:
+        if now_ms < self.now_ms:
+            raise ValueError("the clock must not go backwards")
+        self.now_ms = now_ms
+
+    def _expire(self) -> None:
+        """Waiters past the wait budget leave the queue (R32)."""
+        c = self.cfg
+        if not c.queue_timeout_ms:
+            return
+        keep = deque()
+        for r in self.waiting:
+            if self.now_ms - r.arrival_ms > c.queue_timeout_ms:
+                self.finished[r.id] = (FINISH_TIMEOUT, [])
+                self.outboxes[r.id] = deque()
+                self.side_finished.append((r.id, FINISH_TIMEOUT, 0))
+                self.counts["timed_out"] += 1
+            else:
+                keep.append(r)
+        self.waiting = keep
+
+    def abort(self, rid: int) -> None:
+        """The client went away: stop now, or at the commit of the step in flight (R33)."""
+        for r in list(self.waiting):
+            if r.id == rid:
+                self.waiting.remove(r)
+                self.finished[rid] = (FINISH_ABORTED, [])
+                self.outboxes[rid] = deque()
+                self.side_finished.append((rid, FINISH_ABORTED, 0))
+                self.counts["aborted"] += 1
+                return
+        for r in self.running:
+            if r.id == rid:
+                if r.aborted:
+                    raise ValueError("already aborted")
+                if self._last_plan is not None:
+                    r.aborted = True
+                    return
+                self.side_finished.append((rid, FINISH_ABORTED, len(r.generated)))
+                self.counts["aborted"] += 1
+                self._release(r, FINISH_ABORTED)
+                return
+        raise ValueError("unknown or finished request")
+
+    def read(self, rid: int, cap: int = 1 << 30) -> list:
+        """The client drains up to cap undelivered tokens, oldest first."""
+        box = None
+        for r in self.running:
+            if r.id == rid:
+                box = r.outbox
+        if box is None:
+            box = self.outboxes.get(rid)
+        if box is None:
+            if any(r.id == rid for r in self.waiting):
+                return []
+            raise ValueError("unknown request")
+        out = []
+        while box and len(out) < cap:
+            out.append(box.popleft())
+        return out
+
+    def take_finished(self) -> list:
+        out, self.side_finished = self.side_finished, []
+        return out
 
     def _admit(self, resets: list) -> None:
         """Admission (R9, R10): FCFS; frozen while a row waits for a block."""
@@ -233,6 +339,7 @@ class Scheduler:
     def plan(self) -> Plan:
         c = self.cfg
         resets, stopped = [], []
+        self._expire()
         self._admit(resets)
         while True:
             rows, sampled, waits = self._compose()
@@ -268,17 +375,36 @@ class Scheduler:
             raise RuntimeError("commit without plan")
         if len(tokens) != len(plan.sampled):
             raise ValueError("token count does not match the plan")
+        ob = self.cfg.out_buffer
         by_id = {r.id: r for r in self.running}
         for r in self.running:
             r.n_prefilled += r.pending_prefill
             r.pending_prefill = 0
-        for (rid, _), t in zip(plan.sampled, tokens):
-            by_id[rid].generated.append(int(t))
+        lagging = set()
+        for (rid, _), t in zip(plan.sampled, tokens):      # delivery, row order
+            r = by_id[rid]
+            if r.aborted or rid in lagging:
+                continue
+            if ob and len(r.outbox) >= ob:                  # buffer full: cancel (R30)
+                lagging.add(rid)
+                continue
+            r.generated.append(int(t))
+            if ob:
+                r.outbox.append(int(t))
         done = []
         for r in list(self.running):
-            if len(r.generated) >= r.max_tokens:
-                self._release(r, FINISH_LENGTH)
-                done.append((r.id, FINISH_LENGTH))
+            if r.aborted:
+                why = FINISH_ABORTED
+                self.counts["aborted"] += 1
+            elif r.id in lagging:
+                why = FINISH_LAGGING
+                self.counts["lagging"] += 1
+            elif len(r.generated) >= r.max_tokens:
+                why = FINISH_LENGTH
+            else:
+                continue
+            self._release(r, why)
+            done.append((r.id, why))
         self._last_plan = None
         return done
 
@@ -287,4 +413,4 @@ class Scheduler:
                     free_blocks=len(self.free), outstanding=self._outstanding(),
                     allocated=sum(len(r.blocks) for r in self.running),
                     reserved=sum(r.reserved for r in self.running),
-                    fallback_stops=self.n_fallback)
+                    fallback_stops=self.n_fallback, **self.counts)

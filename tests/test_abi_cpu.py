@@ -189,3 +189,79 @@ def test_cpp_scheduler_rejects_bad_requests(cbd):
         cbd.sched_commit(h, [])
     assert ei.value.status == cbd.ESTATE
     cbd.sched_destroy(h)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_cpp_scheduler_overload_matches_simulator(cbd, seed):
+    """Bounded queue, wait budget, delivery buffers and aborts: the C++
+    scheduler and the simulator, driven in lockstep by the same events
+    (arrivals over a caller-driven clock, aborts between and during steps,
+    clients that read or not), give the same plans and the same outcomes."""
+    from oracle import sched_sim as ss
+    rng = random.Random(500 + seed)
+    kw = dict(n_blocks=rng.choice([40, 200]), block_size=4, max_slots=rng.choice([2, 6]),
+              max_rows=rng.choice([16, 48]), chunk=8, answer_budget=16, max_blocks_per_seq=200,
+              queue_per_slot=rng.choice([2, 8]), queue_timeout_ms=rng.choice([500, 3000]),
+              out_buffer=rng.choice([2, 4]))
+    sim = ss.Scheduler(ss.SchedConfig(**kw))
+    h = cbd.sched_create(**kw)
+    try:
+        t, pending = 0, []
+        for i in range(50):
+            t += rng.choice([0, 10, 50])
+            pending.append((t, i, [rng.randrange(100) for _ in range(rng.randint(1, 30))], rng.randint(1, 30)))
+        slow = set(rng.sample(range(50), 5))
+        t, steps = 0, 0
+        while pending or sim.running or sim.waiting:
+            t += rng.choice([5, 20, 200])
+            sim.set_time(t)
+            cbd.sched_set_time(h, t)
+            while pending and pending[0][0] <= t:
+                _, rid, prompt, mt = pending.pop(0)
+                busy_s = busy_c = False
+                try:
+                    sim.submit(ss.Request(rid, prompt, mt))
+                except ss.Busy:
+                    busy_s = True
+                try:
+                    cbd.sched_submit(h, rid, prompt, mt)
+                except cbd.CbdError as e:
+                    assert e.status == cbd.EBUSY
+                    busy_c = True
+                assert busy_s == busy_c
+            live = [r.id for r in sim.running] + [r.id for r in sim.waiting]
+            if live and rng.random() < 0.05:
+                victim = rng.choice(live)
+                sim.abort(victim)
+                cbd.sched_abort(h, victim)
+            p_s = sim.plan()
+            p_c = cbd.sched_plan(h)
+            assert p_c["rows"] == p_s.rows, f"step {steps}"
+            assert p_c["sampled_ids"] == [i for i, _ in p_s.sampled]
+            assert p_c["resets"] == p_s.resets
+            in_flight = [r.id for r in sim.running if not r.aborted]
+            if in_flight and rng.random() < 0.05:
+                victim = rng.choice(in_flight)
+                sim.abort(victim)
+                cbd.sched_abort(h, victim)
+            toks = [rng.randrange(1000) for _ in p_s.sampled]
+            fin_s = sim.commit(toks)
+            fin_c = cbd.sched_commit(h, toks)
+            assert [(i, r) for i, r, _ in fin_c] == fin_s
+            assert cbd.sched_finished(h) == sim.take_finished()
+            for r in list(sim.running):
+                if r.id not in slow:
+                    assert cbd.sched_read(h, r.id, 2) == sim.read(r.id, 2)
+            st, ss_ = cbd.sched_stats(h), sim.stats()
+            for k in ("running", "waiting", "free_blocks", "allocated", "reserved", "outstanding",
+                      "rejected_busy", "timed_out", "aborted", "lagging"):
+                assert st[k] == ss_[k], k
+            steps += 1
+            assert steps < 20000
+        for rid in sim.finished:
+            assert cbd.sched_output(h, rid) == sim.finished[rid][1]
+            assert cbd.sched_read(h, rid) == sim.read(rid)
+        with pytest.raises(cbd.CbdError):
+            cbd.sched_set_time(h, t - 1)
+    finally:
+        cbd.sched_destroy(h)
