@@ -21,6 +21,13 @@ data path); barrier + max-over-ranks timing.
 
 --impl reference times the CPU oracle on a bounded sample of the same
 workload (no GPU).
+
+--trace serves a continuous-batching request trace instead (7B shape, 64
+slots, Poisson arrivals, prompts from {20, 50, 200, 1000}, outputs
+min(Geometric(1/128), 512), 512-token chunks, <= 2048 rows per step, a
+128-token answer reservation) through the C++ scheduler and the engine
+(continuous_batching_decode_gb300.serve) and prints one line per policy:
+generated tok/s over the wall clock, time to first token, steps and rows.
 """
 from __future__ import annotations
 
@@ -60,6 +67,11 @@ def parse():
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
+    ap.add_argument("--trace", action="store_true", help="serve the request trace (see the module docstring)")
+    ap.add_argument("--trace-requests", type=int, default=2000)
+    ap.add_argument("--trace-rate", type=float, default=0.0, help="requests/s (0: all arrive at t = 0)")
+    ap.add_argument("--trace-blocks", type=int, default=4096, help="KV pool blocks (4096 = ample)")
+    ap.add_argument("--policy", default="both", choices=["forma", "albatross", "both"])
     ap.add_argument("--l2-prefetch-mb", type=int, default=0,
                     help="MiB of the next weight contraction each kernel prefetches into L2 (0: off)")
     return ap.parse_args()
@@ -497,8 +509,54 @@ def run_cbd(args):
         dist.destroy_process_group()
 
 
+def run_trace(args):
+    import torch
+    import continuous_batching_decode_gb300 as cbd
+    from continuous_batching_decode_gb300 import build, serve, synth
+
+    torch.cuda.set_device(0)
+    build.build()
+    s = shape_of(args)
+    slots, rows, mbps = 64, 2048, 64
+    w = synth.make_weights(s, seed=args.seed, device="cuda")
+    e = cbd.engine_create(cbd.make_config(s, max_rows=rows, max_slots=slots, max_blocks_per_seq=mbps), w)
+    del w
+    torch.cuda.empty_cache()
+    reqs = synth.request_trace(args.trace_requests, s["vocab"], seed=args.seed,
+                               rate=args.trace_rate if args.trace_rate > 0 else None)
+    samp = dict(temperature=1.0, top_p=0.3, top_k=0, frequency_penalty=1.0, penalty_decay=0.996)
+    for r in reqs:
+        r["sampling"] = dict(samp, seed=args.seed + 11)
+    policies = ["forma", "albatross"] if args.policy == "both" else [args.policy]
+    for pol in policies:
+        pool = cbd.kv_pool_create(e, args.trace_blocks)
+        srv = serve.Server(e, pool, n_blocks=args.trace_blocks, max_slots=slots, max_rows=rows,
+                           max_blocks_per_seq=mbps, vocab=s["vocab"], chunk=512, answer_budget=128, policy=pol)
+        try:
+            res = srv.run(reqs)
+        finally:
+            srv.close()
+            cbd.kv_pool_destroy(pool)
+        ttft = res["ttft"]
+        line = dict(metric="trace generated tok/s (wall clock, host loop included)", impl="cbd",
+                    value=round(res["tok_s"], 1), unit="tok/s", policy=pol, requests=len(reqs),
+                    generated=res["generated"], wall_s=round(res["wall_s"], 3), steps=res["steps"],
+                    rows_per_step=round(res["rows"] / max(res["steps"], 1), 1),
+                    ttft_s=dict(mean=round(float(ttft.mean()), 4), p50=round(float(np.median(ttft)), 4),
+                                p99=round(float(np.quantile(ttft, 0.99)), 4)),
+                    stalled_rows=res["stats"]["stalled_rows"], fallback_stops=res["stats"]["fallback_stops"],
+                    config=dict(workload="7b-shaped continuous-batching trace", slots=slots, max_rows=rows,
+                                chunk=512, answer_budget=128, pool_blocks=args.trace_blocks,
+                                rate=args.trace_rate or "all at t=0"),
+                    data="synthetic (seeded random-init weights, random prompt ids)")
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.trace:
+        run_trace(args)
+        return
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
             return

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libcbd.so")
 
 OK, EINVAL, ENOMEM, ECUDA, EPOOL, EUNSUPPORTED, EDEVICE, EDEADLOCK, ESTATE, EBUSY = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
 FINISH_LENGTH, FINISH_FALLBACK, FINISH_ABORTED, FINISH_TIMEOUT, FINISH_LAGGING = 1, 2, 3, 4, 5
+POLICY_FORMA, POLICY_ALBATROSS = 0, 1
 
 
 class CbdError(RuntimeError):
@@ -63,7 +64,8 @@ class KernelStat(ctypes.Structure):
 class SchedConfig(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in ("n_blocks", "block_size", "max_slots", "max_rows", "chunk", "answer_budget",
                                      "max_blocks_per_seq", "reserve_answer", "stall_fallback",
-                                     "queue_per_slot", "queue_timeout_ms", "out_buffer")]
+                                     "queue_per_slot", "queue_timeout_ms", "out_buffer",
+                                     "policy", "max_prefill", "prefill_every", "short_prompt")]
 
 
 class Request(ctypes.Structure):
@@ -366,10 +368,11 @@ def sample_static(logits, counters, slots, sampling, uniforms, out_tokens, strea
 # ------------------------------------------------------------------ scheduler
 def sched_create(n_blocks, block_size=32, max_slots=64, max_rows=2048, chunk=512, answer_budget=128,
                  max_blocks_per_seq=1024, reserve_answer=True, stall_fallback=True, queue_per_slot=0,
-                 queue_timeout_ms=0, out_buffer=0):
+                 queue_timeout_ms=0, out_buffer=0, policy="forma", max_prefill=0, prefill_every=0, short_prompt=0):
+    pol = {"forma": POLICY_FORMA, "albatross": POLICY_ALBATROSS}[policy] if isinstance(policy, str) else policy
     cfg = SchedConfig(n_blocks, block_size, max_slots, max_rows, chunk, answer_budget, max_blocks_per_seq,
                       1 if reserve_answer else 0, 1 if stall_fallback else 0, queue_per_slot, queue_timeout_ms,
-                      out_buffer)
+                      out_buffer, pol, max_prefill, prefill_every, short_prompt)
     out = c_vp()
     _check(lib().cbd_sched_create(ctypes.byref(cfg), ctypes.byref(out)))
     _sched_width[out.value] = max_blocks_per_seq

@@ -35,6 +35,14 @@
 // The page wakes queued requests with a coalescing capacity signal; here
 // admission is re-evaluated in every plan, which sees every release since
 // the last one, so no wake-up can be lost.
+//
+// Second composition policy (cfg.policy == CBD_POLICY_ALBATROSS), after the
+// Albatross worker loop ("RWKV Runner Albatross 后端", 连续批处理：Worker 主循环):
+// admission also stops while max_prefill requests are prefilling; a prompt
+// shorter than short_prompt tokens gets one prefill row per step; a longer
+// prompt gets a chunk only in a "sequence step", which comes after every
+// prefill_every steps that carried other rows, or at once when there are
+// none.  Rows stay prefill-first; the reservation rule is unchanged.
 #include <algorithm>
 #include <cstring>
 #include <deque>
@@ -89,6 +97,8 @@ struct cbd_sched {
   std::deque<cbd_finished> side_finished;    // finished outside a commit
   int64_t admit_counter = 0;
   int64_t now_ms = 0;
+  int32_t seq_countdown = 0;       // Albatross: steps left before the next sequence step
+  bool seq_step = false;           // Albatross: the composed step is a sequence step
   bool have_plan = false;
   cbd_sched_stats st{};
   // plan storage
@@ -144,10 +154,20 @@ struct cbd_sched {
       }
     }
   }
+  bool albatross() const { return cfg.policy == CBD_POLICY_ALBATROSS; }
+  int32_t max_prefill() const {
+    return cfg.max_prefill > 0 ? cfg.max_prefill : std::max(cfg.max_slots / 8, 1);   // floor(0.125 slots)
+  }
+  int32_t prefill_every() const { return cfg.prefill_every > 0 ? cfg.prefill_every : 5; }
+  int32_t short_prompt() const { return cfg.short_prompt > 0 ? cfg.short_prompt : 10; }
   void admit() {
     for (auto& r : running)
       if (r->block_wait) return;
+    int32_t prefilling = 0;
+    for (auto& r : running)
+      if (r->n_prefilled < (int32_t)r->prompt.size()) ++prefilling;
     while (!waiting.empty()) {
+      if (albatross() && prefilling >= max_prefill()) return;
       int32_t slot = -1;
       for (int32_t s = 0; s < cfg.max_slots; ++s)
         if (!slots[s]) { slot = s; break; }
@@ -163,6 +183,7 @@ struct cbd_sched {
       slots[slot] = r.get();
       resets.push_back(slot);
       running.push_back(std::move(r));
+      ++prefilling;
     }
   }
   struct Wait { Req* r; bool for_block; };
@@ -174,12 +195,28 @@ struct cbd_sched {
     int32_t budget = cfg.max_rows;
     std::unordered_set<Req*> prefilling;
     for (auto& up : running) up->pending_prefill = 0;
+    seq_step = false;
+    if (albatross()) {
+      bool other = false, any_seq = false;     // rows other than sequence chunks; sequence prompts
+      for (auto& up : running) {
+        const Req& r = *up;
+        const int32_t P = (int32_t)r.prompt.size();
+        if (r.n_prefilled < P) (P < short_prompt() ? other : any_seq) = true;
+        else if (!r.generated.empty() && (int32_t)r.generated.size() < r.max_tokens) other = true;
+      }
+      seq_step = any_seq && (seq_countdown <= 0 || !other);
+    }
     for (auto& up : running) {
       Req& r = *up;
       int32_t P = (int32_t)r.prompt.size();
       if (r.n_prefilled >= P) continue;
+      int32_t take = cfg.chunk;
+      if (albatross()) {
+        if (P < short_prompt()) take = 1;        // one-token prefill, every step
+        else if (!seq_step) continue;            // a sequence prompt waits for its step
+      }
       if (budget == 0) { waits.push_back({&r, false}); continue; }
-      int32_t n = std::min({cfg.chunk, P - r.n_prefilled, budget});
+      int32_t n = std::min({take, P - r.n_prefilled, budget});
       while ((int64_t)r.blocks.size() * cfg.block_size < (int64_t)r.n_prefilled + n && grow(r)) {}
       n = (int32_t)std::min<int64_t>(n, (int64_t)r.blocks.size() * cfg.block_size - r.n_prefilled);
       if (n <= 0) { waits.push_back({&r, true}); continue; }
@@ -237,7 +274,8 @@ cbd_status cbd_sched_create(const cbd_sched_config* cfg, cbd_sched** out) {
   const cbd_sched_config& c = *cfg;
   if (c.n_blocks < 1 || c.block_size < 1 || c.max_slots < 1 || c.max_rows < 1 || c.chunk < 1 ||
       c.answer_budget < 0 || c.max_blocks_per_seq < 1 || c.queue_per_slot < 0 || c.queue_timeout_ms < 0 ||
-      c.out_buffer < 0)
+      c.out_buffer < 0 || c.policy < 0 || c.policy > 1 || c.max_prefill < 0 || c.prefill_every < 0 ||
+      c.short_prompt < 0)
     return cbd::fail(CBD_EINVAL, "scheduler config out of range");
   try {
     auto s = std::make_unique<cbd_sched>();
@@ -308,6 +346,10 @@ cbd_status cbd_sched_plan(cbd_sched* s, cbd_plan* out) {
     s->stopped.push_back(young->id);
     s->st.fallback_stops++;
     s->release(young, CBD_FINISH_FALLBACK);
+  }
+  if (s->albatross() && !s->rows.empty()) {
+    if (s->seq_step) s->seq_countdown = s->prefill_every();
+    else s->seq_countdown = std::max(s->seq_countdown - 1, 0);
   }
   std::unordered_set<Req*> w;
   for (auto& x : waits) w.insert(x.r);

@@ -348,7 +348,23 @@ typedef struct cbd_sched_config {
   int32_t out_buffer;          /* undelivered tokens a request may hold; a
                                 * token that finds its buffer full cancels
                                 * the request (CBD_FINISH_LAGGING)           */
+  /* Composition policy.  CBD_POLICY_FORMA (0): the rules above.
+   * CBD_POLICY_ALBATROSS (1), after the Albatross worker loop ("RWKV Runner
+   * Albatross 后端", section 连续批处理：Worker 主循环): at most max_prefill
+   * requests prefill at a time (admission waits for one to finish); a
+   * prompt shorter than short_prompt tokens is fed one token per step, like
+   * a decode row; longer prompts advance by one chunk only in "sequence
+   * steps", one after every prefill_every steps that carried decode rows
+   * (at once when nothing decodes).  The block reservation is kept.  0 in a
+   * field takes the page's value: max(floor(0.125 max_slots), 1), 5, 10. */
+  int32_t policy;
+  int32_t max_prefill;
+  int32_t prefill_every;
+  int32_t short_prompt;
 } cbd_sched_config;
+
+#define CBD_POLICY_FORMA 0
+#define CBD_POLICY_ALBATROSS 1
 
 typedef struct cbd_request {
   uint64_t id;                 /* unique per scheduler                     */

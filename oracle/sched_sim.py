@@ -60,6 +60,24 @@ admitted.  R32 expiry is checked at each plan, before admission, with a
 caller-driven clock in milliseconds (wait > budget).  R33 an abort of a
 request whose step is in flight (planned, not committed) takes effect at
 that commit, which drops its token, since the step still writes its blocks.
+
+A second composition policy (``policy="albatross"``), from page "RWKV Runner
+Albatross 后端", section 连续批处理：Worker 主循环 (the worker's main loop):
+  * the task pool is filled from the queue up to the batch size, but with
+    at most max_prefill_count = max(int(batch_size * 0.125), 1) requests in
+    prefill at once, so prefill cannot crowd out decoding;
+  * a prompt shorter than min_forward_seq_len = 10 tokens is prefilled one
+    token per step alongside the decode rows, instead of by a sequence
+    forward;
+  * longer prompts are prefilled by sequence forwards, paced by
+    decode_prefill_ratio = 5: one sequence forward after about every 5
+    decode rounds, so long prefills fill the gaps between decode rounds.
+Readings: R34 the batch size is max_slots (the page's one spare slot is for
+its in-place state swaps, which block tables make unnecessary); admission
+keeps the block reservation of R9 and FCFS.  R35 a sequence step gives every
+long prompt in prefill one chunk and also carries the decode and one-token
+rows (the step is mixed); it comes when prefill_every steps with other rows
+have passed since the last one, or at once when no other row exists.
 """
 from __future__ import annotations
 
@@ -104,6 +122,10 @@ class SchedConfig:
     queue_per_slot: int = 0      # waiting requests per slot (0: unbounded)
     queue_timeout_ms: int = 0    # wait budget (0: none)
     out_buffer: int = 0          # undelivered tokens per request (0: unbounded, untracked)
+    policy: str = "forma"        # or "albatross"
+    max_prefill: int = 0         # albatross: 0 -> max(int(0.125 * max_slots), 1)
+    prefill_every: int = 0       # albatross: 0 -> 5 (decode_prefill_ratio)
+    short_prompt: int = 0        # albatross: 0 -> 10 (min_forward_seq_len)
 
 
 @dataclasses.dataclass
@@ -151,6 +173,12 @@ class Scheduler:
         self.side_finished = []     # (id, reason, n_tokens) finished outside a commit
         self.outboxes = {}          # id -> deque of undelivered tokens of finished requests
         self.counts = dict(rejected_busy=0, timed_out=0, aborted=0, lagging=0)
+        self.seq_countdown = 0      # albatross: steps left before the next sequence step
+        c = cfg
+        self.alb = c.policy == "albatross"
+        self.max_prefill = c.max_prefill or max(int(c.max_slots * 0.125), 1)
+        self.prefill_every = c.prefill_every or 5
+        self.short_prompt = c.short_prompt or 10
 
     # -- helpers -------------------------------------------------------
     def _need(self, req: Request) -> int:
@@ -270,7 +298,10 @@ class Scheduler:
         c = self.cfg
         if any(r.block_wait for r in self.running):
             return
+        prefilling = sum(1 for r in self.running if r.n_prefilled < len(r.prompt))
         while self.waiting and None in self.slots:
+            if self.alb and prefilling >= self.max_prefill:
+                return
             head = self.waiting[0]
             need = self._need(head)
             if c.reserve_answer and len(self.free) - self._outstanding() < need:
@@ -283,6 +314,7 @@ class Scheduler:
             self._admit_counter += 1
             self.running.append(head)
             resets.append(head.slot)
+            prefilling += 1
 
     def _compose(self):
         """Rows of one step: prefill chunks first, then one row per decoder.
@@ -296,13 +328,28 @@ class Scheduler:
         prefilling = set()
         for r in self.running:
             r.pending_prefill = 0
+        seq_step = False
+        if self.alb:
+            other = any((r.n_prefilled < len(r.prompt) and len(r.prompt) < self.short_prompt) or
+                        (r.n_prefilled == len(r.prompt) and 0 < len(r.generated) < r.max_tokens)
+                        for r in self.running)
+            any_seq = any(r.n_prefilled < len(r.prompt) and len(r.prompt) >= self.short_prompt
+                          for r in self.running)
+            seq_step = any_seq and (self.seq_countdown <= 0 or not other)
+        self._seq_step = seq_step
         for r in self.running:                                   # prefill chunks
             if r.n_prefilled >= len(r.prompt):
                 continue
+            take = c.chunk
+            if self.alb:
+                if len(r.prompt) < self.short_prompt:
+                    take = 1                                     # one token per step
+                elif not seq_step:
+                    continue                                     # waits for a sequence step
             if budget == 0:
                 waits.append((r, False))
                 continue
-            n = min(c.chunk, len(r.prompt) - r.n_prefilled, budget)
+            n = min(take, len(r.prompt) - r.n_prefilled, budget)
             while len(r.blocks) * c.block_size < r.n_prefilled + n and self._grow(r):
                 pass
             n = min(n, len(r.blocks) * c.block_size - r.n_prefilled)
@@ -351,6 +398,11 @@ class Scheduler:
             stopped.append((young.id, FINISH_LENGTH_FALLBACK))
             self.n_fallback += 1
             self._release(young, FINISH_LENGTH_FALLBACK)
+        if self.alb and rows:
+            if self._seq_step:
+                self.seq_countdown = self.prefill_every
+            else:
+                self.seq_countdown = max(self.seq_countdown - 1, 0)
         waiting_ids = {id(r) for r, _ in waits}
         for r in self.running:
             if id(r) in waiting_ids:

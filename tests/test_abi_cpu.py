@@ -126,12 +126,15 @@ def trace(seed, n, vocab=1000, max_prompt=60, max_out=40):
             for i in range(n)]
 
 
+@pytest.mark.parametrize("policy", ["forma", "albatross"])
 @pytest.mark.parametrize("seed", range(8))
-def test_cpp_scheduler_matches_simulator(cbd, seed):
+def test_cpp_scheduler_matches_simulator(cbd, seed, policy):
     rng = random.Random(100 + seed)
-    cfg = dict(n_blocks=rng.choice([12, 40, 200]), block_size=rng.choice([4, 32]), max_slots=rng.choice([3, 8]),
+    cfg = dict(n_blocks=rng.choice([12, 40, 200]), block_size=rng.choice([4, 32]), max_slots=rng.choice([3, 8, 16]),
                max_rows=rng.choice([12, 64]), chunk=rng.choice([8, 32]), answer_budget=rng.choice([8, 64]),
-               max_blocks_per_seq=256, reserve_answer=True, stall_fallback=True)
+               max_blocks_per_seq=256, reserve_answer=True, stall_fallback=True, policy=policy)
+    if policy == "albatross" and seed % 2:
+        cfg.update(max_prefill=rng.choice([1, 3]), prefill_every=rng.choice([1, 3]), short_prompt=rng.choice([4, 20]))
     run_both(cbd, cfg, trace(seed, 30), seed)
 
 
