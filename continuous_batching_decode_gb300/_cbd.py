@@ -108,6 +108,7 @@ PROTOS = {
     "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_l2_prefetch": (c_i32, [c_vp, c_u64]),
     "cbd_engine_set_fused_norm": (c_i32, [c_vp, c_i32]),
+    "cbd_engine_set_forbidden": (c_i32, [c_vp, _P(c_i32), c_i32]),
     "cbd_engine_profile_read": (c_i32, [c_vp, _P(KernelStat), c_i32, _P(c_i32)]),
     "cbd_kv_pool_create": (c_i32, [c_vp, c_i32, _P(c_vp)]),
     "cbd_kv_pool_destroy": (c_i32, [c_vp]),
@@ -205,6 +206,12 @@ def engine_create(cfg: Config, weights: dict):
 
 def engine_destroy(e) -> None:
     _check(lib().cbd_engine_destroy(e))
+
+
+def engine_set_forbidden(e, ids) -> None:
+    """Token ids the sampler never draws (empty: none); see include/cbd.h."""
+    ia, ip = _i32(list(ids) or [0])
+    _check(lib().cbd_engine_set_forbidden(e, ip, len(list(ids))))
 
 
 def engine_check(e) -> None:

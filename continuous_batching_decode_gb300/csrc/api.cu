@@ -276,6 +276,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_nh = W.take(R * d * 2), o_nl = W.take(R * d * 2), o_ssq = W.take(R * kMaxSsqParts * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
+  const size_t o_fb = W.take((V + 31) / 32 * 4);
   const size_t o_anext = W.take((size_t)dm.L * 4);
 
   e->work_bytes = W.off;
@@ -296,6 +297,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->logits = reinterpret_cast<float*>(wb + o_lg);
   e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
   e->counters = reinterpret_cast<float*>(wb + o_cn);
+  e->forbid = reinterpret_cast<uint32_t*>(wb + o_fb);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
   e->attn_next = reinterpret_cast<int32_t*>(wb + o_anext);
 
@@ -441,6 +443,29 @@ extern "C" cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   e->fuse_norm = enable != 0;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_forbidden(cbd_engine* e, const int32_t* ids, int32_t n) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  const int64_t V = e->dm.V;
+  if (n < 0 || n >= V) return fail(CBD_EINVAL, "%d forbidden ids: must be 0..vocab-1", (int)n);
+  if (n > 0 && !ids) return fail(CBD_EINVAL, "ids is NULL");
+  std::vector<uint32_t> bits((size_t)(V + 31) / 32, 0u);
+  int32_t distinct = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= V) return fail(CBD_EINVAL, "forbidden id %d outside the vocabulary", (int)ids[i]);
+    uint32_t& w = bits[(size_t)ids[i] >> 5];
+    const uint32_t b = 1u << (ids[i] & 31);
+    if (!(w & b)) ++distinct;
+    w |= b;
+  }
+  if (distinct >= V) return fail(CBD_EINVAL, "every token id is forbidden");
+  cudaError_t ce = cudaDeviceSynchronize();      // no step in flight reads the old mask
+  if (ce == cudaSuccess) ce = cudaMemcpy(e->forbid, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) return cuda_fail(ce, "forbidden-token mask");
+  e->n_forbidden = distinct;
   return CBD_OK;
 }
 

@@ -148,6 +148,8 @@ struct cbd_engine {
   float* logits = nullptr;            // [max_slots][V] internal logits
   float* samp_scratch = nullptr;      // [max_slots][V] sampler scratch
   float* counters = nullptr;          // [max_slots][V]
+  uint32_t* forbid = nullptr;         // [ceil(V/32)] bitmap of token ids the sampler never draws
+  int32_t n_forbidden = 0;            // ids set in `forbid` (0: mask off)
   int32_t* err = nullptr;             // device error word
   // staging for cbd_step (pinned host + device), double-buffered
   struct Stage {

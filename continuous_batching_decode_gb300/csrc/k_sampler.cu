@@ -5,6 +5,8 @@
 // sections "适配器" (temperature 1.0, top_p 0.3, top_k 0, frequency penalty 1,
 // decay 0.996) and "Worker 主循环" (penalties, then batched sampling of every
 // row).  The order of operations is this library's reading:
+//   forbidden ids (the engine's mask, Worker 主循环: "forbidden token 屏蔽"
+//   before the penalties) take l = -inf: never chosen, zero mass
 //   l' = (l - presence*[cnt>0]) - frequency*cnt   (fp32, separately rounded)
 //   greedy argmax (ties -> lowest id) if T == 0 or top_k == 1, else
 //   z = l'/T; keep the top_k by (z desc, id asc); the nucleus is the
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ slots,
                                                       const SampDev* __restrict__ samp,
                                                       float* __restrict__ scratch,
+                                                      const uint32_t* __restrict__ forbid,
                                                       int32_t* __restrict__ out, int32_t* err) {
   __shared__ SampShared sh;
   extern __shared__ __align__(16) uint8_t samp_dyn[];
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       const int v = base + u * 32 + lane;
       cv[u] = v < v1 ? cnt[v] : 0.f;
       lv[u] = v < v1 ? lg[v] : 0.f;
+      if (forbid && v < v1 && ((forbid[v >> 5] >> (v & 31)) & 1u)) lv[u] = -INFINITY;
     }
 #pragma unroll
     for (int u = 0; u < kRoundsAhead; ++u) {
@@ -527,7 +531,8 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
 // One launch of the sampler over m rows (shared by cbd_step, cbd_sample and
 // cbd_sample_static).
 cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
-                           const SampDev* samp, float* scratch, int32_t* out_tokens, int32_t* err, cudaStream_t s) {
+                           const SampDev* samp, float* scratch, const uint32_t* forbid, int32_t* out_tokens,
+                           int32_t* err, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
   static bool attr = false;
   if (!attr) {
@@ -549,12 +554,13 @@ cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, c
   at[1].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, sampler_kernel, logits, V, counters, slots, samp, scratch, out_tokens, err);
+  return cudaLaunchKernelEx(&cfg, sampler_kernel, logits, V, counters, slots, samp, scratch, forbid, out_tokens, err);
 }
 
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
                            const SampDev* samp, int32_t* out_tokens, cudaStream_t s) {
-  return sampler_launch(logits, m, e->dm.V, e->counters, slots, samp, e->samp_scratch, out_tokens, e->err, s);
+  return sampler_launch(logits, m, e->dm.V, e->counters, slots, samp, e->samp_scratch,
+                        e->n_forbidden > 0 ? e->forbid : nullptr, out_tokens, e->err, s);
 }
 
 }  // namespace cbd

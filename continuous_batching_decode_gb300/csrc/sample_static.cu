@@ -26,7 +26,8 @@ namespace cbd {
 
 // The sampler launch of k_sampler.cu (same kernel as cbd_sample).
 cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
-                           const SampDev* samp, float* scratch, int32_t* out_tokens, int32_t* err, cudaStream_t s);
+                           const SampDev* samp, float* scratch, const uint32_t* forbid, int32_t* out_tokens,
+                           int32_t* err, cudaStream_t s);
 
 namespace {
 
@@ -108,8 +109,8 @@ extern "C" cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t 
     ce = cudaMemcpyAsync(area + kSlotOff, sl, (size_t)m * sizeof(int32_t), cudaMemcpyHostToDevice, s);
   if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: parameter copy: %s", cudaGetErrorString(ce));
   ce = sampler_launch(logits, m, vocab, counters, reinterpret_cast<const int32_t*>(area + kSlotOff),
-                      reinterpret_cast<const SampDev*>(area + kSampOff), reinterpret_cast<float*>(area), out_tokens,
-                      nullptr, s);
+                      reinterpret_cast<const SampDev*>(area + kSampOff), reinterpret_cast<float*>(area), nullptr,
+                      out_tokens, nullptr, s);
   if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: launch: %s", cudaGetErrorString(ce));
   return CBD_OK;
 }

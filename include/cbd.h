@@ -138,6 +138,17 @@ cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_ma
  * 128-position chunks and the same merge order. */
 cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path);
 
+/* Forbidden tokens (the Albatross worker masks them before the penalties,
+ * "RWKV Runner Albatross 后端", section 连续批处理：Worker 主循环, step 6):
+ * token ids that the sampler of cbd_step, cbd_batch_run and cbd_sample
+ * never draws -- as if their logits were -inf before the penalty, so they
+ * carry no probability mass and greedy rows skip them.  The returned logits
+ * stay raw.  ids: host [n], 0 <= id < vocab, copied; n == 0 clears the mask;
+ * at least one id must stay allowed.  Waits for the device to be idle, so
+ * every step launched afterwards sees the new mask.  cbd_sample_static does
+ * not apply it. */
+cbd_status cbd_engine_set_forbidden(cbd_engine* e, const int32_t* ids, int32_t n);
+
 /* RMSNorm fused into the weight contractions (default on): on the tcgen05
  * path the embedding and the residual epilogues write the next norm's input
  * x * g (hi + lo bf16) and per-row partial sums of x^2, and the QKV and

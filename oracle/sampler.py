@@ -24,6 +24,12 @@ states one (each is a reading listed in the design notes):
    (fp32), then the drawn token's entry gains 1.0 (fp32).
 
 Greedy and sampled rows both update the counters.
+
+Forbidden tokens (section "Worker 主循环" masks them before the penalties):
+0. A forbidden id is removed from the candidates before step 1 -- its logit
+   counts as -inf, so it is never the greedy choice, carries no probability
+   and is never drawn; the remaining steps run over the other ids unchanged.
+   The counters of forbidden ids still decay like every other entry.
 """
 from __future__ import annotations
 
@@ -92,9 +98,17 @@ def draw(kept_ids, kept_p, u: float) -> int:
     return int(kept_ids[min(j, len(kept_ids) - 1)])
 
 
-def sample_row(logits, counters, p: SamplingParams, u: float) -> int:
-    """Steps 1-5 for one row; returns the token id."""
-    l2 = penalize(logits, counters, p.presence_penalty, p.frequency_penalty)
+def mask_forbidden(logits, forbidden) -> np.ndarray:
+    """Step 0: forbidden ids get -inf (fp32)."""
+    l = np.array(logits, dtype=np.float32)
+    if forbidden is not None and len(forbidden):
+        l[np.asarray(forbidden, dtype=np.int64)] = -np.inf
+    return l
+
+
+def sample_row(logits, counters, p: SamplingParams, u: float, forbidden=None) -> int:
+    """Steps 0-5 for one row; returns the token id."""
+    l2 = penalize(mask_forbidden(logits, forbidden), counters, p.presence_penalty, p.frequency_penalty)
     if is_greedy(p):
         return int(np.argmax(l2))            # argmax returns the first maximum
     ids, pk, _ = kept_set(l2, p)

@@ -335,3 +335,58 @@ def test_multi_chunk_rows_and_l2_prefetch(tiny):
         kv = {s: om.SequenceKV(om_.cfg, 320)}
         zo.append(om.prefill(om_, kv, s, p))
     gu.assert_logits_close(res[0], np.array(zo), "multi-chunk rows")
+
+
+def test_forbidden_tokens_on_gpu(tiny):
+    """The engine's forbidden-token mask: ids the oracle sampler (step 0,
+    forbidden ids removed before the penalty) gives for the same logits,
+    counters and uniforms; forbidden ids never drawn; counters updated the
+    same way; clearing the mask restores the unmasked draw."""
+    rng = np.random.default_rng(21)
+    V = tiny.shape["vocab"]
+    cv = gu.counters_view(tiny)
+    configs = [dict(temperature=0.0, frequency_penalty=1.0, penalty_decay=0.996),
+               dict(temperature=1.0, top_p=0.3, frequency_penalty=1.0, penalty_decay=0.996),
+               dict(temperature=0.8, top_p=0.95, top_k=20, presence_penalty=0.5, penalty_decay=0.99)]
+    m = 6
+    mism = checked = 0
+    try:
+        for trial in range(8):
+            lg = rng.normal(0, 2.0, (m, V)).astype(np.float32)
+            c0 = np.where(rng.random((8, V)) < 0.05, rng.integers(1, 5, (8, V)), 0).astype(np.float32)
+            # forbid every row's top few raw logits plus random ids
+            bad = sorted(set(np.argsort(-lg, axis=1)[:, :3].ravel().tolist()) |
+                         set(rng.choice(V, 40, replace=False).tolist()))
+            cbd.engine_set_forbidden(tiny.e, bad)
+            cv.copy_(torch.from_numpy(c0).cuda())
+            slots = list(rng.permutation(8)[:m])
+            samp = [dict(configs[j % 3], seed=trial, request_id=500 + j, token_index=trial) for j in range(m)]
+            us = [float(rng.random()) for _ in range(m)]
+            out = torch.zeros(m, dtype=torch.int32, device="cuda")
+            cbd.sample(tiny.e, torch.from_numpy(lg).cuda(), slots, samp, us, out)
+            cbd.engine_check(tiny.e)
+            toks = out.cpu().numpy()
+            post = cv.cpu().numpy()
+            assert not set(toks.tolist()) & set(bad)
+            for j in range(m):
+                p = gu.sampling_params(samp[j])
+                s = slots[j]
+                np.testing.assert_array_equal(post[s], osamp.update_counters(c0[s], int(toks[j]), p.penalty_decay))
+                checked += 1
+                if gu.sampling_near_tie(osamp.mask_forbidden(lg[j], bad), c0[s], p, us[j]):
+                    continue
+                mism += int(toks[j] != osamp.sample_row(lg[j], c0[s], p, us[j], forbidden=bad))
+        assert mism == 0, f"{mism} of {checked} ids differ"
+        # cleared: the greedy row takes its raw argmax again
+        cbd.engine_set_forbidden(tiny.e, [])
+        cv.zero_()
+        lg = rng.normal(0, 2.0, (1, V)).astype(np.float32)
+        out = torch.zeros(1, dtype=torch.int32, device="cuda")
+        cbd.sample(tiny.e, torch.from_numpy(lg).cuda(), [0], [dict(temperature=0.0)], None, out)
+        assert int(out.cpu()[0]) == int(np.argmax(lg[0]))
+        with pytest.raises(cbd.CbdError):
+            cbd.engine_set_forbidden(tiny.e, list(range(V)))       # nothing left to draw
+        with pytest.raises(cbd.CbdError):
+            cbd.engine_set_forbidden(tiny.e, [V])
+    finally:
+        cbd.engine_set_forbidden(tiny.e, [])

@@ -124,3 +124,42 @@ def test_counter_decay_of_other_tokens():
     assert c2[0] == np.float32(np.float32(1.0) * np.float32(0.996))
     assert c2[2] == np.float32(np.float32(5.0) * np.float32(0.996))
     assert c2[1] == np.float32(1.0)
+
+
+# ---------------------------------------------------------------- forbidden tokens
+def test_forbidden_greedy_takes_the_best_allowed():
+    l = np.array([0.5, 3.0, 2.0, 2.5, -1.0], np.float32)
+    c = np.zeros(5, np.float32)
+    p = os_.SamplingParams(temperature=0.0, frequency_penalty=0.0)
+    assert os_.sample_row(l, c, p, 0.5) == 1
+    assert os_.sample_row(l, c, p, 0.5, forbidden=[1]) == 3
+    assert os_.sample_row(l, c, p, 0.5, forbidden=[1, 3]) == 2
+    assert os_.sample_row(l, c, p, 0.5, forbidden=[0, 1, 2, 3]) == 4     # the only allowed id
+
+
+def test_forbidden_equals_removing_the_ids_from_the_vocabulary():
+    """With ids removed, sampling over the rest (renumbered) is the same draw:
+    the mask reduces to the unmasked algorithm on a smaller vocabulary."""
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        V = 40
+        l = rng.normal(0, 2, V).astype(np.float32)
+        c = np.where(rng.random(V) < 0.2, rng.integers(1, 4, V), 0).astype(np.float32)
+        bad = sorted(rng.choice(V, size=int(rng.integers(1, 12)), replace=False).tolist())
+        keep = np.array([i for i in range(V) if i not in bad])
+        p = os_.SamplingParams(temperature=float(rng.choice([0.0, 0.7, 1.0])), top_p=float(rng.choice([0.3, 0.9, 1.0])),
+                             top_k=int(rng.choice([0, 5])), frequency_penalty=0.5, presence_penalty=0.25)
+        u = float(rng.random())
+        got = os_.sample_row(l, c, p, u, forbidden=bad)
+        ref = int(keep[os_.sample_row(l[keep], c[keep], p, u)])
+        assert got == ref and got not in bad
+
+
+def test_forbidden_ids_are_never_drawn():
+    rng = np.random.default_rng(4)
+    l = np.zeros(16, np.float32)
+    l[3] = 5.0                                     # would dominate the nucleus
+    c = np.zeros(16, np.float32)
+    p = os_.SamplingParams(temperature=1.0, top_p=1.0, frequency_penalty=0.0)
+    seen = {os_.sample_row(l, c, p, float(rng.random()), forbidden=[3, 7]) for _ in range(500)}
+    assert not seen & {3, 7} and len(seen) >= 12
