@@ -12,10 +12,15 @@ one pass of the whole step (embedding, 32 layers, LM head, sampler) for all
 B rows; the weights (14.5 GB) and KV (~9 GB) are far larger than L2, so no
 flush is needed between steps.
 
-value  = B * n_gpus / step time, inputs resident on the device (Batch API).
+value  = B * n_gpus / step time, inputs resident on the device (Batch API),
+         each step replayed as one CUDA graph of the same kernels
+         (cbd_batch_set_graph); the launch-by-launch time is reported in
+         "graph".
 e2e    = the same through cbd_step with host arrays: the step's rows, block
          tables and sampling parameters go host->device and the sampled
-         tokens come back device->host inside every timed step.
+         tokens come back device->host inside every timed step (steps run as
+         cached graphs, cbd_engine_set_step_graph; the launch-by-launch time
+         is reported beside).
 Multi-GPU: independent replicas (one engine per GPU, no collective on the
 data path); barrier + max-over-ranks timing.
 
@@ -359,6 +364,24 @@ def run_cbd(args):
     stream = torch.cuda.current_stream()
     b = cbd.batch_create(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"])
     out = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # launch by launch (the PDL chain enqueued kernel by kernel): reported beside
+    for _ in range(args.warmup):
+        cbd.batch_run(e, pool, b, out)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    th0 = time.perf_counter()
+    for _ in range(args.steps):
+        cbd.batch_run(e, pool, b, out)
+    lbl_host_us = (time.perf_counter() - th0) / args.steps * 1e6
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    lbl = {"ms_per_step": round(ev0.elapsed_time(ev1) / args.steps, 4),
+           "host_enqueue_us_per_step": round(lbl_host_us, 1)}
+    cbd.engine_check(e)
+    # the timed steps replay the step as one CUDA graph (cbd_batch_set_graph:
+    # the same kernels and programmatic edges, one host launch per step)
+    cbd.batch_set_graph(b, True)
     for _ in range(args.warmup):
         cbd.batch_run(e, pool, b, out)
     torch.cuda.synchronize()
@@ -369,10 +392,11 @@ def run_cbd(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    th0 = time.perf_counter()
     for _ in range(args.steps):
         cbd.batch_run(e, pool, b, out)
+    host_us = (time.perf_counter() - th0) / args.steps * 1e6
     ev1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -384,6 +408,10 @@ def run_cbd(args):
     ms = replicas.max_over_ranks(ms_local, dist, "cuda")
     value = replicas.job_throughput(float(B), ms_local / 1000.0, dist, "cuda")
     launches = cbd.batch_launches(b) * args.steps
+
+    graph = {"replay": True, "host_enqueue_us_per_step": round(host_us, 1), "captures": cbd.batch_captures(b),
+             "launch_by_launch": lbl}
+    cbd.batch_set_graph(b, False)
 
     # per-kernel live timing (same batch, same stream, CUDA events per launch)
     cbd.engine_profile(e, True)
@@ -420,25 +448,32 @@ def run_cbd(args):
     e2e = None
     if not args.no_e2e:
         host_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
-        for _ in range(2):
-            cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
-            host_tok.copy_(out, non_blocking=True)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        t0 = time.perf_counter()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
-            host_tok.copy_(out, non_blocking=True)
-            stream.synchronize()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        wall = (time.perf_counter() - t0) / args.steps * 1000.0
-        e_ms = replicas.max_over_ranks(max(ev0.elapsed_time(ev1) / args.steps, wall), dist, "cuda")
+
+        def e2e_ms():
+            for _ in range(3):
+                cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
+                host_tok.copy_(out, non_blocking=True)
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
+                host_tok.copy_(out, non_blocking=True)
+                stream.synchronize()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            wall = (time.perf_counter() - t0) / args.steps * 1000.0
+            return replicas.max_over_ranks(max(ev0.elapsed_time(ev1) / args.steps, wall), dist, "cuda")
+        lbl_ms = e2e_ms()                       # launch by launch
+        cbd.engine_set_step_graph(e, True)      # each cbd_step as one cached graph
+        e_ms = e2e_ms()
+        cbd.engine_set_step_graph(e, False)
         h2d = len(wl["rows"]) * 20 + wl["tables"].nbytes + wl["nbps"].nbytes + len(wl["samp"]) * 48
         e2e = {"value": B * world / (e_ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": B * 4, "ms_per_step": round(e_ms, 4)}
+               "d2h_bytes_per_step": B * 4, "ms_per_step": round(e_ms, 4), "step_graph": True,
+               "launch_by_launch_ms_per_step": round(lbl_ms, 4)}
         cbd.engine_check(e)
 
     cpu = None
@@ -480,7 +515,7 @@ def run_cbd(args):
             "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path,
                            l2_prefetch_mb=args.l2_prefetch_mb),
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu}
+            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "graph": graph}
     if rank == 0:
         print(json.dumps(line), flush=True)
     for Bs in [int(x) for x in args.sweep.split(",") if x.strip()]:

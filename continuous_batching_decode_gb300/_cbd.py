@@ -120,6 +120,10 @@ PROTOS = {
     "cbd_batch_run": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "cbd_batch_destroy": (c_i32, [c_vp]),
     "cbd_batch_launches": (c_i32, [c_vp, _P(c_i32)]),
+    "cbd_batch_set_graph": (c_i32, [c_vp, c_i32]),
+    "cbd_engine_set_step_graph": (c_i32, [c_vp, c_i32]),
+    "cbd_engine_step_graph_captures": (c_i32, [c_vp, _P(c_i32)]),
+    "cbd_batch_captures": (c_i32, [c_vp, _P(c_i32)]),
     "cbd_sample": (c_i32, [c_vp, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
     "cbd_sample_static": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
     "cbd_sched_create": (c_i32, [_P(SchedConfig), _P(c_vp)]),
@@ -348,6 +352,26 @@ def batch_destroy(b) -> None:
 def batch_launches(b) -> int:
     n = c_i32()
     _check(lib().cbd_batch_launches(b, ctypes.byref(n)))
+    return n.value
+
+
+def batch_set_graph(b, enable: bool = True) -> None:
+    _check(lib().cbd_batch_set_graph(b, 1 if enable else 0))
+
+
+def engine_set_step_graph(e, enable: bool = True) -> None:
+    _check(lib().cbd_engine_set_step_graph(e, 1 if enable else 0))
+
+
+def engine_step_graph_captures(e) -> int:
+    n = c_i32()
+    _check(lib().cbd_engine_step_graph_captures(e, ctypes.byref(n)))
+    return n.value
+
+
+def batch_captures(b) -> int:
+    n = c_i32()
+    _check(lib().cbd_batch_captures(b, ctypes.byref(n)))
     return n.value
 
 

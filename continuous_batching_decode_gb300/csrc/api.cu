@@ -366,6 +366,9 @@ extern "C" cbd_status cbd_engine_destroy(cbd_engine* e) {
   if (e->arena) cudaFree(e->arena);
   for (auto& r : e->prof_recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
   for (auto ev : e->prof_free) cudaEventDestroy(ev);
+  for (auto& cache : e->step_graphs)
+    for (auto& g : cache) cudaGraphExecDestroy(g.exec);
+  if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
   delete e->step_batch;
   delete e;
   return CBD_OK;
@@ -427,6 +430,7 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
   if (path < 0 || path > 2) return fail(CBD_EINVAL, "gemm path must be 0, 1 or 2");
   if (gemv_max_rows < 0) return fail(CBD_EINVAL, "gemv_max_rows must be >= 0");
   e->gemm_path = path;
+  ++e->epoch;
   e->gemv_max_rows = gemv_max_rows;
   return CBD_OK;
 }
@@ -436,6 +440,7 @@ extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path)
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   if (path < 0 || path > 2) return fail(CBD_EINVAL, "attention path must be 0, 1 or 2");
   e->attn_path = path;
+  ++e->epoch;
   return CBD_OK;
 }
 
@@ -443,6 +448,7 @@ extern "C" cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   e->fuse_norm = enable != 0;
+  ++e->epoch;
   return CBD_OK;
 }
 
@@ -466,6 +472,7 @@ extern "C" cbd_status cbd_engine_set_forbidden(cbd_engine* e, const int32_t* ids
   if (ce == cudaSuccess) ce = cudaMemcpy(e->forbid, bits.data(), bits.size() * 4, cudaMemcpyHostToDevice);
   if (ce != cudaSuccess) return cuda_fail(ce, "forbidden-token mask");
   e->n_forbidden = distinct;
+  ++e->epoch;
   return CBD_OK;
 }
 
@@ -475,6 +482,7 @@ extern "C" cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes) 
   if (bytes > ((uint64_t)1 << 30)) return fail(CBD_EINVAL, "prefetch of %llu bytes is more than 1 GiB",
                                               (unsigned long long)bytes);
   e->l2_prefetch = (size_t)bytes;
+  ++e->epoch;
   return CBD_OK;
 }
 
@@ -859,12 +867,82 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
   if (img.bytes.size() > sg.bytes) return fail(CBD_EUNSUPPORTED, "step image larger than the staging buffer");
   CBD_CUDA(cudaEventSynchronize(sg.done));  // the step that last used this buffer has finished
   std::memcpy(sg.host, img.bytes.data(), img.bytes.size());
+  if (e->step_graph && !e->prof) {
+    // the upload and the launches as one graph: its kernels' arguments
+    // depend only on the image layout, this staging buffer, the pool, the
+    // outputs and the engine settings, which together make the key
+    const uint64_t key[cbd_engine::kStepGraphKey] = {
+        (uint64_t)img.n_rows, (uint64_t)img.m, (uint64_t)img.n_work, (uint64_t)img.table_slots,
+        (uint64_t)img.max_chunks, (uint64_t)img.bytes.size(), reinterpret_cast<uint64_t>(pool),
+        reinterpret_cast<uint64_t>(out_tokens), reinterpret_cast<uint64_t>(out_logits), e->epoch};
+    auto& cache = e->step_graphs[&sg - e->stage];
+    cbd_engine::StepGraph* hit = nullptr;
+    for (auto& g : cache)
+      if (std::memcmp(g.key, key, sizeof(key)) == 0) hit = &g;
+    if (!hit) {
+      bind_batch(e->step_batch, img, sg.dev);
+      if (!e->cap_stream) CBD_CUDA(cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking));
+      CBD_CUDA(cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeRelaxed));
+      cudaError_t cc = cudaMemcpyAsync(sg.dev, sg.host, img.bytes.size(), cudaMemcpyHostToDevice, e->cap_stream);
+      cbd_status cs = cc == cudaSuccess ? run_batch(e, pool, e->step_batch, out_tokens, out_logits, e->cap_stream)
+                                        : cuda_fail(cc, "staging upload");
+      cudaGraph_t g = nullptr;
+      const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &g);
+      if (cs) {
+        if (g) cudaGraphDestroy(g);
+        return cs;
+      }
+      if (ce != cudaSuccess) return cuda_fail(ce, "graph capture");
+      cudaGraphExec_t exec = nullptr;
+      const cudaError_t ci = cudaGraphInstantiate(&exec, g, 0);
+      cudaGraphDestroy(g);
+      if (ci != cudaSuccess) return cuda_fail(ci, "graph instantiation");
+      if (cache.size() >= cbd_engine::kStepGraphCache) {     // drop the least recently used
+        size_t lru = 0;
+        for (size_t i = 1; i < cache.size(); ++i)
+          if (cache[i].last_use < cache[lru].last_use) lru = i;
+        cudaGraphExecDestroy(cache[lru].exec);
+        cache.erase(cache.begin() + (ptrdiff_t)lru);
+      }
+      cbd_engine::StepGraph ng{};
+      std::memcpy(ng.key, key, sizeof(key));
+      ng.exec = exec;
+      cache.push_back(ng);
+      hit = &cache.back();
+      ++e->step_graph_captures;
+    }
+    hit->last_use = ++e->step_graph_clock;
+    CBD_CUDA(cudaGraphLaunch(hit->exec, s));
+    CBD_CUDA(cudaEventRecord(sg.done, s));
+    return CBD_OK;
+  }
   CBD_CUDA(cudaMemcpyAsync(sg.dev, sg.host, img.bytes.size(), cudaMemcpyHostToDevice, s));
   bind_batch(e->step_batch, img, sg.dev);
   st = run_batch(e, pool, e->step_batch, out_tokens, out_logits, s);
   cudaError_t ce = cudaEventRecord(sg.done, s);
   if (st) return st;
   if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventRecord");
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_step_graph(cbd_engine* e, int32_t enable) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  e->step_graph = enable != 0;
+  if (!e->step_graph) {
+    CBD_CUDA(cudaDeviceSynchronize());
+    for (auto& cache : e->step_graphs) {
+      for (auto& g : cache) cudaGraphExecDestroy(g.exec);
+      cache.clear();
+    }
+  }
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_step_graph_captures(cbd_engine* e, int32_t* n) {
+  clear_error();
+  if (!e || !n) return fail(CBD_EINVAL, "NULL argument");
+  *n = e->step_graph_captures;
   return CBD_OK;
 }
 
@@ -897,12 +975,61 @@ extern "C" cbd_status cbd_batch_create(cbd_engine* e, cbd_kv_pool* pool, const c
   return CBD_OK;
 }
 
+static void drop_graph(cbd_batch* b) {
+  if (b->exec) cudaGraphExecDestroy(b->exec);
+  b->exec = nullptr;
+}
+
 extern "C" cbd_status cbd_batch_run(cbd_engine* e, cbd_kv_pool* pool, cbd_batch* b, int32_t* out_tokens,
                                     float* out_logits, void* stream) {
   clear_error();
   if (!e || !pool || !b) return fail(CBD_EINVAL, "NULL argument");
   if (pool->e != e) return fail(CBD_EINVAL, "pool belongs to another engine");
-  return run_batch(e, pool, b, out_tokens, out_logits, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!b->graph_on || e->prof) return run_batch(e, pool, b, out_tokens, out_logits, s);
+  if (!b->exec || b->g_epoch != e->epoch || b->g_pool != pool || b->g_tok != out_tokens || b->g_lg != out_logits) {
+    // capture the launch sequence on a private stream (nothing executes),
+    // then instantiate it; the graph is replayed into the caller's stream
+    drop_graph(b);
+    if (!e->cap_stream) CBD_CUDA(cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking));
+    CBD_CUDA(cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeRelaxed));
+    const cbd_status st = run_batch(e, pool, b, out_tokens, out_logits, e->cap_stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(e->cap_stream, &g);
+    if (st) {
+      if (g) cudaGraphDestroy(g);
+      return st;
+    }
+    if (ce != cudaSuccess) return cuda_fail(ce, "graph capture");
+    const cudaError_t ci = cudaGraphInstantiate(&b->exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ci != cudaSuccess) {
+      b->exec = nullptr;
+      return cuda_fail(ci, "graph instantiation");
+    }
+    b->g_epoch = e->epoch;
+    b->g_pool = pool;
+    b->g_tok = out_tokens;
+    b->g_lg = out_logits;
+    ++b->captures;
+  }
+  CBD_CUDA(cudaGraphLaunch(b->exec, s));
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_batch_set_graph(cbd_batch* b, int32_t enable) {
+  clear_error();
+  if (!b) return fail(CBD_EINVAL, "batch is NULL");
+  b->graph_on = enable != 0;
+  if (!b->graph_on) drop_graph(b);
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_batch_captures(cbd_batch* b, int32_t* n) {
+  clear_error();
+  if (!b || !n) return fail(CBD_EINVAL, "NULL argument");
+  *n = b->captures;
+  return CBD_OK;
 }
 
 extern "C" cbd_status cbd_batch_destroy(cbd_batch* b) {
@@ -911,6 +1038,7 @@ extern "C" cbd_status cbd_batch_destroy(cbd_batch* b) {
     cudaDeviceSynchronize();
     cudaFree(b->dev);
   }
+  drop_graph(b);
   delete b;
   return CBD_OK;
 }

@@ -160,6 +160,19 @@ struct cbd_engine {
   } stage[2];
   int stage_idx = 0;
   cbd_batch* step_batch = nullptr;    // batch object reused by cbd_step
+  // cbd_step as CUDA graphs (cbd_engine_set_step_graph): per staging buffer,
+  // a few graphs keyed by everything their launches bake in
+  static constexpr int kStepGraphKey = 10;
+  static constexpr size_t kStepGraphCache = 8;
+  struct StepGraph {
+    uint64_t key[kStepGraphKey];
+    cudaGraphExec_t exec;
+    uint64_t last_use;
+  };
+  bool step_graph = false;
+  std::vector<StepGraph> step_graphs[2];
+  uint64_t step_graph_clock = 0;
+  int32_t step_graph_captures = 0;
   // tcgen05 GEMM: tensor maps (built once), partial tiles, counters
   std::vector<CUtensorMap> tmaps;     // per layer: qkv, o, gu, down; then lm_head; then activations
   cbd::TcWork tcw{};
@@ -169,6 +182,8 @@ struct cbd_engine {
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
+  uint64_t epoch = 1;                 // bumped by every setting that changes the launch sequence
+  cudaStream_t cap_stream = nullptr;  // private stream for graph capture
   // optional per-launch timing (cbd_engine_profile)
   bool prof = false;
   struct ProfRec { int cls; cudaEvent_t a, b; };
@@ -197,6 +212,14 @@ struct cbd_batch {
   cbd::AttnWork* work = nullptr;      // [n_work]
   int32_t* row_work = nullptr;        // [n_rows + 1] prefix: first work item of each row
   int32_t launches = 0;
+  // CUDA graph of one run's launch sequence (cbd_batch_set_graph)
+  bool graph_on = false;
+  cudaGraphExec_t exec = nullptr;
+  uint64_t g_epoch = 0;               // engine settings epoch the graph was captured under
+  const void* g_pool = nullptr;
+  const void* g_tok = nullptr;
+  const void* g_lg = nullptr;
+  int32_t captures = 0;
 };
 
 namespace cbd {

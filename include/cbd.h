@@ -290,6 +290,36 @@ cbd_status cbd_batch_destroy(cbd_batch* b);
 /* Number of kernel launches one run of this batch enqueues. */
 cbd_status cbd_batch_launches(cbd_batch* b, int32_t* n_launches);
 
+/* CUDA Graph replay of the batch's launch sequence (the CUDA-graph decode
+ * step that "RWKV Runner Albatross 后端" lists as follow-up work).  With
+ * enable != 0 the next cbd_batch_run captures the step's launches (stream
+ * capture on an engine-owned stream; nothing executes while capturing),
+ * instantiates them as one graph and launches it into `stream`; later runs
+ * with the same pool and output pointers and no engine setting changed since
+ * (GEMM or attention path, fused norm, L2 prefetch, forbidden tokens) launch
+ * the graph again, and any such change captures a new one.  The kernels and
+ * their programmatic-dependency edges are the same as without the graph, so
+ * results are bit-identical; the host enqueues one launch per step instead
+ * of one per kernel.  enable == 0 drops the graph.  Runs with per-launch
+ * profiling on (cbd_engine_profile) do not use the graph. */
+cbd_status cbd_batch_set_graph(cbd_batch* b, int32_t enable);
+/* How many graphs this batch has captured so far. */
+cbd_status cbd_batch_captures(cbd_batch* b, int32_t* n);
+
+/* cbd_step through CUDA graphs: with enable != 0 each cbd_step still
+ * validates its inputs and lays out its staging image on the host, then
+ * launches one graph that uploads the image and runs the step's kernels.
+ * Graphs are cached per staging buffer (up to 8 each, least recently used
+ * dropped), keyed by the step's shape (rows, sampled rows, attention work
+ * items, table slots, longest chunk list, image size), the pool, the output
+ * pointers and the engine settings; a new key captures a new graph (about
+ * the cost of one launch-by-launch step).  Results are bit-identical to the
+ * launch-by-launch step.  enable == 0 frees the cached graphs (waits for
+ * the device).  Not used while per-launch profiling is on. */
+cbd_status cbd_engine_set_step_graph(cbd_engine* e, int32_t enable);
+/* Graphs captured so far by cbd_step (all keys, all staging buffers). */
+cbd_status cbd_engine_step_graph_captures(cbd_engine* e, int32_t* n);
+
 /* Sample m rows of given logits with the same kernel cbd_step uses.
  *   logits (device) [m][V] fp32 (raw); slots (host) [m], distinct;
  *   sampling (host) [m]; uniforms (host, nullable) [m]; out_tokens (device) [m].

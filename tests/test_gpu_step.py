@@ -31,6 +31,7 @@ def tiny(request):
     m = gu.Model("tiny", max_rows=512, max_slots=8, mbps=16)
     cbd.engine_set_gemm_path(m.e, request.param[0])
     cbd.engine_set_attention_path(m.e, request.param[1])
+    m.attn_path = request.param[1]
     yield m
     m.close()
 
@@ -390,3 +391,85 @@ def test_forbidden_tokens_on_gpu(tiny):
             cbd.engine_set_forbidden(tiny.e, [V])
     finally:
         cbd.engine_set_forbidden(tiny.e, [])
+
+
+def test_batch_graph_replay_is_bit_identical(tiny):
+    """cbd_batch_set_graph: the captured graph replays the same kernels, so
+    tokens and logits are bit-identical to the launch-by-launch run; a
+    changed engine setting or output pointer captures a new graph."""
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
+    cv = gu.counters_view(tiny)
+    V = tiny.shape["vocab"]
+    m = sum(1 for r in rows if r[4])
+    b = cbd.batch_create(tiny.e, pool.p, rows, tables, nbps, sampling)
+    try:
+        def run(lg):
+            cv.zero_()
+            tok = torch.zeros(m, dtype=torch.int32, device="cuda")
+            cbd.batch_run(tiny.e, pool.p, b, tok, lg)
+            cbd.engine_check(tiny.e)
+            return tok.cpu().numpy(), lg.cpu().numpy()
+        lg1 = torch.zeros(m, V, dtype=torch.float32, device="cuda")
+        t0, z0 = run(lg1)
+        cbd.batch_set_graph(b, True)
+        for _ in range(3):
+            t, z = run(lg1)
+            np.testing.assert_array_equal(t, t0)
+            np.testing.assert_array_equal(z, z0)
+        assert cbd.batch_captures(b) == 1
+        cbd.engine_set_attention_path(tiny.e, tiny.attn_path)
+        t, z = run(lg1)                      # a setting changed: captured again
+        assert cbd.batch_captures(b) == 2
+        np.testing.assert_array_equal(z, z0)
+        lg2 = torch.zeros(m, V, dtype=torch.float32, device="cuda")
+        t, z = run(lg2)                      # another output buffer: captured again
+        assert cbd.batch_captures(b) == 3
+        np.testing.assert_array_equal(t, t0)
+        np.testing.assert_array_equal(z, z0)
+        cbd.batch_set_graph(b, False)
+        t, z = run(lg1)
+        np.testing.assert_array_equal(z, z0)
+    finally:
+        cbd.batch_destroy(b)
+        pool.close()
+
+
+def test_step_graph_is_bit_identical(tiny):
+    """cbd_engine_set_step_graph: cbd_step uploads and runs through cached
+    graphs with results bit-identical to the launch-by-launch step; one
+    capture per (shape, staging buffer), reused afterwards."""
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 5)
+    cv = gu.counters_view(tiny)
+    V = tiny.shape["vocab"]
+    m = sum(1 for r in rows if r[4])
+    tok = torch.zeros(m, dtype=torch.int32, device="cuda")
+    lg = torch.zeros(m, V, dtype=torch.float32, device="cuda")
+
+    def run(rws):
+        cv.zero_()
+        k = sum(1 for r in rws if r[4])
+        cbd.step(tiny.e, pool.p, rws, tables, nbps, sampling[:k], None, tok, lg)
+        cbd.engine_check(tiny.e)
+        return tok[:k].cpu().numpy(), lg[:k].cpu().numpy()
+    try:
+        t0, z0 = run(rows)
+        c0 = cbd.engine_step_graph_captures(tiny.e)
+        cbd.engine_set_step_graph(tiny.e, True)
+        for i in range(4):
+            t, z = run(rows)
+            np.testing.assert_array_equal(t, t0)
+            np.testing.assert_array_equal(z, z0)
+        assert cbd.engine_step_graph_captures(tiny.e) - c0 == 2        # one per staging buffer
+        short = rows[:3]                                                # another shape: new graphs
+        ts, zs = run(short)
+        ts, zs = run(short)
+        assert cbd.engine_step_graph_captures(tiny.e) - c0 == 4
+        t, z = run(rows)                                                # the first shape is still cached
+        assert cbd.engine_step_graph_captures(tiny.e) - c0 == 4
+        np.testing.assert_array_equal(z, z0)
+        cbd.engine_set_step_graph(tiny.e, False)
+        t1, z1 = run(short)
+        np.testing.assert_array_equal(z1, zs)
+    finally:
+        cbd.engine_set_step_graph(tiny.e, False)
+        pool.close()
