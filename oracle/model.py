@@ -27,6 +27,13 @@ is KV storage to bf16, which mirrors the persistent bf16 KV state.
 Rows of one step are processed layer by layer: every row's k, v for a layer
 is stored before any row of that layer attends, so a prefill row at position
 p sees the earlier rows of its own chunk (causal chunked prefill).
+
+FP8 KV ("大模型推理为什么需要 Continuous Batching", section 6: quantising the
+KV cache, e.g. to FP8, fits more sequences at a small precision cost): with
+``kv_format="e4m3"`` K and V are stored as FP8 E4M3 values instead of bf16
+(round to nearest even, finite values beyond the largest magnitude 448
+saturate; no scale factor -- the page names none, and this model's K and V
+are O(1)).
 """
 from __future__ import annotations
 
@@ -64,6 +71,25 @@ def round_to_bf16(x) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
     m, e = np.frexp(x)
     return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def round_to_e4m3(x) -> np.ndarray:
+    """Round fp64 values to the nearest FP8 E4M3 value (ties to even), as fp64.
+
+    E4M3 (the OCP 8-bit format without infinities): sign, 4 exponent bits
+    with bias 7, 3 fraction bits.  A normal value 1.f * 2^E (E >= -6) has 4
+    significant bits, so its spacing is 2^(E-3); below 2^-6 the subnormals
+    are multiples of 2^-9.  The largest finite magnitude is 448 (exponent
+    field 15 with fraction 110; 111 there is NaN); larger finite inputs
+    saturate to +-448.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                     # a = m * 2^e, m in [0.5, 1): E = e - 1
+    quantum = np.maximum(e - 4, -9)        # log2 of the spacing at a
+    r = np.ldexp(np.rint(np.ldexp(a, -quantum)), quantum)
+    r = np.minimum(r, 448.0)
+    return np.where(np.isnan(x), x, np.copysign(r, x))
 
 
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
@@ -146,8 +172,11 @@ class OracleModel:
     LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm",
                   "w_gate", "w_up", "w_down")
 
-    def __init__(self, cfg: ModelConfig, weights, cache: bool = True):
+    def __init__(self, cfg: ModelConfig, weights, cache: bool = True, kv_format: str = "bf16"):
+        if kv_format not in ("bf16", "e4m3"):
+            raise ValueError(kv_format)
         self.cfg = cfg
+        self.kv_round = round_to_bf16 if kv_format == "bf16" else round_to_e4m3
         self._src = weights
         self._cache = {} if cache else None
 
@@ -198,8 +227,8 @@ def step(model: OracleModel, kv: dict, rows) -> np.ndarray:
         k = rope((h @ w["wk"].T).reshape(n, hkv, hd), pos, cfg.rope_base)
         v = (h @ w["wv"].T).reshape(n, hkv, hd)
         for r in range(n):                          # store all KV first
-            kv[slots[r]].K[l][pos[r]] = round_to_bf16(k[r])
-            kv[slots[r]].V[l][pos[r]] = round_to_bf16(v[r])
+            kv[slots[r]].K[l][pos[r]] = model.kv_round(k[r])
+            kv[slots[r]].V[l][pos[r]] = model.kv_round(v[r])
         o = np.empty((n, hq * hd))
         for r in range(n):                          # then attend causally
             S = kv[slots[r]]

@@ -223,6 +223,60 @@ def test_bf16_rounding_ties_to_even_and_matches_torch():
     np.testing.assert_array_equal(om.round_to_bf16(x.astype(np.float64)), ref)
 
 
+def e4m3_code_value(code: int) -> float:
+    """Value of an FP8 E4M3 bit pattern, straight from the format: sign bit,
+    exponent field E (4 bits, bias 7), fraction F (3 bits); E == 0 is
+    subnormal (F/8 * 2^-6); E == 15 with F == 7 is NaN; no infinities."""
+    sgn = -1.0 if code & 0x80 else 1.0
+    E, F = (code >> 3) & 0xF, code & 7
+    if E == 15 and F == 7:
+        return math.nan
+    if E == 0:
+        return sgn * F / 8 * 2.0 ** -6
+    return sgn * (1 + F / 8) * 2.0 ** (E - 7)
+
+
+def test_e4m3_rounding_against_the_format():
+    finite = sorted({e4m3_code_value(c) for c in range(256) if not math.isnan(e4m3_code_value(c))})
+    assert len(finite) == 253 and finite[-1] == 448.0 and finite[0] == -448.0   # +-0 collapse
+    vals = np.array(finite)
+    np.testing.assert_array_equal(om.round_to_e4m3(vals), vals)         # representable: unchanged
+    pos = [v for v in finite if v >= 0]
+    code_of = {e4m3_code_value(c): c for c in range(128)}
+    for lo, hi in zip(pos, pos[1:]):
+        mid = (lo + hi) / 2
+        even = lo if code_of[lo] % 2 == 0 else hi                          # ties to the even code
+        assert om.round_to_e4m3(mid) == even, (lo, hi)
+        assert om.round_to_e4m3(mid - (hi - lo) * 1e-6) == lo
+        assert om.round_to_e4m3(mid + (hi - lo) * 1e-6) == hi
+        assert om.round_to_e4m3(-mid) == -even
+    assert om.round_to_e4m3(470.0) == 448.0 and om.round_to_e4m3(1e9) == 448.0   # saturation
+    assert om.round_to_e4m3(-1e9) == -448.0
+    assert om.round_to_e4m3(2.0 ** -10) == 0.0 and om.round_to_e4m3(2.0 ** -10 + 1e-12) == 2.0 ** -9
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    x = np.random.default_rng(8).normal(0, 40, size=20000)
+    x = x[np.abs(x) <= 440]
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(om.round_to_e4m3(x.astype(np.float32).astype(np.float64)), ref)
+
+
+def test_e4m3_kv_format_rounds_stored_kv():
+    cfg, w = small_model(seed=3)
+    rows = [(0, 3, 0, 1), (0, 5, 1, 1)]
+    kv = {0: om.SequenceKV(cfg, 4)}
+    om.step(om.OracleModel(cfg, w, kv_format="e4m3"), kv, rows)
+    for l in range(cfg.n_layers):
+        K = kv[0].K[l][:2]
+        np.testing.assert_array_equal(om.round_to_e4m3(K), K)
+    kv_b = {0: om.SequenceKV(cfg, 4)}
+    om.step(om.OracleModel(cfg, w), kv_b, rows)
+    assert np.abs(kv_b[0].K[0][:2] - kv[0].K[0][:2]).max() > 0      # a different rounding is used
+    with pytest.raises(ValueError):
+        om.OracleModel(cfg, w, kv_format="fp16")
+
+
 # ------------------------------------------------------------- invariants
 def tiny_model(seed=0):
     from continuous_batching_decode_gb300 import synth
