@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
     ap.add_argument("--trace", action="store_true", help="serve the request trace (see the module docstring)")
     ap.add_argument("--trace-requests", type=int, default=2000)
     ap.add_argument("--trace-rate", type=float, default=0.0, help="requests/s (0: all arrive at t = 0)")
@@ -108,8 +110,9 @@ def weight_bytes(s):
     return L * per_layer + V * d * 2 + d * 2
 
 
-def kv_pos_bytes(s):
-    return 2 * s["n_layers"] * s["n_kv_heads"] * s["head_dim"] * 2
+def kv_pos_bytes(s, eb=2):
+    """K and V bytes of one cached position over all layers (eb bytes per element)."""
+    return 2 * s["n_layers"] * s["n_kv_heads"] * s["head_dim"] * eb
 
 
 def config_of(args, s, wl, world):
@@ -117,6 +120,7 @@ def config_of(args, s, wl, world):
     return {"workload": (f"{args.shape}-shaped pure-decode step, B={args.B}, ctx U[{args.ctx_lo},{args.ctx_hi}], "
                          "32-position blocks, top_p 0.3 sampling"),
             "B": args.B, "shape": args.shape, "layers": s["n_layers"], "mean_ctx": float(np.mean(wl["ctx"])),
+            "kv": "e4m3" if args.kv == "fp8" else "bf16",
             "l2": "inputs larger than L2 (weights 14.5 GB + KV); no flush",
             "parallelism": f"replicas x{world}"}
 
@@ -186,13 +190,13 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def kernel_bytes(cls, s, B, ctx):
+def kernel_bytes(cls, s, B, ctx, eb=2):
     """Algorithmic bytes one launch of a kernel class must move (7B: see the
     design notes for the per-unit figures)."""
     d, hq, hkv, hd, F, V = s["d_model"], s["n_heads"], s["n_kv_heads"], s["head_dim"], s["ffn_dim"], s["vocab"]
     act = lambda k: B * k * 2 * 2            # hi + lo bf16 activations read
     if cls == "gemm_qkv":
-        return (hq + 2 * hkv) * hd * d * 2 + act(d) + B * hq * hd * 4 + B * 2 * hkv * hd * 2
+        return (hq + 2 * hkv) * hd * d * 2 + act(d) + B * hq * hd * 4 + B * 2 * hkv * hd * eb
     if cls == "gemm_o":
         return d * hq * hd * 2 + act(hq * hd) + 2 * B * d * 4
     if cls == "gemm_gate_up":
@@ -202,7 +206,7 @@ def kernel_bytes(cls, s, B, ctx):
     if cls == "gemm_lm_head":
         return V * d * 2 + act(d) + B * V * 4
     if cls == "attention":
-        return sum(c + 1 for c in ctx) * hkv * hd * 2 * 2 + B * hq * hd * 4 + B * hq * hd * 2 * 2
+        return sum(c + 1 for c in ctx) * hkv * hd * 2 * eb + B * hq * hd * 4 + B * hq * hd * 2 * 2
     if cls == "sampler":
         return B * V * 4 * 4
     return None
@@ -213,20 +217,24 @@ def measured_traffic(cls, args):
     under profiles/ (dram__bytes_read + dram__bytes_write), when it was taken
     on this workload and the kernel's source is unchanged since; else None."""
     import hashlib
-    files = {"attention": ("attn_stream_7b_B32_2layer.md", "k_attn.cu")}
-    if cls not in files or (args.shape, args.B, args.ctx_lo, args.ctx_hi, args.seed) != ("7b", 32, 256, 4096, 0):
+    files = {"attention": ("attn_stream_7b_B32_2layer.md", ("k_attn.cu", "attn_stream.cuh"))}
+    if cls not in files or (args.shape, args.B, args.ctx_lo, args.ctx_hi, args.seed, args.kv) != \
+            ("7b", 32, 256, 4096, 0, "bf16"):
         return None
-    prof, src = files[cls]
+    prof, srcs = files[cls]
     try:
         text = open(os.path.join(ROOT, "profiles", prof)).read()
-        cur = hashlib.sha256(open(os.path.join(ROOT, "continuous_batching_decode_gb300", "csrc", src), "rb").read())
+        cur = hashlib.sha256()
+        for src in srcs:
+            cur.update(open(os.path.join(ROOT, "continuous_batching_decode_gb300", "csrc", src), "rb").read())
     except OSError:
         return None
+    key = "source_sha256 " + "+".join(srcs) + ":"
     val = sha = None
     for line in text.splitlines():
         if line.startswith("traffic_per_launch_bytes:"):
             val = int(line.split(":")[1])
-        if line.startswith(f"source_sha256 {src}:"):
+        if line.startswith(key):
             sha = line.split(":")[1].strip()
     return val if val is not None and sha == cur.hexdigest() else None
 
@@ -322,6 +330,8 @@ def run_reference(args):
 
 
 def run_cbd(args):
+    if args.kv == "fp8":
+        args.no_cpu_baseline = True      # the oracle sample reads a bf16 pool
     import torch
     import continuous_batching_decode_gb300 as cbd
     from continuous_batching_decode_gb300 import build, replicas, synth
@@ -346,7 +356,9 @@ def run_cbd(args):
     B = args.B
     wl = workload(s, B, args.ctx_lo, args.ctx_hi, args.seed)
     w = synth.make_weights(s, seed=args.seed, device="cuda")
-    cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"])
+    fp8 = args.kv == "fp8"
+    eb = 1 if fp8 else 2
+    cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"], kv_fp8=fp8)
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
     cbd.engine_set_attention_path(e, args.attn_path)
@@ -357,10 +369,11 @@ def run_cbd(args):
     pool = cbd.kv_pool_create(e, wl["n_pool"])
     base, nbytes, nb = cbd.kv_pool_data(pool)
     # [L][n_blocks][H_kv][K|V][32 * hd]: each tile in 128-byte-swizzled order
-    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "bf16")
+    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "u8" if fp8 else "bf16")
     gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
     for l in range(s["n_layers"]):
-        kv[l].copy_((torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3).to(torch.bfloat16))
+        r = torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3
+        kv[l].copy_(r.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else r.to(torch.bfloat16))
     stream = torch.cuda.current_stream()
     b = cbd.batch_create(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"])
     out = torch.zeros(B, dtype=torch.int32, device="cuda")
@@ -424,7 +437,7 @@ def run_cbd(args):
     ranked = sorted(((v[1], k) for k, v in prof.items()), reverse=True)
     roof = None
     for _, k in ranked:
-        byt = kernel_bytes(k, s, B, wl["ctx"])
+        byt = kernel_bytes(k, s, B, wl["ctx"], eb)
         if byt:
             n_l, tot = prof[k]
             avg_s = tot / n_l / 1000.0
@@ -434,7 +447,7 @@ def run_cbd(args):
                     "bytes_per_launch": byt, "avg_launch_us": round(avg_s * 1e6, 2)}
             break
     W = weight_bytes(s)
-    A = sum(c + 1 for c in wl["ctx"]) * kv_pos_bytes(s)
+    A = sum(c + 1 for c in wl["ctx"]) * kv_pos_bytes(s, eb)
     step_bytes = W + A
     step_roof = {"W_bytes": W, "BA_bytes": A, "bytes_per_step": step_bytes,
                  "achieved_GBs": round(step_bytes / (ms / 1000.0) / 1e9, 1),
@@ -532,7 +545,7 @@ def run_cbd(args):
         ev1.record(stream)
         torch.cuda.synchronize()
         ms2 = ev0.elapsed_time(ev1) / args.steps
-        by = W + sum(c + 1 for c in wl2["ctx"]) * kv_pos_bytes(s)
+        by = W + sum(c + 1 for c in wl2["ctx"]) * kv_pos_bytes(s, eb)
         print(json.dumps({"sweep_B": Bs, "ms_per_step": round(ms2, 4), "tok_s": round(Bs / ms2 * 1000, 1),
                           "GBs": round(by / ms2 / 1e6, 1), "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}),
               file=sys.stderr, flush=True)

@@ -35,7 +35,7 @@ class Config(ctypes.Structure):
     _fields_ = [("n_layers", c_i32), ("d_model", c_i32), ("n_heads", c_i32), ("n_kv_heads", c_i32),
                 ("head_dim", c_i32), ("ffn_dim", c_i32), ("vocab", c_i32), ("rope_base", c_f32),
                 ("rms_eps", c_f32), ("block_size", c_i32), ("max_rows", c_i32), ("max_slots", c_i32),
-                ("max_blocks_per_seq", c_i32)]
+                ("max_blocks_per_seq", c_i32), ("kv_fp8", c_i32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -184,9 +184,10 @@ def version() -> str:
 
 # ------------------------------------------------------------------ engine
 def make_config(shape: dict, max_rows: int, max_slots: int, max_blocks_per_seq: int,
-                rope_base: float = 10000.0, rms_eps: float = 1e-6) -> Config:
+                rope_base: float = 10000.0, rms_eps: float = 1e-6, kv_fp8: bool = False) -> Config:
     return Config(shape["n_layers"], shape["d_model"], shape["n_heads"], shape["n_kv_heads"], shape["head_dim"],
-                  shape["ffn_dim"], shape["vocab"], rope_base, rms_eps, 32, max_rows, max_slots, max_blocks_per_seq)
+                  shape["ffn_dim"], shape["vocab"], rope_base, rms_eps, 32, max_rows, max_slots, max_blocks_per_seq,
+                  1 if kv_fp8 else 0)
 
 
 def engine_create(cfg: Config, weights: dict):
@@ -493,8 +494,8 @@ class _CAI:
 
 
 def device_view(ptr: int, shape: tuple, dtype: str):
-    """A torch view of libcbd-owned device memory (dtype: 'f32', 'bf16', 'i32')."""
+    """A torch view of libcbd-owned device memory (dtype: 'f32', 'bf16', 'i32', 'u8')."""
     import torch
-    typestr = {"f32": "<f4", "bf16": "<i2", "i32": "<i4"}[dtype]
+    typestr = {"f32": "<f4", "bf16": "<i2", "i32": "<i4", "u8": "|u1"}[dtype]
     t = torch.as_tensor(_CAI(ptr, shape, typestr), device="cuda")
     return t.view(torch.bfloat16) if dtype == "bf16" else t

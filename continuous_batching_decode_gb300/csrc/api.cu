@@ -100,6 +100,7 @@ cbd_status check_config(const cbd_config* c) {
     return fail(CBD_EINVAL, "max_blocks_per_seq out of range");
   if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return fail(CBD_EINVAL, "rope_base/rms_eps invalid");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(CBD_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->kv_fp8 != 0 && c->kv_fp8 != 1) return fail(CBD_EINVAL, "kv_fp8 must be 0 or 1");
   const int g = c->n_heads / c->n_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8) return fail(CBD_EUNSUPPORTED, "n_heads/n_kv_heads must be 1, 2, 4 or 8");
   if (c->d_model % 256 || c->ffn_dim % 256 || (c->n_heads * c->head_dim) % 256)
@@ -143,6 +144,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   dm.qkv_out = (dm.hq + 2 * dm.hkv) * dm.hd;
   dm.max_rows = cfg->max_rows; dm.max_slots = cfg->max_slots; dm.max_blocks_per_seq = cfg->max_blocks_per_seq;
   dm.rope_base = cfg->rope_base; dm.eps = cfg->rms_eps;
+  e->kv_fp8 = cfg->kv_fp8 != 0;
   e->max_pos = dm.max_blocks_per_seq * kBlock;
   const bool ondev = w->on_device != 0;
   CBD_CUDA(cudaDeviceSynchronize());   // weights produced on any stream are complete
@@ -439,6 +441,7 @@ extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path)
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   if (path < 0 || path > 2) return fail(CBD_EINVAL, "attention path must be 0, 1 or 2");
+  if (e->kv_fp8 && path != 0) return fail(CBD_EUNSUPPORTED, "an FP8 KV engine has attention path 0 only");
   e->attn_path = path;
   ++e->epoch;
   return CBD_OK;
@@ -507,13 +510,21 @@ extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv
   if (!e || !out) return fail(CBD_EINVAL, "NULL argument");
   *out = nullptr;
   if (n_blocks < 1) return fail(CBD_EINVAL, "n_blocks must be >= 1");
-  const size_t bytes = (size_t)e->dm.L * 2 * (size_t)n_blocks * e->dm.hkv * kBlock * e->dm.hd * 2;
+  const size_t bytes = (size_t)e->dm.L * 2 * (size_t)n_blocks * e->dm.hkv * kBlock * e->dm.hd * (e->kv_fp8 ? 1 : 2);
   auto p = std::make_unique<cbd_kv_pool>();
   p->e = e;
   p->n_blocks = n_blocks;
   p->bytes = bytes;
   void* b = nullptr;
   CBD_CUDA(cudaMalloc(&b, bytes));
+  if (e->kv_fp8) {
+    // unwritten positions must not hold NaN codes: P = 0 times V there
+    const cudaError_t ce = cudaMemset(b, 0, bytes);
+    if (ce != cudaSuccess) {
+      cudaFree(b);
+      return cuda_fail(ce, "FP8 pool clear");
+    }
+  }
   p->base = static_cast<uint16_t*>(b);
   *out = p.release();
   return CBD_OK;
@@ -746,7 +757,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   ++launches;
   EpiArgs qkv{};
   qkv.kind = kEpiQKV; qkv.out_f32 = e->q; qkv.ld = hqd;
-  qkv.pool = p->base; qkv.n_blocks = p->n_blocks; qkv.hq = dm.hq; qkv.hkv = dm.hkv; qkv.hd = dm.hd;
+  qkv.pool = p->base; qkv.kv_fp8 = e->kv_fp8 ? 1 : 0; qkv.n_blocks = p->n_blocks; qkv.hq = dm.hq; qkv.hkv = dm.hkv; qkv.hd = dm.hd;
   qkv.max_blocks_per_seq = dm.max_blocks_per_seq; qkv.max_pos = e->max_pos; qkv.rope_cs = e->rope_cs;
   qkv.rows = b->rows; qkv.tables = b->tables; qkv.err = e->err;
   EpiArgs res{};

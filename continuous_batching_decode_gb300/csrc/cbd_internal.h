@@ -183,6 +183,7 @@ struct cbd_engine {
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   uint64_t epoch = 1;                 // bumped by every setting that changes the launch sequence
+  bool kv_fp8 = false;                // K/V stored as E4M3 bytes (cbd_config.kv_fp8)
   cudaStream_t cap_stream = nullptr;  // private stream for graph capture
   // optional per-launch timing (cbd_engine_profile)
   bool prof = false;
@@ -193,7 +194,7 @@ struct cbd_engine {
 
 struct cbd_kv_pool {
   cbd_engine* e = nullptr;
-  uint16_t* base = nullptr;
+  uint16_t* base = nullptr;           // bf16 elements, or E4M3 bytes when the engine's KV is FP8
   int32_t n_blocks = 0;
   size_t bytes = 0;
 };
@@ -276,7 +277,8 @@ struct EpiArgs {
   uint16_t* out_lo;
   int ld_act;
   // QKV epilogue
-  uint16_t* pool;            // layer-0 base of the pool
+  uint16_t* pool;            // layer-0 base of the pool (E4M3 bytes when kv_fp8)
+  int kv_fp8;
   int layer, n_blocks, hq, hkv, hd, max_blocks_per_seq, max_pos;
   const float* rope_cs;
   const RowDev* rows;
@@ -312,6 +314,8 @@ PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n);
 // its number of (feature tile x K split) units.
 bool gemm_uses_tc(const cbd_engine* e, int n);
 int gemm_tc_units(int M, int K, int N, int n);
+cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
+                                   const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                              const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,

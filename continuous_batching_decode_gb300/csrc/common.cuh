@@ -3,6 +3,7 @@
 // GEMM variant, so all variants store identical results).
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -116,6 +117,31 @@ __device__ __forceinline__ size_t pool_off(int layer, int kv, int nblocks, int b
   return pool_tile(layer, nblocks, blk, hkv, kvh, kv, hd) + tile_elem(p, dim);
 }
 
+// FP8 (E4M3) pool: the same [L][n_blocks][H_kv][K|V][tile] order with one
+// byte per element, tiles of 32 * hd bytes.  K tile: rows = positions of hd
+// bytes; V tile transposed: rows = head dims of 32 bytes (positions).  In
+// both the 16-byte chunk c of row r sits at c ^ swizzle(r), so that the 8
+// rows an ldmatrix reads hit 8 different bank groups: K rows of 128 bytes
+// use r & 7, of 64 bytes (r >> 1) & 3; V rows of 32 bytes use (r >> 2) & 1.
+template <int HD>
+__host__ __device__ __forceinline__ uint32_t k8_off(int r, int c) {
+  static_assert(HD == 64 || HD == 128, "head dim");
+  return HD == 128 ? (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)) : (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+__host__ __device__ __forceinline__ uint32_t v8_off(int r, int c) { return (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4)); }
+// byte of (position p, dim d) in a K or V FP8 tile
+__host__ __device__ __forceinline__ uint32_t k8_elem(int hd, int p, int d) {
+  return (hd == 128 ? k8_off<128>(p, d >> 4) : k8_off<64>(p, d >> 4)) + (d & 15);
+}
+__host__ __device__ __forceinline__ uint32_t v8_elem(int p, int d) { return v8_off(d, p >> 4) + (p & 15); }
+// two floats -> two E4M3 bytes (round to nearest even, finite values
+// saturate to +-448): `lo` in byte 0, `hi` in byte 1
+__device__ __forceinline__ uint16_t f32x2_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Epilogue for a pair of adjacent output features (f, f+1), f even, of
 // one row.  QKV: f, f+1 are RoPE partners (dims i, i + hd/2 of one q or k
 // head, rows interleaved by the engine's repack) or two consecutive v dims.
@@ -148,6 +174,13 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& ep, int f, int row, floa
       const int blk = ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)];
       if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
       const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 0, hd);
+      if (ep.kv_fp8) {
+        uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + t0;
+        const uint16_t e = f32x2_e4m3x2(ra, rb);
+        t8[k8_elem(hd, rw.pos & 31, i)] = (uint8_t)(e & 0xff);
+        t8[k8_elem(hd, rw.pos & 31, i + half)] = (uint8_t)(e >> 8);
+        return;
+      }
       ep.pool[t0 + tile_elem(rw.pos & 31, i)] = f32_to_bf16(ra);
       ep.pool[t0 + tile_elem(rw.pos & 31, i + half)] = f32_to_bf16(rb);
     }
@@ -156,6 +189,13 @@ __device__ __forceinline__ void epi_pair(const EpiArgs& ep, int f, int row, floa
     const int head = fv / hd, j = fv % hd;
     const int blk = ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)];
     if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return; }
+    if (ep.kv_fp8) {
+      uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 1, hd);
+      const uint16_t e = f32x2_e4m3x2(a, b);
+      t8[v8_elem(rw.pos & 31, j)] = (uint8_t)(e & 0xff);
+      t8[v8_elem(rw.pos & 31, j + 1)] = (uint8_t)(e >> 8);
+      return;
+    }
     size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk, ep.hkv, head, hd, rw.pos & 31, j);
     ep.pool[o] = f32_to_bf16(a);
     ep.pool[o + 1] = f32_to_bf16(b);
@@ -241,8 +281,16 @@ __device__ __forceinline__ void epi_rows(const EpiArgs& ep, int m, int lane, int
       if (row0 + j < n) {
         if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
         const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk[j], ep.hkv, head, 0, hd);
-        ep.pool[t0 + tile_elem(rw[j].pos & 31, i)] = f32_to_bf16(v[j] * cs[j].x - pv[j] * cs[j].y);
-        ep.pool[t0 + tile_elem(rw[j].pos & 31, i + half)] = f32_to_bf16(pv[j] * cs[j].x + v[j] * cs[j].y);
+        const float ra = v[j] * cs[j].x - pv[j] * cs[j].y, rb = pv[j] * cs[j].x + v[j] * cs[j].y;
+        if (ep.kv_fp8) {
+          uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + t0;
+          const uint16_t e = f32x2_e4m3x2(ra, rb);
+          t8[k8_elem(hd, rw[j].pos & 31, i)] = (uint8_t)(e & 0xff);
+          t8[k8_elem(hd, rw[j].pos & 31, i + half)] = (uint8_t)(e >> 8);
+        } else {
+          ep.pool[t0 + tile_elem(rw[j].pos & 31, i)] = f32_to_bf16(ra);
+          ep.pool[t0 + tile_elem(rw[j].pos & 31, i + half)] = f32_to_bf16(rb);
+        }
       }
     return;
   }
@@ -251,6 +299,13 @@ __device__ __forceinline__ void epi_rows(const EpiArgs& ep, int m, int lane, int
   for (int j = 0; j < NB; ++j)
     if (row0 + j < n) {
       if (blk[j] < 0 || blk[j] >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); continue; }
+      if (ep.kv_fp8) {
+        uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + pool_tile(ep.layer, ep.n_blocks, blk[j], ep.hkv, head, 1, hd);
+        const uint16_t e = f32x2_e4m3x2(v[j], pv[j]);
+        t8[v8_elem(rw[j].pos & 31, jd)] = (uint8_t)(e & 0xff);
+        t8[v8_elem(rw[j].pos & 31, jd + 1)] = (uint8_t)(e >> 8);
+        continue;
+      }
       const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk[j], ep.hkv, head, hd, rw[j].pos & 31, jd);
       ep.pool[o] = f32_to_bf16(v[j]);
       ep.pool[o + 1] = f32_to_bf16(pv[j]);

@@ -179,6 +179,12 @@ __device__ __forceinline__ float epi_quad(const EpiArgs& ep, int row, int fg, fl
       const int blk = rinfo[ri].y;
       if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return 0.f; }
       const size_t t0 = pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 0, hd);
+      if (ep.kv_fp8) {          // dims (i, i + 1) and (i + half, i + half + 1): two adjacent bytes each
+        uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + t0;
+        *reinterpret_cast<uint16_t*>(t8 + k8_elem(hd, pos & 31, i)) = f32x2_e4m3x2(r0, r2);
+        *reinterpret_cast<uint16_t*>(t8 + k8_elem(hd, pos & 31, i + half)) = f32x2_e4m3x2(r1, r3);
+        return 0.f;
+      }
       *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i)) = pack_bf16x2(r0, r2);
       *reinterpret_cast<uint32_t*>(ep.pool + t0 + tile_elem(pos & 31, i + half)) = pack_bf16x2(r1, r3);
       return 0.f;
@@ -186,6 +192,15 @@ __device__ __forceinline__ float epi_quad(const EpiArgs& ep, int row, int fg, fl
     const int blk = rinfo[ri].y;
     if (blk < 0 || blk >= ep.n_blocks) { set_err(ep.err, kDevBadBlock); return 0.f; }
     const int fv = fg - nq - nk, head = fv / hd, jd = fv % hd;
+    if (ep.kv_fp8) {            // V is stored transposed: the 4 dims are 4 rows of the tile
+      uint8_t* t8 = reinterpret_cast<uint8_t*>(ep.pool) + pool_tile(ep.layer, ep.n_blocks, blk, ep.hkv, head, 1, hd);
+      const uint16_t e01 = f32x2_e4m3x2(v.x, v.y), e23 = f32x2_e4m3x2(v.z, v.w);
+      t8[v8_elem(pos & 31, jd)] = (uint8_t)(e01 & 0xff);
+      t8[v8_elem(pos & 31, jd + 1)] = (uint8_t)(e01 >> 8);
+      t8[v8_elem(pos & 31, jd + 2)] = (uint8_t)(e23 & 0xff);
+      t8[v8_elem(pos & 31, jd + 3)] = (uint8_t)(e23 >> 8);
+      return 0.f;
+    }
     const size_t o = pool_off(ep.layer, 1, ep.n_blocks, blk, ep.hkv, head, hd, pos & 31, jd);
     *reinterpret_cast<uint2*>(ep.pool + o) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }

@@ -16,6 +16,9 @@ import numpy as np
 MODEL_SHAPES = {
     "tiny": dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64,
                  ffn_dim=768, vocab=4096),
+    # head_dim 128 and 4 query heads per KV head, as in the 7B shape, at toy size
+    "hd128": dict(n_layers=2, d_model=512, n_heads=8, n_kv_heads=2, head_dim=128,
+                  ffn_dim=1024, vocab=4096),
     "1b": dict(n_layers=16, d_model=2048, n_heads=32, n_kv_heads=8, head_dim=64,
                ffn_dim=8192, vocab=65536),
     "7b": dict(n_layers=32, d_model=4096, n_heads=32, n_kv_heads=8, head_dim=128,

@@ -83,6 +83,11 @@ typedef struct cbd_config {
   int32_t max_rows;           /* rows per step (decode + prefill), <= 4096  */
   int32_t max_slots;          /* sequence slots (penalty counters per slot) */
   int32_t max_blocks_per_seq; /* block-table width; max positions / 32      */
+  int32_t kv_fp8;             /* 0: bf16 K/V; 1: FP8 E4M3 K/V ("大模型推理为什么需要
+                               * Continuous Batching" section 6), rounded to
+                               * nearest even and saturated at +-448, no
+                               * scale; half the pool bytes per position.
+                               * Needs attention path 0. */
 } cbd_config;
 
 /* Weights of one layer: bf16, row-major [out][in], no biases. */

@@ -17,10 +17,11 @@ NEAR_TIE = 1e-3
 
 
 class Model:
-    def __init__(self, name, max_rows=64, max_slots=8, mbps=8, seed=0, device_weights=True):
+    def __init__(self, name, max_rows=64, max_slots=8, mbps=8, seed=0, device_weights=True, kv_fp8=False):
         self.shape = synth.MODEL_SHAPES[name]
+        self.kv_fp8 = kv_fp8
         self.w = synth.make_weights(self.shape, seed=seed, device="cuda" if device_weights else "cpu")
-        self.cfg = cbd.make_config(self.shape, max_rows, max_slots, mbps)
+        self.cfg = cbd.make_config(self.shape, max_rows, max_slots, mbps, kv_fp8=kv_fp8)
         self.e = cbd.engine_create(self.cfg, self.w)
         self.mbps = mbps
         self._oracle = None
@@ -28,7 +29,8 @@ class Model:
     def oracle(self, cache=True):
         if self._oracle is None:
             bits = {k: synth.bf16_bits(v) for k, v in self.w.items()}
-            self._oracle = om.OracleModel(om.ModelConfig(**self.shape), bits, cache=cache)
+            self._oracle = om.OracleModel(om.ModelConfig(**self.shape), bits, cache=cache,
+                                          kv_format="e4m3" if self.kv_fp8 else "bf16")
         return self._oracle
 
     def close(self):
@@ -45,13 +47,24 @@ class Pool:
         base, nbytes, nb = cbd.kv_pool_data(self.p)
         s = model.shape
         hd = s["head_dim"]
-        # [L][n_blocks][H_kv][K|V][tile]; a tile stores (position, dim) at a
-        # 128-byte-swizzled offset (see cbd_kv_pool_data in include/cbd.h)
-        self.view = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * hd), "bf16")
+        self.fp8 = model.kv_fp8
         r = np.arange(32)[:, None]
         d = np.arange(hd)[None, :]
-        self.tile_index = torch.as_tensor(((d // 64) * 2048 + r * 64 + ((((d % 64) // 8) ^ (r % 8)) * 8) + d % 8)
-                                          .reshape(-1), device="cuda")
+        if self.fp8:
+            # E4M3 bytes; K tile rows = positions (hd bytes), V tile rows =
+            # dims (32 bytes); 16-byte chunks swizzled per row (include/cbd.h)
+            self.view = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * hd), "u8")
+            kswz = (r % 8) if hd == 128 else ((r // 2) % 4)
+            k_idx = r * hd + (((d // 16) ^ kswz) * 16) + d % 16
+            v_idx = d * 32 + (((r // 16) ^ ((d // 4) % 2)) * 16) + r % 16
+            self.tile_index_kv = [torch.as_tensor(k_idx.reshape(-1), device="cuda"),
+                                  torch.as_tensor(v_idx.reshape(-1), device="cuda")]
+        else:
+            # [L][n_blocks][H_kv][K|V][tile]; a tile stores (position, dim) at a
+            # 128-byte-swizzled offset (see cbd_kv_pool_data in include/cbd.h)
+            self.view = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * hd), "bf16")
+            self.tile_index = torch.as_tensor(((d // 64) * 2048 + r * 64 + ((((d % 64) // 8) ^ (r % 8)) * 8) + d % 8)
+                                              .reshape(-1), device="cuda")
 
     def close(self):
         cbd.kv_pool_destroy(self.p)
@@ -62,7 +75,14 @@ class Pool:
         ids = torch.as_tensor(tables[slot][:nb].astype(np.int64), device="cuda")
         L, _, hkv, _, te = self.view.shape
         hd = te // 32
-        kv = self.view[:, ids][..., self.tile_index].reshape(L, nb, hkv, 2, 32, hd)   # unswizzled
+        if self.fp8:
+            t = self.view[:, ids]
+            k = t[:, :, :, 0][..., self.tile_index_kv[0]]
+            v = t[:, :, :, 1][..., self.tile_index_kv[1]]
+            kv = torch.stack([k, v], dim=3).contiguous().view(torch.float8_e4m3fn).float()
+            kv = kv.reshape(L, nb, hkv, 2, 32, hd)
+        else:
+            kv = self.view[:, ids][..., self.tile_index].reshape(L, nb, hkv, 2, 32, hd)   # unswizzled
         kv = kv.permute(0, 3, 1, 4, 2, 5).reshape(L, 2, nb * 32, hkv, hd)
         kv = kv[:, :, :n_pos].float().cpu().numpy().astype(np.float64)
         return [kv[l, 0] for l in range(L)], [kv[l, 1] for l in range(L)]
