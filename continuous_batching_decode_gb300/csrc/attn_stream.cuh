@@ -69,6 +69,19 @@ template <int HD>
 __host__ __device__ constexpr int attn_stream_smem() {
   return kStreamWarps * attn_stream_slots<HD>() * (32 * HD * 2) + kStreamWarps * 8 * 32 * 4 + 1024;
 }
+// FP8 K/V: the same ring bytes per SM, spread over more warps (the kernel is
+// latency-bound at half the bytes, and more warps per scheduler hide more):
+// 12 warps of 16 KB rings instead of 8 of 24 KB.
+constexpr int kStreamWarps8 = 12;
+template <int HD, bool FP8>
+__host__ __device__ constexpr int stream_warps() { return FP8 ? kStreamWarps8 : kStreamWarps; }
+template <int HD, bool FP8>
+__host__ __device__ constexpr int stream_slots() { return FP8 ? (HD == 128 ? 4 : 8) : attn_stream_slots<HD>(); }
+template <int HD, bool FP8>
+__host__ __device__ constexpr int stream_smem() {
+  return stream_warps<HD, FP8>() * stream_slots<HD, FP8>() * (32 * HD * (FP8 ? 1 : 2)) +
+         stream_warps<HD, FP8>() * 8 * 32 * 4 + 1024;
+}
 
 // FP8 = true: K and V are E4M3 bytes (tile layouts in common.cuh: K
 // [pos][dim], V transposed [dim][pos], both 16-byte-chunk swizzled).  An
@@ -79,7 +92,7 @@ __host__ __device__ constexpr int attn_stream_smem() {
 // the sums are unchanged.  Products run as f16 MMAs, K/V converted exactly,
 // q and P split into f16 hi + lo.
 template <int HD, int G, bool FP8 = false>
-__global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
+__global__ void __launch_bounds__(stream_warps<HD, FP8>() * 32, 1) attn_stream_kernel(
     const uint16_t* __restrict__ pool, const float* __restrict__ q, const RowDev* __restrict__ rows,
     const int32_t* __restrict__ tables, const AttnWork* __restrict__ work, const int32_t* __restrict__ row_work,
     int n_tasks, int layer, int n_blocks, int hkv, int mbps, float* __restrict__ part_o, float* __restrict__ part_ml,
@@ -89,14 +102,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
   constexpr int EB = FP8 ? 1 : 2;          // bytes per K / V element
   constexpr int TILE = 32 * HD * EB;
   constexpr int KS = HD / 16;
-  constexpr int NS = attn_stream_slots<HD>() * (FP8 ? 2 : 1);   // ring slots per warp, one K or V tile each
+  constexpr int NS = stream_slots<HD, FP8>();   // ring slots per warp, one K or V tile each
+  constexpr int NW = stream_warps<HD, FP8>();   // warps per CTA
   constexpr int QN = NS + 1 > 8 ? 16 : 8;   // task queue entries per warp (>= NS + 1)
   extern __shared__ uint8_t sm_raw[];
-  __shared__ __align__(8) uint64_t bar[kStreamWarps][NS];
+  __shared__ __align__(8) uint64_t bar[NW][NS];
   __shared__ int abort_flag;
   // tasks whose blocks this warp's producer has started issuing:
   // (row, start, end, kvh), (wi, task, -, -)
-  __shared__ __align__(16) int tq[kStreamWarps][QN][8];
+  __shared__ __align__(16) int tq[NW][QN][8];
   TR_DECL;
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,16 +118,16 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) attn_stream_kernel(
   const uint32_t raw = tc::smem_u32(sm_raw);
   uint8_t* base = sm_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* ring = base + warp * NS * TILE;               // slot s at s * TILE
-  float* Pw = reinterpret_cast<float*>(base + kStreamWarps * NS * TILE) + warp * 8 * 32;
+  float* Pw = reinterpret_cast<float*>(base + NW * NS * TILE) + warp * 8 * 32;
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kStreamWarps; ++w)
+    for (int w = 0; w < NW; ++w)
       for (int s = 0; s < NS; ++s) tc::mbar_init(&bar[w][s], 1);
     abort_flag = 0;
     tc::fence_mbar_init();
   }
   __syncthreads();
   const int hq = hkv * G;
-  const int gw = blockIdx.x * kStreamWarps + warp, nwarps = gridDim.x * kStreamWarps;
+  const int gw = blockIdx.x * NW + warp, nwarps = gridDim.x * NW;
   const uint64_t kv_policy = tc::policy_evict_first();   // each K/V tile is read once per step
   // A task is one 128-position chunk (work item wi) for one KV head; its
   // record (row, positions, physical blocks) was built on the host.

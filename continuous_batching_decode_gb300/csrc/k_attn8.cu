@@ -15,7 +15,8 @@ template <int HD, int G>
 static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                 const PfSpec& pf, cudaStream_t s) {
   const Dims& dm = e->dm;
-  constexpr int smem = attn_stream_smem<HD>();      // slots are half the size, twice as many
+  constexpr int smem = stream_smem<HD, true>();
+  constexpr int NW = stream_warps<HD, true>();
   static bool attr = false;
   if (!attr) {
     cudaError_t ce =
@@ -24,8 +25,8 @@ static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const
     attr = true;
   }
   const int n_tasks = b->n_work * dm.hkv;
-  const int grid = std::min(e->sm_count, (n_tasks + kStreamWarps - 1) / kStreamWarps);
-  return launch_pdl(attn_stream_kernel<HD, G, true>, dim3(grid), dim3(kStreamWarps * 32), smem, s,
+  const int grid = std::min(e->sm_count, (n_tasks + NW - 1) / NW);
+  return launch_pdl(attn_stream_kernel<HD, G, true>, dim3(grid), dim3(NW * 32), smem, s,
                     (const uint16_t*)p->base, (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
                     (const AttnWork*)b->work, (const int32_t*)b->row_work, n_tasks, layer, p->n_blocks, dm.hkv,
                     dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi, e->act_lo, e->attn_next + layer, pf,
