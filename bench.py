@@ -593,6 +593,7 @@ def run_trace(args):
                     ttft_s=dict(mean=round(float(ttft.mean()), 4), p50=round(float(np.median(ttft)), 4),
                                 p99=round(float(np.quantile(ttft, 0.99)), 4)),
                     stalled_rows=res["stats"]["stalled_rows"], fallback_stops=res["stats"]["fallback_stops"],
+                    host_sched_us_per_step=round(res["sched_us_per_step"], 1),
                     config=dict(workload="7b-shaped continuous-batching trace", slots=slots, max_rows=rows,
                                 chunk=512, answer_budget=128, pool_blocks=args.trace_blocks,
                                 rate=args.trace_rate or "all at t=0"),

@@ -442,6 +442,22 @@ def sched_plan(s) -> dict:
                 stopped=[p.stopped_ids[i] for i in range(p.n_stopped)])
 
 
+def sched_plan_raw(s) -> Plan:
+    """The next plan as the scheduler's own C struct (no Python copies of the
+    rows or tables); valid until the next plan / commit.  See step_plan."""
+    p = Plan()
+    _check(lib().cbd_sched_plan(s, ctypes.byref(p)))
+    return p
+
+
+def step_plan(e, pool, p: Plan, out_tokens, out_logits=None, stream=None) -> None:
+    """cbd_step over a plan from sched_plan_raw: its rows, block tables and
+    sampling parameters go to the engine straight from the scheduler's
+    arrays."""
+    _check(lib().cbd_step(e, pool, p.rows, p.n_rows, p.block_tables, p.table_slots, p.n_blocks_per_slot,
+                          p.sampling, None, _ptr(out_tokens), _ptr(out_logits), _stream(stream)))
+
+
 def sched_commit(s, tokens, cap: int = 4096) -> list:
     ta, tp = _i32(tokens)
     fin = (Finished * cap)()

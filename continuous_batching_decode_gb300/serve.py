@@ -55,6 +55,7 @@ class Server:
         first_tok, done_at, outcome, arrival = {}, {}, {}, {}
         n_gen = 0
         steps = rows_total = 0
+        t_sched = 0.0                      # host time in plan + commit (C++ scheduler + marshalling)
         t_start = time.perf_counter()
         vt = 0.0
 
@@ -78,25 +79,29 @@ class Server:
                     if ex.status != C.EBUSY:
                         raise
                     outcome[r["id"]] = "busy"
-            p = C.sched_plan(self.sched)
-            for slot in p["resets"]:
-                C.slot_reset(self.e, slot)
-            m = len(p["sampled_ids"])
-            if p["rows"]:
-                C.step(self.e, self.pool, p["rows"], p["block_tables"], p["n_blocks_per_slot"], p["sampling"],
-                       None, self.out_tokens)
+            ts = time.perf_counter()
+            p = C.sched_plan_raw(self.sched)       # the plan's arrays go to cbd_step as they are
+            sampled = [p.sampled_ids[j] for j in range(p.n_sampled)]
+            t_sched += time.perf_counter() - ts
+            for j in range(p.n_resets):
+                C.slot_reset(self.e, p.reset_slots[j])
+            m = len(sampled)
+            if p.n_rows:
+                C.step_plan(self.e, self.pool, p, self.out_tokens)
                 toks = self.out_tokens[:m].cpu().numpy().tolist() if m else []
                 steps += 1
-                rows_total += len(p["rows"])
+                rows_total += p.n_rows
             else:
                 toks = []
                 if i < len(reqs) and step_ms is None:        # idle until the next arrival
                     time.sleep(max(0.0, min(reqs[i]["arrival"] - now_s(), 0.01)))
+            ts = time.perf_counter()
             fin = C.sched_commit(self.sched, toks)
+            t_sched += time.perf_counter() - ts
             if step_ms is not None:
                 vt += step_ms / 1000.0
             t = now_s()
-            for rid in p["sampled_ids"]:
+            for rid in sampled:
                 if rid not in first_tok:
                     first_tok[rid] = t
             n_gen += m
@@ -113,4 +118,5 @@ class Server:
         ttft = np.array([first_tok[r] - arrival[r] for r in first_tok if r in arrival])
         return dict(tokens=out, outcome=outcome, ttft=ttft, finish={r: done_at[r] - arrival[r] for r in done_at},
                     generated=n_gen, steps=steps, rows=rows_total, wall_s=wall,
+                    sched_us_per_step=1e6 * t_sched / max(steps, 1),
                     tok_s=n_gen / wall if wall > 0 else float("nan"), stats=C.sched_stats(self.sched))
