@@ -74,6 +74,8 @@ def parse():
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
+    ap.add_argument("--mixed", type=int, default=0,
+                    help="prefill rows (512-row chunks) added to the B decode rows: one mixed-step line")
     ap.add_argument("--trace", action="store_true", help="serve the request trace (see the module docstring)")
     ap.add_argument("--trace-requests", type=int, default=2000)
     ap.add_argument("--trace-rate", type=float, default=0.0, help="requests/s (0: all arrive at t = 0)")
@@ -557,6 +559,99 @@ def run_cbd(args):
         dist.destroy_process_group()
 
 
+def run_mixed(args):
+    """A mixed step (SURVEY a1 composition): the B decode rows of the default
+    workload plus `--mixed` prefill rows, as 512-row chunks at positions
+    0..511 of new slots.  Reports the step time and the weight contractions'
+    algorithmic throughput (2 x parameters x rows) against the measured bf16
+    tensor peak (the contraction is compute-bound at this many rows)."""
+    import torch
+    import continuous_batching_decode_gb300 as cbd
+    from continuous_batching_decode_gb300 import build, synth
+
+    torch.cuda.set_device(0)
+    build.build()
+    s = shape_of(args)
+    B, P = args.B, args.mixed
+    nch = (P + 511) // 512
+    db = synth.decode_batch(B, args.ctx_lo, args.ctx_hi, s["vocab"], args.seed)
+    ctx = db["contexts"]
+    need = {i: (c + 1 + 31) // 32 for i, c in enumerate(ctx)}
+    for j in range(nch):
+        need[B + j] = 16
+    mbps = max((args.ctx_hi + 1 + 31) // 32, 16)
+    n_pool = sum(need.values()) + 8
+    tables, nbps = synth.permuted_tables(need, n_pool, mbps, np.random.default_rng(args.seed + 1))
+    rng = np.random.default_rng(args.seed + 2)
+    rows = [(i, db["tokens"][i], ctx[i], 0, 1) for i in range(B)]
+    for j in range(nch):
+        n = min(512, P - 512 * j)
+        toks = synth.random_tokens(rng, n, s["vocab"])
+        rows += [(B + j, toks[i], i, 1, 1 if i == n - 1 else 0) for i in range(n)]
+    m = sum(1 for r in rows if r[4])
+    samp = [dict(temperature=1.0, top_p=0.3, frequency_penalty=1.0, penalty_decay=0.996, seed=args.seed,
+                 request_id=i) for i in range(m)]
+    w = synth.make_weights(s, seed=args.seed, device="cuda")
+    e = cbd.engine_create(cbd.make_config(s, max_rows=len(rows), max_slots=B + nch, max_blocks_per_seq=mbps), w)
+    del w
+    torch.cuda.empty_cache()
+    pool = cbd.kv_pool_create(e, n_pool)
+    base, nbytes, nb = cbd.kv_pool_data(pool)
+    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "bf16")
+    gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
+    for l in range(s["n_layers"]):
+        kv[l].copy_((torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3).to(torch.bfloat16))
+    b = cbd.batch_create(e, pool, rows, tables, nbps, samp)
+    out = torch.zeros(m, dtype=torch.int32, device="cuda")
+    cbd.batch_set_graph(b, True)
+    for _ in range(args.warmup):
+        cbd.batch_run(e, pool, b, out)
+    torch.cuda.synchronize()
+    cbd.engine_check(e)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        cbd.batch_run(e, pool, b, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    cbd.batch_set_graph(b, False)
+    cbd.engine_profile(e, True)
+    for _ in range(args.steps):
+        cbd.batch_run(e, pool, b, out)
+    prof = cbd.engine_profile_read(e)
+    cbd.engine_profile(e, False)
+    cbd.engine_check(e)
+    d, hq, hkv, hd, F, V, L = (s[k] for k in ("d_model", "n_heads", "n_kv_heads", "head_dim", "ffn_dim", "vocab",
+                                             "n_layers"))
+    layer_params = (hq + 2 * hkv) * hd * d + d * hq * hd + 3 * F * d
+    n = len(rows)
+    flops = 2.0 * (L * layer_params * n + V * d * m)
+    gemm_ms = sum(v[1] for k, v in prof.items() if k.startswith("gemm")) / args.steps
+    try:
+        peak_tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+        kind = "measured"
+    except Exception:
+        peak_tf, kind = 1900.0, "fallback"
+    ach = flops / (gemm_ms / 1000.0) / 1e12
+    line = {"metric": "mixed step: rows/s and weight-contraction TFLOP/s", "impl": "cbd",
+            "value": round(n / (ms / 1000.0), 1), "unit": "rows/s", "ms_per_step": round(ms, 4),
+            "rows": n, "decode_rows": B, "prefill_rows": P, "sampled_rows": m,
+            "gemm": {"bound": "tensor", "achieved": round(ach, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(ach / peak_tf, 4), "peak_kind": kind, "algorithmic_flops": flops,
+                     "ms_per_step": round(gemm_ms, 4),
+                     "note": "2 x params x rows; the MMAs also multiply the lo half of each activation (2x issued)"},
+            "kernels": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
+            "config": {"workload": f"{args.shape}-shaped mixed step: {B} decode rows (ctx U[{args.ctx_lo},"
+                                   f"{args.ctx_hi}]) + {P} prefill rows in 512-row chunks", "shape": args.shape},
+            "data": "synthetic (seeded random-init weights, random bf16 KV, random prompt ids)"}
+    print(json.dumps(line), flush=True)
+    cbd.batch_destroy(b)
+    cbd.kv_pool_destroy(pool)
+    cbd.engine_destroy(e)
+
+
 def run_trace(args):
     import torch
     import continuous_batching_decode_gb300 as cbd
@@ -605,6 +700,9 @@ def main():
     args = parse()
     if args.trace:
         run_trace(args)
+        return
+    if args.mixed:
+        run_mixed(args)
         return
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
