@@ -74,6 +74,10 @@ def parse():
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
+    ap.add_argument("--rows-gemm", type=int, default=256,
+                    help="steps of at least this many rows may run the 128-row-tile GEMM (0 = never)")
+    ap.add_argument("--rows-gemm-force", action="store_true",
+                    help="... on every GEMM of such a step (default: where it fills the GPU well)")
     ap.add_argument("--mixed", type=int, default=0,
                     help="prefill rows (512-row chunks) added to the B decode rows: one mixed-step line")
     ap.add_argument("--trace", action="store_true", help="serve the request trace (see the module docstring)")
@@ -363,6 +367,7 @@ def run_cbd(args):
     cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"], kv_fp8=fp8)
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
+    cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
     cbd.engine_set_attention_path(e, args.attn_path)
     cbd.engine_set_l2_prefetch(e, args.l2_prefetch_mb << 20)
     if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
@@ -560,7 +565,8 @@ def run_cbd(args):
 
 
 def run_mixed(args):
-    """A mixed step (SURVEY a1 composition): the B decode rows of the default
+    """A mixed step ("20.3 服务、批处理与流式" section 20.3.2: prefill chunks
+    share the step with decode rows): the B decode rows of the default
     workload plus `--mixed` prefill rows, as 512-row chunks at positions
     0..511 of new slots.  Reports the step time and the weight contractions'
     algorithmic throughput (2 x parameters x rows) against the measured bf16
@@ -595,6 +601,7 @@ def run_mixed(args):
     e = cbd.engine_create(cbd.make_config(s, max_rows=len(rows), max_slots=B + nch, max_blocks_per_seq=mbps), w)
     del w
     torch.cuda.empty_cache()
+    cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
     pool = cbd.kv_pool_create(e, n_pool)
     base, nbytes, nb = cbd.kv_pool_data(pool)
     kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "bf16")
@@ -644,7 +651,8 @@ def run_mixed(args):
                      "note": "2 x params x rows; the MMAs also multiply the lo half of each activation (2x issued)"},
             "kernels": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
             "config": {"workload": f"{args.shape}-shaped mixed step: {B} decode rows (ctx U[{args.ctx_lo},"
-                                   f"{args.ctx_hi}]) + {P} prefill rows in 512-row chunks", "shape": args.shape},
+                                   f"{args.ctx_hi}]) + {P} prefill rows in 512-row chunks", "shape": args.shape,
+                       "rows_gemm_min": args.rows_gemm, "rows_gemm_force": args.rows_gemm_force},
             "data": "synthetic (seeded random-init weights, random bf16 KV, random prompt ids)"}
     print(json.dumps(line), flush=True)
     cbd.batch_destroy(b)

@@ -105,6 +105,7 @@ PROTOS = {
     "cbd_slot_reset": (c_i32, [c_vp, c_i32, c_vp]),
     "cbd_engine_profile": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_gemm_path": (c_i32, [c_vp, c_i32, c_i32]),
+    "cbd_engine_set_rows_gemm": (c_i32, [c_vp, c_i32, c_i32]),
     "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_l2_prefetch": (c_i32, [c_vp, c_u64]),
     "cbd_engine_set_fused_norm": (c_i32, [c_vp, c_i32]),
@@ -232,6 +233,12 @@ def engine_counters(e) -> int:
 def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 4) -> None:
     """0 automatic, 1 CUDA-core GEMV only, 2 tcgen05 only."""
     _check(lib().cbd_engine_set_gemm_path(e, path, gemv_max_rows))
+
+
+def engine_set_rows_gemm(e, min_rows: int, force: bool = False) -> None:
+    """tcgen05 path: the 128-row-tile kernel from min_rows rows (0 = never),
+    for the GEMMs it fills the GPU well for (every GEMM with force)."""
+    _check(lib().cbd_engine_set_rows_gemm(e, min_rows, 1 if force else 0))
 
 
 def engine_set_attention_path(e, path: int) -> None:

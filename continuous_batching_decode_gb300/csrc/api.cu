@@ -437,6 +437,16 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
   return CBD_OK;
 }
 
+extern "C" cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (min_rows < 0) return fail(CBD_EINVAL, "min_rows must be >= 0");
+  e->rows_gemm_min = min_rows;
+  e->rows_gemm_force = force != 0;
+  ++e->epoch;
+  return CBD_OK;
+}
+
 extern "C" cbd_status cbd_engine_set_attention_path(cbd_engine* e, int32_t path) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
@@ -749,7 +759,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   // epilogues write split(x * g) and per-row partial sums of x^2, and the
   // QKV / gate-up GEMMs apply 1/rms in their epilogues (no norm launches).
   const int o_parts = gemm_tc_units(dm.d, hqd, e->tile_o, n), dn_parts = gemm_tc_units(dm.d, dm.F, e->tile_dn, n);
-  const bool fused = e->fuse_norm && gemm_uses_tc(e, n) && o_parts <= kMaxSsqParts && dn_parts <= kMaxSsqParts;
+  const bool fused = e->fuse_norm && gemm_uses_tc(e, n) && !gemm_uses_rows(e, n) && o_parts <= kMaxSsqParts && dn_parts <= kMaxSsqParts;
   cbd_status st;
   if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, fused ? e->layers[0].attn_norm : nullptr, s); }),
                 "embed")))

@@ -181,6 +181,8 @@ struct cbd_engine {
   size_t l2_prefetch = 0;             // bytes of the next GEMM's weights each kernel prefetches to L2 (off)
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   int gemv_max_rows = 4;              // auto: GEMV up to this many rows
+  int rows_gemm_min = 256;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
+  bool rows_gemm_force = false;       // ... for every GEMM of such a step, however it fills the GPU
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   uint64_t epoch = 1;                 // bumped by every setting that changes the launch sequence
   bool kv_fp8 = false;                // K/V stored as E4M3 bytes (cbd_config.kv_fp8)
@@ -313,6 +315,12 @@ PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n);
 // Whether a GEMM of M x K weights on n rows takes the tcgen05 path, and
 // its number of (feature tile x K split) units.
 bool gemm_uses_tc(const cbd_engine* e, int n);
+// the 128-row-tile persistent kernel (k_gemm_rows.cu) runs this step's GEMMs
+bool gemm_uses_rows(const cbd_engine* e, int n);
+bool gemm_rows_supports(const EpiArgs& ep);
+// the 128-row-tile kernel fills the GPU well enough for this GEMM and row count
+bool gemm_rows_preferred(const TcGemm& g, int n);
+cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStream_t s);
 int gemm_tc_units(int M, int K, int N, int n);
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                    const PfSpec& pf, cudaStream_t s);

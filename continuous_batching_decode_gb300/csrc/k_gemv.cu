@@ -124,6 +124,9 @@ static bool uses_tc(const cbd_engine* e, int n) {
   return e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
 }
 bool gemm_uses_tc(const cbd_engine* e, int n) { return uses_tc(e, n); }
+bool gemm_uses_rows(const cbd_engine* e, int n) {
+  return uses_tc(e, n) && e->rows_gemm_min > 0 && n >= e->rows_gemm_min;
+}
 int gemm_tc_units(int M, int K, int N, int n) {
   int T, NR, KB, S;
   gemm_tc_plan(M, K, N, n, &T, &NR, &KB, &S);
@@ -133,6 +136,8 @@ int gemm_tc_units(int M, int K, int N, int n) {
 cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& ep, const PfSpec& pf,
                         cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
+  if (gemm_uses_rows(e, n) && gemm_rows_supports(ep) && (e->rows_gemm_force || gemm_rows_preferred(op.tc, n)))
+    return launch_gemm_rows(op.tc, n, ep, s);
   if (uses_tc(e, n)) return launch_gemm_tc(op.tc, n, ep, pf, s);
   return launch_gemv(op.W, op.M, op.K, op.tc.N, op.a_hi, op.a_lo, op.lda, n, ep, s);
 }

@@ -137,6 +137,20 @@ cbd_status cbd_engine_check(cbd_engine* e);
  * activations); they differ only in summation order.  Default: 0 and 4. */
 cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_max_rows);
 
+/* On the tcgen05 path, steps of at least min_rows rows (prefill chunks,
+ * "20.3 服务、批处理与流式" section 20.3.2) may run their weight
+ * contractions on a persistent kernel with 128-row activation tiles: each
+ * weight tile feeds 128 rows per pass instead of 64, clusters of up to 4
+ * CTAs share (multicast) each activation tile, and two TMEM accumulators
+ * overlap one tile's epilogue with the next tile's mainloop.  Such a step
+ * runs the RMSNorm as its own kernel.  With force == 0 a GEMM takes this
+ * kernel only where its units fill at least 3/4 of the last wave of
+ * resident clusters (else the 64-row-tile kernel, which splits K); with
+ * force != 0 every GEMM of the step takes it.  Same sums as the other
+ * paths, in another order.  min_rows 0 = never.  Default 256, force 0.
+ * CBD_EINVAL if min_rows < 0. */
+cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force);
+
 /* Choose the attention kernel: 0 = persistent streaming kernel (each warp
  * pipelines its chunks' K/V tiles through a TMA ring; mma.sync; default),
  * 1 = CUDA cores, 2 = one CTA per chunk with mma.sync.  All use the same

@@ -17,8 +17,11 @@ NEAR_TIE = 1e-3
 
 
 class Model:
-    def __init__(self, name, max_rows=64, max_slots=8, mbps=8, seed=0, device_weights=True, kv_fp8=False):
-        self.shape = synth.MODEL_SHAPES[name]
+    def __init__(self, name, max_rows=64, max_slots=8, mbps=8, seed=0, device_weights=True, kv_fp8=False,
+                 layers=None):
+        self.shape = dict(synth.MODEL_SHAPES[name])
+        if layers:
+            self.shape["n_layers"] = layers
         self.kv_fp8 = kv_fp8
         self.w = synth.make_weights(self.shape, seed=seed, device="cuda" if device_weights else "cpu")
         self.cfg = cbd.make_config(self.shape, max_rows, max_slots, mbps, kv_fp8=kv_fp8)
