@@ -106,6 +106,7 @@ PROTOS = {
     "cbd_engine_profile": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_gemm_path": (c_i32, [c_vp, c_i32, c_i32]),
     "cbd_engine_set_rows_gemm": (c_i32, [c_vp, c_i32, c_i32]),
+    "cbd_engine_set_prefill_attention": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_l2_prefetch": (c_i32, [c_vp, c_u64]),
     "cbd_engine_set_fused_norm": (c_i32, [c_vp, c_i32]),
@@ -233,6 +234,11 @@ def engine_counters(e) -> int:
 def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 4) -> None:
     """0 automatic, 1 CUDA-core GEMV only, 2 tcgen05 only."""
     _check(lib().cbd_engine_set_gemm_path(e, path, gemv_max_rows))
+
+
+def engine_set_prefill_attention(e, enable: bool) -> None:
+    """Prefill runs on the prefill attention kernel (attention path 0, bf16 K/V)."""
+    _check(lib().cbd_engine_set_prefill_attention(e, 1 if enable else 0))
 
 
 def engine_set_rows_gemm(e, min_rows: int, force: bool = False) -> None:

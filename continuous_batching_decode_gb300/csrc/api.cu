@@ -307,7 +307,8 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   // ---- staging for cbd_step / cbd_sample
   const size_t stage_bytes = align_up(R * sizeof(RowDev), 16) + 2 * align_up(S * 4, 16) +
                              align_up(S * sizeof(SampDev), 16) + align_up(S * dm.max_blocks_per_seq * 4, 16) +
-                             align_up((size_t)e->max_work * sizeof(AttnWork), 16) + align_up((R + 1) * 4, 16) + 256;
+                             align_up((size_t)e->max_work * sizeof(AttnWork), 16) + align_up((R + 1) * 4, 16) +
+                             align_up(R * sizeof(PfBlock), 16) + align_up(R * 4, 16) + 256;
   for (auto& sg : e->stage) {
     if (e3 == cudaSuccess) e3 = cudaMallocHost(&sg.host, stage_bytes);
     if (e3 == cudaSuccess) e3 = cudaMalloc(&sg.dev, stage_bytes);
@@ -434,6 +435,14 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
   e->gemm_path = path;
   ++e->epoch;
   e->gemv_max_rows = gemv_max_rows;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  e->prefill_attn = enable != 0;
+  ++e->epoch;
   return CBD_OK;
 }
 
@@ -633,7 +642,41 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
     if (s.reserved) return fail(CBD_EINVAL, "sampling %d: reserved field must be 0", j);
     if (uniforms && !(uniforms[j] >= 0.f && uniforms[j] < 1.f)) return fail(CBD_EINVAL, "uniform %d not in [0,1)", j);
   }
-  // work list: fixed 256-position chunks of every row
+  // prefill runs: maximal runs of consecutive positions of one slot (in
+  // any row order), at least kPfMinRun long, cut into blocks from the run's
+  // first position for the prefill attention kernel -- so which rows form
+  // runs, and the blocks, do not depend on the order of the rows
+  std::vector<uint8_t> in_run(n_rows, 0);
+  std::vector<PfBlock> pfb;
+  std::vector<int32_t> pf_rows;
+  {
+    const int BQ = prefill_block_positions(dm.hq / dm.hkv);
+    std::vector<int32_t> ord(n_rows);
+    for (int32_t r = 0; r < n_rows; ++r) ord[r] = r;
+    std::sort(ord.begin(), ord.end(), [&](int32_t x, int32_t y) {
+      return rows[x].slot != rows[y].slot ? rows[x].slot < rows[y].slot : rows[x].pos < rows[y].pos;
+    });
+    for (int32_t a = 0; a < n_rows;) {
+      int32_t b1 = a + 1;
+      while (b1 < n_rows && rows[ord[b1]].slot == rows[ord[a]].slot &&
+             rows[ord[b1]].pos == rows[ord[b1 - 1]].pos + 1)
+        ++b1;
+      if (b1 - a >= kPfMinRun) {
+        const int32_t base = (int32_t)pf_rows.size();
+        for (int32_t i = a; i < b1; ++i) {
+          in_run[ord[i]] = 1;
+          pf_rows.push_back(ord[i]);
+        }
+        for (int32_t k = 0; k < b1 - a; k += BQ)
+          pfb.push_back(PfBlock{base + k, std::min<int32_t>(BQ, b1 - a - k), rows[ord[a + k]].pos, rows[ord[a]].slot});
+      }
+      a = b1;
+    }
+    // longest context first, so the last CTAs to start are the short ones
+    std::stable_sort(pfb.begin(), pfb.end(),
+                     [](const PfBlock& x, const PfBlock& y) { return x.pos0 + x.npos > y.pos0 + y.npos; });
+  }
+  // work list: fixed 128-position chunks of every row
   int64_t n_work = 0;
   for (int32_t r = 0; r < n_rows; ++r) n_work += rows[r].pos / kAttnChunk + 1;
   if (n_work > e->max_work)
@@ -642,6 +685,7 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   // layout
   BatchImage& I = *img;
   I.n_rows = n_rows; I.m = m; I.n_work = (int32_t)n_work; I.table_slots = table_slots;
+  I.n_pfb = (int32_t)pfb.size();
   size_t off = 0;
   auto take = [&](size_t b) { size_t o = off; off = align_up(off + b, 16); return o; };
   I.off_rows = take(n_rows * sizeof(RowDev));
@@ -651,6 +695,8 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   I.off_tables = take((size_t)table_slots * mbps * 4);
   I.off_work = take(n_work * sizeof(AttnWork));
   I.off_row_work = take((n_rows + 1) * 4);
+  I.off_pfb = take(pfb.size() * sizeof(PfBlock));
+  I.off_pf_rows = take(pf_rows.size() * 4);
   I.bytes.assign(off, 0);
   uint8_t* B = I.bytes.data();
   RowDev* rd = reinterpret_cast<RowDev*>(B + I.off_rows);
@@ -663,22 +709,7 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   int32_t max_chunks = 0;
   for (int32_t r = 0; r < n_rows; ++r) {
     const cbd_row& w = rows[r];
-    rd[r] = RowDev{w.slot, w.token, w.pos, (w.is_prefill ? 1 : 0) | (w.sample ? 2 : 0)};
-    rw[r] = wi;
-    const int32_t nch = w.pos / kAttnChunk + 1;
-    max_chunks = std::max(max_chunks, nch);
-    for (int32_t c = 0; c < nch; ++c) {
-      AttnWork a{};
-      a.row = r;
-      a.start = c * kAttnChunk;
-      a.end = std::min(a.start + kAttnChunk, w.pos + 1);
-      a.wn = (wi << 16) | nch;
-      for (int32_t j = 0; j < kAttnChunk / kBlock; ++j) {
-        const int32_t p0 = a.start + j * kBlock;
-        a.blk[j] = p0 < a.end ? tables[(size_t)w.slot * mbps + p0 / kBlock] : -1;
-      }
-      wk[wi++] = a;
-    }
+    rd[r] = RowDev{w.slot, w.token, w.pos, (w.is_prefill ? 1 : 0) | (w.sample ? 2 : 0) | (in_run[r] ? 4 : 0)};
     if (w.sample) {
       const cbd_sampling& s = sp[j];
       sr[j] = r;
@@ -690,13 +721,41 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
       ++j;
     }
   }
+  // work items: rows outside prefill runs first, then the runs' rows (which
+  // the prefill kernel covers when it runs); a row's items are consecutive
+  int32_t n_dec = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int32_t r = 0; r < n_rows; ++r) {
+      if (in_run[r] != pass) continue;
+      const cbd_row& w = rows[r];
+      rw[r] = wi;
+      const int32_t nch = w.pos / kAttnChunk + 1;
+      max_chunks = std::max(max_chunks, nch);
+      for (int32_t c = 0; c < nch; ++c) {
+        AttnWork a{};
+        a.row = r;
+        a.start = c * kAttnChunk;
+        a.end = std::min(a.start + kAttnChunk, w.pos + 1);
+        a.wn = (wi << 16) | nch;
+        for (int32_t k = 0; k < kAttnChunk / kBlock; ++k) {
+          const int32_t p0 = a.start + k * kBlock;
+          a.blk[k] = p0 < a.end ? tables[(size_t)w.slot * mbps + p0 / kBlock] : -1;
+        }
+        wk[wi++] = a;
+      }
+    }
+    if (pass == 0) n_dec = wi;
+  }
   rw[n_rows] = wi;
   I.max_chunks = max_chunks;
-  // largest chunks first (ties in chunk order): dynamic scheduling then
-  // ends on the short last chunks of rows
-  std::stable_sort(wk, wk + wi, [](const AttnWork& x, const AttnWork& y) {
-    return (x.end - x.start) > (y.end - y.start);
-  });
+  I.n_dec = n_dec;
+  // within each part, largest chunks first (ties in chunk order): dynamic
+  // scheduling then ends on the short last chunks of rows
+  auto by_size = [](const AttnWork& x, const AttnWork& y) { return (x.end - x.start) > (y.end - y.start); };
+  std::stable_sort(wk, wk + n_dec, by_size);
+  std::stable_sort(wk + n_dec, wk + wi, by_size);
+  if (!pfb.empty()) std::memcpy(B + I.off_pfb, pfb.data(), pfb.size() * sizeof(PfBlock));
+  if (!pf_rows.empty()) std::memcpy(B + I.off_pf_rows, pf_rows.data(), pf_rows.size() * 4);
   std::memcpy(B + I.off_tables, tables, (size_t)table_slots * mbps * 4);
   return CBD_OK;
 }
@@ -714,6 +773,10 @@ void bind_batch(cbd_batch* b, const BatchImage& I, void* dev) {
   b->tables = reinterpret_cast<int32_t*>(D + I.off_tables);
   b->work = reinterpret_cast<AttnWork*>(D + I.off_work);
   b->row_work = reinterpret_cast<int32_t*>(D + I.off_row_work);
+  b->pfb = reinterpret_cast<PfBlock*>(D + I.off_pfb);
+  b->pf_rows = reinterpret_cast<int32_t*>(D + I.off_pf_rows);
+  b->n_dec = I.n_dec;
+  b->n_pfb = I.n_pfb;
 }
 
 static cudaEvent_t prof_event(cbd_engine* e) {
@@ -846,7 +909,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
     if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res_dn, pf_after_dn, s); }),
                   "down")))
       return st;
-    launches += 6;
+    launches += 4 + attention_launches(e, b);
   }
   if (b->m > 0) {
     float* lg = out_logits ? out_logits : e->logits;
@@ -895,7 +958,8 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
     const uint64_t key[cbd_engine::kStepGraphKey] = {
         (uint64_t)img.n_rows, (uint64_t)img.m, (uint64_t)img.n_work, (uint64_t)img.table_slots,
         (uint64_t)img.max_chunks, (uint64_t)img.bytes.size(), reinterpret_cast<uint64_t>(pool),
-        reinterpret_cast<uint64_t>(out_tokens), reinterpret_cast<uint64_t>(out_logits), e->epoch};
+        reinterpret_cast<uint64_t>(out_tokens), reinterpret_cast<uint64_t>(out_logits), e->epoch,
+        (uint64_t)img.n_dec, (uint64_t)img.n_pfb};
     auto& cache = e->step_graphs[&sg - e->stage];
     cbd_engine::StepGraph* hit = nullptr;
     for (auto& g : cache)
@@ -991,7 +1055,7 @@ extern "C" cbd_status cbd_batch_create(cbd_engine* e, cbd_kv_pool* pool, const c
   bind_batch(b.get(), img, dev);
   b->owns_dev = true;
   // launch count of one run
-  b->launches = 1 + 8 * e->dm.L + (img.m > 0 ? 3 : 0);
+  b->launches = 1 + e->dm.L * (4 + attention_launches(e, b.get()) + (e->fuse_norm ? 0 : 2)) + (img.m > 0 ? 3 : 0);
   *out = b.release();
   return CBD_OK;
 }

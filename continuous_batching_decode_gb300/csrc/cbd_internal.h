@@ -58,6 +58,16 @@ struct AttnWork {
 };
 static_assert(sizeof(AttnWork) == 32, "two 16-byte loads per record");
 
+// A block of prompt rows for the prefill attention kernel: positions
+// pos0 .. pos0 + npos - 1 of `slot`, held by the step's rows
+// pf_rows[idx0 .. idx0 + npos - 1] (in position order).
+struct PfBlock {
+  int32_t idx0, npos, pos0, slot;
+};
+// runs of at least this many consecutive positions of one slot (wherever
+// their rows sit in the step) go to the prefill attention kernel
+constexpr int kPfMinRun = 16;
+
 struct LayerDev {
   const float* attn_norm;            // [d] fp32
   const float* ffn_norm;             // [d] fp32
@@ -162,7 +172,7 @@ struct cbd_engine {
   cbd_batch* step_batch = nullptr;    // batch object reused by cbd_step
   // cbd_step as CUDA graphs (cbd_engine_set_step_graph): per staging buffer,
   // a few graphs keyed by everything their launches bake in
-  static constexpr int kStepGraphKey = 10;
+  static constexpr int kStepGraphKey = 12;
   static constexpr size_t kStepGraphCache = 8;
   struct StepGraph {
     uint64_t key[kStepGraphKey];
@@ -184,6 +194,7 @@ struct cbd_engine {
   int rows_gemm_min = 256;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
   bool rows_gemm_force = false;       // ... for every GEMM of such a step, however it fills the GPU
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
+  bool prefill_attn = true;           // path 0, bf16 K/V: prefill runs on the prefill attention kernel
   uint64_t epoch = 1;                 // bumped by every setting that changes the launch sequence
   bool kv_fp8 = false;                // K/V stored as E4M3 bytes (cbd_config.kv_fp8)
   cudaStream_t cap_stream = nullptr;  // private stream for graph capture
@@ -206,13 +217,17 @@ struct cbd_batch {
   void* dev = nullptr;                // device copy of everything below
   size_t dev_bytes = 0;
   int32_t n_rows = 0, m = 0, n_work = 0, table_slots = 0, max_chunks = 0;
+  int32_t n_dec = 0;                  // work items of rows outside prefill runs (they come first)
+  int32_t n_pfb = 0;                  // prefill attention blocks
   // device pointers into `dev`
   cbd::RowDev* rows = nullptr;
   int32_t* sampled_rows = nullptr;    // [m] row index of each sampled row
   int32_t* sampled_slots = nullptr;   // [m]
   cbd::SampDev* samp = nullptr;       // [m]
   int32_t* tables = nullptr;          // [table_slots][max_blocks_per_seq]
-  cbd::AttnWork* work = nullptr;      // [n_work]
+  cbd::AttnWork* work = nullptr;      // [n_work]: rows outside prefill runs, then rows inside
+  cbd::PfBlock* pfb = nullptr;        // [n_pfb], longest context first
+  int32_t* pf_rows = nullptr;         // rows of the prefill runs, by slot and position
   int32_t* row_work = nullptr;        // [n_rows + 1] prefix: first work item of each row
   int32_t launches = 0;
   // CUDA graph of one run's launch sequence (cbd_batch_set_graph)
@@ -231,8 +246,8 @@ namespace cbd {
 // image (host buffer `img`) with its offsets.  Returns CBD_OK or CBD_EINVAL.
 struct BatchImage {
   std::vector<uint8_t> bytes;
-  size_t off_rows, off_sr, off_ss, off_samp, off_tables, off_work, off_row_work;
-  int32_t n_rows, m, n_work, table_slots, max_chunks;
+  size_t off_rows, off_sr, off_ss, off_samp, off_tables, off_work, off_row_work, off_pfb, off_pf_rows;
+  int32_t n_rows, m, n_work, table_slots, max_chunks, n_dec, n_pfb;
 };
 cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const cbd_row* rows,
                              int32_t n_rows, const int32_t* tables, int32_t table_slots,
@@ -324,6 +339,13 @@ cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStre
 int gemm_tc_units(int M, int K, int N, int n);
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                    const PfSpec& pf, cudaStream_t s);
+// Prefill attention kernel (k_attn_pf.cu): query positions per block for a
+// KV group of G heads, and the launch over b's blocks.
+int prefill_block_positions(int G);
+cudaError_t launch_attn_prefill(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
+                                cudaStream_t s);
+// kernel launches launch_attention makes for b
+int attention_launches(const cbd_engine* e, const cbd_batch* b);
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                              const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,

@@ -355,13 +355,17 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const uint16_t* __restric
 // another.
 template <int HD, int G, bool LOG2>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                    const int32_t* __restrict__ row_work, int hq, int skip_single,
-                                    uint16_t* __restrict__ out_hi, uint16_t* __restrict__ out_lo) {
+                                    const RowDev* __restrict__ rows, const int32_t* __restrict__ row_work, int hq,
+                                    int skip_single, int skip_runs, uint16_t* __restrict__ out_hi,
+                                    uint16_t* __restrict__ out_lo) {
   extern __shared__ float2 sml[];          // [nch][G] (max, sum)
   TR_DECL;
   pdl_trigger();
   const int r = blockIdx.x, kvh = blockIdx.y;
-  const int w0 = row_work[r], nch = row_work[r + 1] - w0;
+  const RowDev rw = rows[r];
+  // rows of prefill runs: written by the prefill kernel when it ran
+  if (skip_runs && (rw.flags & 4)) return;
+  const int w0 = row_work[r], nch = rw.pos / kAttnChunk + 1;
   if (skip_single && nch == 1) return;
   pdl_wait();
   TR_MARK1;
@@ -405,6 +409,16 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
   TR_END(4);
 }
 
+// Prefill runs go to the prefill attention kernel: streaming path, bf16 K/V.
+static bool uses_prefill_kernel(const cbd_engine* e, const cbd_batch* b) {
+  return e->attn_path == 0 && !e->kv_fp8 && e->prefill_attn && b->n_pfb > 0;
+}
+
+int attention_launches(const cbd_engine* e, const cbd_batch* b) {
+  if (uses_prefill_kernel(e, b)) return (b->n_dec > 0 ? 1 : 0) + 2;
+  return 2;
+}
+
 template <int HD, int G>
 static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                  const PfSpec& pf, cudaStream_t s) {
@@ -421,15 +435,23 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
       if (ce != cudaSuccess) return ce;
       attr = true;
     }
-    const int n_tasks = b->n_work * dm.hkv;
-    const int grid = std::min(e->sm_count, (n_tasks + kStreamWarps - 1) / kStreamWarps);
-    cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(kStreamWarps * 32), smem, s,
-                                (const uint16_t*)p->base,
-                                (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
-                                (const AttnWork*)b->work, (const int32_t*)b->row_work, n_tasks, layer, p->n_blocks,
-                                dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi, e->act_lo,
-                                e->attn_next + layer, pf, e->err);
-    if (ce != cudaSuccess) return ce;
+    // with the prefill kernel, the streaming kernel takes the items of rows
+    // outside prefill runs (they come first in the list)
+    const int n_tasks = (uses_prefill_kernel(e, b) ? b->n_dec : b->n_work) * dm.hkv;
+    if (n_tasks > 0) {
+      const int grid = std::min(e->sm_count, (n_tasks + kStreamWarps - 1) / kStreamWarps);
+      cudaError_t ce = launch_pdl(attn_stream_kernel<HD, G>, dim3(grid), dim3(kStreamWarps * 32), smem, s,
+                                  (const uint16_t*)p->base,
+                                  (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
+                                  (const AttnWork*)b->work, (const int32_t*)b->row_work, n_tasks, layer,
+                                  p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->act_hi,
+                                  e->act_lo, e->attn_next + layer, pf, e->err);
+      if (ce != cudaSuccess) return ce;
+    }
+    if (uses_prefill_kernel(e, b)) {
+      cudaError_t ce = launch_attn_prefill(e, p, b, layer, s);
+      if (ce != cudaSuccess) return ce;
+    }
   } else if (e->attn_path == 2) {
     constexpr int smem = attn_mma_smem<HD>();
     static bool attr = false;
@@ -459,8 +481,8 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     if (ce != cudaSuccess) return ce;
   }
   return launch_pdl(combine, dim3(b->n_rows, dm.hkv), dim3(G * HD / 4), csmem, s, (const float*)e->attn_o,
-                    (const float*)e->attn_ml, (const int32_t*)b->row_work, dm.hq, e->attn_path == 0 ? 1 : 0,
-                    e->act_hi, e->act_lo);
+                    (const float*)e->attn_ml, (const RowDev*)b->rows, (const int32_t*)b->row_work, dm.hq,
+                    e->attn_path == 0 ? 1 : 0, uses_prefill_kernel(e, b) ? 1 : 0, e->act_hi, e->act_lo);
 }
 
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,

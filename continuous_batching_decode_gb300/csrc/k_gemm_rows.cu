@@ -88,7 +88,10 @@ __device__ __forceinline__ void rw_epilogue(const EpiArgs& ep, uint32_t taddr, i
   }
 }
 
-template <int N>
+// N = MMA N: the features of a unit; TP = weight tiles (of N / TP rows, the
+// weights' tiling) stacked into its B operand -- two 128-row tiles make one
+// 256-wide unit, so each activation stage feeds twice the MMA work.
+template <int N, int TP>
 __global__ void __launch_bounds__(kRwThreads, 1)
     gemm_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                      const __grid_constant__ CUtensorMap tmL, const RwArgs a, const EpiArgs ep) {
@@ -170,7 +173,11 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         const int nbox = (min(kRwRows, a.n - rt * kRwRows) + 15) / 16;
         tc::mbar_arrive_expect_tx(&full_bar[s], w_bytes + 2u * nbox * 2048u);
         // (no evict-first hint: the NRT units of a feature tile each read it)
-        tc::tma_load_2d(ring + (size_t)s * stage_bytes, &tmW, 0, (t * KB + q) * N, &full_bar[s]);
+        constexpr int NT = N / TP;                  // rows of one weight tile
+#pragma unroll
+        for (int tp = 0; tp < TP; ++tp)
+          tc::tma_load_2d(ring + (size_t)s * stage_bytes + tp * NT * 128, &tmW, 0, ((t * TP + tp) * KB + q) * NT,
+                          &full_bar[s]);
       };
       auto issue_a = [&](long long g) {
         int t, rt, q;
@@ -297,8 +304,8 @@ static int max_clusters(int S) {
   static int cache[kRwMaxCluster + 1] = {0};
   static std::once_flag once;
   std::call_once(once, [] {
-    for (auto k : {gemm_rows_kernel<256>, gemm_rows_kernel<224>, gemm_rows_kernel<192>, gemm_rows_kernel<160>,
-                   gemm_rows_kernel<128>})
+    for (auto k : {gemm_rows_kernel<256, 1>, gemm_rows_kernel<224, 1>, gemm_rows_kernel<192, 1>,
+                   gemm_rows_kernel<160, 1>, gemm_rows_kernel<128, 1>, gemm_rows_kernel<256, 2>})
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRwSmem);
     for (int c = 1; c <= kRwMaxCluster; c *= 2) {
       cudaLaunchConfig_t cfg = {};
@@ -313,7 +320,7 @@ static int max_clusters(int S) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_rows_kernel<256>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_rows_kernel<256, 1>, &cfg) != cudaSuccess) n = 0;
       cache[c] = n;
     }
     cudaGetLastError();
@@ -329,9 +336,12 @@ static int rows_cluster(int T) {
   return 1;
 }
 
+// Weight tiles per unit: 128-row tiles pair up into 256-wide units.
+static int rows_tp(const TcGemm& g) { return g.N == 128 && g.M % 256 == 0 ? 2 : 1; }
+
 bool gemm_rows_preferred(const TcGemm& g, int n) {
   if (g.N <= 0 || g.M % g.N || g.K % kRwBK) return false;
-  const int T = g.M / g.N, S = rows_cluster(T);
+  const int T = g.M / (g.N * rows_tp(g)), S = rows_cluster(T);
   const long long units = (long long)(T / S) * ((n + kRwRows - 1) / kRwRows);
   const int resident = max_clusters(S);
   if (resident <= 0) return false;
@@ -353,7 +363,8 @@ cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStre
   a.n = n;
   a.KB = g.K / kRwBK;
   a.NRT = (n + kRwRows - 1) / kRwRows;
-  const int T = g.M / g.N;
+  const int TP = rows_tp(g);
+  const int T = g.M / (g.N * TP);
   a.S = rows_cluster(T);
   a.units = (T / a.S) * a.NRT;
   a.err = ep.err;
@@ -378,12 +389,13 @@ cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStre
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
+  if (TP == 2) return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<256, 2>, *g.w, *g.hi, *g.lo, a, ep);
   switch (g.N) {
-    case 256: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<256>, *g.w, *g.hi, *g.lo, a, ep);
-    case 224: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<224>, *g.w, *g.hi, *g.lo, a, ep);
-    case 192: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<192>, *g.w, *g.hi, *g.lo, a, ep);
-    case 160: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<160>, *g.w, *g.hi, *g.lo, a, ep);
-    case 128: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<128>, *g.w, *g.hi, *g.lo, a, ep);
+    case 256: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<256, 1>, *g.w, *g.hi, *g.lo, a, ep);
+    case 224: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<224, 1>, *g.w, *g.hi, *g.lo, a, ep);
+    case 192: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<192, 1>, *g.w, *g.hi, *g.lo, a, ep);
+    case 160: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<160, 1>, *g.w, *g.hi, *g.lo, a, ep);
+    case 128: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<128, 1>, *g.w, *g.hi, *g.lo, a, ep);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -137,6 +137,16 @@ cbd_status cbd_engine_check(cbd_engine* e);
  * activations); they differ only in summation order.  Default: 0 and 4. */
 cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_max_rows);
 
+/* Attention of prefill runs (at least 16 rows of one slot at consecutive
+ * positions, wherever they sit in the step's row array: a prompt chunk,
+ * "20.3 服务、批处理与流式" section 20.3.2) on a kernel that takes blocks of
+ * consecutive query positions and streams each K/V block once per block of
+ * queries, instead of once per row.  Applies to attention path 0 with bf16
+ * K/V; the other rows keep the streaming kernel.  Same arithmetic (q and P
+ * split into bf16 hi + lo), summed in another order.  enable != 0: on (the
+ * default). */
+cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
+
 /* On the tcgen05 path, steps of at least min_rows rows (prefill chunks,
  * "20.3 服务、批处理与流式" section 20.3.2) may run their weight
  * contractions on a persistent kernel with 128-row activation tiles: each

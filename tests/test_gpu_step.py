@@ -153,22 +153,34 @@ def test_paging_and_row_order_are_bit_exact(tiny):
 
 
 def test_batched_equals_one_row_at_a_time(tiny):
-    """Batching must not change results: the step's rows run one per step
-    (prompt rows in order) give the same logits."""
+    """Batching does not change results: the step's rows run one per step
+    (prompt rows in order) give the same logits, bit for bit, with the
+    prefill attention kernel off (the streaming kernel sums every row the
+    same way whatever else is in the step); with it on (the default), the
+    40-row prompt chunk is summed in blocks and the logits agree within the
+    tolerance."""
     wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
     g = [dict(temperature=0.0)] * 5
-    toks_b, z_b = gu.run_step(tiny, pool, rows, tables, nbps, g)
+    toks_on, z_on = gu.run_step(tiny, pool, rows, tables, nbps, g)
     pool.close()
-    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
-    zs = []
-    for r in rows:
-        t, z = gu.run_step(tiny, pool, [r], tables, nbps, [dict(temperature=0.0)] if r[4] else [])
-        if r[4]:
-            zs.append(z[0])
-    pool.close()
+    cbd.engine_set_prefill_attention(tiny.e, False)
+    try:
+        wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
+        toks_b, z_b = gu.run_step(tiny, pool, rows, tables, nbps, g)
+        pool.close()
+        wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
+        zs = []
+        for r in rows:
+            t, z = gu.run_step(tiny, pool, [r], tables, nbps, [dict(temperature=0.0)] if r[4] else [])
+            if r[4]:
+                zs.append(z[0])
+        pool.close()
+    finally:
+        cbd.engine_set_prefill_attention(tiny.e, True)
     zs = np.array(zs)
     gu.assert_logits_close(zs, z_b, "batched vs single")
     np.testing.assert_array_equal(zs, z_b)
+    gu.assert_logits_close(z_on, z_b, "prefill kernel on vs off")
 
 
 def test_chunked_prefill_on_gpu(tiny):
