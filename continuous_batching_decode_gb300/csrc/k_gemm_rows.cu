@@ -11,11 +11,19 @@
 //     accumulators alternate: the epilogue warps drain one (TMEM -> registers
 //     -> the kind's epilogue -> global) while the MMA warp fills the other,
 //     so a unit's epilogue overlaps the next unit's mainloop;
-//   * K is not split (there are enough units), so there is no exchange.
+//   * K is not split (there are enough units), so there is no exchange;
+//   * clusters of S <= 4 CTAs take adjacent feature tiles of the same row
+//     tile; each copies 1/S of every stage's activation boxes and multicasts
+//     them to all S, so L2 serves fewer bytes per MMA (the copies, not the
+//     tensor pipe, were the limit with one CTA per unit);
+//   * weights tiled at 128 rows pair two tiles into one 256-wide unit.
 // Epilogues: QKV (RoPE, KV append through the block table), SwiGLU,
-// residual add and logits, per element pair (epi_pair / epi_single, shared
-// with the CUDA-core GEMV); the fused-RMSNorm epilogues stay on the decode
-// kernel, and steps routed here run the separate normalisation kernel.
+// residual add and logits, four features at a time (epi_quad, shared with
+// the 64-row-tile kernel).  A step that may route a GEMM here runs the
+// RMSNorm as its own kernel: folding it into these epilogues (the residual
+// epilogue writing x * g and partial sums of x^2, the consumers scaling by
+// 1/rms) measured no faster, the heavier residual epilogue costing what the
+// norm launches saved.
 #include <algorithm>
 #include <mutex>
 

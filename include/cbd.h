@@ -152,13 +152,13 @@ cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
  * contractions on a persistent kernel with 128-row activation tiles: each
  * weight tile feeds 128 rows per pass instead of 64, clusters of up to 4
  * CTAs share (multicast) each activation tile, and two TMEM accumulators
- * overlap one tile's epilogue with the next tile's mainloop.  Such a step
- * runs the RMSNorm as its own kernel.  With force == 0 a GEMM takes this
- * kernel only where its units fill at least 3/4 of the last wave of
- * resident clusters (else the 64-row-tile kernel, which splits K); with
- * force != 0 every GEMM of the step takes it.  Same sums as the other
- * paths, in another order.  min_rows 0 = never.  Default 256, force 0.
- * CBD_EINVAL if min_rows < 0. */
+ * overlap one tile's epilogue with the next tile's mainloop; such a step
+ * runs the RMSNorm as its own kernel.  With
+ * force == 0 a GEMM takes this kernel only where its units fill at least
+ * 3/4 of the last wave of resident clusters (else the 64-row-tile kernel,
+ * which splits K); with force != 0 every GEMM of the step takes it.  Same
+ * sums as the other paths, in another order.  min_rows 0 = never.
+ * Default 256, force 0.  CBD_EINVAL if min_rows < 0. */
 cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force);
 
 /* Choose the attention kernel: 0 = persistent streaming kernel (each warp
