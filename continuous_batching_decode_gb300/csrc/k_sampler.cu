@@ -1,7 +1,7 @@
 // Fused per-row sampler: penalty from the slot's decayed occurrence
 // counters, temperature, top-k, top-p, a Philox-4x32-10 uniform and an
 // inverse-CDF draw, then the counter update.  Parameters and defaults are
-// those of the Albatross backend article (discosf.com/news/5420690),
+// those of "RWKV Runner Albatross 后端",
 // sections "适配器" (temperature 1.0, top_p 0.3, top_k 0, frequency penalty 1,
 // decay 0.996) and "Worker 主循环" (penalties, then batched sampling of every
 // row).  The order of operations is this library's reading:

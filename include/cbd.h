@@ -3,7 +3,7 @@
  * of a decoder-only GQA transformer on one GB300 (sm_103a).
  *
  * The method, as the pages state it:
- *   - "20.3 服务、批处理与流式" (golang.design, under-the-hood ch. 20),
+ *   - "20.3 服务、批处理与流式",
  *     section 20.3.2 批处理: a decode step reads every weight once for the
  *     whole batch, costing about (W + B*A)/beta; scheduling is per model
  *     iteration, so requests join and leave every step; KV lives in a pool
@@ -14,11 +14,11 @@
  *     prefill chunks first, then one row per decoding sequence, and rows
  *     that do not fit wait instead of being evicted; the Scheduler (what to
  *     run) is kept apart from the Batch (running it).
- *   - "0.8MB 跑通 Qwen 第 14-1 篇" (developer.aliyun.com), sections 1-3: the
+ *   - "0.8MB 跑通 Qwen 第 14-1 篇", sections 1-3: the
  *     rows of one step form a dynamic set whose KV is indexed per request,
- *     computed by batched GQA / normalisation workers; batching must leave
- *     every output unchanged.
- *   - Albatross backend article (discosf.com/news/5420690), sections
+ *     computed by batched GQA / normalisation workers; batched and serial
+ *     runs gave byte-identical greedy outputs (near ties aside).
+ *   - "RWKV Runner Albatross 后端", sections
  *     "适配器" and "Worker 主循环": per-slot sampling parameters held on the
  *     device (temperature, top_p, top_k, presence / frequency penalty with
  *     decay 0.996), applied to every row of the batch after the forward.

@@ -16,16 +16,16 @@ philox     Philox-4x32-10 counter-based generator (Salmon et al., SC'11).
 sched_sim  the admission + step-composition policy, in plain Python.
 
 Sources.  The pages describe the method, not the layer maths:
-  * "20.3 服务、批处理与流式" (golang.design, under-the-hood ch. 20),
+  * "20.3 服务、批处理与流式",
     section 20.3.2 批处理: step cost (W + B*A)/beta, iteration-level
     scheduling, paged KV pool, admission that reserves prompt blocks plus an
     answer budget, prefill chunks first then one row per decoding sequence,
     no eviction; the scaled illustration (4 slots, 4 positions per block,
     8-token chunks, 12 rows per step; Forma: 32 positions, 512-token chunks).
-  * "0.8MB 跑通 Qwen 第 14-1 篇" (developer.aliyun.com), sections 1-3:
+  * "0.8MB 跑通 Qwen 第 14-1 篇", sections 1-3:
     batched decode reads the weights once per step for the whole dynamic set,
     GQA + normalisation workers, and batching leaves outputs byte-identical.
-  * The Albatross backend article (discosf.com/news/5420690), sections
+  * "RWKV Runner Albatross 后端", sections
     "适配器" and "Worker 主循环": sampling defaults temperature 1.0,
     top_p 0.3, top_k 0, frequency penalty 1, penalty decay 0.996; batched
     penalty + sampling after the forward.

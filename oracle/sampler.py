@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY -- see the package docstring for who may import it.
 
-Parameters come from the Albatross backend article (discosf.com/news/5420690),
+Parameters come from "RWKV Runner Albatross 后端",
 section "适配器": temperature 1.0, top_p 0.3, top_k 0, frequency penalty 1,
 penalty decay 0.996 are the defaults; section "Worker 主循环" applies
 presence / frequency penalties and then samples every row of the batch.  The

@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY -- see the package docstring for who may import it.
 
-Source: "20.3 服务、批处理与流式" (golang.design), section 20.3.2 批处理, the
+Source: "20.3 服务、批处理与流式", section 20.3.2 批处理, the
 Forma batch mode and its scaled illustration:
   * all slots share one pool of fixed-size KV blocks (32 positions; the
     illustration scales this to 4), allocated on demand;
