@@ -308,7 +308,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t stage_bytes = align_up(R * sizeof(RowDev), 16) + 2 * align_up(S * 4, 16) +
                              align_up(S * sizeof(SampDev), 16) + align_up(S * dm.max_blocks_per_seq * 4, 16) +
                              align_up((size_t)e->max_work * sizeof(AttnWork), 16) + align_up((R + 1) * 4, 16) +
-                             align_up(R * sizeof(PfBlock), 16) + align_up(R * 4, 16) + 256;
+                             align_up(R * sizeof(PfBlock), 16) + 2 * align_up(R * 4, 16) + 256;
   for (auto& sg : e->stage) {
     if (e3 == cudaSuccess) e3 = cudaMallocHost(&sg.host, stage_bytes);
     if (e3 == cudaSuccess) e3 = cudaMalloc(&sg.dev, stage_bytes);
@@ -697,6 +697,7 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   I.off_row_work = take((n_rows + 1) * 4);
   I.off_pfb = take(pfb.size() * sizeof(PfBlock));
   I.off_pf_rows = take(pf_rows.size() * 4);
+  I.off_comb = take((size_t)n_rows * 4);
   I.bytes.assign(off, 0);
   uint8_t* B = I.bytes.data();
   RowDev* rd = reinterpret_cast<RowDev*>(B + I.off_rows);
@@ -756,6 +757,16 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   std::stable_sort(wk + n_dec, wk + wi, by_size);
   if (!pfb.empty()) std::memcpy(B + I.off_pfb, pfb.data(), pfb.size() * sizeof(PfBlock));
   if (!pf_rows.empty()) std::memcpy(B + I.off_pf_rows, pf_rows.data(), pf_rows.size() * 4);
+  {
+    int32_t* cr = reinterpret_cast<int32_t*>(B + I.off_comb);
+    int32_t k = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int32_t r = 0; r < n_rows; ++r)
+        if (in_run[r] == pass && rows[r].pos >= kAttnChunk) cr[k++] = r;
+      if (pass == 0) I.n_comb_dec = k;
+    }
+    I.n_comb_all = k;
+  }
   std::memcpy(B + I.off_tables, tables, (size_t)table_slots * mbps * 4);
   return CBD_OK;
 }
@@ -775,6 +786,9 @@ void bind_batch(cbd_batch* b, const BatchImage& I, void* dev) {
   b->row_work = reinterpret_cast<int32_t*>(D + I.off_row_work);
   b->pfb = reinterpret_cast<PfBlock*>(D + I.off_pfb);
   b->pf_rows = reinterpret_cast<int32_t*>(D + I.off_pf_rows);
+  b->comb_rows = reinterpret_cast<int32_t*>(D + I.off_comb);
+  b->n_comb_dec = I.n_comb_dec;
+  b->n_comb_all = I.n_comb_all;
   b->n_dec = I.n_dec;
   b->n_pfb = I.n_pfb;
 }
@@ -959,7 +973,7 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
         (uint64_t)img.n_rows, (uint64_t)img.m, (uint64_t)img.n_work, (uint64_t)img.table_slots,
         (uint64_t)img.max_chunks, (uint64_t)img.bytes.size(), reinterpret_cast<uint64_t>(pool),
         reinterpret_cast<uint64_t>(out_tokens), reinterpret_cast<uint64_t>(out_logits), e->epoch,
-        (uint64_t)img.n_dec, (uint64_t)img.n_pfb};
+        (uint64_t)img.n_dec, (uint64_t)img.n_pfb, (uint64_t)img.n_comb_dec, (uint64_t)img.n_comb_all};
     auto& cache = e->step_graphs[&sg - e->stage];
     cbd_engine::StepGraph* hit = nullptr;
     for (auto& g : cache)

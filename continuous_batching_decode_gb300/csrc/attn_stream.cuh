@@ -512,8 +512,7 @@ __global__ void __launch_bounds__(stream_warps<HD, FP8>() * 32, 1) attn_stream_k
         for (int c = 0; c < 4; ++c) o[dt][c] += __shfl_xor_sync(0xffffffffu, o[dt][c], 2);
     }
     if (!alive) break;
-    // the row's chunks are consecutive work items, this one is chunk start / 128
-    const int nch = tk.nch, w0 = tk.wi - tk.start / kAttnChunk;
+    const int nch = tk.nch;
     if (nch == 1) {
       // the row's only chunk: normalise and write the output directly (the
       // merge kernel skips such rows; o * e^0 / (l * e^0) is the same value)

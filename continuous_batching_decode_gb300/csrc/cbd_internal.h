@@ -172,7 +172,7 @@ struct cbd_engine {
   cbd_batch* step_batch = nullptr;    // batch object reused by cbd_step
   // cbd_step as CUDA graphs (cbd_engine_set_step_graph): per staging buffer,
   // a few graphs keyed by everything their launches bake in
-  static constexpr int kStepGraphKey = 12;
+  static constexpr int kStepGraphKey = 14;
   static constexpr size_t kStepGraphCache = 8;
   struct StepGraph {
     uint64_t key[kStepGraphKey];
@@ -228,6 +228,10 @@ struct cbd_batch {
   cbd::AttnWork* work = nullptr;      // [n_work]: rows outside prefill runs, then rows inside
   cbd::PfBlock* pfb = nullptr;        // [n_pfb], longest context first
   int32_t* pf_rows = nullptr;         // rows of the prefill runs, by slot and position
+  // rows whose chunk partials the merge kernel combines (more than one
+  // chunk): those outside prefill runs first (n_comb_dec), then the rest
+  int32_t* comb_rows = nullptr;
+  int32_t n_comb_dec = 0, n_comb_all = 0;
   int32_t* row_work = nullptr;        // [n_rows + 1] prefix: first work item of each row
   int32_t launches = 0;
   // CUDA graph of one run's launch sequence (cbd_batch_set_graph)
@@ -246,8 +250,8 @@ namespace cbd {
 // image (host buffer `img`) with its offsets.  Returns CBD_OK or CBD_EINVAL.
 struct BatchImage {
   std::vector<uint8_t> bytes;
-  size_t off_rows, off_sr, off_ss, off_samp, off_tables, off_work, off_row_work, off_pfb, off_pf_rows;
-  int32_t n_rows, m, n_work, table_slots, max_chunks, n_dec, n_pfb;
+  size_t off_rows, off_sr, off_ss, off_samp, off_tables, off_work, off_row_work, off_pfb, off_pf_rows, off_comb;
+  int32_t n_rows, m, n_work, table_slots, max_chunks, n_dec, n_pfb, n_comb_dec, n_comb_all;
 };
 cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const cbd_row* rows,
                              int32_t n_rows, const int32_t* tables, int32_t table_slots,

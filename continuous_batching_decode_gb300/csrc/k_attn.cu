@@ -355,18 +355,16 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const uint16_t* __restric
 // another.
 template <int HD, int G, bool LOG2>
 __global__ void attn_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                    const RowDev* __restrict__ rows, const int32_t* __restrict__ row_work, int hq,
-                                    int skip_single, int skip_runs, uint16_t* __restrict__ out_hi,
+                                    const RowDev* __restrict__ rows, const int32_t* __restrict__ row_work,
+                                    const int32_t* __restrict__ comb_rows, int hq, uint16_t* __restrict__ out_hi,
                                     uint16_t* __restrict__ out_lo) {
   extern __shared__ float2 sml[];          // [nch][G] (max, sum)
   TR_DECL;
   pdl_trigger();
-  const int r = blockIdx.x, kvh = blockIdx.y;
-  const RowDev rw = rows[r];
-  // rows of prefill runs: written by the prefill kernel when it ran
-  if (skip_runs && (rw.flags & 4)) return;
-  const int w0 = row_work[r], nch = rw.pos / kAttnChunk + 1;
-  if (skip_single && nch == 1) return;
+  // the listed rows (more than one chunk, and not written by the prefill
+  // kernel), or every row when there is no list
+  const int r = comb_rows ? comb_rows[blockIdx.x] : (int)blockIdx.x, kvh = blockIdx.y;
+  const int w0 = row_work[r], nch = rows[r].pos / kAttnChunk + 1;
   pdl_wait();
   TR_MARK1;
   for (int i = threadIdx.x; i < nch * G; i += blockDim.x) {
@@ -414,9 +412,18 @@ static bool uses_prefill_kernel(const cbd_engine* e, const cbd_batch* b) {
   return e->attn_path == 0 && !e->kv_fp8 && e->prefill_attn && b->n_pfb > 0;
 }
 
+// Rows the merge kernel combines: on the streaming path the listed rows with
+// more than one chunk (those outside prefill runs when the prefill kernel
+// writes the runs); on the other paths every row (they write partials only).
+static int merge_rows(const cbd_engine* e, const cbd_batch* b) {
+  if (e->attn_path != 0) return b->n_rows;
+  return uses_prefill_kernel(e, b) ? b->n_comb_dec : b->n_comb_all;
+}
+
 int attention_launches(const cbd_engine* e, const cbd_batch* b) {
-  if (uses_prefill_kernel(e, b)) return (b->n_dec > 0 ? 1 : 0) + 2;
-  return 2;
+  if (e->attn_path != 0 || e->kv_fp8) return 1 + (merge_rows(e, b) > 0 ? 1 : 0);
+  const bool pf = uses_prefill_kernel(e, b);
+  return ((pf ? b->n_dec : b->n_work) > 0 ? 1 : 0) + (pf ? 1 : 0) + (merge_rows(e, b) > 0 ? 1 : 0);
 }
 
 template <int HD, int G>
@@ -472,17 +479,21 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
                                 dm.max_blocks_per_seq, e->attn_o, e->attn_ml, e->err);
     if (ce != cudaSuccess) return ce;
   }
-  // single-chunk rows: the streaming kernel wrote them; the others write partials only
-  // the streaming kernel keeps its maxima in log2 units (exp2 softmax)
+  // the streaming kernels write single-chunk rows themselves (and the
+  // prefill kernel its runs); the other paths write partials only.  The
+  // streaming kernels keep their maxima in log2 units (exp2 softmax).
   const size_t csmem = (size_t)b->max_chunks * G * sizeof(float2);
   auto combine = e->attn_path == 0 ? attn_combine_kernel<HD, G, true> : attn_combine_kernel<HD, G, false>;
   if (csmem > 48 * 1024) {
     cudaError_t ce = cudaFuncSetAttribute(combine, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     if (ce != cudaSuccess) return ce;
   }
-  return launch_pdl(combine, dim3(b->n_rows, dm.hkv), dim3(G * HD / 4), csmem, s, (const float*)e->attn_o,
-                    (const float*)e->attn_ml, (const RowDev*)b->rows, (const int32_t*)b->row_work, dm.hq,
-                    e->attn_path == 0 ? 1 : 0, uses_prefill_kernel(e, b) ? 1 : 0, e->act_hi, e->act_lo);
+  const int nm = merge_rows(e, b);
+  if (nm <= 0) return cudaSuccess;
+  return launch_pdl(combine, dim3(nm, dm.hkv), dim3(G * HD / 4), csmem, s, (const float*)e->attn_o,
+                    (const float*)e->attn_ml, (const RowDev*)b->rows, (const int32_t*)b->row_work,
+                    e->attn_path == 0 ? (const int32_t*)b->comb_rows : (const int32_t*)nullptr, dm.hq, e->act_hi,
+                    e->act_lo);
 }
 
 cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,

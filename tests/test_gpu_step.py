@@ -183,6 +183,30 @@ def test_batched_equals_one_row_at_a_time(tiny):
     gu.assert_logits_close(z_on, z_b, "prefill kernel on vs off")
 
 
+def test_batched_equals_independent_sequences(tiny):
+    """A batched step equals its sequences run as independent steps (each
+    slot's rows alone: the 40-row prompt chunk as one step, each decode row
+    as one), bit for bit, on the default path -- the prompt chunk takes the
+    prefill attention kernel in both, and a row's result there does not
+    depend on the other rows ("0.8MB 跑通 Qwen 第 14-1 篇", section 3:
+    batching left the outputs byte-identical)."""
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 4)
+    g = [dict(temperature=0.0)] * 5
+    toks_b, z_b = gu.run_step(tiny, pool, rows, tables, nbps, g)
+    pool.close()
+    wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 4)
+    zs, ts = [], []
+    for slot in sorted({r[0] for r in rows}):
+        part = [r for r in rows if r[0] == slot]
+        m = sum(1 for r in part if r[4])
+        t, z = gu.run_step(tiny, pool, part, tables, nbps, [dict(temperature=0.0)] * m)
+        zs += list(z)
+        ts += list(t)
+    pool.close()
+    np.testing.assert_array_equal(np.array(zs), z_b)
+    np.testing.assert_array_equal(np.array(ts), toks_b)
+
+
 def test_chunked_prefill_on_gpu(tiny):
     V = tiny.shape["vocab"]
     prompt = list(np.random.default_rng(5).integers(0, V, 40))
