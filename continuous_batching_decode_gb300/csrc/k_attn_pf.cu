@@ -29,8 +29,9 @@ namespace cbd {
 constexpr int kPfQRows = 64;                 // query rows (position x head) per CTA
 constexpr int kPfWarps = kPfQRows / 16;      // consumer warps
 constexpr int kPfStages = 4;
+// K/V ring, then the consumer warps' q tiles (16 rows x HD, bf16 hi and lo)
 template <int HD>
-__host__ __device__ constexpr int pf_smem() { return kPfStages * 2 * (32 * HD * 2) + 128; }
+__host__ __device__ constexpr int pf_smem() { return kPfStages * 2 * (32 * HD * 2) + kPfWarps * 2 * 16 * HD * 2 + 128; }
 
 template <int HD, int G>
 __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
@@ -106,20 +107,29 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
     qpos[i] = valid[i] ? blk.pos0 + lp[i] : nkeys - 1;
     row[i] = valid[i] ? pf_rows[blk.idx0 + lp[i]] : 0;
   }
-  // q (scaled to log2 units) as A fragments, bf16 hi and lo
+  // q (scaled to log2 units), split into bf16 hi and lo, into this warp's
+  // shared tiles [16 rows][HD] (16-byte chunk c of row r at c ^ (r & 7));
+  // the q.K loop reads them back as A fragments with ldmatrix
   const float scale = 1.4426950408889634f / sqrtf((float)HD);
-  uint32_t qh[KS][4], ql[KS][4];
+  uint8_t* qt = ring + kPfStages * 2 * TILE + warp * 2 * (16 * HD * 2);
+  const uint32_t qhb = tc::smem_u32(qt), qlb = qhb + 16 * HD * 2;
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
     for (int f = 0; f < 4; ++f) {
-      const int i = f & 1;                               // a0, a2: row gid; a1, a3: row gid + 8
+      const int i = f & 1;                               // fragment rows gid and gid + 8
       const int d = ks * 16 + (f >> 1) * 8 + tid4 * 2;
       float2 v = make_float2(0.f, 0.f);
       if (valid[i])
         v = *reinterpret_cast<const float2*>(q + ((size_t)row[i] * hq + kvh * G + hh[i]) * HD + d);
-      split_pack(v.x * scale, v.y * scale, qh[ks][f], ql[ks][f]);
+      uint32_t h, l;
+      split_pack(v.x * scale, v.y * scale, h, l);
+      const int rr = gid + 8 * i, chq = d >> 3;
+      const uint32_t off = (uint32_t)(rr * HD * 2 + ((chq ^ (rr & 7)) << 4) + tid4 * 4);
+      *reinterpret_cast<uint32_t*>(qt + off) = h;
+      *reinterpret_cast<uint32_t*>(qt + 16 * HD * 2 + off) = l;
     }
+  __syncwarp();
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
   float o[DT][4];
 #pragma unroll
@@ -133,14 +143,28 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
     if (!tc::mbar_wait(&full[s], (j / kPfStages) & 1, err, &abort_flag)) break;
     const uint32_t kb = tc::smem_u32(ring + s * 2 * TILE), vb = kb + TILE;
     const int nv = min(32, nkeys - j * 32);      // positions of this block inside the sequence
-    // ---- S = q K^T: 4 n-tiles of 8 key positions
-    float sc[4][4];
+    // ---- S = q K^T: 4 n-tiles of 8 key positions; the q hi and q lo
+    // products accumulate in separate chains (so consecutive MMAs do not
+    // wait on each other) and are added once, in a fixed order
+    float sc[4][4], sl[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sc[nt][c] = 0.f;
+      for (int c = 0; c < 4; ++c) {
+        sc[nt][c] = 0.f;
+        sl[nt][c] = 0.f;
+      }
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
+    for (int ks = 0; ks < KS; ++ks) {
+      // q's A fragments for dims ks*16 .. +15: matrices (rows 0-7, dims 0-7),
+      // (rows 8-15, dims 0-7), (rows 0-7, dims 8-15), (rows 8-15, dims 8-15)
+      uint32_t ah[4], al[4];
+      {
+        const int rq = (mi & 1) * 8 + r8, cq = ks * 2 + (mi >> 1);
+        const uint32_t oq = (uint32_t)(rq * HD * 2 + ((cq ^ (rq & 7)) << 4));
+        ldsm_x4(qhb + oq, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(qlb + oq, al[0], al[1], al[2], al[3]);
+      }
 #pragma unroll
       for (int np = 0; np < 2; ++np) {
         // matrices: (n-tile 2np, dims ks*16 + 0..7), (2np, +8..15), (2np+1, +0..7), (2np+1, +8..15)
@@ -148,11 +172,16 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
         const int ch = ks * 2 + (mi & 1);
         uint32_t b0a, b1a, b0b, b1b;
         ldsm_x4(kb + (ch >> 3) * 4096 + swz(r, ch & 7), b0a, b1a, b0b, b1b);
-        mma_bf16_16816(sc[2 * np], qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3], b0a, b1a);
-        mma_bf16_16816(sc[2 * np], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b0a, b1a);
-        mma_bf16_16816(sc[2 * np + 1], qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3], b0b, b1b);
-        mma_bf16_16816(sc[2 * np + 1], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b0b, b1b);
+        mma_bf16_16816(sc[2 * np], ah[0], ah[1], ah[2], ah[3], b0a, b1a);
+        mma_bf16_16816(sl[2 * np], al[0], al[1], al[2], al[3], b0a, b1a);
+        mma_bf16_16816(sc[2 * np + 1], ah[0], ah[1], ah[2], ah[3], b0b, b1b);
+        mma_bf16_16816(sl[2 * np + 1], al[0], al[1], al[2], al[3], b0b, b1b);
       }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sc[nt][c] += sl[nt][c];
     // ---- causal mask and online softmax (rows gid: c = 0, 1; gid + 8: c = 2, 3)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
