@@ -155,10 +155,11 @@ cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
  * overlap one tile's epilogue with the next tile's mainloop; such a step
  * runs the RMSNorm as its own kernel.  With
  * force == 0 a GEMM takes this kernel only where its units fill at least
- * 3/4 of the last wave of resident clusters (else the 64-row-tile kernel,
+ * half of the last wave of resident clusters (else the 64-row-tile kernel,
  * which splits K); with force != 0 every GEMM of the step takes it.  Same
  * sums as the other paths, in another order.  min_rows 0 = never.
- * Default 256, force 0.  CBD_EINVAL if min_rows < 0. */
+ * Default 384 (below it the 64-row-tile kernel with the fused RMSNorm was
+ * faster on the 7B shape), force 0.  CBD_EINVAL if min_rows < 0. */
 cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force);
 
 /* Choose the attention kernel: 0 = persistent streaming kernel (each warp
