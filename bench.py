@@ -554,7 +554,8 @@ def run_cbd(args):
         ms2 = ev0.elapsed_time(ev1) / args.steps
         by = W + sum(c + 1 for c in wl2["ctx"]) * kv_pos_bytes(s, eb)
         print(json.dumps({"sweep_B": Bs, "ms_per_step": round(ms2, 4), "tok_s": round(Bs / ms2 * 1000, 1),
-                          "GBs": round(by / ms2 / 1e6, 1), "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}),
+                          "GBs": round(by / ms2 / 1e6, 1), "frac_of_measured": round(by / ms2 / 1e6 / peak, 4),
+                          "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}),
               file=sys.stderr, flush=True)
         cbd.batch_destroy(b2)
     cbd.batch_destroy(b)

@@ -231,7 +231,7 @@ def engine_counters(e) -> int:
     return p.value
 
 
-def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 4) -> None:
+def engine_set_gemm_path(e, path: int, gemv_max_rows: int = 0) -> None:
     """0 automatic, 1 CUDA-core GEMV only, 2 tcgen05 only."""
     _check(lib().cbd_engine_set_gemm_path(e, path, gemv_max_rows))
 
