@@ -78,6 +78,8 @@ def parse():
                     help="steps of at least this many rows may run the 128-row-tile GEMM (0 = never)")
     ap.add_argument("--rows-gemm-force", action="store_true",
                     help="... on every GEMM of such a step (default: where it fills the GPU well)")
+    ap.add_argument("--no-prefill-attn", action="store_true",
+                    help="mixed step: prompt rows on the streaming attention kernel")
     ap.add_argument("--mixed", type=int, default=0,
                     help="prefill rows (512-row chunks) added to the B decode rows: one mixed-step line")
     ap.add_argument("--trace", action="store_true", help="serve the request trace (see the module docstring)")
@@ -599,16 +601,20 @@ def run_mixed(args):
     samp = [dict(temperature=1.0, top_p=0.3, frequency_penalty=1.0, penalty_decay=0.996, seed=args.seed,
                  request_id=i) for i in range(m)]
     w = synth.make_weights(s, seed=args.seed, device="cuda")
-    e = cbd.engine_create(cbd.make_config(s, max_rows=len(rows), max_slots=B + nch, max_blocks_per_seq=mbps), w)
+    fp8 = args.kv == "fp8"
+    e = cbd.engine_create(cbd.make_config(s, max_rows=len(rows), max_slots=B + nch, max_blocks_per_seq=mbps,
+                                          kv_fp8=fp8), w)
     del w
     torch.cuda.empty_cache()
     cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
+    cbd.engine_set_prefill_attention(e, not args.no_prefill_attn)
     pool = cbd.kv_pool_create(e, n_pool)
     base, nbytes, nb = cbd.kv_pool_data(pool)
-    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "bf16")
+    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "u8" if fp8 else "bf16")
     gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
     for l in range(s["n_layers"]):
-        kv[l].copy_((torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3).to(torch.bfloat16))
+        r = torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3
+        kv[l].copy_(r.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else r.to(torch.bfloat16))
     b = cbd.batch_create(e, pool, rows, tables, nbps, samp)
     out = torch.zeros(m, dtype=torch.int32, device="cuda")
     cbd.batch_set_graph(b, True)
@@ -653,7 +659,8 @@ def run_mixed(args):
             "kernels": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
             "config": {"workload": f"{args.shape}-shaped mixed step: {B} decode rows (ctx U[{args.ctx_lo},"
                                    f"{args.ctx_hi}]) + {P} prefill rows in 512-row chunks", "shape": args.shape,
-                       "rows_gemm_min": args.rows_gemm, "rows_gemm_force": args.rows_gemm_force},
+                       "rows_gemm_min": args.rows_gemm, "rows_gemm_force": args.rows_gemm_force,
+                       "kv": "e4m3" if fp8 else "bf16", "prefill_attention": not args.no_prefill_attn},
             "data": "synthetic (seeded random-init weights, random bf16 KV, random prompt ids)"}
     print(json.dumps(line), flush=True)
     cbd.batch_destroy(b)

@@ -342,7 +342,7 @@ bool gemm_rows_preferred(const TcGemm& g, int n);
 cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStream_t s);
 int gemm_tc_units(int M, int K, int N, int n);
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                                   const PfSpec& pf, cudaStream_t s);
+                                   int n_items, const PfSpec& pf, cudaStream_t s);
 // Prefill attention kernel (k_attn_pf.cu): query positions per block for a
 // KV group of G heads, and the launch over b's blocks.
 int prefill_block_positions(int G);

@@ -407,9 +407,9 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_o, const floa
   TR_END(4);
 }
 
-// Prefill runs go to the prefill attention kernel: streaming path, bf16 K/V.
+// Prefill runs go to the prefill attention kernel (streaming path).
 static bool uses_prefill_kernel(const cbd_engine* e, const cbd_batch* b) {
-  return e->attn_path == 0 && !e->kv_fp8 && e->prefill_attn && b->n_pfb > 0;
+  return e->attn_path == 0 && e->prefill_attn && b->n_pfb > 0;
 }
 
 // Rows the merge kernel combines: on the streaming path the listed rows with
@@ -421,7 +421,7 @@ static int merge_rows(const cbd_engine* e, const cbd_batch* b) {
 }
 
 int attention_launches(const cbd_engine* e, const cbd_batch* b) {
-  if (e->attn_path != 0 || e->kv_fp8) return 1 + (merge_rows(e, b) > 0 ? 1 : 0);
+  if (e->attn_path != 0) return 1 + (merge_rows(e, b) > 0 ? 1 : 0);
   const bool pf = uses_prefill_kernel(e, b);
   return ((pf ? b->n_dec : b->n_work) > 0 ? 1 : 0) + (pf ? 1 : 0) + (merge_rows(e, b) > 0 ? 1 : 0);
 }
@@ -432,8 +432,12 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
   const Dims& dm = e->dm;
   if (e->kv_fp8) {
     if (e->attn_path != 0) return cudaErrorNotSupported;
-    cudaError_t ce = launch_attn_stream_fp8(e, p, b, layer, pf, s);
+    cudaError_t ce = launch_attn_stream_fp8(e, p, b, layer, uses_prefill_kernel(e, b) ? b->n_dec : b->n_work, pf, s);
     if (ce != cudaSuccess) return ce;
+    if (uses_prefill_kernel(e, b)) {
+      ce = launch_attn_prefill(e, p, b, layer, s);
+      if (ce != cudaSuccess) return ce;
+    }
   } else if (e->attn_path == 0) {
     constexpr int smem = attn_stream_smem<HD>();
     static bool attr = false;

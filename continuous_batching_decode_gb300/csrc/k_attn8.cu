@@ -13,7 +13,7 @@ namespace cbd {
 
 template <int HD, int G>
 static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                                const PfSpec& pf, cudaStream_t s) {
+                                int n_items, const PfSpec& pf, cudaStream_t s) {
   const Dims& dm = e->dm;
   constexpr int smem = stream_smem<HD, true>();
   constexpr int NW = stream_warps<HD, true>();
@@ -24,7 +24,8 @@ static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const
     if (ce != cudaSuccess) return ce;
     attr = true;
   }
-  const int n_tasks = b->n_work * dm.hkv;
+  const int n_tasks = n_items * dm.hkv;
+  if (n_tasks <= 0) return cudaSuccess;
   const int grid = std::min(e->sm_count, (n_tasks + NW - 1) / NW);
   return launch_pdl(attn_stream_kernel<HD, G, true>, dim3(grid), dim3(NW * 32), smem, s,
                     (const uint16_t*)p->base, (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,
@@ -34,17 +35,17 @@ static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const
 }
 
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
-                                   const PfSpec& pf, cudaStream_t s) {
+                                   int n_items, const PfSpec& pf, cudaStream_t s) {
   const int G = e->dm.hq / e->dm.hkv;
   const int HD = e->dm.hd;
-  if (HD == 64 && G == 1) return launch_fp8_t<64, 1>(e, p, b, layer, pf, s);
-  if (HD == 64 && G == 2) return launch_fp8_t<64, 2>(e, p, b, layer, pf, s);
-  if (HD == 64 && G == 4) return launch_fp8_t<64, 4>(e, p, b, layer, pf, s);
-  if (HD == 64 && G == 8) return launch_fp8_t<64, 8>(e, p, b, layer, pf, s);
-  if (HD == 128 && G == 1) return launch_fp8_t<128, 1>(e, p, b, layer, pf, s);
-  if (HD == 128 && G == 2) return launch_fp8_t<128, 2>(e, p, b, layer, pf, s);
-  if (HD == 128 && G == 4) return launch_fp8_t<128, 4>(e, p, b, layer, pf, s);
-  if (HD == 128 && G == 8) return launch_fp8_t<128, 8>(e, p, b, layer, pf, s);
+  if (HD == 64 && G == 1) return launch_fp8_t<64, 1>(e, p, b, layer, n_items, pf, s);
+  if (HD == 64 && G == 2) return launch_fp8_t<64, 2>(e, p, b, layer, n_items, pf, s);
+  if (HD == 64 && G == 4) return launch_fp8_t<64, 4>(e, p, b, layer, n_items, pf, s);
+  if (HD == 64 && G == 8) return launch_fp8_t<64, 8>(e, p, b, layer, n_items, pf, s);
+  if (HD == 128 && G == 1) return launch_fp8_t<128, 1>(e, p, b, layer, n_items, pf, s);
+  if (HD == 128 && G == 2) return launch_fp8_t<128, 2>(e, p, b, layer, n_items, pf, s);
+  if (HD == 128 && G == 4) return launch_fp8_t<128, 4>(e, p, b, layer, n_items, pf, s);
+  if (HD == 128 && G == 8) return launch_fp8_t<128, 8>(e, p, b, layer, n_items, pf, s);
   return cudaErrorInvalidValue;
 }
 

@@ -29,17 +29,29 @@ namespace cbd {
 constexpr int kPfQRows = 64;                 // query rows (position x head) per CTA
 constexpr int kPfWarps = kPfQRows / 16;      // consumer warps
 constexpr int kPfStages = 4;
-// K/V ring, then the consumer warps' q tiles (16 rows x HD, bf16 hi and lo)
-template <int HD>
-__host__ __device__ constexpr int pf_smem() { return kPfStages * 2 * (32 * HD * 2) + kPfWarps * 2 * 16 * HD * 2 + 128; }
+// K/V ring, then the consumer warps' q tiles (16 rows x HD, hi and lo)
+template <int HD, bool FP8>
+__host__ __device__ constexpr int pf_smem() {
+  return kPfStages * 2 * (32 * HD * (FP8 ? 1 : 2)) + kPfWarps * 2 * 16 * HD * 2 + 128;
+}
 
-template <int HD, int G>
+// FP8 = true: K and V are E4M3 bytes (K tiles [position][dim], V tiles
+// transposed [dim][position], 16-byte chunks swizzled per row), converted
+// exactly to f16 in registers; q and P are split into f16 hi + lo and the
+// products are f16 MMAs.  An ldmatrix over byte pairs gives a lane 4
+// consecutive bytes of a row, so the MMA's k index is permuted -- k pair
+// (2t, 2t+1) takes bytes 4t, 4t+1 of the 16-byte chunk and (2t+8, 2t+9)
+// bytes 4t+2, 4t+3 -- on both operands of each product: q is stored in that
+// dim order, and the key rows of each q.K n-tile are loaded in the order that
+// puts P's C fragment directly into the A fragment P.V needs (n-tile 2kk + h
+// holds keys kk*16 + 4 (n >> 1) + 2 h + (n & 1), n = 0..7).
+template <int HD, int G, bool FP8>
 __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
     const uint16_t* __restrict__ pool, const float* __restrict__ q, const PfBlock* __restrict__ blocks,
     const int32_t* __restrict__ pf_rows, const int32_t* __restrict__ tables, int layer, int n_blocks, int hkv, int mbps, uint16_t* __restrict__ out_hi,
     uint16_t* __restrict__ out_lo, int32_t* err) {
   static_assert(kPfQRows % G == 0, "a position's heads share a warp");
-  constexpr int TILE = 32 * HD * 2;          // bytes of one K (or V) tile
+  constexpr int TILE = 32 * HD * (FP8 ? 1 : 2);    // bytes of one K (or V) tile
   constexpr int KS = HD / 16;                // k-steps of q.K
   constexpr int DT = HD / 8;                 // n-tiles of P.V
   extern __shared__ uint8_t sm_raw[];
@@ -79,8 +91,8 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
           b = 0;
         }
         tc::mbar_arrive_expect_tx(&full[s], 2 * TILE);
-        tc::bulk_load(ring + s * 2 * TILE, pb + pool_tile(layer, n_blocks, b, hkv, kvh, 0, HD) * 2, 2 * TILE,
-                      &full[s]);
+        tc::bulk_load(ring + s * 2 * TILE, pb + pool_tile(layer, n_blocks, b, hkv, kvh, 0, HD) * (FP8 ? 1 : 2),
+                      2 * TILE, &full[s]);
       }
       if (j < ntiles) {     // gave up: the copies in flight land before the CTA exits
         for (int r = j > kPfStages ? j - kPfStages : 0; r < j; ++r) {
@@ -118,12 +130,16 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
 #pragma unroll
     for (int f = 0; f < 4; ++f) {
       const int i = f & 1;                               // fragment rows gid and gid + 8
+      // fragment k position ks*16 + (f >> 1) * 8 + tid4 * 2 (+1) holds that dim,
+      // or for FP8 dims ks*16 + 4 tid4 + 2 (f >> 1) (+1)
       const int d = ks * 16 + (f >> 1) * 8 + tid4 * 2;
+      const int dq = FP8 ? ks * 16 + tid4 * 4 + (f >> 1) * 2 : d;
       float2 v = make_float2(0.f, 0.f);
       if (valid[i])
-        v = *reinterpret_cast<const float2*>(q + ((size_t)row[i] * hq + kvh * G + hh[i]) * HD + d);
+        v = *reinterpret_cast<const float2*>(q + ((size_t)row[i] * hq + kvh * G + hh[i]) * HD + dq);
       uint32_t h, l;
-      split_pack(v.x * scale, v.y * scale, h, l);
+      if constexpr (FP8) split_pack_h(v.x * scale, v.y * scale, h, l);
+      else split_pack(v.x * scale, v.y * scale, h, l);
       const int rr = gid + 8 * i, chq = d >> 3;
       const uint32_t off = (uint32_t)(rr * HD * 2 + ((chq ^ (rr & 7)) << 4) + tid4 * 4);
       *reinterpret_cast<uint32_t*>(qt + off) = h;
@@ -165,6 +181,18 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
         ldsm_x4(qhb + oq, ah[0], ah[1], ah[2], ah[3]);
         ldsm_x4(qlb + oq, al[0], al[1], al[2], al[3]);
       }
+      if constexpr (FP8) {
+        // matrix mi = n-tile mi: 8 key rows (permuted), the 16-byte chunk of dims ks*16..
+        const int key = (mi >> 1) * 16 + 4 * (r8 >> 1) + 2 * (mi & 1) + (r8 & 1);
+        uint32_t kr[4];
+        ldsm_x4(kb + k8_off<HD>(key, ks), kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const uint32_t b0 = e4m3_lo(kr[nt]), b1 = e4m3_hi(kr[nt]);
+          mma_f16_16816(sc[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
+          mma_f16_16816(sl[nt], al[0], al[1], al[2], al[3], b0, b1);
+        }
+      } else {
 #pragma unroll
       for (int np = 0; np < 2; ++np) {
         // matrices: (n-tile 2np, dims ks*16 + 0..7), (2np, +8..15), (2np+1, +0..7), (2np+1, +8..15)
@@ -177,6 +205,7 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
         mma_bf16_16816(sc[2 * np + 1], ah[0], ah[1], ah[2], ah[3], b0b, b1b);
         mma_bf16_16816(sl[2 * np + 1], al[0], al[1], al[2], al[3], b0b, b1b);
       }
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -188,7 +217,8 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int kp = j * 32 + nt * 8 + tid4 * 2 + (c & 1);
+        const int kp = FP8 ? j * 32 + (nt >> 1) * 16 + tid4 * 4 + (nt & 1) * 2 + (c & 1)
+                           : j * 32 + nt * 8 + tid4 * 2 + (c & 1);
         if (kp > qpos[c >> 1]) sc[nt][c] = -INFINITY;
         mx[c >> 1] = fmaxf(mx[c >> 1], sc[nt][c]);
       }
@@ -219,6 +249,30 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       uint32_t ph[4], pl[4];
+      if constexpr (FP8) {
+        split_pack_h(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+        split_pack_h(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+        split_pack_h(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+        split_pack_h(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+        // V tile rows are dims: matrix mi = dim tile 4 dq + mi, the 16-byte
+        // chunk of positions kk*16..; lane bytes 0,1 / 2,3 are keys
+        // kk*16 + 4 tid4 + 0,1 / + 2,3
+        const int k0 = kk * 16 + tid4 * 4;
+        const uint32_t m0 = (k0 < nv ? 0xffffu : 0u) | (k0 + 1 < nv ? 0xffff0000u : 0u);
+        const uint32_t m1 = (k0 + 2 < nv ? 0xffffu : 0u) | (k0 + 3 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int dq = 0; dq < DT / 4; ++dq) {
+          uint32_t vr[4];
+          ldsm_x4(vb + v8_off((4 * dq + mi) * 8 + r8, kk), vr[0], vr[1], vr[2], vr[3]);
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            // past the sequence (stale pool bytes): zero, since P is 0 there
+            const uint32_t b0 = e4m3_lo(vr[t4]) & m0, b1 = e4m3_hi(vr[t4]) & m1;
+            mma_f16_16816(o[4 * dq + t4], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_f16_16816(o[4 * dq + t4], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          }
+        }
+      } else {
       split_pack(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
       split_pack(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
       split_pack(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
@@ -245,6 +299,7 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
         mma_bf16_16816(o[2 * dp + 1], ph[0], ph[1], ph[2], ph[3], b0b, b1b);
         mma_bf16_16816(o[2 * dp + 1], pl[0], pl[1], pl[2], pl[3], b0b, b1b);
       }
+      }
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&empty[s]);
@@ -270,22 +325,38 @@ __global__ void __launch_bounds__((kPfWarps + 1) * 32, 2) attn_prefill_kernel(
   }
 }
 
-template <int HD, int G>
+template <int HD, int G, bool FP8>
 static cudaError_t launch_pf_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                cudaStream_t s) {
-  constexpr int smem = pf_smem<HD>();
+  constexpr int smem = pf_smem<HD, FP8>();
   static bool attr = false;
   if (!attr) {
     const cudaError_t ce =
-        cudaFuncSetAttribute(attn_prefill_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(attn_prefill_kernel<HD, G, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (ce != cudaSuccess) return ce;
     attr = true;
   }
   const Dims& dm = e->dm;
-  return launch_pdl(attn_prefill_kernel<HD, G>, dim3(b->n_pfb * dm.hkv), dim3((kPfWarps + 1) * 32), smem, s,
+  return launch_pdl(attn_prefill_kernel<HD, G, FP8>, dim3(b->n_pfb * dm.hkv), dim3((kPfWarps + 1) * 32), smem, s,
                     (const uint16_t*)p->base, (const float*)e->q, (const PfBlock*)b->pfb,
-                    (const int32_t*)b->pf_rows, (const int32_t*)b->tables,
-                    layer, p->n_blocks, dm.hkv, dm.max_blocks_per_seq, e->act_hi, e->act_lo, e->err);
+                    (const int32_t*)b->pf_rows, (const int32_t*)b->tables, layer, p->n_blocks, dm.hkv,
+                    dm.max_blocks_per_seq, e->act_hi, e->act_lo, e->err);
+}
+
+template <bool FP8>
+static cudaError_t launch_pf_kv(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
+                                cudaStream_t s) {
+  const int G = e->dm.hq / e->dm.hkv;
+  const int HD = e->dm.hd;
+  if (HD == 64 && G == 1) return launch_pf_t<64, 1, FP8>(e, p, b, layer, s);
+  if (HD == 64 && G == 2) return launch_pf_t<64, 2, FP8>(e, p, b, layer, s);
+  if (HD == 64 && G == 4) return launch_pf_t<64, 4, FP8>(e, p, b, layer, s);
+  if (HD == 64 && G == 8) return launch_pf_t<64, 8, FP8>(e, p, b, layer, s);
+  if (HD == 128 && G == 1) return launch_pf_t<128, 1, FP8>(e, p, b, layer, s);
+  if (HD == 128 && G == 2) return launch_pf_t<128, 2, FP8>(e, p, b, layer, s);
+  if (HD == 128 && G == 4) return launch_pf_t<128, 4, FP8>(e, p, b, layer, s);
+  if (HD == 128 && G == 8) return launch_pf_t<128, 8, FP8>(e, p, b, layer, s);
+  return cudaErrorInvalidValue;
 }
 
 int prefill_block_positions(int G) { return kPfQRows / G; }
@@ -293,17 +364,7 @@ int prefill_block_positions(int G) { return kPfQRows / G; }
 cudaError_t launch_attn_prefill(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                 cudaStream_t s) {
   if (b->n_pfb <= 0) return cudaSuccess;
-  const int G = e->dm.hq / e->dm.hkv;
-  const int HD = e->dm.hd;
-  if (HD == 64 && G == 1) return launch_pf_t<64, 1>(e, p, b, layer, s);
-  if (HD == 64 && G == 2) return launch_pf_t<64, 2>(e, p, b, layer, s);
-  if (HD == 64 && G == 4) return launch_pf_t<64, 4>(e, p, b, layer, s);
-  if (HD == 64 && G == 8) return launch_pf_t<64, 8>(e, p, b, layer, s);
-  if (HD == 128 && G == 1) return launch_pf_t<128, 1>(e, p, b, layer, s);
-  if (HD == 128 && G == 2) return launch_pf_t<128, 2>(e, p, b, layer, s);
-  if (HD == 128 && G == 4) return launch_pf_t<128, 4>(e, p, b, layer, s);
-  if (HD == 128 && G == 8) return launch_pf_t<128, 8>(e, p, b, layer, s);
-  return cudaErrorInvalidValue;
+  return e->kv_fp8 ? launch_pf_kv<true>(e, p, b, layer, s) : launch_pf_kv<false>(e, p, b, layer, s);
 }
 
 }  // namespace cbd

@@ -143,10 +143,10 @@ cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int32_t gemv_ma
  * positions, wherever they sit in the step's row array: a prompt chunk,
  * "20.3 服务、批处理与流式" section 20.3.2) on a kernel that takes blocks of
  * consecutive query positions and streams each K/V block once per block of
- * queries, instead of once per row.  Applies to attention path 0 with bf16
- * K/V; the other rows keep the streaming kernel.  Same arithmetic (q and P
- * split into bf16 hi + lo), summed in another order.  enable != 0: on (the
- * default). */
+ * queries, instead of once per row.  Applies to attention path 0, bf16 or
+ * FP8 K/V; the other rows keep the streaming kernel.  Same arithmetic (q and
+ * P split into hi + lo halves: bf16, or f16 over E4M3 K/V), summed in
+ * another order.  enable != 0: on (the default). */
 cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
 
 /* On the tcgen05 path, steps of at least min_rows rows (prefill chunks,

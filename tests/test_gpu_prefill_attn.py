@@ -1,6 +1,7 @@
 """GPU parity of the prefill attention kernel ("20.3 服务、批处理与流式"
 section 20.3.2: a prompt chunk's rows are consecutive positions of one
-sequence, so a block of them shares each K/V block it reads).
+sequence, so a block of them shares each K/V block it reads), over bf16 and
+FP8 (E4M3) K/V.
 
 Prefill runs (16+ rows of one slot at consecutive positions, in any row
 order) take the kernel; other rows keep the streaming kernel.  The kernel computes the
@@ -68,11 +69,12 @@ def run_case(m, seed, with_kernel, reverse=False):
     return got, z, rows, priors
 
 
+@pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16_kv", "e4m3_kv"])
 @pytest.mark.parametrize("shape", ["tiny", "hd128"])
-def test_prefill_kernel_matches_oracle(shape):
+def test_prefill_kernel_matches_oracle(shape, kv_fp8):
     from continuous_batching_decode_gb300 import build
     build.build()
-    m = gu.Model(shape, max_rows=256, max_slots=8, mbps=16)
+    m = gu.Model(shape, max_rows=256, max_slots=8, mbps=16, kv_fp8=kv_fp8)
     try:
         res = {}
         for on in (True, False):
@@ -90,7 +92,8 @@ def test_prefill_kernel_matches_oracle(shape):
             om.prefill(om_, kv, s, pr)
         z = om.step(om_, kv, [(r[0], r[1], r[2], r[4]) for r in rows])
         for on, (got, zg, _, _) in res.items():
-            gu.assert_logits_close(zg, z, f"{shape} prefill runs, prefill kernel {'on' if on else 'off'}")
+            gu.assert_logits_close(zg, z, f"{shape} ({'e4m3' if kv_fp8 else 'bf16'} KV) prefill runs, "
+                                          f"prefill kernel {'on' if on else 'off'}")
             for j in range(len(z)):
                 if not gu.greedy_near_tie(z[j]):
                     assert got[j] == int(np.argmax(z[j])), f"kernel {on}: row {j}"
