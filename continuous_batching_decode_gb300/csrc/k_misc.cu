@@ -60,59 +60,89 @@ cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, const float* g
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.
-// One CTA per output row, one float4 per thread and pass; `gather`
-// (optional) picks the source row.  The sum of squares is reduced in a fixed
-// order (per-thread sums, then a fixed tree), so a row's result does not
-// depend on the other rows.
+// Four warps per output row (32 when there are fewer rows than SMs), one
+// or two rows per CTA (two when there are rows enough to fill the GPU twice
+// over); `gather`
+// (optional) picks the source row.  Each thread sums the squares of its
+// float4s (i = t, t + threads per row, ...) in order, the warps reduce by a fixed
+// shuffle tree and the four warp sums are added in warp order, so a row's
+// result does not depend on the other rows.  The thread keeps its first 8
+// float4s in registers for the second pass (all of a row of d <= 4096; the
+// rest, if any, is read again).  (One 1024-thread CTA per
+// row spent most of its time in barriers -- 0.68 ms per 544-row step; one
+// warp per row left most SMs idle at 544 rows.)
+constexpr int kNormWarpsPerRow = 4;
+constexpr int kNormMaxWarpsPerRow = 32;
+constexpr int kNormRowsPerCta = 2;
+constexpr int kNormMaxV = 8;                 // float4s a thread keeps in registers
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ g,
-                               const int32_t* __restrict__ gather, int d, float eps,
+                               const int32_t* __restrict__ gather, int n_rows, int d, float eps, int tpr,
                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
-  __shared__ float red[32];
+  __shared__ float red[kNormRowsPerCta * kNormMaxWarpsPerRow];
   TR_DECL;
   pdl_trigger();
   pdl_wait();
   TR_MARK1;
-  const int r = blockIdx.x;
-  const int src = gather ? gather[r] : r;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
+  const int TPR = tpr;                                 // threads per row
+  const int rr = threadIdx.x / TPR, t = threadIdx.x % TPR, wpr = TPR >> 5;
+  const int r = blockIdx.x * (blockDim.x / TPR) + rr;
+  const bool live = r < n_rows;
   const int n4 = d >> 2;
+  float4 v[kNormMaxV];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    const float4 v = xr[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  const float4* xr = nullptr;
+  if (live) {
+    const int src = gather ? gather[r] : r;
+    xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
+#pragma unroll
+    for (int j = 0; j < kNormMaxV; ++j) {
+      const int i = t + j * TPR;
+      v[j] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kNormMaxV; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    for (int i = t + kNormMaxV * TPR; i < n4; i += TPR) {
+      const float4 u = xr[i];
+      ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
+    }
   }
   ss = warp_sum(ss);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) red[w] = ss;
+  if ((t & 31) == 0) red[rr * wpr + (t >> 5)] = ss;
   __syncthreads();
-  if (w == 0) {
-    float t = l < (int)(blockDim.x >> 5) ? red[l] : 0.f;
-    t = warp_sum(t);
-    if (l == 0) red[0] = t;
-  }
-  __syncthreads();
-  const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
+  if (!live) return;
+  float tot = 0.f;
+  for (int w = 0; w < wpr; ++w) tot += red[rr * wpr + w];
+  const float inv = 1.0f / sqrtf(tot / (float)d + eps);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   uint2* h2 = reinterpret_cast<uint2*>(hi + (size_t)r * d);
   uint2* l2 = reinterpret_cast<uint2*>(lo + (size_t)r * d);
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    const float4 v = xr[i], gg = g4[i];
+  auto put = [&](int i, const float4 u) {
+    const float4 gg = g4[i];
     uint16_t h[4], q[4];
-    split_bf16(v.x * inv * gg.x, h[0], q[0]);
-    split_bf16(v.y * inv * gg.y, h[1], q[1]);
-    split_bf16(v.z * inv * gg.z, h[2], q[2]);
-    split_bf16(v.w * inv * gg.w, h[3], q[3]);
+    split_bf16(u.x * inv * gg.x, h[0], q[0]);
+    split_bf16(u.y * inv * gg.y, h[1], q[1]);
+    split_bf16(u.z * inv * gg.z, h[2], q[2]);
+    split_bf16(u.w * inv * gg.w, h[3], q[3]);
     h2[i] = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
     l2[i] = make_uint2(q[0] | ((uint32_t)q[1] << 16), q[2] | ((uint32_t)q[3] << 16));
-  }
+  };
+#pragma unroll
+  for (int j = 0; j < kNormMaxV; ++j)
+    if (t + j * TPR < n4) put(t + j * TPR, v[j]);
+  for (int i = t + kNormMaxV * TPR; i < n4; i += TPR) put(i, xr[i]);
   TR_END(2);
 }
 
 cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, int n_rows,
                            const int32_t* gather, uint16_t* hi, uint16_t* lo, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
-  const int threads = std::min(1024, e->dm.d / 4);
-  return launch_pdl(rmsnorm_kernel, dim3(n_rows), dim3(threads), 0, s, x, g, gather, e->dm.d, e->dm.eps, hi, lo);
+  if (e->dm.d % 4) return cudaErrorInvalidValue;
+  const int rpc = n_rows >= 2 * e->sm_count * kNormRowsPerCta ? kNormRowsPerCta : 1;
+  const int tpr = 32 * (n_rows < e->sm_count ? std::min(kNormMaxWarpsPerRow, std::max(1, e->dm.d / 128))
+                                             : kNormWarpsPerRow);
+  const int ctas = (n_rows + rpc - 1) / rpc;
+  return launch_pdl(rmsnorm_kernel, dim3(ctas), dim3(tpr * rpc), 0, s, x, g, gather, n_rows, e->dm.d, e->dm.eps, tpr,
+                    hi, lo);
 }
 
 }  // namespace cbd
