@@ -10,10 +10,13 @@
 //   * M = 64 query rows (BQ = 64 / G positions x the G query heads of the
 //     KV head), 16 per consumer warp, on mma.sync m16n8k16;
 //   * S = q K^T over a 32-position block (q split into bf16 hi + lo, scaled
-//     to log2 units), causal mask (key position <= query position), online
-//     softmax in exp2, then O += P V with P split into bf16 hi + lo -- the
-//     streaming kernel's arithmetic, summed in another order (one pass over
-//     the row's blocks instead of 128-position chunks merged afterwards);
+//     to log2 units; f16 hi + lo over E4M3 K/V), causal mask (key position
+//     <= query position), online softmax in exp2, then O += P V with P split
+//     the same way -- the streaming kernel's arithmetic, summed in another
+//     order (one pass over the row's blocks instead of 128-position chunks
+//     merged afterwards);
+//   * each consumer warp keeps its 16 rows of q in shared memory and reads
+//     them back as ldmatrix A fragments (registers hold the output);
 //   * one producer warp copies each block's K and V tiles (one contiguous
 //     run in the pool) into a ring of stages; the consumer warps release a
 //     stage once all four have used it.
