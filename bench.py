@@ -678,7 +678,8 @@ def run_trace(args):
     s = shape_of(args)
     slots, rows, mbps = 64, 2048, 64
     w = synth.make_weights(s, seed=args.seed, device="cuda")
-    e = cbd.engine_create(cbd.make_config(s, max_rows=rows, max_slots=slots, max_blocks_per_seq=mbps), w)
+    fp8 = args.kv == "fp8"
+    e = cbd.engine_create(cbd.make_config(s, max_rows=rows, max_slots=slots, max_blocks_per_seq=mbps, kv_fp8=fp8), w)
     del w
     torch.cuda.empty_cache()
     reqs = synth.request_trace(args.trace_requests, s["vocab"], seed=args.seed,
@@ -707,7 +708,7 @@ def run_trace(args):
                     host_sched_us_per_step=round(res["sched_us_per_step"], 1),
                     config=dict(workload="7b-shaped continuous-batching trace", slots=slots, max_rows=rows,
                                 chunk=512, answer_budget=128, pool_blocks=args.trace_blocks,
-                                rate=args.trace_rate or "all at t=0"),
+                                rate=args.trace_rate or "all at t=0", kv="e4m3" if fp8 else "bf16"),
                     data="synthetic (seeded random-init weights, random prompt ids)")
         print(json.dumps(line), flush=True)
 
