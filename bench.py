@@ -74,7 +74,7 @@ def parse():
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
-    ap.add_argument("--rows-gemm", type=int, default=384,
+    ap.add_argument("--rows-gemm", type=int, default=512,
                     help="steps of at least this many rows may run the 128-row-tile GEMM (0 = never)")
     ap.add_argument("--rows-gemm-force", action="store_true",
                     help="... on every GEMM of such a step (default: where it fills the GPU well)")

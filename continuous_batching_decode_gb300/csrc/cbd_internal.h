@@ -191,7 +191,7 @@ struct cbd_engine {
   size_t l2_prefetch = 0;             // bytes of the next GEMM's weights each kernel prefetches to L2 (off)
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   int gemv_max_rows = 0;              // auto: GEMV up to this many rows
-  int rows_gemm_min = 384;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
+  int rows_gemm_min = 512;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
   bool rows_gemm_force = false;       // ... for every GEMM of such a step, however it fills the GPU
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   bool prefill_attn = true;           // path 0, bf16 K/V: prefill runs on the prefill attention kernel

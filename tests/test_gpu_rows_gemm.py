@@ -70,7 +70,7 @@ def test_rows_gemm_matches_oracle(tiny_tc, n_prompt):
         K, V = pool.gather(tables, 4, n_prompt)
         res[rows_min] = (got, z, K[0], V[0])
         pool.close()
-    cbd.engine_set_rows_gemm(m.e, 384, force=False)
+    cbd.engine_set_rows_gemm(m.e, 512, force=False)
     cbd.engine_set_fused_norm(m.e, True)
     om_ = m.oracle()
     kv = {s: om.SequenceKV(om_.cfg, 512) for s in range(5)}
@@ -105,7 +105,7 @@ def test_rows_gemm_is_deterministic(tiny_tc):
         K, V = pool.gather(tables, 4, 300)
         outs.append((got, z, K, V))
         pool.close()
-    cbd.engine_set_rows_gemm(m.e, 384, force=False)
+    cbd.engine_set_rows_gemm(m.e, 512, force=False)
     for a, b in zip(*outs):
         np.testing.assert_array_equal(a, b)
 
@@ -113,7 +113,7 @@ def test_rows_gemm_is_deterministic(tiny_tc):
 def test_rows_gemm_setting_is_validated(tiny_tc):
     with pytest.raises(cbd.CbdError):
         cbd.engine_set_rows_gemm(tiny_tc.e, -1)
-    cbd.engine_set_rows_gemm(tiny_tc.e, 384)
+    cbd.engine_set_rows_gemm(tiny_tc.e, 512)
 
 
 @pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16_kv", "e4m3_kv"])
@@ -181,14 +181,14 @@ def test_rows_gemm_7b_shape_two_layers():
         rows += [(32, t, i, 1, 1 if i == 511 else 0) for i, t in enumerate(prompt)]
         samp = [dict(GREEDY, request_id=s) for s in range(33)]
         res = {}
-        for name, (rows_min, force) in {"auto": (384, False), "forced": (1, True), "off": (0, False)}.items():
+        for name, (rows_min, force) in {"auto": (512, False), "forced": (1, True), "off": (0, False)}.items():
             cbd.engine_set_rows_gemm(m.e, rows_min, force=force)
             pool = m.pool(n_pool)
             for s, pr in enumerate(priors):
                 gu.gpu_prefill(m, pool, s, pr, tables, nbps, chunk=64)
             res[name] = gu.run_step(m, pool, rows, tables, nbps, samp)
             pool.close()
-        cbd.engine_set_rows_gemm(m.e, 384)
+        cbd.engine_set_rows_gemm(m.e, 512)
         om_ = m.oracle(cache=False)
         kv = {s: om.SequenceKV(om_.cfg, 544) for s in range(33)}
         for s, pr in enumerate(priors):
