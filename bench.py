@@ -24,8 +24,17 @@ e2e    = the same through cbd_step with host arrays: the step's rows, block
 Multi-GPU: independent replicas (one engine per GPU, no collective on the
 data path); barrier + max-over-ranks timing.
 
---impl reference times the CPU oracle on a bounded sample of the same
-workload (no GPU).
+sweep  = the same step at every B in --sweep (default 1, 2, 4, 8, 16, 64,
+         128; contexts U[256, 4096], one pool sized for the largest B, each B
+         the first B rows), tok/s and the roofline fraction per B.
+cpu_baseline = one whole step of the CPU oracle (every layer, every row, the
+         LM head) on this workload's shapes, timed once.
+
+--impl reference times the CPU oracle (no GPU): every step is one whole
+oracle step of the same workload.
+
+--gpus N without a torchrun environment re-launches this script under
+torch.distributed.run with N ranks (one engine per GPU).
 
 --trace serves a continuous-batching request trace instead (7B shape, 64
 slots, Poisson arrivals, prompts from {20, 50, 200, 1000}, outputs
@@ -69,7 +78,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override layer count (profiling cases only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--sweep", default="", help="comma-separated B values: extra lines on stderr")
+    ap.add_argument("--sweep", default="1,2,4,8,16,64,128",
+                    help="comma-separated B values timed after the headline step ('' = none)")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
@@ -247,87 +257,83 @@ def measured_traffic(cls, args):
     return val if val is not None and sha == cur.hexdigest() else None
 
 
-def oracle_sample(s, B, ctx, toks, kv_source, weights_l0, seed, min_s=0.0):
-    """Time the CPU oracle on one layer of the step (all B rows) plus the LM
-    head; returns (seconds for a full step, details)."""
+def host_mem_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) / 2**20
+    except OSError:
+        pass
+    return 0.0
+
+
+def oracle_kv(s, ctx, seed):
+    """KV state of the oracle for the timed step: random bf16 values (the
+    device pool holds random bf16 too), one [c+2, H_kv, hd] array per row and
+    per K / V, shared by every layer -- each layer reads and writes the same
+    shapes as with distinct arrays, and the host holds 1/L of the bytes."""
     from oracle import model as om
-    cfg1 = om.ModelConfig(**dict(s, n_layers=1))
-    m1 = om.OracleModel(cfg1, weights_l0)
+    cfg = om.ModelConfig(**s)
+    rng = np.random.default_rng(seed)
     kv = {}
     for i, c in enumerate(ctx):
-        q = om.SequenceKV(cfg1, c + 2)
-        K, V = kv_source(i, c)
-        q.K[0][:c] = K
-        q.V[0][:c] = V
+        q = om.SequenceKV(om.ModelConfig(**dict(s, n_layers=1)), c + 2)
+        shp = (c + 2, s["n_kv_heads"], s["head_dim"])
+        K = om.round_to_bf16(rng.standard_normal(shp, dtype=np.float32).astype(np.float64) * 1.3)
+        V = om.round_to_bf16(rng.standard_normal(shp, dtype=np.float32).astype(np.float64) * 1.3)
+        q.K = [K] * cfg.n_layers
+        q.V = [V] * cfg.n_layers
         q.length = c
         kv[i] = q
-    rows = [(i, toks[i], ctx[i], 1) for i in range(B)]
-    m1.layer(0)
-    if not callable(weights_l0):
-        m1._get("embed")
-    m1._get("final_norm")
-    m1._get("lm_head")
-    # repeat the (idempotent) one-layer step until about min_s seconds of CPU
-    # work have been timed; report the mean
-    reps, t_step = 0, 0.0
-    while True:
-        ta = time.perf_counter()
-        om.step(m1, kv, rows)
-        t_step += time.perf_counter() - ta
-        reps += 1
-        if t_step >= min_s or reps >= 64:
-            break
-    t0, t1 = 0.0, t_step / reps
-    x = np.random.default_rng(seed).normal(size=(B, s["d_model"]))
-    t2 = time.perf_counter()
-    om.rmsnorm(x, m1._get("final_norm"), cfg1.rms_eps) @ m1._get("lm_head").T
-    t3 = time.perf_counter()
-    t_layer = (t1 - t0) - (t3 - t2)
-    full = s["n_layers"] * t_layer + (t3 - t2)
-    return full, dict(layer_s=t_layer, head_s=t3 - t2, sample_s=t_step + (t3 - t2), reps=reps)
+    return kv
 
 
-def cpu_weights_l0(s, seed):
-    """Layer-0 weights, embedding rows and LM head on the host (bf16 bits)."""
-    import torch
+def oracle_model(s, weights, cache):
+    from oracle import model as om
+    return om.OracleModel(om.ModelConfig(**s), weights, cache=cache)
+
+
+def oracle_step_seconds(model, kv, rows):
+    """Wall time of one whole oracle step (all layers, all rows, LM head)."""
+    from oracle import model as om
+    t0 = time.perf_counter()
+    om.step(model, kv, rows)
+    return time.perf_counter() - t0
+
+
+def host_weight_bits(s, seed):
+    """The workload's weights generated on the host (the same seeded draw the
+    device weights come from), as bf16 bit arrays."""
     from continuous_batching_decode_gb300 import synth
-    g = torch.Generator().manual_seed(seed)
-    out = {}
-    for name, shape in synth.weight_shapes(s).items():
-        if not (name.startswith("0.") or name in ("embed", "final_norm", "lm_head")):
-            continue
-        if name.endswith("norm"):
-            t = torch.ones(shape, dtype=torch.bfloat16)
-        else:
-            t = (torch.randn(shape, generator=g) * 0.02).to(torch.bfloat16)
-        out[name] = synth.bf16_bits(t)
-    return out
+    w = synth.make_weights(s, seed=seed, device="cpu")
+    return {k: synth.bf16_bits(v) for k, v in w.items()}
 
 
 def run_reference(args):
-    """CPU oracle arm: each step times one bounded sample of the workload."""
+    """CPU oracle arm: every step is one whole oracle step of the workload
+    (all layers, all B rows, the LM head), on the host cores."""
     s = shape_of(args)
     B = args.B
     wl = workload(s, B, args.ctx_lo, args.ctx_hi, args.seed)
-    w0 = cpu_weights_l0(s, args.seed)
-    rng = np.random.default_rng(args.seed + 2)
-
-    def kv_source(i, c):
-        shp = (c, s["n_kv_heads"], s["head_dim"])
-        from oracle.model import round_to_bf16
-        return round_to_bf16(rng.normal(0, 1.3, shp)), round_to_bf16(rng.normal(0, 1.3, shp))
-
-    toks = [r[1] for r in wl["rows"]]
+    bits = host_weight_bits(s, args.seed)
+    # fp64 copies of every layer stay cached across steps when the host has
+    # room for them (~8 bytes per parameter), else each step upcasts per layer
+    cache = host_mem_available_gb() > 1.5 * 8 * sum(v.size for v in bits.values()) / 2**30
+    model = oracle_model(s, bits, cache)
+    kv = oracle_kv(s, wl["ctx"], args.seed + 2)
+    rows = [(r[0], r[1], r[2], 1) for r in wl["rows"]]
     ts = []
     for i in range(args.warmup + args.steps):
-        full, det = oracle_sample(s, B, wl["ctx"], toks, kv_source, w0, args.seed)
+        t = oracle_step_seconds(model, kv, rows)
         if i >= args.warmup:
-            ts.append(full)
-    t = statistics.median(ts)
+            ts.append(t)
+    t = sum(ts) / len(ts)
     value = B / t
     cores = len(os.sched_getaffinity(0))
-    sample = (f"one of {s['n_layers']} layers for all {B} rows plus the LM head, per step; "
-              f"full step = {s['n_layers']} x layer + head")
+    sample = (f"whole steps: {s['n_layers']} layers for all {B} rows plus the LM head, each timed; fp64 weights "
+              f"{'cached after the first warm-up step' if cache else 'upcast per layer every step'}; KV random bf16 "
+              "per row, shared by the layers")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1000, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -366,23 +372,33 @@ def run_cbd(args):
     w = synth.make_weights(s, seed=args.seed, device="cuda")
     fp8 = args.kv == "fp8"
     eb = 1 if fp8 else 2
-    cfg = cbd.make_config(s, max_rows=max(B, 64), max_slots=max(B, 8), max_blocks_per_seq=wl["mbps"], kv_fp8=fp8)
+    sweep = [int(x) for x in args.sweep.split(",") if x.strip()]
+    b_cap = max([B] + sweep)
+    cfg = cbd.make_config(s, max_rows=max(b_cap, 64), max_slots=max(b_cap, 8), max_blocks_per_seq=wl["mbps"],
+                          kv_fp8=fp8)
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
     cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
     cbd.engine_set_attention_path(e, args.attn_path)
     cbd.engine_set_l2_prefetch(e, args.l2_prefetch_mb << 20)
-    if not (rank == 0 and world == 1 and not args.no_cpu_baseline):
-        del w
+    host_bits = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host_bits = {k: synth.bf16_bits(v) for k, v in w.items()}
+    del w
     torch.cuda.empty_cache()
-    pool = cbd.kv_pool_create(e, wl["n_pool"])
-    base, nbytes, nb = cbd.kv_pool_data(pool)
-    # [L][n_blocks][H_kv][K|V][32 * hd]: each tile in 128-byte-swizzled order
-    kv = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]), "u8" if fp8 else "bf16")
-    gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
-    for l in range(s["n_layers"]):
-        r = torch.randn(kv[l].shape, generator=gen, device="cuda") * 1.3
-        kv[l].copy_(r.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else r.to(torch.bfloat16))
+
+    def make_pool(n_pool):
+        p = cbd.kv_pool_create(e, n_pool)
+        base, nbytes, nb = cbd.kv_pool_data(p)
+        # [L][n_blocks][H_kv][K|V][32 * hd]: each tile in 128-byte-swizzled order
+        view = cbd.device_view(base, (s["n_layers"], nb, s["n_kv_heads"], 2, 32 * s["head_dim"]),
+                               "u8" if fp8 else "bf16")
+        gen = torch.Generator(device="cuda").manual_seed(args.seed + 3)
+        for l in range(s["n_layers"]):
+            r = torch.randn(view[l].shape, generator=gen, device="cuda") * 1.3
+            view[l].copy_(r.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else r.to(torch.bfloat16))
+        return p
+    pool = make_pool(wl["n_pool"])
     stream = torch.cuda.current_stream()
     b = cbd.batch_create(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"])
     out = torch.zeros(B, dtype=torch.int32, device="cuda")
@@ -498,38 +514,51 @@ def run_cbd(args):
                "launch_by_launch_ms_per_step": round(lbl_ms, 4)}
         cbd.engine_check(e)
 
+    cbd.batch_destroy(b)
+    cbd.kv_pool_destroy(pool)
+
+    # B sweep ("20.3 服务、批处理与流式" section 20.3.2: throughput grows with B
+    # while the weight stream is shared): one pool for the largest B, each B
+    # the first B rows of that draw, every step replayed as a graph
+    sweep_out = {}
+    if sweep:
+        wls = workload(s, b_cap, args.ctx_lo, args.ctx_hi, args.seed)
+        pool = make_pool(wls["n_pool"])
+        outs = torch.zeros(b_cap, dtype=torch.int32, device="cuda")
+        for Bs in sorted(set(sweep + [B])):
+            b2 = cbd.batch_create(e, pool, wls["rows"][:Bs], wls["tables"], wls["nbps"], wls["samp"][:Bs])
+            cbd.batch_set_graph(b2, True)
+            for _ in range(args.warmup):
+                cbd.batch_run(e, pool, b2, outs)
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                cbd.batch_run(e, pool, b2, outs)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            ms2 = replicas.max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, "cuda")
+            by = W + sum(c + 1 for c in wls["ctx"][:Bs]) * kv_pos_bytes(s, eb)
+            sweep_out[str(Bs)] = {"ms_per_step": round(ms2, 4), "tok_s": round(Bs * world / ms2 * 1000, 1),
+                                  "mean_ctx": round(float(np.mean(wls["ctx"][:Bs])), 1),
+                                  "GBs": round(by / ms2 / 1e6, 1), "frac_of_measured": round(by / ms2 / 1e6 / peak, 4),
+                                  "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}
+            cbd.batch_destroy(b2)
+        cbd.engine_check(e)
+        cbd.kv_pool_destroy(pool)
+
+    # the CPU oracle, one whole step of this workload on the host cores
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        wbits = {k: synth.bf16_bits(v) for k, v in w.items() if k.startswith("0.") or k in ("final_norm", "lm_head")}
-        wbits["embed"] = None
-        del wbits["embed"]
-        E = w["embed"]
-
-        def src(name, *a):
-            if name == "embed_rows":
-                return synth.bf16_bits(E[torch.as_tensor(a[0], device="cuda")])
-            return wbits[name]
-
-        hd = s["head_dim"]
-        rr, dd = np.arange(32)[:, None], np.arange(hd)[None, :]
-        tidx = torch.as_tensor(((dd // 64) * 2048 + rr * 64 + ((((dd % 64) // 8) ^ (rr % 8)) * 8) + dd % 8).reshape(-1),
-                               device="cuda")
-
-        def kv_source(i, c):
-            nbk = (c + 31) // 32
-            ids = torch.as_tensor(wl["tables"][i][:nbk].astype(np.int64), device="cuda")
-            t = kv[0, ids][..., tidx].reshape(nbk, s["n_kv_heads"], 2, 32, hd)      # unswizzled
-            t = t.permute(2, 0, 3, 1, 4).reshape(2, nbk * 32, s["n_kv_heads"], hd)[:, :c]
-            t = t.float().cpu().numpy().astype(np.float64)
-            return t[0], t[1]
-        toks = [r[1] for r in wl["rows"]]
-        full, det = oracle_sample(s, B, wl["ctx"], toks, kv_source, src, args.seed, min_s=10.0)
-        cpu = {"value": round(B / full, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": (f"layer 0 of {s['n_layers']} for all {B} rows, timed {det['reps']} times "
-                          f"({det['sample_s']:.1f} s of CPU work in all; mean {det['layer_s']:.2f} s) plus the LM "
-                          f"head ({det['head_s']:.2f} s); full step = {s['n_layers']} x layer + head"),
-               "step_s": round(full, 2)}
-        del w
+    if host_bits is not None:
+        model = oracle_model(s, host_bits, cache=False)
+        okv = oracle_kv(s, wl["ctx"], args.seed + 2)
+        t_step = oracle_step_seconds(model, okv, [(r[0], r[1], r[2], 1) for r in wl["rows"]])
+        del okv, model, host_bits
+        cpu = {"value": round(B / t_step, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle", "step_s": round(t_step, 2),
+               "sample": (f"one whole step timed: {s['n_layers']} layers for all {B} rows plus the LM head, fp64 "
+                          "weights upcast per layer; KV random bf16 per row, shared by the layers")}
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -537,31 +566,9 @@ def run_cbd(args):
             "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path,
                            l2_prefetch_mb=args.l2_prefetch_mb),
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "graph": graph}
+            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "graph": graph, "sweep": sweep_out}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for Bs in [int(x) for x in args.sweep.split(",") if x.strip()]:
-        wl2 = workload(s, Bs, args.ctx_lo, args.ctx_hi, args.seed)
-        if wl2["n_pool"] > wl["n_pool"] or Bs > max(B, 8):
-            print(f"sweep B={Bs}: skipped (pool/slots sized for B={B})", file=sys.stderr)
-            continue
-        b2 = cbd.batch_create(e, pool, wl2["rows"], wl2["tables"], wl2["nbps"], wl2["samp"])
-        for _ in range(args.warmup):
-            cbd.batch_run(e, pool, b2, out)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            cbd.batch_run(e, pool, b2, out)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        ms2 = ev0.elapsed_time(ev1) / args.steps
-        by = W + sum(c + 1 for c in wl2["ctx"]) * kv_pos_bytes(s, eb)
-        print(json.dumps({"sweep_B": Bs, "ms_per_step": round(ms2, 4), "tok_s": round(Bs / ms2 * 1000, 1),
-                          "GBs": round(by / ms2 / 1e6, 1), "frac_of_measured": round(by / ms2 / 1e6 / peak, 4),
-                          "frac_of_8TBs": round(by / ms2 / 1e6 / 8000, 4)}),
-              file=sys.stderr, flush=True)
-        cbd.batch_destroy(b2)
-    cbd.batch_destroy(b)
-    cbd.kv_pool_destroy(pool)
     cbd.engine_destroy(e)
     if dist:
         dist.destroy_process_group()
@@ -713,8 +720,24 @@ def run_trace(args):
         print(json.dumps(line), flush=True)
 
 
+def spawn_ranks(n):
+    """Re-run this command under torch.distributed.run with n ranks on this
+    node (127.0.0.1 rendezvous); returns its exit status."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not (args.trace or args.mixed):
+        sys.exit(spawn_ranks(args.gpus))
+    if "WORLD_SIZE" in os.environ:
+        print(f"bench rank {os.environ.get('RANK', '0')} of {os.environ['WORLD_SIZE']}", file=sys.stderr, flush=True)
     if args.trace:
         run_trace(args)
         return

@@ -128,6 +128,8 @@ PROTOS = {
     "cbd_batch_captures": (c_i32, [c_vp, _P(c_i32)]),
     "cbd_sample": (c_i32, [c_vp, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
     "cbd_sample_static": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
+    "cbd_sample_static_check": (c_i32, [c_vp]),
+    "cbd_engine_test_wait_timeout": (c_i32, [c_vp, ctypes.c_int64, c_vp]),
     "cbd_sched_create": (c_i32, [_P(SchedConfig), _P(c_vp)]),
     "cbd_sched_destroy": (c_i32, [c_vp]),
     "cbd_sched_submit": (c_i32, [c_vp, _P(Request)]),
@@ -223,6 +225,10 @@ def engine_set_forbidden(e, ids) -> None:
 
 def engine_check(e) -> None:
     _check(lib().cbd_engine_check(e))
+
+
+def engine_test_wait_timeout(e, limit_cycles: int, stream=None) -> None:
+    _check(lib().cbd_engine_test_wait_timeout(e, int(limit_cycles), _stream(stream)))
 
 
 def engine_counters(e) -> int:
@@ -408,6 +414,12 @@ def sample_static(logits, counters, slots, sampling, uniforms, out_tokens, strea
     ua, uap = _f32(uniforms)
     _check(lib().cbd_sample_static(_ptr(logits), len(sl), int(logits.shape[1]), _ptr(counters),
                                    int(counters.shape[0]), slp, sa, uap, _ptr(out_tokens), _stream(stream)))
+
+
+def sample_static_check(stream=None) -> None:
+    """Raise CbdError (EDEVICE) if a cbd_sample_static call since the last
+    check found no token for a row; clears the error word."""
+    _check(lib().cbd_sample_static_check(_stream(stream)))
 
 
 # ------------------------------------------------------------------ scheduler

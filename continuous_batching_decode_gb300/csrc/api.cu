@@ -30,6 +30,12 @@ static cbd_status cuda_fail(cudaError_t err, const char* what) {
   return fail(err == cudaErrorMemoryAllocation ? CBD_ENOMEM : CBD_ECUDA, "%s: %s", what, cudaGetErrorString(err));
 }
 
+// Entry points that enqueue work, synchronise or allocate for an engine run
+// on the engine's device, whichever device is current in the calling thread.
+#define CBD_ON_DEVICE(dev_)                                                   \
+  DeviceGuard _dg(dev_);                                                      \
+  if (!_dg.ok()) return fail(CBD_ECUDA, "cannot make device %d current", (int)(dev_))
+
 #define CBD_CUDA(call)                                   \
   do {                                                   \
     cudaError_t _e = (call);                             \
@@ -353,12 +359,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   }
   e->step_batch = new cbd_batch();
   e->step_batch->owns_dev = false;
+  e->step_batch->device = e->device;
   *out = e.release();
   return CBD_OK;
 }
 
 extern "C" cbd_status cbd_engine_destroy(cbd_engine* e) {
   if (!e) return CBD_OK;
+  DeviceGuard dg(e->device);
   cudaDeviceSynchronize();
   for (auto& sg : e->stage) {
     if (sg.host) cudaFreeHost(sg.host);
@@ -380,6 +388,7 @@ extern "C" cbd_status cbd_engine_destroy(cbd_engine* e) {
 extern "C" cbd_status cbd_engine_check(cbd_engine* e) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   CBD_CUDA(cudaDeviceSynchronize());
   int32_t v = 0;
   CBD_CUDA(cudaMemcpy(&v, e->err, 4, cudaMemcpyDeviceToHost));
@@ -390,9 +399,20 @@ extern "C" cbd_status cbd_engine_check(cbd_engine* e) {
   return CBD_OK;
 }
 
+extern "C" cbd_status cbd_engine_test_wait_timeout(cbd_engine* e, int64_t limit_cycles, void* stream) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  if (limit_cycles < 1 || limit_cycles > ((int64_t)1 << 31))
+    return fail(CBD_EINVAL, "limit_cycles %lld not in [1, 2^31]", (long long)limit_cycles);
+  CBD_ON_DEVICE(e->device);
+  CBD_CUDA(launch_wait_probe((long long)limit_cycles, e->err, static_cast<cudaStream_t>(stream)));
+  return CBD_OK;
+}
+
 extern "C" cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   CBD_CUDA(cudaDeviceSynchronize());
   for (auto& r : e->prof_recs) { e->prof_free.push_back(r.a); e->prof_free.push_back(r.b); }
   e->prof_recs.clear();
@@ -403,6 +423,7 @@ extern "C" cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable) {
 extern "C" cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* out, int32_t cap, int32_t* n) {
   clear_error();
   if (!e || !n) return fail(CBD_EINVAL, "NULL argument");
+  CBD_ON_DEVICE(e->device);
   CBD_CUDA(cudaDeviceSynchronize());
   std::vector<double> ms(kcCount, 0.0);
   std::vector<int64_t> cnt(kcCount, 0);
@@ -477,6 +498,7 @@ extern "C" cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable) {
 extern "C" cbd_status cbd_engine_set_forbidden(cbd_engine* e, const int32_t* ids, int32_t n) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   const int64_t V = e->dm.V;
   if (n < 0 || n >= V) return fail(CBD_EINVAL, "%d forbidden ids: must be 0..vocab-1", (int)n);
   if (n > 0 && !ids) return fail(CBD_EINVAL, "ids is NULL");
@@ -517,6 +539,7 @@ extern "C" cbd_status cbd_engine_counters(cbd_engine* e, float** counters) {
 extern "C" cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   if (slot < 0 || slot >= e->dm.max_slots) return fail(CBD_EINVAL, "slot %d out of range", slot);
   CBD_CUDA(cudaMemsetAsync(e->counters + (size_t)slot * e->dm.V, 0, (size_t)e->dm.V * 4,
                            static_cast<cudaStream_t>(stream)));
@@ -527,11 +550,13 @@ extern "C" cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream) 
 extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv_pool** out) {
   clear_error();
   if (!e || !out) return fail(CBD_EINVAL, "NULL argument");
+  CBD_ON_DEVICE(e->device);
   *out = nullptr;
   if (n_blocks < 1) return fail(CBD_EINVAL, "n_blocks must be >= 1");
   const size_t bytes = (size_t)e->dm.L * 2 * (size_t)n_blocks * e->dm.hkv * kBlock * e->dm.hd * (e->kv_fp8 ? 1 : 2);
   auto p = std::make_unique<cbd_kv_pool>();
   p->e = e;
+  p->device = e->device;
   p->n_blocks = n_blocks;
   p->bytes = bytes;
   void* b = nullptr;
@@ -551,6 +576,7 @@ extern "C" cbd_status cbd_kv_pool_create(cbd_engine* e, int32_t n_blocks, cbd_kv
 
 extern "C" cbd_status cbd_kv_pool_destroy(cbd_kv_pool* p) {
   if (!p) return CBD_OK;
+  DeviceGuard dg(p->device);
   cudaDeviceSynchronize();
   cudaFree(p->base);
   delete p;
@@ -952,6 +978,8 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
                                const cbd_sampling* sampling, const float* uniforms, int32_t* out_tokens,
                                float* out_logits, void* stream) {
   clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   BatchImage img;
   cbd_status st = build_batch_image(e, pool, rows, n_rows, block_tables, table_slots, n_blocks_per_slot, sampling,
                                     uniforms, &img);
@@ -1027,6 +1055,7 @@ extern "C" cbd_status cbd_step(cbd_engine* e, cbd_kv_pool* pool, const cbd_row* 
 extern "C" cbd_status cbd_engine_set_step_graph(cbd_engine* e, int32_t enable) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   e->step_graph = enable != 0;
   if (!e->step_graph) {
     CBD_CUDA(cudaDeviceSynchronize());
@@ -1052,11 +1081,14 @@ extern "C" cbd_status cbd_batch_create(cbd_engine* e, cbd_kv_pool* pool, const c
   clear_error();
   if (!out) return fail(CBD_EINVAL, "out is NULL");
   *out = nullptr;
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   BatchImage img;
   cbd_status st = build_batch_image(e, pool, rows, n_rows, block_tables, table_slots, n_blocks_per_slot, sampling,
                                     uniforms, &img);
   if (st) return st;
   auto b = std::make_unique<cbd_batch>();
+  b->device = e->device;
   void* dev = nullptr;
   CBD_CUDA(cudaMalloc(&dev, img.bytes.size()));
   cudaError_t ce = cudaMemcpyAsync(dev, img.bytes.data(), img.bytes.size(), cudaMemcpyHostToDevice,
@@ -1084,6 +1116,7 @@ extern "C" cbd_status cbd_batch_run(cbd_engine* e, cbd_kv_pool* pool, cbd_batch*
   clear_error();
   if (!e || !pool || !b) return fail(CBD_EINVAL, "NULL argument");
   if (pool->e != e) return fail(CBD_EINVAL, "pool belongs to another engine");
+  CBD_ON_DEVICE(e->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!b->graph_on || e->prof) return run_batch(e, pool, b, out_tokens, out_logits, s);
   if (!b->exec || b->g_epoch != e->epoch || b->g_pool != pool || b->g_tok != out_tokens || b->g_lg != out_logits) {
@@ -1133,6 +1166,7 @@ extern "C" cbd_status cbd_batch_captures(cbd_batch* b, int32_t* n) {
 
 extern "C" cbd_status cbd_batch_destroy(cbd_batch* b) {
   if (!b) return CBD_OK;
+  DeviceGuard dg(b->device);
   if (b->owns_dev && b->dev) {
     cudaDeviceSynchronize();
     cudaFree(b->dev);
@@ -1153,6 +1187,7 @@ extern "C" cbd_status cbd_sample(cbd_engine* e, const float* logits, int32_t m, 
                                  void* stream) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  CBD_ON_DEVICE(e->device);
   if (m < 1 || m > e->dm.max_slots) return fail(CBD_EINVAL, "m %d not in [1, %d]", m, e->dm.max_slots);
   if (!logits || !slots || !sampling || !out_tokens) return fail(CBD_EINVAL, "NULL argument");
   std::vector<uint8_t> seen(e->dm.max_slots, 0);

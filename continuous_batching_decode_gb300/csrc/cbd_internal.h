@@ -1,9 +1,11 @@
 // Internal declarations shared by the libcbd translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 #include <utility>
 #include <vector>
@@ -18,6 +20,63 @@ namespace cbd {
 // Thread-local message of the last failure; returns `code`.
 cbd_status fail(cbd_status code, const char* fmt, ...);
 void clear_error();
+
+// One-time set-up per CUDA device (kernel attributes, occupancy queries):
+// run(fn) calls fn(device) for the current device until it succeeds once,
+// under a mutex, so two host threads launching first at once, or engines on
+// several devices of one process, each see a finished set-up; *dev receives
+// the current device ordinal.  Later calls cost one cudaGetDevice and one
+// atomic load.
+constexpr int kMaxDevices = 64;
+class DeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& fn, int* dev = nullptr) {
+    int d = 0;
+    cudaError_t ce = cudaGetDevice(&d);
+    if (ce != cudaSuccess) return ce;
+    if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (dev) *dev = d;
+    if (done_[d].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_[d].load(std::memory_order_relaxed)) return cudaSuccess;
+    ce = fn(d);
+    if (ce == cudaSuccess) done_[d].store(true, std::memory_order_release);
+    return ce;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices] = {};
+};
+
+// Makes `dev` the calling thread's current device for the guard's lifetime
+// (entry points that enqueue work for an engine of another device than the
+// current one); ok() is false if the switch failed.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) { ok_ = false; prev_ = -1; return; }
+    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+    else prev_ = -1;
+  }
+  ~DeviceGuard() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+};
+
+// Sets a kernel's dynamic shared-memory limit once per device.
+template <class K>
+inline cudaError_t set_smem_once(DeviceOnce& once, K kernel, int bytes) {
+  return once.run([&](int) { return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+}
 
 constexpr int kBlock = 32;          // positions per KV block
 constexpr int kAttnChunk = 128;     // positions per attention split (4 blocks)
@@ -207,12 +266,14 @@ struct cbd_engine {
 
 struct cbd_kv_pool {
   cbd_engine* e = nullptr;
+  int device = 0;                     // the engine's device
   uint16_t* base = nullptr;           // bf16 elements, or E4M3 bytes when the engine's KV is FP8
   int32_t n_blocks = 0;
   size_t bytes = 0;
 };
 
 struct cbd_batch {
+  int device = 0;                     // the engine's device
   bool owns_dev = true;
   void* dev = nullptr;                // device copy of everything below
   size_t dev_bytes = 0;
@@ -354,6 +415,9 @@ cudaError_t launch_attention(const cbd_engine* e, const cbd_kv_pool* p, const cb
                              const PfSpec& pf, cudaStream_t s);
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
                            const SampDev* samp, int32_t* out_tokens, cudaStream_t s);
+// One CTA whose bounded mbarrier wait runs out after `limit` cycles and
+// records kDevWaitTimeout in `err` (k_misc.cu).
+cudaError_t launch_wait_probe(long long limit, int32_t* err, cudaStream_t s);
 #endif
 
 }  // namespace cbd

@@ -440,11 +440,10 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     }
   } else if (e->attn_path == 0) {
     constexpr int smem = attn_stream_smem<HD>();
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t ce = cudaFuncSetAttribute(attn_stream_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static DeviceOnce attr;
+    {
+      const cudaError_t ce = set_smem_once(attr, attn_stream_kernel<HD, G>, smem);
       if (ce != cudaSuccess) return ce;
-      attr = true;
     }
     // with the prefill kernel, the streaming kernel takes the items of rows
     // outside prefill runs (they come first in the list)
@@ -465,11 +464,10 @@ static cudaError_t launch_attn_t(const cbd_engine* e, const cbd_kv_pool* p, cons
     }
   } else if (e->attn_path == 2) {
     constexpr int smem = attn_mma_smem<HD>();
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t ce = cudaFuncSetAttribute(attn_mma_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static DeviceOnce attr;
+    {
+      const cudaError_t ce = set_smem_once(attr, attn_mma_kernel<HD, G>, smem);
       if (ce != cudaSuccess) return ce;
-      attr = true;
     }
     cudaError_t ce = launch_pdl(attn_mma_kernel<HD, G>, dim3(b->n_work, dm.hkv), dim3(128), smem, s,
                                 (const uint16_t*)p->base, (const float*)e->q, (const RowDev*)b->rows, (const int32_t*)b->tables,

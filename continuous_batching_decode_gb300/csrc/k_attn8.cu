@@ -17,12 +17,10 @@ static cudaError_t launch_fp8_t(const cbd_engine* e, const cbd_kv_pool* p, const
   const Dims& dm = e->dm;
   constexpr int smem = stream_smem<HD, true>();
   constexpr int NW = stream_warps<HD, true>();
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t ce =
-        cudaFuncSetAttribute(attn_stream_kernel<HD, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static DeviceOnce attr;
+  {
+    const cudaError_t ce = set_smem_once(attr, attn_stream_kernel<HD, G, true>, smem);
     if (ce != cudaSuccess) return ce;
-    attr = true;
   }
   const int n_tasks = n_items * dm.hkv;
   if (n_tasks <= 0) return cudaSuccess;

@@ -332,12 +332,10 @@ template <int HD, int G, bool FP8>
 static cudaError_t launch_pf_t(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                cudaStream_t s) {
   constexpr int smem = pf_smem<HD, FP8>();
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t ce =
-        cudaFuncSetAttribute(attn_prefill_kernel<HD, G, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static DeviceOnce attr;
+  {
+    const cudaError_t ce = set_smem_once(attr, attn_prefill_kernel<HD, G, FP8>, smem);
     if (ce != cudaSuccess) return ce;
-    attr = true;
   }
   const Dims& dm = e->dm;
   return launch_pdl(attn_prefill_kernel<HD, G, FP8>, dim3(b->n_pfb * dm.hkv), dim3((kPfWarps + 1) * 32), smem, s,

@@ -12,11 +12,10 @@
 //     -> the kind's epilogue -> global) while the MMA warp fills the other,
 //     so a unit's epilogue overlaps the next unit's mainloop;
 //   * K is not split (there are enough units), so there is no exchange;
-//   * clusters of S <= 4 CTAs take adjacent feature tiles of the same row
-//     tile; each copies 1/S of every stage's activation boxes and multicasts
-//     them to all S, so L2 serves fewer bytes per MMA (the copies, not the
-//     tensor pipe, were the limit with one CTA per unit);
-//   * weights tiled at 128 rows pair two tiles into one 256-wide unit.
+//   * every CTA copies its own activation boxes (one CTA per SM, no
+//     clusters);
+//   * weights tiled at 128 rows pair two tiles into one 256-wide unit, so
+//     each activation stage feeds N = 256.
 // Epilogues: QKV (RoPE, KV append through the block table), SwiGLU,
 // residual add and logits, four features at a time (epi_quad, shared with
 // the 64-row-tile kernel).  A step that may route a GEMM here runs the
@@ -25,7 +24,6 @@
 // 1/rms) measured no faster, the heavier residual epilogue costing what the
 // norm launches saved.
 #include <algorithm>
-#include <mutex>
 
 #include "gemm_epi.cuh"
 
@@ -40,12 +38,9 @@ constexpr int kRwEpiWarps = 8;
 constexpr int kRwThreads = 64 + 32 * kRwEpiWarps;
 constexpr int kRwMaxStages = 8;
 
-constexpr int kRwMaxCluster = 4;
-
 struct RwArgs {
   int n, KB, NRT;                                   // rows, k blocks, row tiles
-  int S;                                            // cluster size: CTAs that share each A tile
-  int units;                                        // cluster units = (T / S) * NRT
+  int units;                                        // (feature tile, row tile) units = T * NRT
   int32_t* err;
 };
 
@@ -119,27 +114,20 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  // Cluster units (feature tiles S tq .. S tq + S - 1, row tile rt) go to
-  // clusters round-robin; rank r of the cluster owns feature tile S tq + r.
-  // The S CTAs of a cluster work on the same row tile in lockstep, so each
-  // issues 1/S of every stage's activation boxes and multicasts them to all.
-  const int S = a.S;
-  const int rank = S > 1 ? (int)cluster_rank() : 0;
-  const int cl = (int)blockIdx.x / S, ncl = (int)gridDim.x / S;
-  const int nu = (a.units - cl + ncl - 1) / ncl;
+  // units (feature tile t, row tile rt), t-major, go to CTAs round-robin
+  const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
+  const int nu = (a.units - cta + ncta - 1) / ncta;
   const int KB = a.KB;
-  const uint16_t cmask = (uint16_t)((1u << S) - 1u);
   auto tile_of = [&](int i, int& t, int& rt) {
-    const int cu = cl + i * ncl;
-    const int tq = cu / a.NRT;
-    rt = cu - tq * a.NRT;
-    t = tq * S + rank;
+    const int u = cta + i * ncta;
+    t = u / a.NRT;
+    rt = u - t * a.NRT;
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
       tc::mbar_init(&full_bar[s], 1);
-      tc::mbar_init(&empty_bar[s], (uint32_t)S);     // every CTA of the cluster frees it
+      tc::mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
@@ -158,7 +146,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   if (warp == 1) tc::tmem_alloc(&tmem_base, kCols);
   tc::tc_fence_before();
   __syncthreads();
-  if (S > 1) cluster_sync_all();        // peers' barriers are initialised before any multicast
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   volatile int* abort_p = &abort_flag;
@@ -193,19 +180,9 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         const int s = (int)(g % ST);
         const int nbox = (min(kRwRows, a.n - rt * kRwRows) + 15) / 16;
         uint8_t* st = ring + (size_t)s * stage_bytes + w_bytes;
-        if (S == 1) {
-          for (int j = 0; j < nbox; ++j) {
-            tc::tma_load_2d(st + j * 2048, &tmH, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
-            tc::tma_load_2d(st + kRwABytes + j * 2048, &tmL, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
-          }
-        } else {
-          // box j of the 2 nbox (hi boxes, then lo boxes) comes from rank j % S
-          for (int j = rank; j < 2 * nbox; j += S) {
-            const bool lo = j >= nbox;
-            const int jb = lo ? j - nbox : j;
-            tc::tma_load_2d_mc(st + (lo ? kRwABytes : 0) + jb * 2048, lo ? &tmL : &tmH, q * kRwBK,
-                               rt * kRwRows + jb * 16, &full_bar[s], cmask);
-          }
+        for (int j = 0; j < nbox; ++j) {
+          tc::tma_load_2d(st + j * 2048, &tmH, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
+          tc::tma_load_2d(st + kRwABytes + j * 2048, &tmL, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
         }
       };
       // weights do not depend on the previous kernel: start them first
@@ -251,8 +228,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             tc::mma_bf16(acc, dH + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
             tc::mma_bf16(acc, dL + 2 * k, dW + 2 * k, idesc, 1u);
           }
-          if (S == 1) tc::mma_commit(&empty_bar[s]);
-          else tc::mma_commit_mc(&empty_bar[s], cmask);   // the stage's boxes came from every CTA
+          tc::mma_commit(&empty_bar[s]);
         }
         if (ok) tc::mma_commit(&acc_full[b]);
       }
@@ -297,9 +273,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
   __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still multicast into it or arrive on its
-  // barriers (every CTA's MMAs, hence its commits, are complete here)
-  if (S > 1) cluster_sync_all();
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kCols);
@@ -307,41 +280,31 @@ __global__ void __launch_bounds__(kRwThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-// Clusters of S CTAs (one per SM) that can be resident at once, S = 1, 2, 4.
-static int max_clusters(int S) {
-  static int cache[kRwMaxCluster + 1] = {0};
-  static std::once_flag once;
-  std::call_once(once, [] {
+// CTAs (one per SM) that can be resident at once, on the current device;
+// also sets the kernels' shared-memory limit there.  0 if the query fails.
+static int max_ctas() {
+  static DeviceOnce once;
+  static int cache[kMaxDevices] = {0};
+  int dev = -1;
+  const cudaError_t ce = once.run([](int d) -> cudaError_t {
     for (auto k : {gemm_rows_kernel<256, 1>, gemm_rows_kernel<224, 1>, gemm_rows_kernel<192, 1>,
-                   gemm_rows_kernel<160, 1>, gemm_rows_kernel<128, 1>, gemm_rows_kernel<256, 2>})
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRwSmem);
-    for (int c = 1; c <= kRwMaxCluster; c *= 2) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(c * 64);
-      cfg.blockDim = dim3(kRwThreads);
-      cfg.dynamicSmemBytes = kRwSmem;
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = c;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_rows_kernel<256, 1>, &cfg) != cudaSuccess) n = 0;
-      cache[c] = n;
+                   gemm_rows_kernel<160, 1>, gemm_rows_kernel<128, 1>, gemm_rows_kernel<256, 2>}) {
+      const cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kRwSmem);
+      if (e1 != cudaSuccess) return e1;
     }
+    int per_sm = 0, sms = 0;
+    cudaError_t e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_rows_kernel<256, 1>, kRwThreads,
+                                                                    kRwSmem);
+    if (e2 == cudaSuccess) e2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    if (e2 != cudaSuccess) return e2;
+    cache[d] = per_sm * sms;
+    return cudaSuccess;
+  }, &dev);
+  if (ce != cudaSuccess) {
     cudaGetLastError();
-  });
-  return cache[S];
-}
-
-// Cluster size for a GEMM of T feature tiles: the largest (<= 4) that
-// divides T and can be resident.
-static int rows_cluster(int T) {
-  for (int c = kRwMaxCluster; c > 1; c /= 2)
-    if (T % c == 0 && max_clusters(c) > 0) return c;
-  return 1;
+    return 0;
+  }
+  return cache[dev];
 }
 
 // Weight tiles per unit: 128-row tiles pair up into 256-wide units.
@@ -349,14 +312,12 @@ static int rows_tp(const TcGemm& g) { return g.N == 128 && g.M % 256 == 0 ? 2 : 
 
 bool gemm_rows_preferred(const TcGemm& g, int n) {
   if (g.N <= 0 || g.M % g.N || g.K % kRwBK) return false;
-  const int T = g.M / (g.N * rows_tp(g)), S = rows_cluster(T);
-  const long long units = (long long)(T / S) * ((n + kRwRows - 1) / kRwRows);
-  const int resident = max_clusters(S);
+  const int T = g.M / (g.N * rows_tp(g));
+  const long long units = (long long)T * ((n + kRwRows - 1) / kRwRows);
+  const int resident = max_ctas();
   if (resident <= 0) return false;
-  // whole units per cluster: a last wave that is mostly empty makes this
-  // kernel slower than the 64-row-tile kernel (which splits K to fill SMs).
-  // Measured (7B, 544 rows): O and down with 20 units for 36 resident
-  // clusters still ran faster here (2.06 vs 2.24, 5.64 vs 6.49 ms per step).
+  // whole units per CTA: a last wave that is mostly empty makes this kernel
+  // slower than the 64-row-tile kernel (which splits K to fill SMs).
   const long long waves = (units + resident - 1) / resident;
   return (double)units / (double)(waves * resident) >= 0.5;
 }
@@ -375,30 +336,20 @@ cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStre
   a.NRT = (n + kRwRows - 1) / kRwRows;
   const int TP = rows_tp(g);
   const int T = g.M / (g.N * TP);
-  a.S = rows_cluster(T);
-  a.units = (T / a.S) * a.NRT;
+  a.units = T * a.NRT;
   a.err = ep.err;
-  const int resident = max_clusters(a.S);
+  const int resident = max_ctas();
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.S * std::min(a.units, resident)));
+  cfg.gridDim = dim3((unsigned)std::min(a.units, resident));
   cfg.blockDim = dim3(kRwThreads);
   cfg.dynamicSmemBytes = kRwSmem;
   cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  int na = 0;
-  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
-  if (a.S > 1) {
-    at[na].id = cudaLaunchAttributeClusterDimension;
-    at[na].val.clusterDim.x = a.S;
-    at[na].val.clusterDim.y = 1;
-    at[na].val.clusterDim.z = 1;
-    ++na;
-  }
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = na;
+  cfg.numAttrs = 1;
   if (TP == 2) return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<256, 2>, *g.w, *g.hi, *g.lo, a, ep);
   switch (g.N) {
     case 256: return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<256, 1>, *g.w, *g.hi, *g.lo, a, ep);

@@ -473,14 +473,19 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
   return r == CUDA_SUCCESS;
 }
 
-// Co-resident clusters of each size (queried once per process).
+// Co-resident clusters of each size on the current device (queried once per
+// device; also sets the kernels' shared-memory limit there).  0 if the
+// query fails.
 static int max_clusters(int S) {
-  static int cache[kTcMaxCluster + 1] = {0};
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static DeviceOnce once;
+  static int cache[kMaxDevices][kTcMaxCluster + 1] = {};
+  int dev = -1;
+  const cudaError_t ce = once.run([](int d) -> cudaError_t {
     for (auto k : {gemm_tc_kernel<256>, gemm_tc_kernel<224>, gemm_tc_kernel<192>, gemm_tc_kernel<160>,
-                   gemm_tc_kernel<128>})
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+                   gemm_tc_kernel<128>}) {
+      const cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+      if (e1 != cudaSuccess) return e1;
+    }
     for (int s = 1; s <= kTcMaxCluster; ++s) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(s * 64);
@@ -494,12 +499,19 @@ static int max_clusters(int S) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN>, &cfg) != cudaSuccess) n = 0;
-      cache[s] = n;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN>, &cfg) != cudaSuccess) {
+        n = 0;
+        cudaGetLastError();
+      }
+      cache[d][s] = n;
     }
+    return cudaSuccess;
+  }, &dev);
+  if (ce != cudaSuccess) {
     cudaGetLastError();
-  });
-  return cache[S];
+    return 0;
+  }
+  return cache[dev][S];
 }
 
 // Cluster size for U units of KB k-blocks: fewest estimated waves x (k-blocks
@@ -569,7 +581,7 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  max_clusters(1);   // sets the kernels' shared-memory limit once
+  if (max_clusters(1) <= 0) return cudaErrorInvalidConfiguration;   // also sets the shared-memory limit
   switch (g.N) {
     case 256: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, *g.w, *g.hi, *g.lo, a, ep, pf);
     case 224: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224>, *g.w, *g.hi, *g.lo, a, ep, pf);

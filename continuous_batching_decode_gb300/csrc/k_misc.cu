@@ -2,6 +2,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace cbd {
 
@@ -143,6 +144,28 @@ cudaError_t launch_rmsnorm(const cbd_engine* e, const float* x, const float* g, 
   const int ctas = (n_rows + rpc - 1) / rpc;
   return launch_pdl(rmsnorm_kernel, dim3(ctas), dim3(tpr * rpc), 0, s, x, g, gather, n_rows, e->dm.d, e->dm.eps, tpr,
                     hi, lo);
+}
+
+// The bounded mbarrier wait that every pipeline of the step's kernels uses,
+// on a barrier that nothing completes: thread 0 gives up after `limit` SM
+// cycles, which records kDevWaitTimeout in the error word, and the kernel
+// returns.  No copy is in flight, no TMEM is held and no peer CTA waits.
+__global__ void wait_probe_kernel(long long limit, int32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) tc::mbar_wait(&bar, 0, err, &abort_flag, limit);
+  __syncthreads();
+}
+
+cudaError_t launch_wait_probe(long long limit, int32_t* err, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(limit, err);
+  return cudaGetLastError();
 }
 
 }  // namespace cbd

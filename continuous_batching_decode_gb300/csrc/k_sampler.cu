@@ -534,11 +534,10 @@ cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, c
                            const SampDev* samp, float* scratch, const uint32_t* forbid, int32_t* out_tokens,
                            int32_t* err, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t ce = cudaFuncSetAttribute(sampler_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampDynSmem);
+  static DeviceOnce attr;
+  {
+    const cudaError_t ce = set_smem_once(attr, sampler_kernel, (int)kSampDynSmem);
     if (ce != cudaSuccess) return ce;
-    attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(m * kSC);

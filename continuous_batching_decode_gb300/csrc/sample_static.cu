@@ -15,8 +15,14 @@
 // The array is part of the library image: every GPU that loads libcbd holds
 // it until the process exits.  It is shared by every call on a device and
 // keeps the last call's contents; everything a call reads from it is written
-// earlier by the same call.  Calls whose work overlaps on the GPU (different
-// streams, no ordering between them) race on the array.
+// earlier by the same call, except the error word, which starts at zero when
+// the library loads, is set by the first row that finds no token, and is
+// cleared only by cbd_sample_static_check.  Calls whose work overlaps on the
+// GPU (different streams, no ordering between them) race on the array.
+//
+// The rows' parameters reach the device as the arguments of a small kernel
+// that writes them into the array, so a call copies nothing from host
+// memory.
 #include <cstring>
 #include <mutex>
 
@@ -36,12 +42,29 @@ constexpr int kStaticVocab = CBD_SAMPLE_STATIC_MAX_VOCAB;
 constexpr size_t kZBytes = (size_t)kStaticRows * kStaticVocab * sizeof(float);
 constexpr size_t kSampOff = kZBytes;
 constexpr size_t kSlotOff = kSampOff + ((kStaticRows * sizeof(SampDev) + 255) / 256) * 256;
-constexpr size_t kAreaBytes = kSlotOff + ((kStaticRows * sizeof(int32_t) + 255) / 256) * 256;
+constexpr size_t kErrOff = kSlotOff + ((kStaticRows * sizeof(int32_t) + 255) / 256) * 256;
+constexpr size_t kAreaBytes = kErrOff + 256;
 
-// [rows][vocab] fp32 scratch, then [rows] SampDev, then [rows] int32 slots.
+// [rows][vocab] fp32 scratch, then [rows] SampDev, then [rows] int32 slots,
+// then the int32 error word.
 static __device__ __align__(256) unsigned char g_sample_area[kAreaBytes];
 
-constexpr int kMaxDevices = 64;
+// The rows' parameters, passed by value to the kernel that stores them.
+struct StaticParams {
+  SampDev sd[kStaticRows];
+  int32_t slots[kStaticRows];
+  int32_t m;
+};
+
+__global__ void store_params_kernel(const StaticParams p) {
+  SampDev* sd = reinterpret_cast<SampDev*>(g_sample_area + kSampOff);
+  int32_t* sl = reinterpret_cast<int32_t*>(g_sample_area + kSlotOff);
+  for (int j = threadIdx.x; j < p.m; j += blockDim.x) {
+    sd[j] = p.sd[j];
+    sl[j] = p.slots[j];
+  }
+}
+
 std::mutex g_mu;
 unsigned char* g_area_ptr[kMaxDevices] = {};
 
@@ -80,8 +103,8 @@ extern "C" cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t 
   if (!logits || !counters || !slots || !sampling || !out_tokens)
     return fail(CBD_EINVAL, "cbd_sample_static: NULL argument");
   if (counter_rows < 1) return fail(CBD_EINVAL, "cbd_sample_static: counter_rows must be >= 1");
-  SampDev sd[kStaticRows];
-  int32_t sl[kStaticRows];
+  StaticParams prm{};
+  prm.m = m;
   for (int32_t j = 0; j < m; ++j) {
     if (slots[j] < 0 || slots[j] >= counter_rows)
       return fail(CBD_EINVAL, "cbd_sample_static: slot %d outside the %d counter rows", slots[j], counter_rows);
@@ -94,23 +117,42 @@ extern "C" cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t 
       return fail(CBD_EINVAL, "cbd_sample_static: sampling %d invalid", j);
     if (uniforms && !(uniforms[j] >= 0.f && uniforms[j] < 1.f))
       return fail(CBD_EINVAL, "cbd_sample_static: uniform %d not in [0,1)", j);
-    sd[j] = SampDev{s.temperature, s.top_p, s.presence_penalty, s.frequency_penalty, s.penalty_decay, s.top_k,
-                    (uint32_t)(s.seed & 0xffffffffu), (uint32_t)(s.seed >> 32),
-                    (uint32_t)(s.request_id & 0xffffffffu), (uint32_t)(s.request_id >> 32), s.token_index,
-                    uniforms ? uniforms[j] : -1.0f};
-    sl[j] = slots[j];
+    prm.sd[j] = SampDev{s.temperature, s.top_p, s.presence_penalty, s.frequency_penalty, s.penalty_decay, s.top_k,
+                        (uint32_t)(s.seed & 0xffffffffu), (uint32_t)(s.seed >> 32),
+                        (uint32_t)(s.request_id & 0xffffffffu), (uint32_t)(s.request_id >> 32), s.token_index,
+                        uniforms ? uniforms[j] : -1.0f};
+    prm.slots[j] = slots[j];
   }
   unsigned char* area = nullptr;
   cbd_status st = area_on_current_device(&area);
   if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t ce = cudaMemcpyAsync(area + kSampOff, sd, (size_t)m * sizeof(SampDev), cudaMemcpyHostToDevice, s);
-  if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(area + kSlotOff, sl, (size_t)m * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: parameter copy: %s", cudaGetErrorString(ce));
+  store_params_kernel<<<1, 32, 0, s>>>(prm);
+  cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: parameter store: %s", cudaGetErrorString(ce));
   ce = sampler_launch(logits, m, vocab, counters, reinterpret_cast<const int32_t*>(area + kSlotOff),
                       reinterpret_cast<const SampDev*>(area + kSampOff), reinterpret_cast<float*>(area), nullptr,
-                      out_tokens, nullptr, s);
+                      out_tokens, reinterpret_cast<int32_t*>(area + kErrOff), s);
   if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static: launch: %s", cudaGetErrorString(ce));
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_sample_static_check(void* stream) {
+  clear_error();
+  unsigned char* area = nullptr;
+  cbd_status st = area_on_current_device(&area);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t ce = cudaMemcpyAsync(&v, area + kErrOff, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static_check: %s", cudaGetErrorString(ce));
+  if (v) {
+    ce = cudaMemsetAsync(area + kErrOff, 0, sizeof(v), s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) return fail(CBD_ECUDA, "cbd_sample_static_check: clear: %s", cudaGetErrorString(ce));
+    return fail(CBD_EDEVICE, "cbd_sample_static: device error code %d%s", v,
+                v == kDevSampler ? " (a row had no token to draw: every logit -inf or NaN)" : "");
+  }
   return CBD_OK;
 }

@@ -37,15 +37,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Cycles a wait may take before it gives up: 2^31 SM cycles, about a second.
+constexpr long long kWaitLimit = 1ll << 31;
+
 // Wait for the phase with the given parity; false (and the error word set)
-// after ~2^31 SM cycles (about a second) or if `abort` is raised.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err, volatile int* abort) {
+// after `limit` SM cycles or if `abort` is raised.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err, volatile int* abort,
+                                          long long limit = kWaitLimit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > (1ll << 31)) {
+    if (clock64() - t0 > limit) {
       set_err(err, kDevWaitTimeout);
       *abort = 1;
       return false;
@@ -212,29 +216,6 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// ---------------------------------------------------------------- clusters
-// 2-D tiled load like tma_load_2d, delivered to the same shared-memory
-// offset in every CTA of the cluster named by `mask` (bit r = rank r), each
-// copy completing the transaction count of the mbarrier at `bar`'s offset in
-// its own CTA.  The same alignment rule on x applies.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// Like mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA
-// of the cluster named by `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
 
 }  // namespace tc
 

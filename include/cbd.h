@@ -115,13 +115,23 @@ typedef struct cbd_engine cbd_engine;
 typedef struct cbd_kv_pool cbd_kv_pool;
 typedef struct cbd_batch cbd_batch;
 
-/* Create an engine on the current CUDA device.  The weights are copied and
- * repacked into an engine-owned device arena (row orders chosen for the
- * kernels' epilogues); the caller may free its buffers when this returns.
- * Also allocates the step's activations, workspaces and the per-slot
- * penalty counters ([max_slots][V] fp32, zero).  Errors: CBD_EINVAL (shape),
- * CBD_EUNSUPPORTED (not an sm_103 device, or a shape the kernels do not
- * cover), CBD_ENOMEM, CBD_ECUDA.  *out is NULL on failure. */
+/* Create an engine on the current CUDA device: the weights that every step
+ * reads once for all of its rows ("20.3 服务、批处理与流式" section 20.3.2: a
+ * decode step costs (W + B*A)/beta, W being streamed once per step whatever
+ * B is; "0.8MB 跑通 Qwen 第 14-1 篇" section 1: the weights are read once per
+ * step for the whole batch), the Batch executor's state that is separate
+ * from the Scheduler (same section of the Forma page), and the per-slot
+ * device state of the Albatross worker ("RWKV Runner Albatross 后端",
+ * section 连续批处理：Worker 主循环: occurrence counters for the penalties,
+ * one row per slot).  The weights are copied and repacked into an
+ * engine-owned device arena (row orders chosen for the kernels'
+ * epilogues); the caller may free its buffers when this returns.  Also
+ * allocates the step's activations, workspaces and the per-slot penalty
+ * counters ([max_slots][V] fp32, zero).  Every later call on the engine,
+ * its pools and batches runs on this device, whichever device is current
+ * in the calling thread.  Errors: CBD_EINVAL (shape), CBD_EUNSUPPORTED (not
+ * an sm_103 device, or a shape the kernels do not cover), CBD_ENOMEM,
+ * CBD_ECUDA.  *out is NULL on failure. */
 cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights* w, cbd_engine** out);
 cbd_status cbd_engine_destroy(cbd_engine* e);
 
@@ -129,6 +139,20 @@ cbd_status cbd_engine_destroy(cbd_engine* e);
  * CBD_EDEVICE with the recorded code (a bounded wait that ran out, an index
  * a kernel refused) in the message; the error word is then cleared. */
 cbd_status cbd_engine_check(cbd_engine* e);
+
+/* Failure path of the step's kernels, exercised on purpose: every pipeline
+ * wait in them (TMA stages, MMA completion, accumulator hand-over) is an
+ * mbarrier wait that gives up after about 2^31 SM cycles, records
+ * kDevWaitTimeout (code 3) in the engine's error word and lets its kernel
+ * wind down instead of hanging the device.  This call launches one
+ * single-warp kernel on `stream` that runs that same wait, with a limit of
+ * limit_cycles (1 .. 2^31), on a shared-memory barrier that nothing
+ * completes -- no copy in flight, no tensor memory, no other CTA involved --
+ * so the wait runs out and the kernel returns.  cbd_engine_check then
+ * reports CBD_EDEVICE with code 3 and clears the word; the engine stays
+ * usable.  For tests of the failure path.  CBD_EINVAL for a limit outside
+ * the range. */
+cbd_status cbd_engine_test_wait_timeout(cbd_engine* e, int64_t limit_cycles, void* stream);
 
 /* Choose how the step's weight contractions run: path 0 = automatic (the
  * CUDA-core GEMV for up to gemv_max_rows rows, tcgen05 tensor cores above),
@@ -152,12 +176,11 @@ cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
 /* On the tcgen05 path, steps of at least min_rows rows (prefill chunks,
  * "20.3 服务、批处理与流式" section 20.3.2) may run their weight
  * contractions on a persistent kernel with 128-row activation tiles: each
- * weight tile feeds 128 rows per pass instead of 64, clusters of up to 4
- * CTAs share (multicast) each activation tile, and two TMEM accumulators
- * overlap one tile's epilogue with the next tile's mainloop; such a step
- * runs the RMSNorm as its own kernel.  With
+ * weight tile feeds 128 rows per pass instead of 64, and two TMEM
+ * accumulators overlap one tile's epilogue with the next tile's mainloop;
+ * such a step runs the RMSNorm as its own kernel.  With
  * force == 0 a GEMM takes this kernel only where its units fill at least
- * half of the last wave of resident clusters (else the 64-row-tile kernel,
+ * half of the last wave of resident CTAs (else the 64-row-tile kernel,
  * which splits K); with force != 0 every GEMM of the step takes it.  Same
  * sums as the other paths, in another order.  min_rows 0 = never.
  * Default 512 (below it the 64-row-tile kernel with the fused RMSNorm was
@@ -222,7 +245,12 @@ typedef struct cbd_kernel_stat {
 cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable);
 cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* out, int32_t cap, int32_t* n);
 
-/* Zero slot `slot`'s counters (a request was admitted to it). */
+/* Zero slot `slot`'s occurrence counters: a request was admitted to the
+ * slot, and its penalty state starts empty ("RWKV Runner Albatross 后端",
+ * section 连续批处理：Worker 主循环: the per-slot penalty state belongs to the
+ * request occupying the slot; "20.3 服务、批处理与流式" section 20.3.2:
+ * sequences join the batch at any iteration).  Stream-ordered on `stream`;
+ * CBD_EINVAL for a slot outside [0, max_slots). */
 cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream);
 
 /* ------------------------------------------------------------ KV pool */
@@ -280,7 +308,15 @@ typedef struct cbd_sampling {
   uint32_t reserved;      /* must be 0 */
 } cbd_sampling;
 
-/* Run one batched step on `stream`.
+/* Run one batched step on `stream`: one model iteration over the step's
+ * row set -- the Batch executing what the Scheduler decided ("20.3 服务、批
+ * 处理与流式" section 20.3.2: iteration-level scheduling, requests join and
+ * leave between iterations; every row reads its own KV through its slot's
+ * block table in the shared pool; prefill chunks and decode rows in one
+ * step), with every weight read once for all rows and per-row attention
+ * over each request's own KV ("0.8MB 跑通 Qwen 第 14-1 篇" sections 1-2),
+ * then the per-row penalties and batched sampling ("RWKV Runner Albatross
+ * 后端", section 连续批处理：Worker 主循环).
  *   rows [n_rows] (host): the step's row set, any order, 1 <= n_rows <= max_rows.
  *   block_tables (host): [table_slots][max_blocks_per_seq] int32, row s maps
  *     slot s's logical block b to a physical pool block; entries past
@@ -375,17 +411,26 @@ cbd_status cbd_sample(cbd_engine* e, const float* logits, int32_t m,
  *   uniforms (host, nullable) [m]; out_tokens (device) [m].
  * Limits: 1 <= m <= CBD_SAMPLE_STATIC_MAX_ROWS, 1 <= vocab <=
  * CBD_SAMPLE_STATIC_MAX_VOCAB; larger sizes return CBD_EINVAL with a message.
- * The array (4 MB + 1 KB) is held by every GPU that loads libcbd until the
+ * The array (4 MB + 1.3 KB) is held by every GPU that loads libcbd until the
  * process exits.  The first call on a device looks up the array's device
  * address; make that first call before any stream capture.  All calls on a
  * device share the array and it keeps the last call's contents (each call
- * writes what it reads); calls that overlap on the GPU race.  Calls no
- * cudaMalloc, cudaFree or other allocating routine. */
+ * writes what it reads); calls that overlap on the GPU race.  A row for
+ * which no token can be drawn (every logit -inf or NaN after the penalty)
+ * gets token 0 and sets an error word in the array, which stays set until
+ * cbd_sample_static_check reads it.  Calls no cudaMalloc, cudaFree or other
+ * allocating routine. */
 #define CBD_SAMPLE_STATIC_MAX_ROWS 16
 #define CBD_SAMPLE_STATIC_MAX_VOCAB 65536
 cbd_status cbd_sample_static(const float* logits, int32_t m, int32_t vocab, float* counters,
                              int32_t counter_rows, const int32_t* slots, const cbd_sampling* sampling,
                              const float* uniforms, int32_t* out_tokens, void* stream);
+/* Error status of the cbd_sample_static calls on the current device since
+ * the last check: waits for `stream`, reads the array's error word and
+ * clears it.  CBD_OK, or CBD_EDEVICE with the code in the message (a row had
+ * no token to draw).  Make sure every call to check has reached `stream`
+ * (or the device) before it.  Allocates nothing. */
+cbd_status cbd_sample_static_check(void* stream);
 
 /* ------------------------------------------------------------ scheduler */
 /* Host-side scheduler ("20.3 服务、批处理与流式" section 20.3.2 and 20.3.4):

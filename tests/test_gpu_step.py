@@ -429,10 +429,33 @@ def test_forbidden_tokens_on_gpu(tiny):
         cbd.engine_set_forbidden(tiny.e, [])
 
 
+def oracle_over_gpu_kv(tiny, wl, pool, tables, rows):
+    """The oracle's logits for the tiny step, with the GPU's prior KV as its
+    state (the only differences left are the step's own arithmetic)."""
+    om_ = tiny.oracle()
+    prior = {s: c for s, c in enumerate(wl["contexts"])}
+    kv = gu.oracle_kv_from_gpu(tiny, pool, tables, prior)
+    kv[4] = om.SequenceKV(om_.cfg, 64)
+    return om.step(om_, kv, [(r[0], r[1], r[2], r[4]) for r in rows])
+
+
+def assert_tokens_match_oracle(tiny, toks, z_gpu, pre, sampling):
+    """Sampled ids equal the oracle sampler's on the GPU's own logits
+    (outside near ties)."""
+    for j in range(len(toks)):
+        p = gu.sampling_params(sampling[j])
+        u = gu.uniform_of(sampling[j])
+        lf = z_gpu[j].astype(np.float32)
+        if not gu.sampling_near_tie(lf, pre[j], p, u):
+            assert toks[j] == osamp.sample_row(lf, pre[j], p, u), f"row {j}"
+
+
 def test_batch_graph_replay_is_bit_identical(tiny):
     """cbd_batch_set_graph: the captured graph replays the same kernels, so
     tokens and logits are bit-identical to the launch-by-launch run; a
-    changed engine setting or output pointer captures a new graph."""
+    changed engine setting or output pointer captures a new graph.  The
+    replayed step is also held to the oracle: logits within the tolerance,
+    sampled ids equal to the oracle sampler's on the replayed logits."""
     wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 3)
     cv = gu.counters_view(tiny)
     V = tiny.shape["vocab"]
@@ -453,6 +476,9 @@ def test_batch_graph_replay_is_bit_identical(tiny):
             np.testing.assert_array_equal(t, t0)
             np.testing.assert_array_equal(z, z0)
         assert cbd.batch_captures(b) == 1
+        zo = oracle_over_gpu_kv(tiny, wl, pool, tables, rows)
+        gu.assert_logits_close(z.astype(np.float64), zo, "graph-replayed batch")
+        assert_tokens_match_oracle(tiny, t, z.astype(np.float64), np.zeros((m, V), np.float32), sampling)
         cbd.engine_set_attention_path(tiny.e, tiny.attn_path)
         t, z = run(lg1)                      # a setting changed: captured again
         assert cbd.batch_captures(b) == 2
@@ -473,7 +499,8 @@ def test_batch_graph_replay_is_bit_identical(tiny):
 def test_step_graph_is_bit_identical(tiny):
     """cbd_engine_set_step_graph: cbd_step uploads and runs through cached
     graphs with results bit-identical to the launch-by-launch step; one
-    capture per (shape, staging buffer), reused afterwards."""
+    capture per (shape, staging buffer), reused afterwards.  The graph-run
+    step is also held to the oracle (logits and sampled ids)."""
     wl, pool, tables, nbps, rows, sampling = tiny_setup(tiny, 5)
     cv = gu.counters_view(tiny)
     V = tiny.shape["vocab"]
@@ -496,6 +523,9 @@ def test_step_graph_is_bit_identical(tiny):
             np.testing.assert_array_equal(t, t0)
             np.testing.assert_array_equal(z, z0)
         assert cbd.engine_step_graph_captures(tiny.e) - c0 == 2        # one per staging buffer
+        zo = oracle_over_gpu_kv(tiny, wl, pool, tables, rows)
+        gu.assert_logits_close(z.astype(np.float64), zo, "graph-run step")
+        assert_tokens_match_oracle(tiny, t, z.astype(np.float64), np.zeros((m, V), np.float32), sampling)
         short = rows[:3]                                                # another shape: new graphs
         ts, zs = run(short)
         ts, zs = run(short)
