@@ -28,6 +28,15 @@ Rows of one step are processed layer by layer: every row's k, v for a layer
 is stored before any row of that layer attends, so a prefill row at position
 p sees the earlier rows of its own chunk (causal chunked prefill).
 
+Int8 weights ("RWKV Runner Albatross 后端", 边界与后续路线: int8-quantised
+weights are listed among the backend's next steps; "大模型推理为什么需要
+Continuous Batching", section 6: quantisation shrinks the bytes a step moves).
+The pages name int8 and no scheme, so this oracle takes the plainest one:
+weight-only, symmetric, one scale per output channel (row) of every matrix the
+step streams (wq, wk, wv, wo, w_gate, w_up, w_down, lm_head; the embedding
+table and the norm gains are unchanged).  With ``weight_format="int8"`` each
+such matrix is replaced by q * s, computed by ``quantize_int8_rows``.
+
 FP8 KV ("大模型推理为什么需要 Continuous Batching", section 6: quantising the
 KV cache, e.g. to FP8, fits more sequences at a small precision cost): with
 ``kv_format="e4m3"`` K and V are stored as FP8 E4M3 values instead of bf16
@@ -90,6 +99,35 @@ def round_to_e4m3(x) -> np.ndarray:
     r = np.ldexp(np.rint(np.ldexp(a, -quantum)), quantum)
     r = np.minimum(r, 448.0)
     return np.where(np.isnan(x), x, np.copysign(r, x))
+
+
+INT8_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head")
+
+
+def quantize_int8_rows(w) -> tuple:
+    """Symmetric per-row int8 quantisation of a matrix of bf16 values.
+
+    For each row r:  a = max_k |w[r, k]| (exact);  s = a / 127 rounded to
+    fp32 (one IEEE single-precision division, nearest even);
+    q[r, k] = w[r, k] / s rounded to the nearest integer, ties to even (the
+    quotient evaluated in fp64), clamped to [-127, 127].  A row of zeros gets
+    s = 0 and q = 0.  Returns (q as int8, s as float32); the dequantised
+    matrix is q * s, exact in fp64.
+    """
+    w = np.asarray(w, dtype=np.float64)
+    a = np.max(np.abs(w), axis=1)
+    s = (a.astype(np.float32) / np.float32(127.0)).astype(np.float32)
+    s64 = s.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(w / s64[:, None])
+    q = np.where(s64[:, None] > 0, q, 0.0)
+    q = np.clip(q, -127, 127).astype(np.int8)
+    return q, s
+
+
+def dequantize_int8_rows(q, s) -> np.ndarray:
+    """q * s per row, in fp64 (exact: 8-bit by 24-bit products)."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float32).astype(np.float64)[:, None]
 
 
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
@@ -167,15 +205,21 @@ class OracleModel:
       "l.w_gate" [F, d], "l.w_up" [F, d], "l.w_down" [d, F].
     With ``cache=False`` each layer is upcast on use and dropped (bounds RAM
     for the 7B shape); ``weights`` may then also be a callable name -> array.
+    ``weight_format="int8"`` replaces every streamed matrix by its per-row
+    int8 quantisation q * s (``quantize_int8_rows``).
     """
 
     LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm",
                   "w_gate", "w_up", "w_down")
 
-    def __init__(self, cfg: ModelConfig, weights, cache: bool = True, kv_format: str = "bf16"):
+    def __init__(self, cfg: ModelConfig, weights, cache: bool = True, kv_format: str = "bf16",
+                 weight_format: str = "bf16"):
         if kv_format not in ("bf16", "e4m3"):
             raise ValueError(kv_format)
+        if weight_format not in ("bf16", "int8"):
+            raise ValueError(weight_format)
         self.cfg = cfg
+        self.int8 = weight_format == "int8"
         self.kv_round = round_to_bf16 if kv_format == "bf16" else round_to_e4m3
         self._src = weights
         self._cache = {} if cache else None
@@ -186,6 +230,8 @@ class OracleModel:
         src = self._src(name) if callable(self._src) else self._src[name]
         a = np.asarray(src)
         arr = bf16_bits_to_f64(a) if a.dtype in (np.uint16, np.int16) else a.astype(np.float64)
+        if self.int8 and name.split(".")[-1] in INT8_MATRICES:
+            arr = dequantize_int8_rows(*quantize_int8_rows(arr))
         if self._cache is not None:
             self._cache[name] = arr
         return arr
