@@ -84,6 +84,8 @@ def parse():
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
+                    help="streamed weight type (int8: per-row scales; the CPU baseline runs the int8 oracle)")
     ap.add_argument("--rows-gemm", type=int, default=512,
                     help="steps of at least this many rows may run the 128-row-tile GEMM (0 = never)")
     ap.add_argument("--rows-gemm-force", action="store_true",
@@ -120,12 +122,15 @@ def shape_of(args):
     return s
 
 
-def weight_bytes(s):
-    """W: every weight streamed once per step (embedding excluded)."""
+def weight_bytes(s, int8=False):
+    """W: every weight streamed once per step (embedding excluded); int8:
+    one byte per weight plus an fp32 scale per matrix row."""
     d, hq, hkv, hd, F, V, L = (s["d_model"], s["n_heads"], s["n_kv_heads"], s["head_dim"], s["ffn_dim"],
                                s["vocab"], s["n_layers"])
-    per_layer = ((hq + 2 * hkv) * hd * d + d * hq * hd + 2 * F * d + d * F) * 2 + 2 * d * 2
-    return L * per_layer + V * d * 2 + d * 2
+    wb = 1 if int8 else 2
+    rows = (hq + 2 * hkv) * hd + d + 2 * F + d
+    per_layer = ((hq + 2 * hkv) * hd * d + d * hq * hd + 2 * F * d + d * F) * wb + 2 * d * 2 + (rows * 4 if int8 else 0)
+    return L * per_layer + V * d * wb + (V * 4 if int8 else 0) + d * 2
 
 
 def kv_pos_bytes(s, eb=2):
@@ -139,7 +144,8 @@ def config_of(args, s, wl, world):
                          "32-position blocks, top_p 0.3 sampling"),
             "B": args.B, "shape": args.shape, "layers": s["n_layers"], "mean_ctx": float(np.mean(wl["ctx"])),
             "kv": "e4m3" if args.kv == "fp8" else "bf16",
-            "l2": "inputs larger than L2 (weights 14.5 GB + KV); no flush",
+            "weights": args.weights,
+            "l2": "inputs larger than L2 (weights 7.2-14.5 GB + KV); no flush",
             "parallelism": f"replicas x{world}"}
 
 
@@ -208,21 +214,23 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def kernel_bytes(cls, s, B, ctx, eb=2):
+def kernel_bytes(cls, s, B, ctx, eb=2, wb=2):
     """Algorithmic bytes one launch of a kernel class must move (7B: see the
-    design notes for the per-unit figures)."""
+    design notes for the per-unit figures); wb = bytes per weight (int8
+    weights add an fp32 scale per row)."""
     d, hq, hkv, hd, F, V = s["d_model"], s["n_heads"], s["n_kv_heads"], s["head_dim"], s["ffn_dim"], s["vocab"]
     act = lambda k: B * k * 2 * 2            # hi + lo bf16 activations read
+    sc = lambda rows: rows * 4 if wb == 1 else 0
     if cls == "gemm_qkv":
-        return (hq + 2 * hkv) * hd * d * 2 + act(d) + B * hq * hd * 4 + B * 2 * hkv * hd * eb
+        return (hq + 2 * hkv) * hd * d * wb + sc((hq + 2 * hkv) * hd) + act(d) + B * hq * hd * 4 + B * 2 * hkv * hd * eb
     if cls == "gemm_o":
-        return d * hq * hd * 2 + act(hq * hd) + 2 * B * d * 4
+        return d * hq * hd * wb + sc(d) + act(hq * hd) + 2 * B * d * 4
     if cls == "gemm_gate_up":
-        return 2 * F * d * 2 + act(d) + B * F * 2 * 2
+        return 2 * F * d * wb + sc(2 * F) + act(d) + B * F * 2 * 2
     if cls == "gemm_down":
-        return d * F * 2 + act(F) + 2 * B * d * 4
+        return d * F * wb + sc(d) + act(F) + 2 * B * d * 4
     if cls == "gemm_lm_head":
-        return V * d * 2 + act(d) + B * V * 4
+        return V * d * wb + sc(V) + act(d) + B * V * 4
     if cls == "attention":
         return sum(c + 1 for c in ctx) * hkv * hd * 2 * eb + B * hq * hd * 4 + B * hq * hd * 2 * 2
     if cls == "sampler":
@@ -289,9 +297,9 @@ def oracle_kv(s, ctx, seed):
     return kv
 
 
-def oracle_model(s, weights, cache):
+def oracle_model(s, weights, cache, int8=False):
     from oracle import model as om
-    return om.OracleModel(om.ModelConfig(**s), weights, cache=cache)
+    return om.OracleModel(om.ModelConfig(**s), weights, cache=cache, weight_format="int8" if int8 else "bf16")
 
 
 def oracle_step_seconds(model, kv, rows):
@@ -320,7 +328,7 @@ def run_reference(args):
     # fp64 copies of every layer stay cached across steps when the host has
     # room for them (~8 bytes per parameter), else each step upcasts per layer
     cache = host_mem_available_gb() > 1.5 * 8 * sum(v.size for v in bits.values()) / 2**30
-    model = oracle_model(s, bits, cache)
+    model = oracle_model(s, bits, cache, args.weights == "int8")
     kv = oracle_kv(s, wl["ctx"], args.seed + 2)
     rows = [(r[0], r[1], r[2], 1) for r in wl["rows"]]
     ts = []
@@ -374,8 +382,10 @@ def run_cbd(args):
     eb = 1 if fp8 else 2
     sweep = [int(x) for x in args.sweep.split(",") if x.strip()]
     b_cap = max([B] + sweep)
+    i8 = args.weights == "int8"
+    wb = 1 if i8 else 2
     cfg = cbd.make_config(s, max_rows=max(b_cap, 64), max_slots=max(b_cap, 8), max_blocks_per_seq=wl["mbps"],
-                          kv_fp8=fp8)
+                          kv_fp8=fp8, weights_int8=i8)
     e = cbd.engine_create(cfg, w)
     cbd.engine_set_gemm_path(e, args.gemm_path)
     cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
@@ -462,7 +472,7 @@ def run_cbd(args):
     ranked = sorted(((v[1], k) for k, v in prof.items()), reverse=True)
     roof = None
     for _, k in ranked:
-        byt = kernel_bytes(k, s, B, wl["ctx"], eb)
+        byt = kernel_bytes(k, s, B, wl["ctx"], eb, wb)
         if byt:
             n_l, tot = prof[k]
             avg_s = tot / n_l / 1000.0
@@ -471,7 +481,7 @@ def run_cbd(args):
                     "frac": round(ach / peak, 4), "traffic": measured_traffic(k, args), "peak_kind": peak_kind,
                     "bytes_per_launch": byt, "avg_launch_us": round(avg_s * 1e6, 2)}
             break
-    W = weight_bytes(s)
+    W = weight_bytes(s, i8)
     A = sum(c + 1 for c in wl["ctx"]) * kv_pos_bytes(s, eb)
     step_bytes = W + A
     step_roof = {"W_bytes": W, "BA_bytes": A, "bytes_per_step": step_bytes,
@@ -551,18 +561,19 @@ def run_cbd(args):
     # the CPU oracle, one whole step of this workload on the host cores
     cpu = None
     if host_bits is not None:
-        model = oracle_model(s, host_bits, cache=False)
+        model = oracle_model(s, host_bits, cache=False, int8=i8)
         okv = oracle_kv(s, wl["ctx"], args.seed + 2)
         t_step = oracle_step_seconds(model, okv, [(r[0], r[1], r[2], 1) for r in wl["rows"]])
         del okv, model, host_bits
         cpu = {"value": round(B / t_step, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
                "kind": "oracle", "step_s": round(t_step, 2),
                "sample": (f"one whole step timed: {s['n_layers']} layers for all {B} rows plus the LM head, fp64 "
-                          "weights upcast per layer; KV random bf16 per row, shared by the layers")}
+                          f"weights upcast per layer{' (quantised to int8 and back)' if i8 else ''}; KV random bf16 "
+                          "per row, shared by the layers")}
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights, random bf16 KV)",
+            "vs_baseline": None, "dtype": "bf16 (int8 weights)" if i8 else "bf16", "data": "synthetic (seeded random-init weights, random bf16 KV)",
             "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path,
                            l2_prefetch_mb=args.l2_prefetch_mb),
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,

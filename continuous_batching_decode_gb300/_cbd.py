@@ -35,7 +35,7 @@ class Config(ctypes.Structure):
     _fields_ = [("n_layers", c_i32), ("d_model", c_i32), ("n_heads", c_i32), ("n_kv_heads", c_i32),
                 ("head_dim", c_i32), ("ffn_dim", c_i32), ("vocab", c_i32), ("rope_base", c_f32),
                 ("rms_eps", c_f32), ("block_size", c_i32), ("max_rows", c_i32), ("max_slots", c_i32),
-                ("max_blocks_per_seq", c_i32), ("kv_fp8", c_i32)]
+                ("max_blocks_per_seq", c_i32), ("kv_fp8", c_i32), ("weights_int8", c_i32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -130,6 +130,7 @@ PROTOS = {
     "cbd_sample_static": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_i32, _P(c_i32), _P(Sampling), _P(c_f32), c_vp, c_vp]),
     "cbd_sample_static_check": (c_i32, [c_vp]),
     "cbd_engine_test_wait_timeout": (c_i32, [c_vp, ctypes.c_int64, c_vp]),
+    "cbd_engine_read_weight": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp]),
     "cbd_sched_create": (c_i32, [_P(SchedConfig), _P(c_vp)]),
     "cbd_sched_destroy": (c_i32, [c_vp]),
     "cbd_sched_submit": (c_i32, [c_vp, _P(Request)]),
@@ -188,10 +189,11 @@ def version() -> str:
 
 # ------------------------------------------------------------------ engine
 def make_config(shape: dict, max_rows: int, max_slots: int, max_blocks_per_seq: int,
-                rope_base: float = 10000.0, rms_eps: float = 1e-6, kv_fp8: bool = False) -> Config:
+                rope_base: float = 10000.0, rms_eps: float = 1e-6, kv_fp8: bool = False,
+                weights_int8: bool = False) -> Config:
     return Config(shape["n_layers"], shape["d_model"], shape["n_heads"], shape["n_kv_heads"], shape["head_dim"],
                   shape["ffn_dim"], shape["vocab"], rope_base, rms_eps, 32, max_rows, max_slots, max_blocks_per_seq,
-                  1 if kv_fp8 else 0)
+                  1 if kv_fp8 else 0, 1 if weights_int8 else 0)
 
 
 def engine_create(cfg: Config, weights: dict):
@@ -229,6 +231,20 @@ def engine_check(e) -> None:
 
 def engine_test_wait_timeout(e, limit_cycles: int, stream=None) -> None:
     _check(lib().cbd_engine_test_wait_timeout(e, int(limit_cycles), _stream(stream)))
+
+
+WEIGHT_QKV, WEIGHT_O, WEIGHT_GATE_UP, WEIGHT_DOWN, WEIGHT_LM_HEAD = 0, 1, 2, 3, 4
+
+
+def engine_read_weight(e, which: int, layer: int, rows: int, cols: int, int8: bool):
+    """The engine's copy of a streamed matrix in its row order (see
+    cbd_engine_read_weight): (uint16 bf16 bits or int8 array [rows][cols],
+    fp32 scales [rows] or None)."""
+    m = np.zeros((rows, cols), dtype=np.int8 if int8 else np.uint16)
+    sc = np.zeros(rows, dtype=np.float32) if int8 else None
+    _check(lib().cbd_engine_read_weight(e, which, layer, m.ctypes.data,
+                                        sc.ctypes.data if sc is not None else None))
+    return m, sc
 
 
 def engine_counters(e) -> int:

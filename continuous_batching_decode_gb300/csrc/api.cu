@@ -66,6 +66,52 @@ __global__ void permute_tile_kernel(uint16_t* __restrict__ dst, const uint16_t* 
     *reinterpret_cast<uint4*>(dst + tiled_off(r, k, N, KB)) = s[c];
   }
 }
+// Per-row int8 quantisation (cbd_config.weights_int8) of a row-major bf16
+// matrix [.][K] into the tiled layout (byte (r, k) at tiled_off(r, k, N,
+// K / 64)): destination row r takes source row perm[r] (or r).  Per row:
+// s = fp32(max|w| / 127) (IEEE single division), q = w / s in fp64 rounded
+// to the nearest integer, ties to even, clamped to [-127, 127]; s = 0 gives
+// q = 0.  One CTA per row.
+__global__ void quantize_tile_kernel(uint8_t* __restrict__ dst, float* __restrict__ scale,
+                                     const uint16_t* __restrict__ src, const int32_t* __restrict__ perm, int K,
+                                     int N) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const int sr = perm ? perm[r] : r;
+  const uint16_t* row = src + (size_t)sr * K;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) m = fmaxf(m, fabsf(bf16_to_f32(row[k])));
+  m = warp_max(m);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) red[w] = m;
+  __syncthreads();
+  if (w == 0) {
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    m = warp_max(m);
+    if (lane == 0) red[0] = m;
+  }
+  __syncthreads();
+  const float s = __fdiv_rn(red[0], 127.0f);
+  if (threadIdx.x == 0) scale[r] = s;
+  const int KB = K / 64;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    int q = 0;
+    if (s > 0.f) {
+      const double v = rint((double)bf16_to_f32(row[k]) / (double)s);
+      q = (int)fmin(fmax(v, -127.0), 127.0);
+    }
+    dst[tiled_off(r, k, N, KB)] = (uint8_t)(int8_t)q;
+  }
+}
+// Tiled matrix (elements of `eb` bytes, N rows per tile) -> row-major [M][K].
+__global__ void untile_kernel(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src, int K, int N, int eb) {
+  const int r = blockIdx.x;
+  const int KB = K / 64;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const size_t o = tiled_off(r, k, N, KB) * (size_t)eb;
+    for (int b = 0; b < eb; ++b) dst[((size_t)r * K + k) * eb + b] = src[o + b];
+  }
+}
 __global__ void bf16_to_f32_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = bf16_to_f32(src[i]);
@@ -107,6 +153,7 @@ cbd_status check_config(const cbd_config* c) {
   if (!(c->rope_base > 0.f) || !(c->rms_eps >= 0.f)) return fail(CBD_EINVAL, "rope_base/rms_eps invalid");
   if (c->head_dim != 64 && c->head_dim != 128) return fail(CBD_EUNSUPPORTED, "head_dim must be 64 or 128");
   if (c->kv_fp8 != 0 && c->kv_fp8 != 1) return fail(CBD_EINVAL, "kv_fp8 must be 0 or 1");
+  if (c->weights_int8 != 0 && c->weights_int8 != 1) return fail(CBD_EINVAL, "weights_int8 must be 0 or 1");
   const int g = c->n_heads / c->n_kv_heads;
   if (g != 1 && g != 2 && g != 4 && g != 8) return fail(CBD_EUNSUPPORTED, "n_heads/n_kv_heads must be 1, 2, 4 or 8");
   if (c->d_model % 256 || c->ffn_dim % 256 || (c->n_heads * c->head_dim) % 256)
@@ -151,19 +198,26 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   dm.max_rows = cfg->max_rows; dm.max_slots = cfg->max_slots; dm.max_blocks_per_seq = cfg->max_blocks_per_seq;
   dm.rope_base = cfg->rope_base; dm.eps = cfg->rms_eps;
   e->kv_fp8 = cfg->kv_fp8 != 0;
+  e->w_int8 = cfg->weights_int8 != 0;
   e->max_pos = dm.max_blocks_per_seq * kBlock;
   const bool ondev = w->on_device != 0;
   CBD_CUDA(cudaDeviceSynchronize());   // weights produced on any stream are complete
   const size_t d = dm.d, V = dm.V, F = dm.F, qo = dm.qkv_out, hqd = (size_t)dm.hq * dm.hd;
 
-  // ---- weight arena
+  // ---- weight arena (streamed matrices: bf16, or int8 plus per-row fp32 scales)
+  const bool i8 = e->w_int8;
+  const size_t eb = i8 ? 1 : 2;
+  auto sc = [&](Arena& a, size_t rows) { return i8 ? a.take(rows * 4) : (size_t)0; };
   Arena A;
-  const size_t o_embed = A.take(V * d * 2), o_lm = A.take(V * d * 2), o_fn = A.take(d * 4);
+  const size_t o_embed = A.take(V * d * 2), o_lm = A.take(V * d * eb), s_lm = sc(A, V), o_fn = A.take(d * 4);
   std::vector<size_t> o_an(dm.L), o_fnn(dm.L), o_qkv(dm.L), o_o(dm.L), o_gu(dm.L), o_dn(dm.L);
+  std::vector<size_t> s_qkv(dm.L), s_o(dm.L), s_gu(dm.L), s_dn(dm.L);
   for (int l = 0; l < dm.L; ++l) {
     o_an[l] = A.take(d * 4); o_fnn[l] = A.take(d * 4);
-    o_qkv[l] = A.take(qo * d * 2); o_o[l] = A.take(d * hqd * 2);
-    o_gu[l] = A.take(2 * F * d * 2); o_dn[l] = A.take(d * F * 2);
+    o_qkv[l] = A.take(qo * d * eb); s_qkv[l] = sc(A, qo);
+    o_o[l] = A.take(d * hqd * eb); s_o[l] = sc(A, d);
+    o_gu[l] = A.take(2 * F * d * eb); s_gu[l] = sc(A, 2 * F);
+    o_dn[l] = A.take(d * F * eb); s_dn[l] = sc(A, d);
   }
   const size_t o_rope = A.take((size_t)e->max_pos * (dm.hd / 2) * 2 * 4);
   e->arena_bytes = A.off;
@@ -174,7 +228,12 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   };
   uint8_t* base = static_cast<uint8_t*>(e->arena);
   e->embed = reinterpret_cast<uint16_t*>(base + o_embed);
-  e->lm_head = reinterpret_cast<uint16_t*>(base + o_lm);
+  if (i8) {
+    e->lm_q = base + o_lm;
+    e->lm_scale = reinterpret_cast<float*>(base + s_lm);
+  } else {
+    e->lm_head = reinterpret_cast<uint16_t*>(base + o_lm);
+  }
   e->final_norm = reinterpret_cast<float*>(base + o_fn);
   e->rope_cs = reinterpret_cast<float*>(base + o_rope);
 
@@ -204,11 +263,17 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->tile_gu = gemm_tc_pick_tile((int)(2 * F), (int)d);
   e->tile_dn = gemm_tc_pick_tile((int)d, (int)F);
   e->tile_lm = gemm_tc_pick_tile((int)V, (int)d);
-  // tmp (row-major [M][K]) -> arena (tiled, N rows per tile), rows permuted when perm is given
-  auto tiled = [&](size_t off, const std::vector<int32_t>* perm, int M, int K, int N) -> cbd_status {
+  // tmp (row-major [M][K]) -> arena (tiled, N rows per tile), rows permuted
+  // when perm is given; int8 engines quantise each row on the way (scales
+  // at soff, in the same row order)
+  auto tiled = [&](size_t off, size_t soff, const std::vector<int32_t>* perm, int M, int K, int N) -> cbd_status {
     if (perm) CBD_CUDA(cudaMemcpy(perm_d, perm->data(), perm->size() * 4, cudaMemcpyHostToDevice));
-    permute_tile_kernel<<<M, 256>>>(reinterpret_cast<uint16_t*>(base + off), static_cast<uint16_t*>(tmp),
-                                    perm ? perm_d : nullptr, K, N);
+    if (i8)
+      quantize_tile_kernel<<<M, 256>>>(base + off, reinterpret_cast<float*>(base + soff), static_cast<uint16_t*>(tmp),
+                                       perm ? perm_d : nullptr, K, N);
+    else
+      permute_tile_kernel<<<M, 256>>>(reinterpret_cast<uint16_t*>(base + off), static_cast<uint16_t*>(tmp),
+                                      perm ? perm_d : nullptr, K, N);
     CBD_CUDA(cudaGetLastError());
     CBD_CUDA(cudaDeviceSynchronize());
     return CBD_OK;
@@ -231,7 +296,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
 #define TRY(x) do { s2 = (x); if (s2) { free_tmp(); cleanup(); return s2; } } while (0)
   TRY(upload(base + o_embed, w->embed, V * d * 2, ondev));
   TRY(upload(tmp, w->lm_head, V * d * 2, ondev));
-  TRY(tiled(o_lm, nullptr, (int)V, (int)d, e->tile_lm));
+  TRY(tiled(o_lm, s_lm, nullptr, (int)V, (int)d, e->tile_lm));
   TRY(gain(o_fn, w->final_norm));
   e->layers.resize(dm.L);
   for (int l = 0; l < dm.L; ++l) {
@@ -242,21 +307,29 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     TRY(upload(t, lw.wq, hqd * d * 2, ondev));
     TRY(upload(t + hqd * d * 2, lw.wk, (size_t)dm.hkv * dm.hd * d * 2, ondev));
     TRY(upload(t + (hqd + (size_t)dm.hkv * dm.hd) * d * 2, lw.wv, (size_t)dm.hkv * dm.hd * d * 2, ondev));
-    TRY(tiled(o_qkv[l], &perm_qkv, (int)qo, (int)d, e->tile_qkv));
+    TRY(tiled(o_qkv[l], s_qkv[l], &perm_qkv, (int)qo, (int)d, e->tile_qkv));
     TRY(upload(t, lw.wo, d * hqd * 2, ondev));
-    TRY(tiled(o_o[l], nullptr, (int)d, (int)hqd, e->tile_o));
+    TRY(tiled(o_o[l], s_o[l], nullptr, (int)d, (int)hqd, e->tile_o));
     TRY(upload(t, lw.w_gate, F * d * 2, ondev));
     TRY(upload(t + F * d * 2, lw.w_up, F * d * 2, ondev));
-    TRY(tiled(o_gu[l], &perm_gu, (int)(2 * F), (int)d, e->tile_gu));
+    TRY(tiled(o_gu[l], s_gu[l], &perm_gu, (int)(2 * F), (int)d, e->tile_gu));
     TRY(upload(t, lw.w_down, d * F * 2, ondev));
-    TRY(tiled(o_dn[l], nullptr, (int)d, (int)F, e->tile_dn));
+    TRY(tiled(o_dn[l], s_dn[l], nullptr, (int)d, (int)F, e->tile_dn));
     LayerDev& L = e->layers[l];
+    L = LayerDev{};
     L.attn_norm = reinterpret_cast<float*>(base + o_an[l]);
     L.ffn_norm = reinterpret_cast<float*>(base + o_fnn[l]);
-    L.w_qkv = reinterpret_cast<uint16_t*>(base + o_qkv[l]);
-    L.w_o = reinterpret_cast<uint16_t*>(base + o_o[l]);
-    L.w_gu = reinterpret_cast<uint16_t*>(base + o_gu[l]);
-    L.w_down = reinterpret_cast<uint16_t*>(base + o_dn[l]);
+    if (i8) {
+      L.q_qkv = base + o_qkv[l]; L.s_qkv = reinterpret_cast<float*>(base + s_qkv[l]);
+      L.q_o = base + o_o[l]; L.s_o = reinterpret_cast<float*>(base + s_o[l]);
+      L.q_gu = base + o_gu[l]; L.s_gu = reinterpret_cast<float*>(base + s_gu[l]);
+      L.q_down = base + o_dn[l]; L.s_down = reinterpret_cast<float*>(base + s_dn[l]);
+    } else {
+      L.w_qkv = reinterpret_cast<uint16_t*>(base + o_qkv[l]);
+      L.w_o = reinterpret_cast<uint16_t*>(base + o_o[l]);
+      L.w_gu = reinterpret_cast<uint16_t*>(base + o_gu[l]);
+      L.w_down = reinterpret_cast<uint16_t*>(base + o_dn[l]);
+    }
   }
 #undef TRY
   free_tmp();
@@ -335,14 +408,22 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     bool ok = true;
     for (int l = 0; l < L && ok; ++l) {
       const LayerDev& Ld = e->layers[l];
-      // tiled weights: a [M*K/64][64] matrix, one 256-row box per 32 KB tile
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, e->tile_qkv);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, e->tile_o);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, e->tile_gu);
-      ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, e->tile_dn);
+      // tiled weights: a [M*K/64][64] matrix, one N-row box per tile (int8: 64 bytes per row)
+      if (i8) {
+        ok = ok && make_tmap_i8(&e->tmaps[4 * l + 0], Ld.q_qkv, qo * d / 64, e->tile_qkv);
+        ok = ok && make_tmap_i8(&e->tmaps[4 * l + 1], Ld.q_o, d * hqd / 64, e->tile_o);
+        ok = ok && make_tmap_i8(&e->tmaps[4 * l + 2], Ld.q_gu, 2 * F * d / 64, e->tile_gu);
+        ok = ok && make_tmap_i8(&e->tmaps[4 * l + 3], Ld.q_down, d * F / 64, e->tile_dn);
+      } else {
+        ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 0], Ld.w_qkv, 64, qo * d / 64, 64, e->tile_qkv);
+        ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 1], Ld.w_o, 64, d * hqd / 64, 64, e->tile_o);
+        ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 2], Ld.w_gu, 64, 2 * F * d / 64, 64, e->tile_gu);
+        ok = ok && make_tmap_bf16(&e->tmaps[4 * l + 3], Ld.w_down, 64, d * F / 64, 64, e->tile_dn);
+      }
     }
     const size_t a0 = (size_t)4 * L + 1;
-    ok = ok && make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, e->tile_lm);
+    ok = ok && (i8 ? make_tmap_i8(&e->tmaps[4 * L], e->lm_q, V * d / 64, e->tile_lm)
+                   : make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, e->tile_lm));
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
     ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);
@@ -452,6 +533,7 @@ extern "C" cbd_status cbd_engine_set_gemm_path(cbd_engine* e, int32_t path, int3
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   if (path < 0 || path > 2) return fail(CBD_EINVAL, "gemm path must be 0, 1 or 2");
+  if (e->w_int8 && path == 1) return fail(CBD_EUNSUPPORTED, "an int8-weight engine has no CUDA-core GEMV path");
   if (gemv_max_rows < 0) return fail(CBD_EINVAL, "gemv_max_rows must be >= 0");
   e->gemm_path = path;
   ++e->epoch;
@@ -527,6 +609,43 @@ extern "C" cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes) 
                                               (unsigned long long)bytes);
   e->l2_prefetch = (size_t)bytes;
   ++e->epoch;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_read_weight(cbd_engine* e, int32_t which, int32_t layer, void* dst, float* scales) {
+  clear_error();
+  if (!e || !dst) return fail(CBD_EINVAL, "NULL argument");
+  if (which < 0 || which > 4) return fail(CBD_EINVAL, "matrix %d: must be 0..4", which);
+  if (which < 4 && (layer < 0 || layer >= e->dm.L)) return fail(CBD_EINVAL, "layer %d out of range", layer);
+  CBD_ON_DEVICE(e->device);
+  const Dims& dm = e->dm;
+  const int hqd = dm.hq * dm.hd;
+  const void* src = nullptr;
+  const float* sc = nullptr;
+  int M = 0, K = 0, N = 0;
+  if (which == 4) {
+    src = e->w_int8 ? (const void*)e->lm_q : (const void*)e->lm_head;
+    sc = e->lm_scale; M = dm.V; K = dm.d; N = e->tile_lm;
+  } else {
+    const LayerDev& L = e->layers[layer];
+    const bool q = e->w_int8;
+    switch (which) {
+      case 0: src = q ? (const void*)L.q_qkv : L.w_qkv; sc = L.s_qkv; M = dm.qkv_out; K = dm.d; N = e->tile_qkv; break;
+      case 1: src = q ? (const void*)L.q_o : L.w_o; sc = L.s_o; M = dm.d; K = hqd; N = e->tile_o; break;
+      case 2: src = q ? (const void*)L.q_gu : L.w_gu; sc = L.s_gu; M = 2 * dm.F; K = dm.d; N = e->tile_gu; break;
+      default: src = q ? (const void*)L.q_down : L.w_down; sc = L.s_down; M = dm.d; K = dm.F; N = e->tile_dn; break;
+    }
+  }
+  const int eb = e->w_int8 ? 1 : 2;
+  const size_t bytes = (size_t)M * K * eb;
+  void* tmp = nullptr;
+  CBD_CUDA(cudaMalloc(&tmp, bytes));
+  untile_kernel<<<M, 256>>>(static_cast<uint8_t*>(tmp), static_cast<const uint8_t*>(src), K, N, eb);
+  cudaError_t ce = cudaGetLastError();
+  if (ce == cudaSuccess) ce = cudaMemcpy(dst, tmp, bytes, cudaMemcpyDeviceToHost);
+  if (ce == cudaSuccess && scales && sc) ce = cudaMemcpy(scales, sc, (size_t)M * 4, cudaMemcpyDeviceToHost);
+  cudaFree(tmp);
+  if (ce != cudaSuccess) return cuda_fail(ce, "read weight");
   return CBD_OK;
 }
 
@@ -895,10 +1014,11 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   // k-blocks of the GEMM after it, so HBM keeps streaming across launches.
   auto g_qkv_of = [&](int l) {
     return GemmOp{e->layers[l].w_qkv, dm.qkv_out, dm.d, in_hi, in_lo, dm.d,
-                  {&tm[4 * l + 0], tm_in_hi, tm_in_lo, dm.qkv_out, dm.d, e->tile_qkv}};
+                  {&tm[4 * l + 0], tm_in_hi, tm_in_lo, dm.qkv_out, dm.d, e->tile_qkv, e->layers[l].s_qkv,
+                   e->layers[l].q_qkv}};
   };
   const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
-                    {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d, e->tile_lm}};
+                    {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d, e->tile_lm, e->lm_scale, e->lm_q}};
   const PfSpec pf_none{};
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
@@ -906,11 +1026,11 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
     qkv.n_parts_in = l == 0 ? 1 : dn_parts;
     const GemmOp g_qkv = g_qkv_of(l);
     const GemmOp g_o{L.w_o, dm.d, hqd, e->act_hi, e->act_lo, hqd,
-                     {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd, e->tile_o}};
+                     {&tm[4 * l + 1], &tm[a0 + 2], &tm[a0 + 3], dm.d, hqd, e->tile_o, L.s_o, L.q_o}};
     const GemmOp g_gu{L.w_gu, 2 * dm.F, dm.d, in_hi, in_lo, dm.d,
-                      {&tm[4 * l + 2], tm_in_hi, tm_in_lo, 2 * dm.F, dm.d, e->tile_gu}};
+                      {&tm[4 * l + 2], tm_in_hi, tm_in_lo, 2 * dm.F, dm.d, e->tile_gu, L.s_gu, L.q_gu}};
     const GemmOp g_dn{L.w_down, dm.d, dm.F, e->ffn_hi, e->ffn_lo, dm.F,
-                      {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F, e->tile_dn}};
+                      {&tm[4 * l + 3], &tm[a0 + 4], &tm[a0 + 5], dm.d, dm.F, e->tile_dn, L.s_down, L.q_down}};
     const PfSpec pf_o = next_prefetch(e, g_o, n), pf_gu = next_prefetch(e, g_gu, n),
                  pf_dn = next_prefetch(e, g_dn, n);
     const PfSpec pf_after_dn = l + 1 < dm.L ? next_prefetch(e, g_qkv_of(l + 1), n)

@@ -130,10 +130,20 @@ constexpr int kPfMinRun = 16;
 struct LayerDev {
   const float* attn_norm;            // [d] fp32
   const float* ffn_norm;             // [d] fp32
-  const uint16_t* w_qkv;             // [(Hq+2Hkv)*hd][d], q/k rows rope-interleaved
+  const uint16_t* w_qkv;             // [(Hq+2Hkv)*hd][d], q/k rows rope-interleaved (bf16 engines)
   const uint16_t* w_o;               // [d][Hq*hd]
   const uint16_t* w_gu;              // [2F][d], rows (gate_i, up_i) interleaved
   const uint16_t* w_down;            // [d][F]
+  // int8 engines (cbd_config.weights_int8): the same matrices, same row
+  // orders and tiling, one signed byte per weight, and per-row fp32 scales
+  const uint8_t* q_qkv;
+  const uint8_t* q_o;
+  const uint8_t* q_gu;
+  const uint8_t* q_down;
+  const float* s_qkv;
+  const float* s_o;
+  const float* s_gu;
+  const float* s_down;
 };
 
 // One weight matrix as the tcgen05 GEMM sees it: tensor maps of the
@@ -144,6 +154,8 @@ struct TcGemm {
   const CUtensorMap* lo;
   int M, K;
   int N;                  // weight rows per tile (the weights' tiling)
+  const float* scale;     // int8 weights: per-row scales (null: bf16 weights)
+  const uint8_t* w8;      // int8 weights: the tiled bytes (tile (t, kb) is one N x 64-byte run)
 };
 struct TcWork {
   float* part;            // [2 * sm_count][128][128] partial tiles
@@ -195,6 +207,9 @@ struct cbd_engine {
   std::vector<cbd::LayerDev> layers;
   const uint16_t* embed = nullptr;
   const uint16_t* lm_head = nullptr;
+  bool w_int8 = false;                // streamed matrices stored as int8 + per-row scales
+  const uint8_t* lm_q = nullptr;      // int8 LM head (tiled) and its scales
+  const float* lm_scale = nullptr;
   const float* final_norm = nullptr;
   const float* rope_cs = nullptr;     // [max_pos][hd/2][2] fp32 (cos, sin)
   int max_pos = 0;
@@ -376,6 +391,8 @@ struct EpiArgs {
   const float* ssq_in;
   int n_parts_in, d_norm;
   float eps;
+  // int8 weights: every sum of feature f is multiplied by w_scale[f] first
+  const float* w_scale;
 };
 cudaError_t launch_gemv(const uint16_t* W, int M, int K, int N, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
                         int n, const EpiArgs& ep, cudaStream_t s);
@@ -387,6 +404,8 @@ void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S);
 int gemm_tc_pick_tile(int M, int K);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
                     uint32_t box_rows);
+// Tensor map of tiled int8 weights [rows][64] bytes, box 64 x box_rows, no swizzle.
+bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
 cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiArgs& epi, const PfSpec& pf,
                         cudaStream_t s);
 // The L2 prefetch a kernel issues for the GEMM `op` that follows it on n rows

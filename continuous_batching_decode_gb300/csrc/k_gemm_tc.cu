@@ -35,6 +35,16 @@
 // stages; warp 1 owns TMEM and issues the MMAs (one thread); warps 2-9 read
 // the accumulator back (warp w owns TMEM lanes 32*(w%4)..+31, warps w and
 // w+4 split the columns) and run the epilogue.
+//
+// Int8 weights (I8; "RWKV Runner Albatross 后端", 边界与后续路线): a stage
+// holds the int8 weight tile (N rows x 64 bytes, one contiguous run of the
+// tiled layout) and the activation tile.  While the mainloop runs, the eight
+// epilogue warps convert each int8 tile into bf16 (exact: every int8 value
+// is a bf16 value) in one of two 128-byte-swizzled buffers that the
+// unchanged bf16 MMA reads as its B operand; the first two tiles are
+// converted before the dependency wait, since weights do not depend on the
+// previous kernel.  The per-row scale multiplies each finished sum in the
+// epilogue: y = s_f * sum_k q[f][k] * (a_hi + a_lo)[k].
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -63,6 +73,7 @@ struct TcArgs {
   int N;                             // weight rows per tile (MMA N): the weights' tiling
   int T, NR, KB, S;                  // feature tiles, row tiles, k blocks, cluster size
   int32_t* err;
+  const uint8_t* w8;                 // int8 weights: tiled bytes, fetched by 1-D bulk copies
 };
 
 __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
@@ -94,7 +105,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // A norm consumer (ep.ssq_in) scales each row's sums by rinv[row] first; a
 // residual-norm producer collects each quad's sum of x^2 in sq[row][quad]
 // and then writes the row's partial for this CTA (quads in order).
-template <int KIND, int N>
+template <int KIND, int N, bool I8>
 __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, int t, int nr, int rows_here,
                                            int et, uint32_t Pbase, const int2* rinfo, const float* rinv, float* sq) {
   const int q0 = rank * (N / 4) / S, q1 = (rank + 1) * (N / 4) / S;
@@ -126,6 +137,10 @@ __device__ __forceinline__ void epi_phase2(const EpiArgs& ep, int S, int rank, i
           acc.x += pv[qr].x; acc.y += pv[qr].y;
           acc.z += pv[qr].z; acc.w += pv[qr].w;
         }
+    }
+    if constexpr (I8) {
+      const float4 ws = *reinterpret_cast<const float4*>(ep.w_scale + fg);
+      acc.x *= ws.x; acc.y *= ws.y; acc.z *= ws.z; acc.w *= ws.w;
     }
     if (scale) {
       const float r = rinv[i];
@@ -166,17 +181,53 @@ template <int N>
 __host__ __device__ constexpr int tc_stages() {
   return kTcRing / (N * kTcBK * 2 + kTcABytes) < kTcMaxStages ? kTcRing / (N * kTcBK * 2 + kTcABytes) : kTcMaxStages;
 }
-
-// One instantiation per tile width N (weight rows per tile, MMA N).
+// Int8 weights: kConvBufs bf16 conversion buffers of N x 128 bytes, then
+// stages of (int8 tile, activation tile) in the rest of the ring.
+constexpr int kConvBufs = 3;
 template <int N>
+__host__ __device__ constexpr int tc_stages8() {
+  return (kTcRing - kConvBufs * N * 128) / (N * kTcBK + kTcABytes) < kTcMaxStages
+             ? (kTcRing - kConvBufs * N * 128) / (N * kTcBK + kTcABytes)
+             : kTcMaxStages;
+}
+
+// Two int8 weights (bytes j, j + 1 of w) -> bf16x2, exactly, the byte j
+// value in the low half.  For a byte b = s|m (sign bit s, low bits m) the
+// permute builds the bf16 words 0x43|b, from which one mask keeps
+// 0x4300|m = 128 + m and the other 0x4300|(s << 7) = 128 or 256; their
+// difference, m - 128 s, is the two's-complement value, and every number
+// involved is an integer below 2^8, exact in bf16.
+__device__ __forceinline__ uint32_t i8pair_bf16x2(uint32_t w, int j) {
+  const uint32_t t = __byte_perm(w, 0x43434343u, 0x5140u + j + (j << 8));
+  const uint32_t val = t & 0xFF7FFF7Fu, sub = t & 0xFF80FF80u;
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(val), "r"(sub));
+  return r;
+}
+// 16 int8 weights -> 16 bf16, as two 16-byte chunks (8 k each, the lower k
+// in the lower half of each 32-bit word).
+__device__ __forceinline__ void i8x16_bf16(uint4 v, uint4& c0, uint4& c1) {
+  c0 = make_uint4(i8pair_bf16x2(v.x, 0), i8pair_bf16x2(v.x, 2), i8pair_bf16x2(v.y, 0), i8pair_bf16x2(v.y, 2));
+  c1 = make_uint4(i8pair_bf16x2(v.z, 0), i8pair_bf16x2(v.z, 2), i8pair_bf16x2(v.w, 0), i8pair_bf16x2(v.w, 2));
+}
+
+// One instantiation per tile width N (weight rows per tile, MMA N) and
+// weight type (I8: int8 weights with per-row scales).
+template <int N, bool I8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmL, const TcArgs a, const EpiArgs ep, const PfSpec pf) {
   static_assert(N % 32 == 0 && N >= 64 && N <= kTcMaxBN, "tile width");
   constexpr uint32_t idesc = tc::idesc_bf16(2 * kTcRows, N);
-  constexpr int ST = tc_stages<N>();
-  constexpr uint32_t w_bytes = (uint32_t)N * kTcBK * 2;        // one weight tile per stage
+  constexpr int ST = I8 ? tc_stages8<N>() : tc_stages<N>();
+  // bf16: a stage is (weight tile, activation tile); int8: (int8 tile,
+  // activation tile), and the two bf16 conversion buffers follow the stages
+  constexpr uint32_t w_bytes = (uint32_t)N * kTcBK * (I8 ? 1 : 2);   // one weight tile per stage
   constexpr uint32_t stage_bytes = w_bytes + kTcABytes;
+  constexpr uint32_t conv_off = (uint32_t)ST * stage_bytes;          // int8: bf16 buffer b at conv_off + b * N * 128
+  static_assert(!I8 || (conv_off % 1024 == 0 && conv_off + kConvBufs * N * 128u <= (uint32_t)kTcRing),
+                "int8 ring layout");
+  static_assert(stage_bytes % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
   constexpr int PS = N + 4;                                     // fp32 partial row stride (padded)
   TR_DECL;
 #ifdef CBD_TRACE
@@ -185,6 +236,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kTcMaxStages], empty_bar[kTcMaxStages];
   __shared__ __align__(8) uint64_t accum_full, mma_done;
+  // int8 weights: int8 tile landed; bf16 buffer converted; bf16 buffer free
+  __shared__ __align__(8) uint64_t w8_full[I8 ? kTcMaxStages : 1], conv_full[I8 ? kConvBufs : 1],
+      conv_free[I8 ? kConvBufs : 1];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int decision;
@@ -209,6 +263,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc::mbar_init(&accum_full, 1);
     tc::mbar_init(&mma_done, 1);
+    if constexpr (I8) {
+      for (int s = 0; s < ST; ++s) tc::mbar_init(&w8_full[s], 1);
+      for (int b = 0; b < kConvBufs; ++b) {
+        tc::mbar_init(&conv_full[b], kEpiThreads / 32);
+        tc::mbar_init(&conv_free[b], 1);
+      }
+    }
     abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -224,7 +285,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   volatile int* abort_p = &abort_flag;
-  if (warp != 0) pdl_wait();          // the producer waits after prefetching weights
+  // the producer waits after prefetching weights; int8 converters after
+  // converting the first weight tiles
+  if (warp == 1 || (warp >= 2 && !I8)) pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -238,13 +301,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       auto issue_w = [&](int q) {
         const int s = q % ST;
         uint8_t* st = ring + (size_t)s * stage_bytes;
-        tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
-        tc::tma_load_2d_hint(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s], w_policy);
+        if constexpr (I8) {
+          // the tile is one contiguous N x 64-byte run: one bulk copy
+          tc::mbar_arrive_expect_tx(&w8_full[s], w_bytes);
+          tc::bulk_load_hint(st, a.w8 + (size_t)(t * a.KB + kb0 + q) * w_bytes, w_bytes, &w8_full[s], w_policy);
+        } else {
+          tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
+          tc::tma_load_2d_hint(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s], w_policy);
+        }
       };
       auto issue_a = [&](int q) {
         const int s = q % ST;
         uint8_t* st = ring + (size_t)s * stage_bytes + w_bytes;
         const int kx = (kb0 + q) * kTcBK;
+        if constexpr (I8) tc::mbar_arrive_expect_tx(&full_bar[s], 2u * nbox * 2048u);
         for (int j = 0; j < nbox; ++j) {
           tc::tma_load_2d(st + j * 2048, &tmH, kx, nr * kTcRows + j * 16, &full_bar[s]);
           tc::tma_load_2d(st + kTcABytes / 2 + j * 2048, &tmL, kx, nr * kTcRows + j * 16, &full_bar[s]);
@@ -274,6 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int r = q > ST ? q - ST : 0; r < q; ++r) {
           int no_abort = 0;
           tc::mbar_wait(&full_bar[r % ST], (r / ST) & 1, nullptr, &no_abort);
+          if constexpr (I8) tc::mbar_wait(&w8_full[r % ST], (r / ST) & 1, nullptr, &no_abort);
         }
       }
     }
@@ -283,15 +354,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int q = 0; q < n_it; ++q) {
         const int s = q % ST;
+        if constexpr (I8)
+          if (!tc::mbar_wait(&conv_full[q % kConvBufs], (q / kConvBufs) & 1, a.err, abort_p)) { ok = false; break; }
         if (!tc::mbar_wait(&full_bar[s], (q / ST) & 1, a.err, abort_p)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t st = tc::smem_u32(ring + (size_t)s * stage_bytes);
-        const uint64_t dW = tc::sdesc_sw128(st);
+        const uint64_t dW = I8 ? tc::sdesc_sw128(tc::smem_u32(ring) + conv_off + (uint32_t)(q % kConvBufs) * N * 128u)
+                               : tc::sdesc_sw128(st);
         const uint64_t dA = tc::sdesc_sw128(st + w_bytes);
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes along K inside the swizzled rows
           tc::mma_bf16(tmem, dA + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(&empty_bar[s]);
+        if constexpr (I8) tc::mma_commit(&conv_free[q % kConvBufs]);
       }
       if (ok && n_it > 0) tc::mma_commit(&accum_full);
       // every MMA issued completes before TMEM is released
@@ -318,33 +393,108 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float* P = reinterpret_cast<float*>(ring);                  // [64][PS] hi + lo
     float* LO = reinterpret_cast<float*>(ring + 64 * PS * 4);    // [64][PS] lo
     const int et = threadIdx.x - 64;
-    if (ep.kind == kEpiQKV) {
-      // the rows' positions and KV blocks, read while the mainloop runs
-      for (int i = et; i < rows_here; i += kEpiThreads) {
-        const RowDev rw = ep.rows[nr * kTcRows + i];
-        rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
+    if constexpr (I8) {
+      // what the epilogue reads from the previous kernel and the staged
+      // batch, fetched while the mainloop runs, after the first weight
+      // tiles are converted (they need no dependency)
+      auto prologue = [&]() {
+        pdl_wait();
+        if (ep.kind == kEpiQKV) {
+          // the rows' positions and KV blocks, read while the mainloop runs
+          for (int i = et; i < rows_here; i += kEpiThreads) {
+            const RowDev rw = ep.rows[nr * kTcRows + i];
+            rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
+          }
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+          epi_prefetch<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+        } else if (ep.kind == kEpiResid) {
+          epi_prefetch<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+        } else if (ep.kind == kEpiResidNorm) {
+          epi_prefetch<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+        }
+        if (ep.ssq_in) {
+          // fused RMSNorm: 1/rms of each row from the producer's partials; a
+          // warp per row, lanes over the partials (all loads in flight), then a
+          // fixed shuffle tree
+          for (int i = warp - 2; i < rows_here; i += kEpiThreads / 32) {
+            const float* sp = ep.ssq_in + (size_t)(nr * kTcRows + i) * kMaxSsqParts;
+            float v[kMaxSsqParts / 32];
+#pragma unroll
+            for (int j = 0; j < kMaxSsqParts / 32; ++j) v[j] = lane + 32 * j < ep.n_parts_in ? sp[lane + 32 * j] : 0.f;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxSsqParts / 32; ++j) acc += v[j];
+            acc = warp_sum(acc);
+            if (lane == 0) rinv[i] = 1.0f / sqrtf(acc / (float)ep.d_norm + ep.eps);
+          }
+        }
+      };
+      // convert each stage's int8 tile into a bf16 buffer the MMA reads;
+      // the prologue runs once every buffer holds a tile
+      bool conv_ok = true;
+      const uint32_t conv_base = tc::smem_u32(ring) + conv_off;
+      for (int q = 0; q < n_it; ++q) {
+        const int s = q % ST, b = q % kConvBufs;
+        if (conv_ok && (!tc::mbar_wait(&w8_full[s], (q / ST) & 1, a.err, abort_p) ||
+                        !tc::mbar_wait(&conv_free[b], ((q / kConvBufs) & 1) ^ 1, a.err, abort_p)))
+          conv_ok = false;
+        conv_ok = __all_sync(0xffffffffu, conv_ok);    // warp-uniform before the warp's arrive
+        if (conv_ok) {
+          const uint8_t* src = ring + (size_t)s * stage_bytes;
+          const uint32_t dst = conv_base + (uint32_t)b * N * 128u;
+          // task i: row i / 4, 16-byte int8 chunk i % 4 -> bf16 chunks 2c, 2c + 1
+#pragma unroll
+          for (int j = 0; j < (N * 4 + kEpiThreads - 1) / kEpiThreads; ++j) {
+            const int i = et + j * kEpiThreads;
+            if (i < N * 4) {
+              const int r = i >> 2, c = i & 3;
+              const uint4 v = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
+              uint4 c0, c1;
+              i8x16_bf16(v, c0, c1);
+              const uint32_t row = dst + (uint32_t)r * 128u;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((((2 * c) ^ (r & 7))) << 4)),
+                           "r"(c0.x), "r"(c0.y), "r"(c0.z), "r"(c0.w) : "memory");
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((((2 * c + 1) ^ (r & 7))) << 4)),
+                           "r"(c1.x), "r"(c1.y), "r"(c1.z), "r"(c1.w) : "memory");
+            }
+          }
+          // the MMA (async proxy) reads what these threads wrote
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&conv_full[b]);
+        }
+        if (q == (n_it < kConvBufs ? n_it : kConvBufs) - 1) prologue();
       }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      epi_prefetch<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
-    } else if (ep.kind == kEpiResid) {
-      epi_prefetch<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
-    } else if (ep.kind == kEpiResidNorm) {
-      epi_prefetch<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
-    }
-    if (ep.ssq_in) {
-      // fused RMSNorm: 1/rms of each row from the producer's partials; a
-      // warp per row, lanes over the partials (all loads in flight), then a
-      // fixed shuffle tree
-      for (int i = warp - 2; i < rows_here; i += kEpiThreads / 32) {
-        const float* sp = ep.ssq_in + (size_t)(nr * kTcRows + i) * kMaxSsqParts;
-        float v[kMaxSsqParts / 32];
+      if (n_it == 0) prologue();
+    } else {
+      if (ep.kind == kEpiQKV) {
+        // the rows' positions and KV blocks, read while the mainloop runs
+        for (int i = et; i < rows_here; i += kEpiThreads) {
+          const RowDev rw = ep.rows[nr * kTcRows + i];
+          rinfo[i] = make_int2(rw.pos, ep.tables[(size_t)rw.slot * ep.max_blocks_per_seq + (rw.pos >> 5)]);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        epi_prefetch<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      } else if (ep.kind == kEpiResid) {
+        epi_prefetch<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      } else if (ep.kind == kEpiResidNorm) {
+        epi_prefetch<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, rinfo);
+      }
+      if (ep.ssq_in) {
+        // fused RMSNorm: 1/rms of each row from the producer's partials; a
+        // warp per row, lanes over the partials (all loads in flight), then a
+        // fixed shuffle tree
+        for (int i = warp - 2; i < rows_here; i += kEpiThreads / 32) {
+          const float* sp = ep.ssq_in + (size_t)(nr * kTcRows + i) * kMaxSsqParts;
+          float v[kMaxSsqParts / 32];
 #pragma unroll
-        for (int j = 0; j < kMaxSsqParts / 32; ++j) v[j] = lane + 32 * j < ep.n_parts_in ? sp[lane + 32 * j] : 0.f;
-        float acc = 0.f;
+          for (int j = 0; j < kMaxSsqParts / 32; ++j) v[j] = lane + 32 * j < ep.n_parts_in ? sp[lane + 32 * j] : 0.f;
+          float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxSsqParts / 32; ++j) acc += v[j];
-        acc = warp_sum(acc);
-        if (lane == 0) rinv[i] = 1.0f / sqrtf(acc / (float)ep.d_norm + ep.eps);
+          for (int j = 0; j < kMaxSsqParts / 32; ++j) acc += v[j];
+          acc = warp_sum(acc);
+          if (lane == 0) rinv[i] = 1.0f / sqrtf(acc / (float)ep.d_norm + ep.eps);
+        }
       }
     }
     if (n_it > 0) tc::mbar_wait(&accum_full, 0, a.err, abort_p);
@@ -418,11 +568,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t Pbase = tc::smem_u32(ring);
     float* sq = reinterpret_cast<float*>(ring + 64 * PS * 4);   // the LO area, free after phase 1
     switch (ep.kind) {
-      case kEpiQKV: epi_phase2<kEpiQKV, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiResid: epi_phase2<kEpiResid, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiResidNorm: epi_phase2<kEpiResidNorm, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
-      default: epi_phase2<kEpiLogits, N>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiQKV: epi_phase2<kEpiQKV, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResid: epi_phase2<kEpiResid, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiResidNorm: epi_phase2<kEpiResidNorm, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      case kEpiSwiGLU: epi_phase2<kEpiSwiGLU, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
+      default: epi_phase2<kEpiLogits, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
     }
   }
 #ifdef CBD_TRACE
@@ -473,6 +623,19 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_i8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {64, rows};
+  cuuint64_t strides[1] = {64};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Co-resident clusters of each size on the current device (queried once per
 // device; also sets the kernels' shared-memory limit there).  0 if the
 // query fails.
@@ -481,8 +644,10 @@ static int max_clusters(int S) {
   static int cache[kMaxDevices][kTcMaxCluster + 1] = {};
   int dev = -1;
   const cudaError_t ce = once.run([](int d) -> cudaError_t {
-    for (auto k : {gemm_tc_kernel<256>, gemm_tc_kernel<224>, gemm_tc_kernel<192>, gemm_tc_kernel<160>,
-                   gemm_tc_kernel<128>}) {
+    for (auto k : {gemm_tc_kernel<256, false>, gemm_tc_kernel<224, false>, gemm_tc_kernel<192, false>,
+                   gemm_tc_kernel<160, false>, gemm_tc_kernel<128, false>, gemm_tc_kernel<256, true>,
+                   gemm_tc_kernel<224, true>, gemm_tc_kernel<192, true>, gemm_tc_kernel<160, true>,
+                   gemm_tc_kernel<128, true>}) {
       const cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
       if (e1 != cudaSuccess) return e1;
     }
@@ -499,7 +664,7 @@ static int max_clusters(int S) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN, false>, &cfg) != cudaSuccess) {
         n = 0;
         cudaGetLastError();
       }
@@ -559,6 +724,8 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   if (g.M % g.N || g.K % kTcBK) return cudaErrorInvalidValue;
   TcArgs a{};
   a.M = g.M; a.K = g.K; a.n = n; a.N = g.N;
+  a.w8 = g.w8;
+  if (g.scale && !g.w8) return cudaErrorInvalidValue;
   gemm_tc_plan(g.M, g.K, g.N, n, &a.T, &a.NR, &a.KB, &a.S);
   a.err = ep.err;
   const long long U = (long long)a.T * a.NR;
@@ -583,11 +750,16 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   cfg.numAttrs = na;
   if (max_clusters(1) <= 0) return cudaErrorInvalidConfiguration;   // also sets the shared-memory limit
   switch (g.N) {
-    case 256: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 224: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 192: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 160: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 128: return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 256: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
+                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 224: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
+                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 192: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
+                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 160: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
+                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 128: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
+                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -120,12 +120,14 @@ cudaError_t launch_gemv(const uint16_t* W, int M, int K, int TN, const uint16_t*
 
 // Path choice: the CUDA-core GEMV for a handful of rows, the tcgen05 GEMM
 // above that (or as forced by cbd_engine_set_gemm_path).
+// Int8-weight engines run every contraction on the tcgen05 kernel with
+// 64-row tiles (the only one with the int8 -> bf16 conversion stage).
 static bool uses_tc(const cbd_engine* e, int n) {
-  return e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
+  return e->w_int8 || e->gemm_path == 2 || (e->gemm_path == 0 && n > e->gemv_max_rows);
 }
 bool gemm_uses_tc(const cbd_engine* e, int n) { return uses_tc(e, n); }
 bool gemm_uses_rows(const cbd_engine* e, int n) {
-  return uses_tc(e, n) && e->rows_gemm_min > 0 && n >= e->rows_gemm_min;
+  return !e->w_int8 && uses_tc(e, n) && e->rows_gemm_min > 0 && n >= e->rows_gemm_min;
 }
 int gemm_tc_units(int M, int K, int N, int n) {
   int T, NR, KB, S;
@@ -138,13 +140,20 @@ cudaError_t launch_gemm(const cbd_engine* e, const GemmOp& op, int n, const EpiA
   if (n <= 0) return cudaSuccess;
   if (gemm_uses_rows(e, n) && gemm_rows_supports(ep) && (e->rows_gemm_force || gemm_rows_preferred(op.tc, n)))
     return launch_gemm_rows(op.tc, n, ep, s);
-  if (uses_tc(e, n)) return launch_gemm_tc(op.tc, n, ep, pf, s);
+  if (uses_tc(e, n)) {
+    if (op.tc.scale) {
+      EpiArgs e8 = ep;
+      e8.w_scale = op.tc.scale;
+      return launch_gemm_tc(op.tc, n, e8, PfSpec{}, s);
+    }
+    return launch_gemm_tc(op.tc, n, ep, pf, s);
+  }
   return launch_gemv(op.W, op.M, op.K, op.tc.N, op.a_hi, op.a_lo, op.lda, n, ep, s);
 }
 
 PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n) {
   PfSpec pf{};
-  if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n)) return pf;
+  if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n) || e->w_int8) return pf;
   int T, NR, KB, S;
   gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N, n, &T, &NR, &KB, &S);
   const long long units = (long long)T * S;

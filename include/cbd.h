@@ -88,6 +88,19 @@ typedef struct cbd_config {
                                * nearest even and saturated at +-448, no
                                * scale; half the pool bytes per position.
                                * Needs attention path 0. */
+  int32_t weights_int8;       /* 0: the streamed weights stay bf16; 1: int8
+                               * weights ("RWKV Runner Albatross 后端",
+                               * 边界与后续路线: int8-quantised weights as
+                               * follow-up work).  Every matrix the step
+                               * streams (q, k, v, o, gate, up, down, LM head)
+                               * is quantised per output row when the engine
+                               * is created: s = fp32(max|w| / 127), q =
+                               * nearest integer to w / s (ties to even; the
+                               * quotient in fp64), clamped to +-127; the step
+                               * computes s * sum(q * a), fp32 accumulation.
+                               * The embedding and the norm gains stay as
+                               * given.  Half the weight bytes per step.  Needs
+                               * gemm path 0 or 2 (tensor cores). */
 } cbd_config;
 
 /* Weights of one layer: bf16, row-major [out][in], no biases. */
@@ -226,6 +239,17 @@ cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable);
  * only: results are identical with any setting.
  * Errors: CBD_EINVAL for a NULL engine or more than 1 GiB. */
 cbd_status cbd_engine_set_l2_prefetch(cbd_engine* e, uint64_t bytes);
+
+/* The engine's copy of one streamed weight matrix, for inspection and
+ * tests: which = 0 (q, k and v rows as the QKV contraction holds them: per
+ * head of q and then of k, output dims in the order 0, hd/2, 1, hd/2+1, ...,
+ * so each RoPE pair is adjacent; then v in its own order), 1 (o), 2 (gate
+ * and up interleaved: gate row i, up row i, gate row i+1, ...), 3 (down),
+ * 4 (LM head; layer ignored).  dst (host): the matrix row-major in that row
+ * order, [M][K] -- bf16 for a bf16 engine, int8 for an int8 engine; scales
+ * (host, nullable): [M] fp32 per-row scales of an int8 engine.  Synchronous.
+ * CBD_EINVAL for a bad index. */
+cbd_status cbd_engine_read_weight(cbd_engine* e, int32_t which, int32_t layer, void* dst, float* scales);
 
 /* Device pointer of the per-slot occurrence counters, [max_slots][V] fp32,
  * owned by the engine (for inspection and for seeding tests). */

@@ -18,13 +18,14 @@ NEAR_TIE = 1e-3
 
 class Model:
     def __init__(self, name, max_rows=64, max_slots=8, mbps=8, seed=0, device_weights=True, kv_fp8=False,
-                 layers=None):
+                 layers=None, weights_int8=False):
         self.shape = dict(synth.MODEL_SHAPES[name])
         if layers:
             self.shape["n_layers"] = layers
         self.kv_fp8 = kv_fp8
+        self.int8 = weights_int8
         self.w = synth.make_weights(self.shape, seed=seed, device="cuda" if device_weights else "cpu")
-        self.cfg = cbd.make_config(self.shape, max_rows, max_slots, mbps, kv_fp8=kv_fp8)
+        self.cfg = cbd.make_config(self.shape, max_rows, max_slots, mbps, kv_fp8=kv_fp8, weights_int8=weights_int8)
         self.e = cbd.engine_create(self.cfg, self.w)
         self.mbps = mbps
         self._oracle = None
@@ -33,7 +34,8 @@ class Model:
         if self._oracle is None:
             bits = {k: synth.bf16_bits(v) for k, v in self.w.items()}
             self._oracle = om.OracleModel(om.ModelConfig(**self.shape), bits, cache=cache,
-                                          kv_format="e4m3" if self.kv_fp8 else "bf16")
+                                          kv_format="e4m3" if self.kv_fp8 else "bf16",
+                                          weight_format="int8" if self.int8 else "bf16")
         return self._oracle
 
     def close(self):
