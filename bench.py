@@ -82,6 +82,8 @@ def parse():
                     help="comma-separated B values timed after the headline step ('' = none)")
     ap.add_argument("--gemm-path", type=int, default=0, help="0 auto, 1 CUDA-core GEMV, 2 tcgen05")
     ap.add_argument("--attn-path", type=int, default=0, help="0 streaming mma.sync, 1 CUDA cores, 2 per-chunk mma.sync")
+    ap.add_argument("--gemm-chain", action="store_true",
+                    help="decode contractions of a layer as one persistent chain instead of one launch each")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
@@ -229,6 +231,12 @@ def kernel_bytes(cls, s, B, ctx, eb=2, wb=2):
         return 2 * F * d * wb + sc(2 * F) + act(d) + B * F * 2 * 2
     if cls == "gemm_down":
         return d * F * wb + sc(d) + act(F) + 2 * B * d * 4
+    if cls == "gemm_chain":
+        # one launch per layer: O, gate/up and down, plus the next layer's
+        # QKV in all but the last layer's; the mean over the layers
+        L = s["n_layers"]
+        per = sum(kernel_bytes(k, s, B, ctx, eb, wb) for k in ("gemm_o", "gemm_gate_up", "gemm_down"))
+        return (L * per + (L - 1) * kernel_bytes("gemm_qkv", s, B, ctx, eb, wb)) / L
     if cls == "gemm_lm_head":
         return V * d * wb + sc(V) + act(d) + B * V * 4
     if cls == "attention":
@@ -391,6 +399,7 @@ def run_cbd(args):
     cbd.engine_set_rows_gemm(e, args.rows_gemm, args.rows_gemm_force)
     cbd.engine_set_attention_path(e, args.attn_path)
     cbd.engine_set_l2_prefetch(e, args.l2_prefetch_mb << 20)
+    cbd.engine_set_gemm_chain(e, args.gemm_chain)
     host_bits = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host_bits = {k: synth.bf16_bits(v) for k, v in w.items()}
@@ -575,7 +584,7 @@ def run_cbd(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 (int8 weights)" if i8 else "bf16", "data": "synthetic (seeded random-init weights, random bf16 KV)",
             "config": dict(config_of(args, s, wl, world), gemm_path=args.gemm_path, attn_path=args.attn_path,
-                           l2_prefetch_mb=args.l2_prefetch_mb),
+                           l2_prefetch_mb=args.l2_prefetch_mb, gemm_chain=args.gemm_chain),
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, "graph": graph, "sweep": sweep_out}
     if rank == 0:

@@ -110,6 +110,7 @@ PROTOS = {
     "cbd_engine_set_attention_path": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_l2_prefetch": (c_i32, [c_vp, c_u64]),
     "cbd_engine_set_fused_norm": (c_i32, [c_vp, c_i32]),
+    "cbd_engine_set_gemm_chain": (c_i32, [c_vp, c_i32]),
     "cbd_engine_set_forbidden": (c_i32, [c_vp, _P(c_i32), c_i32]),
     "cbd_engine_profile_read": (c_i32, [c_vp, _P(KernelStat), c_i32, _P(c_i32)]),
     "cbd_kv_pool_create": (c_i32, [c_vp, c_i32, _P(c_vp)]),
@@ -277,6 +278,11 @@ def engine_set_attention_path(e, path: int) -> None:
 def engine_set_fused_norm(e, enable: bool) -> None:
     """RMSNorm folded into the tensor-core GEMM epilogues (default on)."""
     _check(lib().cbd_engine_set_fused_norm(e, 1 if enable else 0))
+
+
+def engine_set_gemm_chain(e, enable: bool) -> None:
+    """Decode layers' O, gate/up, down and next-QKV contractions as one persistent launch (default off)."""
+    _check(lib().cbd_engine_set_gemm_chain(e, 1 if enable else 0))
 
 
 def engine_set_l2_prefetch(e, nbytes: int) -> None:

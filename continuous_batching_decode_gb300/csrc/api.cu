@@ -46,8 +46,9 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Kernel classes for cbd_engine_profile.
 static const char* kKernelClass[] = {"embed", "rmsnorm", "gemm_qkv", "attention", "gemm_o",
-                                     "gemm_gate_up", "gemm_down", "final_norm", "gemm_lm_head", "sampler"};
-enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, kcSamp, kcCount };
+                                     "gemm_gate_up", "gemm_down", "final_norm", "gemm_lm_head", "sampler",
+                                     "gemm_chain"};
+enum KClass { kcEmbed, kcNorm, kcQKV, kcAttn, kcO, kcGU, kcDown, kcFinal, kcLM, kcSamp, kcChain, kcCount };
 
 
 // ---------------------------------------------------------------- repack
@@ -358,7 +359,8 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
   const size_t o_fb = W.take((V + 31) / 32 * 4);
-  const size_t o_anext = W.take((size_t)dm.L * 4);
+  // per layer: the attention task counter, then the GEMM chain's barriers
+  const size_t o_anext = W.take((size_t)dm.L * (1 + kChainMaxPhases) * 4);
 
   e->work_bytes = W.off;
   cudaError_t e3 = cudaMalloc(&e->work, e->work_bytes);
@@ -381,6 +383,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->forbid = reinterpret_cast<uint32_t*>(wb + o_fb);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
   e->attn_next = reinterpret_cast<int32_t*>(wb + o_anext);
+  e->chain_sync = reinterpret_cast<uint32_t*>(wb + o_anext + (size_t)dm.L * 4);
 
   e3 = cudaMemset(e->work, 0, e->work_bytes);
   // ---- staging for cbd_step / cbd_sample
@@ -573,6 +576,14 @@ extern "C" cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable) {
   clear_error();
   if (!e) return fail(CBD_EINVAL, "engine is NULL");
   e->fuse_norm = enable != 0;
+  ++e->epoch;
+  return CBD_OK;
+}
+
+extern "C" cbd_status cbd_engine_set_gemm_chain(cbd_engine* e, int32_t enable) {
+  clear_error();
+  if (!e) return fail(CBD_EINVAL, "engine is NULL");
+  e->gemm_chain = enable != 0;
   ++e->epoch;
   return CBD_OK;
 }
@@ -1020,6 +1031,11 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   const GemmOp g_lm{e->lm_head, dm.V, dm.d, e->act_hi, e->act_lo, dm.d,
                     {&tm[4 * dm.L], &tm[a0 + 0], &tm[a0 + 1], dm.V, dm.d, e->tile_lm, e->lm_scale, e->lm_q}};
   const PfSpec pf_none{};
+  // Decode steps (one activation tile of rows) on the fused tcgen05 path
+  // run each layer's O, gate/up and down contractions and the next layer's
+  // QKV as one persistent launch with the same sums (k_gemm_chain.cu).
+  const bool chain = e->gemm_chain && fused && !e->w_int8 && n <= 64;
+  bool qkv_done = false;              // this layer's QKV ran inside the previous layer's chain
   for (int l = 0; l < dm.L; ++l) {
     const LayerDev& L = e->layers[l];
     qkv.layer = l;
@@ -1050,10 +1066,39 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
         return st;
       ++launches;
     }
-    if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, pf_none, s); }),
-                  "qkv")))
-      return st;
+    if (!qkv_done) {
+      if ((st = chk(timed(e, kcQKV, s, [&] { return launch_gemm(e, g_qkv, n, qkv, pf_none, s); }),
+                    "qkv")))
+        return st;
+      ++launches;
+    }
     if ((st = chk(timed(e, kcAttn, s, [&] { return launch_attention(e, p, b, l, pf_o, s); }), "attention"))) return st;
+    launches += attention_launches(e, b);
+    qkv_done = false;
+    if (chain) {
+      TcGemm cg[kChainMaxPhases] = {g_o.tc, g_gu.tc, g_dn.tc};
+      EpiArgs ce[kChainMaxPhases] = {res_o, glu, res_dn};
+      int np = 3;
+      if (l + 1 < dm.L) {
+        cg[3] = g_qkv_of(l + 1).tc;
+        ce[3] = qkv;
+        ce[3].layer = l + 1;
+        ce[3].n_parts_in = dn_parts;
+        np = 4;
+      }
+      // the next layer's QKV joins the chain only if its K split fits the
+      // chain's clusters; otherwise it runs on its own at the next layer
+      if (np == 4 && !gemm_chain_possible(cg, np, n)) np = 3;
+      if (gemm_chain_possible(cg, np, n)) {
+        uint32_t* sync = e->chain_sync + (size_t)l * kChainMaxPhases;
+        if ((st = chk(timed(e, kcChain, s, [&] { return launch_gemm_chain(cg, ce, np, n, sync, e->l2_prefetch, s); }),
+                      "gemm_chain")))
+          return st;
+        ++launches;
+        qkv_done = np == 4;
+        continue;
+      }
+    }
     if ((st = chk(timed(e, kcO, s, [&] { return launch_gemm(e, g_o, n, res_o, pf_gu, s); }),
                   "o_proj")))
       return st;
@@ -1069,7 +1114,7 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
     if ((st = chk(timed(e, kcDown, s, [&] { return launch_gemm(e, g_dn, n, res_dn, pf_after_dn, s); }),
                   "down")))
       return st;
-    launches += 4 + attention_launches(e, b);
+    launches += 3;
   }
   if (b->m > 0) {
     float* lg = out_logits ? out_logits : e->logits;

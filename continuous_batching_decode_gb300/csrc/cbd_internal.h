@@ -228,6 +228,7 @@ struct cbd_engine {
   float* attn_o = nullptr;            // [max_work][Hq][hd] partial outputs
   float* attn_ml = nullptr;           // [max_work][Hq][2] (max, sum)
   int32_t* attn_next = nullptr;       // [L] attention task counters, zeroed at the start of each step
+  uint32_t* chain_sync = nullptr;     // [L][kChainMaxPhases] GEMM-chain grid barriers, zeroed with attn_next
   int max_work = 0;
   float* logits = nullptr;            // [max_slots][V] internal logits
   float* samp_scratch = nullptr;      // [max_slots][V] sampler scratch
@@ -264,6 +265,7 @@ struct cbd_engine {
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   size_t l2_prefetch = 0;             // bytes of the next GEMM's weights each kernel prefetches to L2 (off)
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
+  bool gemm_chain = false;            // decode: O, gate/up, down and the next QKV as one persistent launch
   int gemv_max_rows = 0;              // auto: GEMV up to this many rows
   int rows_gemm_min = 512;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
   bool rows_gemm_force = false;       // ... for every GEMM of such a step, however it fills the GPU
@@ -420,6 +422,18 @@ bool gemm_rows_supports(const EpiArgs& ep);
 // the 128-row-tile kernel fills the GPU well enough for this GEMM and row count
 bool gemm_rows_preferred(const TcGemm& g, int n);
 cudaError_t launch_gemm_rows(const TcGemm& g, int n, const EpiArgs& ep, cudaStream_t s);
+// Persistent chain of up to kChainMaxPhases decode GEMMs in one launch
+// (k_gemm_chain.cu): the phases run in order, separated by grid barriers on
+// the counters sync[0 .. n_phases - 2] (zero at launch), each with the
+// per-launch kernel's K split and epilogue, so the sums are the same.
+// Possible for 1..64 rows, bf16 weights, 128- or 256-row tiles, K splits
+// of 1, 2 or 4 and at most as many CTAs as fit on the GPU at once.
+constexpr int kChainMaxPhases = 4;
+// pf_bytes: weights of each phase after the first prefetched into L2 (spread
+// over its CTAs) while the previous phase finishes; 0: none.
+bool gemm_chain_possible(const TcGemm* g, int n_phases, int n);
+cudaError_t launch_gemm_chain(const TcGemm* g, const EpiArgs* ep, int n_phases, int n, uint32_t* sync,
+                              size_t pf_bytes, cudaStream_t s);
 int gemm_tc_units(int M, int K, int N, int n);
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                    int n_items, const PfSpec& pf, cudaStream_t s);

@@ -8,14 +8,15 @@ namespace cbd {
 
 // x[r][:] = E[token_r][:] as fp32 (the residual stream starts at the
 // embedding row of the row's token).
-// CTA 0 also zeroes the step's per-layer attention task counters (every
+// CTA 0 also zeroes the step's counters (per layer: the attention task
+// counter and the GEMM chain's grid barriers, n_counters in all; every
 // kernel of the previous step has completed once this kernel passes its
 // dependency wait).
 // With g != null (fused RMSNorm of layer 0) it also writes split(x * g) to
 // norm_hi / norm_lo and the row's sum of x^2 (per-thread sums, then a fixed
 // tree) as the row's only partial in ssq.
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
-                             float* __restrict__ x, int32_t* __restrict__ attn_next, int n_layers,
+                             float* __restrict__ x, int32_t* __restrict__ counters, int n_counters,
                              const float* __restrict__ g, uint16_t* __restrict__ norm_hi,
                              uint16_t* __restrict__ norm_lo, float* __restrict__ ssq) {
   __shared__ float red[32];
@@ -25,7 +26,7 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
   TR_MARK1;
   const int r = blockIdx.x;
   if (r == 0)
-    for (int i = threadIdx.x; i < n_layers; i += blockDim.x) attn_next[i] = 0;
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const uint16_t* src = E + (size_t)rows[r].token * d;
   float* dst = x + (size_t)r * d;
   float ss = 0.f;
@@ -56,7 +57,8 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
 
 cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, const float* g, cudaStream_t s) {
   return launch_pdl(embed_kernel, dim3(b->n_rows), dim3(256), 0, s, (const uint16_t*)e->embed,
-                    (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L, g, e->norm_hi, e->norm_lo,
+                    (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L * (1 + kChainMaxPhases), g,
+                    e->norm_hi, e->norm_lo,
                     e->ssq);
 }
 

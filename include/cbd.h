@@ -228,6 +228,26 @@ cbd_status cbd_engine_set_forbidden(cbd_engine* e, const int32_t* ids, int32_t n
  * activations at different points).  Errors: CBD_EINVAL for a NULL engine. */
 cbd_status cbd_engine_set_fused_norm(cbd_engine* e, int32_t enable);
 
+/* Decode steps as persistent contraction chains (default off): on the
+ * tcgen05 path with the fused RMSNorm, bf16 weights and at most 64 rows,
+ * each layer's O, gate/up and down contractions and the next layer's QKV
+ * run as the phases of one launch, separated by grid-wide barriers instead
+ * of kernel boundaries, so each phase's first weight tiles stream while the
+ * previous phase's epilogue runs ("20.3 服务、批处理与流式", 20.3.2: a decode
+ * step costs (W + B*A)/beta, the time between weight streams is overhead).
+ * Every phase keeps the per-launch kernel's tiles, K split and epilogue:
+ * results are bit-identical with the setting on or off.  Shapes the chain
+ * does not cover (another tile width or K split, more CTAs than fit on the
+ * GPU at once) take the per-launch kernels.  enable != 0: on.  Off by
+ * default: on GB300 (7B shape, 32 rows) the chained step measured 5.43 ms
+ * against 4.73 ms launch by launch -- each phase boundary still costs ~10 us
+ * (the slowest CTA's tail, the exchange of partial sums and the grid
+ * barrier), and CTAs held to the end of the chain keep the next attention
+ * launch from starting early on their SMs.  cbd_engine_set_l2_prefetch also
+ * applies inside the chain (each phase's weights beyond the staged tiles).
+ * Errors: CBD_EINVAL for a NULL engine. */
+cbd_status cbd_engine_set_gemm_chain(cbd_engine* e, int32_t enable);
+
 /* L2 prefetch across kernel boundaries: once a kernel of the step has issued
  * its last load, it asks L2 to fetch the first k-blocks of the next weight
  * contraction's work units, up to `bytes` in all, so HBM could keep
