@@ -18,11 +18,17 @@
 // owns ids [r*V/kSC, (r+1)*V/kSC) and its warp w a contiguous part of that,
 // walked in coalesced 32-id rounds, so id-ordered prefix sums are a prefix
 // over the cluster's CTAs (read over distributed shared memory, rank order)
-// plus one over warps plus per-round warp scans.  Probability masses are
-// fixed-point integers (exp(z - zmax) * 2^40), so every sum, threshold and
-// scan is exact and independent of thread timing; the k-th largest key and
-// the top-p cutoff are found by 8-bit radix selection over order-preserving
-// 32-bit keys of z.
+// plus one over warps plus per-round warp scans.  A CTA keeps its ids' z in
+// shared memory (up to kZCache ids; beyond that they live in the scratch
+// row).  Probability masses are fixed-point integers (exp(z - zmax) * 2^40),
+// so every sum, threshold and scan is exact and independent of thread
+// timing.  The k-th largest key is found by 8-bit radix selection over
+// order-preserving 32-bit keys of z.  The top-p cutoff: 8-bit radix passes
+// over the same keys build the cluster's histograms of counts and masses
+// (the first pass also gives the total mass S) and narrow down the bucket
+// where the cumulative mass in descending key order reaches ceil(top_p * S);
+// as soon as that bucket holds at most kCandCap elements, they are gathered
+// from the cluster, sorted by (key desc, id asc) and scanned exactly.
 #include "common.cuh"
 
 namespace cbd {
@@ -52,12 +58,32 @@ __device__ __forceinline__ uint32_t ord_key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The float whose key ord_key gives (+0 for a zero).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
 
-// Radix histograms: every warp owns a private [256] count and mass
-// histogram in dynamic shared memory; the block then sums them bin by bin
-// in warp order (and the cluster over its CTAs in rank order).
+// Shared memory.  Radix histograms: every warp owns a private [256] count
+// and mass histogram; the block then sums them bin by bin in warp order (and
+// the cluster over its CTAs in rank order) -- no atomics, so no contention on
+// the few buckets most keys share.  Then the cutoff bucket's candidates.
 constexpr int kHistBins = 256;
-constexpr size_t kSampDynSmem = (size_t)(kST / 32) * kHistBins * (sizeof(uint32_t) + sizeof(unsigned long long));
+constexpr int kCandCap = 1024;        // candidates gathered and sorted exactly
+constexpr int kZCache = 16384;        // ids per CTA whose z stay in shared memory
+struct Cand {
+  uint32_t key;
+  int32_t id;
+  unsigned long long mass;
+};
+// dynamic layout: z [kZCache] f32 | counts [32][256] u32 | masses [32][256]
+// u64 | own candidates [kCandCap] | gathered candidates [kCandCap]
+constexpr size_t kSmZ = 0;
+constexpr size_t kSmHc = kSmZ + (size_t)kZCache * 4;
+constexpr size_t kSmHm = kSmHc + (size_t)(kST / 32) * kHistBins * 4;
+constexpr size_t kSmOwn = kSmHm + (size_t)(kST / 32) * kHistBins * 8;
+constexpr size_t kSmAll = kSmOwn + (size_t)kCandCap * sizeof(Cand);
+constexpr size_t kSampDynSmem = kSmAll + (size_t)kCandCap * sizeof(Cand);
+static_assert(kSampDynSmem + sizeof(unsigned long long) * 1024 <= 227 * 1024, "shared memory");
 
 // Add the participating lanes' (digit, mass) to this warp's histogram: the
 // lanes holding the same digit are one match group; its count is a popcount
@@ -80,7 +106,6 @@ __device__ __forceinline__ void warp_hist_add(bool part, uint32_t dg, unsigned l
   }
   if (leader) hc[dg] += __popc(grp);
 }
-
 struct SampShared {
   unsigned long long wsum[32];
   uint32_t wkey[32];
@@ -89,8 +114,9 @@ struct SampShared {
   uint32_t hc[256];
   unsigned long long chm[256];       // the cluster's histogram (rank order sum)
   uint32_t chc[256];
-  uint32_t sel_prefix, sel_mask;
-  unsigned long long sel_above, sel_rem;
+  uint32_t sel_prefix, sel_mask, sel_cnt, ncand;
+  int32_t sel_found;
+  unsigned long long sel_above, sel_rem, sel_target;
   int32_t tok;
   int32_t cut_id;
   unsigned long long cx;             // a value this CTA shares with its cluster
@@ -128,12 +154,13 @@ __device__ __forceinline__ void cluster_scan(unsigned long long x, SampShared& s
                                              unsigned long long* before, unsigned long long* total) {
   if (threadIdx.x == 0) sh.cx = x;
   csync();
-  unsigned long long b = 0, t = 0;
+  unsigned long long v[kSC], b = 0, t = 0;
+#pragma unroll
+  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) v[r] = cld_u64(&sh.cx, r);   // all loads in flight
 #pragma unroll
   for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
-    const unsigned long long v = cld_u64(&sh.cx, r);
-    if (r < my) b += v;
-    t += v;
+    if (r < my) b += v[r];
+    t += v[r];
   }
   csync();      // every peer has read sh.cx before it is written again
   *before = b;
@@ -144,12 +171,17 @@ __device__ __forceinline__ void cluster_scan(unsigned long long x, SampShared& s
 __device__ __forceinline__ void cluster_hist(SampShared& sh, bool masses) {
   csync();
   for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) {
-    uint32_t c = 0;
-    unsigned long long mm = 0;
+    uint32_t cv[kSC], c = 0;
+    unsigned long long mv[kSC], mm = 0;
+#pragma unroll
+    for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {     // all loads in flight, then the sums in rank order
+      cv[r] = cld_u32(&sh.hc[b], r);
+      mv[r] = masses ? cld_u64(&sh.hm[b], r) : 0ull;
+    }
 #pragma unroll
     for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
-      c += cld_u32(&sh.hc[b], r);
-      if (masses) mm += cld_u64(&sh.hm[b], r);
+      c += cv[r];
+      mm += mv[r];
     }
     sh.chc[b] = c;
     sh.chm[b] = mm;
@@ -160,9 +192,11 @@ __device__ __forceinline__ void cluster_hist(SampShared& sh, bool masses) {
 __device__ __forceinline__ int32_t cluster_min_i32(int32_t x, SampShared& sh) {
   if (threadIdx.x == 0) sh.cidx = x;
   csync();
-  int32_t m = 0x7fffffff;
+  int32_t v[kSC], m = 0x7fffffff;
 #pragma unroll
-  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) m = min(m, (int32_t)cld_u32(&sh.cidx, r));
+  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) v[r] = (int32_t)cld_u32(&sh.cidx, r);
+#pragma unroll
+  for (uint32_t r = 0; r < (uint32_t)kSC; ++r) m = min(m, v[r]);
   csync();
   return m;
 }
@@ -188,15 +222,16 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 // rounds of `src` before running the rounds' bodies in order: a pass costs a
 // few memory round trips instead of one per round.  f(v, valid, value) runs
 // on every lane for every round (so it may use ballots and shuffles).
+// Id v is read at src[v - off].
 constexpr int kRoundsAhead = 16;
 template <class F>
-__device__ __forceinline__ void for_each_id(const float* __restrict__ src, int v0, int v1, int lane, F&& f) {
+__device__ __forceinline__ void for_each_id(const float* src, int off, int v0, int v1, int lane, F&& f) {
   for (int base = v0; base < v1; base += 32 * kRoundsAhead) {
     float val[kRoundsAhead];
 #pragma unroll
     for (int u = 0; u < kRoundsAhead; ++u) {
       const int v = base + u * 32 + lane;
-      val[u] = v < v1 ? src[v] : 0.f;
+      val[u] = v < v1 ? src[v - off] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kRoundsAhead; ++u) {
@@ -204,6 +239,43 @@ __device__ __forceinline__ void for_each_id(const float* __restrict__ src, int v
       f(v, v < v1, val[u]);
     }
   }
+}
+
+// One warp over the 256 bins of a cluster histogram in descending digit
+// order (lane L holds digits 255 - 8L .. 248 - 8L): the first digit whose
+// running total, starting from `base`, reaches `need` (>= 1, so an empty
+// bin is never chosen), and the running total before it.  -1 (and the
+// grand total) if no digit reaches it.  v64 (masses) or v32 (counts).
+__device__ __forceinline__ int warp_first_reach(const unsigned long long* v64, const uint32_t* v32,
+                                                unsigned long long base, unsigned long long need, int lane,
+                                                unsigned long long* before) {
+  unsigned long long vals[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int d = 255 - 8 * lane - j;
+    vals[j] = v64 ? v64[d] : (unsigned long long)v32[d];
+    sum += vals[j];
+  }
+  const unsigned long long incl = warp_incl_scan_u64(sum, lane);
+  const unsigned bal = __ballot_sync(0xffffffffu, base + incl >= need);
+  if (!bal) {
+    *before = base + __shfl_sync(0xffffffffu, incl, 31);
+    return -1;
+  }
+  const int L = __ffs(bal) - 1;
+  int d = -1;
+  unsigned long long run = base + incl - sum;
+  if (lane == L) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (d < 0) {
+        if (run + vals[j] >= need) d = 255 - 8 * lane - j;
+        else run += vals[j];
+      }
+    }
+  }
+  *before = __shfl_sync(0xffffffffu, run, L);
+  return __shfl_sync(0xffffffffu, d, L);
 }
 
 // Exclusive prefix over the 32 warps of one value per warp (lane 0's value
@@ -235,8 +307,11 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       int32_t* __restrict__ out, int32_t* err) {
   __shared__ SampShared sh;
   extern __shared__ __align__(16) uint8_t samp_dyn[];
-  unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn);       // [32][256] masses
-  uint32_t* whc = reinterpret_cast<uint32_t*>(whm + (kST / 32) * kHistBins);       // [32][256] counts
+  float* zc = reinterpret_cast<float*>(samp_dyn + kSmZ);
+  uint32_t* whc = reinterpret_cast<uint32_t*>(samp_dyn + kSmHc);                       // [32][256] counts
+  unsigned long long* whm = reinterpret_cast<unsigned long long*>(samp_dyn + kSmHm);   // [32][256] masses
+  Cand* own = reinterpret_cast<Cand*>(samp_dyn + kSmOwn);
+  Cand* all = reinterpret_cast<Cand*>(samp_dyn + kSmAll);
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.x / kSC, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -244,7 +319,6 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   const SampDev sp = samp[row];
   const float* lg = logits + (size_t)row * V;
   float* cnt = counters + (size_t)slots[row] * V;
-  float* z = scratch + (size_t)row * V;
   // this CTA's ids [c0, c1); warp w's part of them [v0, v1)
   const int c0 = (int)((long long)V * my / kSC), c1 = (int)((long long)V * (my + 1) / kSC);
   const int PW = ((c1 - c0 + 32 * 32 - 1) / (32 * 32)) * 32;   // ids per warp, a multiple of 32
@@ -252,6 +326,10 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   const int v1 = min(c1, v0 + PW);
   const bool greedy = sp.temperature == 0.0f || sp.top_k == 1;
   const unsigned lt_mask = (1u << lane) - 1u;
+  // z of id v at zs[v - zoff]: shared memory, or the scratch row
+  const bool cached = c1 - c0 <= kZCache;
+  float* zs = cached ? zc : scratch + (size_t)row * V;
+  const int zoff = cached ? c0 : 0;
 
   // 1. penalty (and temperature); best key, lowest id on ties
   uint32_t bk = 0;
@@ -273,7 +351,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       const float l1 = __fsub_rn(lv[u], c > 0.0f ? sp.presence : 0.0f);
       const float l2 = __fsub_rn(l1, __fmul_rn(sp.frequency, c));
       const float val = greedy ? l2 : __fdiv_rn(l2, sp.temperature);
-      z[v] = val;
+      zs[v - zoff] = val;
       const uint32_t k = ord_key(val);
       if (bi == 0x7fffffff || k > bk) { bk = k; bi = v; }
     }
@@ -308,11 +386,12 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       if (oi != 0x7fffffff && (idx == 0x7fffffff || ok > k || (ok == k && oi < idx))) { k = ok; idx = oi; }
     }
     sh.tok = idx;
+    sh.sel_mask = k;         // the best key (z of the best id)
   }
   csync();
 
   if (!greedy) {
-    const float zmax = z[sh.tok];
+    const float zmax = key_float(sh.sel_mask);
     // 2. top-k: radix-select the k-th largest key; keep key > tk, and the
     //    lowest-id `need` elements with key == tk.
     if (sp.top_k > 0 && sp.top_k < V) {
@@ -321,7 +400,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < (kST / 32) * kHistBins; i += kST) whc[i] = 0;
         __syncthreads();
-        for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+        for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
           const uint32_t k = ord_key(zv);
           warp_hist_add(valid && (k & mask) == prefix, (k >> shift) & 255u, 0ull, whc + w * kHistBins, nullptr,
                         lane);
@@ -333,16 +412,19 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
           sh.hc[b] = c;
         }
         cluster_hist(sh, false);
-        if (tid == 0) {
-          unsigned long long cum = 0;
-          int d = 255;
-          for (; d > 0; --d) {
-            if (cum + sh.chc[d] >= rem) break;
-            cum += sh.chc[d];
+        if (w == 0) {
+          // the digit holding the rem-th largest key (descending digits)
+          unsigned long long cum;
+          int d = warp_first_reach(nullptr, sh.chc, 0ull, rem, lane, &cum);
+          if (d < 0) {       // cannot happen: rem <= the keys left; take digit 0
+            d = 0;
+            cum -= sh.chc[0];
           }
-          sh.sel_rem = rem - cum;
-          sh.sel_prefix = prefix | ((uint32_t)d << shift);
-          sh.sel_mask = mask | (255u << shift);
+          if (lane == 0) {
+            sh.sel_rem = rem - cum;
+            sh.sel_prefix = prefix | ((uint32_t)d << shift);
+            sh.sel_mask = mask | (255u << shift);
+          }
         }
         __syncthreads();
         prefix = sh.sel_prefix;
@@ -353,17 +435,17 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       const unsigned long long need_eq = rem;
       // rank among equal keys in id order
       unsigned long long eq = 0;
-      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { eq += valid && ord_key(zv) == tk; });
+      for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) { eq += valid && ord_key(zv) == tk; });
       unsigned long long tot, cbefore, ctot;
       unsigned long long base = warp_prefix(warp_sum_u64(eq), sh, &tot);
       cluster_scan(tot, sh, my, &cbefore, &ctot);
       base += cbefore;
-      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+      for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
         const uint32_t k = valid ? ord_key(zv) : 0u;
         const unsigned bal = __ballot_sync(0xffffffffu, valid && k == tk);
         if (valid) {
-          if (k < tk) z[v] = -INFINITY;
-          else if (k == tk && base + __popc(bal & lt_mask) >= need_eq) z[v] = -INFINITY;
+          if (k < tk) zs[v - zoff] = -INFINITY;
+          else if (k == tk && base + __popc(bal & lt_mask) >= need_eq) zs[v - zoff] = -INFINITY;
         }
         base += __popc(bal);
       });
@@ -376,65 +458,178 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       if (zv == -INFINITY) return 0ull;
       return __float2ull_rn(expf(zv - zmax) * kFix);
     };
-    // 4. top-p cutoff: shortest prefix by (key desc, id asc) with mass >= top_p * S
+    // 4. top-p cutoff: shortest prefix by (key desc, id asc) with mass >=
+    //    top_p * S; the first element past it is (tp, cut_id)
     bool use_cut = false;
     uint32_t tp = 0;
     int32_t cut_id = 0x7fffffff;
     if (sp.top_p < 1.0f) {
-      unsigned long long mine = 0;
-      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += mass(zv); });
-      unsigned long long S, Sb;
-      (void)warp_prefix(warp_sum_u64(mine), sh, &S);
-      cluster_scan(S, sh, my, &Sb, &S);
-      // cumulative mass >= top_p * S  <=>  cumulative >= ceil(top_p * S)
-      const unsigned long long target = (unsigned long long)ceil((double)sp.top_p * (double)S);
-      if (S >= target) {
-        use_cut = true;
-        uint32_t prefix = 0, mask = 0;
-        unsigned long long above = 0;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
-          __syncthreads();
-          for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
-            const uint32_t k = ord_key(zv);
-            const bool part = valid && zv != -INFINITY && (k & mask) == prefix;
-            warp_hist_add(part, (k >> shift) & 255u, part ? mass(zv) : 0ull, whc + w * kHistBins, whm + w * kHistBins,
-                          lane);
-          });
-          __syncthreads();
-          for (int b = tid; b < kHistBins; b += kST) {
-            uint32_t c = 0;
-            unsigned long long mm = 0;
-            for (int ww = 0; ww < kST / 32; ++ww) {
-              c += whc[ww * kHistBins + b];
-              mm += whm[ww * kHistBins + b];
-            }
-            sh.hc[b] = c;
-            sh.hm[b] = mm;
+      uint32_t prefix = 0, mask = 0, cnt_b = 0;
+      unsigned long long above = 0, target = 0;
+      // 4a. the bucket where the cumulative mass (descending keys) reaches
+      //     the target, 8 bits at a time while it holds more than kCandCap
+      //     elements; the first pass also gives the total mass S
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < (kST / 32) * kHistBins; i += kST) { whc[i] = 0; whm[i] = 0; }
+        __syncthreads();
+        for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
+          const uint32_t k = ord_key(zv);
+          const bool part = valid && zv != -INFINITY && (k & mask) == prefix;
+          warp_hist_add(part, (k >> shift) & 255u, part ? mass(zv) : 0ull, whc + w * kHistBins, whm + w * kHistBins,
+                        lane);
+        });
+        __syncthreads();
+        for (int b = tid; b < kHistBins; b += kST) {
+          uint32_t c = 0;
+          unsigned long long mm = 0;
+          for (int ww = 0; ww < kST / 32; ++ww) {
+            c += whc[ww * kHistBins + b];
+            mm += whm[ww * kHistBins + b];
           }
-          cluster_hist(sh, true);
-          if (tid == 0) {
-            int d = 255, last = -1;
-            for (; d >= 0; --d) {
-              if (sh.chc[d] == 0) continue;
-              last = d;
-              if (above + sh.chm[d] >= target) break;
-              above += sh.chm[d];
-            }
-            if (d < 0) d = last;        // rounding: take the lowest non-empty digit
-            sh.sel_rem = above;
-            sh.sel_prefix = prefix | ((uint32_t)d << shift);
-            sh.sel_mask = mask | (255u << shift);
-          }
-          __syncthreads();
-          prefix = sh.sel_prefix;
-          mask = sh.sel_mask;
-          above = sh.sel_rem;
+          sh.hc[b] = c;
+          sh.hm[b] = mm;
         }
+        cluster_hist(sh, true);
+        if (w == 0) {
+          if (shift == 24) {
+            // cumulative mass >= top_p * S  <=>  cumulative >= ceil(top_p * S)
+            unsigned long long S = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S += sh.chm[8 * lane + j];
+            S = warp_sum_u64(S);
+            const unsigned long long tg = (unsigned long long)ceil((double)sp.top_p * (double)S);
+            if (lane == 0) {
+              sh.sel_target = tg;
+              sh.sel_found = S >= tg;
+            }
+            __syncwarp();
+          }
+          if (sh.sel_found) {
+            // need >= 1: with a zero target the highest non-empty digit (it
+            // holds zmax, mass 2^40) is the one the cumulative reaches first
+            const unsigned long long tg = sh.sel_target;
+            const unsigned long long need = tg > above ? tg : above + 1;
+            unsigned long long bef;
+            int d = warp_first_reach(sh.chm, nullptr, above, need, lane, &bef);
+            if (d < 0) {      // cannot happen with exact sums: the lowest non-empty digit
+              d = 0;
+              while (d < 255 && sh.chc[d] == 0) ++d;
+              bef = above;
+            }
+            if (lane == 0) {
+              sh.sel_rem = bef;
+              sh.sel_prefix = prefix | ((uint32_t)d << shift);
+              sh.sel_cnt = sh.chc[d];
+            }
+          }
+        }
+        __syncthreads();
+        if (!sh.sel_found) break;      // S < target: no cutoff
+        use_cut = true;
+        target = sh.sel_target;
+        prefix = sh.sel_prefix;
+        mask |= 255u << shift;
+        above = sh.sel_rem;
+        cnt_b = sh.sel_cnt;
+        __syncthreads();
+        if (cnt_b <= (uint32_t)kCandCap) break;
+      }
+      if (use_cut && cnt_b <= (uint32_t)kCandCap) {
+        // 4b. the bucket's elements from the whole cluster, sorted by (key
+        //     desc, id asc); the first whose cumulative mass reaches the
+        //     target is the cutoff
+        if (tid == 0) sh.ncand = 0;
+        __syncthreads();
+        for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
+          const uint32_t k = ord_key(zv);
+          const bool part = valid && zv != -INFINITY && (k & mask) == prefix;
+          const unsigned bal = __ballot_sync(0xffffffffu, part);
+          uint32_t slot0 = 0;
+          if (lane == 0 && bal) slot0 = atomicAdd(&sh.ncand, (uint32_t)__popc(bal));
+          slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+          if (part) {
+            const uint32_t slot = slot0 + __popc(bal & lt_mask);
+            if (slot < (uint32_t)kCandCap) own[slot] = Cand{k, v, mass(zv)};
+          }
+        });
+        __syncthreads();
+        csync();
+        uint32_t nr[kSC], n = 0;
+#pragma unroll
+        for (uint32_t r = 0; r < (uint32_t)kSC; ++r) {
+          nr[r] = min(cld_u32(&sh.ncand, r), (uint32_t)kCandCap);
+          n += nr[r];
+        }
+        n = min(n, (uint32_t)kCandCap);
+        uint32_t n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        for (uint32_t i = tid; i < n2; i += kST) {
+          Cand c{0u, 0x7fffffff, 0ull};      // padding: after every real key
+          if (i < n) {
+            uint32_t r = 0, j = i;
+            while (r + 1 < (uint32_t)kSC && j >= nr[r]) { j -= nr[r]; ++r; }
+            const uint32_t a = cmap(&own[j], r);
+            uint32_t k, id, mlo, mhi;
+            asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(k), "=r"(id), "=r"(mlo), "=r"(mhi)
+                         : "r"(a)
+                         : "memory");
+            c = Cand{k, (int32_t)id, ((unsigned long long)mhi << 32) | mlo};
+          }
+          all[i] = c;
+        }
+        csync();      // every peer has read this CTA's candidates
+        // bitonic sort of [0, n2) into (key desc, id asc) order
+        for (uint32_t k2 = 2; k2 <= n2; k2 <<= 1) {
+          for (uint32_t j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+            for (uint32_t i = tid; i < n2; i += kST) {
+              const uint32_t l = i ^ j2;
+              if (l > i) {
+                const Cand a = all[i], b = all[l];
+                const bool b_first = b.key > a.key || (b.key == a.key && b.id < a.id);
+                if (((i & k2) == 0) == b_first) {
+                  all[i] = b;
+                  all[l] = a;
+                }
+              }
+            }
+            __syncthreads();
+          }
+        }
+        // cumulative masses in that order; the first that reaches the target
+        const unsigned long long q0 = 2 * tid < n ? all[2 * tid].mass : 0ull;
+        const unsigned long long q1 = 2 * tid + 1 < n ? all[2 * tid + 1].mass : 0ull;
+        const unsigned long long y = q0 + q1;
+        const unsigned long long yi = warp_incl_scan_u64(y, lane);
+        unsigned long long ytot;
+        const unsigned long long yincl = warp_prefix(__shfl_sync(0xffffffffu, yi, 31), sh, &ytot) + yi;
+        const unsigned long long yex = yincl - y;
+        if (tid == 0) sh.sel_found = 0;
+        __syncthreads();
+        const unsigned long long need = target > above ? target - above : 1ull;
+        int hit = -1;
+        if (2 * tid < n && yex < need && yex + q0 >= need) hit = 0;
+        else if (2 * tid + 1 < n && yex + q0 < need && yex + q0 + q1 >= need) hit = 1;
+        if (hit >= 0) {
+          sh.ckey = all[2 * tid + hit].key;
+          sh.cut_id = all[2 * tid + hit].id;
+          sh.sel_found = 1;
+        }
+        __syncthreads();
+        if (sh.sel_found) {
+          tp = sh.ckey;
+          cut_id = sh.cut_id;
+        } else {      // cannot happen with exact sums: keep the bucket's tie group
+          tp = n ? all[n - 1].key : prefix;
+          cut_id = V;
+        }
+      } else if (use_cut) {
+        // 4c. more than kCandCap elements share one key: among them, in
+        //     ascending id order, the first where the cumulative mass reaches
+        //     the target
         tp = prefix;
-        // among key == tp, ascending id: first id where above + cum >= target
         unsigned long long eqm = 0;
-        for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+        for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
           if (valid && zv != -INFINITY && ord_key(zv) == tp) eqm += mass(zv);
         });
         unsigned long long tot, cbefore, ctot;
@@ -447,7 +642,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
         if (above + wbase + wtot >= target) {   // the crossing may lie in this warp
           unsigned long long run = above + wbase;
           bool found = false;
-          for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+          for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
             if (found) return;
             const bool eqk = valid && zv != -INFINITY && ord_key(zv) == tp;
             const unsigned long long mv = eqk ? mass(zv) : 0ull;
@@ -481,7 +676,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
       return mass(zv);
     };
     unsigned long long mine = 0;
-    for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += kept_mass_z(v, zv); });
+    for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) { if (valid) mine += kept_mass_z(v, zv); });
     const unsigned long long wtot = warp_sum_u64(mine);
     unsigned long long Sk, cbefore;
     const unsigned long long wbase0 = warp_prefix(wtot, sh, &Sk);
@@ -493,7 +688,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
     if (wbase <= T && wbase + wtot > T) {
       unsigned long long run = wbase;
       bool found = false;
-      for_each_id(z, v0, v1, lane, [&](int v, bool valid, float zv) {
+      for_each_id(zs, zoff, v0, v1, lane, [&](int v, bool valid, float zv) {
         if (found) return;
         const unsigned long long mv = valid ? kept_mass_z(v, zv) : 0ull;
         const unsigned long long inc = warp_incl_scan_u64(mv, lane);
@@ -520,7 +715,7 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   // 6. counters: every CTA decays its ids, then the drawn token's owner
   //    counts it
   const int tok = sh.tok;
-  for_each_id(cnt, v0, v1, lane, [&](int v, bool valid, float c) { if (valid) cnt[v] = __fmul_rn(c, sp.decay); });
+  for_each_id(cnt, 0, v0, v1, lane, [&](int v, bool valid, float c) { if (valid) cnt[v] = __fmul_rn(c, sp.decay); });
   __syncthreads();
   if (tid == 0) {
     if (tok >= c0 && tok < c1) cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
