@@ -991,7 +991,8 @@ static cbd_status run_batch(cbd_engine* e, cbd_kv_pool* p, cbd_batch* b, int32_t
   // Fused RMSNorm on the tensor-core path: the embedding and the residual
   // epilogues write split(x * g) and per-row partial sums of x^2, and the
   // QKV / gate-up GEMMs apply 1/rms in their epilogues (no norm launches).
-  const int o_parts = gemm_tc_units(dm.d, hqd, e->tile_o, n), dn_parts = gemm_tc_units(dm.d, dm.F, e->tile_dn, n);
+  const int o_parts = gemm_tc_units(dm.d, hqd, e->tile_o, n, e->w_int8),
+            dn_parts = gemm_tc_units(dm.d, dm.F, e->tile_dn, n, e->w_int8);
   const bool fused = e->fuse_norm && gemm_uses_tc(e, n) && !gemm_uses_rows(e, n) && o_parts <= kMaxSsqParts && dn_parts <= kMaxSsqParts;
   cbd_status st;
   if ((st = chk(timed(e, kcEmbed, s, [&] { return launch_embed(e, b, fused ? e->layers[0].attn_norm : nullptr, s); }),

@@ -399,9 +399,13 @@ struct EpiArgs {
 cudaError_t launch_gemv(const uint16_t* W, int M, int K, int N, const uint16_t* a_hi, const uint16_t* a_lo, int lda,
                         int n, const EpiArgs& ep, cudaStream_t s);
 cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSpec& pf, cudaStream_t s);
-// The tcgen05 GEMM's work split for M x K weights and n rows: feature tiles,
-// row tiles, k-blocks and the cluster (K split) size.
-void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S);
+// The tcgen05 GEMM's work split for M x K weights and n rows, RT row tiles
+// of 64 per CTA: feature tiles, row tiles, k-blocks and the cluster (K
+// split) size.
+void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, int* S);
+// Row tiles per CTA the tcgen05 GEMM takes for n rows (2 above 64 rows with
+// bf16 weights, else 1).
+int gemm_tc_row_tiles(int n, bool int8);
 // Tile width (weight rows per tile) for an M x K weight matrix on this GPU.
 int gemm_tc_pick_tile(int M, int K);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
@@ -434,7 +438,7 @@ constexpr int kChainMaxPhases = 4;
 bool gemm_chain_possible(const TcGemm* g, int n_phases, int n);
 cudaError_t launch_gemm_chain(const TcGemm* g, const EpiArgs* ep, int n_phases, int n, uint32_t* sync,
                               size_t pf_bytes, cudaStream_t s);
-int gemm_tc_units(int M, int K, int N, int n);
+int gemm_tc_units(int M, int K, int N, int n, bool int8);
 cudaError_t launch_attn_stream_fp8(const cbd_engine* e, const cbd_kv_pool* p, const cbd_batch* b, int layer,
                                    int n_items, const PfSpec& pf, cudaStream_t s);
 // Prefill attention kernel (k_attn_pf.cu): query positions per block for a

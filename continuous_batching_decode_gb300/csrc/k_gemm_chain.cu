@@ -600,7 +600,7 @@ static bool chain_plan(const TcGemm* g, int n_phases, int n, ChainArgs* a, int* 
     ChainPhase& ph = a->ph[p];
     int NR;
     ph.N = g[p].N;
-    gemm_tc_plan(g[p].M, g[p].K, g[p].N, n, &ph.T, &NR, &ph.KB, &ph.S);
+    gemm_tc_plan(g[p].M, g[p].K, g[p].N, n, 1, &ph.T, &NR, &ph.KB, &ph.S);
     // the per-launch kernel's K split (so the same sums), one that divides
     // the cluster, at least one k-block per rank
     if ((ph.S != 1 && ph.S != 2 && ph.S != 4 && ph.S != 8) || ph.KB < ph.S || NR != 1) return false;

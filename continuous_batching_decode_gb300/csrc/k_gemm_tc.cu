@@ -31,6 +31,14 @@
 // depend on timing) and runs the epilogue.  No partials go to global memory
 // and no CTA waits on a flag.
 //
+// Two row tiles per CTA (RT = 2, bf16 weights, more than 64 rows): a stage
+// holds one weight tile and the activation tiles of rows 0-63 and 64-127,
+// and each k-step issues two MMAs into two TMEM accumulators (columns 0..N-1
+// and N..2N-1), so a weight tile is read once for 128 rows instead of once
+// per 64; the hi/lo fold runs in place over both, and phase 2 covers all 128
+// rows.  Per row the sums are those of the one-tile kernel with the same K
+// split.
+//
 // CTA = 10 warps: warp 0 issues TMA loads into a ring of shared-memory
 // stages; warp 1 owns TMEM and issues the MMAs (one thread); warps 2-9 read
 // the accumulator back (warp w owns TMEM lanes 32*(w%4)..+31, warps w and
@@ -177,9 +185,10 @@ __device__ __forceinline__ void epi_prefetch(const EpiArgs& ep, int S, int rank,
   }
 }
 
-template <int N>
+template <int N, int RT = 1>
 __host__ __device__ constexpr int tc_stages() {
-  return kTcRing / (N * kTcBK * 2 + kTcABytes) < kTcMaxStages ? kTcRing / (N * kTcBK * 2 + kTcABytes) : kTcMaxStages;
+  return kTcRing / (N * kTcBK * 2 + RT * kTcABytes) < kTcMaxStages ? kTcRing / (N * kTcBK * 2 + RT * kTcABytes)
+                                                                     : kTcMaxStages;
 }
 // Int8 weights: kConvBufs bf16 conversion buffers of N x 128 bytes, then
 // stages of (int8 tile, activation tile) in the rest of the ring.
@@ -211,19 +220,21 @@ __device__ __forceinline__ void i8x16_bf16(uint4 v, uint4& c0, uint4& c1) {
   c1 = make_uint4(i8pair_bf16x2(v.z, 0), i8pair_bf16x2(v.z, 2), i8pair_bf16x2(v.w, 0), i8pair_bf16x2(v.w, 2));
 }
 
-// One instantiation per tile width N (weight rows per tile, MMA N) and
-// weight type (I8: int8 weights with per-row scales).
-template <int N, bool I8>
+// One instantiation per tile width N (weight rows per tile, MMA N), weight
+// type (I8: int8 weights with per-row scales) and row tiles per CTA (RT).
+template <int N, bool I8, int RT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                    const __grid_constant__ CUtensorMap tmL, const TcArgs a, const EpiArgs ep, const PfSpec pf) {
   static_assert(N % 32 == 0 && N >= 64 && N <= kTcMaxBN, "tile width");
+  static_assert(RT == 1 || (RT == 2 && !I8), "two row tiles: bf16 weights");
   constexpr uint32_t idesc = tc::idesc_bf16(2 * kTcRows, N);
-  constexpr int ST = I8 ? tc_stages8<N>() : tc_stages<N>();
-  // bf16: a stage is (weight tile, activation tile); int8: (int8 tile,
+  constexpr int ST = I8 ? tc_stages8<N>() : tc_stages<N, RT>();
+  constexpr uint32_t tmem_cols = RT == 2 ? 2 * kTcMaxBN : kTcMaxBN;
+  // bf16: a stage is (weight tile, RT activation tiles); int8: (int8 tile,
   // activation tile), and the two bf16 conversion buffers follow the stages
   constexpr uint32_t w_bytes = (uint32_t)N * kTcBK * (I8 ? 1 : 2);   // one weight tile per stage
-  constexpr uint32_t stage_bytes = w_bytes + kTcABytes;
+  constexpr uint32_t stage_bytes = w_bytes + RT * kTcABytes;
   constexpr uint32_t conv_off = (uint32_t)ST * stage_bytes;          // int8: bf16 buffer b at conv_off + b * N * 128
   static_assert(!I8 || (conv_off % 1024 == 0 && conv_off + kConvBufs * N * 128u <= (uint32_t)kTcRing),
                 "int8 ring layout");
@@ -242,17 +253,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int decision;
-  __shared__ int2 rinfo[kTcRows];           // QKV epilogue: (position, KV block) of each tile row
-  __shared__ float rinv[kTcRows];           // fused RMSNorm consumer: 1/rms of each tile row
+  __shared__ int2 rinfo[kTcRows * RT];      // QKV epilogue: (position, KV block) of each tile row
+  __shared__ float rinv[kTcRows * RT];      // fused RMSNorm consumer: 1/rms of each tile row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  // unit = (feature tile t, row tile nr); the cluster's ranks split K
+  // unit = (feature tile t, row tiles nr .. nr + RT - 1); the cluster's
+  // ranks split K
   const int S = a.S;
   const int rank = S > 1 ? (int)cluster_rank() : 0;
   const int unit = blockIdx.x / S;
-  const int nr = unit % a.NR, t = unit / a.NR;
+  const int NP = (a.NR + RT - 1) / RT;
+  const int nr = (unit % NP) * RT, t = unit / NP;
+  const int rows_cta = min(kTcRows * RT, a.n - nr * kTcRows);   // activation rows of this CTA
   const int kb0 = rank * a.KB / S, kb1 = (rank + 1) * a.KB / S;
   const int n_it = kb1 - kb0;
 
@@ -279,7 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::prefetch_tmap(&tmL);
   }
   pdl_trigger();
-  if (warp == 1) tc::tmem_alloc(&tmem_base, kTcMaxBN);
+  if (warp == 1) tc::tmem_alloc(&tmem_base, tmem_cols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -295,8 +309,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // activation rows are loaded in 16-row boxes, only as many as the
       // tile has rows; the MMA rows past them read stale shared memory and
       // land in TMEM lanes the epilogue never reads
-      const int nbox = (min(kTcRows, a.n - nr * kTcRows) + 15) / 16;
-      const uint32_t stage_tx = w_bytes + 2u * nbox * 2048u;
+      const int nbox = (min(kTcRows, rows_cta) + 15) / 16;
+      const int nbox1 = RT == 2 ? (max(0, rows_cta - kTcRows) + 15) / 16 : 0;   // second row tile
+      const uint32_t stage_tx = w_bytes + 2u * (nbox + nbox1) * 2048u;
       const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
       auto issue_w = [&](int q) {
         const int s = q % ST;
@@ -318,6 +333,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < nbox; ++j) {
           tc::tma_load_2d(st + j * 2048, &tmH, kx, nr * kTcRows + j * 16, &full_bar[s]);
           tc::tma_load_2d(st + kTcABytes / 2 + j * 2048, &tmL, kx, nr * kTcRows + j * 16, &full_bar[s]);
+        }
+        for (int j = 0; j < nbox1; ++j) {
+          tc::tma_load_2d(st + kTcABytes + j * 2048, &tmH, kx, (nr + 1) * kTcRows + j * 16, &full_bar[s]);
+          tc::tma_load_2d(st + kTcABytes + kTcABytes / 2 + j * 2048, &tmL, kx, (nr + 1) * kTcRows + j * 16,
+                          &full_bar[s]);
         }
       };
       // weights do not depend on the previous kernel: start streaming them
@@ -352,6 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
+      const bool two = RT == 2 && rows_cta > kTcRows;    // the second row tile has rows
       for (int q = 0; q < n_it; ++q) {
         const int s = q % ST;
         if constexpr (I8)
@@ -365,6 +386,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes along K inside the swizzled rows
           tc::mma_bf16(tmem, dA + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
+        if (RT == 2 && two) {
+          const uint64_t dA1 = tc::sdesc_sw128(st + w_bytes + kTcABytes);
+#pragma unroll
+          for (int k = 0; k < kTcBK / 16; ++k)
+            tc::mma_bf16(tmem + (uint32_t)N, dA1 + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
+        }
         tc::mma_commit(&empty_bar[s]);
         if constexpr (I8) tc::mma_commit(&conv_free[q % kConvBufs]);
       }
@@ -386,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // column halves on 32-column boundaries
     constexpr int c_mid = ((N / 2 + 31) / 32) * 32;
     const int c_lo = (warp - 2) < 4 ? 0 : c_mid, c_hi = (warp - 2) < 4 ? c_mid : N;
-    const int rows_here = min(kTcRows, a.n - nr * kTcRows);
+    const int rows_here = rows_cta;
     const int rl = (lg & 1) * 32 + lane;           // tile row of this lane
     const bool has_rows = (lg & 1) * 32 < rows_here;
     const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16);
@@ -520,6 +547,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) { v[j] = __uint_as_float(x0[j]); v[32 + j] = two ? __uint_as_float(x1[j]) : 0.f; }
     };
+    if constexpr (RT == 2) {
+      // both accumulators, in place: P [128][PS]; the lo warps store their
+      // lanes, then the hi warps add their own to them (hi + lo per element)
+      for (int pass = 0; pass < 2; ++pass) {
+        if ((pass == 0) == (lg >= 2)) {
+#pragma unroll 1
+          for (int acc = 0; acc < 2; ++acc) {
+            if (acc * kTcRows + (lg & 1) * 32 >= rows_here) continue;
+            float* prow = P + (acc * kTcRows + rl) * PS;
+#pragma unroll 1
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+              uint32_t x[32];
+              if (!skip) {
+                tc::tmem_ld32_nowait(taddr + (uint32_t)(acc * N + c0), x);
+                tc::tmem_wait_ld();
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = 0u;
+              }
+              float4* dst = reinterpret_cast<float4*>(prow + c0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float4 v = make_float4(__uint_as_float(x[4 * j]), __uint_as_float(x[4 * j + 1]),
+                                       __uint_as_float(x[4 * j + 2]), __uint_as_float(x[4 * j + 3]));
+                if (pass == 1) {
+                  const float4 l4 = dst[j];
+                  v = make_float4(v.x + l4.x, v.y + l4.y, v.z + l4.z, v.w + l4.w);
+                }
+                dst[j] = v;
+              }
+            }
+          }
+        }
+        if (pass == 0) asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      }
+    } else {
     if (lg >= 2 && has_rows) {
 #pragma unroll 1
       for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
@@ -549,6 +612,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
       }
     }
+    }
 #ifdef CBD_TRACE
     _e1 = gtimer();
 #endif
@@ -564,9 +628,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp >= 2) {
     // ------------------------------------------------ epilogue phase 2: reduce over ranks, finish
     const int et = threadIdx.x - 64;
-    const int rows_here = min(kTcRows, a.n - nr * kTcRows);
+    const int rows_here = rows_cta;
     const uint32_t Pbase = tc::smem_u32(ring);
-    float* sq = reinterpret_cast<float*>(ring + 64 * PS * 4);   // the LO area, free after phase 1
+    // the residual-norm sums: after P (the LO area, free after phase 1, when RT = 1)
+    float* sq = reinterpret_cast<float*>(ring + kTcRows * RT * PS * 4);
     switch (ep.kind) {
       case kEpiQKV: epi_phase2<kEpiQKV, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
       case kEpiResid: epi_phase2<kEpiResid, N, I8>(ep, S, rank, t, nr, rows_here, et, Pbase, rinfo, rinv, sq); break;
@@ -589,7 +654,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   TR_END((16u << 12) | (unsigned)(a.M >> 8));
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, kTcMaxBN);
+    tc::tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -644,10 +709,11 @@ static int max_clusters(int S) {
   static int cache[kMaxDevices][kTcMaxCluster + 1] = {};
   int dev = -1;
   const cudaError_t ce = once.run([](int d) -> cudaError_t {
-    for (auto k : {gemm_tc_kernel<256, false>, gemm_tc_kernel<224, false>, gemm_tc_kernel<192, false>,
-                   gemm_tc_kernel<160, false>, gemm_tc_kernel<128, false>, gemm_tc_kernel<256, true>,
-                   gemm_tc_kernel<224, true>, gemm_tc_kernel<192, true>, gemm_tc_kernel<160, true>,
-                   gemm_tc_kernel<128, true>}) {
+    for (auto k : {gemm_tc_kernel<256, false, 1>, gemm_tc_kernel<224, false, 1>, gemm_tc_kernel<192, false, 1>,
+                   gemm_tc_kernel<160, false, 1>, gemm_tc_kernel<128, false, 1>, gemm_tc_kernel<256, true, 1>,
+                   gemm_tc_kernel<224, true, 1>, gemm_tc_kernel<192, true, 1>, gemm_tc_kernel<160, true, 1>,
+                   gemm_tc_kernel<128, true, 1>, gemm_tc_kernel<256, false, 2>, gemm_tc_kernel<224, false, 2>,
+                   gemm_tc_kernel<192, false, 2>, gemm_tc_kernel<160, false, 2>, gemm_tc_kernel<128, false, 2>}) {
       const cudaError_t e1 = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
       if (e1 != cudaSuccess) return e1;
     }
@@ -664,7 +730,7 @@ static int max_clusters(int S) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN, false>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kTcMaxBN, false, 1>, &cfg) != cudaSuccess) {
         n = 0;
         cudaGetLastError();
       }
@@ -695,11 +761,13 @@ static int choose_cluster(long long U, int KB) {
   return best;
 }
 
-void gemm_tc_plan(int M, int K, int N, int n, int* T, int* NR, int* KB, int* S) {
+int gemm_tc_row_tiles(int n, bool int8) { return !int8 && n > kTcRows ? 2 : 1; }
+
+void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, int* S) {
   *T = M / N;
   *NR = (n + kTcRows - 1) / kTcRows;
   *KB = K / kTcBK;
-  *S = choose_cluster((long long)*T * *NR, *KB);
+  *S = choose_cluster((long long)*T * ((*NR + RT - 1) / RT), *KB);
 }
 
 // Weight rows per tile for an M x K matrix: the widest tile that divides M,
@@ -726,9 +794,10 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   a.M = g.M; a.K = g.K; a.n = n; a.N = g.N;
   a.w8 = g.w8;
   if (g.scale && !g.w8) return cudaErrorInvalidValue;
-  gemm_tc_plan(g.M, g.K, g.N, n, &a.T, &a.NR, &a.KB, &a.S);
+  const int RT = gemm_tc_row_tiles(n, g.scale != nullptr);
+  gemm_tc_plan(g.M, g.K, g.N, n, RT, &a.T, &a.NR, &a.KB, &a.S);
   a.err = ep.err;
-  const long long U = (long long)a.T * a.NR;
+  const long long U = (long long)a.T * ((a.NR + RT - 1) / RT);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(U * a.S));
   cfg.blockDim = dim3(kTcThreads);
@@ -749,19 +818,20 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   cfg.attrs = at;
   cfg.numAttrs = na;
   if (max_clusters(1) <= 0) return cudaErrorInvalidConfiguration;   // also sets the shared-memory limit
+  // bf16 weights: RT row tiles per CTA; int8: one
+#define CBD_TC_LAUNCH(NN)                                                                                  \
+  return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, true, 1>, *g.w, *g.hi, *g.lo, a, ep, pf)    \
+                 : (RT == 2 ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, false, 2>, *g.w, *g.hi, *g.lo, a, ep, pf) \
+                            : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, false, 1>, *g.w, *g.hi, *g.lo, a, ep, pf))
   switch (g.N) {
-    case 256: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
-                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<256, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 224: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
-                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<224, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 192: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
-                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<192, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 160: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
-                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<160, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
-    case 128: return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128, true>, *g.w, *g.hi, *g.lo, a, ep, pf)
-                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<128, false>, *g.w, *g.hi, *g.lo, a, ep, pf);
+    case 256: CBD_TC_LAUNCH(256);
+    case 224: CBD_TC_LAUNCH(224);
+    case 192: CBD_TC_LAUNCH(192);
+    case 160: CBD_TC_LAUNCH(160);
+    case 128: CBD_TC_LAUNCH(128);
     default: return cudaErrorInvalidValue;
   }
+#undef CBD_TC_LAUNCH
 }
 
 CBD_TRACE_BIND(gemm_tc)

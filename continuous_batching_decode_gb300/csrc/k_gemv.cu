@@ -129,9 +129,9 @@ bool gemm_uses_tc(const cbd_engine* e, int n) { return uses_tc(e, n); }
 bool gemm_uses_rows(const cbd_engine* e, int n) {
   return !e->w_int8 && uses_tc(e, n) && e->rows_gemm_min > 0 && n >= e->rows_gemm_min;
 }
-int gemm_tc_units(int M, int K, int N, int n) {
+int gemm_tc_units(int M, int K, int N, int n, bool int8) {
   int T, NR, KB, S;
-  gemm_tc_plan(M, K, N, n, &T, &NR, &KB, &S);
+  gemm_tc_plan(M, K, N, n, gemm_tc_row_tiles(n, int8), &T, &NR, &KB, &S);
   return T * S;
 }
 
@@ -155,7 +155,7 @@ PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n) {
   PfSpec pf{};
   if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n) || e->w_int8) return pf;
   int T, NR, KB, S;
-  gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N, n, &T, &NR, &KB, &S);
+  gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N, n, gemm_tc_row_tiles(n, false), &T, &NR, &KB, &S);
   const long long units = (long long)T * S;
   const long long per_unit = (KB + S - 1) / S;
   long long P = (long long)(e->l2_prefetch / ((size_t)op.tc.N * 128)) / units;
