@@ -192,13 +192,15 @@ cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
  * weight tile feeds 128 rows per pass instead of 64, and two TMEM
  * accumulators overlap one tile's epilogue with the next tile's mainloop;
  * such a step runs the RMSNorm as its own kernel.  With
- * force == 0 a GEMM takes this kernel only where its units fill at least
- * half of the last wave of resident CTAs (else the 64-row-tile kernel,
- * which splits K); with force != 0 every GEMM of the step takes it.  Same
- * sums as the other paths, in another order.  min_rows 0 = never.
- * Default 512 (below it the 64-row-tile kernel with the fused RMSNorm was
- * faster on the 7B shape: 18.36 vs 19.12 ms at 416 rows; 21.46 vs 19.84 ms
- * the other way at 544), force 0.  CBD_EINVAL if min_rows < 0. */
+ * force == 0 a GEMM takes this kernel only where its weights are tiled 128
+ * rows wide and its units fill at least half of the last wave of resident
+ * CTAs (else the 64-row-tile kernel, which takes two row tiles per CTA and
+ * splits K); with force != 0 every GEMM of the step takes it.  Same sums as
+ * the other paths, in another order.  min_rows 0 = never.  Default 640
+ * (7B shape on GB300: 22.54 vs 23.00 ms at 544 rows with the 64-row-tile
+ * kernel and the fused RMSNorm; 29.98 vs 33.91 ms and 53.98 vs 62.22 ms
+ * the other way at 1056 and 2080 rows), force 0.  CBD_EINVAL if
+ * min_rows < 0. */
 cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force);
 
 /* Choose the attention kernel: 0 = persistent streaming kernel (each warp
