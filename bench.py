@@ -501,35 +501,78 @@ def run_cbd(args):
     kernels = {k: {"launches": v[0], "ms_per_step": round(v[1] / args.steps, 4),
                    "share": round(v[1] / sum(x[1] for x in prof.values()), 4)} for k, v in prof.items()}
 
-    # end to end through cbd_step: host arrays in, tokens out, every step
+    # end to end through cbd_step: host arrays in, tokens out, every step.
+    # The inputs are marshalled once into the C layout (cbd.rows_table /
+    # sampling_table); every step then writes the tokens the previous step
+    # drew into the rows, as a decode loop does (positions stay fixed, so
+    # every step does the same work).
     e2e = None
     if not args.no_e2e:
         host_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
+        rows_t = cbd.rows_table(wl["rows"])
+        samp_t = cbd.sampling_table(wl["samp"])
+        tables_t = np.ascontiguousarray(wl["tables"], dtype=np.int32)
+        nbps_t = np.ascontiguousarray(wl["nbps"], dtype=np.int32)
+        tok_np = host_tok.numpy()
+
+        def one_step():
+            cbd.step(e, pool, rows_t, tables_t, nbps_t, samp_t, None, out)
+            host_tok.copy_(out, non_blocking=True)
+            stream.synchronize()
+            rows_t["token"] = tok_np
+            samp_t["token_index"] += 1
 
         def e2e_ms():
             for _ in range(3):
-                cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
-                host_tok.copy_(out, non_blocking=True)
+                one_step()
             torch.cuda.synchronize()
             if dist:
                 dist.barrier()
             t0 = time.perf_counter()
             ev0.record(stream)
             for _ in range(args.steps):
-                cbd.step(e, pool, wl["rows"], wl["tables"], wl["nbps"], wl["samp"], None, out)
-                host_tok.copy_(out, non_blocking=True)
-                stream.synchronize()
+                one_step()
             ev1.record(stream)
             torch.cuda.synchronize()
             wall = (time.perf_counter() - t0) / args.steps * 1000.0
             return replicas.max_over_ranks(max(ev0.elapsed_time(ev1) / args.steps, wall), dist, "cuda")
         lbl_ms = e2e_ms()                       # launch by launch
         cbd.engine_set_step_graph(e, True)      # each cbd_step as one cached graph
-        e_ms = e2e_ms()
+        sync_ms = e2e_ms()
+
+        # Pipelined decode loop: rows carry CBD_TOKEN_LAST (each slot's
+        # last drawn token, read on the device), so the host enqueues step
+        # k + 1 without waiting for step k's tokens; every step's tokens are
+        # still copied back, asynchronously, into a pinned ring.
+        rows_last = rows_t.copy()
+        rows_last["token"] = cbd.TOKEN_LAST
+        ring = torch.zeros(args.steps, B, dtype=torch.int32).pin_memory()
+
+        def pipelined_ms():
+            for _ in range(3):
+                one_step()                      # explicit tokens: every slot has a last token
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            t0 = time.perf_counter()
+            ev0.record(stream)
+            for k in range(args.steps):
+                cbd.step(e, pool, rows_last, tables_t, nbps_t, samp_t, None, out)
+                ring[k].copy_(out, non_blocking=True)
+                samp_t["token_index"] += 1
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            wall = (time.perf_counter() - t0) / args.steps * 1000.0
+            return replicas.max_over_ranks(max(ev0.elapsed_time(ev1) / args.steps, wall), dist, "cuda")
+        e_ms = pipelined_ms()
         cbd.engine_set_step_graph(e, False)
         h2d = len(wl["rows"]) * 20 + wl["tables"].nbytes + wl["nbps"].nbytes + len(wl["samp"]) * 48
         e2e = {"value": B * world / (e_ms / 1000.0), "unit": "tok/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": B * 4, "ms_per_step": round(e_ms, 4), "step_graph": True,
+               "loop": "pipelined: each step's rows take the slot's last drawn token on the device "
+                       "(CBD_TOKEN_LAST) and its tokens are copied back asynchronously; positions fixed",
+               "sync_loop": {"value": B * world / (sync_ms / 1000.0), "ms_per_step": round(sync_ms, 4),
+                             "loop": "tokens read back and fed in from the host before the next step"},
                "launch_by_launch_ms_per_step": round(lbl_ms, 4)}
         cbd.engine_check(e)
 

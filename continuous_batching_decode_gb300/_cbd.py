@@ -47,6 +47,9 @@ class Weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(LayerWeights))]
 
 
+TOKEN_LAST = -1       # cbd_row.token: the token the engine last sampled for the row's slot
+
+
 class Row(ctypes.Structure):
     _fields_ = [("slot", c_i32), ("token", c_i32), ("pos", c_i32), ("is_prefill", c_i32), ("sample", c_i32)]
 
@@ -323,6 +326,68 @@ def kv_pool_data(p):
 
 
 # ------------------------------------------------------------------ step
+# NumPy views of cbd_row and cbd_sampling with the C layout: a caller may
+# build its step inputs once as such arrays and update fields in place
+# (tokens, positions, token_index) instead of passing Python tuples and
+# dicts that are converted on every call.
+ROW_DTYPE = np.dtype({"names": [n for n, _ in Row._fields_],
+                      "formats": ["<i4"] * 5,
+                      "offsets": [getattr(Row, n).offset for n, _ in Row._fields_],
+                      "itemsize": ctypes.sizeof(Row)})
+SAMPLING_DTYPE = np.dtype({"names": [n for n, _ in Sampling._fields_],
+                           "formats": ["<f4", "<f4", "<i4", "<f4", "<f4", "<f4", "<u8", "<u8", "<u4", "<u4"],
+                           "offsets": [getattr(Sampling, n).offset for n, _ in Sampling._fields_],
+                           "itemsize": ctypes.sizeof(Sampling)})
+
+
+def rows_table(rows) -> np.ndarray:
+    """rows as a ROW_DTYPE array (a copy; fields may then be updated in place)."""
+    a = np.zeros(len(rows), ROW_DTYPE)
+    for i, r in enumerate(rows):
+        a[i] = tuple(int(v) for v in r)
+    return a
+
+
+def sampling_table(params) -> np.ndarray:
+    """Sampling dicts as a SAMPLING_DTYPE array (missing fields -> defaults)."""
+    params = list(params)
+    a = np.zeros(max(1, len(params)), SAMPLING_DTYPE)
+    for i, p in enumerate(params):
+        a[i] = (float(p.get("temperature", 0.0)), float(p.get("top_p", 1.0)), int(p.get("top_k", 0)),
+                float(p.get("presence_penalty", 0.0)), float(p.get("frequency_penalty", 0.0)),
+                float(p.get("penalty_decay", 1.0)), int(p.get("seed", 0)), int(p.get("request_id", 0)),
+                int(p.get("token_index", 0)), 0)
+    return a if params else a[:0]
+
+
+def _rows_arg(rows):
+    """(keep-alive, pointer, count) for cbd_row inputs: a ROW_DTYPE array or a
+    ctypes Row array as they are, anything else converted."""
+    if isinstance(rows, np.ndarray):
+        if rows.dtype != ROW_DTYPE:
+            raise TypeError(f"rows array dtype {rows.dtype} is not ROW_DTYPE")
+        a = np.ascontiguousarray(rows)
+        return a, a.ctypes.data_as(_P(Row)), len(a)
+    if isinstance(rows, ctypes.Array) and rows._type_ is Row:
+        return rows, rows, len(rows)
+    ra = rows_array(rows)
+    return ra, ra, len(ra)
+
+
+def _sampling_arg(params):
+    if isinstance(params, np.ndarray):
+        if params.dtype != SAMPLING_DTYPE:
+            raise TypeError(f"sampling array dtype {params.dtype} is not SAMPLING_DTYPE")
+        a = np.ascontiguousarray(params)
+        if len(a) == 0:
+            a = np.zeros(1, SAMPLING_DTYPE)
+        return a, a.ctypes.data_as(_P(Sampling))
+    if isinstance(params, ctypes.Array) and params._type_ is Sampling:
+        return params, params
+    sa = sampling_array(params)
+    return sa, sa
+
+
 def rows_array(rows) -> ctypes.Array:
     """rows: iterable of (slot, token, pos, is_prefill, sample)."""
     rows = [tuple(int(v) for v in r) for r in rows]
@@ -359,26 +424,27 @@ def _f32(a):
 def step(e, pool, rows, block_tables, n_blocks_per_slot, sampling, uniforms, out_tokens, out_logits=None,
          stream=None) -> None:
     """One batched step.  rows: (slot, token, pos, is_prefill, sample)
-    tuples; block_tables [S][max_blocks_per_seq] int32; n_blocks_per_slot [S];
-    sampling: one dict per sampled row (row order); uniforms: None or [m]
-    floats; out_tokens / out_logits: device tensors (int32 [m], fp32 [m][V])."""
-    ra = rows_array(rows)
+    tuples, or a ROW_DTYPE / ctypes Row array; block_tables [S][max_blocks_per_seq] int32;
+    n_blocks_per_slot [S]; sampling: one dict per sampled row (row order), or
+    a SAMPLING_DTYPE / ctypes Sampling array; uniforms: None or [m] floats;
+    out_tokens / out_logits: device tensors (int32 [m], fp32 [m][V])."""
+    ra, rp, nr = _rows_arg(rows)
     bt, btp = _i32(block_tables)
     nb, nbp = _i32(n_blocks_per_slot)
-    sa = sampling_array(sampling)
+    sa, sp = _sampling_arg(sampling)
     ua, uap = _f32(uniforms)
-    _check(lib().cbd_step(e, pool, ra, len(ra), btp, int(bt.shape[0]), nbp, sa, uap, _ptr(out_tokens),
+    _check(lib().cbd_step(e, pool, rp, nr, btp, int(bt.shape[0]), nbp, sp, uap, _ptr(out_tokens),
                           _ptr(out_logits), _stream(stream)))
 
 
 def batch_create(e, pool, rows, block_tables, n_blocks_per_slot, sampling, uniforms=None, stream=None):
-    ra = rows_array(rows)
+    ra, rp, nr = _rows_arg(rows)
     bt, btp = _i32(block_tables)
     nb, nbp = _i32(n_blocks_per_slot)
-    sa = sampling_array(sampling)
+    sa, sp = _sampling_arg(sampling)
     ua, uap = _f32(uniforms)
     out = c_vp()
-    _check(lib().cbd_batch_create(e, pool, ra, len(ra), btp, int(bt.shape[0]), nbp, sa, uap, ctypes.byref(out),
+    _check(lib().cbd_batch_create(e, pool, rp, nr, btp, int(bt.shape[0]), nbp, sp, uap, ctypes.byref(out),
                                   _stream(stream)))
     return out.value
 

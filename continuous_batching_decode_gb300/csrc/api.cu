@@ -359,6 +359,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
   const size_t o_fb = W.take((V + 31) / 32 * 4);
+  const size_t o_last = W.take(S * 4);
   // per layer: the attention task counter, then the GEMM chain's barriers
   const size_t o_anext = W.take((size_t)dm.L * (1 + kChainMaxPhases) * 4);
 
@@ -381,6 +382,7 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   e->samp_scratch = reinterpret_cast<float*>(wb + o_sc);
   e->counters = reinterpret_cast<float*>(wb + o_cn);
   e->forbid = reinterpret_cast<uint32_t*>(wb + o_fb);
+  e->last_tok = reinterpret_cast<int32_t*>(wb + o_last);
   e->err = reinterpret_cast<int32_t*>(wb + o_err);
   e->attn_next = reinterpret_cast<int32_t*>(wb + o_anext);
   e->chain_sync = reinterpret_cast<uint32_t*>(wb + o_anext + (size_t)dm.L * 4);
@@ -673,6 +675,7 @@ extern "C" cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream) 
   if (slot < 0 || slot >= e->dm.max_slots) return fail(CBD_EINVAL, "slot %d out of range", slot);
   CBD_CUDA(cudaMemsetAsync(e->counters + (size_t)slot * e->dm.V, 0, (size_t)e->dm.V * 4,
                            static_cast<cudaStream_t>(stream)));
+  CBD_CUDA(cudaMemsetAsync(e->last_tok + slot, 0, 4, static_cast<cudaStream_t>(stream)));
   return CBD_OK;
 }
 
@@ -741,7 +744,11 @@ cbd_status build_batch_image(const cbd_engine* e, const cbd_kv_pool* pool, const
   for (int32_t r = 0; r < n_rows; ++r) {
     const cbd_row& w = rows[r];
     if (w.slot < 0 || w.slot >= table_slots) return fail(CBD_EINVAL, "row %d: slot %d out of range", r, w.slot);
-    if (w.token < 0 || w.token >= dm.V) return fail(CBD_EINVAL, "row %d: token %d out of range", r, w.token);
+    if (w.token == CBD_TOKEN_LAST) {
+      if (w.is_prefill) return fail(CBD_EINVAL, "row %d: CBD_TOKEN_LAST on a prefill row", r);
+    } else if (w.token < 0 || w.token >= dm.V) {
+      return fail(CBD_EINVAL, "row %d: token %d out of range", r, w.token);
+    }
     const int32_t nb = nbps[w.slot];
     if (nb < 1 || nb > mbps) return fail(CBD_EINVAL, "slot %d: n_blocks %d not in [1, %d]", w.slot, nb, mbps);
     if (w.pos < 0 || w.pos >= nb * kBlock)

@@ -233,6 +233,7 @@ struct cbd_engine {
   float* logits = nullptr;            // [max_slots][V] internal logits
   float* samp_scratch = nullptr;      // [max_slots][V] sampler scratch
   float* counters = nullptr;          // [max_slots][V]
+  int32_t* last_tok = nullptr;        // [max_slots] the token last sampled for each slot (CBD_TOKEN_LAST)
   uint32_t* forbid = nullptr;         // [ceil(V/32)] bitmap of token ids the sampler never draws
   int32_t n_forbidden = 0;            // ids set in `forbid` (0: mask off)
   int32_t* err = nullptr;             // device error word

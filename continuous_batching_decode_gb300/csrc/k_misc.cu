@@ -7,7 +7,8 @@
 namespace cbd {
 
 // x[r][:] = E[token_r][:] as fp32 (the residual stream starts at the
-// embedding row of the row's token).
+// embedding row of the row's token; CBD_TOKEN_LAST: the token last sampled
+// for the row's slot, which the previous step's sampler stored).
 // CTA 0 also zeroes the step's counters (per layer: the attention task
 // counter and the GEMM chain's grid barriers, n_counters in all; every
 // kernel of the previous step has completed once this kernel passes its
@@ -18,7 +19,8 @@ namespace cbd {
 __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __restrict__ rows, int d,
                              float* __restrict__ x, int32_t* __restrict__ counters, int n_counters,
                              const float* __restrict__ g, uint16_t* __restrict__ norm_hi,
-                             uint16_t* __restrict__ norm_lo, float* __restrict__ ssq) {
+                             uint16_t* __restrict__ norm_lo, float* __restrict__ ssq,
+                             const int32_t* __restrict__ last_tok) {
   __shared__ float red[32];
   TR_DECL;
   pdl_trigger();
@@ -27,7 +29,8 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
   const int r = blockIdx.x;
   if (r == 0)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
-  const uint16_t* src = E + (size_t)rows[r].token * d;
+  const int tok = rows[r].token >= 0 ? rows[r].token : last_tok[rows[r].slot];
+  const uint16_t* src = E + (size_t)tok * d;
   float* dst = x + (size_t)r * d;
   float ss = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
@@ -59,7 +62,7 @@ cudaError_t launch_embed(const cbd_engine* e, const cbd_batch* b, const float* g
   return launch_pdl(embed_kernel, dim3(b->n_rows), dim3(256), 0, s, (const uint16_t*)e->embed,
                     (const RowDev*)b->rows, e->dm.d, e->x, e->attn_next, e->dm.L * (1 + kChainMaxPhases), g,
                     e->norm_hi, e->norm_lo,
-                    e->ssq);
+                    e->ssq, (const int32_t*)e->last_tok);
 }
 
 // h = x / sqrt(mean(x^2) + eps) * g, written as hi + lo bf16 halves.

@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
                                                       const SampDev* __restrict__ samp,
                                                       float* __restrict__ scratch,
                                                       const uint32_t* __restrict__ forbid,
-                                                      int32_t* __restrict__ out, int32_t* err) {
+                                                      int32_t* __restrict__ out, int32_t* err,
+                                                      int32_t* __restrict__ last_tok) {
   __shared__ SampShared sh;
   extern __shared__ __align__(16) uint8_t samp_dyn[];
   float* zc = reinterpret_cast<float*>(samp_dyn + kSmZ);
@@ -719,15 +720,19 @@ __global__ void __launch_bounds__(kST) sampler_kernel(const float* __restrict__ 
   __syncthreads();
   if (tid == 0) {
     if (tok >= c0 && tok < c1) cnt[tok] = __fadd_rn(cnt[tok], 1.0f);
-    if (my == 0) out[row] = tok;
+    if (my == 0) {
+      out[row] = tok;
+      if (last_tok) last_tok[slots[row]] = tok;     // the slot's last token (CBD_TOKEN_LAST)
+    }
   }
 }
 
-// One launch of the sampler over m rows (shared by cbd_step, cbd_sample and
-// cbd_sample_static).
-cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
-                           const SampDev* samp, float* scratch, const uint32_t* forbid, int32_t* out_tokens,
-                           int32_t* err, cudaStream_t s) {
+// One launch of the sampler over m rows (cbd_step and cbd_sample record
+// each drawn token as its slot's last token in last_tok; cbd_sample_static
+// passes none).
+static cudaError_t sampler_launch_ex(const float* logits, int m, int V, float* counters, const int32_t* slots,
+                                     const SampDev* samp, float* scratch, const uint32_t* forbid,
+                                     int32_t* out_tokens, int32_t* err, int32_t* last_tok, cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
   static DeviceOnce attr;
   {
@@ -748,13 +753,20 @@ cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, c
   at[1].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, sampler_kernel, logits, V, counters, slots, samp, scratch, forbid, out_tokens, err);
+  return cudaLaunchKernelEx(&cfg, sampler_kernel, logits, V, counters, slots, samp, scratch, forbid, out_tokens, err,
+                            last_tok);
+}
+
+cudaError_t sampler_launch(const float* logits, int m, int V, float* counters, const int32_t* slots,
+                           const SampDev* samp, float* scratch, const uint32_t* forbid, int32_t* out_tokens,
+                           int32_t* err, cudaStream_t s) {
+  return sampler_launch_ex(logits, m, V, counters, slots, samp, scratch, forbid, out_tokens, err, nullptr, s);
 }
 
 cudaError_t launch_sampler(const cbd_engine* e, const float* logits, int m, const int32_t* slots,
                            const SampDev* samp, int32_t* out_tokens, cudaStream_t s) {
-  return sampler_launch(logits, m, e->dm.V, e->counters, slots, samp, e->samp_scratch,
-                        e->n_forbidden > 0 ? e->forbid : nullptr, out_tokens, e->err, s);
+  return sampler_launch_ex(logits, m, e->dm.V, e->counters, slots, samp, e->samp_scratch,
+                           e->n_forbidden > 0 ? e->forbid : nullptr, out_tokens, e->err, e->last_tok, s);
 }
 
 }  // namespace cbd

@@ -291,12 +291,13 @@ typedef struct cbd_kernel_stat {
 cbd_status cbd_engine_profile(cbd_engine* e, int32_t enable);
 cbd_status cbd_engine_profile_read(cbd_engine* e, cbd_kernel_stat* out, int32_t cap, int32_t* n);
 
-/* Zero slot `slot`'s occurrence counters: a request was admitted to the
- * slot, and its penalty state starts empty ("RWKV Runner Albatross 后端",
- * section 连续批处理：Worker 主循环: the per-slot penalty state belongs to the
- * request occupying the slot; "20.3 服务、批处理与流式" section 20.3.2:
- * sequences join the batch at any iteration).  Stream-ordered on `stream`;
- * CBD_EINVAL for a slot outside [0, max_slots). */
+/* Zero slot `slot`'s occurrence counters and its last sampled token
+ * (CBD_TOKEN_LAST): a request was admitted to the slot, and its penalty
+ * state starts empty ("RWKV Runner Albatross 后端", section 连续批处理：Worker
+ * 主循环: the per-slot penalty state belongs to the request occupying the
+ * slot; "20.3 服务、批处理与流式" section 20.3.2: sequences join the batch at
+ * any iteration).  Stream-ordered on `stream`; CBD_EINVAL for a slot outside
+ * [0, max_slots). */
 cbd_status cbd_slot_reset(cbd_engine* e, int32_t slot, void* stream);
 
 /* ------------------------------------------------------------ KV pool */
@@ -323,6 +324,15 @@ cbd_status cbd_kv_pool_data(cbd_kv_pool* p, void** base, uint64_t* bytes, int32_
  * sees the earlier rows of its own chunk.  sample != 0 marks rows whose
  * logits are produced and sampled (every decode row; the last row of a
  * prefill chunk that completes its prompt). */
+/* cbd_row.token of a decode row may be CBD_TOKEN_LAST: the token that this
+ * engine's sampler last drew for the row's slot (cbd_step, cbd_batch_run or
+ * cbd_sample, in stream order; 0 after engine creation or cbd_slot_reset),
+ * read on the device.  A decode loop can then enqueue step k + 1 before step
+ * k's tokens reach the host ("20.3 服务、批处理与流式" 20.3.2: the next
+ * iteration's inputs are the previous iteration's outputs), reading each
+ * step's tokens back asynchronously.  Not allowed on prefill rows. */
+#define CBD_TOKEN_LAST (-1)
+
 typedef struct cbd_row {
   int32_t slot;
   int32_t token;

@@ -268,3 +268,22 @@ def test_cpp_scheduler_overload_matches_simulator(cbd, seed):
             cbd.sched_set_time(h, t - 1)
     finally:
         cbd.sched_destroy(h)
+
+
+def test_numpy_step_inputs_have_the_c_layout():
+    """ROW_DTYPE / SAMPLING_DTYPE arrays are byte-for-byte the cbd_row /
+    cbd_sampling arrays the C ABI reads, so step() may pass them as they are."""
+    import ctypes
+    import numpy as np
+    from continuous_batching_decode_gb300 import _cbd as c
+    assert c.ROW_DTYPE.itemsize == ctypes.sizeof(c.Row) == 20
+    assert c.SAMPLING_DTYPE.itemsize == ctypes.sizeof(c.Sampling) == 48
+    rows = [(1, 2, 3, 0, 1), (4, 5, 6, 1, 0), (7, 65535, 4095, 0, 1)]
+    assert bytes(c.rows_table(rows).data) == bytes(c.rows_array(rows))
+    sp = [dict(temperature=0.7, top_p=0.9, top_k=5, presence_penalty=0.1, frequency_penalty=0.2,
+               penalty_decay=0.99, seed=2 ** 40 + 3, request_id=2 ** 33 + 7, token_index=9), dict()]
+    assert bytes(c.sampling_table(sp).data) == bytes(c.sampling_array(sp))
+    a, p, n = c._rows_arg(c.rows_table(rows))
+    assert n == 3 and ctypes.addressof(p.contents) == a.ctypes.data
+    with __import__("pytest").raises(TypeError):
+        c._rows_arg(np.zeros(3, np.int32))
