@@ -192,14 +192,13 @@ __host__ __device__ constexpr int tc_stages() {
 }
 // Int8 weights: kConvBufs bf16 conversion buffers of N x 128 bytes, then
 // stages of (int8 tile, activation tile) in the rest of the ring.
-constexpr int kConvBufs = 3;
+constexpr int kConvBufs = 2;   // 2: one more int8 stage at N = 256 (7B step 5.61 -> 5.49 ms) than with 3
 template <int N>
 __host__ __device__ constexpr int tc_stages8() {
   return (kTcRing - kConvBufs * N * 128) / (N * kTcBK + kTcABytes) < kTcMaxStages
              ? (kTcRing - kConvBufs * N * 128) / (N * kTcBK + kTcABytes)
              : kTcMaxStages;
 }
-
 // Two int8 weights (bytes j, j + 1 of w) -> bf16x2, exactly, the byte j
 // value in the low half.  For a byte b = s|m (sign bit s, low bits m) the
 // permute builds the bf16 words 0x43|b, from which one mask keeps
@@ -229,14 +228,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(N % 32 == 0 && N >= 64 && N <= kTcMaxBN, "tile width");
   static_assert(RT == 1 || (RT == 2 && !I8), "two row tiles: bf16 weights");
   constexpr uint32_t idesc = tc::idesc_bf16(2 * kTcRows, N);
-  constexpr int ST = I8 ? tc_stages8<N>() : tc_stages<N, RT>();
+  constexpr int ST0 = I8 ? tc_stages8<N>() : tc_stages<N, RT>();
   constexpr uint32_t tmem_cols = RT == 2 ? 2 * kTcMaxBN : kTcMaxBN;
   // bf16: a stage is (weight tile, RT activation tiles); int8: (int8 tile,
   // activation tile), and the two bf16 conversion buffers follow the stages
   constexpr uint32_t w_bytes = (uint32_t)N * kTcBK * (I8 ? 1 : 2);   // one weight tile per stage
   constexpr uint32_t stage_bytes = w_bytes + RT * kTcABytes;
-  constexpr uint32_t conv_off = (uint32_t)ST * stage_bytes;          // int8: bf16 buffer b at conv_off + b * N * 128
-  static_assert(!I8 || (conv_off % 1024 == 0 && conv_off + kConvBufs * N * 128u <= (uint32_t)kTcRing),
+  constexpr uint32_t conv_off0 = (uint32_t)ST0 * stage_bytes;       // int8: bf16 buffer b at conv_off + b * N * 128
+  static_assert(!I8 || (conv_off0 % 1024 == 0 && conv_off0 + kConvBufs * N * 128u <= (uint32_t)kTcRing),
                 "int8 ring layout");
   static_assert(stage_bytes % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
   constexpr int PS = N + 4;                                     // fp32 partial row stride (padded)
@@ -269,6 +268,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int rows_cta = min(kTcRows * RT, a.n - nr * kTcRows);   // activation rows of this CTA
   const int kb0 = rank * a.KB / S, kb1 = (rank + 1) * a.KB / S;
   const int n_it = kb1 - kb0;
+  // stage s: weight (or int8) tile at w_off(s), activation tiles from a_off(s)
+  constexpr int ST = ST0;
+  constexpr uint32_t conv_off = conv_off0;
+  auto w_off = [](int s) -> uint32_t { return (uint32_t)s * stage_bytes; };
+  auto a_off = [](int s) -> uint32_t { return (uint32_t)s * stage_bytes + w_bytes; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
       auto issue_w = [&](int q) {
         const int s = q % ST;
-        uint8_t* st = ring + (size_t)s * stage_bytes;
+        uint8_t* st = ring + w_off(s);
         if constexpr (I8) {
           // the tile is one contiguous N x 64-byte run: one bulk copy
           tc::mbar_arrive_expect_tx(&w8_full[s], w_bytes);
@@ -327,7 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       auto issue_a = [&](int q) {
         const int s = q % ST;
-        uint8_t* st = ring + (size_t)s * stage_bytes + w_bytes;
+        uint8_t* st = ring + a_off(s);
         const int kx = (kb0 + q) * kTcBK;
         if constexpr (I8) tc::mbar_arrive_expect_tx(&full_bar[s], 2u * nbox * 2048u);
         for (int j = 0; j < nbox; ++j) {
@@ -379,15 +383,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc::mbar_wait(&conv_full[q % kConvBufs], (q / kConvBufs) & 1, a.err, abort_p)) { ok = false; break; }
         if (!tc::mbar_wait(&full_bar[s], (q / ST) & 1, a.err, abort_p)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t st = tc::smem_u32(ring + (size_t)s * stage_bytes);
-        const uint64_t dW = I8 ? tc::sdesc_sw128(tc::smem_u32(ring) + conv_off + (uint32_t)(q % kConvBufs) * N * 128u)
-                               : tc::sdesc_sw128(st);
-        const uint64_t dA = tc::sdesc_sw128(st + w_bytes);
+        const uint32_t rb = tc::smem_u32(ring);
+        const uint64_t dW = I8 ? tc::sdesc_sw128(rb + conv_off + (uint32_t)(q % kConvBufs) * N * 128u)
+                               : tc::sdesc_sw128(rb + w_off(s));
+        const uint64_t dA = tc::sdesc_sw128(rb + a_off(s));
 #pragma unroll
         for (int k = 0; k < kTcBK / 16; ++k)   // 16 bf16 = 32 bytes along K inside the swizzled rows
           tc::mma_bf16(tmem, dA + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
         if (RT == 2 && two) {
-          const uint64_t dA1 = tc::sdesc_sw128(st + w_bytes + kTcABytes);
+          const uint64_t dA1 = tc::sdesc_sw128(rb + a_off(s) + kTcABytes);   // second row tile (never packed)
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k)
             tc::mma_bf16(tmem + (uint32_t)N, dA1 + 2 * k, dW + 2 * k, idesc, (q > 0 || k > 0) ? 1u : 0u);
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           conv_ok = false;
         conv_ok = __all_sync(0xffffffffu, conv_ok);    // warp-uniform before the warp's arrive
         if (conv_ok) {
-          const uint8_t* src = ring + (size_t)s * stage_bytes;
+          const uint8_t* src = ring + w_off(s);
           const uint32_t dst = conv_base + (uint32_t)b * N * 128u;
           // task i: row i / 4, 16-byte int8 chunk i % 4 -> bf16 chunks 2c, 2c + 1
 #pragma unroll
