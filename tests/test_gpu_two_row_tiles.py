@@ -22,12 +22,17 @@ if torch.cuda.is_available():
     from tests import gpu_util as gu
 
 
-@pytest.mark.parametrize("B", [65, 97, 128, 200])
-def test_two_row_tiles_decode_matches_oracle(B):
+@pytest.mark.parametrize("B,fp8,int8", [(65, False, False), (97, False, False), (128, False, False),
+                                         (200, False, False), (100, True, False), (100, False, True)])
+def test_two_row_tiles_decode_matches_oracle(B, fp8, int8):
+    """Also with an E4M3 KV pool (the QKV epilogue stores E4M3 for rows
+    64-127) and with int8 weights (one row tile per CTA, two row tiles
+    overall), each against the oracle of the same format."""
     from continuous_batching_decode_gb300 import build
     build.build()
     lo, hi, seed = 64, 640, B
-    m = gu.Model("7b", max_rows=256, max_slots=B, mbps=(hi + 1 + 31) // 32, layers=2)
+    m = gu.Model("7b", max_rows=256, max_slots=B, mbps=(hi + 1 + 31) // 32, layers=2, kv_fp8=fp8,
+                 weights_int8=int8)
     try:
         V = m.shape["vocab"]
         db = synth.decode_batch(B, lo, hi, V, seed)
@@ -38,8 +43,8 @@ def test_two_row_tiles_decode_matches_oracle(B):
         pool = m.pool(n_pool)
         gen = torch.Generator(device="cuda").manual_seed(seed + 3)
         for l in range(m.shape["n_layers"]):
-            pool.view[l].copy_((torch.randn(pool.view[l].shape, generator=gen, device="cuda") * 1.3)
-                               .to(torch.bfloat16))
+            v = torch.randn(pool.view[l].shape, generator=gen, device="cuda") * 1.3
+            pool.view[l].copy_(v.to(torch.float8_e4m3fn).view(torch.uint8) if fp8 else v.to(torch.bfloat16))
         start = pool.view.clone()
         rows = [(i, db["tokens"][i], ctx[i], 0, 1) for i in range(B)]
         samp = [dict(temperature=0.0, seed=seed, request_id=i) for i in range(B)]
@@ -53,8 +58,8 @@ def test_two_row_tiles_decode_matches_oracle(B):
         check = sorted({0, 1, 31, 32, 62, 63, 64, 65, 100, 126, 127, 128, 129, 150, B - 2, B - 1} & set(range(B)))
         kv = gu.oracle_kv_from_gpu(m, pool, tables, {i: ctx[i] for i in check})
         zr = om.step(m.oracle(), kv, [(i, rows[i][1], ctx[i], 1) for i in check])
-        mx, mean = gu.assert_logits_close(z[check], zr, f"B={B}")
-        print(f"B={B}: rows {check}: max-abs {mx:.3g} mean-abs {mean:.3g}")
+        mx, mean = gu.assert_logits_close(z[check], zr, f"B={B} fp8={fp8} int8={int8}")
+        print(f"B={B} fp8={fp8} int8={int8}: rows {check}: max-abs {mx:.3g} mean-abs {mean:.3g}")
         for j, i in enumerate(check):
             if not gu.greedy_near_tie(z[i]):
                 assert toks[i] == int(np.argmax(zr[j])), f"row {i}"
