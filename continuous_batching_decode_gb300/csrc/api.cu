@@ -353,9 +353,11 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
   const size_t chunks_per_seq = ((size_t)e->max_pos + kAttnChunk - 1) / kAttnChunk;
   e->max_work = (int)std::min<size_t>(R * chunks_per_seq, (size_t)1 << 16);
   Arena W;
-  const size_t o_x = W.take(R * d * 4), o_ah = W.take(R * act_w * 2), o_al = W.take(R * act_w * 2);
-  const size_t o_fh = W.take(R * F * 2), o_fl = W.take(R * F * 2), o_q = W.take(R * hqd * 4);
-  const size_t o_nh = W.take(R * d * 2), o_nl = W.take(R * d * 2), o_ssq = W.take(R * kMaxSsqParts * 4);
+  // GEMM inputs: rows padded to whole activation boxes
+  const size_t RA = (R + kActBoxRows - 1) / kActBoxRows * kActBoxRows;
+  const size_t o_x = W.take(R * d * 4), o_ah = W.take(RA * act_w * 2), o_al = W.take(RA * act_w * 2);
+  const size_t o_fh = W.take(RA * F * 2), o_fl = W.take(RA * F * 2), o_q = W.take(R * hqd * 4);
+  const size_t o_nh = W.take(RA * d * 2), o_nl = W.take(RA * d * 2), o_ssq = W.take(R * kMaxSsqParts * 4);
   const size_t o_ao = W.take((size_t)e->max_work * hqd * 4), o_aml = W.take((size_t)e->max_work * dm.hq * 2 * 4);
   const size_t o_lg = W.take(S * V * 4), o_sc = W.take(S * V * 4), o_cn = W.take(S * V * 4), o_err = W.take(16);
   const size_t o_fb = W.take((V + 31) / 32 * 4);
@@ -405,8 +407,8 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     cbd_engine_destroy(raw);
     return cuda_fail(e3, "engine workspaces");
   }
-  // tensor maps for the tcgen05 GEMM: weights (box 128 rows) and the
-  // activation matrices in each layout the step uses (box 16 rows)
+  // tensor maps for the tcgen05 GEMM: weights (one tile per box) and the
+  // activation matrices in each layout the step uses (box 64 rows)
   {
     const int L = dm.L;
     e->tmaps.resize((size_t)4 * L + 1 + 8);
@@ -429,14 +431,14 @@ extern "C" cbd_status cbd_engine_create(const cbd_config* cfg, const cbd_weights
     const size_t a0 = (size_t)4 * L + 1;
     ok = ok && (i8 ? make_tmap_i8(&e->tmaps[4 * L], e->lm_q, V * d / 64, e->tile_lm)
                    : make_tmap_bf16(&e->tmaps[4 * L], e->lm_head, 64, V * d / 64, 64, e->tile_lm));
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, R, d, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, R, d, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, R, hqd, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 3], e->act_lo, hqd, R, hqd, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 4], e->ffn_hi, F, R, F, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 5], e->ffn_lo, F, R, F, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 6], e->norm_hi, d, R, d, 16);
-    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 7], e->norm_lo, d, R, d, 16);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 0], e->act_hi, d, RA, d, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 1], e->act_lo, d, RA, d, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 2], e->act_hi, hqd, RA, hqd, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 3], e->act_lo, hqd, RA, hqd, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 4], e->ffn_hi, F, RA, F, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 5], e->ffn_lo, F, RA, F, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 6], e->norm_hi, d, RA, d, kActBoxRows);
+    ok = ok && make_tmap_bf16(&e->tmaps[a0 + 7], e->norm_lo, d, RA, d, kActBoxRows);
     if (!ok) {
       cbd_engine* raw = e.release();
       cbd_engine_destroy(raw);

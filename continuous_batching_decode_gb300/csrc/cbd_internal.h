@@ -409,6 +409,14 @@ void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, 
 int gemm_tc_row_tiles(int n, bool int8);
 // Tile width (weight rows per tile) for an M x K weight matrix on this GPU.
 int gemm_tc_pick_tile(int M, int K);
+// Activation matrices (hi / lo bf16 GEMM inputs) are read by the GEMMs in
+// boxes of 64 rows x 64 k: one TMA instruction per row tile and half, since
+// each tiled copy has a fixed issue cost (on GB300 a 128-row-tile weight
+// stream fed by four 16-row boxes per half ran at 4.3 TB/s, by one box at
+// 4.9 TB/s).  The buffers hold a multiple of 64 rows so that a box never
+// leaves them; rows past a step's last row hold stale values and land in
+// accumulator lanes no epilogue reads.
+constexpr int kActBoxRows = 64;
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
                     uint32_t box_rows);
 // Tensor map of tiled int8 weights [rows][64] bytes, box 64 x box_rows, no swizzle.

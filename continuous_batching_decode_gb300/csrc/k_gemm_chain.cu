@@ -295,8 +295,10 @@ __global__ void __launch_bounds__(kChThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
-      // activation rows in 16-row boxes, only as many as there are rows
-      const int nbox = (rows_here + 15) / 16;
+      // activation rows: one 64-row box per half (hi, lo); rows past the
+      // last one land in TMEM lanes no epilogue reads
+      static_assert(kActBoxRows == kChRows, "one activation box per row tile");
+      constexpr uint32_t abox = kChABytes / 2;
       uint32_t fpar = 0;                                     // per slot: fills so far, mod 2
       bool ok = true;
       for (int p = 0; p < a.n_phases && ok; ++p) {
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kChThreads, 1)
           const int s = q % ST;
           if (!tc::mbar_wait(&empty_bar[s], ((fpar >> s) & 1u) ^ 1u, err, abort_p)) return false;
           fpar ^= 1u << s;
-          tc::mbar_arrive_expect_tx(&full_bar[s], wb + 2u * nbox * 2048u);
+          tc::mbar_arrive_expect_tx(&full_bar[s], wb + 2u * abox);
           tc::tma_load_2d_hint(ring + (size_t)s * sb, &maps.m[p][0], 0, (t * ph.KB + kb0 + q) * N, &full_bar[s],
                                w_policy);
           return true;
@@ -325,10 +327,8 @@ __global__ void __launch_bounds__(kChThreads, 1)
           const int s = q % ST;
           uint8_t* st = ring + (size_t)s * sb + wb;
           const int kx = (kb0 + q) * kChBK;
-          for (int j = 0; j < nbox; ++j) {
-            tc::tma_load_2d(st + j * 2048, &maps.m[p][1], kx, j * 16, &full_bar[s]);
-            tc::tma_load_2d(st + kChABytes / 2 + j * 2048, &maps.m[p][2], kx, j * 16, &full_bar[s]);
-          }
+          tc::tma_load_2d(st, &maps.m[p][1], kx, 0, &full_bar[s]);
+          tc::tma_load_2d(st + abox, &maps.m[p][2], kx, 0, &full_bar[s]);
         };
         const int npre = min(n_it, pre);
         int q = 0;

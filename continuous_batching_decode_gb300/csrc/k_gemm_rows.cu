@@ -32,6 +32,8 @@ namespace cbd {
 constexpr int kRwRows = 128;                        // activation rows per tile (MMA M)
 constexpr int kRwBK = 64;                           // k per stage (one 128-byte swizzle row)
 constexpr int kRwABytes = kRwRows * kRwBK * 2;      // 16 KB: the hi (or lo) tile of one stage
+constexpr uint32_t kABox = kActBoxRows * kRwBK * 2;  // 8 KB: one activation box (64 rows x 64 k)
+static_assert(kRwRows % kActBoxRows == 0, "whole activation boxes per row tile");
 constexpr int kRwRing = 192 * 1024;
 constexpr int kRwSmem = kRwRing + 1024;
 constexpr int kRwEpiWarps = 8;
@@ -165,8 +167,8 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         int t, rt, q;
         unit_of(g, t, rt, q);
         const int s = (int)(g % ST);
-        const int nbox = (min(kRwRows, a.n - rt * kRwRows) + 15) / 16;
-        tc::mbar_arrive_expect_tx(&full_bar[s], w_bytes + 2u * nbox * 2048u);
+        const int nbox = (min(kRwRows, a.n - rt * kRwRows) + kActBoxRows - 1) / kActBoxRows;
+        tc::mbar_arrive_expect_tx(&full_bar[s], w_bytes + 2u * nbox * kABox);
         // (no evict-first hint: the NRT units of a feature tile each read it)
         constexpr int NT = N / TP;                  // rows of one weight tile
 #pragma unroll
@@ -178,11 +180,11 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         int t, rt, q;
         unit_of(g, t, rt, q);
         const int s = (int)(g % ST);
-        const int nbox = (min(kRwRows, a.n - rt * kRwRows) + 15) / 16;
+        const int nbox = (min(kRwRows, a.n - rt * kRwRows) + kActBoxRows - 1) / kActBoxRows;
         uint8_t* st = ring + (size_t)s * stage_bytes + w_bytes;
         for (int j = 0; j < nbox; ++j) {
-          tc::tma_load_2d(st + j * 2048, &tmH, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
-          tc::tma_load_2d(st + kRwABytes + j * 2048, &tmL, q * kRwBK, rt * kRwRows + j * 16, &full_bar[s]);
+          tc::tma_load_2d(st + j * kABox, &tmH, q * kRwBK, rt * kRwRows + j * kActBoxRows, &full_bar[s]);
+          tc::tma_load_2d(st + kRwABytes + j * kABox, &tmL, q * kRwBK, rt * kRwRows + j * kActBoxRows, &full_bar[s]);
         }
       };
       // weights do not depend on the previous kernel: start them first

@@ -310,12 +310,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      // activation rows are loaded in 16-row boxes, only as many as the
-      // tile has rows; the MMA rows past them read stale shared memory and
-      // land in TMEM lanes the epilogue never reads
-      const int nbox = (min(kTcRows, rows_cta) + 15) / 16;
-      const int nbox1 = RT == 2 ? (max(0, rows_cta - kTcRows) + 15) / 16 : 0;   // second row tile
-      const uint32_t stage_tx = w_bytes + 2u * (nbox + nbox1) * 2048u;
+      // activation rows: one 64-row box per row tile and half (hi, lo);
+      // rows past the tile's last row carry stale values into TMEM lanes
+      // the epilogue never reads
+      static_assert(kActBoxRows == kTcRows, "one activation box per row tile");
+      constexpr uint32_t abox = kTcABytes / 2;
+      const int nbox1 = RT == 2 && rows_cta > kTcRows ? 1 : 0;   // second row tile
+      const uint32_t stage_tx = w_bytes + 2u * (1 + nbox1) * abox;
       const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
       auto issue_w = [&](int q) {
         const int s = q % ST;
@@ -333,15 +334,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = q % ST;
         uint8_t* st = ring + a_off(s);
         const int kx = (kb0 + q) * kTcBK;
-        if constexpr (I8) tc::mbar_arrive_expect_tx(&full_bar[s], 2u * nbox * 2048u);
-        for (int j = 0; j < nbox; ++j) {
-          tc::tma_load_2d(st + j * 2048, &tmH, kx, nr * kTcRows + j * 16, &full_bar[s]);
-          tc::tma_load_2d(st + kTcABytes / 2 + j * 2048, &tmL, kx, nr * kTcRows + j * 16, &full_bar[s]);
-        }
-        for (int j = 0; j < nbox1; ++j) {
-          tc::tma_load_2d(st + kTcABytes + j * 2048, &tmH, kx, (nr + 1) * kTcRows + j * 16, &full_bar[s]);
-          tc::tma_load_2d(st + kTcABytes + kTcABytes / 2 + j * 2048, &tmL, kx, (nr + 1) * kTcRows + j * 16,
-                          &full_bar[s]);
+        if constexpr (I8) tc::mbar_arrive_expect_tx(&full_bar[s], 2u * abox);
+        tc::tma_load_2d(st, &tmH, kx, nr * kTcRows, &full_bar[s]);
+        tc::tma_load_2d(st + abox, &tmL, kx, nr * kTcRows, &full_bar[s]);
+        if (nbox1) {
+          tc::tma_load_2d(st + kTcABytes, &tmH, kx, (nr + 1) * kTcRows, &full_bar[s]);
+          tc::tma_load_2d(st + kTcABytes + abox, &tmL, kx, (nr + 1) * kTcRows, &full_bar[s]);
         }
       };
       // weights do not depend on the previous kernel: start streaming them
