@@ -157,11 +157,6 @@ struct TcGemm {
   const float* scale;     // int8 weights: per-row scales (null: bf16 weights)
   const uint8_t* w8;      // int8 weights: the tiled bytes (tile (t, kb) is one N x 64-byte run)
 };
-struct TcWork {
-  float* part;            // [2 * sm_count][128][128] partial tiles
-  int32_t* counters;      // [max_units] arrival counters (zero between launches)
-  long long max_units;
-};
 // Pre-tiled weights: with a tile width of N rows (chosen per matrix), tile
 // (t, kb) -- N output features x 64 k -- is one contiguous N * 128-byte run
 // at byte offset (t * KB + kb) * N * 128; element (r, k) sits at
@@ -261,7 +256,6 @@ struct cbd_engine {
   int32_t step_graph_captures = 0;
   // tcgen05 GEMM: tensor maps (built once), partial tiles, counters
   std::vector<CUtensorMap> tmaps;     // per layer: qkv, o, gu, down; then lm_head; then activations
-  cbd::TcWork tcw{};
   int tile_qkv = 256, tile_o = 256, tile_gu = 256, tile_dn = 256, tile_lm = 256;   // weight tile widths
   int gemm_path = 0;                  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   size_t l2_prefetch = 0;             // bytes of the next GEMM's weights each kernel prefetches to L2 (off)
