@@ -88,7 +88,7 @@ def parse():
                     help="KV pool element type (fp8: E4M3; skips the CPU baseline)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "int8"],
                     help="streamed weight type (int8: per-row scales; the CPU baseline runs the int8 oracle)")
-    ap.add_argument("--rows-gemm", type=int, default=640,
+    ap.add_argument("--rows-gemm", type=int, default=256,
                     help="steps of at least this many rows may run the 128-row-tile GEMM (0 = never)")
     ap.add_argument("--rows-gemm-force", action="store_true",
                     help="... on every GEMM of such a step (default: where it fills the GPU well)")

@@ -262,7 +262,7 @@ struct cbd_engine {
   bool fuse_norm = true;              // RMSNorm folded into the GEMM epilogues (tcgen05 path)
   bool gemm_chain = false;            // decode: O, gate/up, down and the next QKV as one persistent launch
   int gemv_max_rows = 0;              // auto: GEMV up to this many rows
-  int rows_gemm_min = 640;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
+  int rows_gemm_min = 256;            // tcgen05 path: 128-row-tile kernel from this many rows (0 = never)
   bool rows_gemm_force = false;       // ... for every GEMM of such a step, however it fills the GPU
   int attn_path = 0;                  // 0 tensor cores (mma.sync), 1 CUDA cores
   bool prefill_attn = true;           // path 0, bf16 K/V: prefill runs on the prefill attention kernel

@@ -196,11 +196,12 @@ cbd_status cbd_engine_set_prefill_attention(cbd_engine* e, int32_t enable);
  * rows wide and its units fill at least half of the last wave of resident
  * CTAs (else the 64-row-tile kernel, which takes two row tiles per CTA and
  * splits K); with force != 0 every GEMM of the step takes it.  Same sums as
- * the other paths, in another order.  min_rows 0 = never.  Default 640
- * (7B shape on GB300: 22.54 vs 23.00 ms at 544 rows with the 64-row-tile
- * kernel and the fused RMSNorm; 29.98 vs 33.91 ms and 53.98 vs 62.22 ms
- * the other way at 1056 and 2080 rows), force 0.  CBD_EINVAL if
- * min_rows < 0. */
+ * the other paths, in another order.  min_rows 0 = never.  Default 256
+ * (7B shape on GB300, both kernels copying one activation box per 64 rows:
+ * 12.37 vs 12.45 ms at 288 rows and 17.59 vs 18.58 ms at 544 rows against
+ * the 64-row-tile kernel with the fused RMSNorm; 9.11 vs 8.96 ms the other
+ * way at 160 rows; 42.82 vs 48.11 ms at 2080 rows against the 64-row-tile
+ * kernel everywhere), force 0.  CBD_EINVAL if min_rows < 0. */
 cbd_status cbd_engine_set_rows_gemm(cbd_engine* e, int32_t min_rows, int32_t force);
 
 /* Choose the attention kernel: 0 = persistent streaming kernel (each warp
