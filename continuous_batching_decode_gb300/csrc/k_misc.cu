@@ -30,18 +30,39 @@ __global__ void embed_kernel(const uint16_t* __restrict__ E, const RowDev* __res
   if (r == 0)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int tok = rows[r].token >= 0 ? rows[r].token : last_tok[rows[r].slot];
-  const uint16_t* src = E + (size_t)tok * d;
+  // 8 elements (16 bytes of the bf16 row) per thread and round; d is a
+  // multiple of 256, so every access is whole and aligned
+  const uint4* src = reinterpret_cast<const uint4*>(E + (size_t)tok * d);
   float* dst = x + (size_t)r * d;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = bf16_to_f32(src[i]);
-    dst[i] = v;
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+    const uint4 w = src[c];
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(wv[j] << 16);
+      v[2 * j + 1] = __uint_as_float(wv[j] & 0xffff0000u);
+    }
+    float4* d4 = reinterpret_cast<float4*>(dst + 8 * c);
+    d4[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d4[1] = make_float4(v[4], v[5], v[6], v[7]);
     if (g) {
-      uint16_t h, l;
-      split_bf16(v * g[i], h, l);
-      norm_hi[(size_t)r * d + i] = h;
-      norm_lo[(size_t)r * d + i] = l;
-      ss += v * v;
+      const float4 g0 = reinterpret_cast<const float4*>(g)[2 * c], g1 = reinterpret_cast<const float4*>(g)[2 * c + 1];
+      const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      uint16_t h[8], l[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        split_bf16(v[j] * gv[j], h[j], l[j]);
+        ss += v[j] * v[j];
+      }
+      const size_t o = (size_t)r * d + 8 * c;
+      *reinterpret_cast<uint4*>(norm_hi + o) =
+          make_uint4(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16), h[4] | ((uint32_t)h[5] << 16),
+                     h[6] | ((uint32_t)h[7] << 16));
+      *reinterpret_cast<uint4*>(norm_lo + o) =
+          make_uint4(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16), l[4] | ((uint32_t)l[5] << 16),
+                     l[6] | ((uint32_t)l[7] << 16));
     }
   }
   if (g) {
