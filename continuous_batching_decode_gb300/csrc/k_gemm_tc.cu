@@ -779,7 +779,11 @@ void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, 
 // instead of 96 (4.79 vs 4.81 ms per step); narrower tiles for the wide
 // matrices ran slower (QKV 4.94, gate/up 5.20 ms): HBM is already saturated
 // while their weights stream, and the per-stage cost and the activation
-// traffic per weight byte grow as the tile narrows.
+// traffic per weight byte grow as the tile narrows.  Tiles that only fill
+// more SMs (224 rows for gate/up: 128 CTAs instead of 112; 192 for QKV: 128
+// instead of 120) gained 0.7-1.2 % on decode steps of 32-128 rows but lost
+// 11 % at 544 rows and 1.4 % at 2080 (more units per tile row, and a last
+// wave that is mostly empty), so the widest tile stays.
 int gemm_tc_pick_tile(int M, int K) {
   (void)K;
   int best = kTcMaxBN;
