@@ -401,6 +401,10 @@ void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, 
 // Row tiles per CTA the tcgen05 GEMM takes for n rows (2 above 64 rows with
 // bf16 weights, else 1).
 int gemm_tc_row_tiles(int n, bool int8);
+// Weight tiles (of N rows) per unit of the tcgen05 GEMM for n rows: 2 for
+// 128-row tiles in steps of more than 128 rows (256-wide units), else 1.
+// The unit width N * P is what gemm_tc_plan takes.
+int gemm_tc_pair(int M, int N, int n, bool int8);
 // Tile width (weight rows per tile) for an M x K weight matrix on this GPU.
 int gemm_tc_pick_tile(int M, int K);
 // Activation matrices (hi / lo bf16 GEMM inputs) are read by the GEMMs in

@@ -324,9 +324,13 @@ bool gemm_rows_preferred(const TcGemm& g, int n) {
   const int resident = max_ctas();
   if (resident <= 0) return false;
   // whole units per CTA: a last wave that is mostly empty makes this kernel
-  // slower than the 64-row-tile kernel (which splits K to fill SMs).
+  // slower than the 64-row-tile kernel (which splits K to fill SMs and, past
+  // 128 rows, pairs these tiles into 256-wide units).  Measured on GB300
+  // (7B): 544 rows, 80 units on 152 SMs, 17.66 ms against 16.40 with the
+  // other kernel; 1056 and 2080 rows (144 and 272 units) 24.15 / 43.68 ms
+  // against 24.65 / 44.90.
   const long long waves = (units + resident - 1) / resident;
-  return (double)units / (double)(waves * resident) >= 0.5;
+  return (double)units / (double)(waves * resident) >= 0.6;
 }
 
 bool gemm_rows_supports(const EpiArgs& ep) {

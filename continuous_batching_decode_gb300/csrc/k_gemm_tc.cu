@@ -78,8 +78,9 @@ constexpr int kTcMaxCluster = 8;
 
 struct TcArgs {
   int M, K, n;                       // weight rows, reduction length, activation rows
-  int N;                             // weight rows per tile (MMA N): the weights' tiling
-  int T, NR, KB, S;                  // feature tiles, row tiles, k blocks, cluster size
+  int N;                             // weight rows per unit (MMA N)
+  int P;                             // weight tiles per unit (2: two 128-row tiles side by side)
+  int T, NR, KB, S;                  // feature units, row tiles, k blocks, cluster size
   int32_t* err;
   const uint8_t* w8;                 // int8 weights: tiled bytes, fetched by 1-D bulk copies
 };
@@ -318,6 +319,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nbox1 = RT == 2 && rows_cta > kTcRows ? 1 : 0;   // second row tile
       const uint32_t stage_tx = w_bytes + 2u * (1 + nbox1) * abox;
       const uint64_t w_policy = tc::policy_evict_first();   // weights are read once per step
+      // weight tiles 2t and 2t + 1 of N / 2 rows form a unit only with two
+      // row tiles per CTA (steps of more than 128 rows)
+      const bool paired = RT == 2 && a.P == 2;
       auto issue_w = [&](int q) {
         const int s = q % ST;
         uint8_t* st = ring + w_off(s);
@@ -327,7 +331,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::bulk_load_hint(st, a.w8 + (size_t)(t * a.KB + kb0 + q) * w_bytes, w_bytes, &w8_full[s], w_policy);
         } else {
           tc::mbar_arrive_expect_tx(&full_bar[s], stage_tx);
-          tc::tma_load_2d_hint(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s], w_policy);
+          if (RT == 2 && paired) {
+            // the two tiles stacked along the MMA's N
+            tc::tma_load_2d_hint(st, &tmW, 0, ((2 * t) * a.KB + kb0 + q) * (N / 2), &full_bar[s], w_policy);
+            tc::tma_load_2d_hint(st + (N / 2) * 128, &tmW, 0, ((2 * t + 1) * a.KB + kb0 + q) * (N / 2),
+                                 &full_bar[s], w_policy);
+          } else {
+            tc::tma_load_2d_hint(st, &tmW, 0, (t * a.KB + kb0 + q) * N, &full_bar[s], w_policy);
+          }
         }
       };
       auto issue_a = [&](int q) {
@@ -765,6 +776,18 @@ static int choose_cluster(long long U, int KB) {
 
 int gemm_tc_row_tiles(int n, bool int8) { return !int8 && n > kTcRows ? 2 : 1; }
 
+// Weight tiles per unit: in steps of more than 128 rows (two row tiles per
+// CTA, at least two pairs of them), matrices tiled 128 rows wide (the 7B O
+// and down projections) run as 256-wide units of two tiles, as the
+// 256-row-tiled matrices do: a stage then carries as many weight bytes per
+// activation byte, and each MMA covers 256 features.  Measured on GB300
+// (7B): the 544-row mixed step 16.40 ms against 18.58 with 128-wide units
+// (and 17.66 with the 128-row-tile kernel for O and down); B = 128 decode
+// (one pair of row tiles) 10.71 against 10.41, hence not there.
+int gemm_tc_pair(int M, int N, int n, bool int8) {
+  return !int8 && n > 2 * kTcRows && N == 128 && (M / N) % 2 == 0 ? 2 : 1;
+}
+
 void gemm_tc_plan(int M, int K, int N, int n, int RT, int* T, int* NR, int* KB, int* S) {
   *T = M / N;
   *NR = (n + kTcRows - 1) / kTcRows;
@@ -797,11 +820,13 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   if (n <= 0) return cudaSuccess;
   if (g.M % g.N || g.K % kTcBK) return cudaErrorInvalidValue;
   TcArgs a{};
-  a.M = g.M; a.K = g.K; a.n = n; a.N = g.N;
+  a.M = g.M; a.K = g.K; a.n = n;
   a.w8 = g.w8;
   if (g.scale && !g.w8) return cudaErrorInvalidValue;
   const int RT = gemm_tc_row_tiles(n, g.scale != nullptr);
-  gemm_tc_plan(g.M, g.K, g.N, n, RT, &a.T, &a.NR, &a.KB, &a.S);
+  a.P = gemm_tc_pair(g.M, g.N, n, g.scale != nullptr);
+  a.N = g.N * a.P;
+  gemm_tc_plan(g.M, g.K, a.N, n, RT, &a.T, &a.NR, &a.KB, &a.S);
   a.err = ep.err;
   const long long U = (long long)a.T * ((a.NR + RT - 1) / RT);
   cudaLaunchConfig_t cfg = {};
@@ -829,7 +854,7 @@ cudaError_t launch_gemm_tc(const TcGemm& g, int n, const EpiArgs& ep, const PfSp
   return g.scale ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, true, 1>, *g.w, *g.hi, *g.lo, a, ep, pf)    \
                  : (RT == 2 ? cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, false, 2>, *g.w, *g.hi, *g.lo, a, ep, pf) \
                             : cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NN, false, 1>, *g.w, *g.hi, *g.lo, a, ep, pf))
-  switch (g.N) {
+  switch (a.N) {
     case 256: CBD_TC_LAUNCH(256);
     case 224: CBD_TC_LAUNCH(224);
     case 192: CBD_TC_LAUNCH(192);

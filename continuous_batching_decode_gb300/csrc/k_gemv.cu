@@ -131,7 +131,8 @@ bool gemm_uses_rows(const cbd_engine* e, int n) {
 }
 int gemm_tc_units(int M, int K, int N, int n, bool int8) {
   int T, NR, KB, S;
-  gemm_tc_plan(M, K, N, n, gemm_tc_row_tiles(n, int8), &T, &NR, &KB, &S);
+  const int RT = gemm_tc_row_tiles(n, int8);
+  gemm_tc_plan(M, K, N * gemm_tc_pair(M, N, n, int8), n, RT, &T, &NR, &KB, &S);
   return T * S;
 }
 
@@ -155,7 +156,9 @@ PfSpec next_prefetch(const cbd_engine* e, const GemmOp& op, int n) {
   PfSpec pf{};
   if (n <= 0 || e->l2_prefetch == 0 || !uses_tc(e, n) || e->w_int8) return pf;
   int T, NR, KB, S;
-  gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N, n, gemm_tc_row_tiles(n, false), &T, &NR, &KB, &S);
+  const int RT = gemm_tc_row_tiles(n, false), TP = gemm_tc_pair(op.tc.M, op.tc.N, n, false);
+  gemm_tc_plan(op.tc.M, op.tc.K, op.tc.N * TP, n, RT, &T, &NR, &KB, &S);
+  T *= TP;                           // per weight tile: a unit's tiles read the same k-blocks
   const long long units = (long long)T * S;
   const long long per_unit = (KB + S - 1) / S;
   long long P = (long long)(e->l2_prefetch / ((size_t)op.tc.N * 128)) / units;
