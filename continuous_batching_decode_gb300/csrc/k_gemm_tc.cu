@@ -37,7 +37,9 @@
 // and N..2N-1), so a weight tile is read once for 128 rows instead of once
 // per 64; the hi/lo fold runs in place over both, and phase 2 covers all 128
 // rows.  Per row the sums are those of the one-tile kernel with the same K
-// split.
+// split.  In steps of more than 128 rows, weights tiled 128 rows wide run as
+// 256-wide units of two tiles (two weight boxes per stage stacked along the
+// MMA's N), as the 256-row-tiled matrices do.
 //
 // CTA = 10 warps: warp 0 issues TMA loads into a ring of shared-memory
 // stages; warp 1 owns TMEM and issues the MMAs (one thread); warps 2-9 read
